@@ -1,0 +1,238 @@
+"""GB300 (sm_103a) chunked gated delta-rule training: KDA and GDN over packed
+variable-length documents, head dimension 128.
+
+This module is a thin ctypes binding over ``lib/libgdr.so`` (the C ABI declared
+in ``include/gdr.h``).  It only marshals arguments: torch tensors provide
+device memory and the current CUDA stream, and every step of the computation
+runs in the library's CUDA kernels.  There is no CPU fallback: if the library
+is missing, every call raises.
+
+Entry points carry the C names (``kda_workspace_bytes``, ``kda_fwd``,
+``kda_bwd``, ``gdn_workspace_bytes``, ``gdn_fwd``, ``gdn_bwd``,
+``gdr_status_string``).  Outputs and workspaces are allocated with torch when
+the caller does not pass them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libgdr.so")
+
+# Status codes (include/gdr.h).
+GDR_OK = 0
+GDR_INVALID_ARG = 1
+GDR_BAD_CU_SEQLENS = 2
+GDR_WORKSPACE_TOO_SMALL = 3
+GDR_UNSUPPORTED = 4
+GDR_STALE_WORKSPACE = 5
+GDR_CUDA_ERROR = 6
+
+EXPORTED = (
+    "gdr_status_string",
+    "kda_workspace_bytes",
+    "kda_fwd",
+    "kda_bwd",
+    "gdn_workspace_bytes",
+    "gdn_fwd",
+    "gdn_bwd",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+P = ctypes.c_void_p
+I32 = ctypes.c_int32
+I64 = ctypes.c_int64
+SZ = ctypes.c_size_t
+F32 = ctypes.c_float
+PI32 = ctypes.POINTER(ctypes.c_int32)
+PSZ = ctypes.POINTER(ctypes.c_size_t)
+
+_SIGS = {
+    "gdr_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "kda_workspace_bytes": ([I64, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
+    "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
+    "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P], ctypes.c_int),
+    "kda_bwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, P, P, P, P, P, P, P, SZ, P],
+                ctypes.c_int),
+    "gdn_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P],
+                ctypes.c_int),
+    "gdn_bwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, I32, F32, P, P, P, P, SZ, P, P, P, P, P, P, P, SZ, P],
+                ctypes.c_int),
+}
+
+
+class GdrError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def load(path: str = LIB_PATH):
+    """Load libgdr.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libgdr.so not found at {path}; build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(path)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().gdr_status_string(int(status)).decode()
+
+
+gdr_status_string = status_string
+
+
+def _check(status: int, where: str):
+    if status != GDR_OK:
+        if status in (GDR_INVALID_ARG, GDR_BAD_CU_SEQLENS, GDR_WORKSPACE_TOO_SMALL):
+            raise ValueError(f"{where}: {status_string(status)}")
+        raise GdrError(status, where)
+
+
+def _cu_host(cu_seqlens_host):
+    import numpy as np
+    if hasattr(cu_seqlens_host, "detach"):
+        cu_seqlens_host = cu_seqlens_host.detach().cpu().numpy()
+    arr = np.ascontiguousarray(np.asarray(cu_seqlens_host, dtype=np.int32))
+    return arr, arr.ctypes.data_as(PI32)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def kda_workspace_bytes(T: int, H: int, cu_seqlens_host):
+    """(saved_bytes, scratch_bytes) for a KDA problem; host only."""
+    arr, p = _cu_host(cu_seqlens_host)
+    sb, cb = SZ(0), SZ(0)
+    _check(load().kda_workspace_bytes(T, H, arr.shape[0] - 1, p, ctypes.byref(sb), ctypes.byref(cb)),
+           "kda_workspace_bytes")
+    return sb.value, cb.value
+
+
+def gdn_workspace_bytes(T: int, Hqk: int, HV: int, cu_seqlens_host):
+    arr, p = _cu_host(cu_seqlens_host)
+    sb, cb = SZ(0), SZ(0)
+    _check(load().gdn_workspace_bytes(T, Hqk, HV, arr.shape[0] - 1, p, ctypes.byref(sb), ctypes.byref(cb)),
+           "gdn_workspace_bytes")
+    return sb.value, cb.value
+
+
+def _empty_bytes(n, device):
+    import torch
+    return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
+
+
+def _fwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out, ht, want_ht, saved,
+         save_for_bwd, scratch, stream):
+    import torch
+    T, Hqk, D = q.shape
+    HV = v.shape[1]
+    arr, cup = _cu_host(cu_seqlens_host)
+    N = arr.shape[0] - 1
+    if variant == "kda":
+        sb, cb = kda_workspace_bytes(T, HV, arr)
+    else:
+        sb, cb = gdn_workspace_bytes(T, Hqk, HV, arr)
+    dev = q.device
+    if out is None:
+        out = torch.empty((T, HV, D), dtype=torch.bfloat16, device=dev)
+    if ht is None and want_ht:
+        ht = torch.empty((N, HV, D, D), dtype=torch.float32, device=dev)
+    if save_for_bwd and saved is None:
+        saved = _empty_bytes(sb, dev)
+    if saved is None and scratch is None:
+        scratch = _empty_bytes(sb, dev)
+    lib = load()
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), cup, N, T]
+    args += [HV] if variant == "kda" else [Hqk, HV]
+    args += [float(scale), _ptr(h0), _ptr(out), _ptr(ht), _ptr(saved),
+             0 if saved is None else saved.numel(), int(bool(save_for_bwd)), _ptr(scratch),
+             0 if scratch is None else scratch.numel(), _stream(stream)]
+    fn = lib.kda_fwd if variant == "kda" else lib.gdn_fwd
+    _check(fn(*args), f"{variant}_fwd")
+    return out, ht, saved
+
+
+def _bwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0, scratch,
+         grads, stream):
+    import torch
+    T, Hqk, D = q.shape
+    HV = v.shape[1]
+    arr, cup = _cu_host(cu_seqlens_host)
+    N = arr.shape[0] - 1
+    if variant == "kda":
+        sb, cb = kda_workspace_bytes(T, HV, arr)
+    else:
+        sb, cb = gdn_workspace_bytes(T, Hqk, HV, arr)
+    dev = q.device
+    grads = dict(grads or {})
+    grads.setdefault("dq", torch.empty_like(q))
+    grads.setdefault("dk", torch.empty_like(k))
+    grads.setdefault("dv", torch.empty_like(v))
+    grads.setdefault("dg", torch.empty_like(g))
+    grads.setdefault("dbeta", torch.empty_like(beta))
+    if want_dh0:
+        grads.setdefault("dh0", torch.empty((N, HV, D, D), dtype=torch.float32, device=dev))
+    if scratch is None:
+        scratch = _empty_bytes(cb, dev)
+    lib = load()
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), cup, N, T]
+    args += [HV] if variant == "kda" else [Hqk, HV]
+    args += [float(scale), _ptr(h0), _ptr(dout), _ptr(dht), _ptr(saved), saved.numel(),
+             _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dg"]), _ptr(grads["dbeta"]),
+             _ptr(grads.get("dh0")), _ptr(scratch), scratch.numel(), _stream(stream)]
+    fn = lib.kda_bwd if variant == "kda" else lib.gdn_bwd
+    _check(fn(*args), f"{variant}_bwd")
+    return grads
+
+
+def kda_fwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0=None, out=None, ht=None, want_ht=True,
+            saved=None, save_for_bwd=True, scratch=None, stream=None):
+    """KDA forward.  q, k, v bf16 [T,H,128]; g fp32 [T,H,128]; beta bf16 [T,H];
+    cu_seqlens int32 device [N+1] and its host copy.  Returns (out, ht, saved)."""
+    return _fwd("kda", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out, ht, want_ht, saved,
+                save_for_bwd, scratch, stream)
+
+
+def kda_bwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0=None, dht=None, want_dh0=False,
+            scratch=None, grads=None, stream=None):
+    """KDA backward from `saved` (filled by kda_fwd(save_for_bwd=True)).
+    Returns a dict with dq, dk, dv, dg, dbeta (and dh0 when want_dh0)."""
+    return _bwd("kda", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0,
+                scratch, grads, stream)
+
+
+def gdn_fwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0=None, out=None, ht=None, want_ht=True,
+            saved=None, save_for_bwd=True, scratch=None, stream=None):
+    """GDN forward.  q, k bf16 [T,Hqk,128]; v bf16 [T,HV,128]; g, beta fp32
+    [T,HV].  Returns (out, ht, saved)."""
+    return _fwd("gdn", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out, ht, want_ht, saved,
+                save_for_bwd, scratch, stream)
+
+
+def gdn_bwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0=None, dht=None, want_dh0=False,
+            scratch=None, grads=None, stream=None):
+    return _bwd("gdn", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0,
+                scratch, grads, stream)

@@ -1,0 +1,464 @@
+// gdr_api.cu -- the C ABI (include/gdr.h): validation, planning, workspace
+// layout, the saved-buffer stamp, and the launch sequences.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/gdr.h"
+#include "gdr_common.cuh"
+#include "gdr_kernels.h"
+
+namespace gdr {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kRankLimit = 4096;  // documents ranked longest-first on the device up to this count
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// ---------------------------------------------------------------------------
+// Planning kernel: document and chunk tables from the device cu_seqlens, and
+// the longest-first document order for the walks (the LPT rule of PR #7723
+// "perf(cake_gdn): prefetch offset adjoint walk, default LPT segment plan",
+// applied here to whole documents on one GPU).  One block; no host copy.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N, DocDesc* docs, ChunkDesc* chunks,
+                                               int* order) {
+  __shared__ int part[1024];
+  __shared__ int lens[kRankLimit];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int per = (N + nt - 1) / nt;
+  const int n0 = min(N, tid * per), n1 = min(N, n0 + per);
+  int sum = 0;
+  for (int n = n0; n < n1; ++n) sum += (cu[n + 1] - cu[n] + CH - 1) / CH;
+  part[tid] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int i = 0; i < nt; ++i) {
+      const int v = part[i];
+      part[i] = acc;
+      acc += v;
+    }
+  }
+  __syncthreads();
+  int c = part[tid];
+  for (int n = n0; n < n1; ++n) {
+    const int tok0 = cu[n], len = cu[n + 1] - tok0, nch = (len + CH - 1) / CH;
+    docs[n] = DocDesc{tok0, len, c, nch};
+    for (int j = 0; j < nch; ++j) chunks[c + j] = ChunkDesc{tok0 + CH * j, min(CH, len - CH * j), n, j};
+    c += nch;
+  }
+  if (N <= kRankLimit) {
+    for (int n = tid; n < N; n += nt) lens[n] = cu[n + 1] - cu[n];
+    __syncthreads();
+    for (int n = tid; n < N; n += nt) {
+      const int ln = lens[n];
+      int rank = 0;
+      for (int m = 0; m < N; ++m) rank += (lens[m] > ln) || (lens[m] == ln && m < n);
+      order[rank] = n;
+    }
+  } else {
+    for (int n = tid; n < N; n += nt) order[n] = n;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout.
+// ---------------------------------------------------------------------------
+struct Layout {
+  int64_t NC = 0;
+  size_t docs = 0, chunks = 0, order = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, gam = 0, tape = 0;
+  size_t saved_total = 0;
+  size_t dstape = 0, ddelta = 0, dqs = 0, dw = 0, dkd = 0, dgam = 0, dqp = 0, dkp = 0;
+  size_t bwd_total = 0;
+};
+
+Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
+  Layout L;
+  L.NC = NC;
+  const size_t tile = (size_t)NC * HV * CH * DK * sizeof(float);
+  const size_t sq = (size_t)NC * HV * CH * CH * sizeof(float);
+  const size_t vec = (size_t)NC * HV * DK * sizeof(float);
+  const size_t st = (size_t)NC * HV * DK * DK * sizeof(float);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.docs = take((size_t)std::max(N, 1) * sizeof(DocDesc));
+  L.chunks = take((size_t)std::max<int64_t>(NC, 1) * sizeof(ChunkDesc));
+  L.order = take((size_t)std::max(N, 1) * sizeof(int));
+  L.w = take(tile);
+  L.u = take(tile);
+  L.qp = take(tile);
+  L.kd = take(tile);
+  L.delta = take(tile);
+  L.aqk = take(sq);
+  L.gam = take(vec);
+  L.tape = take(st);
+  L.saved_total = o;
+  o = 0;
+  L.dstape = take(st);
+  L.ddelta = take(tile);
+  L.dqs = take(tile);
+  L.dw = take(tile);
+  L.dkd = take(tile);
+  L.dgam = take(vec);
+  if (grouped) {
+    L.dqp = take(tile);
+    L.dkp = take(tile);
+  }
+  L.bwd_total = o;
+  return L;
+}
+
+// Validates cu_seqlens_host and counts chunks.
+gdr_status plan_host(int64_t T, int32_t N, const int32_t* cu, int64_t* NC) {
+  if (N < 0 || T < 0) return GDR_INVALID_ARG;
+  if (!cu) return GDR_INVALID_ARG;
+  if (cu[0] != 0 || (int64_t)cu[N] != T) return GDR_BAD_CU_SEQLENS;
+  if (T > INT32_MAX) return GDR_INVALID_ARG;
+  int64_t nc = 0;
+  for (int32_t n = 0; n < N; ++n) {
+    if (cu[n + 1] < cu[n]) return GDR_BAD_CU_SEQLENS;
+    nc += (cu[n + 1] - cu[n] + CH - 1) / CH;
+  }
+  *NC = nc;
+  return GDR_OK;
+}
+
+uint64_t hash_cu(const int32_t* cu, int32_t N) {
+  uint64_t h = 1469598103934665603ull;
+  for (int32_t i = 0; i <= N; ++i) {
+    h ^= (uint32_t)cu[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+// Stamp of a saved buffer: which forward filled it.  Host-side registry keyed
+// by the buffer address (no device read, no host synchronization).
+struct Stamp {
+  int64_t T;
+  int32_t N, Hqk, HV, variant;
+  uint64_t cu_hash;
+};
+std::mutex g_stamp_mu;
+std::unordered_map<const void*, Stamp> g_stamps;
+
+void stamp_set(const void* saved, const Stamp& s) {
+  std::lock_guard<std::mutex> lk(g_stamp_mu);
+  g_stamps[saved] = s;
+}
+bool stamp_check(const void* saved, const Stamp& s) {
+  std::lock_guard<std::mutex> lk(g_stamp_mu);
+  auto it = g_stamps.find(saved);
+  if (it == g_stamps.end()) return false;
+  const Stamp& r = it->second;
+  return r.T == s.T && r.N == s.N && r.Hqk == s.Hqk && r.HV == s.HV && r.variant == s.variant &&
+         r.cu_hash == s.cu_hash;
+}
+
+gdr_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDR_CUDA_ERROR;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return GDR_CUDA_ERROR;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return GDR_CUDA_ERROR;
+  if (major != 10 || minor != 3) return GDR_UNSUPPORTED;
+  return GDR_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 152;
+}
+
+// Warps per walk CTA (each warp carries 16 value columns): spread the
+// (document, head) chains over at least the SM count when they are few.
+int walk_warps(int64_t chains) {
+  if (const char* e = std::getenv("GDR_WALK_WARPS")) {
+    const int v = std::atoi(e);
+    if (v == 1 || v == 2 || v == 4 || v == 8) return v;
+  }
+  const int sms = sm_count();
+  if (chains >= sms) return 8;
+  if (chains * 2 >= sms) return 4;
+  if (chains * 4 >= sms) return 2;
+  return 1;
+}
+
+bool aligned(const void* p) { return ((uintptr_t)p % kAlign) == 0; }
+
+gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_CUDA_ERROR; }
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+template <typename T>
+const T* at(const void* base, size_t off) {
+  return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
+}
+
+gdr_status workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const int32_t* cu, size_t* saved_bytes,
+                           size_t* scratch_bytes) {
+  if (Hqk <= 0 || HV <= 0 || HV % Hqk != 0) return GDR_INVALID_ARG;
+  int64_t NC = 0;
+  const gdr_status st = plan_host(T, N, cu, &NC);
+  if (st != GDR_OK) return st;
+  const Layout L = make_layout(NC, N, HV, HV != Hqk);
+  if (saved_bytes) *saved_bytes = L.saved_total;
+  if (scratch_bytes) *scratch_bytes = L.bwd_total;
+  return GDR_OK;
+}
+
+gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, const float* g, const void* beta,
+                    const int32_t* cu, const int32_t* cu_host, int32_t N, int64_t T, int32_t Hqk, int32_t HV,
+                    float scale, const float* h0, void* out, float* ht, void* saved, size_t saved_bytes,
+                    int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  if (Hqk <= 0 || HV <= 0 || HV % Hqk != 0) return GDR_INVALID_ARG;
+  int64_t NC = 0;
+  gdr_status st = plan_host(T, N, cu_host, &NC);
+  if (st != GDR_OK) return st;
+  if (N == 0) return GDR_OK;
+  if (!cu) return GDR_INVALID_ARG;
+  if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDR_INVALID_ARG;
+  if (save_for_bwd && !saved) return GDR_INVALID_ARG;
+  const Layout L = make_layout(NC, N, HV, HV != Hqk);
+  void* base = saved ? saved : scratch;
+  const size_t have = saved ? saved_bytes : scratch_bytes;
+  if (!base) return GDR_INVALID_ARG;
+  if (!aligned(base)) return GDR_INVALID_ARG;
+  if (have < L.saved_total) return GDR_WORKSPACE_TOO_SMALL;
+  st = check_device();
+  if (st != GDR_OK) return st;
+
+  DocDesc* docs = at<DocDesc>(base, L.docs);
+  ChunkDesc* chunks = at<ChunkDesc>(base, L.chunks);
+  int* order = at<int>(base, L.order);
+  k_plan<<<1, 1024, 0, stream>>>(cu, N, docs, chunks, order);
+  if (cudaGetLastError() != cudaSuccess) return GDR_CUDA_ERROR;
+  const bool vec = variant == 0;
+  PrepArgs pa{};
+  pa.q = static_cast<const __nv_bfloat16*>(q);
+  pa.k = static_cast<const __nv_bfloat16*>(k);
+  pa.v = static_cast<const __nv_bfloat16*>(v);
+  pa.g = g;
+  pa.beta = beta;
+  pa.chunks = chunks;
+  pa.Hqk = Hqk;
+  pa.HV = HV;
+  pa.w = at<float>(base, L.w);
+  pa.u = at<float>(base, L.u);
+  pa.qp = at<float>(base, L.qp);
+  pa.kd = at<float>(base, L.kd);
+  pa.aqk = at<float>(base, L.aqk);
+  pa.gam = at<float>(base, L.gam);
+  st = cuda_status(launch_prep(pa, (int)NC, vec, vec, stream));
+  if (st != GDR_OK) return st;
+  WalkArgs wa{};
+  wa.docs = docs;
+  wa.order = order;
+  wa.HV = HV;
+  wa.w = pa.w;
+  wa.u = pa.u;
+  wa.kd = pa.kd;
+  wa.gam = pa.gam;
+  wa.h0 = h0;
+  wa.tape = at<float>(base, L.tape);
+  wa.delta = at<float>(base, L.delta);
+  wa.ht = ht;
+  st = cuda_status(launch_walk_fwd(wa, N, walk_warps((int64_t)N * HV), stream));
+  if (st != GDR_OK) return st;
+  OutArgs oa{};
+  oa.chunks = chunks;
+  oa.HV = HV;
+  oa.scale = scale;
+  oa.qp = pa.qp;
+  oa.tape = wa.tape;
+  oa.aqk = pa.aqk;
+  oa.delta = wa.delta;
+  oa.out = static_cast<__nv_bfloat16*>(out);
+  st = cuda_status(launch_out(oa, (int)NC, stream));
+  if (st != GDR_OK) return st;
+  if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, hash_cu(cu_host, N)});
+  return GDR_OK;
+}
+
+gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, const float* g, const void* beta,
+                    const int32_t* cu, const int32_t* cu_host, int32_t N, int64_t T, int32_t Hqk, int32_t HV,
+                    float scale, const void* dout, const float* dht, const void* saved, size_t saved_bytes,
+                    void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* scratch,
+                    size_t scratch_bytes, cudaStream_t stream) {
+  if (Hqk <= 0 || HV <= 0 || HV % Hqk != 0) return GDR_INVALID_ARG;
+  int64_t NC = 0;
+  gdr_status st = plan_host(T, N, cu_host, &NC);
+  if (st != GDR_OK) return st;
+  if (N == 0) return GDR_OK;
+  if (!cu || !saved || !scratch) return GDR_INVALID_ARG;
+  if (T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta)) return GDR_INVALID_ARG;
+  if (!aligned(saved) || !aligned(scratch)) return GDR_INVALID_ARG;
+  const Layout L = make_layout(NC, N, HV, HV != Hqk);
+  if (saved_bytes < L.saved_total || scratch_bytes < L.bwd_total) return GDR_WORKSPACE_TOO_SMALL;
+  if (!stamp_check(saved, Stamp{T, N, Hqk, HV, variant, hash_cu(cu_host, N)})) return GDR_STALE_WORKSPACE;
+  st = check_device();
+  if (st != GDR_OK) return st;
+  const bool vec = variant == 0;
+  const DocDesc* docs = at<DocDesc>(saved, L.docs);
+  const ChunkDesc* chunks = at<ChunkDesc>(saved, L.chunks);
+  const int* order = at<int>(saved, L.order);
+
+  WalkBwdArgs wb{};
+  wb.docs = docs;
+  wb.order = order;
+  wb.chunks = chunks;
+  wb.HV = HV;
+  wb.scale = scale;
+  wb.w = at<float>(saved, L.w);
+  wb.qp = at<float>(saved, L.qp);
+  wb.kd = at<float>(saved, L.kd);
+  wb.aqk = at<float>(saved, L.aqk);
+  wb.gam = at<float>(saved, L.gam);
+  wb.dout = static_cast<const __nv_bfloat16*>(dout);
+  wb.dht = dht;
+  wb.dstape = at<float>(scratch, L.dstape);
+  wb.ddelta = at<float>(scratch, L.ddelta);
+  wb.dh0 = dh0;
+  st = cuda_status(launch_walk_bwd(wb, N, walk_warps((int64_t)N * HV), stream));
+  if (st != GDR_OK) return st;
+
+  GradStateArgs gs{};
+  gs.chunks = chunks;
+  gs.HV = HV;
+  gs.scale = scale;
+  gs.dout = wb.dout;
+  gs.tape = at<float>(saved, L.tape);
+  gs.dstape = wb.dstape;
+  gs.delta = at<float>(saved, L.delta);
+  gs.ddelta = wb.ddelta;
+  gs.dqs = at<float>(scratch, L.dqs);
+  gs.dw = at<float>(scratch, L.dw);
+  gs.dkd = at<float>(scratch, L.dkd);
+  gs.dgam = at<float>(scratch, L.dgam);
+  st = cuda_status(launch_grad_state(gs, (int)NC, stream));
+  if (st != GDR_OK) return st;
+
+  GradArgs ga{};
+  ga.q = static_cast<const __nv_bfloat16*>(q);
+  ga.k = static_cast<const __nv_bfloat16*>(k);
+  ga.v = static_cast<const __nv_bfloat16*>(v);
+  ga.g = g;
+  ga.beta = beta;
+  ga.dout = wb.dout;
+  ga.chunks = chunks;
+  ga.Hqk = Hqk;
+  ga.HV = HV;
+  ga.scale = scale;
+  ga.w = wb.w;
+  ga.u = at<float>(saved, L.u);
+  ga.kd = wb.kd;
+  ga.gam = wb.gam;
+  ga.aqk = wb.aqk;
+  ga.delta = gs.delta;
+  ga.ddelta = wb.ddelta;
+  ga.dqs = gs.dqs;
+  ga.dw = gs.dw;
+  ga.dkd = gs.dkd;
+  ga.dgam = gs.dgam;
+  ga.dq = static_cast<__nv_bfloat16*>(dq);
+  ga.dk = static_cast<__nv_bfloat16*>(dk);
+  ga.dv = static_cast<__nv_bfloat16*>(dv);
+  const bool grouped = HV != Hqk;
+  ga.dq_part = grouped ? at<float>(scratch, L.dqp) : nullptr;
+  ga.dk_part = grouped ? at<float>(scratch, L.dkp) : nullptr;
+  ga.dg = dg;
+  ga.dbeta = dbeta;
+  st = cuda_status(launch_grad(ga, (int)NC, vec, vec, stream));
+  if (st != GDR_OK) return st;
+  if (grouped) {
+    GroupReduceArgs gr{};
+    gr.chunks = chunks;
+    gr.Hqk = Hqk;
+    gr.HV = HV;
+    gr.dq_part = ga.dq_part;
+    gr.dk_part = ga.dk_part;
+    gr.dq = ga.dq;
+    gr.dk = ga.dk;
+    st = cuda_status(launch_group_reduce(gr, (int)NC, stream));
+    if (st != GDR_OK) return st;
+  }
+  return GDR_OK;
+}
+
+}  // namespace
+}  // namespace gdr
+
+extern "C" {
+
+const char* gdr_status_string(gdr_status s) {
+  switch (s) {
+    case GDR_OK: return "GDR_OK";
+    case GDR_INVALID_ARG: return "GDR_INVALID_ARG";
+    case GDR_BAD_CU_SEQLENS: return "GDR_BAD_CU_SEQLENS";
+    case GDR_WORKSPACE_TOO_SMALL: return "GDR_WORKSPACE_TOO_SMALL";
+    case GDR_UNSUPPORTED: return "GDR_UNSUPPORTED";
+    case GDR_STALE_WORKSPACE: return "GDR_STALE_WORKSPACE";
+    case GDR_CUDA_ERROR: return "GDR_CUDA_ERROR";
+    default: return "GDR_UNKNOWN_STATUS";
+  }
+}
+
+gdr_status kda_workspace_bytes(int64_t T, int32_t H, int32_t N, const int32_t* cu_seqlens_host, size_t* saved_bytes,
+                               size_t* scratch_bytes) {
+  return gdr::workspace_bytes(T, H, H, N, cu_seqlens_host, saved_bytes, scratch_bytes);
+}
+
+gdr_status gdn_workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const int32_t* cu_seqlens_host,
+                               size_t* saved_bytes, size_t* scratch_bytes) {
+  return gdr::workspace_bytes(T, Hqk, HV, N, cu_seqlens_host, saved_bytes, scratch_bytes);
+}
+
+gdr_status kda_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
+                   float scale, const float* h0, gdr_bf16* out, float* ht, void* saved, size_t saved_bytes,
+                   int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  return gdr::fwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, h0, out, ht, saved,
+                       saved_bytes, save_for_bwd, scratch, scratch_bytes, stream);
+}
+
+gdr_status kda_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
+                   float scale, const float* h0, const gdr_bf16* dout, const float* dht, const void* saved,
+                   size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg, gdr_bf16* dbeta,
+                   float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  (void)h0;
+  return gdr::bwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, dout, dht, saved,
+                       saved_bytes, dq, dk, dv, dg, dbeta, dh0, scratch, scratch_bytes, stream);
+}
+
+gdr_status gdn_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t Hqk,
+                   int32_t HV, float scale, const float* h0, gdr_bf16* out, float* ht, void* saved,
+                   size_t saved_bytes, int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  return gdr::fwd_impl(1, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, Hqk, HV, scale, h0, out, ht, saved,
+                       saved_bytes, save_for_bwd, scratch, scratch_bytes, stream);
+}
+
+gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t Hqk,
+                   int32_t HV, float scale, const float* h0, const gdr_bf16* dout, const float* dht,
+                   const void* saved, size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg,
+                   float* dbeta, float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  (void)h0;
+  return gdr::bwd_impl(1, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, Hqk, HV, scale, dout, dht, saved,
+                       saved_bytes, dq, dk, dv, dg, dbeta, dh0, scratch, scratch_bytes, stream);
+}
+
+}  // extern "C"

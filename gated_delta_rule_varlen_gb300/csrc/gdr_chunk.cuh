@@ -1,0 +1,375 @@
+// gdr_chunk.cuh -- chunk-local building blocks shared by the prep and the
+// gradient kernels: tile loads with the gate cumsum, the gated Gram matrices,
+// the unit-lower-triangular inverse and the gated "apply" products of the
+// backward.  One CTA of 4 warps works on one (chunk, value head); warp I owns
+// rows 16I .. 16I+15 of every 64-row result.
+#pragma once
+#include "gdr_common.cuh"
+
+namespace gdr {
+
+struct ChunkSmem {
+  float K[CH * LDT];  // k as FP32 (rows >= len are zero)
+  float Q[CH * LDT];  // q as FP32
+  float G[CH * LDT];  // per-channel gate: chunk-local cumsum of g, times log2(e)
+  float gs[CH];       // scalar gate: chunk-local cumsum of g, times log2(e)
+  float beta[CH];
+  float At[CH * LDS];  // strict_tril of the gated Gram K K^T (without beta)
+  float T[CH * LDS];   // (I + diag(beta) At)^-1
+  float tmp[3 * 256];
+};
+
+// Loads k, q (of Q/K head hq), the gate (cumsum, base-2 scaled) and beta of
+// value head h for the chunk rows [tok0, tok0+len).  Rows >= len are zero
+// (zero gate rows keep the cumsum flat, so gc at row 63 equals gc at the
+// chunk's last token).
+template <bool VEC, typename BetaT>
+__device__ void load_chunk(ChunkSmem& s, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                           const float* __restrict__ g, const BetaT* __restrict__ beta, int tok0, int len, int hq,
+                           int h, int Hqk, int HV) {
+  const int tid = threadIdx.x;
+  for (int e = tid; e < CH * DK / 2; e += blockDim.x) {
+    const int i = e / (DK / 2), d = (e % (DK / 2)) * 2;
+    float2 kv = make_float2(0.f, 0.f), qv = make_float2(0.f, 0.f);
+    if (i < len) {
+      const size_t off = ((size_t)(tok0 + i) * Hqk + hq) * DK + d;
+      kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(k + off));
+      qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q + off));
+    }
+    *reinterpret_cast<float2*>(&s.K[i * LDT + d]) = kv;
+    *reinterpret_cast<float2*>(&s.Q[i * LDT + d]) = qv;
+    if (VEC) {
+      float2 gv = make_float2(0.f, 0.f);
+      if (i < len) gv = *reinterpret_cast<const float2*>(g + ((size_t)(tok0 + i) * HV + h) * DK + d);
+      gv.x *= LOG2E;
+      gv.y *= LOG2E;
+      *reinterpret_cast<float2*>(&s.G[i * LDT + d]) = gv;
+    }
+  }
+  if (tid < CH) {
+    const bool ok = tid < len;
+    s.beta[tid] = ok ? to_f<BetaT>(beta[(size_t)(tok0 + tid) * HV + h]) : 0.f;
+    if (!VEC) s.gs[tid] = ok ? g[(size_t)(tok0 + tid) * HV + h] * LOG2E : 0.f;
+  }
+  __syncthreads();
+  if (VEC) {
+    if (tid < DK) {
+      float acc = 0.f;
+      for (int i = 0; i < CH; ++i) {
+        acc += s.G[i * LDT + tid];
+        s.G[i * LDT + tid] = acc;
+      }
+    }
+  } else if (tid == 0) {
+    float acc = 0.f;
+    for (int i = 0; i < CH; ++i) {
+      acc += s.gs[i];
+      s.gs[i] = acc;
+    }
+  }
+  __syncthreads();
+}
+
+// Gated Gram matrices of one chunk.
+//   At[i][j]  = sum_c K_ic K_jc exp(gc_ic - gc_jc)   for j <  i (else 0)  -> s.At
+//   Aqk[i][j] = sum_c Q_ic K_jc exp(gc_ic - gc_jc)   for j <= i (else 0)  -> aqk (global, [64][64])
+// Per-channel gates use the block factorization described in gdr_common.cuh.
+template <bool VEC, bool WITH_QK>
+__device__ void gram(ChunkSmem& s, float* __restrict__ aqk) {
+  const int I = threadIdx.x >> 5, i0 = 16 * I;
+  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+  float accK[8][4], accQ[8][4];
+  zero_acc(accK);
+  zero_acc(accQ);
+  if (VEC) {
+    float dK[2][4], dQ[2][4];
+    zero_acc(dK);
+    zero_acc(dQ);
+#pragma unroll 2
+    for (int kk = 0; kk < 16; ++kk) {
+      const int c0 = kk * 8 + t, c1 = c0 + 4;
+      const float* G = s.G;
+      const float* K = s.K;
+      const float* Q = s.Q;
+      const int r0 = (i0 + g) * LDT, r1 = (i0 + g + 8) * LDT;
+      // Off-diagonal blocks: reference = gc at the end of block I-1.
+      if (I > 0) {
+        const float b0 = G[(i0 - 1) * LDT + c0], b1 = G[(i0 - 1) * LDT + c1];
+        const float e00 = ex2(G[r0 + c0] - b0), e10 = ex2(G[r1 + c0] - b0);
+        const float e01 = ex2(G[r0 + c1] - b1), e11 = ex2(G[r1 + c1] - b1);
+        uint32_t aK[4] = {tf32(K[r0 + c0] * e00), tf32(K[r1 + c0] * e10), tf32(K[r0 + c1] * e01),
+                          tf32(K[r1 + c1] * e11)};
+        uint32_t aQ[4] = {tf32(Q[r0 + c0] * e00), tf32(Q[r1 + c0] * e10), tf32(Q[r0 + c1] * e01),
+                          tf32(Q[r1 + c1] * e11)};
+#pragma unroll
+        for (int nt = 0; nt < 6; ++nt) {
+          if (nt < 2 * I) {
+            const int j = nt * 8 + g;
+            uint32_t b[2] = {tf32(K[j * LDT + c0] * ex2(b0 - G[j * LDT + c0])),
+                             tf32(K[j * LDT + c1] * ex2(b1 - G[j * LDT + c1]))};
+            mma8(accK[nt], aK, b);
+            if (WITH_QK) mma8(accQ[nt], aQ, b);
+          }
+        }
+      }
+      // Diagonal block: reference = gc at row i0 + 7.
+      {
+        const float m0 = G[(i0 + 7) * LDT + c0], m1 = G[(i0 + 7) * LDT + c1];
+        const float e00 = ex2(G[r0 + c0] - m0), e10 = ex2(G[r1 + c0] - m0);
+        const float e01 = ex2(G[r0 + c1] - m1), e11 = ex2(G[r1 + c1] - m1);
+        uint32_t aK[4] = {tf32(K[r0 + c0] * e00), tf32(K[r1 + c0] * e10), tf32(K[r0 + c1] * e01),
+                          tf32(K[r1 + c1] * e11)};
+        uint32_t aQ[4] = {tf32(Q[r0 + c0] * e00), tf32(Q[r1 + c0] * e10), tf32(Q[r0 + c1] * e01),
+                          tf32(Q[r1 + c1] * e11)};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int j = i0 + nt * 8 + g;
+          uint32_t b[2] = {tf32(K[j * LDT + c0] * ex2(m0 - G[j * LDT + c0])),
+                           tf32(K[j * LDT + c1] * ex2(m1 - G[j * LDT + c1]))};
+          mma8(dK[nt], aK, b);
+          if (WITH_QK) mma8(dQ[nt], aQ, b);
+        }
+      }
+    }
+    // Scatter: off-diagonal n-tiles [0, 2I), diagonal tiles 2I, 2I+1, zeros above.
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
+        float vK = 0.f, vQ = 0.f;
+        if (nt < 2 * I) {
+          vK = accK[nt][r];
+          vQ = accQ[nt][r];
+        } else if (nt == 2 * I || nt == 2 * I + 1) {
+          const int dn = nt - 2 * I;
+          const int lrow = row, lcol = dn * 8 + 2 * t + (r & 1);
+          vK = lcol < lrow ? dK[dn][r] : 0.f;
+          vQ = lcol <= lrow ? dQ[dn][r] : 0.f;
+        }
+        s.At[(i0 + row) * LDS + col] = vK;
+        if (WITH_QK) aqk[(i0 + row) * CH + col] = vQ;
+      }
+    }
+  } else {
+#pragma unroll 2
+    for (int kk = 0; kk < 16; ++kk) {
+      const int c0 = kk * 8 + t, c1 = c0 + 4;
+      const int r0 = (i0 + g) * LDT, r1 = (i0 + g + 8) * LDT;
+      uint32_t aK[4] = {tf32(s.K[r0 + c0]), tf32(s.K[r1 + c0]), tf32(s.K[r0 + c1]), tf32(s.K[r1 + c1])};
+      uint32_t aQ[4] = {tf32(s.Q[r0 + c0]), tf32(s.Q[r1 + c0]), tf32(s.Q[r0 + c1]), tf32(s.Q[r1 + c1])};
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        if (nt < 2 * I + 2) {
+          const int j = nt * 8 + g;
+          uint32_t b[2] = {tf32(s.K[j * LDT + c0]), tf32(s.K[j * LDT + c1])};
+          mma8(accK[nt], aK, b);
+          if (WITH_QK) mma8(accQ[nt], aQ, b);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = i0 + g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
+        float vK = 0.f, vQ = 0.f;
+        if (col <= row) {
+          const float dec = ex2(s.gs[row] - s.gs[col]);
+          vQ = accQ[nt][r] * dec;
+          if (col < row) vK = accK[nt][r] * dec;
+        }
+        s.At[row * LDS + col] = vK;
+        if (WITH_QK) aqk[row * CH + col] = vQ;
+      }
+    }
+  }
+}
+
+// s.T = (I + diag(beta) At)^-1, unit lower triangular.  Diagonal 16x16 blocks
+// by forward substitution (one warp each), then off-diagonal blocks by
+// distance: T_IJ = -T_II * sum_{K=J}^{I-1} A_IK T_KJ.  FP32 on CUDA cores.
+__device__ inline void invert(ChunkSmem& s) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
+  if (lane < 16) {
+    const int i0 = warp * 16, j = lane;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = (i == j) ? 1.f : 0.f;
+      const float bi = s.beta[i0 + i];
+#pragma unroll
+      for (int m = 0; m < i; ++m) acc -= bi * s.At[(i0 + i) * LDS + i0 + m] * x[m];
+      x[i] = acc;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s.T[(i0 + i) * LDS + i0 + j] = x[i];
+  }
+  // Zero the strictly upper blocks.
+  for (int e = tid; e < CH * CH; e += blockDim.x) {
+    const int i = e >> 6, j = e & 63;
+    if ((j >> 4) > (i >> 4)) s.T[i * LDS + j] = 0.f;
+  }
+  __syncthreads();
+  for (int d = 1; d <= 3; ++d) {
+    const int npairs = 4 - d;
+    for (int e = tid; e < npairs * 256; e += blockDim.x) {
+      const int J = e >> 8, I = J + d, r = (e >> 4) & 15, c = e & 15;
+      const float bi = s.beta[16 * I + r];
+      float acc = 0.f;
+      for (int Kb = J; Kb < I; ++Kb)
+#pragma unroll 4
+        for (int m = 0; m < 16; ++m)
+          acc += s.At[(16 * I + r) * LDS + 16 * Kb + m] * s.T[(16 * Kb + m) * LDS + 16 * J + c];
+      s.tmp[e] = bi * acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < npairs * 256; e += blockDim.x) {
+      const int J = e >> 8, I = J + d, r = (e >> 4) & 15, c = e & 15;
+      float acc = 0.f;
+      for (int m = 0; m <= r; ++m) acc += s.T[(16 * I + r) * LDS + 16 * I + m] * s.tmp[(J << 8) + m * 16 + c];
+      s.T[(16 * I + r) * LDS + 16 * J + c] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
+// Z_i += sum_{j<=i} M_ij Y_j * exp(gc_i - gc_j)   (rows i of this warp's block)
+// M is a masked [64][64] shared tile (stride LDS); Y a [64][128] shared tile.
+template <bool VEC>
+__device__ void left_apply(const ChunkSmem& s, const float* __restrict__ M, const float* __restrict__ Y,
+                           float (&Z)[16][4]) {
+  const int I = threadIdx.x >> 5, i0 = 16 * I;
+  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+  if (VEC) {
+    float acc[16][4];
+    zero_acc(acc);
+    if (I > 0) {
+      for (int kk = 0; kk < 2 * I; ++kk) {  // j in [0, 16I)
+        const int j0 = kk * 8 + t, j1 = j0 + 4;
+        uint32_t a[4] = {tf32(M[(i0 + g) * LDS + j0]), tf32(M[(i0 + g + 8) * LDS + j0]),
+                         tf32(M[(i0 + g) * LDS + j1]), tf32(M[(i0 + g + 8) * LDS + j1])};
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          const int c = nt * 8 + g;
+          const float bI = s.G[(i0 - 1) * LDT + c];
+          uint32_t b[2] = {tf32(Y[j0 * LDT + c] * ex2(bI - s.G[j0 * LDT + c])),
+                           tf32(Y[j1 * LDT + c] * ex2(bI - s.G[j1 * LDT + c]))};
+          mma8(acc[nt], a, b);
+        }
+      }
+      acc_foreach(acc, [&](int r, int col, float& x) {
+        Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[(i0 + r) * LDT + col] - s.G[(i0 - 1) * LDT + col]);
+      });
+    }
+    zero_acc(acc);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {  // j in the diagonal block
+      const int j0 = i0 + kk * 8 + t, j1 = j0 + 4;
+      uint32_t a[4] = {tf32(M[(i0 + g) * LDS + j0]), tf32(M[(i0 + g + 8) * LDS + j0]),
+                       tf32(M[(i0 + g) * LDS + j1]), tf32(M[(i0 + g + 8) * LDS + j1])};
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int c = nt * 8 + g;
+        const float mI = s.G[(i0 + 7) * LDT + c];
+        uint32_t b[2] = {tf32(Y[j0 * LDT + c] * ex2(mI - s.G[j0 * LDT + c])),
+                         tf32(Y[j1 * LDT + c] * ex2(mI - s.G[j1 * LDT + c]))};
+        mma8(acc[nt], a, b);
+      }
+    }
+    acc_foreach(acc, [&](int r, int col, float& x) {
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[(i0 + r) * LDT + col] - s.G[(i0 + 7) * LDT + col]);
+    });
+  } else {
+    for (int kk = 0; kk < 2 * I + 2; ++kk) {
+      const int j0 = kk * 8 + t, j1 = j0 + 4;
+      const int ra = i0 + g, rb = i0 + g + 8;
+      auto mv = [&](int i, int j) { return j <= i ? M[i * LDS + j] * ex2(s.gs[i] - s.gs[j]) : 0.f; };
+      uint32_t a[4] = {tf32(mv(ra, j0)), tf32(mv(rb, j0)), tf32(mv(ra, j1)), tf32(mv(rb, j1))};
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int c = nt * 8 + g;
+        uint32_t b[2] = {tf32(Y[j0 * LDT + c]), tf32(Y[j1 * LDT + c])};
+        mma8(Z[nt], a, b);
+      }
+    }
+  }
+}
+
+// Z_j += sum_{i>=j} (M0_ij Y0_i + beta_i M1_ij Y1_i) * exp(gc_i - gc_j)
+// (rows j of this warp's block).  M0, M1 masked [64][64] shared tiles.
+template <bool VEC>
+__device__ void right_apply2(const ChunkSmem& s, const float* __restrict__ M0, const float* __restrict__ Y0,
+                             const float* __restrict__ M1, const float* __restrict__ Y1, float (&Z)[16][4]) {
+  const int J = threadIdx.x >> 5, j0b = 16 * J;
+  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+  if (VEC) {
+    float acc[16][4];
+    zero_acc(acc);
+    const int ref = j0b + 15;  // gc at the end of block J
+    for (int kk = 2 * J + 2; kk < 8; ++kk) {  // i in blocks after J
+      const int ia = kk * 8 + t, ib = ia + 4;
+      uint32_t a0[4] = {tf32(M0[ia * LDS + j0b + g]), tf32(M0[ia * LDS + j0b + g + 8]),
+                        tf32(M0[ib * LDS + j0b + g]), tf32(M0[ib * LDS + j0b + g + 8])};
+      uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + j0b + g]), tf32(s.beta[ia] * M1[ia * LDS + j0b + g + 8]),
+                        tf32(s.beta[ib] * M1[ib * LDS + j0b + g]), tf32(s.beta[ib] * M1[ib * LDS + j0b + g + 8])};
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int c = nt * 8 + g;
+        const float bJ = s.G[ref * LDT + c];
+        const float ea = ex2(s.G[ia * LDT + c] - bJ), eb = ex2(s.G[ib * LDT + c] - bJ);
+        uint32_t b0[2] = {tf32(Y0[ia * LDT + c] * ea), tf32(Y0[ib * LDT + c] * eb)};
+        uint32_t b1[2] = {tf32(Y1[ia * LDT + c] * ea), tf32(Y1[ib * LDT + c] * eb)};
+        mma8(acc[nt], a0, b0);
+        mma8(acc[nt], a1, b1);
+      }
+    }
+    acc_foreach(acc, [&](int r, int col, float& x) {
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[ref * LDT + col] - s.G[(j0b + r) * LDT + col]);
+    });
+    zero_acc(acc);
+    const int mref = j0b + 7;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int ia = j0b + kk * 8 + t, ib = ia + 4;
+      uint32_t a0[4] = {tf32(M0[ia * LDS + j0b + g]), tf32(M0[ia * LDS + j0b + g + 8]),
+                        tf32(M0[ib * LDS + j0b + g]), tf32(M0[ib * LDS + j0b + g + 8])};
+      uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + j0b + g]), tf32(s.beta[ia] * M1[ia * LDS + j0b + g + 8]),
+                        tf32(s.beta[ib] * M1[ib * LDS + j0b + g]), tf32(s.beta[ib] * M1[ib * LDS + j0b + g + 8])};
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int c = nt * 8 + g;
+        const float mJ = s.G[mref * LDT + c];
+        const float ea = ex2(s.G[ia * LDT + c] - mJ), eb = ex2(s.G[ib * LDT + c] - mJ);
+        uint32_t b0[2] = {tf32(Y0[ia * LDT + c] * ea), tf32(Y0[ib * LDT + c] * eb)};
+        uint32_t b1[2] = {tf32(Y1[ia * LDT + c] * ea), tf32(Y1[ib * LDT + c] * eb)};
+        mma8(acc[nt], a0, b0);
+        mma8(acc[nt], a1, b1);
+      }
+    }
+    acc_foreach(acc, [&](int r, int col, float& x) {
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[mref * LDT + col] - s.G[(j0b + r) * LDT + col]);
+    });
+  } else {
+    for (int kk = 2 * J; kk < 8; ++kk) {
+      const int ia = kk * 8 + t, ib = ia + 4;
+      const int ja = j0b + g, jb = j0b + g + 8;
+      auto dec = [&](int i, int j) { return i >= j ? ex2(s.gs[i] - s.gs[j]) : 0.f; };
+      const float da0 = dec(ia, ja), da1 = dec(ia, jb), db0 = dec(ib, ja), db1 = dec(ib, jb);
+      uint32_t a0[4] = {tf32(M0[ia * LDS + ja] * da0), tf32(M0[ia * LDS + jb] * da1), tf32(M0[ib * LDS + ja] * db0),
+                        tf32(M0[ib * LDS + jb] * db1)};
+      uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + ja] * da0), tf32(s.beta[ia] * M1[ia * LDS + jb] * da1),
+                        tf32(s.beta[ib] * M1[ib * LDS + ja] * db0), tf32(s.beta[ib] * M1[ib * LDS + jb] * db1)};
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int c = nt * 8 + g;
+        uint32_t b0[2] = {tf32(Y0[ia * LDT + c]), tf32(Y0[ib * LDT + c])};
+        uint32_t b1[2] = {tf32(Y1[ia * LDT + c]), tf32(Y1[ib * LDT + c])};
+        mma8(Z[nt], a0, b0);
+        mma8(Z[nt], a1, b1);
+      }
+    }
+  }
+}
+
+}  // namespace gdr

@@ -1,0 +1,152 @@
+// gdr_common.cuh -- shared device helpers for the chunked gated delta rule.
+//
+// Chunked form (chunk C = 64 tokens, head dim 128), per (document, value head)
+// chain, derived from the token recurrence
+//   S_t = (I - beta_t k_t k_t^T) diag(exp g_t) S_{t-1} + beta_t k_t v_t^T,
+//   o_t = scale * S_t^T q_t
+// (the method of flashinfer PR #8218 "feat(cake_kda): ... Cake KDA
+// context-parallel (KCP) autograd backend" and PR #7723 "perf(cake_gdn):
+// prefetch offset adjoint walk, default LPT segment plan").  Inside one chunk
+// with start state S0, chunk-local cumulative log-decay gc_i = sum_{j<=i} g_j,
+// Gamma_i = exp(gc_i), gamma = Gamma_last:
+//   At  = strict_tril( (K*Gamma) (K/Gamma)^T )    (never formed that way: see
+//   Aqk = tril( (Q*Gamma) (K/Gamma)^T )             the block factorization)
+//   T   = (I + diag(beta) At)^-1
+//   w   = T diag(beta) (K*Gamma),   u = T diag(beta) V
+//   Delta = u - w S0
+//   O   = scale ( (Q*Gamma) S0 + Aqk Delta )
+//   S_end = diag(gamma) S0 + Kd^T Delta,   Kd = K * exp(gc_last - gc)
+//
+// Per-channel decays exp(gc_i - gc_j) are never split as exp(gc_i)*exp(-gc_j)
+// over a whole chunk (exp(-gc) overflows FP32 after ~18 tokens at g = -5).
+// Instead products over channels are factored per 16-row block pair with a
+// reference point between the two rows: for rows i in block I and j in an
+// earlier block, ref = gc at the end of block I-1 makes both factors <= 1;
+// inside a diagonal block, ref = gc at the block's 8th row bounds each factor
+// by exp(8 * max|g|) (< FP32 max for g >= -10).
+//
+// Matrix products use warp-level mma.sync m16n8k8 with TF32 operands
+// (round-to-nearest) and FP32 accumulation.  BF16 operands were measured on
+// the CPU emulation to miss the output tolerance; TF32 does not.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gdr {
+
+constexpr int CH = 64;     // chunk length (tokens)
+constexpr int DK = 128;    // head dimension (K = V = 128)
+constexpr int LDT = 132;   // shared-memory row stride of a [64][128] FP32 tile
+constexpr int LDS = 68;    // shared-memory row stride of a [64][64] FP32 tile
+constexpr float LOG2E = 1.4426950408889634f;
+
+// One 64-token chunk of one document.  Chunks restart at every document start.
+struct ChunkDesc {
+  int tok0;   // first token (index into the packed T axis)
+  int len;    // 1..64 valid rows
+  int doc;    // document index
+  int idx;    // chunk index within the document
+};
+
+// One document: its token range and its chunks [chunk0, chunk0 + nchunks).
+struct DocDesc {
+  int tok0, len, chunk0, nchunks;
+};
+
+__device__ __forceinline__ uint32_t tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// 2^x (the PTX approximate base-2 exponential).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D += A * B, m16n8k8, TF32 inputs, FP32 accumulate.
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
+
+// Fragment coordinates (PTX m16n8k8 .tf32 layouts):
+//   A: a0 (g, t) a1 (g+8, t) a2 (g, t+4) a3 (g+8, t+4)      [row, k]
+//   B: b0 (t, g) b1 (t+4, g)                                [k, col]
+//   C: c0 (g, 2t) c1 (g, 2t+1) c2 (g+8, 2t) c3 (g+8, 2t+1)  [row, col]
+// with g = lane / 4, t = lane % 4.
+
+// One k-step of 8 (k0 .. k0+7) of a warp product C[16 x 8*NT] += A * B over
+// n-tiles [nt0, nt1).  fa(i, k) and fb(k, n) return FP32 values.
+template <int NT, class FA, class FB>
+__device__ __forceinline__ void mma_kstep(float (&acc)[NT][4], int k0, int nt0, int nt1, FA fa, FB fb) {
+  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+  uint32_t a[4];
+  a[0] = tf32(fa(g, k0 + t));
+  a[1] = tf32(fa(g + 8, k0 + t));
+  a[2] = tf32(fa(g, k0 + t + 4));
+  a[3] = tf32(fa(g + 8, k0 + t + 4));
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    if (nt < nt0 || nt >= nt1) continue;
+    uint32_t b[2];
+    b[0] = tf32(fb(k0 + t, nt * 8 + g));
+    b[1] = tf32(fb(k0 + t + 4, nt * 8 + g));
+    mma8(acc[nt], a, b);
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+}
+
+// Visit every accumulator element: f(row, col, value&) with row in [0,16).
+template <int NT, class F>
+__device__ __forceinline__ void acc_foreach(float (&acc)[NT][4], F f) {
+  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) f(g + 8 * (r >> 1), nt * 8 + 2 * t + (r & 1), acc[nt][r]);
+  }
+}
+
+__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float ldg_bf(const __nv_bfloat16* p) { return __bfloat162float(__ldg(p)); }
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Offsets into the chunk-major intermediate buffers.
+__device__ __forceinline__ size_t tile_off(int chunk, int h, int HV) {  // [NC][HV][64][128]
+  return ((size_t)chunk * HV + h) * (CH * DK);
+}
+__device__ __forceinline__ size_t sq_off(int chunk, int h, int HV) {    // [NC][HV][64][64]
+  return ((size_t)chunk * HV + h) * (CH * CH);
+}
+__device__ __forceinline__ size_t state_off(int chunk, int h, int HV) { // [NC][HV][128][128]
+  return ((size_t)chunk * HV + h) * (DK * DK);
+}
+
+}  // namespace gdr

@@ -1,0 +1,97 @@
+// gdr_kernels.h -- kernel argument blocks and launchers (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gdr {
+
+struct ChunkDesc;
+struct DocDesc;
+
+// Chunk-major intermediates: tiles [NC][HV][64][128] FP32, Aqk [NC][HV][64][64],
+// gamma [NC][HV][128], state tapes [NC][HV][128][128] (S[k][v]).
+struct PrepArgs {
+  const __nv_bfloat16 *q, *k, *v;
+  const float* g;
+  const void* beta;  // bf16 (KDA) or fp32 (GDN)
+  const ChunkDesc* chunks;
+  int Hqk, HV;
+  float *w, *u, *qp, *kd, *aqk, *gam;
+};
+
+struct WalkArgs {
+  const DocDesc* docs;
+  const int* order;  // documents, longest first
+  int HV;
+  const float *w, *u, *kd, *gam;
+  const float* h0;   // [N][HV][128][128] or null
+  float* tape;       // S0 per chunk, or null
+  float* delta;      // Delta per chunk, or null
+  float* ht;         // [N][HV][128][128] or null
+};
+
+struct OutArgs {
+  const ChunkDesc* chunks;
+  int HV;
+  float scale;
+  const float *qp, *tape, *aqk, *delta;
+  __nv_bfloat16* out;  // [T][HV][128]
+};
+
+struct WalkBwdArgs {
+  const DocDesc* docs;
+  const int* order;
+  const ChunkDesc* chunks;
+  int HV;
+  float scale;
+  const float *w, *qp, *kd, *aqk, *gam;
+  const __nv_bfloat16* dout;  // [T][HV][128]
+  const float* dht;           // [N][HV][128][128] or null
+  float* dstape;              // dS (adjoint of each chunk's end state)
+  float* ddelta;              // dDelta per chunk
+  float* dh0;                 // or null
+};
+
+struct GradStateArgs {
+  const ChunkDesc* chunks;
+  int HV;
+  float scale;
+  const __nv_bfloat16* dout;
+  const float *tape, *dstape, *delta, *ddelta;
+  float *dqs, *dw, *dkd, *dgam;  // scratch outputs
+};
+
+struct GradArgs {
+  const __nv_bfloat16 *q, *k, *v;
+  const float* g;
+  const void* beta;
+  const __nv_bfloat16* dout;
+  const ChunkDesc* chunks;
+  int Hqk, HV;
+  float scale;
+  const float *w, *u, *kd, *gam, *aqk, *delta, *ddelta;
+  const float *dqs, *dw, *dkd, *dgam;
+  // outputs
+  __nv_bfloat16 *dq, *dk, *dv;   // dq/dk written directly when HV == Hqk
+  float *dq_part, *dk_part;      // [NC][HV][64][128] per value head when HV > Hqk
+  float* dg;
+  void* dbeta;
+};
+
+struct GroupReduceArgs {
+  const ChunkDesc* chunks;
+  int Hqk, HV;
+  const float *dq_part, *dk_part;
+  __nv_bfloat16 *dq, *dk;
+};
+
+cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
+cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int warps_per_cta, cudaStream_t st);
+cudaError_t launch_out(const OutArgs& a, int nchunks, cudaStream_t st);
+cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, cudaStream_t st);
+cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st);
+cudaError_t launch_grad(const GradArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
+cudaError_t launch_group_reduce(const GroupReduceArgs& a, int nchunks, cudaStream_t st);
+
+}  // namespace gdr

@@ -1,0 +1,130 @@
+/* gdr.h -- C ABI of the GB300 gated delta-rule training library (libgdr.so).
+ *
+ * Chunked training (forward and backward) of gated delta-rule linear
+ * attention over packed variable-length documents, head dimension 128, on one
+ * GPU (sm_103a), in two variants:
+ *
+ *   KDA  (Kimi Delta Attention): a per-channel log-decay gate g[t][h][0..127].
+ *        flashinfer PR #8218 "feat(cake_kda): with grad, add non-deterministic
+ *        Cake KDA context-parallel (KCP) autograd backend", opening description
+ *        and "Workload" paragraph: packed documents, q/k/v BF16 [T,H,128] with q
+ *        and k L2-normalized, g FP32 [T,H,128] pre-activated (no sigmoid, no
+ *        softplus, no in-kernel L2 norm), beta BF16 [T,H].
+ *   GDN  (Gated DeltaNet): a scalar log-decay per (token, value head) and
+ *        grouped Q/K heads.  flashinfer PR #7723 "perf(cake_gdn): prefetch
+ *        offset adjoint walk, default LPT segment plan", opening description:
+ *        BF16 q/k/v/out/dout, FP32 g and beta, (H_qk, HV) runtime parameters,
+ *        dq/dk reduced in FP32 over the value heads of each Q/K head and
+ *        converted to the output type once.
+ *
+ * The recurrence, per (document, value head), state S (K x V = 128 x 128,
+ * stored S[k][v]) reset to h0[doc] (or zero) at every document start:
+ *     S_t = (I - beta_t k_t k_t^T) diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *     ht[doc] = S after the document's last token.
+ * exp(g_t) scales the K index (rows) of S.  For GDN, value head j uses Q/K
+ * head j / (HV / Hqk) (contiguous groups).
+ *
+ * Conventions (all entry points):
+ *   - Pointers without a _host suffix are DEVICE pointers; buffers are dense,
+ *     row-major, and owned by the caller.  The library never allocates device
+ *     memory and never synchronizes the host with the device: every call only
+ *     enqueues work on `stream` and returns.
+ *   - Layouts.  q, k, dq, dk: [T][Hqk][128] BF16 (KDA: Hqk = HV = H).
+ *     v, out, dout, dv: [T][HV][128] BF16.  KDA g, dg: [T][H][128] FP32;
+ *     GDN g, dg: [T][HV] FP32.  KDA beta, dbeta: [T][H] BF16; GDN beta, dbeta:
+ *     [T][HV] FP32.  States h0, ht, dht, dh0: [N][HV][128][128] FP32, S[k][v].
+ *   - cu_seqlens: int32 [N+1] with cu[0] = 0, non-decreasing, cu[N] = T.
+ *     Empty documents are allowed (their state passes h0 -> ht).  The device
+ *     copy and the host copy (cu_seqlens_host) must hold the same values; the
+ *     host copy sizes the launches, the device copy drives the kernels.
+ *   - Gate precondition: g finite and >= -10 (the per-block gate
+ *     factorization keeps every exponent below FP32 overflow for 8 tokens x
+ *     10 = 80 < 88.7).  Outside that range results are unspecified.
+ *   - Workspaces.  `saved` carries the forward's intermediates to the
+ *     backward; `scratch` holds temporaries.  Sizes come from
+ *     *_workspace_bytes.  Both must be 256-byte aligned.  `saved` belongs to
+ *     the caller between a forward with save_for_bwd = 1 and the backward.
+ *   - Errors are returned as gdr_status, never thrown; a call that returns an
+ *     error has enqueued nothing (except GDR_CUDA_ERROR from a launch).
+ *   - Calls on one stream are ordered; calls that share a workspace must not
+ *     overlap on the GPU.
+ *   - Results are deterministic (no floating-point atomics).
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gdr_bf16; /* raw bfloat16 bits */
+typedef int gdr_status;
+
+#define GDR_OK 0
+#define GDR_INVALID_ARG 1          /* null pointer, bad size, bad head counts, misaligned workspace */
+#define GDR_BAD_CU_SEQLENS 2       /* cu[0] != 0, decreasing, or cu[N] != T */
+#define GDR_WORKSPACE_TOO_SMALL 3  /* saved_bytes / scratch_bytes below *_workspace_bytes */
+#define GDR_UNSUPPORTED 4          /* device is not sm_103 (GB300 / B300) */
+#define GDR_STALE_WORKSPACE 5      /* `saved` not filled by a matching forward with save_for_bwd = 1 */
+#define GDR_CUDA_ERROR 6           /* a CUDA launch or runtime call failed */
+
+/* Human-readable name of a status code (static string). */
+const char* gdr_status_string(gdr_status status);
+
+/* Workspace sizes for a KDA problem (host-only; no CUDA calls).
+ * saved_bytes: the forward's intermediates kept for the backward (chunk
+ * tables, w, u, Q*Gamma, Kd, Delta, Aqk, gamma, and the per-chunk state tape).
+ * scratch_bytes: temporaries of the backward.  A forward called without a
+ * `saved` buffer keeps its intermediates in `scratch`, which must then hold
+ * saved_bytes.  Returns GDR_BAD_CU_SEQLENS or GDR_INVALID_ARG on bad input. */
+gdr_status kda_workspace_bytes(int64_t T, int32_t H, int32_t N, const int32_t* cu_seqlens_host,
+                               size_t* saved_bytes, size_t* scratch_bytes);
+
+/* KDA forward.  Writes out [T][H][128] and, when non-null, ht [N][H][128][128].
+ * h0 may be null (zero initial state).  When save_for_bwd is non-zero, the
+ * intermediates go to `saved` (saved_bytes >= the queried size) and the
+ * buffer is stamped for kda_bwd; otherwise `saved` may be null and the
+ * intermediates go to `scratch`. */
+gdr_status kda_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
+                   float scale, const float* h0, gdr_bf16* out, float* ht, void* saved, size_t saved_bytes,
+                   int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+
+/* KDA backward from a forward with save_for_bwd = 1 on the same inputs.
+ * dout [T][H][128]; dht may be null (zero).  Writes dq, dk, dv [T][H][128]
+ * BF16, dg [T][H][128] FP32, dbeta [T][H] BF16 and, when non-null, dh0.
+ * Returns GDR_STALE_WORKSPACE when `saved` was not stamped by a forward with
+ * the same T, H, N and cu_seqlens in this process. */
+gdr_status kda_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
+                   float scale, const float* h0, const gdr_bf16* dout, const float* dht, const void* saved,
+                   size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg, gdr_bf16* dbeta,
+                   float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+
+/* GDN counterparts: Hqk Q/K heads, HV value heads (HV % Hqk == 0), scalar
+ * FP32 gate g [T][HV] and FP32 beta [T][HV]; dq/dk are [T][Hqk][128], summed
+ * in FP32 over the value heads of each Q/K head. */
+gdr_status gdn_workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const int32_t* cu_seqlens_host,
+                               size_t* saved_bytes, size_t* scratch_bytes);
+
+gdr_status gdn_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t Hqk,
+                   int32_t HV, float scale, const float* h0, gdr_bf16* out, float* ht, void* saved,
+                   size_t saved_bytes, int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+
+gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const float* beta,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t Hqk,
+                   int32_t HV, float scale, const float* h0, const gdr_bf16* dout, const float* dht,
+                   const void* saved, size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg,
+                   float* dbeta, float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H_ */

@@ -1,0 +1,66 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the binding and
+the FP64 oracle on the same seeded inputs, and compare.
+
+Tolerances (relative L2 over the whole compared tensor): out and ht 3e-3,
+every gradient (dq, dk, dv, dg, dbeta, dh0) 1e-2.
+"""
+import numpy as np
+import torch
+
+import oracle
+
+TOL = {"out": 3e-3, "ht": 3e-3, "dq": 1e-2, "dk": 1e-2, "dv": 1e-2, "dg": 1e-2, "dbeta": 1e-2, "dh0": 1e-2}
+SCALE = 128 ** -0.5
+
+
+def rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    nb = np.linalg.norm(b)
+    if nb == 0.0:
+        return float(np.linalg.norm(a))
+    return float(np.linalg.norm(a - b) / nb)
+
+
+def f64(t):
+    return None if t is None else t.detach().double().cpu().numpy()
+
+
+def run_gpu(variant, x, cu, scale=SCALE, h0=None, dht=None, backward=True, want_dh0=False, dev="cuda"):
+    import gated_delta_rule_varlen_gb300 as gdr
+
+    xd = {k: v.to(dev) for k, v in x.items()}
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=dev)
+    h0d = None if h0 is None else h0.to(dev)
+    dhtd = None if dht is None else dht.to(dev)
+    fwd = gdr.kda_fwd if variant == "kda" else gdr.gdn_fwd
+    bwd = gdr.kda_bwd if variant == "kda" else gdr.gdn_bwd
+    out, ht, saved = fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, scale, h0=h0d,
+                         save_for_bwd=backward)
+    res = {"out": out, "ht": ht}
+    if backward:
+        res.update(bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, scale, xd["dout"], saved, h0=h0d,
+                       dht=dhtd, want_dh0=want_dh0))
+    torch.cuda.synchronize()
+    return res
+
+
+def run_oracle(x, cu, scale=SCALE, h0=None, dht=None, backward=True):
+    f = {k: f64(v) for k, v in x.items()}
+    return oracle.run(f["q"], f["k"], f["v"], f["g"], f["beta"], cu, scale, h0=f64(h0),
+                      dout=f["dout"] if backward else None, dht=f64(dht))
+
+
+def compare(gpu, ref, names=None):
+    names = names or [n for n in TOL if n in gpu and n in ref and gpu[n] is not None]
+    errs = {}
+    for n in names:
+        errs[n] = rel(f64(gpu[n]) if torch.is_tensor(gpu[n]) else gpu[n], ref[n])
+    return errs
+
+
+def assert_within(errs, tol=TOL):
+    bad = {k: v for k, v in errs.items() if not (v <= tol[k])}
+    msg = " ".join(f"{k}={v:.3e}" for k, v in errs.items())
+    assert not bad, f"parity failed: {bad} (all: {msg})"
+    return msg

@@ -1,0 +1,204 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle on
+the same seeded inputs.  Small cases compare every element; the full-size
+workloads compare sampled (document, head) chains, which the oracle computes
+independently of the rest of the pack.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import SCALE, TOL, assert_within, compare, f64, rel, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import gated_delta_rule_varlen_gb300 as gdr
+    gdr.load()
+
+
+def _case(variant, lengths, Hqk, HV, seed=0, h0=False, dht=False, glow=-5.0, ghigh=0.0):
+    T = sum(lengths)
+    cu = synth.cu_from_lengths(lengths)
+    x = synth.make_inputs(variant, T, Hqk, HV, 128, seed=seed, gate_low=glow, gate_high=ghigh)
+    h0t = synth.make_states(len(lengths), HV, 128, seed=seed + 11, scale=0.05) if h0 else None
+    dhtt = synth.make_states(len(lengths), HV, 128, seed=seed + 12, scale=0.05) if dht else None
+    return x, cu, h0t, dhtt
+
+
+def _check(variant, lengths, Hqk, HV, **kw):
+    x, cu, h0, dht = _case(variant, lengths, Hqk, HV, **kw)
+    gpu = run_gpu(variant, x, cu, h0=h0, dht=dht, want_dh0=h0 is not None)
+    ref = run_oracle(x, cu, h0=h0, dht=dht)
+    errs = compare(gpu, ref)
+    print(variant, lengths, assert_within(errs))
+    return gpu, ref
+
+
+def test_kda_tiny_config():
+    # One document of 512 tokens, H = 1, seed 0.
+    _check("kda", [512], 1, 1)
+
+
+def test_kda_ragged_edges_with_states():
+    _check("kda", [1, 63, 64, 65, 0, 127, 128, 129, 200], 2, 2, seed=1, h0=True, dht=True)
+
+
+def test_gdn_grouped_ragged_with_states():
+    _check("gdn", [5, 64, 130, 0, 71], 2, 6, seed=2, h0=True, dht=True)
+
+
+def test_gdn_production_heads_small_pack():
+    _check("gdn", [300, 211], 16, 48, seed=3)
+
+
+def test_kda_mild_gates_long_document():
+    # Gates near zero keep the state alive across all 64 chunks.
+    _check("kda", [4096], 1, 1, seed=4, glow=-0.05, h0=True, dht=True)
+
+
+def test_gdn_mild_gates_long_document():
+    _check("gdn", [4096], 1, 2, seed=5, glow=-0.05, h0=True)
+
+
+def test_kda_zero_gate():
+    _check("kda", [1000], 1, 1, seed=6, glow=0.0, ghigh=0.0)
+
+
+def test_kda_strong_gates_lower_bound():
+    # Gates down to -10 (the library's stated lower bound).
+    _check("kda", [300], 1, 1, seed=7, glow=-10.0)
+
+
+def test_packed_equals_per_document_bitwise():
+    lengths = [70, 1, 130, 64]
+    x, cu, h0, dht = _case("kda", lengths, 2, 2, seed=8, h0=True, dht=True)
+    whole = run_gpu("kda", x, cu, h0=h0, dht=dht, want_dh0=True)
+    for n in range(len(lengths)):
+        s, e = cu[n], cu[n + 1]
+        xs = {k: v[s:e] for k, v in x.items()}
+        one = run_gpu("kda", xs, [0, e - s], h0=h0[n:n + 1], dht=dht[n:n + 1], want_dh0=True)
+        for name in ("out", "dq", "dk", "dv", "dg", "dbeta"):
+            assert torch.equal(whole[name][s:e], one[name]), name
+        assert torch.equal(whole["ht"][n], one["ht"][0])
+        assert torch.equal(whole["dh0"][n], one["dh0"][0])
+
+
+def test_repeat_is_bitwise_deterministic():
+    x, cu, h0, dht = _case("gdn", [200, 333], 2, 6, seed=9)
+    a = run_gpu("gdn", x, cu)
+    b = run_gpu("gdn", x, cu)
+    for name in ("out", "ht", "dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(a[name], b[name]), name
+
+
+def test_empty_documents_pass_state_through():
+    x, cu, h0, dht = _case("kda", [0, 0], 1, 1, seed=10, h0=True, dht=True)
+    gpu = run_gpu("kda", x, cu, h0=h0, dht=dht, want_dh0=True)
+    assert torch.equal(gpu["ht"].cpu(), h0)
+    assert torch.equal(gpu["dh0"].cpu(), dht)
+
+
+def test_workspace_errors_on_gpu():
+    import gated_delta_rule_varlen_gb300 as gdr
+    x, cu, _, _ = _case("kda", [100], 1, 1, seed=11)
+    xd = {k: v.cuda() for k, v in x.items()}
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    out, ht, saved = gdr.kda_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE)
+    # A saved buffer stamped for another pack is rejected.
+    with pytest.raises(gdr.GdrError) as ei:
+        cu2 = [0, 50, 100]
+        gdr.kda_bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], torch.tensor(cu2, dtype=torch.int32,
+                    device="cuda"), cu2, SCALE, xd["dout"], saved)
+    assert ei.value.status == gdr.GDR_STALE_WORKSPACE
+    # Too-small scratch.
+    with pytest.raises(ValueError):
+        gdr.kda_bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE, xd["dout"], saved,
+                    scratch=torch.empty(1024, dtype=torch.uint8, device="cuda"))
+
+
+def test_ckpt_sequence_matches_plain_backward():
+    # ckpt = forward (no save), forward (save), backward: same results as forward + backward.
+    import gated_delta_rule_varlen_gb300 as gdr
+    x, cu, _, _ = _case("kda", [300, 77], 2, 2, seed=12)
+    xd = {k: v.cuda() for k, v in x.items()}
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    a = run_gpu("kda", x, cu)
+    o1, _, _ = gdr.kda_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE, save_for_bwd=False)
+    o2, _, saved = gdr.kda_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE)
+    gr = gdr.kda_bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE, xd["dout"], saved)
+    assert torch.equal(o1, a["out"]) and torch.equal(o2, a["out"])
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(gr[name], a[name]), name
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: sampled chains.
+# ---------------------------------------------------------------------------
+def _full_case(name, seed=0):
+    wl = synth.workload(name)
+    x = synth.make_inputs(wl.variant, wl.T, wl.Hqk, wl.HV, 128, seed=seed, device="cuda")
+    return wl, x
+
+
+def _sample_check(wl, x, gpu, samples):
+    """samples: list of (doc, qk_head).  The oracle runs the chains of that
+    document for every value head of the Q/K head (GDN: the whole group)."""
+    from concurrent.futures import ThreadPoolExecutor
+    cu = wl.cu_seqlens
+    G = wl.HV // wl.Hqk
+
+    def one(sample):
+        n, hq = sample
+        s, e = cu[n], cu[n + 1]
+        hv = list(range(hq * G, hq * G + G))
+        xs = {
+            "q": x["q"][s:e, hq:hq + 1].cpu(), "k": x["k"][s:e, hq:hq + 1].cpu(),
+            "v": x["v"][s:e, hv].cpu(), "g": x["g"][s:e, hv].cpu(), "beta": x["beta"][s:e, hv].cpu(),
+            "dout": x["dout"][s:e, hv].cpu(),
+        }
+        ref = run_oracle(xs, [0, e - s])
+        got = {
+            "out": f64(gpu["out"][s:e, hv]), "ht": f64(gpu["ht"][n, hv]), "dq": f64(gpu["dq"][s:e, hq:hq + 1]),
+            "dk": f64(gpu["dk"][s:e, hq:hq + 1]), "dv": f64(gpu["dv"][s:e, hv]), "dg": f64(gpu["dg"][s:e, hv]),
+            "dbeta": f64(gpu["dbeta"][s:e, hv]),
+        }
+        return sample, {k: rel(got[k], ref[k]) for k in got}
+
+    with ThreadPoolExecutor(max_workers=len(samples)) as ex:
+        results = list(ex.map(one, samples))
+    for sample, errs in results:
+        print(wl.name, sample, assert_within(errs))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,samples", [
+    ("kda_pack_h16", [(0, 3), (3, 11)]),
+    ("kda_pack_h4", [(1, 0)]),
+    ("kda_pack_h64", [(2, 63)]),
+])
+def test_fullsize_kda_sampled_chains(name, samples):
+    wl, x = _full_case(name)
+    gpu = run_gpu("kda", x, wl.cu_seqlens)
+    for k in ("out", "dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.isfinite(gpu[k]).all(), k
+    _sample_check(wl, x, gpu, samples)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,samples", [
+    ("gdn_p1", [(None, 7)]),
+    ("gdn_1doc", [(0, 2)]),
+])
+def test_fullsize_gdn_sampled_chains(name, samples):
+    wl, x = _full_case(name)
+    if samples[0][0] is None:  # the shortest document of the seeded pack
+        samples = [(int(np.argmin(wl.lengths)), samples[0][1])]
+    gpu = run_gpu("gdn", x, wl.cu_seqlens)
+    for k in ("out", "dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.isfinite(gpu[k]).all(), k
+    _sample_check(wl, x, gpu, samples)
