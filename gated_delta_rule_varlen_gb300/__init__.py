@@ -38,6 +38,8 @@ EXPORTED = (
     "gdn_workspace_bytes",
     "gdn_fwd",
     "gdn_bwd",
+    "gdr_profile_enable",
+    "gdr_profile_report",
 )
 
 _lock = threading.Lock()
@@ -53,6 +55,8 @@ PSZ = ctypes.POINTER(ctypes.c_size_t)
 
 _SIGS = {
     "gdr_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "gdr_profile_enable": ([ctypes.c_int], ctypes.c_int),
+    "gdr_profile_report": ([ctypes.c_char_p, SZ], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P], ctypes.c_int),
@@ -236,3 +240,19 @@ def gdn_bwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h
             scratch=None, grads=None, stream=None):
     return _bwd("gdn", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0,
                 scratch, grads, stream)
+
+
+def gdr_profile_enable(on: bool = True):
+    """Start (True) or stop (False) per-kernel CUDA-event timing; starting clears old records."""
+    load().gdr_profile_enable(int(bool(on)))
+
+
+def gdr_profile_report():
+    """{kernel name: (launches, total_ms)} of the launches recorded while profiling was on."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    _check(load().gdr_profile_report(buf, len(buf)), "gdr_profile_report")
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, n, ms = line.split()
+        out[name] = (int(n), float(ms))
+    return out

@@ -5,6 +5,10 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
+#include <string>
+#include <map>
+#include <vector>
+#include <cstdio>
 
 #include "../../include/gdr.h"
 #include "gdr_common.cuh"
@@ -198,6 +202,46 @@ bool aligned(const void* p) { return ((uintptr_t)p % kAlign) == 0; }
 
 gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_CUDA_ERROR; }
 
+// ---------------------------------------------------------------------------
+// Opt-in per-kernel timing for benchmarks: while enabled, every launch is
+// bracketed by a pair of CUDA events recorded on the launch's stream.
+// ---------------------------------------------------------------------------
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+
+void prof_clear_locked() {
+  for (auto& r : g_prof) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof.clear();
+}
+
+struct ProfScope {
+  cudaStream_t st;
+  bool on;
+  ProfScope(const char* name, cudaStream_t s) : st(s), on(false) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return;
+    ProfRec r{name, nullptr, nullptr};
+    if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
+    cudaEventRecord(r.a, st);
+    g_prof.push_back(r);
+    on = true;
+  }
+  ~ProfScope() {
+    if (!on) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    cudaEventRecord(g_prof.back().b, st);
+  }
+};
+
+
 template <typename T>
 T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
@@ -243,7 +287,10 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   DocDesc* docs = at<DocDesc>(base, L.docs);
   ChunkDesc* chunks = at<ChunkDesc>(base, L.chunks);
   int* order = at<int>(base, L.order);
-  k_plan<<<1, 1024, 0, stream>>>(cu, N, docs, chunks, order);
+  {
+    ProfScope ps("plan", stream);
+    k_plan<<<1, 1024, 0, stream>>>(cu, N, docs, chunks, order);
+  }
   if (cudaGetLastError() != cudaSuccess) return GDR_CUDA_ERROR;
   const bool vec = variant == 0;
   PrepArgs pa{};
@@ -261,7 +308,10 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   pa.kd = at<float>(base, L.kd);
   pa.aqk = at<float>(base, L.aqk);
   pa.gam = at<float>(base, L.gam);
-  st = cuda_status(launch_prep(pa, (int)NC, vec, vec, stream));
+  {
+    ProfScope ps("prep", stream);
+    st = cuda_status(launch_prep(pa, (int)NC, vec, vec, stream));
+  }
   if (st != GDR_OK) return st;
   WalkArgs wa{};
   wa.docs = docs;
@@ -275,7 +325,10 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   wa.tape = at<float>(base, L.tape);
   wa.delta = at<float>(base, L.delta);
   wa.ht = ht;
-  st = cuda_status(launch_walk_fwd(wa, N, walk_warps((int64_t)N * HV), stream));
+  {
+    ProfScope ps("walk_fwd", stream);
+    st = cuda_status(launch_walk_fwd(wa, N, walk_warps((int64_t)N * HV), stream));
+  }
   if (st != GDR_OK) return st;
   OutArgs oa{};
   oa.chunks = chunks;
@@ -286,7 +339,10 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   oa.aqk = pa.aqk;
   oa.delta = wa.delta;
   oa.out = static_cast<__nv_bfloat16*>(out);
-  st = cuda_status(launch_out(oa, (int)NC, stream));
+  {
+    ProfScope ps("out", stream);
+    st = cuda_status(launch_out(oa, (int)NC, stream));
+  }
   if (st != GDR_OK) return st;
   if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, hash_cu(cu_host, N)});
   return GDR_OK;
@@ -331,7 +387,10 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   wb.dstape = at<float>(scratch, L.dstape);
   wb.ddelta = at<float>(scratch, L.ddelta);
   wb.dh0 = dh0;
-  st = cuda_status(launch_walk_bwd(wb, N, walk_warps((int64_t)N * HV), stream));
+  {
+    ProfScope ps("walk_bwd", stream);
+    st = cuda_status(launch_walk_bwd(wb, N, walk_warps((int64_t)N * HV), stream));
+  }
   if (st != GDR_OK) return st;
 
   GradStateArgs gs{};
@@ -347,7 +406,10 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   gs.dw = at<float>(scratch, L.dw);
   gs.dkd = at<float>(scratch, L.dkd);
   gs.dgam = at<float>(scratch, L.dgam);
-  st = cuda_status(launch_grad_state(gs, (int)NC, stream));
+  {
+    ProfScope ps("grad_state", stream);
+    st = cuda_status(launch_grad_state(gs, (int)NC, stream));
+  }
   if (st != GDR_OK) return st;
 
   GradArgs ga{};
@@ -380,7 +442,10 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   ga.dk_part = grouped ? at<float>(scratch, L.dkp) : nullptr;
   ga.dg = dg;
   ga.dbeta = dbeta;
-  st = cuda_status(launch_grad(ga, (int)NC, vec, vec, stream));
+  {
+    ProfScope ps("grad", stream);
+    st = cuda_status(launch_grad(ga, (int)NC, vec, vec, stream));
+  }
   if (st != GDR_OK) return st;
   if (grouped) {
     GroupReduceArgs gr{};
@@ -391,7 +456,10 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
     gr.dk_part = ga.dk_part;
     gr.dq = ga.dq;
     gr.dk = ga.dk;
-    st = cuda_status(launch_group_reduce(gr, (int)NC, stream));
+    {
+      ProfScope ps("group_reduce", stream);
+      st = cuda_status(launch_group_reduce(gr, (int)NC, stream));
+    }
     if (st != GDR_OK) return st;
   }
   return GDR_OK;
@@ -459,6 +527,41 @@ gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
   (void)h0;
   return gdr::bwd_impl(1, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, Hqk, HV, scale, dout, dht, saved,
                        saved_bytes, dq, dk, dv, dg, dbeta, dh0, scratch, scratch_bytes, stream);
+}
+
+int gdr_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(gdr::g_prof_mu);
+  if (on) gdr::prof_clear_locked();
+  gdr::g_prof_on = on != 0;
+  return GDR_OK;
+}
+
+gdr_status gdr_profile_report(char* buf, size_t buf_bytes) {
+  std::lock_guard<std::mutex> lk(gdr::g_prof_mu);
+  std::map<std::string, std::pair<int, double>> agg;
+  std::vector<std::string> order;
+  for (auto& r : gdr::g_prof) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return GDR_CUDA_ERROR;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return GDR_CUDA_ERROR;
+    auto it = agg.find(r.name);
+    if (it == agg.end()) {
+      order.push_back(r.name);
+      agg[r.name] = {1, (double)ms};
+    } else {
+      it->second.first += 1;
+      it->second.second += ms;
+    }
+  }
+  std::string out;
+  for (auto& n : order) {
+    char line[160];
+    std::snprintf(line, sizeof(line), "%s %d %.6f\n", n.c_str(), agg[n].first, agg[n].second);
+    out += line;
+  }
+  if (!buf || buf_bytes < out.size() + 1) return GDR_INVALID_ARG;
+  std::memcpy(buf, out.c_str(), out.size() + 1);
+  return GDR_OK;
 }
 
 }  // extern "C"

@@ -123,6 +123,17 @@ gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
                    const void* saved, size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg,
                    float* dbeta, float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 
+/* Benchmark support (no counterpart on the pages): opt-in per-kernel timing.
+ * gdr_profile_enable(1) clears previous records and makes every subsequent
+ * kernel launch of this library record a pair of CUDA events on its stream;
+ * gdr_profile_enable(0) stops recording and keeps the records for the report.  gdr_profile_report synchronizes the
+ * recorded events and writes one line per kernel, "<name> <launches>
+ * <total_ms>\n", in first-launch order, NUL-terminated, into buf; it returns
+ * GDR_INVALID_ARG if buf_bytes is too small.  Kernel names: plan, prep,
+ * walk_fwd, out, walk_bwd, grad_state, grad, group_reduce. */
+int gdr_profile_enable(int on);
+gdr_status gdr_profile_report(char* buf, size_t buf_bytes);
+
 #ifdef __cplusplus
 }
 #endif
