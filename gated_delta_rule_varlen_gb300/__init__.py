@@ -35,6 +35,7 @@ EXPORTED = (
     "kda_workspace_bytes",
     "kda_fwd",
     "kda_bwd",
+    "kda_fwd_noalloc",
     "gdn_workspace_bytes",
     "gdn_fwd",
     "gdn_bwd",
@@ -62,6 +63,7 @@ _SIGS = {
     "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P], ctypes.c_int),
     "kda_bwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, P, P, P, P, P, P, P, SZ, P],
                 ctypes.c_int),
+    "kda_fwd_noalloc": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P], ctypes.c_int),
     "gdn_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P],
                 ctypes.c_int),
     "gdn_bwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, I32, F32, P, P, P, P, SZ, P, P, P, P, P, P, P, SZ, P],
@@ -256,3 +258,15 @@ def gdr_profile_report():
         name, n, ms = line.split()
         out[name] = (int(n), float(ms))
     return out
+
+
+def kda_fwd_noalloc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, out, ht=None, h0=None, stream=None):
+    """KDA forward whose intermediates live in the library's fixed 64 MiB device
+    array (for callers that cannot allocate; see include/gdr.h).  `out` (and
+    `ht`, if wanted) must be preallocated: this wrapper allocates nothing."""
+    T, H, _ = q.shape
+    arr, cup = _cu_host(cu_seqlens_host)
+    st = load().kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), cup,
+                                arr.shape[0] - 1, T, H, float(scale), _ptr(h0), _ptr(out), _ptr(ht), _stream(stream))
+    _check(st, "kda_fwd_noalloc")
+    return out, ht

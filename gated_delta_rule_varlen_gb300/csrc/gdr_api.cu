@@ -465,6 +465,41 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   return GDR_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// Fixed device scratch for the no-allocation forward (kda_fwd_noalloc).
+// Every GPU that loads this library holds this array until the process exits.
+// Host code must not use the symbol itself as a device address: the device
+// address is looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device (looked up on the
+// first call per device; later calls reuse it).  Returns null on failure.
+void* static_scratch_ptr(gdr_status* st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *st = GDR_CUDA_ERROR;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+      *st = GDR_CUDA_ERROR;
+      return nullptr;
+    }
+    g_static_ptr[dev] = p;
+  }
+  *st = GDR_OK;
+  return g_static_ptr[dev];
+}
+
 }  // namespace
 }  // namespace gdr
 
@@ -527,6 +562,22 @@ gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
   (void)h0;
   return gdr::bwd_impl(1, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, Hqk, HV, scale, dout, dht, saved,
                        saved_bytes, dq, dk, dv, dg, dbeta, dh0, scratch, scratch_bytes, stream);
+}
+
+gdr_status kda_fwd_noalloc(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g,
+                           const gdr_bf16* beta, const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                           int32_t N, int64_t T, int32_t H, float scale, const float* h0, gdr_bf16* out, float* ht,
+                           cudaStream_t stream) {
+  size_t need = 0;
+  const gdr_status qs = gdr::workspace_bytes(T, H, H, N, cu_seqlens_host, &need, nullptr);
+  if (qs != GDR_OK) return qs;
+  if (need > gdr::kStaticScratchBytes) return GDR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return GDR_OK;
+  gdr_status st = GDR_OK;
+  void* scratch = gdr::static_scratch_ptr(&st);
+  if (!scratch) return st;
+  return gdr::fwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, h0, out, ht, nullptr, 0,
+                       0, scratch, gdr::kStaticScratchBytes, stream);
 }
 
 int gdr_profile_enable(int on) {

@@ -106,6 +106,34 @@ gdr_status kda_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
                    size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg, gdr_bf16* dbeta,
                    float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 
+/* No-allocation KDA forward.  The paper has no counterpart; this entry point
+ * exists for callers that cannot allocate device memory at call time: code
+ * running under CUDA stream capture in global mode (where cudaMalloc is not
+ * permitted), engines and plugins whose host framework owns every device byte
+ * and forbids side allocations, and real-time paths that must not take the
+ * allocator's locks or risk an out-of-memory failure mid-step.
+ *
+ * Same arguments and results as kda_fwd with save_for_bwd = 0, but the
+ * forward's intermediates live in one fixed 64 MiB device array inside the
+ * library (held by every GPU that loads the library until the process exits)
+ * instead of caller-provided workspaces, and nothing is saved for a backward.
+ * Limit: the problem's intermediates (the saved_bytes that kda_workspace_bytes
+ * reports for the same T, H, cu_seqlens) must fit in 64 MiB -- about 270
+ * (chunk, head) pairs, e.g. 4096 tokens at H = 4; larger problems are rejected
+ * with GDR_WORKSPACE_TOO_SMALL before anything is enqueued.  The call itself
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array, which keeps
+ * the previous call's contents; no byte of it needs to start at zero (each
+ * call writes everything it reads).  Calls that overlap on the GPU (for
+ * example on two streams) race on the array and must be serialized. */
+gdr_status kda_fwd_noalloc(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g,
+                           const gdr_bf16* beta, const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                           int32_t N, int64_t T, int32_t H, float scale, const float* h0, gdr_bf16* out, float* ht,
+                           cudaStream_t stream);
+
 /* GDN counterparts: Hqk Q/K heads, HV value heads (HV % Hqk == 0), scalar
  * FP32 gate g [T][HV] and FP32 beta [T][HV]; dq/dk are [T][Hqk][128], summed
  * in FP32 over the value heads of each Q/K head. */
