@@ -86,7 +86,7 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
   const size_t tile = (size_t)NC * HV * CH * DK * sizeof(float);
   const size_t sq = (size_t)NC * HV * CH * CH * sizeof(float);
   const size_t vec = (size_t)NC * HV * DK * sizeof(float);
-  const size_t st = (size_t)NC * HV * DK * DK * sizeof(float);
+  const size_t st = (size_t)NC * HV * DK * DK * sizeof(uint16_t);  // BF16 state tapes
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -322,7 +322,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   wa.kd = pa.kd;
   wa.gam = pa.gam;
   wa.h0 = h0;
-  wa.tape = at<float>(base, L.tape);
+  wa.tape = at<__nv_bfloat16>(base, L.tape);
   wa.delta = at<float>(base, L.delta);
   wa.ht = ht;
   {
@@ -384,7 +384,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   wb.gam = at<float>(saved, L.gam);
   wb.dout = static_cast<const __nv_bfloat16*>(dout);
   wb.dht = dht;
-  wb.dstape = at<float>(scratch, L.dstape);
+  wb.dstape = at<__nv_bfloat16>(scratch, L.dstape);
   wb.ddelta = at<float>(scratch, L.ddelta);
   wb.dh0 = dh0;
   {
@@ -398,7 +398,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   gs.HV = HV;
   gs.scale = scale;
   gs.dout = wb.dout;
-  gs.tape = at<float>(saved, L.tape);
+  gs.tape = at<__nv_bfloat16>(saved, L.tape);
   gs.dstape = wb.dstape;
   gs.delta = at<float>(saved, L.delta);
   gs.ddelta = wb.ddelta;

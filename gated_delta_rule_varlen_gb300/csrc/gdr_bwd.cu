@@ -25,20 +25,33 @@ namespace gdr {
 // ---------------------------------------------------------------------------
 // Reverse adjoint walk (one CTA per (document, value head, value-column
 // slice), chunks in reverse).  Each warp owns 16 value columns of dS^T.
-// The "adjoint walk" of PR #7723 "perf(cake_gdn): prefetch offset adjoint
-// walk, default LPT segment plan" (opening description).
+// Per chunk: phase 1 uses Aqk, Kd, dO (tiles of group A, double-buffered),
+// phase 2 uses Qp, w (group B, single-buffered, copied while phase 1 of the
+// same chunk runs).  The "adjoint walk" of PR #7723 "perf(cake_gdn):
+// prefetch offset adjoint walk, default LPT segment plan" (opening
+// description), which also loads its operands one step ahead.
 // ---------------------------------------------------------------------------
+template <int NW>
+struct WalkBwdA {
+  float Aqk[CH * LDS];
+  float Kd[CH * LDT];
+  uint16_t dO[CH * (NW * 16 + 8)];
+  float gam[DK];
+};
+struct WalkBwdB {
+  float Qp[CH * LDT];
+  float W[CH * LDT];
+};
+
 template <int NW>
 __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
   constexpr int VS = 8 / NW;
-  constexpr int LDU = NW * 16 + 4;
-  extern __shared__ __align__(16) float smf[];
-  float* sAqk = smf;                 // [64][LDS]
-  float* sKd = sAqk + CH * LDS;      // [64][LDT]
-  float* sQp = sKd + CH * LDT;
-  float* sW = sQp + CH * LDT;
-  float* sDO = sW + CH * LDT;        // [64][LDU]
-  float* sGam = sDO + CH * LDU;
+  constexpr int LDO = NW * 16 + 8;  // row stride (elements) of the BF16 dO slice
+  constexpr int NTH = NW * 32;
+  using SA = WalkBwdA<NW>;
+  extern __shared__ __align__(16) unsigned char smraw[];
+  SA* sa = reinterpret_cast<SA*>(smraw);
+  WalkBwdB& sb = *reinterpret_cast<WalkBwdB*>(smraw + 2 * sizeof(SA));
   const int doc = a.order[blockIdx.x / VS];
   const int h = blockIdx.y;
   const DocDesc dd = a.docs[doc];
@@ -47,39 +60,60 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
   const int vcta = (blockIdx.x % VS) * NW * 16;
   const int v0 = vcta + warp * 16, w16 = warp * 16;
   const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
+  const int n = dd.nchunks;
+
+  auto issueA = [&](int s, SA& A) {  // step s processes chunk n-1-s
+    const int chunk = dd.chunk0 + n - 1 - s;
+    const ChunkDesc cd = a.chunks[chunk];
+    const size_t toff = tile_off(chunk, h, a.HV);
+    const size_t qoff = sq_off(chunk, h, a.HV);
+    for (int e = threadIdx.x; e < CH * DK / 4; e += NTH) {
+      const int i = e >> 5, c4 = (e & 31) * 4;
+      cp_async16(&A.Kd[i * LDT + c4], &a.kd[toff + i * DK + c4]);
+    }
+    for (int e = threadIdx.x; e < CH * CH / 4; e += NTH) {
+      const int i = e >> 4, c4 = (e & 15) * 4;
+      cp_async16(&A.Aqk[i * LDS + c4], &a.aqk[qoff + i * CH + c4]);
+    }
+    for (int e = threadIdx.x; e < CH * NW * 2; e += NTH) {  // 16-byte pieces of 8 BF16
+      const int i = e / (NW * 2), c8 = (e % (NW * 2)) * 8;
+      if (i < cd.len) {
+        cp_async16(&A.dO[i * LDO + c8], &a.dout[((size_t)(cd.tok0 + i) * a.HV + h) * DK + vcta + c8]);
+      } else {
+        *reinterpret_cast<uint4*>(&A.dO[i * LDO + c8]) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    for (int e = threadIdx.x; e < DK / 4; e += NTH)
+      cp_async16(&A.gam[e * 4], &a.gam[((size_t)chunk * a.HV + h) * DK + e * 4]);
+  };
+  auto issueB = [&](int s) {
+    const int chunk = dd.chunk0 + n - 1 - s;
+    const size_t toff = tile_off(chunk, h, a.HV);
+    for (int e = threadIdx.x; e < CH * DK / 4; e += NTH) {
+      const int i = e >> 5, c4 = (e & 31) * 4;
+      cp_async16(&sb.Qp[i * LDT + c4], &a.qp[toff + i * DK + c4]);
+      cp_async16(&sb.W[i * LDT + c4], &a.w[toff + i * DK + c4]);
+    }
+  };
 
   float S[16][4];  // dS^T rows v0+g(+8), cols c
   acc_foreach(S, [&](int r, int c, float& x) { x = a.dht ? a.dht[sidx + (size_t)c * DK + v0 + r] : 0.f; });
 
-  for (int m = dd.nchunks - 1; m >= 0; --m) {
-    const int chunk = dd.chunk0 + m;
-    const ChunkDesc cd = a.chunks[chunk];
+  if (n > 0) issueA(0, sa[0]);
+  cp_async_commit();
+  if (n > 0) issueB(0);
+  cp_async_commit();
+  for (int s = 0; s < n; ++s) {
+    const int chunk = dd.chunk0 + n - 1 - s;
     const size_t toff = tile_off(chunk, h, a.HV);
-    const size_t qoff = sq_off(chunk, h, a.HV);
+    if (s + 1 < n) issueA(s + 1, sa[(s + 1) & 1]);
+    cp_async_commit();
+    cp_async_wait<2>();  // group A of this step
     __syncthreads();
-    for (int e = threadIdx.x; e < CH * DK / 4; e += NW * 32) {
-      const int i = e >> 5, c4 = (e & 31) * 4;
-      *reinterpret_cast<float4*>(&sKd[i * LDT + c4]) = *reinterpret_cast<const float4*>(&a.kd[toff + i * DK + c4]);
-      *reinterpret_cast<float4*>(&sQp[i * LDT + c4]) = *reinterpret_cast<const float4*>(&a.qp[toff + i * DK + c4]);
-      *reinterpret_cast<float4*>(&sW[i * LDT + c4]) = *reinterpret_cast<const float4*>(&a.w[toff + i * DK + c4]);
-    }
-    for (int e = threadIdx.x; e < CH * CH / 4; e += NW * 32) {
-      const int i = e >> 4, c4 = (e & 15) * 4;
-      *reinterpret_cast<float4*>(&sAqk[i * LDS + c4]) = *reinterpret_cast<const float4*>(&a.aqk[qoff + i * CH + c4]);
-    }
-    for (int e = threadIdx.x; e < CH * NW * 8; e += NW * 32) {
-      const int i = e / (NW * 8), c2 = (e % (NW * 8)) * 2;
-      float2 v = make_float2(0.f, 0.f);
-      if (i < cd.len)
-        v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
-            &a.dout[((size_t)(cd.tok0 + i) * a.HV + h) * DK + vcta + c2]));
-      *reinterpret_cast<float2*>(&sDO[i * LDU + c2]) = v;
-    }
-    for (int e = threadIdx.x; e < DK; e += NW * 32) sGam[e] = a.gam[((size_t)chunk * a.HV + h) * DK + e];
-    __syncthreads();
+    const SA& A = sa[s & 1];
     {
-      float* tp = a.dstape + state_off(chunk, h, a.HV);
-      acc_foreach(S, [&](int r, int c, float& x) { tp[(size_t)c * DK + v0 + r] = x; });
+      __nv_bfloat16* tp = a.dstape + state_off(chunk, h, a.HV);
+      acc_foreach(S, [&](int r, int c, float& x) { tp[(size_t)c * DK + v0 + r] = __float2bfloat16_rn(x); });
     }
     // E = dDelta^T (16 x 64) = scale dO^T Aqk + dS^T Kd^T
     float E[8][4];
@@ -87,12 +121,12 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int ia = kk * 8 + t, ib = ia + 4;
-      uint32_t av[4] = {tf32(sDO[ia * LDU + w16 + g]), tf32(sDO[ia * LDU + w16 + g + 8]),
-                        tf32(sDO[ib * LDU + w16 + g]), tf32(sDO[ib * LDU + w16 + g + 8])};
+      uint32_t av[4] = {tf32(bfbits2f(A.dO[ia * LDO + w16 + g])), tf32(bfbits2f(A.dO[ia * LDO + w16 + g + 8])),
+                        tf32(bfbits2f(A.dO[ib * LDO + w16 + g])), tf32(bfbits2f(A.dO[ib * LDO + w16 + g + 8]))};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         if (nt <= kk) {
-          uint32_t b[2] = {tf32(sAqk[ia * LDS + nt * 8 + g]), tf32(sAqk[ib * LDS + nt * 8 + g])};
+          uint32_t b[2] = {tf32(A.Aqk[ia * LDS + nt * 8 + g]), tf32(A.Aqk[ib * LDS + nt * 8 + g])};
           mma8(E[nt], av, b);
         }
       }
@@ -103,22 +137,26 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
       uint32_t av[4] = {tf32(S[kk][0]), tf32(S[kk][2]), tf32(S[kk][1]), tf32(S[kk][3])};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        const float2 kv = *reinterpret_cast<const float2*>(&sKd[(nt * 8 + g) * LDT + kk * 8 + 2 * t]);
+        const float2 kv = *reinterpret_cast<const float2*>(&A.Kd[(nt * 8 + g) * LDT + kk * 8 + 2 * t]);
         uint32_t b[2] = {tf32(kv.x), tf32(kv.y)};
         mma8(E[nt], av, b);
       }
     }
     acc_foreach(E, [&](int r, int j, float& x) { a.ddelta[toff + (size_t)j * DK + v0 + r] = x; });
+    cp_async_wait<1>();  // group B of this step
+    __syncthreads();
     // dS^T <- dS^T diag(gamma) + scale dO^T Qp - dDelta^T w
-    acc_foreach(S, [&](int r, int c, float& x) { x *= sGam[c]; });
+    acc_foreach(S, [&](int r, int c, float& x) { x *= A.gam[c]; });
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int ia = kk * 8 + t, ib = ia + 4;
-      uint32_t av[4] = {tf32(a.scale * sDO[ia * LDU + w16 + g]), tf32(a.scale * sDO[ia * LDU + w16 + g + 8]),
-                        tf32(a.scale * sDO[ib * LDU + w16 + g]), tf32(a.scale * sDO[ib * LDU + w16 + g + 8])};
+      uint32_t av[4] = {tf32(a.scale * bfbits2f(A.dO[ia * LDO + w16 + g])),
+                        tf32(a.scale * bfbits2f(A.dO[ia * LDO + w16 + g + 8])),
+                        tf32(a.scale * bfbits2f(A.dO[ib * LDO + w16 + g])),
+                        tf32(a.scale * bfbits2f(A.dO[ib * LDO + w16 + g + 8]))};
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {tf32(sQp[ia * LDT + nt * 8 + g]), tf32(sQp[ib * LDT + nt * 8 + g])};
+        uint32_t b[2] = {tf32(sb.Qp[ia * LDT + nt * 8 + g]), tf32(sb.Qp[ib * LDT + nt * 8 + g])};
         mma8(S[nt], av, b);
       }
     }
@@ -128,65 +166,109 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
       const int j0 = kk * 8 + 2 * t;
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {tf32(sW[j0 * LDT + nt * 8 + g]), tf32(sW[(j0 + 1) * LDT + nt * 8 + g])};
+        uint32_t b[2] = {tf32(sb.W[j0 * LDT + nt * 8 + g]), tf32(sb.W[(j0 + 1) * LDT + nt * 8 + g])};
         mma8(S[nt], av, b);
       }
     }
+    __syncthreads();
+    if (s + 1 < n) issueB(s + 1);
+    cp_async_commit();
   }
   if (a.dh0) acc_foreach(S, [&](int r, int c, float& x) { a.dh0[sidx + (size_t)c * DK + v0 + r] = x; });
 }
 
 // ---------------------------------------------------------------------------
-// State-side products (one CTA per (chunk, value head)):
+// State-side products (one CTA of 8 warps per (chunk, value head)):
 //   dqs = scale dO S0^T,  dw = -dDelta S0^T,  dKd = Delta dS^T,
 //   dgam[c] = sum_v dS[c][v] S0[c][v].
+// Warp w: rows 16 (w % 4), columns 64 (w / 4).  Operands staged in shared
+// memory with cp.async in two groups (S0, dO, dDelta first; dS, Delta second).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) k_grad_state(GradStateArgs a) {
+constexpr int LDB = DK + 8;  // row stride (elements) of a [128][128] BF16 shared tile
+struct GradStateSmem {
+  uint16_t S0[DK * LDB];
+  uint16_t dS[DK * LDB];
+  uint16_t dO[CH * LDB];
+  float Dl[CH * LDT];
+  float dDl[CH * LDT];
+};
+
+__global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  GradStateSmem& s = *reinterpret_cast<GradStateSmem*>(smraw);
   const int chunk = blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
-  const int I = threadIdx.x >> 5, i0 = 16 * I;
+  const int warp = threadIdx.x >> 5, I = warp & 3, i0 = 16 * I, n0 = (warp >> 2) * 64;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
-  const float* S0 = a.tape + state_off(chunk, h, a.HV);
-  const float* dS = a.dstape + state_off(chunk, h, a.HV);
-  const float* dl = a.delta + toff;
-  const float* ddl = a.ddelta + toff;
-  auto dO = [&](int i, int v) -> float {
-    const int row = i0 + i;
-    return row < cd.len ? ldg_bf(&a.dout[((size_t)(cd.tok0 + row) * a.HV + h) * DK + v]) : 0.f;
-  };
+  const __nv_bfloat16* S0 = a.tape + state_off(chunk, h, a.HV);
+  const __nv_bfloat16* dS = a.dstape + state_off(chunk, h, a.HV);
+  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {
+    const int c = e >> 4, v8 = (e & 15) * 8;
+    cp_async16(&s.S0[c * LDB + v8], &S0[c * DK + v8]);
+  }
+  for (int e = threadIdx.x; e < CH * DK / 8; e += 256) {
+    const int i = e >> 4, v8 = (e & 15) * 8;
+    if (i < cd.len)
+      cp_async16(&s.dO[i * LDB + v8], &a.dout[((size_t)(cd.tok0 + i) * a.HV + h) * DK + v8]);
+    else
+      *reinterpret_cast<uint4*>(&s.dO[i * LDB + v8]) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
+    const int i = e >> 5, c4 = (e & 31) * 4;
+    cp_async16(&s.dDl[i * LDT + c4], &a.ddelta[toff + i * DK + c4]);
+  }
+  cp_async_commit();
+  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {
+    const int c = e >> 4, v8 = (e & 15) * 8;
+    cp_async16(&s.dS[c * LDB + v8], &dS[c * DK + v8]);
+  }
+  for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
+    const int i = e >> 5, c4 = (e & 31) * 4;
+    cp_async16(&s.Dl[i * LDT + c4], &a.delta[toff + i * DK + c4]);
+  }
+  cp_async_commit();
+  cp_async_wait<1>();
+  __syncthreads();
   {
-    float dq[16][4], dw[16][4];
+    float dq[8][4], dw[8][4];
     zero_acc(dq);
     zero_acc(dw);
     for (int kk = 0; kk < 16; ++kk) {
       const int va = kk * 8 + t, vb = va + 4;
-      uint32_t aO[4] = {tf32(dO(g, va)), tf32(dO(g + 8, va)), tf32(dO(g, vb)), tf32(dO(g + 8, vb))};
-      uint32_t aD[4] = {tf32(__ldg(&ddl[(i0 + g) * DK + va])), tf32(__ldg(&ddl[(i0 + g + 8) * DK + va])),
-                        tf32(__ldg(&ddl[(i0 + g) * DK + vb])), tf32(__ldg(&ddl[(i0 + g + 8) * DK + vb]))};
+      const int r0 = i0 + g, r1 = i0 + g + 8;
+      uint32_t aO[4] = {tf32(bfbits2f(s.dO[r0 * LDB + va])), tf32(bfbits2f(s.dO[r1 * LDB + va])),
+                        tf32(bfbits2f(s.dO[r0 * LDB + vb])), tf32(bfbits2f(s.dO[r1 * LDB + vb]))};
+      uint32_t aD[4] = {tf32(s.dDl[r0 * LDT + va]), tf32(s.dDl[r1 * LDT + va]), tf32(s.dDl[r0 * LDT + vb]),
+                        tf32(s.dDl[r1 * LDT + vb])};
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + g;
-        uint32_t b[2] = {tf32(__ldg(&S0[c * DK + va])), tf32(__ldg(&S0[c * DK + vb]))};
+      for (int nt = 0; nt < 8; ++nt) {
+        const int c = n0 + nt * 8 + g;
+        uint32_t b[2] = {tf32(bfbits2f(s.S0[c * LDB + va])), tf32(bfbits2f(s.S0[c * LDB + vb]))};
         mma8(dq[nt], aO, b);
         mma8(dw[nt], aD, b);
       }
     }
-    acc_foreach(dq, [&](int r, int c, float& x) { a.dqs[toff + (i0 + r) * DK + c] = a.scale * x; });
-    acc_foreach(dw, [&](int r, int c, float& x) { a.dw[toff + (i0 + r) * DK + c] = -x; });
+    acc_foreach(dq, [&](int r, int c, float& x) { a.dqs[toff + (i0 + r) * DK + n0 + c] = a.scale * x; });
+    acc_foreach(dw, [&](int r, int c, float& x) { a.dw[toff + (i0 + r) * DK + n0 + c] = -x; });
   }
+  cp_async_wait<0>();
+  __syncthreads();
   {
-    float acc[16][4];
+    float acc[8][4];
     zero_acc(acc);
     for (int kk = 0; kk < 16; ++kk)
-      mma_kstep<16>(acc, kk * 8, 0, 16, [&](int i, int v) { return __ldg(&dl[(i0 + i) * DK + v]); },
-                    [&](int v, int c) { return __ldg(&dS[c * DK + v]); });
-    acc_foreach(acc, [&](int r, int c, float& x) { a.dkd[toff + (i0 + r) * DK + c] = x; });
+      mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int v) { return s.Dl[(i0 + i) * LDT + v]; },
+                   [&](int v, int c) { return bfbits2f(s.dS[(n0 + c) * LDB + v]); });
+    acc_foreach(acc, [&](int r, int c, float& x) { a.dkd[toff + (i0 + r) * DK + n0 + c] = x; });
   }
-  for (int c = I * 32; c < I * 32 + 32; ++c) {
-    const float4 x = *reinterpret_cast<const float4*>(&S0[c * DK + lane * 4]);
-    const float4 y = *reinterpret_cast<const float4*>(&dS[c * DK + lane * 4]);
-    float sum = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+  for (int c = warp * 16; c < warp * 16 + 16; ++c) {
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int v = lane * 4 + q;
+      sum += bfbits2f(s.S0[c * LDB + v]) * bfbits2f(s.dS[c * LDB + v]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane == 0) a.dgam[((size_t)chunk * a.HV + h) * DK + c] = sum;
@@ -200,7 +282,7 @@ __global__ void __launch_bounds__(128) k_grad_state(GradStateArgs a) {
 // "fused gradient" / "gate epilogue" stages named on PR #8218.
 // ---------------------------------------------------------------------------
 struct GradSmem {
-  ChunkSmem c;
+  ChunkSmemB c;
   float dAqk[CH * LDS];
   float dK[CH * LDT];
   float dG[CH * LDT];
@@ -213,7 +295,7 @@ template <bool VEC, typename BetaT>
 __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   GradSmem& sg = *reinterpret_cast<GradSmem*>(smem_raw);
-  ChunkSmem& s = sg.c;
+  ChunkSmemB& s = sg.c;
   const int chunk = blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
@@ -222,6 +304,14 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
   if (tid < CH) sg.dbeta[tid] = 0.f;
+  // dw and dDelta (the B operands of X and Y) go into the dK / dG tiles, which
+  // are free until X and Y are formed.
+  for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
+    const int i = e >> 5, c4 = (e & 31) * 4;
+    cp_async16(&sg.dK[i * LDT + c4], &a.dw[toff + i * DK + c4]);
+    cp_async16(&sg.dG[i * LDT + c4], &a.ddelta[toff + i * DK + c4]);
+  }
+  cp_async_commit();
   load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
                          a.HV);
   gram<VEC, false>(s, nullptr);
@@ -252,8 +342,8 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
   zero_acc(X);
   zero_acc(Y);
   {
-    const float* dw = a.dw + toff;
-    const float* dd = a.ddelta + toff;
+    const float* dw = sg.dK;
+    const float* dd = sg.dG;
     for (int kk = 2 * I; kk < 8; ++kk) {
       const int ja = kk * 8 + t, jb = ja + 4;
       uint32_t av[4] = {tf32(s.T[ja * LDS + i0 + g]), tf32(s.T[ja * LDS + i0 + g + 8]),
@@ -261,13 +351,48 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         const int c = nt * 8 + g;
-        uint32_t bx[2] = {tf32(__ldg(&dw[ja * DK + c])), tf32(__ldg(&dw[jb * DK + c]))};
-        uint32_t by[2] = {tf32(__ldg(&dd[ja * DK + c])), tf32(__ldg(&dd[jb * DK + c]))};
+        uint32_t bx[2] = {tf32(dw[ja * LDT + c]), tf32(dw[jb * LDT + c])};
+        uint32_t by[2] = {tf32(dd[ja * LDT + c]), tf32(dd[jb * LDT + c])};
         mma8(X[nt], av, bx);
         mma8(Y[nt], av, by);
       }
     }
   }
+  __syncthreads();
+  // w and u (B operands of dA) into the dK / dG tiles.
+  for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
+    const int i = e >> 5, c4 = (e & 31) * 4;
+    cp_async16(&sg.dK[i * LDT + c4], &a.w[toff + i * DK + c4]);
+    cp_async16(&sg.dG[i * LDT + c4], &a.u[toff + i * DK + c4]);
+  }
+  cp_async_commit();
+  // dA = -strict_tril(X w^T + Y u^T)  -> overwrites s.T once every warp is done with T.
+  float dAacc[8][4];
+  zero_acc(dAacc);
+  cp_async_wait<0>();
+  __syncthreads();
+  {
+    const float* w = sg.dK;
+    const float* u = sg.dG;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      uint32_t ax[4] = {tf32(X[kk][0]), tf32(X[kk][2]), tf32(X[kk][1]), tf32(X[kk][3])};
+      uint32_t ay[4] = {tf32(Y[kk][0]), tf32(Y[kk][2]), tf32(Y[kk][1]), tf32(Y[kk][3])};
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        if (nt < 2 * I + 2) {
+          const int j = nt * 8 + g;
+          const float2 wv = *reinterpret_cast<const float2*>(&w[j * LDT + kk * 8 + 2 * t]);
+          const float2 uv = *reinterpret_cast<const float2*>(&u[j * LDT + kk * 8 + 2 * t]);
+          uint32_t bw[2] = {__float_as_uint(wv.x), __float_as_uint(wv.y)};
+          uint32_t bu[2] = {__float_as_uint(uv.x), __float_as_uint(uv.y)};
+          mma8(dAacc[nt], ax, bw);
+          mma8(dAacc[nt], ay, bu);
+        }
+      }
+    }
+  }
+  __syncthreads();
   // Row-local: dV, dbeta (X.Kp + Y.V), dKp' from X.
   {
     float db0 = 0.f, db1 = 0.f;
@@ -278,7 +403,7 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
         const int row = g + 8 * (r >> 1), c = nt * 8 + 2 * t + (r & 1);
         const int i = i0 + row;
         const float e = ex2(gl(i, c));
-        const float kv = s.K[i * LDT + c];
+        const float kv = s.k(i, c);
         const float vv = i < cd.len ? ldg_bf(&a.v[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c]) : 0.f;
         const float part = X[nt][r] * kv * e + Y[nt][r] * vv;
         if (row < 8) db0 += part; else db1 += part;
@@ -297,31 +422,7 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
       sg.dbeta[i0 + g + 8] += db1;
     }
   }
-  // dA = -strict_tril(X w^T + Y u^T)  -> overwrites s.T once every warp is done with T.
-  float dAacc[8][4];
-  zero_acc(dAacc);
-  {
-    const float* w = a.w + toff;
-    const float* u = a.u + toff;
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      uint32_t ax[4] = {tf32(X[kk][0]), tf32(X[kk][2]), tf32(X[kk][1]), tf32(X[kk][3])};
-      uint32_t ay[4] = {tf32(Y[kk][0]), tf32(Y[kk][2]), tf32(Y[kk][1]), tf32(Y[kk][3])};
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        if (nt < 2 * I + 2) {
-          const int j = nt * 8 + g;
-          const float2 wv = __ldg(reinterpret_cast<const float2*>(&w[j * DK + kk * 8 + 2 * t]));
-          const float2 uv = __ldg(reinterpret_cast<const float2*>(&u[j * DK + kk * 8 + 2 * t]));
-          uint32_t bw[2] = {tf32(wv.x), tf32(wv.y)};
-          uint32_t bu[2] = {tf32(uv.x), tf32(uv.y)};
-          mma8(dAacc[nt], ax, bw);
-          mma8(dAacc[nt], ay, bu);
-        }
-      }
-    }
-  }
-  __syncthreads();
+
   float* sDA = s.T;
   acc_foreach(dAacc, [&](int r, int col, float& x) { sDA[(i0 + r) * LDS + col] = col < i0 + r ? -x : 0.f; });
   __syncthreads();
@@ -334,23 +435,23 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
   {
     float Z[16][4];
     zero_acc(Z);
-    left_apply<VEC>(s, sDA, s.K, Z);
+    left_apply<VEC>(s, sDA, [&](int j, int c) { return s.k(j, c); }, Z);
     acc_foreach(Z, [&](int r, int c, float& x) {
       const int i = i0 + r;
       const float v = s.beta[i] * x;
       sg.dK[i * LDT + c] += v;
-      sg.dG[i * LDT + c] += s.K[i * LDT + c] * v;
+      sg.dG[i * LDT + c] += s.k(i, c) * v;
     });
   }
   // dQ = dqs * Gamma + [dAqk (x) decay] K
   {
     float Z[16][4];
     zero_acc(Z);
-    left_apply<VEC>(s, sg.dAqk, s.K, Z);
+    left_apply<VEC>(s, sg.dAqk, [&](int j, int c) { return s.k(j, c); }, Z);
     acc_foreach(Z, [&](int r, int c, float& x) {
       const int i = i0 + r;
       const float dq = __ldg(&a.dqs[toff + i * DK + c]) * ex2(gl(i, c)) + x;
-      sg.dG[i * LDT + c] += s.Q[i * LDT + c] * dq;
+      sg.dG[i * LDT + c] += s.q(i, c) * dq;
       if (a.dq_part) {
         a.dq_part[toff + i * DK + c] = dq;
       } else if (i < cd.len) {
@@ -362,11 +463,12 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
   {
     float Z[16][4];
     zero_acc(Z);
-    right_apply2<VEC>(s, sg.dAqk, s.Q, sDA, s.K, Z);
+    right_apply2<VEC>(s, sg.dAqk, [&](int i, int c) { return s.q(i, c); }, sDA, [&](int i, int c) { return s.k(i, c); },
+                      Z);
     acc_foreach(Z, [&](int r, int c, float& x) {
       const int i = i0 + r;
       sg.dK[i * LDT + c] += x;
-      sg.dG[i * LDT + c] -= s.K[i * LDT + c] * x;
+      sg.dG[i * LDT + c] -= s.k(i, c) * x;
     });
   }
   // dKd terms (own rows), column sums of Kd*dKd, then dk.
@@ -463,8 +565,7 @@ __global__ void __launch_bounds__(256) k_group_reduce(GroupReduceArgs a) {
 // ---------------------------------------------------------------------------
 template <int NW>
 static cudaError_t launch_walk_bwd_nw(const WalkBwdArgs& a, int ndocs, cudaStream_t st) {
-  constexpr int LDU = NW * 16 + 4;
-  const size_t sm = (size_t)(CH * LDS + 3 * CH * LDT + CH * LDU + DK) * sizeof(float);
+  const size_t sm = 2 * sizeof(WalkBwdA<NW>) + sizeof(WalkBwdB);
   cudaFuncSetAttribute(k_walk_bwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   dim3 grid(ndocs * (8 / NW), a.HV);
   k_walk_bwd<NW><<<grid, NW * 32, sm, st>>>(a);
@@ -483,7 +584,9 @@ cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, 
 
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st) {
   if (nchunks == 0) return cudaSuccess;
-  k_grad_state<<<dim3(nchunks, a.HV), 128, 0, st>>>(a);
+  const size_t sm = sizeof(GradStateSmem);
+  cudaFuncSetAttribute(k_grad_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  k_grad_state<<<dim3(nchunks, a.HV), 256, sm, st>>>(a);
   return cudaGetLastError();
 }
 

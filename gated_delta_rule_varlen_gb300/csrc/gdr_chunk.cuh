@@ -8,42 +8,76 @@
 
 namespace gdr {
 
-struct ChunkSmem {
-  float K[CH * LDT];  // k as FP32 (rows >= len are zero)
-  float Q[CH * LDT];  // q as FP32
+// Shared-memory tiles of one chunk.  K and Q are kept either as FP32 (ET =
+// float) or as their exact BF16 input bits (ET = uint16_t, half the space).
+template <typename ET>
+struct ChunkSmemT {
+  static constexpr int LD = sizeof(ET) == 4 ? LDT : DK + 8;  // row stride (elements) of K and Q
+  ET K[CH * LD];      // k (rows >= len are zero)
+  ET Q[CH * LD];      // q
   float G[CH * LDT];  // per-channel gate: chunk-local cumsum of g, times log2(e)
   float gs[CH];       // scalar gate: chunk-local cumsum of g, times log2(e)
   float beta[CH];
   float At[CH * LDS];  // strict_tril of the gated Gram K K^T (without beta)
   float T[CH * LDS];   // (I + diag(beta) At)^-1
   float tmp[3 * 256];
+  __device__ __forceinline__ float k(int i, int c) const { return elem(K[i * LD + c]); }
+  __device__ __forceinline__ float q(int i, int c) const { return elem(Q[i * LD + c]); }
+  static __device__ __forceinline__ float elem(float x) { return x; }
+  static __device__ __forceinline__ float elem(uint16_t x) { return bfbits2f(x); }
 };
+using ChunkSmem = ChunkSmemT<float>;
+using ChunkSmemB = ChunkSmemT<uint16_t>;
 
 // Loads k, q (of Q/K head hq), the gate (cumsum, base-2 scaled) and beta of
 // value head h for the chunk rows [tok0, tok0+len).  Rows >= len are zero
 // (zero gate rows keep the cumsum flat, so gc at row 63 equals gc at the
 // chunk's last token).
-template <bool VEC, typename BetaT>
-__device__ void load_chunk(ChunkSmem& s, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+template <bool VEC, typename BetaT, typename ET>
+__device__ void load_chunk(ChunkSmemT<ET>& s, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                            const float* __restrict__ g, const BetaT* __restrict__ beta, int tok0, int len, int hq,
                            int h, int Hqk, int HV) {
+  constexpr int LD = ChunkSmemT<ET>::LD;
   const int tid = threadIdx.x;
-  for (int e = tid; e < CH * DK / 2; e += blockDim.x) {
-    const int i = e / (DK / 2), d = (e % (DK / 2)) * 2;
-    float2 kv = make_float2(0.f, 0.f), qv = make_float2(0.f, 0.f);
-    if (i < len) {
-      const size_t off = ((size_t)(tok0 + i) * Hqk + hq) * DK + d;
-      kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(k + off));
-      qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q + off));
+  if (sizeof(ET) == 2) {
+    // Raw BF16 rows straight into shared memory (16-byte async copies).
+    for (int e = tid; e < CH * DK / 8; e += blockDim.x) {
+      const int i = e >> 4, d8 = (e & 15) * 8;
+      if (i < len) {
+        const size_t off = ((size_t)(tok0 + i) * Hqk + hq) * DK + d8;
+        cp_async16(&s.K[i * LD + d8], k + off);
+        cp_async16(&s.Q[i * LD + d8], q + off);
+      } else {
+        *reinterpret_cast<uint4*>(&s.K[i * LD + d8]) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(&s.Q[i * LD + d8]) = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
-    *reinterpret_cast<float2*>(&s.K[i * LDT + d]) = kv;
-    *reinterpret_cast<float2*>(&s.Q[i * LDT + d]) = qv;
     if (VEC) {
-      float2 gv = make_float2(0.f, 0.f);
-      if (i < len) gv = *reinterpret_cast<const float2*>(g + ((size_t)(tok0 + i) * HV + h) * DK + d);
-      gv.x *= LOG2E;
-      gv.y *= LOG2E;
-      *reinterpret_cast<float2*>(&s.G[i * LDT + d]) = gv;
+      for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
+        const int i = e >> 5, d4 = (e & 31) * 4;
+        if (i < len)
+          cp_async16(&s.G[i * LDT + d4], g + ((size_t)(tok0 + i) * HV + h) * DK + d4);
+        else
+          *reinterpret_cast<float4*>(&s.G[i * LDT + d4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    cp_async_commit();
+  } else {
+    for (int e = tid; e < CH * DK / 2; e += blockDim.x) {
+      const int i = e / (DK / 2), d = (e % (DK / 2)) * 2;
+      float2 kv = make_float2(0.f, 0.f), qv = make_float2(0.f, 0.f);
+      if (i < len) {
+        const size_t off = ((size_t)(tok0 + i) * Hqk + hq) * DK + d;
+        kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(k + off));
+        qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q + off));
+      }
+      *reinterpret_cast<float2*>(reinterpret_cast<float*>(&s.K[0]) + i * LD + d) = kv;
+      *reinterpret_cast<float2*>(reinterpret_cast<float*>(&s.Q[0]) + i * LD + d) = qv;
+      if (VEC) {
+        float2 gv = make_float2(0.f, 0.f);
+        if (i < len) gv = *reinterpret_cast<const float2*>(g + ((size_t)(tok0 + i) * HV + h) * DK + d);
+        *reinterpret_cast<float2*>(&s.G[i * LDT + d]) = gv;
+      }
     }
   }
   if (tid < CH) {
@@ -51,12 +85,14 @@ __device__ void load_chunk(ChunkSmem& s, const __nv_bfloat16* __restrict__ q, co
     s.beta[tid] = ok ? to_f<BetaT>(beta[(size_t)(tok0 + tid) * HV + h]) : 0.f;
     if (!VEC) s.gs[tid] = ok ? g[(size_t)(tok0 + tid) * HV + h] * LOG2E : 0.f;
   }
+  if (sizeof(ET) == 2) cp_async_wait<0>();
   __syncthreads();
   if (VEC) {
     if (tid < DK) {
       float acc = 0.f;
+#pragma unroll 8
       for (int i = 0; i < CH; ++i) {
-        acc += s.G[i * LDT + tid];
+        acc += s.G[i * LDT + tid] * LOG2E;
         s.G[i * LDT + tid] = acc;
       }
     }
@@ -74,10 +110,12 @@ __device__ void load_chunk(ChunkSmem& s, const __nv_bfloat16* __restrict__ q, co
 //   At[i][j]  = sum_c K_ic K_jc exp(gc_ic - gc_jc)   for j <  i (else 0)  -> s.At
 //   Aqk[i][j] = sum_c Q_ic K_jc exp(gc_ic - gc_jc)   for j <= i (else 0)  -> aqk (global, [64][64])
 // Per-channel gates use the block factorization described in gdr_common.cuh.
-template <bool VEC, bool WITH_QK>
-__device__ void gram(ChunkSmem& s, float* __restrict__ aqk) {
+// Aqk is stored rounded to TF32 (it is only ever an MMA operand).
+template <bool VEC, bool WITH_QK, typename ET>
+__device__ void gram(ChunkSmemT<ET>& s, float* __restrict__ aqk) {
   const int I = threadIdx.x >> 5, i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+  const int ra = i0 + g, rb = i0 + g + 8;
   float accK[8][4], accQ[8][4];
   zero_acc(accK);
   zero_acc(accQ);
@@ -85,28 +123,24 @@ __device__ void gram(ChunkSmem& s, float* __restrict__ aqk) {
     float dK[2][4], dQ[2][4];
     zero_acc(dK);
     zero_acc(dQ);
+    const float* G = s.G;
 #pragma unroll 2
     for (int kk = 0; kk < 16; ++kk) {
       const int c0 = kk * 8 + t, c1 = c0 + 4;
-      const float* G = s.G;
-      const float* K = s.K;
-      const float* Q = s.Q;
-      const int r0 = (i0 + g) * LDT, r1 = (i0 + g + 8) * LDT;
+      const float ka0 = s.k(ra, c0), kb0 = s.k(rb, c0), ka1 = s.k(ra, c1), kb1 = s.k(rb, c1);
+      const float qa0 = s.q(ra, c0), qb0 = s.q(rb, c0), qa1 = s.q(ra, c1), qb1 = s.q(rb, c1);
+      const float ga0 = G[ra * LDT + c0], gb0 = G[rb * LDT + c0], ga1 = G[ra * LDT + c1], gb1 = G[rb * LDT + c1];
       // Off-diagonal blocks: reference = gc at the end of block I-1.
       if (I > 0) {
         const float b0 = G[(i0 - 1) * LDT + c0], b1 = G[(i0 - 1) * LDT + c1];
-        const float e00 = ex2(G[r0 + c0] - b0), e10 = ex2(G[r1 + c0] - b0);
-        const float e01 = ex2(G[r0 + c1] - b1), e11 = ex2(G[r1 + c1] - b1);
-        uint32_t aK[4] = {tf32(K[r0 + c0] * e00), tf32(K[r1 + c0] * e10), tf32(K[r0 + c1] * e01),
-                          tf32(K[r1 + c1] * e11)};
-        uint32_t aQ[4] = {tf32(Q[r0 + c0] * e00), tf32(Q[r1 + c0] * e10), tf32(Q[r0 + c1] * e01),
-                          tf32(Q[r1 + c1] * e11)};
+        const float e00 = ex2(ga0 - b0), e10 = ex2(gb0 - b0), e01 = ex2(ga1 - b1), e11 = ex2(gb1 - b1);
+        uint32_t aK[4] = {tf32(ka0 * e00), tf32(kb0 * e10), tf32(ka1 * e01), tf32(kb1 * e11)};
+        uint32_t aQ[4] = {tf32(qa0 * e00), tf32(qb0 * e10), tf32(qa1 * e01), tf32(qb1 * e11)};
 #pragma unroll
         for (int nt = 0; nt < 6; ++nt) {
           if (nt < 2 * I) {
             const int j = nt * 8 + g;
-            uint32_t b[2] = {tf32(K[j * LDT + c0] * ex2(b0 - G[j * LDT + c0])),
-                             tf32(K[j * LDT + c1] * ex2(b1 - G[j * LDT + c1]))};
+            uint32_t b[2] = {tf32(s.k(j, c0) * ex2(b0 - G[j * LDT + c0])), tf32(s.k(j, c1) * ex2(b1 - G[j * LDT + c1]))};
             mma8(accK[nt], aK, b);
             if (WITH_QK) mma8(accQ[nt], aQ, b);
           }
@@ -115,17 +149,13 @@ __device__ void gram(ChunkSmem& s, float* __restrict__ aqk) {
       // Diagonal block: reference = gc at row i0 + 7.
       {
         const float m0 = G[(i0 + 7) * LDT + c0], m1 = G[(i0 + 7) * LDT + c1];
-        const float e00 = ex2(G[r0 + c0] - m0), e10 = ex2(G[r1 + c0] - m0);
-        const float e01 = ex2(G[r0 + c1] - m1), e11 = ex2(G[r1 + c1] - m1);
-        uint32_t aK[4] = {tf32(K[r0 + c0] * e00), tf32(K[r1 + c0] * e10), tf32(K[r0 + c1] * e01),
-                          tf32(K[r1 + c1] * e11)};
-        uint32_t aQ[4] = {tf32(Q[r0 + c0] * e00), tf32(Q[r1 + c0] * e10), tf32(Q[r0 + c1] * e01),
-                          tf32(Q[r1 + c1] * e11)};
+        const float e00 = ex2(ga0 - m0), e10 = ex2(gb0 - m0), e01 = ex2(ga1 - m1), e11 = ex2(gb1 - m1);
+        uint32_t aK[4] = {tf32(ka0 * e00), tf32(kb0 * e10), tf32(ka1 * e01), tf32(kb1 * e11)};
+        uint32_t aQ[4] = {tf32(qa0 * e00), tf32(qb0 * e10), tf32(qa1 * e01), tf32(qb1 * e11)};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int j = i0 + nt * 8 + g;
-          uint32_t b[2] = {tf32(K[j * LDT + c0] * ex2(m0 - G[j * LDT + c0])),
-                           tf32(K[j * LDT + c1] * ex2(m1 - G[j * LDT + c1]))};
+          uint32_t b[2] = {tf32(s.k(j, c0) * ex2(m0 - G[j * LDT + c0])), tf32(s.k(j, c1) * ex2(m1 - G[j * LDT + c1]))};
           mma8(dK[nt], aK, b);
           if (WITH_QK) mma8(dQ[nt], aQ, b);
         }
@@ -143,26 +173,25 @@ __device__ void gram(ChunkSmem& s, float* __restrict__ aqk) {
           vQ = accQ[nt][r];
         } else if (nt == 2 * I || nt == 2 * I + 1) {
           const int dn = nt - 2 * I;
-          const int lrow = row, lcol = dn * 8 + 2 * t + (r & 1);
-          vK = lcol < lrow ? dK[dn][r] : 0.f;
-          vQ = lcol <= lrow ? dQ[dn][r] : 0.f;
+          const int lcol = dn * 8 + 2 * t + (r & 1);
+          vK = lcol < row ? dK[dn][r] : 0.f;
+          vQ = lcol <= row ? dQ[dn][r] : 0.f;
         }
         s.At[(i0 + row) * LDS + col] = vK;
-        if (WITH_QK) aqk[(i0 + row) * CH + col] = vQ;
+        if (WITH_QK) aqk[(i0 + row) * CH + col] = __uint_as_float(tf32(vQ));
       }
     }
   } else {
 #pragma unroll 2
     for (int kk = 0; kk < 16; ++kk) {
       const int c0 = kk * 8 + t, c1 = c0 + 4;
-      const int r0 = (i0 + g) * LDT, r1 = (i0 + g + 8) * LDT;
-      uint32_t aK[4] = {tf32(s.K[r0 + c0]), tf32(s.K[r1 + c0]), tf32(s.K[r0 + c1]), tf32(s.K[r1 + c1])};
-      uint32_t aQ[4] = {tf32(s.Q[r0 + c0]), tf32(s.Q[r1 + c0]), tf32(s.Q[r0 + c1]), tf32(s.Q[r1 + c1])};
+      uint32_t aK[4] = {tf32(s.k(ra, c0)), tf32(s.k(rb, c0)), tf32(s.k(ra, c1)), tf32(s.k(rb, c1))};
+      uint32_t aQ[4] = {tf32(s.q(ra, c0)), tf32(s.q(rb, c0)), tf32(s.q(ra, c1)), tf32(s.q(rb, c1))};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         if (nt < 2 * I + 2) {
           const int j = nt * 8 + g;
-          uint32_t b[2] = {tf32(s.K[j * LDT + c0]), tf32(s.K[j * LDT + c1])};
+          uint32_t b[2] = {tf32(s.k(j, c0)), tf32(s.k(j, c1))};
           mma8(accK[nt], aK, b);
           if (WITH_QK) mma8(accQ[nt], aQ, b);
         }
@@ -180,7 +209,7 @@ __device__ void gram(ChunkSmem& s, float* __restrict__ aqk) {
           if (col < row) vK = accK[nt][r] * dec;
         }
         s.At[row * LDS + col] = vK;
-        if (WITH_QK) aqk[row * CH + col] = vQ;
+        if (WITH_QK) aqk[row * CH + col] = __uint_as_float(tf32(vQ));
       }
     }
   }
@@ -189,7 +218,8 @@ __device__ void gram(ChunkSmem& s, float* __restrict__ aqk) {
 // s.T = (I + diag(beta) At)^-1, unit lower triangular.  Diagonal 16x16 blocks
 // by forward substitution (one warp each), then off-diagonal blocks by
 // distance: T_IJ = -T_II * sum_{K=J}^{I-1} A_IK T_KJ.  FP32 on CUDA cores.
-__device__ inline void invert(ChunkSmem& s) {
+template <typename ET>
+__device__ void invert(ChunkSmemT<ET>& s) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   if (lane < 16) {
     const int i0 = warp * 16, j = lane;
@@ -235,10 +265,9 @@ __device__ inline void invert(ChunkSmem& s) {
 }
 
 // Z_i += sum_{j<=i} M_ij Y_j * exp(gc_i - gc_j)   (rows i of this warp's block)
-// M is a masked [64][64] shared tile (stride LDS); Y a [64][128] shared tile.
-template <bool VEC>
-__device__ void left_apply(const ChunkSmem& s, const float* __restrict__ M, const float* __restrict__ Y,
-                           float (&Z)[16][4]) {
+// M is a masked [64][64] shared tile (stride LDS); fy(j, c) returns Y_jc.
+template <bool VEC, typename ET, class FY>
+__device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M, FY fy, float (&Z)[16][4]) {
   const int I = threadIdx.x >> 5, i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   if (VEC) {
@@ -253,8 +282,7 @@ __device__ void left_apply(const ChunkSmem& s, const float* __restrict__ M, cons
         for (int nt = 0; nt < 16; ++nt) {
           const int c = nt * 8 + g;
           const float bI = s.G[(i0 - 1) * LDT + c];
-          uint32_t b[2] = {tf32(Y[j0 * LDT + c] * ex2(bI - s.G[j0 * LDT + c])),
-                           tf32(Y[j1 * LDT + c] * ex2(bI - s.G[j1 * LDT + c]))};
+          uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LDT + c]))};
           mma8(acc[nt], a, b);
         }
       }
@@ -272,8 +300,7 @@ __device__ void left_apply(const ChunkSmem& s, const float* __restrict__ M, cons
       for (int nt = 0; nt < 16; ++nt) {
         const int c = nt * 8 + g;
         const float mI = s.G[(i0 + 7) * LDT + c];
-        uint32_t b[2] = {tf32(Y[j0 * LDT + c] * ex2(mI - s.G[j0 * LDT + c])),
-                         tf32(Y[j1 * LDT + c] * ex2(mI - s.G[j1 * LDT + c]))};
+        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LDT + c]))};
         mma8(acc[nt], a, b);
       }
     }
@@ -289,7 +316,7 @@ __device__ void left_apply(const ChunkSmem& s, const float* __restrict__ M, cons
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         const int c = nt * 8 + g;
-        uint32_t b[2] = {tf32(Y[j0 * LDT + c]), tf32(Y[j1 * LDT + c])};
+        uint32_t b[2] = {tf32(fy(j0, c)), tf32(fy(j1, c))};
         mma8(Z[nt], a, b);
       }
     }
@@ -297,10 +324,11 @@ __device__ void left_apply(const ChunkSmem& s, const float* __restrict__ M, cons
 }
 
 // Z_j += sum_{i>=j} (M0_ij Y0_i + beta_i M1_ij Y1_i) * exp(gc_i - gc_j)
-// (rows j of this warp's block).  M0, M1 masked [64][64] shared tiles.
-template <bool VEC>
-__device__ void right_apply2(const ChunkSmem& s, const float* __restrict__ M0, const float* __restrict__ Y0,
-                             const float* __restrict__ M1, const float* __restrict__ Y1, float (&Z)[16][4]) {
+// (rows j of this warp's block).  M0, M1 masked [64][64] shared tiles;
+// f0(i, c), f1(i, c) return Y0_ic, Y1_ic.
+template <bool VEC, typename ET, class F0, class F1>
+__device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M0, F0 f0, const float* __restrict__ M1,
+                             F1 f1, float (&Z)[16][4]) {
   const int J = threadIdx.x >> 5, j0b = 16 * J;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   if (VEC) {
@@ -318,8 +346,8 @@ __device__ void right_apply2(const ChunkSmem& s, const float* __restrict__ M0, c
         const int c = nt * 8 + g;
         const float bJ = s.G[ref * LDT + c];
         const float ea = ex2(s.G[ia * LDT + c] - bJ), eb = ex2(s.G[ib * LDT + c] - bJ);
-        uint32_t b0[2] = {tf32(Y0[ia * LDT + c] * ea), tf32(Y0[ib * LDT + c] * eb)};
-        uint32_t b1[2] = {tf32(Y1[ia * LDT + c] * ea), tf32(Y1[ib * LDT + c] * eb)};
+        uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
+        uint32_t b1[2] = {tf32(f1(ia, c) * ea), tf32(f1(ib, c) * eb)};
         mma8(acc[nt], a0, b0);
         mma8(acc[nt], a1, b1);
       }
@@ -341,8 +369,8 @@ __device__ void right_apply2(const ChunkSmem& s, const float* __restrict__ M0, c
         const int c = nt * 8 + g;
         const float mJ = s.G[mref * LDT + c];
         const float ea = ex2(s.G[ia * LDT + c] - mJ), eb = ex2(s.G[ib * LDT + c] - mJ);
-        uint32_t b0[2] = {tf32(Y0[ia * LDT + c] * ea), tf32(Y0[ib * LDT + c] * eb)};
-        uint32_t b1[2] = {tf32(Y1[ia * LDT + c] * ea), tf32(Y1[ib * LDT + c] * eb)};
+        uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
+        uint32_t b1[2] = {tf32(f1(ia, c) * ea), tf32(f1(ib, c) * eb)};
         mma8(acc[nt], a0, b0);
         mma8(acc[nt], a1, b1);
       }
@@ -363,8 +391,8 @@ __device__ void right_apply2(const ChunkSmem& s, const float* __restrict__ M0, c
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         const int c = nt * 8 + g;
-        uint32_t b0[2] = {tf32(Y0[ia * LDT + c]), tf32(Y0[ib * LDT + c])};
-        uint32_t b1[2] = {tf32(Y1[ia * LDT + c]), tf32(Y1[ib * LDT + c])};
+        uint32_t b0[2] = {tf32(f0(ia, c)), tf32(f0(ib, c))};
+        uint32_t b1[2] = {tf32(f1(ia, c)), tf32(f1(ib, c))};
         mma8(Z[nt], a0, b0);
         mma8(Z[nt], a1, b1);
       }

@@ -26,7 +26,7 @@ struct WalkArgs {
   int HV;
   const float *w, *u, *kd, *gam;
   const float* h0;   // [N][HV][128][128] or null
-  float* tape;       // S0 per chunk, or null
+  __nv_bfloat16* tape;  // S0 per chunk (BF16), or null
   float* delta;      // Delta per chunk, or null
   float* ht;         // [N][HV][128][128] or null
 };
@@ -35,7 +35,8 @@ struct OutArgs {
   const ChunkDesc* chunks;
   int HV;
   float scale;
-  const float *qp, *tape, *aqk, *delta;
+  const float *qp, *aqk, *delta;
+  const __nv_bfloat16* tape;
   __nv_bfloat16* out;  // [T][HV][128]
 };
 
@@ -48,7 +49,7 @@ struct WalkBwdArgs {
   const float *w, *qp, *kd, *aqk, *gam;
   const __nv_bfloat16* dout;  // [T][HV][128]
   const float* dht;           // [N][HV][128][128] or null
-  float* dstape;              // dS (adjoint of each chunk's end state)
+  __nv_bfloat16* dstape;      // dS (adjoint of each chunk's end state), BF16
   float* ddelta;              // dDelta per chunk
   float* dh0;                 // or null
 };
@@ -58,7 +59,8 @@ struct GradStateArgs {
   int HV;
   float scale;
   const __nv_bfloat16* dout;
-  const float *tape, *dstape, *delta, *ddelta;
+  const __nv_bfloat16 *tape, *dstape;
+  const float *delta, *ddelta;
   float *dqs, *dw, *dkd, *dgam;  // scratch outputs
 };
 
