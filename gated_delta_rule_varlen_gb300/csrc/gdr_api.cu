@@ -184,18 +184,19 @@ int sm_count() {
   return n > 0 ? n : 152;
 }
 
-// Warps per walk CTA (each warp carries 16 value columns): spread the
-// (document, head) chains over at least the SM count when they are few.
+// Warps per walk CTA (each warp carries 16 value columns, a chain's 128
+// columns are split over 8 / warps CTAs).  A walk CTA fills most of an SM's
+// shared memory, so one runs per SM: take the fewest warps per CTA (the most
+// SMs per chain) that still fit every CTA in one wave.
 int walk_warps(int64_t chains) {
   if (const char* e = std::getenv("GDR_WALK_WARPS")) {
     const int v = std::atoi(e);
     if (v == 1 || v == 2 || v == 4 || v == 8) return v;
   }
-  const int sms = sm_count();
-  if (chains >= sms) return 8;
-  if (chains * 2 >= sms) return 4;
-  if (chains * 4 >= sms) return 2;
-  return 1;
+  const int64_t sms = sm_count();
+  for (int nw = 1; nw < 8; nw *= 2)
+    if (chains * (8 / nw) <= sms) return nw;
+  return 8;
 }
 
 bool aligned(const void* p) { return ((uintptr_t)p % kAlign) == 0; }

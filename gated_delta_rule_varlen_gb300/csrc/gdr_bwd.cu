@@ -52,8 +52,9 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
   extern __shared__ __align__(16) unsigned char smraw[];
   SA* sa = reinterpret_cast<SA*>(smraw);
   WalkBwdB& sb = *reinterpret_cast<WalkBwdB*>(smraw + 2 * sizeof(SA));
-  const int doc = a.order[blockIdx.x / VS];
-  const int h = blockIdx.y;
+  const int rank = blockIdx.x / (a.HV * VS);  // longest document first, all its heads
+  const int h = (blockIdx.x / VS) % a.HV;
+  const int doc = a.order[rank];
   const DocDesc dd = a.docs[doc];
   const int warp = threadIdx.x >> 5;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
@@ -111,9 +112,15 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
     cp_async_wait<2>();  // group A of this step
     __syncthreads();
     const SA& A = sa[s & 1];
-    {
+    {  // dS^T, [v][c], as BF16 pairs
       __nv_bfloat16* tp = a.dstape + state_off(chunk, h, a.HV);
-      acc_foreach(S, [&](int r, int c, float& x) { tp[(size_t)c * DK + v0 + r] = __float2bfloat16_rn(x); });
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int c = nt * 8 + 2 * t;
+        *reinterpret_cast<__nv_bfloat162*>(&tp[(size_t)(v0 + g) * DK + c]) = __floats2bfloat162_rn(S[nt][0], S[nt][1]);
+        *reinterpret_cast<__nv_bfloat162*>(&tp[(size_t)(v0 + g + 8) * DK + c]) =
+            __floats2bfloat162_rn(S[nt][2], S[nt][3]);
+      }
     }
     // E = dDelta^T (16 x 64) = scale dO^T Aqk + dS^T Kd^T
     float E[8][4];
@@ -121,12 +128,12 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int ia = kk * 8 + t, ib = ia + 4;
-      uint32_t av[4] = {tf32(bfbits2f(A.dO[ia * LDO + w16 + g])), tf32(bfbits2f(A.dO[ia * LDO + w16 + g + 8])),
-                        tf32(bfbits2f(A.dO[ib * LDO + w16 + g])), tf32(bfbits2f(A.dO[ib * LDO + w16 + g + 8]))};
+      uint32_t av[4] = {(uint32_t)A.dO[ia * LDO + w16 + g] << 16, (uint32_t)A.dO[ia * LDO + w16 + g + 8] << 16,
+                        (uint32_t)A.dO[ib * LDO + w16 + g] << 16, (uint32_t)A.dO[ib * LDO + w16 + g + 8] << 16};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         if (nt <= kk) {
-          uint32_t b[2] = {tf32(A.Aqk[ia * LDS + nt * 8 + g]), tf32(A.Aqk[ib * LDS + nt * 8 + g])};
+          uint32_t b[2] = {__float_as_uint(A.Aqk[ia * LDS + nt * 8 + g]), __float_as_uint(A.Aqk[ib * LDS + nt * 8 + g])};
           mma8(E[nt], av, b);
         }
       }
@@ -138,7 +145,7 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const float2 kv = *reinterpret_cast<const float2*>(&A.Kd[(nt * 8 + g) * LDT + kk * 8 + 2 * t]);
-        uint32_t b[2] = {tf32(kv.x), tf32(kv.y)};
+        uint32_t b[2] = {__float_as_uint(kv.x), __float_as_uint(kv.y)};
         mma8(E[nt], av, b);
       }
     }
@@ -156,7 +163,7 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
                         tf32(a.scale * bfbits2f(A.dO[ib * LDO + w16 + g + 8]))};
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {tf32(sb.Qp[ia * LDT + nt * 8 + g]), tf32(sb.Qp[ib * LDT + nt * 8 + g])};
+        uint32_t b[2] = {__float_as_uint(sb.Qp[ia * LDT + nt * 8 + g]), __float_as_uint(sb.Qp[ib * LDT + nt * 8 + g])};
         mma8(S[nt], av, b);
       }
     }
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
       const int j0 = kk * 8 + 2 * t;
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {tf32(sb.W[j0 * LDT + nt * 8 + g]), tf32(sb.W[(j0 + 1) * LDT + nt * 8 + g])};
+        uint32_t b[2] = {__float_as_uint(sb.W[j0 * LDT + nt * 8 + g]), __float_as_uint(sb.W[(j0 + 1) * LDT + nt * 8 + g])};
         mma8(S[nt], av, b);
       }
     }
@@ -203,9 +210,9 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
   const size_t toff = tile_off(chunk, h, a.HV);
   const __nv_bfloat16* S0 = a.tape + state_off(chunk, h, a.HV);
   const __nv_bfloat16* dS = a.dstape + state_off(chunk, h, a.HV);
-  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {
-    const int c = e >> 4, v8 = (e & 15) * 8;
-    cp_async16(&s.S0[c * LDB + v8], &S0[c * DK + v8]);
+  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // S0^T rows [v][c]
+    const int v = e >> 4, c8 = (e & 15) * 8;
+    cp_async16(&s.S0[v * LDB + c8], &S0[v * DK + c8]);
   }
   for (int e = threadIdx.x; e < CH * DK / 8; e += 256) {
     const int i = e >> 4, v8 = (e & 15) * 8;
@@ -219,9 +226,9 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
     cp_async16(&s.dDl[i * LDT + c4], &a.ddelta[toff + i * DK + c4]);
   }
   cp_async_commit();
-  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {
-    const int c = e >> 4, v8 = (e & 15) * 8;
-    cp_async16(&s.dS[c * LDB + v8], &dS[c * DK + v8]);
+  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // dS^T rows [v][c]
+    const int v = e >> 4, c8 = (e & 15) * 8;
+    cp_async16(&s.dS[v * LDB + c8], &dS[v * DK + c8]);
   }
   for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
     const int i = e >> 5, c4 = (e & 31) * 4;
@@ -237,14 +244,14 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
     for (int kk = 0; kk < 16; ++kk) {
       const int va = kk * 8 + t, vb = va + 4;
       const int r0 = i0 + g, r1 = i0 + g + 8;
-      uint32_t aO[4] = {tf32(bfbits2f(s.dO[r0 * LDB + va])), tf32(bfbits2f(s.dO[r1 * LDB + va])),
-                        tf32(bfbits2f(s.dO[r0 * LDB + vb])), tf32(bfbits2f(s.dO[r1 * LDB + vb]))};
+      uint32_t aO[4] = {(uint32_t)s.dO[r0 * LDB + va] << 16, (uint32_t)s.dO[r1 * LDB + va] << 16,
+                        (uint32_t)s.dO[r0 * LDB + vb] << 16, (uint32_t)s.dO[r1 * LDB + vb] << 16};
       uint32_t aD[4] = {tf32(s.dDl[r0 * LDT + va]), tf32(s.dDl[r1 * LDT + va]), tf32(s.dDl[r0 * LDT + vb]),
                         tf32(s.dDl[r1 * LDT + vb])};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int c = n0 + nt * 8 + g;
-        uint32_t b[2] = {tf32(bfbits2f(s.S0[c * LDB + va])), tf32(bfbits2f(s.S0[c * LDB + vb]))};
+        uint32_t b[2] = {(uint32_t)s.S0[va * LDB + c] << 16, (uint32_t)s.S0[vb * LDB + c] << 16};
         mma8(dq[nt], aO, b);
         mma8(dw[nt], aD, b);
       }
@@ -259,19 +266,15 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
     zero_acc(acc);
     for (int kk = 0; kk < 16; ++kk)
       mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int v) { return s.Dl[(i0 + i) * LDT + v]; },
-                   [&](int v, int c) { return bfbits2f(s.dS[(n0 + c) * LDB + v]); });
+                   [&](int v, int c) { return bfbits2f(s.dS[v * LDB + n0 + c]); });
     acc_foreach(acc, [&](int r, int c, float& x) { a.dkd[toff + (i0 + r) * DK + n0 + c] = x; });
   }
-  for (int c = warp * 16; c < warp * 16 + 16; ++c) {
+  if (threadIdx.x < DK) {  // dgam[c] = sum_v S0[c][v] dS[c][v]  (column sums of the [v][c] tiles)
+    const int c = threadIdx.x;
     float sum = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int v = lane * 4 + q;
-      sum += bfbits2f(s.S0[c * LDB + v]) * bfbits2f(s.dS[c * LDB + v]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) a.dgam[((size_t)chunk * a.HV + h) * DK + c] = sum;
+#pragma unroll 8
+    for (int v = 0; v < DK; ++v) sum += bfbits2f(s.S0[v * LDB + c]) * bfbits2f(s.dS[v * LDB + c]);
+    a.dgam[((size_t)chunk * a.HV + h) * DK + c] = sum;
   }
 }
 
@@ -567,7 +570,7 @@ template <int NW>
 static cudaError_t launch_walk_bwd_nw(const WalkBwdArgs& a, int ndocs, cudaStream_t st) {
   const size_t sm = 2 * sizeof(WalkBwdA<NW>) + sizeof(WalkBwdB);
   cudaFuncSetAttribute(k_walk_bwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  dim3 grid(ndocs * (8 / NW), a.HV);
+  dim3 grid(ndocs * a.HV * (8 / NW));
   k_walk_bwd<NW><<<grid, NW * 32, sm, st>>>(a);
   return cudaGetLastError();
 }

@@ -106,8 +106,11 @@ __global__ void __launch_bounds__(NW * 32) k_walk_fwd(WalkArgs a) {
   using Stage = WalkFwdStage<NW>;
   extern __shared__ __align__(16) unsigned char smraw[];
   Stage* stg = reinterpret_cast<Stage*>(smraw);
-  const int doc = a.order[blockIdx.x / VS];
-  const int h = blockIdx.y;
+  // Block index -> (document rank, head, value slice): all heads and slices
+  // of the longest document first.
+  const int rank = blockIdx.x / (a.HV * VS);
+  const int h = (blockIdx.x / VS) % a.HV;
+  const int doc = a.order[rank];
   const DocDesc dd = a.docs[doc];
   const int warp = threadIdx.x >> 5;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
@@ -144,9 +147,15 @@ __global__ void __launch_bounds__(NW * 32) k_walk_fwd(WalkArgs a) {
     cp_async_wait<1>();
     __syncthreads();
     const Stage& sm = stg[m & 1];
-    if (a.tape) {
+    if (a.tape) {  // S0^T, [v][c], as BF16 pairs
       __nv_bfloat16* tp = a.tape + state_off(chunk, h, a.HV);
-      acc_foreach(S, [&](int r, int c, float& x) { tp[(size_t)c * DK + v0 + r] = __float2bfloat16_rn(x); });
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int c = nt * 8 + 2 * t;
+        *reinterpret_cast<__nv_bfloat162*>(&tp[(size_t)(v0 + g) * DK + c]) = __floats2bfloat162_rn(S[nt][0], S[nt][1]);
+        *reinterpret_cast<__nv_bfloat162*>(&tp[(size_t)(v0 + g + 8) * DK + c]) =
+            __floats2bfloat162_rn(S[nt][2], S[nt][3]);
+      }
     }
     // P = S^T w^T   (16 x 64)
     float P[8][4];
@@ -157,7 +166,7 @@ __global__ void __launch_bounds__(NW * 32) k_walk_fwd(WalkArgs a) {
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const float2 wv = *reinterpret_cast<const float2*>(&sm.W[(nt * 8 + g) * LDT + kk * 8 + 2 * t]);
-        uint32_t b[2] = {tf32(wv.x), tf32(wv.y)};
+        uint32_t b[2] = {__float_as_uint(wv.x), __float_as_uint(wv.y)};  // stored TF32-rounded
         mma8(P[nt], av, b);
       }
     }
@@ -172,7 +181,8 @@ __global__ void __launch_bounds__(NW * 32) k_walk_fwd(WalkArgs a) {
       const int j0 = kk * 8 + 2 * t;
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {tf32(sm.Kd[j0 * LDT + nt * 8 + g]), tf32(sm.Kd[(j0 + 1) * LDT + nt * 8 + g])};
+        uint32_t b[2] = {__float_as_uint(sm.Kd[j0 * LDT + nt * 8 + g]),
+                         __float_as_uint(sm.Kd[(j0 + 1) * LDT + nt * 8 + g])};
         mma8(S[nt], av, b);
       }
     }
@@ -205,9 +215,9 @@ __global__ void __launch_bounds__(256) k_out(OutArgs a) {
   const size_t toff = tile_off(chunk, h, a.HV);
   const __nv_bfloat16* S0 = a.tape + state_off(chunk, h, a.HV);
   const float* aqk = a.aqk + sq_off(chunk, h, a.HV);
-  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {
-    const int c = e >> 4, v8 = (e & 15) * 8;
-    cp_async16(&s.S0[c * LDB + v8], &S0[c * DK + v8]);
+  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // S0^T rows
+    const int v = e >> 4, c8 = (e & 15) * 8;
+    cp_async16(&s.S0[v * LDB + c8], &S0[v * DK + c8]);
   }
   for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
     const int i = e >> 5, c4 = (e & 31) * 4;
@@ -229,7 +239,7 @@ __global__ void __launch_bounds__(256) k_out(OutArgs a) {
   zero_acc(acc);
   for (int kk = 0; kk < 16; ++kk)
     mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int c) { return s.Qp[(i0 + i) * LDT + c]; },
-                 [&](int c, int v) { return bfbits2f(s.S0[c * LDB + n0 + v]); });
+                 [&](int c, int v) { return bfbits2f(s.S0[(n0 + v) * LDB + c]); });
   cp_async_wait<0>();
   __syncthreads();
   for (int kk = 0; kk < 2 * I + 2; ++kk)
@@ -268,7 +278,7 @@ template <int NW>
 static cudaError_t launch_walk_fwd_nw(const WalkArgs& a, int ndocs, cudaStream_t st) {
   const size_t sm = 2 * sizeof(WalkFwdStage<NW>);
   cudaFuncSetAttribute(k_walk_fwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  dim3 grid(ndocs * (8 / NW), a.HV);
+  dim3 grid(ndocs * a.HV * (8 / NW));
   k_walk_fwd<NW><<<grid, NW * 32, sm, st>>>(a);
   return cudaGetLastError();
 }

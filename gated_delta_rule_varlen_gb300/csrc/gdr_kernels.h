@@ -10,7 +10,7 @@ struct ChunkDesc;
 struct DocDesc;
 
 // Chunk-major intermediates: tiles [NC][HV][64][128] FP32, Aqk [NC][HV][64][64],
-// gamma [NC][HV][128], state tapes [NC][HV][128][128] (S[k][v]).
+// gamma [NC][HV][128], BF16 state tapes [NC][HV][128][128] stored transposed (S^T[v][k]).
 struct PrepArgs {
   const __nv_bfloat16 *q, *k, *v;
   const float* g;
