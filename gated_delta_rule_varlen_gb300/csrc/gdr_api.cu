@@ -76,7 +76,7 @@ struct Layout {
   int64_t NC = 0;
   size_t docs = 0, chunks = 0, order = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, gam = 0, tape = 0;
   size_t saved_total = 0;
-  size_t dstape = 0, ddelta = 0, dqs = 0, dw = 0, dkd = 0, dgam = 0, dqp = 0, dkp = 0;
+  size_t dstape = 0, ddelta = 0, dqs = 0, dw = 0, dkd = 0, dgam = 0, daqk = 0, dqp = 0, dkp = 0;
   size_t bwd_total = 0;
 };
 
@@ -112,6 +112,7 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
   L.dw = take(tile);
   L.dkd = take(tile);
   L.dgam = take(vec);
+  L.daqk = take(sq);
   if (grouped) {
     L.dqp = take(tile);
     L.dkp = take(tile);
@@ -407,6 +408,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   gs.dw = at<float>(scratch, L.dw);
   gs.dkd = at<float>(scratch, L.dkd);
   gs.dgam = at<float>(scratch, L.dgam);
+  gs.daqk = at<float>(scratch, L.daqk);
   {
     ProfScope ps("grad_state", stream);
     st = cuda_status(launch_grad_state(gs, (int)NC, stream));
@@ -435,6 +437,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   ga.dw = gs.dw;
   ga.dkd = gs.dkd;
   ga.dgam = gs.dgam;
+  ga.daqk = gs.daqk;
   ga.dq = static_cast<__nv_bfloat16*>(dq);
   ga.dk = static_cast<__nv_bfloat16*>(dk);
   ga.dv = static_cast<__nv_bfloat16*>(dv);

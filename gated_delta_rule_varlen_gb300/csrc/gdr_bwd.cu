@@ -269,6 +269,30 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
                    [&](int v, int c) { return bfbits2f(s.dS[v * LDB + n0 + c]); });
     acc_foreach(acc, [&](int r, int c, float& x) { a.dkd[toff + (i0 + r) * DK + n0 + c] = x; });
   }
+  {  // dAqk = scale tril(dO Delta^T): this warp's rows, columns j in [32 (w / 4), +32)
+    const int jt0 = (warp >> 2) * 4;
+    float acc[4][4];
+    zero_acc(acc);
+    for (int kk = 0; kk < 16; ++kk) {
+      const int va = kk * 8 + t, vb = va + 4;
+      const int r0 = i0 + g, r1 = i0 + g + 8;
+      uint32_t aO[4] = {(uint32_t)s.dO[r0 * LDB + va] << 16, (uint32_t)s.dO[r1 * LDB + va] << 16,
+                        (uint32_t)s.dO[r0 * LDB + vb] << 16, (uint32_t)s.dO[r1 * LDB + vb] << 16};
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        if (jt0 + nt < 2 * I + 2) {
+          const int j = (jt0 + nt) * 8 + g;
+          uint32_t b[2] = {tf32(s.Dl[j * LDT + va]), tf32(s.Dl[j * LDT + vb])};
+          mma8(acc[nt], aO, b);
+        }
+      }
+    }
+    float* daqk = a.daqk + sq_off(chunk, h, a.HV);
+    acc_foreach(acc, [&](int r, int col, float& x) {
+      const int i = i0 + r, j = jt0 * 8 + col;
+      daqk[i * CH + j] = j <= i ? a.scale * x : 0.f;
+    });
+  }
   if (threadIdx.x < DK) {  // dgam[c] = sum_v S0[c][v] dS[c][v]  (column sums of the [v][c] tiles)
     const int c = threadIdx.x;
     float sum = 0.f;
@@ -289,59 +313,49 @@ struct GradSmem {
   float dAqk[CH * LDS];
   float dK[CH * LDT];
   float dG[CH * LDT];
-  float dbeta[CH];
+  float dbeta[2][CH];
   float col[4 * DK];
   float rowsum[CH];
 };
 
+// 8 warps: warp w owns rows 16 (w % 4) .. +15 and channels 64 (w / 4) .. +63
+// of every per-row result.  The one product that contracts over channels (dA)
+// is summed over the two channel halves in two ordered passes.
 template <bool VEC, typename BetaT>
-__global__ void __launch_bounds__(128) k_grad(GradArgs a) {
+__global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   GradSmem& sg = *reinterpret_cast<GradSmem*>(smem_raw);
   ChunkSmemB& s = sg.c;
   const int chunk = blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
-  const int tid = threadIdx.x;
-  const int I = tid >> 5, i0 = 16 * I;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int I = warp & 3, i0 = 16 * I, hc = warp >> 2, c0 = 64 * hc;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
-  if (tid < CH) sg.dbeta[tid] = 0.f;
+  const size_t qoff = sq_off(chunk, h, a.HV);
+  if (tid < 2 * CH) (&sg.dbeta[0][0])[tid] = 0.f;
   // dw and dDelta (the B operands of X and Y) go into the dK / dG tiles, which
-  // are free until X and Y are formed.
+  // are free until X and Y are formed; dAqk into its own tile.
   for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
     const int i = e >> 5, c4 = (e & 31) * 4;
     cp_async16(&sg.dK[i * LDT + c4], &a.dw[toff + i * DK + c4]);
     cp_async16(&sg.dG[i * LDT + c4], &a.ddelta[toff + i * DK + c4]);
   }
+  for (int e = tid; e < CH * CH / 4; e += blockDim.x) {
+    const int i = e >> 4, c4 = (e & 15) * 4;
+    cp_async16(&sg.dAqk[i * LDS + c4], &a.daqk[qoff + i * CH + c4]);
+  }
   cp_async_commit();
   load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
                          a.HV);
-  gram<VEC, false>(s, nullptr);
+  if (warp < 4) gram<VEC, false>(s, nullptr);
   __syncthreads();
   invert(s);
   auto gl = [&](int i, int c) -> float { return VEC ? s.G[i * LDT + c] : s.gs[i]; };
 
-  // dAqk = scale tril(dO Delta^T)
-  {
-    const float* dl = a.delta + toff;
-    float acc[8][4];
-    zero_acc(acc);
-    for (int kk = 0; kk < 16; ++kk)
-      mma_kstep<8>(
-          acc, kk * 8, 0, 2 * I + 2,
-          [&](int i, int v) {
-            const int row = i0 + i;
-            return row < cd.len ? ldg_bf(&a.dout[((size_t)(cd.tok0 + row) * a.HV + h) * DK + v]) : 0.f;
-          },
-          [&](int v, int j) { return __ldg(&dl[j * DK + v]); });
-    acc_foreach(acc, [&](int r, int col, float& x) {
-      sg.dAqk[(i0 + r) * LDS + col] = col <= i0 + r ? a.scale * x : 0.f;
-    });
-  }
-
-  // X = T^T dw, Y = T^T dDelta (rows of this warp; T^T is upper triangular)
-  float X[16][4], Y[16][4];
+  // X = T^T dw, Y = T^T dDelta (rows of block I, this warp's channel half)
+  float X[8][4], Y[8][4];
   zero_acc(X);
   zero_acc(Y);
   {
@@ -352,8 +366,8 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
       uint32_t av[4] = {tf32(s.T[ja * LDS + i0 + g]), tf32(s.T[ja * LDS + i0 + g + 8]),
                         tf32(s.T[jb * LDS + i0 + g]), tf32(s.T[jb * LDS + i0 + g + 8])};
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + g;
+      for (int nt = 0; nt < 8; ++nt) {
+        const int c = c0 + nt * 8 + g;
         uint32_t bx[2] = {tf32(dw[ja * LDT + c]), tf32(dw[jb * LDT + c])};
         uint32_t by[2] = {tf32(dd[ja * LDT + c]), tf32(dd[jb * LDT + c])};
         mma8(X[nt], av, bx);
@@ -369,7 +383,7 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
     cp_async16(&sg.dG[i * LDT + c4], &a.u[toff + i * DK + c4]);
   }
   cp_async_commit();
-  // dA = -strict_tril(X w^T + Y u^T)  -> overwrites s.T once every warp is done with T.
+  // Partial dA over this warp's channel half: X w^T + Y u^T.
   float dAacc[8][4];
   zero_acc(dAacc);
   cp_async_wait<0>();
@@ -378,15 +392,16 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
     const float* w = sg.dK;
     const float* u = sg.dG;
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
+    for (int kk = 0; kk < 8; ++kk) {
       uint32_t ax[4] = {tf32(X[kk][0]), tf32(X[kk][2]), tf32(X[kk][1]), tf32(X[kk][3])};
       uint32_t ay[4] = {tf32(Y[kk][0]), tf32(Y[kk][2]), tf32(Y[kk][1]), tf32(Y[kk][3])};
+      const int cc = c0 + kk * 8 + 2 * t;
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         if (nt < 2 * I + 2) {
           const int j = nt * 8 + g;
-          const float2 wv = *reinterpret_cast<const float2*>(&w[j * LDT + kk * 8 + 2 * t]);
-          const float2 uv = *reinterpret_cast<const float2*>(&u[j * LDT + kk * 8 + 2 * t]);
+          const float2 wv = *reinterpret_cast<const float2*>(&w[j * LDT + cc]);
+          const float2 uv = *reinterpret_cast<const float2*>(&u[j * LDT + cc]);
           uint32_t bw[2] = {__float_as_uint(wv.x), __float_as_uint(wv.y)};
           uint32_t bu[2] = {__float_as_uint(uv.x), __float_as_uint(uv.y)};
           mma8(dAacc[nt], ax, bw);
@@ -395,15 +410,23 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
       }
     }
   }
+  // dA = -strict_tril(sum of the two halves) into s.T (T is no longer read).
+  float* sDA = s.T;
+  if (hc == 0)
+    acc_foreach(dAacc, [&](int r, int col, float& x) { sDA[(i0 + r) * LDS + col] = col < i0 + r ? -x : 0.f; });
   __syncthreads();
-  // Row-local: dV, dbeta (X.Kp + Y.V), dKp' from X.
+  if (hc == 1)
+    acc_foreach(dAacc, [&](int r, int col, float& x) {
+      if (col < i0 + r) sDA[(i0 + r) * LDS + col] -= x;
+    });
+  // Row-local (this warp's rows and channel half): dV, dbeta (X.Kp + Y.V), dKp' from X.
   {
     float db0 = 0.f, db1 = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
+    for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int row = g + 8 * (r >> 1), c = nt * 8 + 2 * t + (r & 1);
+        const int row = g + 8 * (r >> 1), c = c0 + nt * 8 + 2 * t + (r & 1);
         const int i = i0 + row;
         const float e = ex2(gl(i, c));
         const float kv = s.k(i, c);
@@ -421,26 +444,25 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
     db1 += __shfl_xor_sync(0xffffffffu, db1, 1);
     db1 += __shfl_xor_sync(0xffffffffu, db1, 2);
     if (t == 0) {
-      sg.dbeta[i0 + g] += db0;
-      sg.dbeta[i0 + g + 8] += db1;
+      sg.dbeta[hc][i0 + g] += db0;
+      sg.dbeta[hc][i0 + g + 8] += db1;
     }
   }
-
-  float* sDA = s.T;
-  acc_foreach(dAacc, [&](int r, int col, float& x) { sDA[(i0 + r) * LDS + col] = col < i0 + r ? -x : 0.f; });
   __syncthreads();
   if (tid < CH) {
     float acc = 0.f;
     for (int j = 0; j < tid; ++j) acc += sDA[tid * LDS + j] * s.At[tid * LDS + j];
-    sg.dbeta[tid] += acc;
+    sg.dbeta[0][tid] += acc;
   }
+  auto kf = [&](int j, int c) { return s.k(j, c); };
+  auto qf = [&](int j, int c) { return s.q(j, c); };
   // dKp' += beta [dA (x) decay] K
   {
-    float Z[16][4];
+    float Z[8][4];
     zero_acc(Z);
-    left_apply<VEC>(s, sDA, [&](int j, int c) { return s.k(j, c); }, Z);
-    acc_foreach(Z, [&](int r, int c, float& x) {
-      const int i = i0 + r;
+    left_apply<VEC, 8>(s, sDA, kf, Z, I, c0);
+    acc_foreach(Z, [&](int r, int col, float& x) {
+      const int i = i0 + r, c = c0 + col;
       const float v = s.beta[i] * x;
       sg.dK[i * LDT + c] += v;
       sg.dG[i * LDT + c] += s.k(i, c) * v;
@@ -448,11 +470,11 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
   }
   // dQ = dqs * Gamma + [dAqk (x) decay] K
   {
-    float Z[16][4];
+    float Z[8][4];
     zero_acc(Z);
-    left_apply<VEC>(s, sg.dAqk, [&](int j, int c) { return s.k(j, c); }, Z);
-    acc_foreach(Z, [&](int r, int c, float& x) {
-      const int i = i0 + r;
+    left_apply<VEC, 8>(s, sg.dAqk, kf, Z, I, c0);
+    acc_foreach(Z, [&](int r, int col, float& x) {
+      const int i = i0 + r, c = c0 + col;
       const float dq = __ldg(&a.dqs[toff + i * DK + c]) * ex2(gl(i, c)) + x;
       sg.dG[i * LDT + c] += s.q(i, c) * dq;
       if (a.dq_part) {
@@ -464,50 +486,40 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
   }
   // dKn' = [dAqk (x) decay]^T Q + [beta dA (x) decay]^T K
   {
-    float Z[16][4];
+    float Z[8][4];
     zero_acc(Z);
-    right_apply2<VEC>(s, sg.dAqk, [&](int i, int c) { return s.q(i, c); }, sDA, [&](int i, int c) { return s.k(i, c); },
-                      Z);
-    acc_foreach(Z, [&](int r, int c, float& x) {
-      const int i = i0 + r;
+    right_apply2<VEC, 8>(s, sg.dAqk, qf, sDA, kf, Z, I, c0);
+    acc_foreach(Z, [&](int r, int col, float& x) {
+      const int i = i0 + r, c = c0 + col;
       sg.dK[i * LDT + c] += x;
       sg.dG[i * LDT + c] -= s.k(i, c) * x;
     });
   }
-  // dKd terms (own rows), column sums of Kd*dKd, then dk.
+  // dKd terms (own rows and channels), column sums of Kd*dKd, then dk.
   {
     const float* dkd = a.dkd + toff;
     const float* kd = a.kd + toff;
-    float csum[4] = {0.f, 0.f, 0.f, 0.f};
+    float csum[2] = {0.f, 0.f};
     for (int rr = 0; rr < 16; ++rr) {
       const int i = i0 + rr;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int c = lane * 4 + q4;
+      for (int q2 = 0; q2 < 2; ++q2) {
+        const int c = c0 + lane * 2 + q2;
         const float x = __ldg(&dkd[i * DK + c]);
         const float kdv = __ldg(&kd[i * DK + c]);
         const float glast = VEC ? s.G[(CH - 1) * LDT + c] : s.gs[CH - 1];
-        sg.dK[i * LDT + c] += x * ex2(glast - gl(i, c));
+        const float dk = sg.dK[i * LDT + c] + x * ex2(glast - gl(i, c));
         sg.dG[i * LDT + c] -= kdv * x;
-        csum[q4] += kdv * x;
-      }
-    }
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) sg.col[I * DK + lane * 4 + q4] = csum[q4];
-    __syncwarp();
-    for (int rr = 0; rr < 16; ++rr) {
-      const int i = i0 + rr;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int c = lane * 4 + q4;
-        const float x = sg.dK[i * LDT + c];
+        csum[q2] += kdv * x;
         if (a.dk_part) {
-          a.dk_part[toff + i * DK + c] = x;
+          a.dk_part[toff + i * DK + c] = dk;
         } else if (i < cd.len) {
-          a.dk[((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + c] = __float2bfloat16_rn(x);
+          a.dk[((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + c] = __float2bfloat16_rn(dk);
         }
       }
     }
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) sg.col[I * DK + c0 + lane * 2 + q2] = csum[q2];
   }
   __syncthreads();
   const float* gam = a.gam + ((size_t)chunk * a.HV + h) * DK;
@@ -541,7 +553,8 @@ __global__ void __launch_bounds__(128) k_grad(GradArgs a) {
     }
   }
   if (tid < cd.len)
-    reinterpret_cast<BetaT*>(a.dbeta)[(size_t)(cd.tok0 + tid) * a.HV + h] = from_f<BetaT>(sg.dbeta[tid]);
+    reinterpret_cast<BetaT*>(a.dbeta)[(size_t)(cd.tok0 + tid) * a.HV + h] =
+        from_f<BetaT>(sg.dbeta[0][tid] + sg.dbeta[1][tid]);
 }
 
 // dq / dk of a Q/K head = FP32 sum over its value heads, rounded once.
@@ -599,16 +612,16 @@ cudaError_t launch_grad(const GradArgs& a, int nchunks, bool vec, bool beta_bf16
   dim3 grid(nchunks, a.HV);
   if (vec && beta_bf16) {
     cudaFuncSetAttribute(k_grad<true, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_grad<true, __nv_bfloat16><<<grid, 128, sm, st>>>(a);
+    k_grad<true, __nv_bfloat16><<<grid, 256, sm, st>>>(a);
   } else if (vec) {
     cudaFuncSetAttribute(k_grad<true, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_grad<true, float><<<grid, 128, sm, st>>>(a);
+    k_grad<true, float><<<grid, 256, sm, st>>>(a);
   } else if (beta_bf16) {
     cudaFuncSetAttribute(k_grad<false, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_grad<false, __nv_bfloat16><<<grid, 128, sm, st>>>(a);
+    k_grad<false, __nv_bfloat16><<<grid, 256, sm, st>>>(a);
   } else {
     cudaFuncSetAttribute(k_grad<false, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_grad<false, float><<<grid, 128, sm, st>>>(a);
+    k_grad<false, float><<<grid, 256, sm, st>>>(a);
   }
   return cudaGetLastError();
 }

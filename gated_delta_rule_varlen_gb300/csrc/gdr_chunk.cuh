@@ -221,7 +221,7 @@ __device__ void gram(ChunkSmemT<ET>& s, float* __restrict__ aqk) {
 template <typename ET>
 __device__ void invert(ChunkSmemT<ET>& s) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
-  if (lane < 16) {
+  if (warp < 4 && lane < 16) {
     const int i0 = warp * 16, j = lane;
     float x[16];
 #pragma unroll
@@ -264,14 +264,16 @@ __device__ void invert(ChunkSmemT<ET>& s) {
   }
 }
 
-// Z_i += sum_{j<=i} M_ij Y_j * exp(gc_i - gc_j)   (rows i of this warp's block)
-// M is a masked [64][64] shared tile (stride LDS); fy(j, c) returns Y_jc.
-template <bool VEC, typename ET, class FY>
-__device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M, FY fy, float (&Z)[16][4]) {
-  const int I = threadIdx.x >> 5, i0 = 16 * I;
+// Z_i += sum_{j<=i} M_ij Y_j * exp(gc_i - gc_j) for rows i of block I
+// (16I .. 16I+15) and channels c0 .. c0 + 8 NT - 1.  M is a masked [64][64]
+// shared tile (stride LDS); fy(j, c) returns Y_jc.
+template <bool VEC, int NT, typename ET, class FY>
+__device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M, FY fy, float (&Z)[NT][4], int I,
+                           int c0) {
+  const int i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   if (VEC) {
-    float acc[16][4];
+    float acc[NT][4];
     zero_acc(acc);
     if (I > 0) {
       for (int kk = 0; kk < 2 * I; ++kk) {  // j in [0, 16I)
@@ -279,15 +281,16 @@ __device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M,
         uint32_t a[4] = {tf32(M[(i0 + g) * LDS + j0]), tf32(M[(i0 + g + 8) * LDS + j0]),
                          tf32(M[(i0 + g) * LDS + j1]), tf32(M[(i0 + g + 8) * LDS + j1])};
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          const int c = nt * 8 + g;
+        for (int nt = 0; nt < NT; ++nt) {
+          const int c = c0 + nt * 8 + g;
           const float bI = s.G[(i0 - 1) * LDT + c];
           uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LDT + c]))};
           mma8(acc[nt], a, b);
         }
       }
       acc_foreach(acc, [&](int r, int col, float& x) {
-        Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[(i0 + r) * LDT + col] - s.G[(i0 - 1) * LDT + col]);
+        Z[col >> 3][(r >> 3) * 2 + (col & 1)] +=
+            x * ex2(s.G[(i0 + r) * LDT + c0 + col] - s.G[(i0 - 1) * LDT + c0 + col]);
       });
     }
     zero_acc(acc);
@@ -297,15 +300,15 @@ __device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M,
       uint32_t a[4] = {tf32(M[(i0 + g) * LDS + j0]), tf32(M[(i0 + g + 8) * LDS + j0]),
                        tf32(M[(i0 + g) * LDS + j1]), tf32(M[(i0 + g + 8) * LDS + j1])};
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + g;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = c0 + nt * 8 + g;
         const float mI = s.G[(i0 + 7) * LDT + c];
         uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LDT + c]))};
         mma8(acc[nt], a, b);
       }
     }
     acc_foreach(acc, [&](int r, int col, float& x) {
-      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[(i0 + r) * LDT + col] - s.G[(i0 + 7) * LDT + col]);
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[(i0 + r) * LDT + c0 + col] - s.G[(i0 + 7) * LDT + c0 + col]);
     });
   } else {
     for (int kk = 0; kk < 2 * I + 2; ++kk) {
@@ -314,8 +317,8 @@ __device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M,
       auto mv = [&](int i, int j) { return j <= i ? M[i * LDS + j] * ex2(s.gs[i] - s.gs[j]) : 0.f; };
       uint32_t a[4] = {tf32(mv(ra, j0)), tf32(mv(rb, j0)), tf32(mv(ra, j1)), tf32(mv(rb, j1))};
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + g;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = c0 + nt * 8 + g;
         uint32_t b[2] = {tf32(fy(j0, c)), tf32(fy(j1, c))};
         mma8(Z[nt], a, b);
       }
@@ -323,16 +326,16 @@ __device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M,
   }
 }
 
-// Z_j += sum_{i>=j} (M0_ij Y0_i + beta_i M1_ij Y1_i) * exp(gc_i - gc_j)
-// (rows j of this warp's block).  M0, M1 masked [64][64] shared tiles;
-// f0(i, c), f1(i, c) return Y0_ic, Y1_ic.
-template <bool VEC, typename ET, class F0, class F1>
+// Z_j += sum_{i>=j} (M0_ij Y0_i + beta_i M1_ij Y1_i) * exp(gc_i - gc_j) for rows
+// j of block J and channels c0 .. c0 + 8 NT - 1.  M0, M1 masked [64][64]
+// shared tiles; f0(i, c), f1(i, c) return Y0_ic, Y1_ic.
+template <bool VEC, int NT, typename ET, class F0, class F1>
 __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M0, F0 f0, const float* __restrict__ M1,
-                             F1 f1, float (&Z)[16][4]) {
-  const int J = threadIdx.x >> 5, j0b = 16 * J;
+                             F1 f1, float (&Z)[NT][4], int J, int c0) {
+  const int j0b = 16 * J;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   if (VEC) {
-    float acc[16][4];
+    float acc[NT][4];
     zero_acc(acc);
     const int ref = j0b + 15;  // gc at the end of block J
     for (int kk = 2 * J + 2; kk < 8; ++kk) {  // i in blocks after J
@@ -342,8 +345,8 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
       uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + j0b + g]), tf32(s.beta[ia] * M1[ia * LDS + j0b + g + 8]),
                         tf32(s.beta[ib] * M1[ib * LDS + j0b + g]), tf32(s.beta[ib] * M1[ib * LDS + j0b + g + 8])};
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + g;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = c0 + nt * 8 + g;
         const float bJ = s.G[ref * LDT + c];
         const float ea = ex2(s.G[ia * LDT + c] - bJ), eb = ex2(s.G[ib * LDT + c] - bJ);
         uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
@@ -353,7 +356,7 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
       }
     }
     acc_foreach(acc, [&](int r, int col, float& x) {
-      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[ref * LDT + col] - s.G[(j0b + r) * LDT + col]);
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[ref * LDT + c0 + col] - s.G[(j0b + r) * LDT + c0 + col]);
     });
     zero_acc(acc);
     const int mref = j0b + 7;
@@ -365,8 +368,8 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
       uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + j0b + g]), tf32(s.beta[ia] * M1[ia * LDS + j0b + g + 8]),
                         tf32(s.beta[ib] * M1[ib * LDS + j0b + g]), tf32(s.beta[ib] * M1[ib * LDS + j0b + g + 8])};
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + g;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = c0 + nt * 8 + g;
         const float mJ = s.G[mref * LDT + c];
         const float ea = ex2(s.G[ia * LDT + c] - mJ), eb = ex2(s.G[ib * LDT + c] - mJ);
         uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
@@ -376,7 +379,7 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
       }
     }
     acc_foreach(acc, [&](int r, int col, float& x) {
-      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[mref * LDT + col] - s.G[(j0b + r) * LDT + col]);
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[mref * LDT + c0 + col] - s.G[(j0b + r) * LDT + c0 + col]);
     });
   } else {
     for (int kk = 2 * J; kk < 8; ++kk) {
@@ -389,8 +392,8 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
       uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + ja] * da0), tf32(s.beta[ia] * M1[ia * LDS + jb] * da1),
                         tf32(s.beta[ib] * M1[ib * LDS + ja] * db0), tf32(s.beta[ib] * M1[ib * LDS + jb] * db1)};
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + g;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = c0 + nt * 8 + g;
         uint32_t b0[2] = {tf32(f0(ia, c)), tf32(f0(ib, c))};
         uint32_t b1[2] = {tf32(f1(ia, c)), tf32(f1(ib, c))};
         mma8(Z[nt], a0, b0);

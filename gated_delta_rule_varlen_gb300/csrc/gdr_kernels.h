@@ -62,6 +62,7 @@ struct GradStateArgs {
   const __nv_bfloat16 *tape, *dstape;
   const float *delta, *ddelta;
   float *dqs, *dw, *dkd, *dgam;  // scratch outputs
+  float* daqk;                   // scale * tril(dO Delta^T), [NC][HV][64][64]
 };
 
 struct GradArgs {
@@ -73,7 +74,7 @@ struct GradArgs {
   int Hqk, HV;
   float scale;
   const float *w, *u, *kd, *gam, *aqk, *delta, *ddelta;
-  const float *dqs, *dw, *dkd, *dgam;
+  const float *dqs, *dw, *dkd, *dgam, *daqk;
   // outputs
   __nv_bfloat16 *dq, *dk, *dv;   // dq/dk written directly when HV == Hqk
   float *dq_part, *dk_part;      // [NC][HV][64][128] per value head when HV > Hqk
