@@ -29,6 +29,7 @@ GDR_WORKSPACE_TOO_SMALL = 3
 GDR_UNSUPPORTED = 4
 GDR_STALE_WORKSPACE = 5
 GDR_CUDA_ERROR = 6
+GDR_DEVICE_TIMEOUT = 7
 
 EXPORTED = (
     "gdr_status_string",
@@ -41,6 +42,7 @@ EXPORTED = (
     "gdn_bwd",
     "gdr_profile_enable",
     "gdr_profile_report",
+    "gdr_check_device",
 )
 
 _lock = threading.Lock()
@@ -57,6 +59,7 @@ PSZ = ctypes.POINTER(ctypes.c_size_t)
 _SIGS = {
     "gdr_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "gdr_profile_enable": ([ctypes.c_int], ctypes.c_int),
+    "gdr_check_device": ([], ctypes.c_int),
     "gdr_profile_report": ([ctypes.c_char_p, SZ], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
@@ -270,3 +273,9 @@ def kda_fwd_noalloc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, out, h
                                 arr.shape[0] - 1, T, H, float(scale), _ptr(h0), _ptr(out), _ptr(ht), _stream(stream))
     _check(st, "kda_fwd_noalloc")
     return out, ht
+
+
+def gdr_check_device():
+    """Synchronize and raise GdrError if a kernel of the library timed out a
+    bounded wait (or a CUDA error occurred) since the last check."""
+    _check(load().gdr_check_device(), "gdr_check_device")

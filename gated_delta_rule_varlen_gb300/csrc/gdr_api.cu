@@ -10,6 +10,8 @@
 #include <vector>
 #include <cstdio>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/gdr.h"
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
@@ -205,6 +207,55 @@ bool aligned(const void* p) { return ((uintptr_t)p % kAlign) == 0; }
 gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_CUDA_ERROR; }
 
 // ---------------------------------------------------------------------------
+// TMA tensor maps (encoded on the host; the driver entry point is fetched
+// through the runtime, so the library does not link the driver library).
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// A row-major FP32 matrix [rows][cols] read in boxes of 32 columns (128 bytes,
+// 128-byte swizzle) x box_rows rows.
+bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * sizeof(float)};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Device error word: a kernel whose bounded wait runs out writes a non-zero
+// code here (and skips the work that depended on the wait).
+static __device__ int g_device_error;
+std::mutex g_err_mu;
+int* g_err_ptr[64] = {};
+
+int* device_error_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+
+// ---------------------------------------------------------------------------
 // Opt-in per-kernel timing for benchmarks: while enabled, every launch is
 // bracketed by a pair of CUDA events recorded on the launch's stream.
 // ---------------------------------------------------------------------------
@@ -337,8 +388,8 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   oa.HV = HV;
   oa.scale = scale;
   oa.qp = pa.qp;
-  oa.tape = wa.tape;
   oa.aqk = pa.aqk;
+  oa.tape = wa.tape;
   oa.delta = wa.delta;
   oa.out = static_cast<__nv_bfloat16*>(out);
   {
@@ -518,6 +569,7 @@ const char* gdr_status_string(gdr_status s) {
     case GDR_UNSUPPORTED: return "GDR_UNSUPPORTED";
     case GDR_STALE_WORKSPACE: return "GDR_STALE_WORKSPACE";
     case GDR_CUDA_ERROR: return "GDR_CUDA_ERROR";
+    case GDR_DEVICE_TIMEOUT: return "GDR_DEVICE_TIMEOUT";
     default: return "GDR_UNKNOWN_STATUS";
   }
 }
@@ -582,6 +634,20 @@ gdr_status kda_fwd_noalloc(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16*
   if (!scratch) return st;
   return gdr::fwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, h0, out, ht, nullptr, 0,
                        0, scratch, gdr::kStaticScratchBytes, stream);
+}
+
+gdr_status gdr_check_device(void) {
+  int* p = gdr::device_error_ptr();
+  if (!p) return GDR_CUDA_ERROR;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GDR_CUDA_ERROR;
+  int code = 0;
+  if (cudaMemcpy(&code, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GDR_CUDA_ERROR;
+  if (code != 0) {
+    const int zero = 0;
+    cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return GDR_DEVICE_TIMEOUT;
+  }
+  return GDR_OK;
 }
 
 int gdr_profile_enable(int on) {

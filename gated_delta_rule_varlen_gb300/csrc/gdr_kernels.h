@@ -1,5 +1,6 @@
 // gdr_kernels.h -- kernel argument blocks and launchers (internal to the library).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>

@@ -72,6 +72,7 @@ typedef int gdr_status;
 #define GDR_UNSUPPORTED 4          /* device is not sm_103 (GB300 / B300) */
 #define GDR_STALE_WORKSPACE 5      /* `saved` not filled by a matching forward with save_for_bwd = 1 */
 #define GDR_CUDA_ERROR 6           /* a CUDA launch or runtime call failed */
+#define GDR_DEVICE_TIMEOUT 7       /* a kernel's bounded wait ran out (reported by gdr_check_device) */
 
 /* Human-readable name of a status code (static string). */
 const char* gdr_status_string(gdr_status status);
@@ -150,6 +151,14 @@ gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
                    int32_t HV, float scale, const float* h0, const gdr_bf16* dout, const float* dht,
                    const void* saved, size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg,
                    float* dbeta, float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+
+/* Diagnostic (no counterpart on the pages): synchronizes the current device
+ * and reports whether any kernel of this library gave up a bounded wait on
+ * its own asynchronous copies or tensor-core operations since the last check
+ * (GDR_DEVICE_TIMEOUT; the word is then cleared), or a CUDA error occurred
+ * (GDR_CUDA_ERROR).  Kernels never spin without a time limit; a kernel that
+ * times out skips the dependent work, so its outputs are then incomplete. */
+gdr_status gdr_check_device(void);
 
 /* Benchmark support (no counterpart on the pages): opt-in per-kernel timing.
  * gdr_profile_enable(1) clears previous records and makes every subsequent

@@ -42,6 +42,7 @@ def run_gpu(variant, x, cu, scale=SCALE, h0=None, dht=None, backward=True, want_
         res.update(bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, scale, xd["dout"], saved, h0=h0d,
                        dht=dhtd, want_dh0=want_dh0))
     torch.cuda.synchronize()
+    gdr.gdr_check_device()  # no kernel gave up a bounded wait
     return res
 
 

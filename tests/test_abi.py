@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(gdr):
 
 def test_status_strings(gdr):
     names = {0: "GDR_OK", 1: "GDR_INVALID_ARG", 2: "GDR_BAD_CU_SEQLENS", 3: "GDR_WORKSPACE_TOO_SMALL",
-             4: "GDR_UNSUPPORTED", 5: "GDR_STALE_WORKSPACE", 6: "GDR_CUDA_ERROR"}
+             4: "GDR_UNSUPPORTED", 5: "GDR_STALE_WORKSPACE", 6: "GDR_CUDA_ERROR", 7: "GDR_DEVICE_TIMEOUT"}
     for code, name in names.items():
         assert gdr.status_string(code) == name
     assert gdr.status_string(99) == "GDR_UNKNOWN_STATUS"
