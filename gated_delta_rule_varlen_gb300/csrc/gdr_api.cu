@@ -202,6 +202,19 @@ int walk_warps(int64_t chains) {
   return 8;
 }
 
+// Value columns per tensor-core walk CTA (16, 32 or 64; one CTA per SM):
+// the narrowest slice that still fits every CTA in one wave, else 64.
+int walk_tc_cols(int64_t chains) {
+  if (const char* e = std::getenv("GDR_WALK_COLS")) {
+    const int v = std::atoi(e);
+    if (v == 16 || v == 32 || v == 64) return v;
+  }
+  const int64_t sms = sm_count();
+  for (int cols = 16; cols < 64; cols *= 2)
+    if (chains * (DK / cols) <= sms) return cols;
+  return 64;
+}
+
 bool aligned(const void* p) { return ((uintptr_t)p % kAlign) == 0; }
 
 gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_CUDA_ERROR; }
@@ -370,17 +383,20 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   wa.docs = docs;
   wa.order = order;
   wa.HV = HV;
-  wa.w = pa.w;
   wa.u = pa.u;
-  wa.kd = pa.kd;
   wa.gam = pa.gam;
+  wa.err = device_error_ptr();
+  if (!wa.err) return GDR_CUDA_ERROR;
+  if (NC > 0 && (!fp32_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, CH) ||
+                 !fp32_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, DK)))
+    return GDR_CUDA_ERROR;
   wa.h0 = h0;
   wa.tape = at<__nv_bfloat16>(base, L.tape);
   wa.delta = at<float>(base, L.delta);
   wa.ht = ht;
   {
     ProfScope ps("walk_fwd", stream);
-    st = cuda_status(launch_walk_fwd(wa, N, walk_warps((int64_t)N * HV), stream));
+    st = cuda_status(launch_walk_fwd(wa, N, walk_tc_cols((int64_t)N * HV), stream));
   }
   if (st != GDR_OK) return st;
   OutArgs oa{};

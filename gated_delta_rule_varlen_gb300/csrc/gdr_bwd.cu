@@ -34,7 +34,7 @@ namespace gdr {
 template <int NW>
 struct WalkBwdA {
   float Aqk[CH * LDS];
-  float Kd[CH * LDT];
+  float Kd[DK * LDS];  // Kd^T, [c][j]
   uint16_t dO[CH * (NW * 16 + 8)];
   float gam[DK];
 };
@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
     const size_t toff = tile_off(chunk, h, a.HV);
     const size_t qoff = sq_off(chunk, h, a.HV);
     for (int e = threadIdx.x; e < CH * DK / 4; e += NTH) {
-      const int i = e >> 5, c4 = (e & 31) * 4;
-      cp_async16(&A.Kd[i * LDT + c4], &a.kd[toff + i * DK + c4]);
+      const int c = e >> 4, j4 = (e & 15) * 4;
+      cp_async16(&A.Kd[c * LDS + j4], &a.kd[toff + c * CH + j4]);
     }
     for (int e = threadIdx.x; e < CH * CH / 4; e += NTH) {
       const int i = e >> 4, c4 = (e & 15) * 4;
@@ -144,8 +144,8 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
       uint32_t av[4] = {tf32(S[kk][0]), tf32(S[kk][2]), tf32(S[kk][1]), tf32(S[kk][3])};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        const float2 kv = *reinterpret_cast<const float2*>(&A.Kd[(nt * 8 + g) * LDT + kk * 8 + 2 * t]);
-        uint32_t b[2] = {__float_as_uint(kv.x), __float_as_uint(kv.y)};
+        uint32_t b[2] = {__float_as_uint(A.Kd[(kk * 8 + 2 * t) * LDS + nt * 8 + g]),
+                         __float_as_uint(A.Kd[(kk * 8 + 2 * t + 1) * LDS + nt * 8 + g])};
         mma8(E[nt], av, b);
       }
     }
@@ -210,9 +210,9 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
   const size_t toff = tile_off(chunk, h, a.HV);
   const __nv_bfloat16* S0 = a.tape + state_off(chunk, h, a.HV);
   const __nv_bfloat16* dS = a.dstape + state_off(chunk, h, a.HV);
-  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // S0^T rows [v][c]
-    const int v = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(&s.S0[v * LDB + c8], &S0[v * DK + c8]);
+  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // S0 rows [c][v]
+    const int c = e >> 4, v8 = (e & 15) * 8;
+    cp_async16(&s.S0[c * LDB + v8], &S0[c * DK + v8]);
   }
   for (int e = threadIdx.x; e < CH * DK / 8; e += 256) {
     const int i = e >> 4, v8 = (e & 15) * 8;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int c = n0 + nt * 8 + g;
-        uint32_t b[2] = {(uint32_t)s.S0[va * LDB + c] << 16, (uint32_t)s.S0[vb * LDB + c] << 16};
+        uint32_t b[2] = {(uint32_t)s.S0[c * LDB + va] << 16, (uint32_t)s.S0[c * LDB + vb] << 16};
         mma8(dq[nt], aO, b);
         mma8(dw[nt], aD, b);
       }
@@ -293,11 +293,11 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
       daqk[i * CH + j] = j <= i ? a.scale * x : 0.f;
     });
   }
-  if (threadIdx.x < DK) {  // dgam[c] = sum_v S0[c][v] dS[c][v]  (column sums of the [v][c] tiles)
+  if (threadIdx.x < DK) {  // dgam[c] = sum_v S0[c][v] dS[c][v]  (S0 tile [c][v], dS tile [v][c])
     const int c = threadIdx.x;
     float sum = 0.f;
 #pragma unroll 8
-    for (int v = 0; v < DK; ++v) sum += bfbits2f(s.S0[v * LDB + c]) * bfbits2f(s.dS[v * LDB + c]);
+    for (int v = 0; v < DK; ++v) sum += bfbits2f(s.S0[c * LDB + v]) * bfbits2f(s.dS[v * LDB + c]);
     a.dgam[((size_t)chunk * a.HV + h) * DK + c] = sum;
   }
 }
@@ -498,7 +498,6 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   // dKd terms (own rows and channels), column sums of Kd*dKd, then dk.
   {
     const float* dkd = a.dkd + toff;
-    const float* kd = a.kd + toff;
     float csum[2] = {0.f, 0.f};
     for (int rr = 0; rr < 16; ++rr) {
       const int i = i0 + rr;
@@ -506,9 +505,10 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
       for (int q2 = 0; q2 < 2; ++q2) {
         const int c = c0 + lane * 2 + q2;
         const float x = __ldg(&dkd[i * DK + c]);
-        const float kdv = __ldg(&kd[i * DK + c]);
         const float glast = VEC ? s.G[(CH - 1) * LDT + c] : s.gs[CH - 1];
-        const float dk = sg.dK[i * LDT + c] + x * ex2(glast - gl(i, c));
+        const float ed = ex2(glast - gl(i, c));
+        const float kdv = s.k(i, c) * ed;  // Kd = K * exp(gc_last - gc)
+        const float dk = sg.dK[i * LDT + c] + x * ed;
         sg.dG[i * LDT + c] -= kdv * x;
         csum[q2] += kdv * x;
         if (a.dk_part) {

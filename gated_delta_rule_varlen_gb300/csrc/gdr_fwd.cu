@@ -1,6 +1,7 @@
 // gdr_fwd.cu -- forward kernels: WY prep, inter-chunk state walk, output.
 #include "gdr_chunk.cuh"
 #include "gdr_kernels.h"
+#include "gdr_tc.cuh"
 
 namespace gdr {
 
@@ -33,8 +34,14 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
     const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
     a.qp[toff + e] = __uint_as_float(tf32(s.q(i, d) * ex2(gl)));
-    a.kd[toff + e] = __uint_as_float(tf32(s.k(i, d) * ex2(glast - gl)));
     if (i == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d] = ex2(glast);
+  }
+  // Kd stored transposed, [c][j] (the K-major A operand of the walk's state update).
+  for (int e = threadIdx.x; e < CH * DK; e += blockDim.x) {
+    const int d = e >> 6, i = e & 63;
+    const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
+    const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
+    a.kd[toff + e] = __uint_as_float(tf32(s.k(i, d) * ex2(glast - gl)));
   }
   __syncthreads();
   // Q tile <- v rows (async; used for u), G tile <- beta * K * Gamma (for w).
@@ -80,115 +87,225 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// State walk (one CTA per (document, value head, value-column slice), the
-// document's chunks in order; documents issued longest first).  Each warp owns
-// 16 value columns of the FP32 state, held transposed (S^T: 16 x 128) in
-// mma accumulators, and per chunk:
-//   tape <- S0 (BF16);  Delta = u - w S0;  S <- diag(gamma) S0 + Kd^T Delta.
-// The next chunk's w, Kd, u slice and gamma are copied into the other half of
-// a double buffer with cp.async while the current chunk is computed.
+// State walk on the tensor cores (one CTA of 4 warps per (document, value
+// head, N-column value slice); the document's chunks in order, documents
+// issued longest first).  The FP32 state slice S[c][v0 .. v0+N) lives in
+// tensor memory, one channel c per TMEM lane (= thread).  Per chunk:
+//   tape <- S0 (BF16 row per thread);  S0 -> swizzled TF32 operand tile;
+//   P = w S0          (tcgen05.mma M = 64 tokens, N, K = 128)
+//   Delta = u - P     (rows of P back from TMEM; Delta -> operand tile)
+//   S <- diag(gamma) S0 + Kd^T Delta   (gamma applied in TMEM, then
+//                      tcgen05.mma M = 128 channels, N, K = 64 accumulating)
+// w and Kd^T arrive by TMA into a double buffer two chunks ahead; u and
+// gamma by cp.async.  Waits are bounded; a timed-out wait ends the walk for
+// the whole CTA and sets the device error word.
 // The "state walk" of PR #8638 (opening description) and the walks of
 // PR #7723 (opening description).
 // ---------------------------------------------------------------------------
-template <int NW>
-struct WalkFwdStage {
-  float W[CH * LDT];
-  float Kd[CH * LDT];
-  float U[CH * (NW * 16 + 4)];
-  float gam[DK];
+template <int N>
+struct WalkTcSmem {
+  float W[2][CH * DK];      // A of P: w, rows j, K = c (four 64 x 32 column blocks)
+  float KdT[2][DK * CH];    // A of the update: Kd^T, rows c, K = j (two 128 x 32 column blocks)
+  float Sop[N * DK];        // B of P: S0, rows v, K = c
+  float Dop[N * CH];        // B of the update: Delta, rows v, K = j
+  float U[2][CH * (N + 4)];
+  float gam[2][DK];
+  uint64_t bar_tma[2], bar_p, bar_u;
+  uint32_t tmem;
 };
 
-template <int NW>
-__global__ void __launch_bounds__(NW * 32) k_walk_fwd(WalkArgs a) {
-  constexpr int VS = 8 / NW;         // CTAs per (doc, head)
-  constexpr int LDU = NW * 16 + 4;   // row stride of the u slice
-  constexpr int NTH = NW * 32;
-  using Stage = WalkFwdStage<NW>;
-  extern __shared__ __align__(16) unsigned char smraw[];
-  Stage* stg = reinterpret_cast<Stage*>(smraw);
-  // Block index -> (document rank, head, value slice): all heads and slices
-  // of the longest document first.
-  const int rank = blockIdx.x / (a.HV * VS);
+template <int N>
+__global__ void __launch_bounds__(128) k_walk_fwd(const __grid_constant__ WalkArgs a) {
+  constexpr int VS = DK / N;  // CTAs per (doc, head)
+  constexpr int LDU = N + 4;
+  constexpr uint32_t TCOLS = 2 * N < 32 ? 32 : 2 * N;
+  extern __shared__ unsigned char smraw[];
+  WalkTcSmem<N>& s = *reinterpret_cast<WalkTcSmem<N>*>(tc::align1024(smraw));
+  const int rank = blockIdx.x / (a.HV * VS);  // all heads and slices of the longest document first
   const int h = (blockIdx.x / VS) % a.HV;
   const int doc = a.order[rank];
   const DocDesc dd = a.docs[doc];
-  const int warp = threadIdx.x >> 5;
-  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
-  const int vcta = (blockIdx.x % VS) * NW * 16;
-  const int v0 = vcta + warp * 16;
+  const int n = dd.nchunks;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
+  const int v0 = (blockIdx.x % VS) * N;
   const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
 
-  auto issue = [&](int m, Stage& s) {
+  if (tid == 0) {
+    tc::mbar_init(&s.bar_tma[0], 1);
+    tc::mbar_init(&s.bar_tma[1], 1);
+    tc::mbar_init(&s.bar_p, 1);
+    tc::mbar_init(&s.bar_u, 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&s.tmem, TCOLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s.tmem;
+  const uint32_t tS = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes; S in columns [0, N)
+  const uint32_t tP = tS + N;                                // P in columns [N, 2N)
+
+  int issued = 0;  // TMA stages issued (thread 0's count is the one that matters)
+  auto issue = [&](int m) {
+    const int b = m & 1;
     const int chunk = dd.chunk0 + m;
+    const int item = chunk * a.HV + h;
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(&s.bar_tma[b], 2 * CH * DK * 4);
+      for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(&s.W[b][kb * CH * 32], &a.w_map, kb * 32, item * CH, &s.bar_tma[b]);
+      for (int kb = 0; kb < 2; ++kb)
+        tc::tma_load_2d(&s.KdT[b][kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_tma[b]);
+    }
     const size_t toff = tile_off(chunk, h, a.HV);
-    for (int e = threadIdx.x; e < CH * DK / 4; e += NTH) {
-      const int i = e >> 5, c4 = (e & 31) * 4;
-      cp_async16(&s.W[i * LDT + c4], &a.w[toff + i * DK + c4]);
-      cp_async16(&s.Kd[i * LDT + c4], &a.kd[toff + i * DK + c4]);
+    for (int e = tid; e < CH * N / 4; e += 128) {
+      const int i = e / (N / 4), c4 = (e % (N / 4)) * 4;
+      cp_async16(&s.U[b][i * LDU + c4], &a.u[toff + (size_t)i * DK + v0 + c4]);
     }
-    for (int e = threadIdx.x; e < CH * NW * 4; e += NTH) {
-      const int i = e / (NW * 4), c4 = (e % (NW * 4)) * 4;
-      cp_async16(&s.U[i * LDU + c4], &a.u[toff + i * DK + vcta + c4]);
-    }
-    for (int e = threadIdx.x; e < DK / 4; e += NTH)
-      cp_async16(&s.gam[e * 4], &a.gam[((size_t)chunk * a.HV + h) * DK + e * 4]);
+    if (tid < DK / 4) cp_async16(&s.gam[b][tid * 4], &a.gam[((size_t)chunk * a.HV + h) * DK + tid * 4]);
+    ++issued;
   };
 
-  float S[16][4];  // S^T rows v0+g(+8), cols c
-  acc_foreach(S, [&](int r, int c, float& x) { x = a.h0 ? a.h0[sidx + (size_t)c * DK + v0 + r] : 0.f; });
+  // S <- h0 (or 0)
+#pragma unroll
+  for (int cb = 0; cb < N; cb += 16) {
+    uint32_t r[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      r[q] = __float_as_uint(a.h0 ? a.h0[sidx + (size_t)tid * DK + v0 + cb + q] : 0.f);
+    tc::tmem_st16(tS + cb, r);
+  }
+  tc::tmem_wait_st();
 
-  if (dd.nchunks > 0) issue(0, stg[0]);
+  if (n > 0) issue(0);
   cp_async_commit();
-  for (int m = 0; m < dd.nchunks; ++m) {
+  if (n > 1) issue(1);
+  cp_async_commit();
+  constexpr uint32_t idP = tc::idesc_tf32(CH, N), idU = tc::idesc_tf32(DK, N);
+  unsigned char* sop = reinterpret_cast<unsigned char*>(s.Sop);
+  unsigned char* dop = reinterpret_cast<unsigned char*>(s.Dop);
+  bool ok = true;
+  int m = 0;
+  for (; m < n; ++m) {
+    const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     const size_t toff = tile_off(chunk, h, a.HV);
-    if (m + 1 < dd.nchunks) issue(m + 1, stg[(m + 1) & 1]);
-    cp_async_commit();
     cp_async_wait<1>();
+    ok = tc::mbar_wait(&s.bar_tma[b], (m >> 1) & 1) && ok;
+    tc::tc_fence_before();
+    if (!__syncthreads_and(ok)) break;
+    tc::tc_fence_after();
+    // S0 row c = tid (all loads in flight, one wait).
+    uint32_t sr[N];
+#pragma unroll
+    for (int cb = 0; cb < N; cb += 16) tc::tmem_ld16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&sr[cb]));
+    tc::tmem_wait_ld();
+    // S0 as the B operand of P (row v, k = c).
+#pragma unroll
+    for (int v = 0; v < N; ++v) *reinterpret_cast<uint32_t*>(sop + tc::sw128_offset(v, tid, N)) = tf32(__uint_as_float(sr[v]));
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
     __syncthreads();
-    const Stage& sm = stg[m & 1];
-    if (a.tape) {  // S0^T, [v][c], as BF16 pairs
-      __nv_bfloat16* tp = a.tape + state_off(chunk, h, a.HV);
+    tc::tc_fence_after();
+    if (tid == 0) {
+      const uint64_t aw = tc::desc_k_sw128(s.W[b]), bs = tc::desc_k_sw128(s.Sop);
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + 2 * t;
-        *reinterpret_cast<__nv_bfloat162*>(&tp[(size_t)(v0 + g) * DK + c]) = __floats2bfloat162_rn(S[nt][0], S[nt][1]);
-        *reinterpret_cast<__nv_bfloat162*>(&tp[(size_t)(v0 + g + 8) * DK + c]) =
-            __floats2bfloat162_rn(S[nt][2], S[nt][3]);
+      for (int k = 0; k < DK / 8; ++k)
+        tc::mma_tf32(tmem + N, aw + (uint64_t)((((k >> 2) * CH * 128) + (k & 3) * 32) >> 4),
+                     bs + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idP, k > 0);
+      tc::mma_commit(&s.bar_p);
+    }
+    // While P runs: the tape row and diag(gamma) S0 back into TMEM (columns the P MMA does not touch).
+    if (a.tape) {  // S0[c][v0 .. v0+N) as BF16
+      uint4* tp = reinterpret_cast<uint4*>(a.tape + state_off(chunk, h, a.HV) + (size_t)tid * DK + v0);
+#pragma unroll
+      for (int q = 0; q < N; q += 8) {
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(sr[q]), __uint_as_float(sr[q + 1]));
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(sr[q + 2]), __uint_as_float(sr[q + 3]));
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(sr[q + 4]), __uint_as_float(sr[q + 5]));
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(sr[q + 6]), __uint_as_float(sr[q + 7]));
+        tp[q / 8] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                               *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
       }
     }
-    // P = S^T w^T   (16 x 64)
-    float P[8][4];
-    zero_acc(P);
+    {
+      const float gm = s.gam[b][tid];
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      uint32_t av[4] = {tf32(S[kk][0]), tf32(S[kk][2]), tf32(S[kk][1]), tf32(S[kk][3])};
+      for (int v = 0; v < N; ++v) sr[v] = __float_as_uint(__uint_as_float(sr[v]) * gm);
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const float2 wv = *reinterpret_cast<const float2*>(&sm.W[(nt * 8 + g) * LDT + kk * 8 + 2 * t]);
-        uint32_t b[2] = {__float_as_uint(wv.x), __float_as_uint(wv.y)};  // stored TF32-rounded
-        mma8(P[nt], av, b);
+      for (int cb = 0; cb < N; cb += 16) tc::tmem_st16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&sr[cb]));
+      tc::tmem_wait_st();
+    }
+    ok = tc::mbar_wait(&s.bar_p, m & 1) && ok;
+    tc::tc_fence_after();
+    // Delta rows j = 16 warp + lane (TMEM lanes 0-15 of each warp hold the M = 64 result).
+    {
+      uint32_t pr[N];
+#pragma unroll
+      for (int cb = 0; cb < N; cb += 16) tc::tmem_ld16(tP + cb, *reinterpret_cast<uint32_t(*)[16]>(&pr[cb]));
+      tc::tmem_wait_ld();
+      float pv[N];
+#pragma unroll
+      for (int v = 0; v < N; ++v) pv[v] = __uint_as_float(pr[v]);
+      if (lane < 16) {
+        const int j = 16 * warp + lane;
+        const float* ur = &s.U[b][j * LDU];
+        float4* dr = reinterpret_cast<float4*>(a.delta + toff + (size_t)j * DK + v0);
+#pragma unroll
+        for (int v = 0; v < N; v += 4) {
+          float4 d;
+          d.x = ur[v] - pv[v];
+          d.y = ur[v + 1] - pv[v + 1];
+          d.z = ur[v + 2] - pv[v + 2];
+          d.w = ur[v + 3] - pv[v + 3];
+          if (a.delta) dr[v / 4] = d;
+          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v, j, N)) = tf32(d.x);
+          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v + 1, j, N)) = tf32(d.y);
+          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v + 2, j, N)) = tf32(d.z);
+          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v + 3, j, N)) = tf32(d.w);
+        }
       }
     }
-    // Delta^T = u^T - P
-    acc_foreach(P, [&](int r, int j, float& x) { x = sm.U[j * LDU + warp * 16 + r] - x; });
-    if (a.delta) acc_foreach(P, [&](int r, int j, float& x) { a.delta[toff + (size_t)j * DK + v0 + r] = x; });
-    // S^T <- S^T diag(gamma) + Delta^T Kd
-    acc_foreach(S, [&](int r, int c, float& x) { x *= sm.gam[c]; });
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t av[4] = {tf32(P[kk][0]), tf32(P[kk][2]), tf32(P[kk][1]), tf32(P[kk][3])};
-      const int j0 = kk * 8 + 2 * t;
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {__float_as_uint(sm.Kd[j0 * LDT + nt * 8 + g]),
-                         __float_as_uint(sm.Kd[(j0 + 1) * LDT + nt * 8 + g])};
-        mma8(S[nt], av, b);
-      }
-    }
+    tc::fence_proxy_async();
+    tc::tc_fence_before();
     __syncthreads();
+    tc::tc_fence_after();
+    if (tid == 0) {
+      const uint64_t ak = tc::desc_k_sw128(s.KdT[b]), bd = tc::desc_k_sw128(s.Dop);
+#pragma unroll
+      for (int k = 0; k < CH / 8; ++k)
+        tc::mma_tf32(tmem, ak + (uint64_t)((((k >> 2) * DK * 128) + (k & 3) * 32) >> 4),
+                     bd + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idU, 1);
+      tc::mma_commit(&s.bar_u);
+    }
+    ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
+    tc::tc_fence_after();
+    // Stage b is free again (its tiles were read by the two MMAs and the threads above).
+    if (m + 2 < n) issue(m + 2);
+    cp_async_commit();
   }
-  if (a.ht) acc_foreach(S, [&](int r, int c, float& x) { a.ht[sidx + (size_t)c * DK + v0 + r] = x; });
+  if (m < n) {
+    // A wait ran out: record it and drain this CTA's copies still in flight.
+    if (tid == 0) {
+      atomicExch(a.err, 3);
+      for (int q = m; q < issued; ++q) tc::mbar_wait(&s.bar_tma[q & 1], (q >> 1) & 1);
+    }
+    cp_async_wait<0>();
+  } else if (a.ht) {
+#pragma unroll
+    for (int cb = 0; cb < N; cb += 16) {
+      uint32_t r[16];
+      tc::tmem_ld16(tS + cb, r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 16; ++q) a.ht[sidx + (size_t)tid * DK + v0 + cb + q] = __uint_as_float(r[q]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -215,9 +332,9 @@ __global__ void __launch_bounds__(256) k_out(OutArgs a) {
   const size_t toff = tile_off(chunk, h, a.HV);
   const __nv_bfloat16* S0 = a.tape + state_off(chunk, h, a.HV);
   const float* aqk = a.aqk + sq_off(chunk, h, a.HV);
-  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // S0^T rows
-    const int v = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(&s.S0[v * LDB + c8], &S0[v * DK + c8]);
+  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // S0 rows [c][v]
+    const int c = e >> 4, v8 = (e & 15) * 8;
+    cp_async16(&s.S0[c * LDB + v8], &S0[c * DK + v8]);
   }
   for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
     const int i = e >> 5, c4 = (e & 31) * 4;
@@ -239,7 +356,7 @@ __global__ void __launch_bounds__(256) k_out(OutArgs a) {
   zero_acc(acc);
   for (int kk = 0; kk < 16; ++kk)
     mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int c) { return s.Qp[(i0 + i) * LDT + c]; },
-                 [&](int c, int v) { return bfbits2f(s.S0[(n0 + v) * LDB + c]); });
+                 [&](int c, int v) { return bfbits2f(s.S0[c * LDB + n0 + v]); });
   cp_async_wait<0>();
   __syncthreads();
   for (int kk = 0; kk < 2 * I + 2; ++kk)
@@ -274,22 +391,21 @@ cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16
   return cudaGetLastError();
 }
 
-template <int NW>
-static cudaError_t launch_walk_fwd_nw(const WalkArgs& a, int ndocs, cudaStream_t st) {
-  const size_t sm = 2 * sizeof(WalkFwdStage<NW>);
-  cudaFuncSetAttribute(k_walk_fwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  dim3 grid(ndocs * a.HV * (8 / NW));
-  k_walk_fwd<NW><<<grid, NW * 32, sm, st>>>(a);
+template <int N>
+static cudaError_t launch_walk_fwd_n(const WalkArgs& a, int ndocs, cudaStream_t st) {
+  const size_t sm = sizeof(WalkTcSmem<N>) + 1024;
+  cudaFuncSetAttribute(k_walk_fwd<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  dim3 grid(ndocs * a.HV * (DK / N));
+  k_walk_fwd<N><<<grid, 128, sm, st>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int warps_per_cta, cudaStream_t st) {
+cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int cols_per_cta, cudaStream_t st) {
   if (ndocs == 0) return cudaSuccess;
-  switch (warps_per_cta) {
-    case 1: return launch_walk_fwd_nw<1>(a, ndocs, st);
-    case 2: return launch_walk_fwd_nw<2>(a, ndocs, st);
-    case 4: return launch_walk_fwd_nw<4>(a, ndocs, st);
-    default: return launch_walk_fwd_nw<8>(a, ndocs, st);
+  switch (cols_per_cta) {
+    case 16: return launch_walk_fwd_n<16>(a, ndocs, st);
+    case 32: return launch_walk_fwd_n<32>(a, ndocs, st);
+    default: return launch_walk_fwd_n<64>(a, ndocs, st);
   }
 }
 

@@ -11,7 +11,8 @@ struct ChunkDesc;
 struct DocDesc;
 
 // Chunk-major intermediates: tiles [NC][HV][64][128] FP32, Aqk [NC][HV][64][64],
-// gamma [NC][HV][128], BF16 state tapes [NC][HV][128][128] stored transposed (S^T[v][k]).
+// Kd stored transposed per chunk ([NC][HV][128 c][64 j]), gamma [NC][HV][128],
+// BF16 state tapes [NC][HV][128][128]: S0 as S[c][v], dS transposed (dS^T[v][c]).
 struct PrepArgs {
   const __nv_bfloat16 *q, *k, *v;
   const float* g;
@@ -22,14 +23,17 @@ struct PrepArgs {
 };
 
 struct WalkArgs {
+  CUtensorMap w_map;    // w as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
+  CUtensorMap kdt_map;  // Kd^T as a 2-D FP32 tensor [NC*HV*128][64], 32 x 128 boxes, 128-byte swizzle
   const DocDesc* docs;
   const int* order;  // documents, longest first
   int HV;
-  const float *w, *u, *kd, *gam;
+  const float *u, *gam;
   const float* h0;   // [N][HV][128][128] or null
-  __nv_bfloat16* tape;  // S0 per chunk (BF16), or null
+  __nv_bfloat16* tape;  // S0 per chunk (BF16, S[c][v]), or null
   float* delta;      // Delta per chunk, or null
   float* ht;         // [N][HV][128][128] or null
+  int* err;          // device error word
 };
 
 struct OutArgs {
@@ -91,7 +95,7 @@ struct GroupReduceArgs {
 };
 
 cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
-cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int warps_per_cta, cudaStream_t st);
+cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int cols_per_cta, cudaStream_t st);
 cudaError_t launch_out(const OutArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, cudaStream_t st);
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st);
