@@ -388,7 +388,8 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   wa.err = device_error_ptr();
   if (!wa.err) return GDR_CUDA_ERROR;
   if (NC > 0 && (!fp32_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, CH) ||
-                 !fp32_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, DK)))
+                 !fp32_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, DK) ||
+                 !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, CH)))
     return GDR_CUDA_ERROR;
   wa.h0 = h0;
   wa.tape = at<__nv_bfloat16>(base, L.tape);

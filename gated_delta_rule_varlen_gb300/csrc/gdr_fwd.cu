@@ -104,21 +104,25 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
 // ---------------------------------------------------------------------------
 template <int N>
 struct WalkTcSmem {
+  static constexpr int UB = N < 32 ? 1 : N / 32;  // 32-column TMA boxes of the u slice
   float W[2][CH * DK];      // A of P: w, rows j, K = c (four 64 x 32 column blocks)
   float KdT[2][DK * CH];    // A of the update: Kd^T, rows c, K = j (two 128 x 32 column blocks)
   float Sop[N * DK];        // B of P: S0, rows v, K = c
   float Dop[N * CH];        // B of the update: Delta, rows v, K = j
-  float U[2][CH * (N + 4)];
+  float U[2][CH * 32 * UB]; // u slice, rows j, 32-column swizzled blocks
   float gam[2][DK];
   uint64_t bar_tma[2], bar_p, bar_u;
   uint32_t tmem;
 };
 
+// 4 data warps (thread t <-> TMEM lane t <-> channel c = t) and one issuer
+// warp (warp 4, lane 0) that issues the TMA copies and the MMAs.
 template <int N>
-__global__ void __launch_bounds__(128) k_walk_fwd(const __grid_constant__ WalkArgs a) {
+__global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkArgs a) {
   constexpr int VS = DK / N;  // CTAs per (doc, head)
-  constexpr int LDU = N + 4;
+  constexpr int UB = WalkTcSmem<N>::UB;
   constexpr uint32_t TCOLS = 2 * N < 32 ? 32 : 2 * N;
+  constexpr uint32_t STAGE_BYTES = (2 * CH * DK + CH * 32 * UB + DK) * 4;
   extern __shared__ unsigned char smraw[];
   WalkTcSmem<N>& s = *reinterpret_cast<WalkTcSmem<N>*>(tc::align1024(smraw));
   const int rank = blockIdx.x / (a.HV * VS);  // all heads and slices of the longest document first
@@ -127,10 +131,11 @@ __global__ void __launch_bounds__(128) k_walk_fwd(const __grid_constant__ WalkAr
   const DocDesc dd = a.docs[doc];
   const int n = dd.nchunks;
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
+  const bool issuer = tid == 128;
   const int v0 = (blockIdx.x % VS) * N;
   const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
 
-  if (tid == 0) {
+  if (issuer) {
     tc::mbar_init(&s.bar_tma[0], 1);
     tc::mbar_init(&s.bar_tma[1], 1);
     tc::mbar_init(&s.bar_p, 1);
@@ -145,44 +150,38 @@ __global__ void __launch_bounds__(128) k_walk_fwd(const __grid_constant__ WalkAr
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = s.tmem;
-  const uint32_t tS = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes; S in columns [0, N)
-  const uint32_t tP = tS + N;                                // P in columns [N, 2N)
+  const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes; S in columns [0, N)
+  const uint32_t tP = tS + N;                                      // P in columns [N, 2N)
 
-  int issued = 0;  // TMA stages issued (thread 0's count is the one that matters)
-  auto issue = [&](int m) {
+  auto issue = [&](int m) {  // issuer only
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     const int item = chunk * a.HV + h;
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(&s.bar_tma[b], 2 * CH * DK * 4);
-      for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(&s.W[b][kb * CH * 32], &a.w_map, kb * 32, item * CH, &s.bar_tma[b]);
-      for (int kb = 0; kb < 2; ++kb)
-        tc::tma_load_2d(&s.KdT[b][kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_tma[b]);
-    }
-    const size_t toff = tile_off(chunk, h, a.HV);
-    for (int e = tid; e < CH * N / 4; e += 128) {
-      const int i = e / (N / 4), c4 = (e % (N / 4)) * 4;
-      cp_async16(&s.U[b][i * LDU + c4], &a.u[toff + (size_t)i * DK + v0 + c4]);
-    }
-    if (tid < DK / 4) cp_async16(&s.gam[b][tid * 4], &a.gam[((size_t)chunk * a.HV + h) * DK + tid * 4]);
-    ++issued;
+    tc::mbar_arrive_expect_tx(&s.bar_tma[b], STAGE_BYTES);
+    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(&s.W[b][kb * CH * 32], &a.w_map, kb * 32, item * CH, &s.bar_tma[b]);
+    for (int kb = 0; kb < 2; ++kb)
+      tc::tma_load_2d(&s.KdT[b][kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_tma[b]);
+    for (int ub = 0; ub < UB; ++ub)
+      tc::tma_load_2d(&s.U[b][ub * CH * 32], &a.u_map, v0 + 32 * ub, item * CH, &s.bar_tma[b]);
+    tc::bulk_load(s.gam[b], &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, &s.bar_tma[b]);
   };
 
-  // S <- h0 (or 0)
+  if (tid < DK) {  // S <- h0 (or 0)
 #pragma unroll
-  for (int cb = 0; cb < N; cb += 16) {
-    uint32_t r[16];
+    for (int cb = 0; cb < N; cb += 16) {
+      uint32_t r[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
-      r[q] = __float_as_uint(a.h0 ? a.h0[sidx + (size_t)tid * DK + v0 + cb + q] : 0.f);
-    tc::tmem_st16(tS + cb, r);
+      for (int q = 0; q < 16; ++q)
+        r[q] = __float_as_uint(a.h0 ? a.h0[sidx + (size_t)tid * DK + v0 + cb + q] : 0.f);
+      tc::tmem_st16(tS + cb, r);
+    }
+    tc::tmem_wait_st();
   }
-  tc::tmem_wait_st();
-
-  if (n > 0) issue(0);
-  cp_async_commit();
-  if (n > 1) issue(1);
-  cp_async_commit();
+  int issued = 0;
+  if (issuer) {
+    if (n > 0) issue(0), ++issued;
+    if (n > 1) issue(1), ++issued;
+  }
   constexpr uint32_t idP = tc::idesc_tf32(CH, N), idU = tc::idesc_tf32(DK, N);
   unsigned char* sop = reinterpret_cast<unsigned char*>(s.Sop);
   unsigned char* dop = reinterpret_cast<unsigned char*>(s.Dop);
@@ -192,24 +191,25 @@ __global__ void __launch_bounds__(128) k_walk_fwd(const __grid_constant__ WalkAr
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     const size_t toff = tile_off(chunk, h, a.HV);
-    cp_async_wait<1>();
-    ok = tc::mbar_wait(&s.bar_tma[b], (m >> 1) & 1) && ok;
+    if (tid < DK) ok = tc::mbar_wait(&s.bar_tma[b], (m >> 1) & 1) && ok;
     tc::tc_fence_before();
     if (!__syncthreads_and(ok)) break;
     tc::tc_fence_after();
-    // S0 row c = tid (all loads in flight, one wait).
     uint32_t sr[N];
+    if (tid < DK) {
+      // S0 row c = tid; S0 as the B operand of P (row v, k = c).
 #pragma unroll
-    for (int cb = 0; cb < N; cb += 16) tc::tmem_ld16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&sr[cb]));
-    tc::tmem_wait_ld();
-    // S0 as the B operand of P (row v, k = c).
+      for (int cb = 0; cb < N; cb += 16) tc::tmem_ld16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&sr[cb]));
+      tc::tmem_wait_ld();
 #pragma unroll
-    for (int v = 0; v < N; ++v) *reinterpret_cast<uint32_t*>(sop + tc::sw128_offset(v, tid, N)) = tf32(__uint_as_float(sr[v]));
-    tc::fence_proxy_async();
+      for (int v = 0; v < N; ++v)
+        *reinterpret_cast<uint32_t*>(sop + tc::sw128_offset(v, tid, N)) = tf32(__uint_as_float(sr[v]));
+      tc::fence_proxy_async();
+    }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (tid == 0) {
+    if (issuer) {
       const uint64_t aw = tc::desc_k_sw128(s.W[b]), bs = tc::desc_k_sw128(s.Sop);
 #pragma unroll
       for (int k = 0; k < DK / 8; ++k)
@@ -217,62 +217,57 @@ __global__ void __launch_bounds__(128) k_walk_fwd(const __grid_constant__ WalkAr
                      bs + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idP, k > 0);
       tc::mma_commit(&s.bar_p);
     }
-    // While P runs: the tape row and diag(gamma) S0 back into TMEM (columns the P MMA does not touch).
-    if (a.tape) {  // S0[c][v0 .. v0+N) as BF16
-      uint4* tp = reinterpret_cast<uint4*>(a.tape + state_off(chunk, h, a.HV) + (size_t)tid * DK + v0);
+    if (tid < DK) {
+      // While P runs: the tape row and diag(gamma) S0 back into TMEM (columns P does not touch).
+      if (a.tape) {  // S0[c][v0 .. v0+N) as BF16
+        uint4* tp = reinterpret_cast<uint4*>(a.tape + state_off(chunk, h, a.HV) + (size_t)tid * DK + v0);
 #pragma unroll
-      for (int q = 0; q < N; q += 8) {
-        __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(sr[q]), __uint_as_float(sr[q + 1]));
-        __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(sr[q + 2]), __uint_as_float(sr[q + 3]));
-        __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(sr[q + 4]), __uint_as_float(sr[q + 5]));
-        __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(sr[q + 6]), __uint_as_float(sr[q + 7]));
-        tp[q / 8] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
-                               *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+        for (int q = 0; q < N; q += 8) {
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(sr[q]), __uint_as_float(sr[q + 1]));
+          __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(sr[q + 2]), __uint_as_float(sr[q + 3]));
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(sr[q + 4]), __uint_as_float(sr[q + 5]));
+          __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(sr[q + 6]), __uint_as_float(sr[q + 7]));
+          tp[q / 8] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                                 *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+        }
       }
-    }
-    {
       const float gm = s.gam[b][tid];
 #pragma unroll
       for (int v = 0; v < N; ++v) sr[v] = __float_as_uint(__uint_as_float(sr[v]) * gm);
 #pragma unroll
       for (int cb = 0; cb < N; cb += 16) tc::tmem_st16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&sr[cb]));
       tc::tmem_wait_st();
-    }
-    ok = tc::mbar_wait(&s.bar_p, m & 1) && ok;
-    tc::tc_fence_after();
-    // Delta rows j = 16 warp + lane (TMEM lanes 0-15 of each warp hold the M = 64 result).
-    {
-      uint32_t pr[N];
+      ok = tc::mbar_wait(&s.bar_p, m & 1) && ok;
+      tc::tc_fence_after();
+      // Delta = u - P over the 16-row block of this warp, spread over all 32 lanes:
+      // rows j0 = 16 warp + g and j0 + 8, columns 8q + 2u (+1).
+      uint32_t pr[N / 2];
 #pragma unroll
-      for (int cb = 0; cb < N; cb += 16) tc::tmem_ld16(tP + cb, *reinterpret_cast<uint32_t(*)[16]>(&pr[cb]));
+      for (int cb = 0; cb < N; cb += 16) tc::tmem_ld16x256b_x2(tP + cb, *reinterpret_cast<uint32_t(*)[8]>(&pr[cb / 2]));
       tc::tmem_wait_ld();
-      float pv[N];
+      const int g = lane >> 2, u2 = (lane & 3) * 2;
+      const unsigned char* ub = reinterpret_cast<const unsigned char*>(s.U[b]);
 #pragma unroll
-      for (int v = 0; v < N; ++v) pv[v] = __uint_as_float(pr[v]);
-      if (lane < 16) {
-        const int j = 16 * warp + lane;
-        const float* ur = &s.U[b][j * LDU];
-        float4* dr = reinterpret_cast<float4*>(a.delta + toff + (size_t)j * DK + v0);
+      for (int hr = 0; hr < 2; ++hr) {
+        const int j = 16 * warp + g + 8 * hr;
+        float* drow = a.delta ? a.delta + toff + (size_t)j * DK + v0 : nullptr;
 #pragma unroll
-        for (int v = 0; v < N; v += 4) {
-          float4 d;
-          d.x = ur[v] - pv[v];
-          d.y = ur[v + 1] - pv[v + 1];
-          d.z = ur[v + 2] - pv[v + 2];
-          d.w = ur[v + 3] - pv[v + 3];
-          if (a.delta) dr[v / 4] = d;
-          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v, j, N)) = tf32(d.x);
-          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v + 1, j, N)) = tf32(d.y);
-          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v + 2, j, N)) = tf32(d.z);
-          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v + 3, j, N)) = tf32(d.w);
+        for (int q = 0; q < N / 8; ++q) {
+          const int v = 8 * q + u2;
+          const float2 uu = *reinterpret_cast<const float2*>(ub + tc::sw128_offset(j, v, CH));
+          const float d0 = uu.x - __uint_as_float(pr[4 * q + 2 * hr]);
+          const float d1 = uu.y - __uint_as_float(pr[4 * q + 2 * hr + 1]);
+          if (drow) *reinterpret_cast<float2*>(drow + v) = make_float2(d0, d1);
+          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v, j, N)) = tf32(d0);
+          *reinterpret_cast<uint32_t*>(dop + tc::sw128_offset(v + 1, j, N)) = tf32(d1);
         }
       }
+      tc::fence_proxy_async();
     }
-    tc::fence_proxy_async();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (tid == 0) {
+    if (issuer) {
       const uint64_t ak = tc::desc_k_sw128(s.KdT[b]), bd = tc::desc_k_sw128(s.Dop);
 #pragma unroll
       for (int k = 0; k < CH / 8; ++k)
@@ -280,20 +275,18 @@ __global__ void __launch_bounds__(128) k_walk_fwd(const __grid_constant__ WalkAr
                      bd + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idU, 1);
       tc::mma_commit(&s.bar_u);
     }
-    ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
+    // Everyone (the issuer to refill stage b, the data warps before reading S) waits for the update.
+    if (tid < DK || issuer) ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
     tc::tc_fence_after();
-    // Stage b is free again (its tiles were read by the two MMAs and the threads above).
-    if (m + 2 < n) issue(m + 2);
-    cp_async_commit();
+    if (issuer && ok && m + 2 < n) issue(m + 2), ++issued;
   }
   if (m < n) {
-    // A wait ran out: record it and drain this CTA's copies still in flight.
-    if (tid == 0) {
+    // A wait ran out: record it and drain the copies still in flight.
+    if (issuer) {
       atomicExch(a.err, 3);
       for (int q = m; q < issued; ++q) tc::mbar_wait(&s.bar_tma[q & 1], (q >> 1) & 1);
     }
-    cp_async_wait<0>();
-  } else if (a.ht) {
+  } else if (a.ht && tid < DK) {
 #pragma unroll
     for (int cb = 0; cb < N; cb += 16) {
       uint32_t r[16];
@@ -396,7 +389,7 @@ static cudaError_t launch_walk_fwd_n(const WalkArgs& a, int ndocs, cudaStream_t 
   const size_t sm = sizeof(WalkTcSmem<N>) + 1024;
   cudaFuncSetAttribute(k_walk_fwd<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   dim3 grid(ndocs * a.HV * (DK / N));
-  k_walk_fwd<N><<<grid, 128, sm, st>>>(a);
+  k_walk_fwd<N><<<grid, 160, sm, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@ struct PrepArgs {
 struct WalkArgs {
   CUtensorMap w_map;    // w as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
   CUtensorMap kdt_map;  // Kd^T as a 2-D FP32 tensor [NC*HV*128][64], 32 x 128 boxes, 128-byte swizzle
+  CUtensorMap u_map;    // u as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
   const DocDesc* docs;
   const int* order;  // documents, longest first
   int HV;
