@@ -354,6 +354,18 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   invert(s);
   auto gl = [&](int i, int c) -> float { return VEC ? s.G[i * LDT + c] : s.gs[i]; };
 
+  // v of this thread's accumulator positions (rows i0+g, i0+g+8; channel pairs),
+  // fetched now so that its latency hides behind X, Y and dA.
+  __nv_bfloat162 vpre[8][2];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = i0 + g + 8 * hr;
+      vpre[nt][hr] = i < cd.len ? *reinterpret_cast<const __nv_bfloat162*>(
+                                      &a.v[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c0 + nt * 8 + 2 * t])
+                                : __floats2bfloat162_rn(0.f, 0.f);
+    }
   // X = T^T dw, Y = T^T dDelta (rows of block I, this warp's channel half)
   float X[8][4], Y[8][4];
   zero_acc(X);
@@ -425,18 +437,24 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int row = g + 8 * (r >> 1), c = c0 + nt * 8 + 2 * t + (r & 1);
-        const int i = i0 + row;
-        const float e = ex2(gl(i, c));
-        const float kv = s.k(i, c);
-        const float vv = i < cd.len ? ldg_bf(&a.v[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c]) : 0.f;
-        const float part = X[nt][r] * kv * e + Y[nt][r] * vv;
-        if (row < 8) db0 += part; else db1 += part;
-        if (i < cd.len) a.dv[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c] = __float2bfloat16_rn(s.beta[i] * Y[nt][r]);
-        const float dkp = s.beta[i] * X[nt][r] * e;
-        sg.dK[i * LDT + c] = dkp;
-        sg.dG[i * LDT + c] = kv * dkp;
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
+        const float2 vv = __bfloat1622float2(vpre[nt][hr]);
+        float part = 0.f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float x = X[nt][2 * hr + q], y = Y[nt][2 * hr + q];
+          const float e = ex2(gl(i, c + q));
+          const float kv = s.k(i, c + q);
+          part += x * kv * e + y * (q ? vv.y : vv.x);
+          const float dkp = s.beta[i] * x * e;
+          sg.dK[i * LDT + c + q] = dkp;
+          sg.dG[i * LDT + c + q] = kv * dkp;
+        }
+        if (hr == 0) db0 += part; else db1 += part;
+        if (i < cd.len)
+          *reinterpret_cast<__nv_bfloat162*>(&a.dv[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c]) =
+              __floats2bfloat162_rn(s.beta[i] * Y[nt][2 * hr], s.beta[i] * Y[nt][2 * hr + 1]);
       }
     }
     db0 += __shfl_xor_sync(0xffffffffu, db0, 1);
@@ -456,6 +474,13 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   }
   auto kf = [&](int j, int c) { return s.k(j, c); };
   auto qf = [&](int j, int c) { return s.q(j, c); };
+  // dqs at this thread's accumulator positions, fetched ahead of the two applies.
+  float2 dqspre[8][2];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr)
+      dqspre[nt][hr] = __ldg(reinterpret_cast<const float2*>(&a.dqs[toff + (i0 + g + 8 * hr) * DK + c0 + nt * 8 + 2 * t]));
   // dKp' += beta [dA (x) decay] K
   {
     float Z[8][4];
@@ -473,17 +498,28 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
     float Z[8][4];
     zero_acc(Z);
     left_apply<VEC, 8>(s, sg.dAqk, kf, Z, I, c0);
-    acc_foreach(Z, [&](int r, int col, float& x) {
-      const int i = i0 + r, c = c0 + col;
-      const float dq = __ldg(&a.dqs[toff + i * DK + c]) * ex2(gl(i, c)) + x;
-      sg.dG[i * LDT + c] += s.q(i, c) * dq;
-      if (a.dq_part) {
-        a.dq_part[toff + i * DK + c] = dq;
-      } else if (i < cd.len) {
-        a.dq[((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + c] = __float2bfloat16_rn(dq);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
+        const float dq0 = dqspre[nt][hr].x * ex2(gl(i, c)) + Z[nt][2 * hr];
+        const float dq1 = dqspre[nt][hr].y * ex2(gl(i, c + 1)) + Z[nt][2 * hr + 1];
+        sg.dG[i * LDT + c] += s.q(i, c) * dq0;
+        sg.dG[i * LDT + c + 1] += s.q(i, c + 1) * dq1;
+        if (a.dq_part) {
+          *reinterpret_cast<float2*>(&a.dq_part[toff + i * DK + c]) = make_float2(dq0, dq1);
+        } else if (i < cd.len) {
+          *reinterpret_cast<__nv_bfloat162*>(&a.dq[((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + c]) =
+              __floats2bfloat162_rn(dq0, dq1);
+        }
       }
-    });
   }
+  // dKd of this warp's rows and channel pairs, fetched ahead of the last apply.
+  float2 dkdpre[16];
+#pragma unroll
+  for (int rr = 0; rr < 16; ++rr)
+    dkdpre[rr] = __ldg(reinterpret_cast<const float2*>(&a.dkd[toff + (i0 + rr) * DK + c0 + lane * 2]));
   // dKn' = [dAqk (x) decay]^T Q + [beta dA (x) decay]^T K
   {
     float Z[8][4];
@@ -497,25 +533,29 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   }
   // dKd terms (own rows and channels), column sums of Kd*dKd, then dk.
   {
-    const float* dkd = a.dkd + toff;
     float csum[2] = {0.f, 0.f};
+    const int cp = c0 + lane * 2;
+    const float gl0 = VEC ? s.G[(CH - 1) * LDT + cp] : s.gs[CH - 1];
+    const float gl1 = VEC ? s.G[(CH - 1) * LDT + cp + 1] : s.gs[CH - 1];
+#pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
       const int i = i0 + rr;
+      float dk[2];
 #pragma unroll
       for (int q2 = 0; q2 < 2; ++q2) {
-        const int c = c0 + lane * 2 + q2;
-        const float x = __ldg(&dkd[i * DK + c]);
-        const float glast = VEC ? s.G[(CH - 1) * LDT + c] : s.gs[CH - 1];
-        const float ed = ex2(glast - gl(i, c));
+        const int c = cp + q2;
+        const float x = q2 ? dkdpre[rr].y : dkdpre[rr].x;
+        const float ed = ex2((q2 ? gl1 : gl0) - gl(i, c));
         const float kdv = s.k(i, c) * ed;  // Kd = K * exp(gc_last - gc)
-        const float dk = sg.dK[i * LDT + c] + x * ed;
+        dk[q2] = sg.dK[i * LDT + c] + x * ed;
         sg.dG[i * LDT + c] -= kdv * x;
         csum[q2] += kdv * x;
-        if (a.dk_part) {
-          a.dk_part[toff + i * DK + c] = dk;
-        } else if (i < cd.len) {
-          a.dk[((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + c] = __float2bfloat16_rn(dk);
-        }
+      }
+      if (a.dk_part) {
+        *reinterpret_cast<float2*>(&a.dk_part[toff + i * DK + cp]) = make_float2(dk[0], dk[1]);
+      } else if (i < cd.len) {
+        *reinterpret_cast<__nv_bfloat162*>(&a.dk[((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + cp]) =
+            __floats2bfloat162_rn(dk[0], dk[1]);
       }
     }
 #pragma unroll
@@ -525,14 +565,21 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   const float* gam = a.gam + ((size_t)chunk * a.HV + h) * DK;
   const float* dgam = a.dgam + ((size_t)chunk * a.HV + h) * DK;
   if (VEC) {
-    if (tid < DK) {
-      const int c = tid;
-      const float extra = gam[c] * dgam[c] + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
-      float acc = extra;
-      for (int i = CH - 1; i >= 0; --i) {
-        acc += sg.dG[i * LDT + c];
-        if (i < cd.len) a.dg[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c] = acc;
-      }
+    // Reverse cumsum over rows: threads 128..255 take rows 63..32, threads
+    // 0..127 rows 31..0 starting from the sum of rows 32..63.
+    const int c = tid & (DK - 1), half = tid >> 7;
+    float acc = gam[c] * dgam[c] + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
+    if (half == 0) {
+      float up[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = CH / 2; i < CH; ++i) up[i & 3] += sg.dG[i * LDT + c];
+      acc += (up[0] + up[1]) + (up[2] + up[3]);
+    }
+    const int hi = half ? CH - 1 : CH / 2 - 1;
+#pragma unroll 8
+    for (int i = hi; i > hi - CH / 2; --i) {
+      acc += sg.dG[i * LDT + c];
+      if (i < cd.len) a.dg[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c] = acc;
     }
   } else {
     if (tid < CH) {
