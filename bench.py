@@ -42,14 +42,14 @@ _TILE = D * 4           # one FP32 row of a [64][128] intermediate
 _STATE = D * D * 4 / C  # one FP32 128x128 state per chunk, per token
 KERNEL_MODEL = {
     # name: (bytes per token-head, flops per token-head)
-    "prep": (3 * 2 * D + 4 * D + 2 + 4 * _TILE + C * 4 + 4 * D / C,
+    "prep": (3 * 2 * D + 4 * D + 2 + 4 * _TILE + 3 * C * 4 + 4 * D / C,
              2 * (2 * 0.5 * C * D) + 2 * (2 * 0.5 * C * D) + C * C / 3),
     "walk_fwd": (3 * _TILE + _STATE + _TILE + 4 * D / C, 2 * (2 * D * D)),
     "out": (_TILE + _STATE + C * 4 + _TILE + 2 * D, 2 * D * D + 2 * 0.5 * C * D),
     "walk_bwd": (C * 4 + 3 * _TILE + 2 * D + _STATE + _TILE, 2 * (2 * D * D) + 2 * D * D + 2 * 0.5 * C * D),
     "grad_state": (2 * D + 2 * _STATE + 2 * _TILE + 3 * _TILE + 4 * D / C, 3 * (2 * D * D)),
-    "grad": (3 * 2 * D + 4 * D + 2 + 2 * D + 3 * _TILE + C * 4 + 2 * _TILE + 3 * _TILE + 3 * 2 * D + 4 * D + 2,
-             12 * (2 * 0.5 * C * D) + 2 * (2 * C * D) + C * C / 3),
+    "grad": (3 * 2 * D + 4 * D + 2 + 2 * D + 3 * _TILE + 3 * C * 4 + 2 * _TILE + 3 * _TILE + 3 * 2 * D + 4 * D + 2,
+             11 * (2 * 0.5 * C * D) + 2 * (2 * C * D)),
 }
 
 

@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N
 // ---------------------------------------------------------------------------
 struct Layout {
   int64_t NC = 0;
-  size_t docs = 0, chunks = 0, order = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, gam = 0, tape = 0;
+  size_t docs = 0, chunks = 0, order = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, amat = 0, tmat = 0,
+         gam = 0, tape = 0;
   size_t saved_total = 0;
   size_t dstape = 0, ddelta = 0, dqs = 0, dw = 0, dkd = 0, dgam = 0, daqk = 0, dqp = 0, dkp = 0;
   size_t bwd_total = 0;
@@ -104,6 +105,8 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
   L.kd = take(tile);
   L.delta = take(tile);
   L.aqk = take(sq);
+  L.amat = take(sq);
+  L.tmat = take(sq);
   L.gam = take(vec);
   L.tape = take(st);
   L.saved_total = o;
@@ -374,6 +377,8 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   pa.kd = at<float>(base, L.kd);
   pa.aqk = at<float>(base, L.aqk);
   pa.gam = at<float>(base, L.gam);
+  pa.amat = save_for_bwd ? at<float>(base, L.amat) : nullptr;
+  pa.tmat = save_for_bwd ? at<float>(base, L.tmat) : nullptr;
   {
     ProfScope ps("prep", stream);
     st = cuda_status(launch_prep(pa, (int)NC, vec, vec, stream));
@@ -506,6 +511,8 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   ga.dkd = gs.dkd;
   ga.dgam = gs.dgam;
   ga.daqk = gs.daqk;
+  ga.amat = at<float>(saved, L.amat);
+  ga.tmat = at<float>(saved, L.tmat);
   ga.dq = static_cast<__nv_bfloat16*>(dq);
   ga.dk = static_cast<__nv_bfloat16*>(dk);
   ga.dv = static_cast<__nv_bfloat16*>(dv);

@@ -342,16 +342,16 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
     cp_async16(&sg.dK[i * LDT + c4], &a.dw[toff + i * DK + c4]);
     cp_async16(&sg.dG[i * LDT + c4], &a.ddelta[toff + i * DK + c4]);
   }
+  // dAqk, and the forward's At and T of this chunk.
   for (int e = tid; e < CH * CH / 4; e += blockDim.x) {
     const int i = e >> 4, c4 = (e & 15) * 4;
     cp_async16(&sg.dAqk[i * LDS + c4], &a.daqk[qoff + i * CH + c4]);
+    cp_async16(&s.At[i * LDS + c4], &a.amat[qoff + i * CH + c4]);
+    cp_async16(&s.T[i * LDS + c4], &a.tmat[qoff + i * CH + c4]);
   }
   cp_async_commit();
   load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
                          a.HV);
-  if (warp < 4) gram<VEC, false>(s, nullptr);
-  __syncthreads();
-  invert(s);
   auto gl = [&](int i, int c) -> float { return VEC ? s.G[i * LDT + c] : s.gs[i]; };
 
   // v of this thread's accumulator positions (rows i0+g, i0+g+8; channel pairs),

@@ -215,9 +215,13 @@ __device__ void gram(ChunkSmemT<ET>& s, float* __restrict__ aqk) {
   }
 }
 
-// s.T = (I + diag(beta) At)^-1, unit lower triangular.  Diagonal 16x16 blocks
-// by forward substitution (one warp each), then off-diagonal blocks by
-// distance: T_IJ = -T_II * sum_{K=J}^{I-1} A_IK T_KJ.  FP32 on CUDA cores.
+// s.T = (I + diag(beta) At)^-1, unit lower triangular, in FP32 on CUDA cores.
+// Diagonal 16x16 blocks by forward substitution (warp I, one column per lane
+// of its first 16), then the blocks below them column block by column block:
+// warp J computes, for I = J+1 .. 3 in order,
+//   T_IJ = -T_II * diag(beta_I) * sum_{K=J}^{I-1} At_IK T_KJ,
+// which needs only blocks of column J that the same warp made before, so the
+// off-diagonal part synchronizes within the warp only.  Needs >= 4 warps.
 template <typename ET>
 __device__ void invert(ChunkSmemT<ET>& s) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
@@ -241,27 +245,54 @@ __device__ void invert(ChunkSmemT<ET>& s) {
     if ((j >> 4) > (i >> 4)) s.T[i * LDS + j] = 0.f;
   }
   __syncthreads();
-  for (int d = 1; d <= 3; ++d) {
-    const int npairs = 4 - d;
-    for (int e = tid; e < npairs * 256; e += blockDim.x) {
-      const int J = e >> 8, I = J + d, r = (e >> 4) & 15, c = e & 15;
-      const float bi = s.beta[16 * I + r];
-      float acc = 0.f;
-      for (int Kb = J; Kb < I; ++Kb)
+  if (warp < 3) {
+    const int J = warp, r = lane >> 1, half = (lane & 1) * 8, cb = 16 * J + half;
+    float* tmp = s.tmp + warp * 256;  // [16][16]: diag(beta_I) sum_K At_IK T_KJ
+    for (int I = J + 1; I < 4; ++I) {
+      const int row = 16 * I + r;
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
 #pragma unroll 4
-        for (int m = 0; m < 16; ++m)
-          acc += s.At[(16 * I + r) * LDS + 16 * Kb + m] * s.T[(16 * Kb + m) * LDS + 16 * J + c];
-      s.tmp[e] = bi * acc;
+      for (int k = 16 * J; k < 16 * I; ++k) {
+        const float av = s.At[row * LDS + k];
+        const float4 t0 = *reinterpret_cast<const float4*>(&s.T[k * LDS + cb]);
+        const float4 t1 = *reinterpret_cast<const float4*>(&s.T[k * LDS + cb + 4]);
+        acc[0] += av * t0.x;
+        acc[1] += av * t0.y;
+        acc[2] += av * t0.z;
+        acc[3] += av * t0.w;
+        acc[4] += av * t1.x;
+        acc[5] += av * t1.y;
+        acc[6] += av * t1.z;
+        acc[7] += av * t1.w;
+      }
+      const float bi = s.beta[row];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) tmp[r * 16 + half + q] = bi * acc[q];
+      __syncwarp();
+      float out[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) out[q] = 0.f;
+      for (int m = 0; m <= r; ++m) {
+        const float tv = s.T[row * LDS + 16 * I + m];
+        const float4 x0 = *reinterpret_cast<const float4*>(&tmp[m * 16 + half]);
+        const float4 x1 = *reinterpret_cast<const float4*>(&tmp[m * 16 + half + 4]);
+        out[0] += tv * x0.x;
+        out[1] += tv * x0.y;
+        out[2] += tv * x0.z;
+        out[3] += tv * x0.w;
+        out[4] += tv * x1.x;
+        out[5] += tv * x1.y;
+        out[6] += tv * x1.z;
+        out[7] += tv * x1.w;
+      }
+      *reinterpret_cast<float4*>(&s.T[row * LDS + cb]) = make_float4(-out[0], -out[1], -out[2], -out[3]);
+      *reinterpret_cast<float4*>(&s.T[row * LDS + cb + 4]) = make_float4(-out[4], -out[5], -out[6], -out[7]);
+      __syncwarp();
     }
-    __syncthreads();
-    for (int e = tid; e < npairs * 256; e += blockDim.x) {
-      const int J = e >> 8, I = J + d, r = (e >> 4) & 15, c = e & 15;
-      float acc = 0.f;
-      for (int m = 0; m <= r; ++m) acc += s.T[(16 * I + r) * LDS + 16 * I + m] * s.tmp[(J << 8) + m * 16 + c];
-      s.T[(16 * I + r) * LDS + 16 * J + c] = -acc;
-    }
-    __syncthreads();
   }
+  __syncthreads();
 }
 
 // Z_i += sum_{j<=i} M_ij Y_j * exp(gc_i - gc_j) for rows i of block I

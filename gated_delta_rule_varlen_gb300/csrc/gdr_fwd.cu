@@ -26,6 +26,15 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
   gram<VEC, true>(s, a.aqk + sq_off(chunk, h, a.HV));
   __syncthreads();
   invert(s);
+  // At and T for the backward: the values its gradient kernel needs, bit for bit.
+  if (a.amat) {
+    const size_t qo = sq_off(chunk, h, a.HV);
+    for (int e = threadIdx.x; e < CH * CH / 4; e += blockDim.x) {
+      const int i = e >> 4, j4 = (e & 15) * 4;
+      *reinterpret_cast<float4*>(&a.amat[qo + i * CH + j4]) = *reinterpret_cast<const float4*>(&s.At[i * LDS + j4]);
+      *reinterpret_cast<float4*>(&a.tmat[qo + i * CH + j4]) = *reinterpret_cast<const float4*>(&s.T[i * LDS + j4]);
+    }
+  }
   // Qp, Kd, gamma (elementwise; factors exp(gc) and exp(gc_last - gc) are <= 1).
   // Qp and Kd are only ever MMA operands: stored rounded to TF32.
   const size_t toff = tile_off(chunk, h, a.HV);
@@ -37,11 +46,14 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
     if (i == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d] = ex2(glast);
   }
   // Kd stored transposed, [c][j] (the K-major A operand of the walk's state update).
+  // A warp covers rows i = 8k .. 8k+7 of channels d .. d+3 (lane bits 0-2 -> i,
+  // 3-4 -> d): shared reads are conflict-free, each 8-lane group writes 32 bytes.
   for (int e = threadIdx.x; e < CH * DK; e += blockDim.x) {
-    const int d = e >> 6, i = e & 63;
+    const int l = e & 31, w = e >> 5;
+    const int i = (l & 7) + 8 * (w & 7), d = 4 * (w >> 3) + (l >> 3);
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
     const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
-    a.kd[toff + e] = __uint_as_float(tf32(s.k(i, d) * ex2(glast - gl)));
+    a.kd[toff + d * CH + i] = __uint_as_float(tf32(s.k(i, d) * ex2(glast - gl)));
   }
   __syncthreads();
   // Q tile <- v rows (async; used for u), G tile <- beta * K * Gamma (for w).

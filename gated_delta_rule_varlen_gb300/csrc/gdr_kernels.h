@@ -20,6 +20,7 @@ struct PrepArgs {
   const ChunkDesc* chunks;
   int Hqk, HV;
   float *w, *u, *qp, *kd, *aqk, *gam;
+  float *amat, *tmat;  // At and T per chunk ([64][64] FP32), or null when nothing is saved
 };
 
 struct WalkArgs {
@@ -81,6 +82,7 @@ struct GradArgs {
   float scale;
   const float *w, *u, *kd, *gam, *aqk, *delta, *ddelta;
   const float *dqs, *dw, *dkd, *dgam, *daqk;
+  const float *amat, *tmat;  // At and T of each chunk, saved by the forward
   // outputs
   __nv_bfloat16 *dq, *dk, *dv;   // dq/dk written directly when HV == Hqk
   float *dq_part, *dk_part;      // [NC][HV][64][128] per value head when HV > Hqk

@@ -79,7 +79,8 @@ const char* gdr_status_string(gdr_status status);
 
 /* Workspace sizes for a KDA problem (host-only; no CUDA calls).
  * saved_bytes: the forward's intermediates kept for the backward (chunk
- * tables, w, u, Q*Gamma, Kd, Delta, Aqk, gamma, and the per-chunk state tape).
+ * tables, w, u, Q*Gamma, Kd, Delta, Aqk, At, T, gamma, and the per-chunk state
+ * tape).
  * scratch_bytes: temporaries of the backward.  A forward called without a
  * `saved` buffer keeps its intermediates in `scratch`, which must then hold
  * saved_bytes.  Returns GDR_BAD_CU_SEQLENS or GDR_INVALID_ARG on bad input. */
