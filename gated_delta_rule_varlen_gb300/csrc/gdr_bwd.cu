@@ -335,6 +335,10 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   const size_t toff = tile_off(chunk, h, a.HV);
   const size_t qoff = sq_off(chunk, h, a.HV);
   if (tid < 2 * CH) (&sg.dbeta[0][0])[tid] = 0.f;
+  // gamma * dgamma of channel tid % 128 (per-channel gate), for the dg epilogue.
+  const float gdg = VEC ? __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))]) *
+                              __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))])
+                        : 0.f;
   // dw and dDelta (the B operands of X and Y) go into the dK / dG tiles, which
   // are free until X and Y are formed; dAqk into its own tile.
   for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
@@ -481,30 +485,29 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr)
       dqspre[nt][hr] = __ldg(reinterpret_cast<const float2*>(&a.dqs[toff + (i0 + g + 8 * hr) * DK + c0 + nt * 8 + 2 * t]));
-  // dKp' += beta [dA (x) decay] K
-  {
-    float Z[8][4];
-    zero_acc(Z);
-    left_apply<VEC, 8>(s, sDA, kf, Z, I, c0);
-    acc_foreach(Z, [&](int r, int col, float& x) {
-      const int i = i0 + r, c = c0 + col;
+  // dKp' += beta [dA (x) decay] K  and  dQ = dqs * Gamma + [dAqk (x) decay] K,
+  // one 32-channel half at a time.
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int cq = c0 + 32 * hh;
+    float Z0[4][4], Z1[4][4];
+    zero_acc(Z0);
+    zero_acc(Z1);
+    left_apply2<VEC, 4>(s, sDA, sg.dAqk, kf, Z0, Z1, I, cq);
+    acc_foreach(Z0, [&](int r, int col, float& x) {
+      const int i = i0 + r, c = cq + col;
       const float v = s.beta[i] * x;
       sg.dK[i * LDT + c] += v;
       sg.dG[i * LDT + c] += s.k(i, c) * v;
     });
-  }
-  // dQ = dqs * Gamma + [dAqk (x) decay] K
-  {
-    float Z[8][4];
-    zero_acc(Z);
-    left_apply<VEC, 8>(s, sg.dAqk, kf, Z, I, c0);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        const int i = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
-        const float dq0 = dqspre[nt][hr].x * ex2(gl(i, c)) + Z[nt][2 * hr];
-        const float dq1 = dqspre[nt][hr].y * ex2(gl(i, c + 1)) + Z[nt][2 * hr + 1];
+        const int i = i0 + g + 8 * hr, c = cq + nt * 8 + 2 * t;
+        const float2 dqs = dqspre[4 * hh + nt][hr];
+        const float dq0 = dqs.x * ex2(gl(i, c)) + Z1[nt][2 * hr];
+        const float dq1 = dqs.y * ex2(gl(i, c + 1)) + Z1[nt][2 * hr + 1];
         sg.dG[i * LDT + c] += s.q(i, c) * dq0;
         sg.dG[i * LDT + c + 1] += s.q(i, c + 1) * dq1;
         if (a.dq_part) {
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
     // Reverse cumsum over rows: threads 128..255 take rows 63..32, threads
     // 0..127 rows 31..0 starting from the sum of rows 32..63.
     const int c = tid & (DK - 1), half = tid >> 7;
-    float acc = gam[c] * dgam[c] + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
+    float acc = gdg + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
     if (half == 0) {
       float up[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll

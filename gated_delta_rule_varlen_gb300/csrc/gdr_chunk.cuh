@@ -357,6 +357,96 @@ __device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M,
   }
 }
 
+// Two left applies that share Y: Z0 += [M0 (x) decay] Y, Z1 += [M1 (x) decay] Y
+// over the rows of block I and channels c0 .. c0 + 8 NT - 1 (each gated Y
+// fragment is formed once and feeds both products).
+template <bool VEC, int NT, typename ET, class FY>
+__device__ void left_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M0, const float* __restrict__ M1, FY fy,
+                            float (&Z0)[NT][4], float (&Z1)[NT][4], int I, int c0) {
+  const int i0 = 16 * I;
+  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+  if (VEC) {
+    float acc0[NT][4], acc1[NT][4];
+    auto afrag = [&](const float* M, int j0, int j1, uint32_t (&a)[4]) {
+      a[0] = tf32(M[(i0 + g) * LDS + j0]);
+      a[1] = tf32(M[(i0 + g + 8) * LDS + j0]);
+      a[2] = tf32(M[(i0 + g) * LDS + j1]);
+      a[3] = tf32(M[(i0 + g + 8) * LDS + j1]);
+    };
+    if (I > 0) {
+      zero_acc(acc0);
+      zero_acc(acc1);
+      for (int kk = 0; kk < 2 * I; ++kk) {  // j in [0, 16I): reference gc at row 16I - 1
+        const int j0 = kk * 8 + t, j1 = j0 + 4;
+        uint32_t a0[4], a1[4];
+        afrag(M0, j0, j1, a0);
+        afrag(M1, j0, j1, a1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int c = c0 + nt * 8 + g;
+          const float bI = s.G[(i0 - 1) * LDT + c];
+          uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LDT + c]))};
+          mma8(acc0[nt], a0, b);
+          mma8(acc1[nt], a1, b);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int row = g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
+          const float e = ex2(s.G[(i0 + row) * LDT + c0 + col] - s.G[(i0 - 1) * LDT + c0 + col]);
+          Z0[nt][r] += acc0[nt][r] * e;
+          Z1[nt][r] += acc1[nt][r] * e;
+        }
+    }
+    zero_acc(acc0);
+    zero_acc(acc1);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {  // j in the diagonal block: reference gc at row 16I + 7
+      const int j0 = i0 + kk * 8 + t, j1 = j0 + 4;
+      uint32_t a0[4], a1[4];
+      afrag(M0, j0, j1, a0);
+      afrag(M1, j0, j1, a1);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = c0 + nt * 8 + g;
+        const float mI = s.G[(i0 + 7) * LDT + c];
+        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LDT + c]))};
+        mma8(acc0[nt], a0, b);
+        mma8(acc1[nt], a1, b);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
+        const float e = ex2(s.G[(i0 + row) * LDT + c0 + col] - s.G[(i0 + 7) * LDT + c0 + col]);
+        Z0[nt][r] += acc0[nt][r] * e;
+        Z1[nt][r] += acc1[nt][r] * e;
+      }
+  } else {
+    const int ra = i0 + g, rb = i0 + g + 8;
+    for (int kk = 0; kk < 2 * I + 2; ++kk) {
+      const int j0 = kk * 8 + t, j1 = j0 + 4;
+      auto dec = [&](int i, int j) { return j <= i ? ex2(s.gs[i] - s.gs[j]) : 0.f; };
+      const float d00 = dec(ra, j0), d10 = dec(rb, j0), d01 = dec(ra, j1), d11 = dec(rb, j1);
+      uint32_t a0[4] = {tf32(M0[ra * LDS + j0] * d00), tf32(M0[rb * LDS + j0] * d10), tf32(M0[ra * LDS + j1] * d01),
+                        tf32(M0[rb * LDS + j1] * d11)};
+      uint32_t a1[4] = {tf32(M1[ra * LDS + j0] * d00), tf32(M1[rb * LDS + j0] * d10), tf32(M1[ra * LDS + j1] * d01),
+                        tf32(M1[rb * LDS + j1] * d11)};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = c0 + nt * 8 + g;
+        uint32_t b[2] = {tf32(fy(j0, c)), tf32(fy(j1, c))};
+        mma8(Z0[nt], a0, b);
+        mma8(Z1[nt], a1, b);
+      }
+    }
+  }
+}
+
 // Z_j += sum_{i>=j} (M0_ij Y0_i + beta_i M1_ij Y1_i) * exp(gc_i - gc_j) for rows
 // j of block J and channels c0 .. c0 + 8 NT - 1.  M0, M1 masked [64][64]
 // shared tiles; f0(i, c), f1(i, c) return Y0_ic, Y1_ic.
