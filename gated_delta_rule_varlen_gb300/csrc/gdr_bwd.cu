@@ -309,23 +309,25 @@ __global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
 // "fused gradient" / "gate epilogue" stages named on PR #8218.
 // ---------------------------------------------------------------------------
 struct GradSmem {
-  ChunkSmemB c;
+  ChunkSmemBB c;
   float dAqk[CH * LDS];
-  float dK[CH * LDT];
-  float dG[CH * LDT];
-  float dbeta[2][CH];
+  float dK[CH * LDF];  // staging: dw, then w; finally unused
+  float dG[CH * LDF];  // staging: dDelta, then u; finally the gate adjoint dgc
+  float dbeta[3][CH];  // per channel half (X.Kp + Y.V), and sum_j dA_ij At_ij
   float col[4 * DK];
   float rowsum[CH];
 };
 
 // 8 warps: warp w owns rows 16 (w % 4) .. +15 and channels 64 (w / 4) .. +63
-// of every per-row result.  The one product that contracts over channels (dA)
-// is summed over the two channel halves in two ordered passes.
+// of every per-row result, held in registers in the m16n8 accumulator layout
+// (thread: rows i0 + g and i0 + g + 8, channel pairs c0 + 8 nt + 2 t).  The one
+// product that contracts over channels (dA) is summed over the two channel
+// halves in two ordered passes.
 template <bool VEC, typename BetaT>
-__global__ void __launch_bounds__(256) k_grad(GradArgs a) {
+__global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   GradSmem& sg = *reinterpret_cast<GradSmem*>(smem_raw);
-  ChunkSmemB& s = sg.c;
+  ChunkSmemBB& s = sg.c;
   const int chunk = blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
@@ -334,19 +336,17 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
   const size_t qoff = sq_off(chunk, h, a.HV);
-  if (tid < 2 * CH) (&sg.dbeta[0][0])[tid] = 0.f;
   // gamma * dgamma of channel tid % 128 (per-channel gate), for the dg epilogue.
   const float gdg = VEC ? __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))]) *
                               __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))])
                         : 0.f;
-  // dw and dDelta (the B operands of X and Y) go into the dK / dG tiles, which
-  // are free until X and Y are formed; dAqk into its own tile.
+  // dw and dDelta (the B operands of X and Y) into the staging tiles; dAqk,
+  // and the forward's At and T of this chunk.
   for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
     const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&sg.dK[i * LDT + c4], &a.dw[toff + i * DK + c4]);
-    cp_async16(&sg.dG[i * LDT + c4], &a.ddelta[toff + i * DK + c4]);
+    cp_async16(&sg.dK[i * LDF + c4], &a.dw[toff + i * DK + c4]);
+    cp_async16(&sg.dG[i * LDF + c4], &a.ddelta[toff + i * DK + c4]);
   }
-  // dAqk, and the forward's At and T of this chunk.
   for (int e = tid; e < CH * CH / 4; e += blockDim.x) {
     const int i = e >> 4, c4 = (e & 15) * 4;
     cp_async16(&sg.dAqk[i * LDS + c4], &a.daqk[qoff + i * CH + c4]);
@@ -356,10 +356,11 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   cp_async_commit();
   load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
                          a.HV);
-  auto gl = [&](int i, int c) -> float { return VEC ? s.G[i * LDT + c] : s.gs[i]; };
+  // Gate of (i, c) and (i, c + 1).
+  auto gl2 = [&](int i, int c) -> float2 { return VEC ? s.g2(i, c) : make_float2(s.gs[i], s.gs[i]); };
 
-  // v of this thread's accumulator positions (rows i0+g, i0+g+8; channel pairs),
-  // fetched now so that its latency hides behind X, Y and dA.
+  // v of this thread's accumulator positions, fetched now so that its latency
+  // hides behind X, Y and dA.
   __nv_bfloat162 vpre[8][2];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt)
@@ -384,19 +385,19 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int c = c0 + nt * 8 + g;
-        uint32_t bx[2] = {tf32(dw[ja * LDT + c]), tf32(dw[jb * LDT + c])};
-        uint32_t by[2] = {tf32(dd[ja * LDT + c]), tf32(dd[jb * LDT + c])};
+        uint32_t bx[2] = {tf32(dw[ja * LDF + c]), tf32(dw[jb * LDF + c])};
+        uint32_t by[2] = {tf32(dd[ja * LDF + c]), tf32(dd[jb * LDF + c])};
         mma8(X[nt], av, bx);
         mma8(Y[nt], av, by);
       }
     }
   }
   __syncthreads();
-  // w and u (B operands of dA) into the dK / dG tiles.
+  // w and u (B operands of dA) into the staging tiles.
   for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
     const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&sg.dK[i * LDT + c4], &a.w[toff + i * DK + c4]);
-    cp_async16(&sg.dG[i * LDT + c4], &a.u[toff + i * DK + c4]);
+    cp_async16(&sg.dK[i * LDF + c4], &a.w[toff + i * DK + c4]);
+    cp_async16(&sg.dG[i * LDF + c4], &a.u[toff + i * DK + c4]);
   }
   cp_async_commit();
   // Partial dA over this warp's channel half: X w^T + Y u^T.
@@ -416,8 +417,8 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
       for (int nt = 0; nt < 8; ++nt) {
         if (nt < 2 * I + 2) {
           const int j = nt * 8 + g;
-          const float2 wv = *reinterpret_cast<const float2*>(&w[j * LDT + cc]);
-          const float2 uv = *reinterpret_cast<const float2*>(&u[j * LDT + cc]);
+          const float2 wv = *reinterpret_cast<const float2*>(&w[j * LDF + cc]);
+          const float2 uv = *reinterpret_cast<const float2*>(&u[j * LDF + cc]);
           uint32_t bw[2] = {__float_as_uint(wv.x), __float_as_uint(wv.y)};
           uint32_t bu[2] = {__float_as_uint(uv.x), __float_as_uint(uv.y)};
           mma8(dAacc[nt], ax, bw);
@@ -427,15 +428,33 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
     }
   }
   // dA = -strict_tril(sum of the two halves) into s.T (T is no longer read).
+  // The second pass also forms sum_j dA_ij At_ij of its rows (part of dbeta).
   float* sDA = s.T;
   if (hc == 0)
     acc_foreach(dAacc, [&](int r, int col, float& x) { sDA[(i0 + r) * LDS + col] = col < i0 + r ? -x : 0.f; });
   __syncthreads();
-  if (hc == 1)
+  if (hc == 1) {
+    float p0 = 0.f, p1 = 0.f;
     acc_foreach(dAacc, [&](int r, int col, float& x) {
-      if (col < i0 + r) sDA[(i0 + r) * LDS + col] -= x;
+      const int i = i0 + r;
+      if (col < i) {
+        const float d = sDA[i * LDS + col] - x;
+        sDA[i * LDS + col] = d;
+        if (r < 8) p0 += d * s.At[i * LDS + col]; else p1 += d * s.At[i * LDS + col];
+      }
     });
-  // Row-local (this warp's rows and channel half): dV, dbeta (X.Kp + Y.V), dKp' from X.
+    p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+    p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+    p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+    p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+    if (t == 0) {
+      sg.dbeta[2][i0 + g] = p0;
+      sg.dbeta[2][i0 + g + 8] = p1;
+    }
+  }
+  // dK, dG: this warp's rows and channel half, accumulator layout.
+  float dKr[8][4], dGr[8][4];
+  // Row-local: dV, dbeta (X.Kp + Y.V), dKp' = beta X Gamma.
   {
     float db0 = 0.f, db1 = 0.f;
 #pragma unroll
@@ -444,21 +463,20 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
       for (int hr = 0; hr < 2; ++hr) {
         const int i = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
         const float2 vv = __bfloat1622float2(vpre[nt][hr]);
-        float part = 0.f;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float x = X[nt][2 * hr + q], y = Y[nt][2 * hr + q];
-          const float e = ex2(gl(i, c + q));
-          const float kv = s.k(i, c + q);
-          part += x * kv * e + y * (q ? vv.y : vv.x);
-          const float dkp = s.beta[i] * x * e;
-          sg.dK[i * LDT + c + q] = dkp;
-          sg.dG[i * LDT + c + q] = kv * dkp;
-        }
+        const float2 kv = s.k2(i, c), gv = gl2(i, c);
+        const float bi = s.beta[i];
+        const float x0 = X[nt][2 * hr], x1 = X[nt][2 * hr + 1];
+        const float e0 = ex2(gv.x), e1 = ex2(gv.y);
+        const float part = (x0 * kv.x * e0 + Y[nt][2 * hr] * vv.x) + (x1 * kv.y * e1 + Y[nt][2 * hr + 1] * vv.y);
         if (hr == 0) db0 += part; else db1 += part;
+        const float dkp0 = bi * x0 * e0, dkp1 = bi * x1 * e1;
+        dKr[nt][2 * hr] = dkp0;
+        dKr[nt][2 * hr + 1] = dkp1;
+        dGr[nt][2 * hr] = kv.x * dkp0;
+        dGr[nt][2 * hr + 1] = kv.y * dkp1;
         if (i < cd.len)
           *reinterpret_cast<__nv_bfloat162*>(&a.dv[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c]) =
-              __floats2bfloat162_rn(s.beta[i] * Y[nt][2 * hr], s.beta[i] * Y[nt][2 * hr + 1]);
+              __floats2bfloat162_rn(bi * Y[nt][2 * hr], bi * Y[nt][2 * hr + 1]);
       }
     }
     db0 += __shfl_xor_sync(0xffffffffu, db0, 1);
@@ -466,19 +484,14 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
     db1 += __shfl_xor_sync(0xffffffffu, db1, 1);
     db1 += __shfl_xor_sync(0xffffffffu, db1, 2);
     if (t == 0) {
-      sg.dbeta[hc][i0 + g] += db0;
-      sg.dbeta[hc][i0 + g + 8] += db1;
+      sg.dbeta[hc][i0 + g] = db0;
+      sg.dbeta[hc][i0 + g + 8] = db1;
     }
   }
-  __syncthreads();
-  if (tid < CH) {
-    float acc = 0.f;
-    for (int j = 0; j < tid; ++j) acc += sDA[tid * LDS + j] * s.At[tid * LDS + j];
-    sg.dbeta[0][tid] += acc;
-  }
+  __syncthreads();  // dA complete
   auto kf = [&](int j, int c) { return s.k(j, c); };
   auto qf = [&](int j, int c) { return s.q(j, c); };
-  // dqs at this thread's accumulator positions, fetched ahead of the two applies.
+  // dqs at this thread's accumulator positions, fetched ahead of the applies.
   float2 dqspre[8][2];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt)
@@ -494,22 +507,23 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
     zero_acc(Z0);
     zero_acc(Z1);
     left_apply2<VEC, 4>(s, sDA, sg.dAqk, kf, Z0, Z1, I, cq);
-    acc_foreach(Z0, [&](int r, int col, float& x) {
-      const int i = i0 + r, c = cq + col;
-      const float v = s.beta[i] * x;
-      sg.dK[i * LDT + c] += v;
-      sg.dG[i * LDT + c] += s.k(i, c) * v;
-    });
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        const int i = i0 + g + 8 * hr, c = cq + nt * 8 + 2 * t;
-        const float2 dqs = dqspre[4 * hh + nt][hr];
-        const float dq0 = dqs.x * ex2(gl(i, c)) + Z1[nt][2 * hr];
-        const float dq1 = dqs.y * ex2(gl(i, c + 1)) + Z1[nt][2 * hr + 1];
-        sg.dG[i * LDT + c] += s.q(i, c) * dq0;
-        sg.dG[i * LDT + c + 1] += s.q(i, c + 1) * dq1;
+        const int i = i0 + g + 8 * hr, c = cq + nt * 8 + 2 * t, n = 4 * hh + nt;
+        const float bi = s.beta[i];
+        const float2 kv = s.k2(i, c), qv = s.q2(i, c), gv = gl2(i, c);
+        const float v0 = bi * Z0[nt][2 * hr], v1 = bi * Z0[nt][2 * hr + 1];
+        dKr[n][2 * hr] += v0;
+        dKr[n][2 * hr + 1] += v1;
+        dGr[n][2 * hr] += kv.x * v0;
+        dGr[n][2 * hr + 1] += kv.y * v1;
+        const float2 dqs = dqspre[n][hr];
+        const float dq0 = dqs.x * ex2(gv.x) + Z1[nt][2 * hr];
+        const float dq1 = dqs.y * ex2(gv.y) + Z1[nt][2 * hr + 1];
+        dGr[n][2 * hr] += qv.x * dq0;
+        dGr[n][2 * hr + 1] += qv.y * dq1;
         if (a.dq_part) {
           *reinterpret_cast<float2*>(&a.dq_part[toff + i * DK + c]) = make_float2(dq0, dq1);
         } else if (i < cd.len) {
@@ -518,55 +532,74 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
         }
       }
   }
-  // dKd of this warp's rows and channel pairs, fetched ahead of the last apply.
-  float2 dkdpre[16];
+  // dKd at this thread's accumulator positions, fetched ahead of the last apply.
+  float2 dkdpre[8][2];
 #pragma unroll
-  for (int rr = 0; rr < 16; ++rr)
-    dkdpre[rr] = __ldg(reinterpret_cast<const float2*>(&a.dkd[toff + (i0 + rr) * DK + c0 + lane * 2]));
-  // dKn' = [dAqk (x) decay]^T Q + [beta dA (x) decay]^T K
-  {
-    float Z[8][4];
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr)
+      dkdpre[nt][hr] = __ldg(reinterpret_cast<const float2*>(&a.dkd[toff + (i0 + g + 8 * hr) * DK + c0 + nt * 8 + 2 * t]));
+  // dKn' = [dAqk (x) decay]^T Q + [beta dA (x) decay]^T K, one 32-channel half at a time.
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int cq = c0 + 32 * hh;
+    float Z[4][4];
     zero_acc(Z);
-    right_apply2<VEC, 8>(s, sg.dAqk, qf, sDA, kf, Z, I, c0);
-    acc_foreach(Z, [&](int r, int col, float& x) {
-      const int i = i0 + r, c = c0 + col;
-      sg.dK[i * LDT + c] += x;
-      sg.dG[i * LDT + c] -= s.k(i, c) * x;
-    });
+    right_apply2<VEC, 4>(s, sg.dAqk, qf, sDA, kf, Z, I, cq);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = i0 + g + 8 * hr, c = cq + nt * 8 + 2 * t, n = 4 * hh + nt;
+        const float2 kv = s.k2(i, c);
+        dKr[n][2 * hr] += Z[nt][2 * hr];
+        dKr[n][2 * hr + 1] += Z[nt][2 * hr + 1];
+        dGr[n][2 * hr] -= kv.x * Z[nt][2 * hr];
+        dGr[n][2 * hr + 1] -= kv.y * Z[nt][2 * hr + 1];
+      }
   }
-  // dKd terms (own rows and channels), column sums of Kd*dKd, then dk.
+  // dKd terms, dk, and the column sums of Kd*dKd over this warp's rows.
   {
-    float csum[2] = {0.f, 0.f};
-    const int cp = c0 + lane * 2;
-    const float gl0 = VEC ? s.G[(CH - 1) * LDT + cp] : s.gs[CH - 1];
-    const float gl1 = VEC ? s.G[(CH - 1) * LDT + cp + 1] : s.gs[CH - 1];
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      const int i = i0 + rr;
-      float dk[2];
+    for (int nt = 0; nt < 8; ++nt) {
+      const int c = c0 + nt * 8 + 2 * t;
+      const float2 glast = gl2(CH - 1, c);
+      float cs0 = 0.f, cs1 = 0.f;
 #pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        const int c = cp + q2;
-        const float x = q2 ? dkdpre[rr].y : dkdpre[rr].x;
-        const float ed = ex2((q2 ? gl1 : gl0) - gl(i, c));
-        const float kdv = s.k(i, c) * ed;  // Kd = K * exp(gc_last - gc)
-        dk[q2] = sg.dK[i * LDT + c] + x * ed;
-        sg.dG[i * LDT + c] -= kdv * x;
-        csum[q2] += kdv * x;
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = i0 + g + 8 * hr;
+        const float2 kv = s.k2(i, c), gv = gl2(i, c), x = dkdpre[nt][hr];
+        const float ed0 = ex2(glast.x - gv.x), ed1 = ex2(glast.y - gv.y);
+        const float kd0 = kv.x * ed0, kd1 = kv.y * ed1;  // Kd = K * exp(gc_last - gc)
+        const float dk0 = dKr[nt][2 * hr] + x.x * ed0, dk1 = dKr[nt][2 * hr + 1] + x.y * ed1;
+        dGr[nt][2 * hr] -= kd0 * x.x;
+        dGr[nt][2 * hr + 1] -= kd1 * x.y;
+        cs0 += kd0 * x.x;
+        cs1 += kd1 * x.y;
+        if (a.dk_part) {
+          *reinterpret_cast<float2*>(&a.dk_part[toff + i * DK + c]) = make_float2(dk0, dk1);
+        } else if (i < cd.len) {
+          *reinterpret_cast<__nv_bfloat162*>(&a.dk[((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + c]) =
+              __floats2bfloat162_rn(dk0, dk1);
+        }
       }
-      if (a.dk_part) {
-        *reinterpret_cast<float2*>(&a.dk_part[toff + i * DK + cp]) = make_float2(dk[0], dk[1]);
-      } else if (i < cd.len) {
-        *reinterpret_cast<__nv_bfloat162*>(&a.dk[((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + cp]) =
-            __floats2bfloat162_rn(dk[0], dk[1]);
+#pragma unroll
+      for (int m = 4; m < 32; m <<= 1) {
+        cs0 += __shfl_xor_sync(0xffffffffu, cs0, m);
+        cs1 += __shfl_xor_sync(0xffffffffu, cs1, m);
       }
+      if (g == 0) *reinterpret_cast<float2*>(&sg.col[I * DK + c]) = make_float2(cs0, cs1);
     }
-#pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) sg.col[I * DK + c0 + lane * 2 + q2] = csum[q2];
   }
+  // The gate adjoint dgc of this warp's positions into the (free) staging tile.
+  float* dG = sg.dG;
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr)
+      *reinterpret_cast<float2*>(&dG[(i0 + g + 8 * hr) * LDF + c0 + nt * 8 + 2 * t]) =
+          make_float2(dGr[nt][2 * hr], dGr[nt][2 * hr + 1]);
   __syncthreads();
-  const float* gam = a.gam + ((size_t)chunk * a.HV + h) * DK;
-  const float* dgam = a.dgam + ((size_t)chunk * a.HV + h) * DK;
   if (VEC) {
     // Reverse cumsum over rows: threads 128..255 take rows 63..32, threads
     // 0..127 rows 31..0 starting from the sum of rows 32..63.
@@ -575,23 +608,25 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
     if (half == 0) {
       float up[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = CH / 2; i < CH; ++i) up[i & 3] += sg.dG[i * LDT + c];
+      for (int i = CH / 2; i < CH; ++i) up[i & 3] += dG[i * LDF + c];
       acc += (up[0] + up[1]) + (up[2] + up[3]);
     }
     const int hi = half ? CH - 1 : CH / 2 - 1;
 #pragma unroll 8
     for (int i = hi; i > hi - CH / 2; --i) {
-      acc += sg.dG[i * LDT + c];
+      acc += dG[i * LDF + c];
       if (i < cd.len) a.dg[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c] = acc;
     }
   } else {
     if (tid < CH) {
       float acc = 0.f;
-      for (int c = 0; c < DK; ++c) acc += sg.dG[tid * LDT + c];
+      for (int c = 0; c < DK; ++c) acc += dG[tid * LDF + c];
       sg.rowsum[tid] = acc;
     }
     __syncthreads();
     if (tid == 0) {
+      const float* gam = a.gam + ((size_t)chunk * a.HV + h) * DK;
+      const float* dgam = a.dgam + ((size_t)chunk * a.HV + h) * DK;
       float extra = 0.f;
       for (int c = 0; c < DK; ++c)
         extra += gam[c] * dgam[c] + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
@@ -604,7 +639,7 @@ __global__ void __launch_bounds__(256) k_grad(GradArgs a) {
   }
   if (tid < cd.len)
     reinterpret_cast<BetaT*>(a.dbeta)[(size_t)(cd.tok0 + tid) * a.HV + h] =
-        from_f<BetaT>(sg.dbeta[0][tid] + sg.dbeta[1][tid]);
+        from_f<BetaT>((sg.dbeta[0][tid] + sg.dbeta[2][tid]) + sg.dbeta[1][tid]);
 }
 
 // dq / dk of a Q/K head = FP32 sum over its value heads, rounded once.

@@ -10,12 +10,17 @@ namespace gdr {
 
 // Shared-memory tiles of one chunk.  K and Q are kept either as FP32 (ET =
 // float) or as their exact BF16 input bits (ET = uint16_t, half the space).
-template <typename ET>
+// LG_ is the row stride of the gate tile: 132 (= 4 mod 32) suits fragment
+// reads with the row on the group index (A operands of K K^T), 136 (= 8 mod 32)
+// fragment reads with the row on the thread-in-group index (B operands of the
+// applies) and float2 reads of accumulator positions.
+template <typename ET, int LG_ = LDT>
 struct ChunkSmemT {
   static constexpr int LD = sizeof(ET) == 4 ? LDT : DK + 8;  // row stride (elements) of K and Q
+  static constexpr int LG = LG_;
   ET K[CH * LD];      // k (rows >= len are zero)
   ET Q[CH * LD];      // q
-  float G[CH * LDT];  // per-channel gate: chunk-local cumsum of g, times log2(e)
+  float G[CH * LG];   // per-channel gate: chunk-local cumsum of g, times log2(e)
   float gs[CH];       // scalar gate: chunk-local cumsum of g, times log2(e)
   float beta[CH];
   float At[CH * LDS];  // strict_tril of the gated Gram K K^T (without beta)
@@ -23,18 +28,29 @@ struct ChunkSmemT {
   float tmp[3 * 256];
   __device__ __forceinline__ float k(int i, int c) const { return elem(K[i * LD + c]); }
   __device__ __forceinline__ float q(int i, int c) const { return elem(Q[i * LD + c]); }
+  // Elements (i, c) and (i, c + 1), c even.
+  __device__ __forceinline__ float2 k2(int i, int c) const { return pair(&K[i * LD + c]); }
+  __device__ __forceinline__ float2 q2(int i, int c) const { return pair(&Q[i * LD + c]); }
+  __device__ __forceinline__ float2 g2(int i, int c) const { return *reinterpret_cast<const float2*>(&G[i * LG + c]); }
+  static __device__ __forceinline__ float2 pair(const float* p) { return *reinterpret_cast<const float2*>(p); }
+  static __device__ __forceinline__ float2 pair(const uint16_t* p) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
   static __device__ __forceinline__ float elem(float x) { return x; }
   static __device__ __forceinline__ float elem(uint16_t x) { return bfbits2f(x); }
 };
 using ChunkSmem = ChunkSmemT<float>;
 using ChunkSmemB = ChunkSmemT<uint16_t>;
+constexpr int LDF = 136;  // FP32 [64][128] tile stride for B-operand-style reads
+using ChunkSmemBB = ChunkSmemT<uint16_t, LDF>;
 
 // Loads k, q (of Q/K head hq), the gate (cumsum, base-2 scaled) and beta of
 // value head h for the chunk rows [tok0, tok0+len).  Rows >= len are zero
 // (zero gate rows keep the cumsum flat, so gc at row 63 equals gc at the
 // chunk's last token).
-template <bool VEC, typename BetaT, typename ET>
-__device__ void load_chunk(ChunkSmemT<ET>& s, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+template <bool VEC, typename BetaT, typename ET, int LG>
+__device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                            const float* __restrict__ g, const BetaT* __restrict__ beta, int tok0, int len, int hq,
                            int h, int Hqk, int HV) {
   constexpr int LD = ChunkSmemT<ET>::LD;
@@ -56,9 +72,9 @@ __device__ void load_chunk(ChunkSmemT<ET>& s, const __nv_bfloat16* __restrict__ 
       for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
         const int i = e >> 5, d4 = (e & 31) * 4;
         if (i < len)
-          cp_async16(&s.G[i * LDT + d4], g + ((size_t)(tok0 + i) * HV + h) * DK + d4);
+          cp_async16(&s.G[i * LG + d4], g + ((size_t)(tok0 + i) * HV + h) * DK + d4);
         else
-          *reinterpret_cast<float4*>(&s.G[i * LDT + d4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(&s.G[i * LG + d4]) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     cp_async_commit();
@@ -76,7 +92,7 @@ __device__ void load_chunk(ChunkSmemT<ET>& s, const __nv_bfloat16* __restrict__ 
       if (VEC) {
         float2 gv = make_float2(0.f, 0.f);
         if (i < len) gv = *reinterpret_cast<const float2*>(g + ((size_t)(tok0 + i) * HV + h) * DK + d);
-        *reinterpret_cast<float2*>(&s.G[i * LDT + d]) = gv;
+        *reinterpret_cast<float2*>(&s.G[i * LG + d]) = gv;
       }
     }
   }
@@ -92,8 +108,8 @@ __device__ void load_chunk(ChunkSmemT<ET>& s, const __nv_bfloat16* __restrict__ 
       float acc = 0.f;
 #pragma unroll 8
       for (int i = 0; i < CH; ++i) {
-        acc += s.G[i * LDT + tid] * LOG2E;
-        s.G[i * LDT + tid] = acc;
+        acc += s.G[i * LG + tid] * LOG2E;
+        s.G[i * LG + tid] = acc;
       }
     }
   } else if (tid == 0) {
@@ -111,8 +127,8 @@ __device__ void load_chunk(ChunkSmemT<ET>& s, const __nv_bfloat16* __restrict__ 
 //   Aqk[i][j] = sum_c Q_ic K_jc exp(gc_ic - gc_jc)   for j <= i (else 0)  -> aqk (global, [64][64])
 // Per-channel gates use the block factorization described in gdr_common.cuh.
 // Aqk is stored rounded to TF32 (it is only ever an MMA operand).
-template <bool VEC, bool WITH_QK, typename ET>
-__device__ void gram(ChunkSmemT<ET>& s, float* __restrict__ aqk) {
+template <bool VEC, bool WITH_QK, typename ET, int LG>
+__device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
   const int I = threadIdx.x >> 5, i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const int ra = i0 + g, rb = i0 + g + 8;
@@ -129,10 +145,10 @@ __device__ void gram(ChunkSmemT<ET>& s, float* __restrict__ aqk) {
       const int c0 = kk * 8 + t, c1 = c0 + 4;
       const float ka0 = s.k(ra, c0), kb0 = s.k(rb, c0), ka1 = s.k(ra, c1), kb1 = s.k(rb, c1);
       const float qa0 = s.q(ra, c0), qb0 = s.q(rb, c0), qa1 = s.q(ra, c1), qb1 = s.q(rb, c1);
-      const float ga0 = G[ra * LDT + c0], gb0 = G[rb * LDT + c0], ga1 = G[ra * LDT + c1], gb1 = G[rb * LDT + c1];
+      const float ga0 = G[ra * LG + c0], gb0 = G[rb * LG + c0], ga1 = G[ra * LG + c1], gb1 = G[rb * LG + c1];
       // Off-diagonal blocks: reference = gc at the end of block I-1.
       if (I > 0) {
-        const float b0 = G[(i0 - 1) * LDT + c0], b1 = G[(i0 - 1) * LDT + c1];
+        const float b0 = G[(i0 - 1) * LG + c0], b1 = G[(i0 - 1) * LG + c1];
         const float e00 = ex2(ga0 - b0), e10 = ex2(gb0 - b0), e01 = ex2(ga1 - b1), e11 = ex2(gb1 - b1);
         uint32_t aK[4] = {tf32(ka0 * e00), tf32(kb0 * e10), tf32(ka1 * e01), tf32(kb1 * e11)};
         uint32_t aQ[4] = {tf32(qa0 * e00), tf32(qb0 * e10), tf32(qa1 * e01), tf32(qb1 * e11)};
@@ -140,7 +156,7 @@ __device__ void gram(ChunkSmemT<ET>& s, float* __restrict__ aqk) {
         for (int nt = 0; nt < 6; ++nt) {
           if (nt < 2 * I) {
             const int j = nt * 8 + g;
-            uint32_t b[2] = {tf32(s.k(j, c0) * ex2(b0 - G[j * LDT + c0])), tf32(s.k(j, c1) * ex2(b1 - G[j * LDT + c1]))};
+            uint32_t b[2] = {tf32(s.k(j, c0) * ex2(b0 - G[j * LG + c0])), tf32(s.k(j, c1) * ex2(b1 - G[j * LG + c1]))};
             mma8(accK[nt], aK, b);
             if (WITH_QK) mma8(accQ[nt], aQ, b);
           }
@@ -148,14 +164,14 @@ __device__ void gram(ChunkSmemT<ET>& s, float* __restrict__ aqk) {
       }
       // Diagonal block: reference = gc at row i0 + 7.
       {
-        const float m0 = G[(i0 + 7) * LDT + c0], m1 = G[(i0 + 7) * LDT + c1];
+        const float m0 = G[(i0 + 7) * LG + c0], m1 = G[(i0 + 7) * LG + c1];
         const float e00 = ex2(ga0 - m0), e10 = ex2(gb0 - m0), e01 = ex2(ga1 - m1), e11 = ex2(gb1 - m1);
         uint32_t aK[4] = {tf32(ka0 * e00), tf32(kb0 * e10), tf32(ka1 * e01), tf32(kb1 * e11)};
         uint32_t aQ[4] = {tf32(qa0 * e00), tf32(qb0 * e10), tf32(qa1 * e01), tf32(qb1 * e11)};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int j = i0 + nt * 8 + g;
-          uint32_t b[2] = {tf32(s.k(j, c0) * ex2(m0 - G[j * LDT + c0])), tf32(s.k(j, c1) * ex2(m1 - G[j * LDT + c1]))};
+          uint32_t b[2] = {tf32(s.k(j, c0) * ex2(m0 - G[j * LG + c0])), tf32(s.k(j, c1) * ex2(m1 - G[j * LG + c1]))};
           mma8(dK[nt], aK, b);
           if (WITH_QK) mma8(dQ[nt], aQ, b);
         }
@@ -222,8 +238,8 @@ __device__ void gram(ChunkSmemT<ET>& s, float* __restrict__ aqk) {
 //   T_IJ = -T_II * diag(beta_I) * sum_{K=J}^{I-1} At_IK T_KJ,
 // which needs only blocks of column J that the same warp made before, so the
 // off-diagonal part synchronizes within the warp only.  Needs >= 4 warps.
-template <typename ET>
-__device__ void invert(ChunkSmemT<ET>& s) {
+template <typename ET, int LG>
+__device__ void invert(ChunkSmemT<ET, LG>& s) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   if (warp < 4 && lane < 16) {
     const int i0 = warp * 16, j = lane;
@@ -298,8 +314,8 @@ __device__ void invert(ChunkSmemT<ET>& s) {
 // Z_i += sum_{j<=i} M_ij Y_j * exp(gc_i - gc_j) for rows i of block I
 // (16I .. 16I+15) and channels c0 .. c0 + 8 NT - 1.  M is a masked [64][64]
 // shared tile (stride LDS); fy(j, c) returns Y_jc.
-template <bool VEC, int NT, typename ET, class FY>
-__device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M, FY fy, float (&Z)[NT][4], int I,
+template <bool VEC, int NT, typename ET, int LG, class FY>
+__device__ void left_apply(const ChunkSmemT<ET, LG>& s, const float* __restrict__ M, FY fy, float (&Z)[NT][4], int I,
                            int c0) {
   const int i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
@@ -314,14 +330,14 @@ __device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M,
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int c = c0 + nt * 8 + g;
-          const float bI = s.G[(i0 - 1) * LDT + c];
-          uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LDT + c]))};
+          const float bI = s.G[(i0 - 1) * LG + c];
+          uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LG + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LG + c]))};
           mma8(acc[nt], a, b);
         }
       }
       acc_foreach(acc, [&](int r, int col, float& x) {
         Z[col >> 3][(r >> 3) * 2 + (col & 1)] +=
-            x * ex2(s.G[(i0 + r) * LDT + c0 + col] - s.G[(i0 - 1) * LDT + c0 + col]);
+            x * ex2(s.G[(i0 + r) * LG + c0 + col] - s.G[(i0 - 1) * LG + c0 + col]);
       });
     }
     zero_acc(acc);
@@ -333,13 +349,13 @@ __device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M,
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
-        const float mI = s.G[(i0 + 7) * LDT + c];
-        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LDT + c]))};
+        const float mI = s.G[(i0 + 7) * LG + c];
+        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LG + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LG + c]))};
         mma8(acc[nt], a, b);
       }
     }
     acc_foreach(acc, [&](int r, int col, float& x) {
-      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[(i0 + r) * LDT + c0 + col] - s.G[(i0 + 7) * LDT + c0 + col]);
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[(i0 + r) * LG + c0 + col] - s.G[(i0 + 7) * LG + c0 + col]);
     });
   } else {
     for (int kk = 0; kk < 2 * I + 2; ++kk) {
@@ -360,8 +376,8 @@ __device__ void left_apply(const ChunkSmemT<ET>& s, const float* __restrict__ M,
 // Two left applies that share Y: Z0 += [M0 (x) decay] Y, Z1 += [M1 (x) decay] Y
 // over the rows of block I and channels c0 .. c0 + 8 NT - 1 (each gated Y
 // fragment is formed once and feeds both products).
-template <bool VEC, int NT, typename ET, class FY>
-__device__ void left_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M0, const float* __restrict__ M1, FY fy,
+template <bool VEC, int NT, typename ET, int LG, class FY>
+__device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict__ M0, const float* __restrict__ M1, FY fy,
                             float (&Z0)[NT][4], float (&Z1)[NT][4], int I, int c0) {
   const int i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
@@ -384,8 +400,8 @@ __device__ void left_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int c = c0 + nt * 8 + g;
-          const float bI = s.G[(i0 - 1) * LDT + c];
-          uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LDT + c]))};
+          const float bI = s.G[(i0 - 1) * LG + c];
+          uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LG + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LG + c]))};
           mma8(acc0[nt], a0, b);
           mma8(acc1[nt], a1, b);
         }
@@ -395,7 +411,7 @@ __device__ void left_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int row = g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
-          const float e = ex2(s.G[(i0 + row) * LDT + c0 + col] - s.G[(i0 - 1) * LDT + c0 + col]);
+          const float e = ex2(s.G[(i0 + row) * LG + c0 + col] - s.G[(i0 - 1) * LG + c0 + col]);
           Z0[nt][r] += acc0[nt][r] * e;
           Z1[nt][r] += acc1[nt][r] * e;
         }
@@ -411,8 +427,8 @@ __device__ void left_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
-        const float mI = s.G[(i0 + 7) * LDT + c];
-        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LDT + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LDT + c]))};
+        const float mI = s.G[(i0 + 7) * LG + c];
+        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LG + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LG + c]))};
         mma8(acc0[nt], a0, b);
         mma8(acc1[nt], a1, b);
       }
@@ -422,7 +438,7 @@ __device__ void left_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int row = g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
-        const float e = ex2(s.G[(i0 + row) * LDT + c0 + col] - s.G[(i0 + 7) * LDT + c0 + col]);
+        const float e = ex2(s.G[(i0 + row) * LG + c0 + col] - s.G[(i0 + 7) * LG + c0 + col]);
         Z0[nt][r] += acc0[nt][r] * e;
         Z1[nt][r] += acc1[nt][r] * e;
       }
@@ -450,8 +466,8 @@ __device__ void left_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M
 // Z_j += sum_{i>=j} (M0_ij Y0_i + beta_i M1_ij Y1_i) * exp(gc_i - gc_j) for rows
 // j of block J and channels c0 .. c0 + 8 NT - 1.  M0, M1 masked [64][64]
 // shared tiles; f0(i, c), f1(i, c) return Y0_ic, Y1_ic.
-template <bool VEC, int NT, typename ET, class F0, class F1>
-__device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ M0, F0 f0, const float* __restrict__ M1,
+template <bool VEC, int NT, typename ET, int LG, class F0, class F1>
+__device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict__ M0, F0 f0, const float* __restrict__ M1,
                              F1 f1, float (&Z)[NT][4], int J, int c0) {
   const int j0b = 16 * J;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
@@ -468,8 +484,8 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
-        const float bJ = s.G[ref * LDT + c];
-        const float ea = ex2(s.G[ia * LDT + c] - bJ), eb = ex2(s.G[ib * LDT + c] - bJ);
+        const float bJ = s.G[ref * LG + c];
+        const float ea = ex2(s.G[ia * LG + c] - bJ), eb = ex2(s.G[ib * LG + c] - bJ);
         uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
         uint32_t b1[2] = {tf32(f1(ia, c) * ea), tf32(f1(ib, c) * eb)};
         mma8(acc[nt], a0, b0);
@@ -477,7 +493,7 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
       }
     }
     acc_foreach(acc, [&](int r, int col, float& x) {
-      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[ref * LDT + c0 + col] - s.G[(j0b + r) * LDT + c0 + col]);
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[ref * LG + c0 + col] - s.G[(j0b + r) * LG + c0 + col]);
     });
     zero_acc(acc);
     const int mref = j0b + 7;
@@ -491,8 +507,8 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
-        const float mJ = s.G[mref * LDT + c];
-        const float ea = ex2(s.G[ia * LDT + c] - mJ), eb = ex2(s.G[ib * LDT + c] - mJ);
+        const float mJ = s.G[mref * LG + c];
+        const float ea = ex2(s.G[ia * LG + c] - mJ), eb = ex2(s.G[ib * LG + c] - mJ);
         uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
         uint32_t b1[2] = {tf32(f1(ia, c) * ea), tf32(f1(ib, c) * eb)};
         mma8(acc[nt], a0, b0);
@@ -500,7 +516,7 @@ __device__ void right_apply2(const ChunkSmemT<ET>& s, const float* __restrict__ 
       }
     }
     acc_foreach(acc, [&](int r, int col, float& x) {
-      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[mref * LDT + c0 + col] - s.G[(j0b + r) * LDT + c0 + col]);
+      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[mref * LG + c0 + col] - s.G[(j0b + r) * LG + c0 + col]);
     });
   } else {
     for (int kk = 2 * J; kk < 8; ++kk) {
