@@ -44,10 +44,12 @@ KERNEL_MODEL = {
     # name: (bytes per token-head, flops per token-head)
     "prep": (3 * 2 * D + 4 * D + 2 + 4 * _TILE + 3 * C * 4 + 4 * D / C,
              2 * (2 * 0.5 * C * D) + 2 * (2 * 0.5 * C * D) + C * C / 3),
-    "walk_fwd": (3 * _TILE + _STATE + _TILE + 4 * D / C, 2 * (2 * D * D)),
-    "out": (_TILE + _STATE + C * 4 + _TILE + 2 * D, 2 * D * D + 2 * 0.5 * C * D),
-    "walk_bwd": (C * 4 + 3 * _TILE + 2 * D + _STATE + _TILE, 2 * (2 * D * D) + 2 * D * D + 2 * 0.5 * C * D),
-    "grad_state": (2 * D + 2 * _STATE + 2 * _TILE + 3 * _TILE + 4 * D / C, 3 * (2 * D * D)),
+    # state walk with the outputs: reads w, u, Kd^T, Q Gamma, Aqk, gamma; writes
+    # Delta, the BF16 state tape and the BF16 output.
+    "walk_fwd": (4 * _TILE + C * 4 + 4 * D / C + _TILE + _STATE / 2 + 2 * D,
+                 3 * (2 * D * D) + 2 * 0.5 * C * D),
+    "walk_bwd": (C * 4 + 3 * _TILE + 2 * D + _STATE / 2 + _TILE, 2 * (2 * D * D) + 2 * D * D + 2 * 0.5 * C * D),
+    "grad_state": (2 * D + _STATE + 2 * _TILE + 3 * _TILE + 4 * D / C + C * 4, 3 * (2 * D * D)),
     "grad": (3 * 2 * D + 4 * D + 2 + 2 * D + 3 * _TILE + 3 * C * 4 + 2 * _TILE + 3 * _TILE + 3 * 2 * D + 4 * D + 2,
              11 * (2 * 0.5 * C * D) + 2 * (2 * C * D)),
 }

@@ -394,29 +394,20 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   if (!wa.err) return GDR_CUDA_ERROR;
   if (NC > 0 && (!fp32_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, CH) ||
                  !fp32_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, DK) ||
-                 !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, CH)))
+                 !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, CH) ||
+                 !fp32_map(&wa.qp_map, pa.qp, (uint64_t)NC * HV * CH, DK, CH) ||
+                 !fp32_map(&wa.aqk_map, pa.aqk, (uint64_t)NC * HV * CH, CH, CH)))
     return GDR_CUDA_ERROR;
   wa.h0 = h0;
-  wa.tape = at<__nv_bfloat16>(base, L.tape);
-  wa.delta = at<float>(base, L.delta);
+  // The state tape and Delta are only kept for a backward.
+  wa.tape = save_for_bwd ? at<__nv_bfloat16>(base, L.tape) : nullptr;
+  wa.delta = save_for_bwd ? at<float>(base, L.delta) : nullptr;
   wa.ht = ht;
+  wa.out = static_cast<__nv_bfloat16*>(out);
+  wa.scale = scale;
   {
     ProfScope ps("walk_fwd", stream);
     st = cuda_status(launch_walk_fwd(wa, N, walk_tc_cols((int64_t)N * HV), stream));
-  }
-  if (st != GDR_OK) return st;
-  OutArgs oa{};
-  oa.chunks = chunks;
-  oa.HV = HV;
-  oa.scale = scale;
-  oa.qp = pa.qp;
-  oa.aqk = pa.aqk;
-  oa.tape = wa.tape;
-  oa.delta = wa.delta;
-  oa.out = static_cast<__nv_bfloat16*>(out);
-  {
-    ProfScope ps("out", stream);
-    st = cuda_status(launch_out(oa, (int)NC, stream));
   }
   if (st != GDR_OK) return st;
   if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, hash_cu(cu_host, N)});

@@ -99,31 +99,38 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// State walk on the tensor cores (one CTA of 4 warps per (document, value
-// head, N-column value slice); the document's chunks in order, documents
-// issued longest first).  The FP32 state slice S[c][v0 .. v0+N) lives in
-// tensor memory, one channel c per TMEM lane (= thread).  Per chunk:
+// State walk with the chunk outputs, on the tensor cores (one CTA per
+// (document, value head, N-column value slice); the document's chunks in
+// order, documents issued longest first).  The FP32 state slice
+// S[c][v0 .. v0+N) lives in tensor memory, one channel c per TMEM lane.
+// Per chunk:
 //   tape <- S0 (BF16 row per thread);  S0 -> swizzled TF32 operand tile;
-//   P = w S0          (tcgen05.mma M = 64 tokens, N, K = 128)
-//   Delta = u - P     (rows of P back from TMEM; Delta -> operand tile)
+//   P = w S0                 (tcgen05.mma M = 64 tokens, N, K = 128)
+//   Delta = u - P            (rows of P back from TMEM; Delta -> operand tile)
 //   S <- diag(gamma) S0 + Kd^T Delta   (gamma applied in TMEM, then
-//                      tcgen05.mma M = 128 channels, N, K = 64 accumulating)
-// w and Kd^T arrive by TMA into a double buffer two chunks ahead; u and
-// gamma by cp.async.  Waits are bounded; a timed-out wait ends the walk for
+//                            M = 128 channels, N, K = 64 accumulating)
+//   O = Qp S0 + Aqk Delta    (M = 64 tokens, N, K = 128 + 64, reusing the
+//                            S0 and Delta operand tiles), written out as
+//                            scale * O in BF16 while the next chunk's P runs.
+// w, u and gamma arrive by TMA two chunks ahead (double buffer); Kd^T, Qp
+// and Aqk one chunk ahead (single buffer, refilled once the chunk's last
+// products are done).  Waits are bounded; a timed-out wait ends the walk for
 // the whole CTA and sets the device error word.
-// The "state walk" of PR #8638 (opening description) and the walks of
-// PR #7723 (opening description).
+// The "state walk" and "output program" of PR #8638 (opening description)
+// and the walks of PR #7723 (opening description), fused.
 // ---------------------------------------------------------------------------
 template <int N>
 struct WalkTcSmem {
   static constexpr int UB = N < 32 ? 1 : N / 32;  // 32-column TMA boxes of the u slice
   float W[2][CH * DK];      // A of P: w, rows j, K = c (four 64 x 32 column blocks)
-  float KdT[2][DK * CH];    // A of the update: Kd^T, rows c, K = j (two 128 x 32 column blocks)
-  float Sop[N * DK];        // B of P: S0, rows v, K = c
-  float Dop[N * CH];        // B of the update: Delta, rows v, K = j
+  float KdT[DK * CH];       // A of the update: Kd^T, rows c, K = j (two 128 x 32 column blocks)
+  float Qp[CH * DK];        // A of O: Q Gamma, rows i, K = c (four 64 x 32 column blocks)
+  float Aqk[CH * CH];       // A of O: Aqk, rows i, K = j (two 64 x 32 column blocks)
+  float Sop[N * DK];        // B of P and O: S0, rows v, K = c
+  float Dop[N * CH];        // B of the update and O: Delta, rows v, K = j
   float U[2][CH * 32 * UB]; // u slice, rows j, 32-column swizzled blocks
   float gam[2][DK];
-  uint64_t bar_tma[2], bar_p, bar_u;
+  uint64_t bar_w[2], bar_k, bar_p, bar_u;
   uint32_t tmem;
 };
 
@@ -133,8 +140,9 @@ template <int N>
 __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkArgs a) {
   constexpr int VS = DK / N;  // CTAs per (doc, head)
   constexpr int UB = WalkTcSmem<N>::UB;
-  constexpr uint32_t TCOLS = 2 * N < 32 ? 32 : 2 * N;
-  constexpr uint32_t STAGE_BYTES = (2 * CH * DK + CH * 32 * UB + DK) * 4;
+  constexpr uint32_t TCOLS = 4 * N < 32 ? 32 : 4 * N;  // S, P, O[2]
+  constexpr uint32_t W_BYTES = (CH * DK + CH * 32 * UB + DK) * 4;
+  constexpr uint32_t K_BYTES = (DK * CH + CH * DK + CH * CH) * 4;
   extern __shared__ unsigned char smraw[];
   WalkTcSmem<N>& s = *reinterpret_cast<WalkTcSmem<N>*>(tc::align1024(smraw));
   const int rank = blockIdx.x / (a.HV * VS);  // all heads and slices of the longest document first
@@ -148,8 +156,9 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
 
   if (issuer) {
-    tc::mbar_init(&s.bar_tma[0], 1);
-    tc::mbar_init(&s.bar_tma[1], 1);
+    tc::mbar_init(&s.bar_w[0], 1);
+    tc::mbar_init(&s.bar_w[1], 1);
+    tc::mbar_init(&s.bar_k, 1);
     tc::mbar_init(&s.bar_p, 1);
     tc::mbar_init(&s.bar_u, 1);
     tc::mbar_fence_init();
@@ -164,18 +173,45 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   const uint32_t tmem = s.tmem;
   const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes; S in columns [0, N)
   const uint32_t tP = tS + N;                                      // P in columns [N, 2N)
+  const uint32_t tO = tS + 2 * N;                                  // O[b] in columns [2N + bN, 3N + bN)
 
-  auto issue = [&](int m) {  // issuer only
+  auto issue_w = [&](int m) {  // issuer only: w, u, gamma of chunk m into stage m & 1
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     const int item = chunk * a.HV + h;
-    tc::mbar_arrive_expect_tx(&s.bar_tma[b], STAGE_BYTES);
-    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(&s.W[b][kb * CH * 32], &a.w_map, kb * 32, item * CH, &s.bar_tma[b]);
-    for (int kb = 0; kb < 2; ++kb)
-      tc::tma_load_2d(&s.KdT[b][kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_tma[b]);
+    tc::mbar_arrive_expect_tx(&s.bar_w[b], W_BYTES);
+    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(&s.W[b][kb * CH * 32], &a.w_map, kb * 32, item * CH, &s.bar_w[b]);
     for (int ub = 0; ub < UB; ++ub)
-      tc::tma_load_2d(&s.U[b][ub * CH * 32], &a.u_map, v0 + 32 * ub, item * CH, &s.bar_tma[b]);
-    tc::bulk_load(s.gam[b], &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, &s.bar_tma[b]);
+      tc::tma_load_2d(&s.U[b][ub * CH * 32], &a.u_map, v0 + 32 * ub, item * CH, &s.bar_w[b]);
+    tc::bulk_load(s.gam[b], &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, &s.bar_w[b]);
+  };
+  auto issue_k = [&](int m) {  // issuer only: Kd^T, Qp, Aqk of chunk m
+    const int item = (dd.chunk0 + m) * a.HV + h;
+    tc::mbar_arrive_expect_tx(&s.bar_k, K_BYTES);
+    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(&s.KdT[kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_k);
+    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(&s.Qp[kb * CH * 32], &a.qp_map, kb * 32, item * CH, &s.bar_k);
+    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(&s.Aqk[kb * CH * 32], &a.aqk_map, kb * 32, item * CH, &s.bar_k);
+  };
+  // scale * O of chunk m (TMEM buffer m & 1) -> out, rows below the chunk's length.
+  auto write_out = [&](int m) {  // data warps only
+    const int i0 = 64 * m, len = min(CH, dd.len - i0);
+    uint32_t orr[N / 2];
+#pragma unroll
+    for (int cb = 0; cb < N; cb += 16)
+      tc::tmem_ld16x256b_x2(tO + (m & 1) * N + cb, *reinterpret_cast<uint32_t(*)[8]>(&orr[cb / 2]));
+    tc::tmem_wait_ld();
+    const int g = lane >> 2, u2 = (lane & 3) * 2;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = 16 * warp + g + 8 * hr;
+      if (i < len) {
+        __nv_bfloat16* orow = a.out + ((size_t)(dd.tok0 + i0 + i) * a.HV + h) * DK + v0;
+#pragma unroll
+        for (int q = 0; q < N / 8; ++q)
+          *reinterpret_cast<__nv_bfloat162*>(orow + 8 * q + u2) = __floats2bfloat162_rn(
+              a.scale * __uint_as_float(orr[4 * q + 2 * hr]), a.scale * __uint_as_float(orr[4 * q + 2 * hr + 1]));
+      }
+    }
   };
 
   if (tid < DK) {  // S <- h0 (or 0)
@@ -189,10 +225,10 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
     }
     tc::tmem_wait_st();
   }
-  int issued = 0;
+  int issued_w = 0, issued_k = 0, waited_k = 0;
   if (issuer) {
-    if (n > 0) issue(0), ++issued;
-    if (n > 1) issue(1), ++issued;
+    if (n > 0) issue_w(0), issue_k(0), ++issued_w, ++issued_k;
+    if (n > 1) issue_w(1), ++issued_w;
   }
   constexpr uint32_t idP = tc::idesc_tf32(CH, N), idU = tc::idesc_tf32(DK, N);
   unsigned char* sop = reinterpret_cast<unsigned char*>(s.Sop);
@@ -203,13 +239,13 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     const size_t toff = tile_off(chunk, h, a.HV);
-    if (tid < DK) ok = tc::mbar_wait(&s.bar_tma[b], (m >> 1) & 1) && ok;
+    if (tid < DK) ok = tc::mbar_wait(&s.bar_w[b], (m >> 1) & 1) && ok;
     tc::tc_fence_before();
     if (!__syncthreads_and(ok)) break;
     tc::tc_fence_after();
     uint32_t sr[N];
     if (tid < DK) {
-      // S0 row c = tid; S0 as the B operand of P (row v, k = c).
+      // S0 row c = tid; S0 as the B operand of P and O (row v, k = c).
 #pragma unroll
       for (int cb = 0; cb < N; cb += 16) tc::tmem_ld16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&sr[cb]));
       tc::tmem_wait_ld();
@@ -230,7 +266,8 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
       tc::mma_commit(&s.bar_p);
     }
     if (tid < DK) {
-      // While P runs: the tape row and diag(gamma) S0 back into TMEM (columns P does not touch).
+      // While P runs: the tape row, diag(gamma) S0 back into TMEM (columns P
+      // does not touch), and the previous chunk's output.
       if (a.tape) {  // S0[c][v0 .. v0+N) as BF16
         uint4* tp = reinterpret_cast<uint4*>(a.tape + state_off(chunk, h, a.HV) + (size_t)tid * DK + v0);
 #pragma unroll
@@ -249,6 +286,7 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
 #pragma unroll
       for (int cb = 0; cb < N; cb += 16) tc::tmem_st16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&sr[cb]));
       tc::tmem_wait_st();
+      if (m > 0) write_out(m - 1);
       ok = tc::mbar_wait(&s.bar_p, m & 1) && ok;
       tc::tc_fence_after();
       // Delta = u - P over the 16-row block of this warp, spread over all 32 lanes:
@@ -280,97 +318,61 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
     __syncthreads();
     tc::tc_fence_after();
     if (issuer) {
-      const uint64_t ak = tc::desc_k_sw128(s.KdT[b]), bd = tc::desc_k_sw128(s.Dop);
+      const bool kready = tc::mbar_wait(&s.bar_k, m & 1);
+      ok = kready && ok;
+      if (kready) {
+        ++waited_k;
+        const uint64_t ak = tc::desc_k_sw128(s.KdT), bd = tc::desc_k_sw128(s.Dop);
+        const uint64_t aq = tc::desc_k_sw128(s.Qp), bs = tc::desc_k_sw128(s.Sop);
+        const uint64_t aa = tc::desc_k_sw128(s.Aqk);
+        const uint32_t dO = tmem + 2 * N + b * N;
 #pragma unroll
-      for (int k = 0; k < CH / 8; ++k)
-        tc::mma_tf32(tmem, ak + (uint64_t)((((k >> 2) * DK * 128) + (k & 3) * 32) >> 4),
-                     bd + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idU, 1);
+        for (int k = 0; k < CH / 8; ++k)
+          tc::mma_tf32(tmem, ak + (uint64_t)((((k >> 2) * DK * 128) + (k & 3) * 32) >> 4),
+                       bd + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idU, 1);
+#pragma unroll
+        for (int k = 0; k < DK / 8; ++k)
+          tc::mma_tf32(dO, aq + (uint64_t)((((k >> 2) * CH * 128) + (k & 3) * 32) >> 4),
+                       bs + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idP, k > 0);
+#pragma unroll
+        for (int k = 0; k < CH / 8; ++k)
+          tc::mma_tf32(dO, aa + (uint64_t)((((k >> 2) * CH * 128) + (k & 3) * 32) >> 4),
+                       bd + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idP, 1);
+      }
       tc::mma_commit(&s.bar_u);
     }
-    // Everyone (the issuer to refill stage b, the data warps before reading S) waits for the update.
+    // Everyone (the issuer to refill the buffers, the data warps before
+    // reading S) waits for the update and O.
     if (tid < DK || issuer) ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
     tc::tc_fence_after();
-    if (issuer && ok && m + 2 < n) issue(m + 2), ++issued;
+    if (issuer && ok) {
+      if (m + 2 < n) issue_w(m + 2), ++issued_w;
+      if (m + 1 < n) issue_k(m + 1), ++issued_k;
+    }
   }
   if (m < n) {
     // A wait ran out: record it and drain the copies still in flight.
     if (issuer) {
       atomicExch(a.err, 3);
-      for (int q = m; q < issued; ++q) tc::mbar_wait(&s.bar_tma[q & 1], (q >> 1) & 1);
+      for (int q = m; q < issued_w; ++q) tc::mbar_wait(&s.bar_w[q & 1], (q >> 1) & 1);
+      for (int q = waited_k; q < issued_k; ++q) tc::mbar_wait(&s.bar_k, q & 1);
     }
-  } else if (a.ht && tid < DK) {
+  } else if (tid < DK) {
+    if (n > 0) write_out(n - 1);
+    if (a.ht) {
 #pragma unroll
-    for (int cb = 0; cb < N; cb += 16) {
-      uint32_t r[16];
-      tc::tmem_ld16(tS + cb, r);
-      tc::tmem_wait_ld();
+      for (int cb = 0; cb < N; cb += 16) {
+        uint32_t r[16];
+        tc::tmem_ld16(tS + cb, r);
+        tc::tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 16; ++q) a.ht[sidx + (size_t)tid * DK + v0 + cb + q] = __uint_as_float(r[q]);
+        for (int q = 0; q < 16; ++q) a.ht[sidx + (size_t)tid * DK + v0 + cb + q] = __uint_as_float(r[q]);
+      }
     }
   }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
-}
-
-// ---------------------------------------------------------------------------
-// Output (one CTA of 8 warps per (chunk, value head)):
-//   O = scale (Qp S0 + Aqk Delta),  warp w: rows 16 (w % 4), columns 64 (w / 4).
-// Operands are staged in shared memory with cp.async in two groups so that
-// the Aqk / Delta copy overlaps the Qp S0 product.
-// The "output program" of PR #8218 (kcp_fwd_o) and PR #8638.
-// ---------------------------------------------------------------------------
-constexpr int LDB = DK + 8;  // row stride (elements) of a [128][128] BF16 shared tile
-struct OutSmem {
-  uint16_t S0[DK * LDB];
-  float Qp[CH * LDT];
-  float Aqk[CH * LDS];
-  float Dl[CH * LDT];
-};
-
-__global__ void __launch_bounds__(256) k_out(OutArgs a) {
-  extern __shared__ __align__(16) unsigned char smraw[];
-  OutSmem& s = *reinterpret_cast<OutSmem*>(smraw);
-  const int chunk = blockIdx.x, h = blockIdx.y;
-  const ChunkDesc cd = a.chunks[chunk];
-  const int warp = threadIdx.x >> 5, I = warp & 3, i0 = 16 * I, n0 = (warp >> 2) * 64;
-  const size_t toff = tile_off(chunk, h, a.HV);
-  const __nv_bfloat16* S0 = a.tape + state_off(chunk, h, a.HV);
-  const float* aqk = a.aqk + sq_off(chunk, h, a.HV);
-  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // S0 rows [c][v]
-    const int c = e >> 4, v8 = (e & 15) * 8;
-    cp_async16(&s.S0[c * LDB + v8], &S0[c * DK + v8]);
-  }
-  for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
-    const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&s.Qp[i * LDT + c4], &a.qp[toff + i * DK + c4]);
-  }
-  cp_async_commit();
-  for (int e = threadIdx.x; e < CH * CH / 4; e += 256) {
-    const int i = e >> 4, c4 = (e & 15) * 4;
-    cp_async16(&s.Aqk[i * LDS + c4], &aqk[i * CH + c4]);
-  }
-  for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
-    const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&s.Dl[i * LDT + c4], &a.delta[toff + i * DK + c4]);
-  }
-  cp_async_commit();
-  cp_async_wait<1>();
-  __syncthreads();
-  float acc[8][4];
-  zero_acc(acc);
-  for (int kk = 0; kk < 16; ++kk)
-    mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int c) { return s.Qp[(i0 + i) * LDT + c]; },
-                 [&](int c, int v) { return bfbits2f(s.S0[c * LDB + n0 + v]); });
-  cp_async_wait<0>();
-  __syncthreads();
-  for (int kk = 0; kk < 2 * I + 2; ++kk)
-    mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.Aqk[(i0 + i) * LDS + j]; },
-                 [&](int j, int v) { return s.Dl[j * LDT + n0 + v]; });
-  acc_foreach(acc, [&](int r, int c, float& x) {
-    const int i = i0 + r;
-    if (i < cd.len) a.out[((size_t)(cd.tok0 + i) * a.HV + h) * DK + n0 + c] = __float2bfloat16_rn(a.scale * x);
-  });
 }
 
 // ---------------------------------------------------------------------------
@@ -414,13 +416,5 @@ cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int cols_per_cta, cuda
   }
 }
 
-cudaError_t launch_out(const OutArgs& a, int nchunks, cudaStream_t st) {
-  if (nchunks == 0) return cudaSuccess;
-  dim3 grid(nchunks, a.HV);
-  const size_t sm = sizeof(OutSmem);
-  cudaFuncSetAttribute(k_out, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  k_out<<<grid, 256, sm, st>>>(a);
-  return cudaGetLastError();
-}
 
 }  // namespace gdr

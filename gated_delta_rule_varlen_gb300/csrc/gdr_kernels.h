@@ -27,6 +27,8 @@ struct WalkArgs {
   CUtensorMap w_map;    // w as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
   CUtensorMap kdt_map;  // Kd^T as a 2-D FP32 tensor [NC*HV*128][64], 32 x 128 boxes, 128-byte swizzle
   CUtensorMap u_map;    // u as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
+  CUtensorMap qp_map;   // Q Gamma as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
+  CUtensorMap aqk_map;  // Aqk as a 2-D FP32 tensor [NC*HV*64][64], 32 x 64 boxes, 128-byte swizzle
   const DocDesc* docs;
   const int* order;  // documents, longest first
   int HV;
@@ -35,17 +37,11 @@ struct WalkArgs {
   __nv_bfloat16* tape;  // S0 per chunk (BF16, S[c][v]), or null
   float* delta;      // Delta per chunk, or null
   float* ht;         // [N][HV][128][128] or null
+  __nv_bfloat16* out;  // [T][HV][128]
+  float scale;
   int* err;          // device error word
 };
 
-struct OutArgs {
-  const ChunkDesc* chunks;
-  int HV;
-  float scale;
-  const float *qp, *aqk, *delta;
-  const __nv_bfloat16* tape;
-  __nv_bfloat16* out;  // [T][HV][128]
-};
 
 struct WalkBwdArgs {
   const DocDesc* docs;
@@ -99,7 +95,6 @@ struct GroupReduceArgs {
 
 cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
 cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int cols_per_cta, cudaStream_t st);
-cudaError_t launch_out(const OutArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, cudaStream_t st);
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_grad(const GradArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
