@@ -122,26 +122,30 @@ __device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restric
   __syncthreads();
 }
 
-// Gated Gram matrices of one chunk.
+// Gated Gram matrices of one chunk,
 //   At[i][j]  = sum_c K_ic K_jc exp(gc_ic - gc_jc)   for j <  i (else 0)  -> s.At
 //   Aqk[i][j] = sum_c Q_ic K_jc exp(gc_ic - gc_jc)   for j <= i (else 0)  -> aqk (global, [64][64])
+// on 8 warps: warp w takes row block I = w % 4 and channels [64 (w / 4), +64).
 // Per-channel gates use the block factorization described in gdr_common.cuh.
+// The upper channel half leaves its partial sums in s.At and s.T (free until
+// the inverse); the lower half adds them in, masks, and writes the results.
 // Aqk is stored rounded to TF32 (it is only ever an MMA operand).
-template <bool VEC, bool WITH_QK, typename ET, int LG>
+template <bool VEC, typename ET, int LG>
 __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
-  const int I = threadIdx.x >> 5, i0 = 16 * I;
+  const int warp = threadIdx.x >> 5, I = warp & 3, hk = warp >> 2, i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const int ra = i0 + g, rb = i0 + g + 8;
-  float accK[8][4], accQ[8][4];
+  const float* G = s.G;
+  // Off-diagonal n-tiles [0, 2I) (and, with a scalar gate, the diagonal ones)
+  // in accK/accQ; diagonal n-tiles 2I, 2I+1 of a per-channel gate in dK/dQ.
+  float accK[8][4], accQ[8][4], dK[2][4], dQ[2][4];
   zero_acc(accK);
   zero_acc(accQ);
+  zero_acc(dK);
+  zero_acc(dQ);
   if (VEC) {
-    float dK[2][4], dQ[2][4];
-    zero_acc(dK);
-    zero_acc(dQ);
-    const float* G = s.G;
 #pragma unroll 2
-    for (int kk = 0; kk < 16; ++kk) {
+    for (int kk = 8 * hk; kk < 8 * hk + 8; ++kk) {
       const int c0 = kk * 8 + t, c1 = c0 + 4;
       const float ka0 = s.k(ra, c0), kb0 = s.k(rb, c0), ka1 = s.k(ra, c1), kb1 = s.k(rb, c1);
       const float qa0 = s.q(ra, c0), qb0 = s.q(rb, c0), qa1 = s.q(ra, c1), qb1 = s.q(rb, c1);
@@ -158,7 +162,7 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
             const int j = nt * 8 + g;
             uint32_t b[2] = {tf32(s.k(j, c0) * ex2(b0 - G[j * LG + c0])), tf32(s.k(j, c1) * ex2(b1 - G[j * LG + c1]))};
             mma8(accK[nt], aK, b);
-            if (WITH_QK) mma8(accQ[nt], aQ, b);
+            mma8(accQ[nt], aQ, b);
           }
         }
       }
@@ -173,33 +177,13 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
           const int j = i0 + nt * 8 + g;
           uint32_t b[2] = {tf32(s.k(j, c0) * ex2(m0 - G[j * LG + c0])), tf32(s.k(j, c1) * ex2(m1 - G[j * LG + c1]))};
           mma8(dK[nt], aK, b);
-          if (WITH_QK) mma8(dQ[nt], aQ, b);
+          mma8(dQ[nt], aQ, b);
         }
-      }
-    }
-    // Scatter: off-diagonal n-tiles [0, 2I), diagonal tiles 2I, 2I+1, zeros above.
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int row = g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
-        float vK = 0.f, vQ = 0.f;
-        if (nt < 2 * I) {
-          vK = accK[nt][r];
-          vQ = accQ[nt][r];
-        } else if (nt == 2 * I || nt == 2 * I + 1) {
-          const int dn = nt - 2 * I;
-          const int lcol = dn * 8 + 2 * t + (r & 1);
-          vK = lcol < row ? dK[dn][r] : 0.f;
-          vQ = lcol <= row ? dQ[dn][r] : 0.f;
-        }
-        s.At[(i0 + row) * LDS + col] = vK;
-        if (WITH_QK) aqk[(i0 + row) * CH + col] = __uint_as_float(tf32(vQ));
       }
     }
   } else {
 #pragma unroll 2
-    for (int kk = 0; kk < 16; ++kk) {
+    for (int kk = 8 * hk; kk < 8 * hk + 8; ++kk) {
       const int c0 = kk * 8 + t, c1 = c0 + 4;
       uint32_t aK[4] = {tf32(s.k(ra, c0)), tf32(s.k(rb, c0)), tf32(s.k(ra, c1)), tf32(s.k(rb, c1))};
       uint32_t aQ[4] = {tf32(s.q(ra, c0)), tf32(s.q(rb, c0)), tf32(s.q(ra, c1)), tf32(s.q(rb, c1))};
@@ -209,35 +193,63 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
           const int j = nt * 8 + g;
           uint32_t b[2] = {tf32(s.k(j, c0)), tf32(s.k(j, c1))};
           mma8(accK[nt], aK, b);
-          if (WITH_QK) mma8(accQ[nt], aQ, b);
+          mma8(accQ[nt], aQ, b);
         }
       }
     }
+  }
+  // Raw (unmasked) sum of this warp's channel half at accumulator slot (nt, r).
+  auto raw = [&](const float (&acc)[8][4], const float (&dg)[2][4], int nt, int r) -> float {
+    if (VEC && nt == 2 * I) return dg[0][r];
+    if (VEC && nt == 2 * I + 1) return dg[1][r];
+    return acc[nt][r];
+  };
+  float* tq = s.T;  // partial Aqk of the upper channel half
+  if (hk == 1) {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = i0 + g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
+        if (nt < 2 * I + 2) {
+          s.At[row * LDS + col] = raw(accK, dK, nt, r);
+          tq[row * LDS + col] = raw(accQ, dQ, nt, r);
+        }
+      }
+  }
+  __syncthreads();
+  if (hk == 0) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int row = i0 + g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
         float vK = 0.f, vQ = 0.f;
-        if (col <= row) {
-          const float dec = ex2(s.gs[row] - s.gs[col]);
-          vQ = accQ[nt][r] * dec;
-          if (col < row) vK = accK[nt][r] * dec;
+        if (nt < 2 * I + 2 && col <= row) {
+          vK = raw(accK, dK, nt, r) + s.At[row * LDS + col];
+          vQ = raw(accQ, dQ, nt, r) + tq[row * LDS + col];
+          if (!VEC) {
+            const float dec = ex2(s.gs[row] - s.gs[col]);
+            vK *= dec;
+            vQ *= dec;
+          }
+          if (col == row) vK = 0.f;
         }
         s.At[row * LDS + col] = vK;
-        if (WITH_QK) aqk[row * CH + col] = __uint_as_float(tf32(vQ));
+        aqk[row * CH + col] = __uint_as_float(tf32(vQ));
       }
-    }
   }
+  __syncthreads();
 }
 
-// s.T = (I + diag(beta) At)^-1, unit lower triangular, in FP32 on CUDA cores.
-// Diagonal 16x16 blocks by forward substitution (warp I, one column per lane
-// of its first 16), then the blocks below them column block by column block:
-// warp J computes, for I = J+1 .. 3 in order,
+// s.T = (I + diag(beta) At)^-1, unit lower triangular, in FP32 on CUDA cores,
+// on 8 warps.  Diagonal 16x16 blocks by forward substitution (warp I < 4,
+// one column per lane of its first 16), then the blocks below them column
+// block by column block: warps J and J + 4 (J < 3) take columns
+// [16 J + 8 (w / 4), +8) of column block J and compute, for I = J+1 .. 3 in order,
 //   T_IJ = -T_II * diag(beta_I) * sum_{K=J}^{I-1} At_IK T_KJ,
-// which needs only blocks of column J that the same warp made before, so the
-// off-diagonal part synchronizes within the warp only.  Needs >= 4 warps.
+// which needs only blocks of those columns that the same warp made before,
+// so the off-diagonal part synchronizes within the warp only.
 template <typename ET, int LG>
 __device__ void invert(ChunkSmemT<ET, LG>& s) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
@@ -261,50 +273,36 @@ __device__ void invert(ChunkSmemT<ET, LG>& s) {
     if ((j >> 4) > (i >> 4)) s.T[i * LDS + j] = 0.f;
   }
   __syncthreads();
-  if (warp < 3) {
-    const int J = warp, r = lane >> 1, half = (lane & 1) * 8, cb = 16 * J + half;
-    float* tmp = s.tmp + warp * 256;  // [16][16]: diag(beta_I) sum_K At_IK T_KJ
+  if ((warp & 3) < 3) {
+    const int J = warp & 3, r = lane >> 1, q4 = (lane & 1) * 4;
+    const int cw = 8 * (warp >> 2);          // column offset of this warp inside block J
+    const int cb = 16 * J + cw + q4;         // this lane's first column
+    float* tmp = s.tmp + ((warp >> 2) * 3 + J) * 128;  // [16][8]: diag(beta_I) sum_K At_IK T_KJ
     for (int I = J + 1; I < 4; ++I) {
       const int row = 16 * I + r;
-      float acc[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
       for (int k = 16 * J; k < 16 * I; ++k) {
         const float av = s.At[row * LDS + k];
-        const float4 t0 = *reinterpret_cast<const float4*>(&s.T[k * LDS + cb]);
-        const float4 t1 = *reinterpret_cast<const float4*>(&s.T[k * LDS + cb + 4]);
-        acc[0] += av * t0.x;
-        acc[1] += av * t0.y;
-        acc[2] += av * t0.z;
-        acc[3] += av * t0.w;
-        acc[4] += av * t1.x;
-        acc[5] += av * t1.y;
-        acc[6] += av * t1.z;
-        acc[7] += av * t1.w;
+        const float4 tv = *reinterpret_cast<const float4*>(&s.T[k * LDS + cb]);
+        acc[0] += av * tv.x;
+        acc[1] += av * tv.y;
+        acc[2] += av * tv.z;
+        acc[3] += av * tv.w;
       }
       const float bi = s.beta[row];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) tmp[r * 16 + half + q] = bi * acc[q];
+      *reinterpret_cast<float4*>(&tmp[r * 8 + q4]) = make_float4(bi * acc[0], bi * acc[1], bi * acc[2], bi * acc[3]);
       __syncwarp();
-      float out[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) out[q] = 0.f;
+      float out[4] = {0.f, 0.f, 0.f, 0.f};
       for (int m = 0; m <= r; ++m) {
         const float tv = s.T[row * LDS + 16 * I + m];
-        const float4 x0 = *reinterpret_cast<const float4*>(&tmp[m * 16 + half]);
-        const float4 x1 = *reinterpret_cast<const float4*>(&tmp[m * 16 + half + 4]);
-        out[0] += tv * x0.x;
-        out[1] += tv * x0.y;
-        out[2] += tv * x0.z;
-        out[3] += tv * x0.w;
-        out[4] += tv * x1.x;
-        out[5] += tv * x1.y;
-        out[6] += tv * x1.z;
-        out[7] += tv * x1.w;
+        const float4 x = *reinterpret_cast<const float4*>(&tmp[m * 8 + q4]);
+        out[0] += tv * x.x;
+        out[1] += tv * x.y;
+        out[2] += tv * x.z;
+        out[3] += tv * x.w;
       }
       *reinterpret_cast<float4*>(&s.T[row * LDS + cb]) = make_float4(-out[0], -out[1], -out[2], -out[3]);
-      *reinterpret_cast<float4*>(&s.T[row * LDS + cb + 4]) = make_float4(-out[4], -out[5], -out[6], -out[7]);
       __syncwarp();
     }
   }

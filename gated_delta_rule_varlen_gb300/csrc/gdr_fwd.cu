@@ -6,30 +6,30 @@
 namespace gdr {
 
 // ---------------------------------------------------------------------------
-// Prep (one CTA per (chunk, value head)): gate cumsum, gated Gram matrices,
-// T = (I + diag(beta) At)^-1, and the chunk tiles the walk and the output
-// need:  w = T beta (K*Gamma),  u = T beta V,  Qp = Q*Gamma,
-// Kd = K*exp(gc_last - gc),  gamma = exp(gc_last),  Aqk.
+// Prep (one CTA of 8 warps per (chunk, value head)): gate cumsum, gated Gram
+// matrices, T = (I + diag(beta) At)^-1, and the chunk tiles the walk and the
+// backward need:  w = T beta (K*Gamma),  u = T beta V,  Qp = Q*Gamma,
+// Kd = K*exp(gc_last - gc),  gamma = exp(gc_last),  Aqk, At, T.
 // The "prep program" of PR #8638 "perf(cake_gdn_kcp): ... graph-replay
 // checkpoint recompute hands its tapes to the backward" (opening description).
 // ---------------------------------------------------------------------------
 template <bool VEC, typename BetaT>
-__global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
+__global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ChunkSmemB& s = *reinterpret_cast<ChunkSmemB*>(smem_raw);
   constexpr int LDK = ChunkSmemB::LD;
   const int chunk = blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
+  const int tid = threadIdx.x, warp = tid >> 5;
   load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
                          a.HV);
-  gram<VEC, true>(s, a.aqk + sq_off(chunk, h, a.HV));
-  __syncthreads();
+  gram<VEC>(s, a.aqk + sq_off(chunk, h, a.HV));
   invert(s);
   // At and T for the backward: the values its gradient kernel needs, bit for bit.
   if (a.amat) {
     const size_t qo = sq_off(chunk, h, a.HV);
-    for (int e = threadIdx.x; e < CH * CH / 4; e += blockDim.x) {
+    for (int e = tid; e < CH * CH / 4; e += blockDim.x) {
       const int i = e >> 4, j4 = (e & 15) * 4;
       *reinterpret_cast<float4*>(&a.amat[qo + i * CH + j4]) = *reinterpret_cast<const float4*>(&s.At[i * LDS + j4]);
       *reinterpret_cast<float4*>(&a.tmat[qo + i * CH + j4]) = *reinterpret_cast<const float4*>(&s.T[i * LDS + j4]);
@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
   // Qp, Kd, gamma (elementwise; factors exp(gc) and exp(gc_last - gc) are <= 1).
   // Qp and Kd are only ever MMA operands: stored rounded to TF32.
   const size_t toff = tile_off(chunk, h, a.HV);
-  for (int e = threadIdx.x; e < CH * DK; e += blockDim.x) {
+  for (int e = tid; e < CH * DK; e += blockDim.x) {
     const int i = e >> 7, d = e & 127;
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
     const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
   // Kd stored transposed, [c][j] (the K-major A operand of the walk's state update).
   // A warp covers rows i = 8k .. 8k+7 of channels d .. d+3 (lane bits 0-2 -> i,
   // 3-4 -> d): shared reads are conflict-free, each 8-lane group writes 32 bytes.
-  for (int e = threadIdx.x; e < CH * DK; e += blockDim.x) {
+  for (int e = tid; e < CH * DK; e += blockDim.x) {
     const int l = e & 31, w = e >> 5;
     const int i = (l & 7) + 8 * (w & 7), d = 4 * (w >> 3) + (l >> 3);
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
     a.kd[toff + d * CH + i] = __uint_as_float(tf32(s.k(i, d) * ex2(glast - gl)));
   }
   __syncthreads();
-  // Q tile <- v rows (async; used for u), G tile <- beta * K * Gamma (for w).
-  for (int e = threadIdx.x; e < CH * DK / 8; e += blockDim.x) {
+  // Q tile <- v rows (async), G tile <- beta * K * Gamma (B of w).
+  for (int e = tid; e < CH * DK / 8; e += blockDim.x) {
     const int i = e >> 4, d8 = (e & 15) * 8;
     if (i < cd.len)
       cp_async16(&s.Q[i * LDK + d8], a.v + ((size_t)(cd.tok0 + i) * a.HV + h) * DK + d8);
@@ -65,36 +65,38 @@ __global__ void __launch_bounds__(128) k_prep(PrepArgs a) {
       *reinterpret_cast<uint4*>(&s.Q[i * LDK + d8]) = make_uint4(0u, 0u, 0u, 0u);
   }
   cp_async_commit();
-  for (int e = threadIdx.x; e < CH * DK; e += blockDim.x) {
+  for (int e = tid; e < CH * DK; e += blockDim.x) {
     const int i = e >> 7, d = e & 127;
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
     s.G[i * LDT + d] = s.beta[i] * s.k(i, d) * ex2(gl);
   }
-  __syncthreads();
-  const int I = threadIdx.x >> 5, i0 = 16 * I;
-  {
-    float acc[16][4];
-    zero_acc(acc);
-    for (int kk = 0; kk < 2 * I + 2; ++kk)
-      mma_kstep<16>(acc, kk * 8, 0, 16, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
-                    [&](int j, int c) { return s.G[j * LDT + c]; });
-    acc_foreach(acc, [&](int r, int c, float& x) { a.w[toff + (i0 + r) * DK + c] = __uint_as_float(tf32(x)); });
-  }
   cp_async_wait<0>();
   __syncthreads();
-  // G tile <- beta * V
-  for (int e = threadIdx.x; e < CH * DK; e += blockDim.x) {
-    const int i = e >> 7, d = e & 127;
-    s.G[i * LDT + d] = s.beta[i] * s.q(i, d);
-  }
-  __syncthreads();
+  // w (warps 0-3) and u (warps 4-7) = T B over rows j <= i.  Warp q of a
+  // product takes channel half q % 2 of row blocks {3, 0} (q < 2) or {2, 1},
+  // so that the four warps do equal work.  B of u, beta_j V_jc, is formed from
+  // the BF16 v tile as it is read.
   {
-    float acc[16][4];
-    zero_acc(acc);
-    for (int kk = 0; kk < 2 * I + 2; ++kk)
-      mma_kstep<16>(acc, kk * 8, 0, 16, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
-                    [&](int j, int c) { return s.G[j * LDT + c]; });
-    acc_foreach(acc, [&](int r, int c, float& x) { a.u[toff + (i0 + r) * DK + c] = __uint_as_float(tf32(x)); });
+    const int prod = warp >> 2, q = warp & 3, c0 = 64 * (q & 1);
+    const int Ia = (q >> 1) ? 2 : 3, Ib = 3 - Ia;
+    float* out = prod ? a.u : a.w;
+    auto bw = [&](int j, int c) { return s.G[j * LDT + c]; };
+    auto bu = [&](int j, int c) { return s.beta[j] * s.q(j, c); };
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int I = pass ? Ib : Ia, i0 = 16 * I;
+      float acc[8][4];
+      zero_acc(acc);
+      for (int kk = 0; kk < 2 * I + 2; ++kk) {
+        if (prod)
+          mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
+                       [&](int j, int c) { return bu(j, c0 + c); });
+        else
+          mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
+                       [&](int j, int c) { return bw(j, c0 + c); });
+      }
+      acc_foreach(acc, [&](int r, int c, float& x) { out[toff + (i0 + r) * DK + c0 + c] = __uint_as_float(tf32(x)); });
+    }
   }
 }
 
@@ -384,16 +386,16 @@ cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16
   dim3 grid(nchunks, a.HV);
   if (vec && beta_bf16) {
     cudaFuncSetAttribute(k_prep<true, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_prep<true, __nv_bfloat16><<<grid, 128, sm, st>>>(a);
+    k_prep<true, __nv_bfloat16><<<grid, 256, sm, st>>>(a);
   } else if (vec) {
     cudaFuncSetAttribute(k_prep<true, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_prep<true, float><<<grid, 128, sm, st>>>(a);
+    k_prep<true, float><<<grid, 256, sm, st>>>(a);
   } else if (beta_bf16) {
     cudaFuncSetAttribute(k_prep<false, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_prep<false, __nv_bfloat16><<<grid, 128, sm, st>>>(a);
+    k_prep<false, __nv_bfloat16><<<grid, 256, sm, st>>>(a);
   } else {
     cudaFuncSetAttribute(k_prep<false, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_prep<false, float><<<grid, 128, sm, st>>>(a);
+    k_prep<false, float><<<grid, 256, sm, st>>>(a);
   }
   return cudaGetLastError();
 }
