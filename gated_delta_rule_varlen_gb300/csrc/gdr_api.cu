@@ -219,6 +219,9 @@ int walk_tc_cols(int64_t chains) {
 }
 
 bool aligned(const void* p) { return ((uintptr_t)p % kAlign) == 0; }
+// Tensors the kernels copy in 16-byte pieces (q, k, v, g, dout) or store in
+// pairs must start on these boundaries.
+bool aligned_to(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
 gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_CUDA_ERROR; }
 
@@ -343,6 +346,8 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   if (N == 0) return GDR_OK;
   if (!cu) return GDR_INVALID_ARG;
   if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDR_INVALID_ARG;
+  if (!aligned_to(q, 16) || !aligned_to(k, 16) || !aligned_to(v, 16) || !aligned_to(g, 16) || !aligned_to(out, 4))
+    return GDR_INVALID_ARG;
   if (save_for_bwd && !saved) return GDR_INVALID_ARG;
   const Layout L = make_layout(NC, N, HV, HV != Hqk);
   void* base = saved ? saved : scratch;
@@ -426,6 +431,9 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   if (N == 0) return GDR_OK;
   if (!cu || !saved || !scratch) return GDR_INVALID_ARG;
   if (T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta)) return GDR_INVALID_ARG;
+  if (!aligned_to(q, 16) || !aligned_to(k, 16) || !aligned_to(v, 16) || !aligned_to(g, 16) || !aligned_to(dout, 16) ||
+      !aligned_to(dq, 4) || !aligned_to(dk, 4) || !aligned_to(dv, 4))
+    return GDR_INVALID_ARG;
   if (!aligned(saved) || !aligned(scratch)) return GDR_INVALID_ARG;
   const Layout L = make_layout(NC, N, HV, HV != Hqk);
   if (saved_bytes < L.saved_total || scratch_bytes < L.bwd_total) return GDR_WORKSPACE_TOO_SMALL;

@@ -39,8 +39,8 @@ struct WalkBwdA {
   float gam[DK];
 };
 struct WalkBwdB {
-  float Qp[CH * LDT];
-  float W[CH * LDT];
+  float Qp[CH * LDF];  // read with the row on the thread-in-group index
+  float W[CH * LDT];   // read on rows 2t, 2t+1
 };
 
 template <int NW>
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
     const size_t toff = tile_off(chunk, h, a.HV);
     for (int e = threadIdx.x; e < CH * DK / 4; e += NTH) {
       const int i = e >> 5, c4 = (e & 31) * 4;
-      cp_async16(&sb.Qp[i * LDT + c4], &a.qp[toff + i * DK + c4]);
+      cp_async16(&sb.Qp[i * LDF + c4], &a.qp[toff + i * DK + c4]);
       cp_async16(&sb.W[i * LDT + c4], &a.w[toff + i * DK + c4]);
     }
   };
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
                         tf32(a.scale * bfbits2f(A.dO[ib * LDO + w16 + g + 8]))};
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {__float_as_uint(sb.Qp[ia * LDT + nt * 8 + g]), __float_as_uint(sb.Qp[ib * LDT + nt * 8 + g])};
+        uint32_t b[2] = {__float_as_uint(sb.Qp[ia * LDF + nt * 8 + g]), __float_as_uint(sb.Qp[ib * LDF + nt * 8 + g])};
         mma8(S[nt], av, b);
       }
     }

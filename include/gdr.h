@@ -43,7 +43,10 @@
  *     10 = 80 < 88.7).  Outside that range results are unspecified.
  *   - Workspaces.  `saved` carries the forward's intermediates to the
  *     backward; `scratch` holds temporaries.  Sizes come from
- *     *_workspace_bytes.  Both must be 256-byte aligned.  `saved` belongs to
+ *     *_workspace_bytes.  Both must be 256-byte aligned.
+ *   - Alignment of the tensors: q, k, v, g and dout start on a 16-byte
+ *     boundary (the kernels copy their rows in 16-byte pieces), out, dq, dk
+ *     and dv on a 4-byte boundary; otherwise GDR_INVALID_ARG.  `saved` belongs to
  *     the caller between a forward with save_for_bwd = 1 and the backward.
  *   - Errors are returned as gdr_status, never thrown; a call that returns an
  *     error has enqueued nothing (except GDR_CUDA_ERROR from a launch).

@@ -104,6 +104,14 @@ def test_forward_host_validation_before_any_cuda_call(gdr):
     # save_for_bwd without a saved buffer
     st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, None, 0, 1, p, 1 << 40, None)
     assert st == gdr.GDR_INVALID_ARG
+    # q not on a 16-byte boundary (its rows are copied in 16-byte pieces)
+    st = lib.kda_fwd(ctypes.c_void_p(0x10008), p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, p, 1 << 40, 1,
+                     None, 0, None)
+    assert st == gdr.GDR_INVALID_ARG
+    # out not on a 4-byte boundary
+    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, ctypes.c_void_p(0x10002), None, p, 1 << 40, 1,
+                     None, 0, None)
+    assert st == gdr.GDR_INVALID_ARG
     # GDN: HV not a multiple of Hqk
     st = lib.gdn_fwd(p, p, p, p, p, p, cup, 2, 11, 4, 6, 1.0, None, p, None, p, 1 << 40, 1, None, 0, None)
     assert st == gdr.GDR_INVALID_ARG
@@ -126,6 +134,10 @@ def test_backward_rejects_unstamped_workspace(gdr):
     st = lib.gdn_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 3, 1.0, None, p, None, _fake(512), big, p, p, p, p, p, None,
                      _fake(1024), big, None)
     assert st == gdr.GDR_STALE_WORKSPACE
+    # dout not on a 16-byte boundary
+    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, ctypes.c_void_p(0x10004), None, _fake(512), big, p,
+                     p, p, p, p, None, _fake(1024), big, None)
+    assert st == gdr.GDR_INVALID_ARG
     # Too-small scratch is reported before the stamp.
     st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, _fake(512), big, p, p, p, p, p, None,
                      _fake(1024), 256, None)
