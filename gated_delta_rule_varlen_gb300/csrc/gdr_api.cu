@@ -99,12 +99,12 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
   L.docs = take((size_t)std::max(N, 1) * sizeof(DocDesc));
   L.chunks = take((size_t)std::max<int64_t>(NC, 1) * sizeof(ChunkDesc));
   L.order = take((size_t)std::max(N, 1) * sizeof(int));
-  L.w = take(tile);
+  L.w = take((size_t)NC * HV * CH * LDT * sizeof(float));
   L.u = take(tile);
-  L.qp = take(tile);
-  L.kd = take(tile);
+  L.qp = take((size_t)NC * HV * CH * LDF * sizeof(float));
+  L.kd = take((size_t)NC * HV * DK * LDS * sizeof(float));
   L.delta = take(tile);
-  L.aqk = take(sq);
+  L.aqk = take((size_t)NC * HV * CH * LDS * sizeof(float));
   L.amat = take(sq);
   L.tmat = take(sq);
   L.gam = take(vec);
@@ -243,11 +243,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // A row-major FP32 matrix [rows][cols] read in boxes of 32 columns (128 bytes,
 // 128-byte swizzle) x box_rows rows.
-bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// rows x cols FP32 tensor whose rows are `pitch` elements apart.
+bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch, uint32_t box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * sizeof(float)};
+  cuuint64_t strides[1] = {pitch * sizeof(float)};
   cuuint32_t box[2] = {32, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
@@ -397,11 +398,11 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   wa.gam = pa.gam;
   wa.err = device_error_ptr();
   if (!wa.err) return GDR_CUDA_ERROR;
-  if (NC > 0 && (!fp32_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, CH) ||
-                 !fp32_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, DK) ||
-                 !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, CH) ||
-                 !fp32_map(&wa.qp_map, pa.qp, (uint64_t)NC * HV * CH, DK, CH) ||
-                 !fp32_map(&wa.aqk_map, pa.aqk, (uint64_t)NC * HV * CH, CH, CH)))
+  if (NC > 0 && (!fp32_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, LDT, CH) ||
+                 !fp32_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, LDS, DK) ||
+                 !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, DK, CH) ||
+                 !fp32_map(&wa.qp_map, pa.qp, (uint64_t)NC * HV * CH, DK, LDF, CH) ||
+                 !fp32_map(&wa.aqk_map, pa.aqk, (uint64_t)NC * HV * CH, CH, LDS, CH)))
     return GDR_CUDA_ERROR;
   wa.h0 = h0;
   // The state tape and Delta are only kept for a backward.
@@ -461,6 +462,8 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   wb.dstape = at<__nv_bfloat16>(scratch, L.dstape);
   wb.ddelta = at<float>(scratch, L.ddelta);
   wb.dh0 = dh0;
+  wb.err = device_error_ptr();
+  if (!wb.err) return GDR_CUDA_ERROR;
   {
     ProfScope ps("walk_bwd", stream);
     st = cuda_status(launch_walk_bwd(wb, N, walk_warps((int64_t)N * HV), stream));

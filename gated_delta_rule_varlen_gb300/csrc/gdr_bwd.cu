@@ -19,6 +19,7 @@
 // where [M (x) decay]_ij = M_ij exp(gc_i - gc_j) per channel.
 #include "gdr_chunk.cuh"
 #include "gdr_kernels.h"
+#include "gdr_tc.cuh"
 
 namespace gdr {
 
@@ -27,7 +28,10 @@ namespace gdr {
 // slice), chunks in reverse).  Each warp owns 16 value columns of dS^T.
 // Per chunk: phase 1 uses Aqk, Kd, dO (tiles of group A, double-buffered),
 // phase 2 uses Qp, w (group B, single-buffered, copied while phase 1 of the
-// same chunk runs).  The "adjoint walk" of PR #7723 "perf(cake_gdn):
+// same chunk runs).  The saved tiles are stored with their shared-memory
+// pitch and arrive as one bulk copy each on an mbarrier (waits bounded: a
+// timed-out wait ends the walk and sets the device error word); the dO
+// slice comes by cp.async.  The "adjoint walk" of PR #7723 "perf(cake_gdn):
 // prefetch offset adjoint walk, default LPT segment plan" (opening
 // description), which also loads its operands one step ahead.
 // ---------------------------------------------------------------------------
@@ -41,6 +45,7 @@ struct WalkBwdA {
 struct WalkBwdB {
   float Qp[CH * LDF];  // read with the row on the thread-in-group index
   float W[CH * LDT];   // read on rows 2t, 2t+1
+  uint64_t barA[2], barB;
 };
 
 template <int NW>
@@ -63,18 +68,22 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
   const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
   const int n = dd.nchunks;
 
-  auto issueA = [&](int s, SA& A) {  // step s processes chunk n-1-s
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&sb.barA[0], 1);
+    tc::mbar_init(&sb.barA[1], 1);
+    tc::mbar_init(&sb.barB, 1);
+    tc::mbar_fence_init();
+  }
+  __syncthreads();
+
+  auto issueA = [&](int s, SA& A, uint64_t* bar) {  // step s processes chunk n-1-s
     const int chunk = dd.chunk0 + n - 1 - s;
     const ChunkDesc cd = a.chunks[chunk];
-    const size_t toff = tile_off(chunk, h, a.HV);
-    const size_t qoff = sq_off(chunk, h, a.HV);
-    for (int e = threadIdx.x; e < CH * DK / 4; e += NTH) {
-      const int c = e >> 4, j4 = (e & 15) * 4;
-      cp_async16(&A.Kd[c * LDS + j4], &a.kd[toff + c * CH + j4]);
-    }
-    for (int e = threadIdx.x; e < CH * CH / 4; e += NTH) {
-      const int i = e >> 4, c4 = (e & 15) * 4;
-      cp_async16(&A.Aqk[i * LDS + c4], &a.aqk[qoff + i * CH + c4]);
+    if (threadIdx.x == 0) {
+      tc::mbar_arrive_expect_tx(bar, (DK * LDS + CH * LDS + DK) * 4);
+      tc::bulk_load(A.Kd, &a.kd[kd_off(chunk, h, a.HV)], DK * LDS * 4, bar);
+      tc::bulk_load(A.Aqk, &a.aqk[aqk_off(chunk, h, a.HV)], CH * LDS * 4, bar);
+      tc::bulk_load(A.gam, &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, bar);
     }
     for (int e = threadIdx.x; e < CH * NW * 2; e += NTH) {  // 16-byte pieces of 8 BF16
       const int i = e / (NW * 2), c8 = (e % (NW * 2)) * 8;
@@ -84,33 +93,38 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
         *reinterpret_cast<uint4*>(&A.dO[i * LDO + c8]) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    for (int e = threadIdx.x; e < DK / 4; e += NTH)
-      cp_async16(&A.gam[e * 4], &a.gam[((size_t)chunk * a.HV + h) * DK + e * 4]);
   };
-  auto issueB = [&](int s) {
+  auto issueB = [&](int s) {  // thread 0
     const int chunk = dd.chunk0 + n - 1 - s;
-    const size_t toff = tile_off(chunk, h, a.HV);
-    for (int e = threadIdx.x; e < CH * DK / 4; e += NTH) {
-      const int i = e >> 5, c4 = (e & 31) * 4;
-      cp_async16(&sb.Qp[i * LDF + c4], &a.qp[toff + i * DK + c4]);
-      cp_async16(&sb.W[i * LDT + c4], &a.w[toff + i * DK + c4]);
-    }
+    tc::mbar_arrive_expect_tx(&sb.barB, (CH * LDF + CH * LDT) * 4);
+    tc::bulk_load(sb.Qp, &a.qp[qp_off(chunk, h, a.HV)], CH * LDF * 4, &sb.barB);
+    tc::bulk_load(sb.W, &a.w[w_off(chunk, h, a.HV)], CH * LDT * 4, &sb.barB);
   };
 
   float S[16][4];  // dS^T rows v0+g(+8), cols c
   acc_foreach(S, [&](int r, int c, float& x) { x = a.dht ? a.dht[sidx + (size_t)c * DK + v0 + r] : 0.f; });
 
-  if (n > 0) issueA(0, sa[0]);
+  int issuedA = 0, issuedB = 0, doneA = 0, doneB = 0;
+  if (n > 0) {
+    issueA(0, sa[0], &sb.barA[0]);
+    if (threadIdx.x == 0) issueB(0);
+    issuedA = issuedB = 1;
+  }
   cp_async_commit();
-  if (n > 0) issueB(0);
-  cp_async_commit();
-  for (int s = 0; s < n; ++s) {
+  bool ok = true;
+  int s = 0;
+  for (; s < n; ++s) {
     const int chunk = dd.chunk0 + n - 1 - s;
     const size_t toff = tile_off(chunk, h, a.HV);
-    if (s + 1 < n) issueA(s + 1, sa[(s + 1) & 1]);
+    if (s + 1 < n) {  // buffer (s+1) & 1 was last read in step s-1
+      issueA(s + 1, sa[(s + 1) & 1], &sb.barA[(s + 1) & 1]);
+      issuedA = s + 2;
+    }
     cp_async_commit();
-    cp_async_wait<2>();  // group A of this step
-    __syncthreads();
+    cp_async_wait<1>();  // dO of this step
+    ok = tc::mbar_wait(&sb.barA[s & 1], (s >> 1) & 1) && ok;  // Kd, Aqk, gamma of this step
+    if (!__syncthreads_and(ok)) break;
+    doneA = s + 1;
     const SA& A = sa[s & 1];
     {  // dS^T, [v][c], as BF16 pairs
       __nv_bfloat16* tp = a.dstape + state_off(chunk, h, a.HV);
@@ -150,8 +164,9 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
       }
     }
     acc_foreach(E, [&](int r, int j, float& x) { a.ddelta[toff + (size_t)j * DK + v0 + r] = x; });
-    cp_async_wait<1>();  // group B of this step
-    __syncthreads();
+    ok = tc::mbar_wait(&sb.barB, s & 1) && ok;  // Qp, w of this step
+    if (!__syncthreads_and(ok)) break;
+    doneB = s + 1;
     // dS^T <- dS^T diag(gamma) + scale dO^T Qp - dDelta^T w
     acc_foreach(S, [&](int r, int c, float& x) { x *= A.gam[c]; });
 #pragma unroll
@@ -178,8 +193,20 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
       }
     }
     __syncthreads();
-    if (s + 1 < n) issueB(s + 1);
-    cp_async_commit();
+    if (s + 1 < n) {
+      if (threadIdx.x == 0) issueB(s + 1);
+      issuedB = s + 2;
+    }
+  }
+  cp_async_wait<0>();
+  if (s < n) {
+    // A wait ran out: record it and drain the copies still in flight.
+    if (threadIdx.x == 0) {
+      atomicExch(a.err, 4);
+      for (int q = doneA; q < issuedA; ++q) tc::mbar_wait(&sb.barA[q & 1], (q >> 1) & 1);
+      for (int q = doneB; q < issuedB; ++q) tc::mbar_wait(&sb.barB, q & 1);
+    }
+    return;
   }
   if (a.dh0) acc_foreach(S, [&](int r, int c, float& x) { a.dh0[sidx + (size_t)c * DK + v0 + r] = x; });
 }
@@ -396,7 +423,7 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
   // w and u (B operands of dA) into the staging tiles.
   for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
     const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&sg.dK[i * LDF + c4], &a.w[toff + i * DK + c4]);
+    cp_async16(&sg.dK[i * LDF + c4], &a.w[w_off(chunk, h, a.HV) + i * LDT + c4]);
     cp_async16(&sg.dG[i * LDF + c4], &a.u[toff + i * DK + c4]);
   }
   cp_async_commit();

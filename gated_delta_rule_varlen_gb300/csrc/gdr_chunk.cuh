@@ -42,7 +42,6 @@ struct ChunkSmemT {
 };
 using ChunkSmem = ChunkSmemT<float>;
 using ChunkSmemB = ChunkSmemT<uint16_t>;
-constexpr int LDF = 136;  // FP32 [64][128] tile stride for B-operand-style reads
 using ChunkSmemBB = ChunkSmemT<uint16_t, LDF>;
 
 // Loads k, q (of Q/K head hq), the gate (cumsum, base-2 scaled) and beta of
@@ -129,7 +128,7 @@ __device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restric
 // Per-channel gates use the block factorization described in gdr_common.cuh.
 // The upper channel half leaves its partial sums in s.At and s.T (free until
 // the inverse); the lower half adds them in, masks, and writes the results.
-// Aqk is stored rounded to TF32 (it is only ever an MMA operand).
+// Aqk is stored rounded to TF32 (it is only ever an MMA operand), rows LDS apart.
 template <bool VEC, typename ET, int LG>
 __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
   const int warp = threadIdx.x >> 5, I = warp & 3, hk = warp >> 2, i0 = 16 * I;
@@ -236,7 +235,7 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
           if (col == row) vK = 0.f;
         }
         s.At[row * LDS + col] = vK;
-        aqk[row * CH + col] = __uint_as_float(tf32(vQ));
+        aqk[row * LDS + col] = __uint_as_float(tf32(vQ));
       }
   }
   __syncthreads();

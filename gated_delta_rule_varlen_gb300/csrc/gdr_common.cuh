@@ -39,6 +39,7 @@ constexpr int CH = 64;     // chunk length (tokens)
 constexpr int DK = 128;    // head dimension (K = V = 128)
 constexpr int LDT = 132;   // shared-memory row stride of a [64][128] FP32 tile
 constexpr int LDS = 68;    // shared-memory row stride of a [64][64] FP32 tile
+constexpr int LDF = 136;   // [64][128] FP32 tile stride for reads with the row on the thread-in-group index
 constexpr float LOG2E = 1.4426950408889634f;
 
 // One 64-token chunk of one document.  Chunks restart at every document start.
@@ -165,5 +166,12 @@ __device__ __forceinline__ size_t sq_off(int chunk, int h, int HV) {    // [NC][
 __device__ __forceinline__ size_t state_off(int chunk, int h, int HV) { // [NC][HV][128][128]
   return ((size_t)chunk * HV + h) * (DK * DK);
 }
+// Saved tiles that the walks copy whole are kept in HBM with the padded row
+// pitch of their shared-memory copies, so that one bulk copy moves a tile:
+//   w [64][LDT],  Q Gamma [64][LDF],  Kd^T [128][LDS],  Aqk [64][LDS].
+__device__ __forceinline__ size_t w_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDT); }
+__device__ __forceinline__ size_t qp_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDF); }
+__device__ __forceinline__ size_t kd_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (DK * LDS); }
+__device__ __forceinline__ size_t aqk_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDS); }
 
 }  // namespace gdr

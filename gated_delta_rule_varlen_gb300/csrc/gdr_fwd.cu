@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5;
   load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
                          a.HV);
-  gram<VEC>(s, a.aqk + sq_off(chunk, h, a.HV));
+  gram<VEC>(s, a.aqk + aqk_off(chunk, h, a.HV));
   invert(s);
   // At and T for the backward: the values its gradient kernel needs, bit for bit.
   if (a.amat) {
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
     const int i = e >> 7, d = e & 127;
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
     const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
-    a.qp[toff + e] = __uint_as_float(tf32(s.q(i, d) * ex2(gl)));
+    a.qp[qp_off(chunk, h, a.HV) + i * LDF + d] = __uint_as_float(tf32(s.q(i, d) * ex2(gl)));
     if (i == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d] = ex2(glast);
   }
   // Kd stored transposed, [c][j] (the K-major A operand of the walk's state update).
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
     const int i = (l & 7) + 8 * (w & 7), d = 4 * (w >> 3) + (l >> 3);
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
     const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
-    a.kd[toff + d * CH + i] = __uint_as_float(tf32(s.k(i, d) * ex2(glast - gl)));
+    a.kd[kd_off(chunk, h, a.HV) + d * LDS + i] = __uint_as_float(tf32(s.k(i, d) * ex2(glast - gl)));
   }
   __syncthreads();
   // Q tile <- v rows (async), G tile <- beta * K * Gamma (B of w).
@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   {
     const int prod = warp >> 2, q = warp & 3, c0 = 64 * (q & 1);
     const int Ia = (q >> 1) ? 2 : 3, Ib = 3 - Ia;
-    float* out = prod ? a.u : a.w;
+    float* out = prod ? a.u + toff : a.w + w_off(chunk, h, a.HV);
+    const int ldo = prod ? DK : LDT;
     auto bw = [&](int j, int c) { return s.G[j * LDT + c]; };
     auto bu = [&](int j, int c) { return s.beta[j] * s.q(j, c); };
 #pragma unroll
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
           mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
                        [&](int j, int c) { return bw(j, c0 + c); });
       }
-      acc_foreach(acc, [&](int r, int c, float& x) { out[toff + (i0 + r) * DK + c0 + c] = __uint_as_float(tf32(x)); });
+      acc_foreach(acc, [&](int r, int c, float& x) { out[(i0 + r) * ldo + c0 + c] = __uint_as_float(tf32(x)); });
     }
   }
 }

@@ -19,16 +19,17 @@ struct PrepArgs {
   const void* beta;  // bf16 (KDA) or fp32 (GDN)
   const ChunkDesc* chunks;
   int Hqk, HV;
-  float *w, *u, *qp, *kd, *aqk, *gam;
+  float *w, *u, *qp, *kd, *aqk, *gam;  // w, qp, kd, aqk with the padded pitches of gdr_common.cuh
   float *amat, *tmat;  // At and T per chunk ([64][64] FP32), or null when nothing is saved
 };
 
 struct WalkArgs {
-  CUtensorMap w_map;    // w as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
-  CUtensorMap kdt_map;  // Kd^T as a 2-D FP32 tensor [NC*HV*128][64], 32 x 128 boxes, 128-byte swizzle
-  CUtensorMap u_map;    // u as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
-  CUtensorMap qp_map;   // Q Gamma as a 2-D FP32 tensor [NC*HV*64][128], 32 x 64 boxes, 128-byte swizzle
-  CUtensorMap aqk_map;  // Aqk as a 2-D FP32 tensor [NC*HV*64][64], 32 x 64 boxes, 128-byte swizzle
+  // 2-D FP32 tensor maps (rows x columns, row pitch), 32-column boxes, 128-byte swizzle:
+  CUtensorMap w_map;    // w        [NC*HV*64][128], pitch LDT, 32 x 64 boxes
+  CUtensorMap kdt_map;  // Kd^T     [NC*HV*128][64], pitch LDS, 32 x 128 boxes
+  CUtensorMap u_map;    // u        [NC*HV*64][128], pitch 128, 32 x 64 boxes
+  CUtensorMap qp_map;   // Q Gamma  [NC*HV*64][128], pitch LDF, 32 x 64 boxes
+  CUtensorMap aqk_map;  // Aqk      [NC*HV*64][64],  pitch LDS, 32 x 64 boxes
   const DocDesc* docs;
   const int* order;  // documents, longest first
   int HV;
@@ -55,6 +56,7 @@ struct WalkBwdArgs {
   __nv_bfloat16* dstape;      // dS (adjoint of each chunk's end state), BF16
   float* ddelta;              // dDelta per chunk
   float* dh0;                 // or null
+  int* err;                   // device error word
 };
 
 struct GradStateArgs {
