@@ -43,6 +43,8 @@ EXPORTED = (
     "gdr_profile_enable",
     "gdr_profile_report",
     "gdr_check_device",
+    "gdr_inject_device_error",
+    "gdr_selftest_wait",
 )
 
 _lock = threading.Lock()
@@ -60,6 +62,8 @@ _SIGS = {
     "gdr_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "gdr_profile_enable": ([ctypes.c_int], ctypes.c_int),
     "gdr_check_device": ([], ctypes.c_int),
+    "gdr_inject_device_error": ([ctypes.c_int], ctypes.c_int),
+    "gdr_selftest_wait": ([ctypes.c_uint64, P], ctypes.c_int),
     "gdr_profile_report": ([ctypes.c_char_p, SZ], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
@@ -279,3 +283,15 @@ def gdr_check_device():
     """Synchronize and raise GdrError if a kernel of the library timed out a
     bounded wait (or a CUDA error occurred) since the last check."""
     _check(load().gdr_check_device(), "gdr_check_device")
+
+
+def gdr_inject_device_error(code: int = 1):
+    """Write `code` into the device error word, as a timed-out kernel would
+    (host-side fault injection for tests of the error path)."""
+    _check(load().gdr_inject_device_error(int(code)), "gdr_inject_device_error")
+
+
+def gdr_selftest_wait(limit_ns: int, stream=None):
+    """Enqueue a kernel whose bounded wait on a barrier that nothing completes
+    runs out after limit_ns; gdr_check_device() then raises GDR_DEVICE_TIMEOUT."""
+    _check(load().gdr_selftest_wait(int(limit_ns), _stream(stream)), "gdr_selftest_wait")

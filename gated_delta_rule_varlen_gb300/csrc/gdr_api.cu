@@ -15,6 +15,7 @@
 #include "../../include/gdr.h"
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
+#include "gdr_tc.cuh"
 
 namespace gdr {
 namespace {
@@ -258,6 +259,18 @@ bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
 
 // Device error word: a kernel whose bounded wait runs out writes a non-zero
 // code here (and skips the work that depended on the wait).
+// One warp waits on a barrier that nothing completes, with the walks' bounded
+// wait; when the limit runs out the timeout is recorded in the error word.
+__global__ void k_selftest_wait(uint64_t limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_fence_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0, limit_ns)) atomicExch(err, 5);
+}
+
 static __device__ int g_device_error;
 std::mutex g_err_mu;
 int* g_err_ptr[64] = {};
@@ -660,6 +673,21 @@ gdr_status kda_fwd_noalloc(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16*
   if (!scratch) return st;
   return gdr::fwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, h0, out, ht, nullptr, 0,
                        0, scratch, gdr::kStaticScratchBytes, stream);
+}
+
+gdr_status gdr_inject_device_error(int code) {
+  if (code <= 0) return GDR_INVALID_ARG;
+  int* p = gdr::device_error_ptr();
+  if (!p) return GDR_CUDA_ERROR;
+  return cudaMemcpy(p, &code, sizeof(int), cudaMemcpyHostToDevice) == cudaSuccess ? GDR_OK : GDR_CUDA_ERROR;
+}
+
+gdr_status gdr_selftest_wait(uint64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns < 1 || limit_ns > 100000000ull) return GDR_INVALID_ARG;
+  int* p = gdr::device_error_ptr();
+  if (!p) return GDR_CUDA_ERROR;
+  gdr::k_selftest_wait<<<1, 32, 0, stream>>>(limit_ns, p);
+  return gdr::cuda_status(cudaGetLastError());
 }
 
 gdr_status gdr_check_device(void) {

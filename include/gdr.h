@@ -164,6 +164,20 @@ gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
  * times out skips the dependent work, so its outputs are then incomplete. */
 gdr_status gdr_check_device(void);
 
+/* Failure-detection diagnostics (no counterpart on the pages; they exist so
+ * that callers and tests can exercise the timeout path without faulting or
+ * hanging a GPU).
+ * gdr_inject_device_error(code): writes a non-zero `code` into the current
+ * device's error word, as a kernel whose bounded wait ran out would; the next
+ * gdr_check_device returns GDR_DEVICE_TIMEOUT.  code <= 0: GDR_INVALID_ARG.
+ * gdr_selftest_wait(limit_ns, stream): enqueues one kernel that waits, with
+ * the same bounded mbarrier wait as the walks, on a barrier that nothing
+ * completes; after limit_ns nanoseconds (1 <= limit_ns <= 1e8, else
+ * GDR_INVALID_ARG) it records the timeout in the error word and exits.
+ * Device error codes: 3 forward walk, 4 backward walk, 5 this self-test. */
+gdr_status gdr_inject_device_error(int code);
+gdr_status gdr_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
+
 /* Benchmark support (no counterpart on the pages): opt-in per-kernel timing.
  * gdr_profile_enable(1) clears previous records and makes every subsequent
  * kernel launch of this library record a pair of CUDA events on its stream;
@@ -171,7 +185,7 @@ gdr_status gdr_check_device(void);
  * recorded events and writes one line per kernel, "<name> <launches>
  * <total_ms>\n", in first-launch order, NUL-terminated, into buf; it returns
  * GDR_INVALID_ARG if buf_bytes is too small.  Kernel names: plan, prep,
- * walk_fwd, out, walk_bwd, grad_state, grad, group_reduce. */
+ * walk_fwd, walk_bwd, grad_state, grad, group_reduce. */
 int gdr_profile_enable(int on);
 gdr_status gdr_profile_report(char* buf, size_t buf_bytes);
 

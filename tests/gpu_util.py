@@ -35,12 +35,29 @@ def run_gpu(variant, x, cu, scale=SCALE, h0=None, dht=None, backward=True, want_
     dhtd = None if dht is None else dht.to(dev)
     fwd = gdr.kda_fwd if variant == "kda" else gdr.gdn_fwd
     bwd = gdr.kda_bwd if variant == "kda" else gdr.gdn_bwd
-    out, ht, saved = fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, scale, h0=h0d,
+    # Outputs and workspaces start as NaN (workspace bytes 0xFF: a NaN in FP32
+    # and BF16), so a read of memory nothing wrote shows up in the comparison.
+    T, Hqk, D = xd["q"].shape
+    HV, N = xd["v"].shape[1], len(cu) - 1
+    if variant == "kda":
+        sb, cb = gdr.kda_workspace_bytes(T, HV, cu)
+    else:
+        sb, cb = gdr.gdn_workspace_bytes(T, Hqk, HV, cu)
+    poison = lambda n: torch.full((max(int(n), 256),), 0xFF, dtype=torch.uint8, device=dev)
+    nan = float("nan")
+    out = torch.full((T, HV, D), nan, dtype=torch.bfloat16, device=dev)
+    ht = torch.full((N, HV, D, D), nan, dtype=torch.float32, device=dev)
+    out, ht, saved = fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, scale, h0=h0d, out=out, ht=ht,
+                         saved=poison(sb) if backward else None, scratch=None if backward else poison(sb),
                          save_for_bwd=backward)
     res = {"out": out, "ht": ht}
     if backward:
+        grads = {n: torch.full_like(xd[src], nan) for n, src in
+                 (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dg", "g"), ("dbeta", "beta"))}
+        if want_dh0:
+            grads["dh0"] = torch.full((N, HV, D, D), nan, dtype=torch.float32, device=dev)
         res.update(bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, scale, xd["dout"], saved, h0=h0d,
-                       dht=dhtd, want_dh0=want_dh0))
+                       dht=dhtd, want_dh0=want_dh0, scratch=poison(cb), grads=grads))
     torch.cuda.synchronize()
     gdr.gdr_check_device()  # no kernel gave up a bounded wait
     return res

@@ -154,3 +154,11 @@ def test_binding_fails_loudly_without_library(tmp_path):
             m.load(str(tmp_path / "missing.so"))
     finally:
         m._lib = saved
+
+
+def test_diagnostics_validate_arguments_before_any_cuda_call(gdr):
+    lib = gdr.load()
+    assert lib.gdr_inject_device_error(0) == gdr.GDR_INVALID_ARG
+    assert lib.gdr_inject_device_error(-3) == gdr.GDR_INVALID_ARG
+    assert lib.gdr_selftest_wait(0, None) == gdr.GDR_INVALID_ARG
+    assert lib.gdr_selftest_wait(100000001, None) == gdr.GDR_INVALID_ARG
