@@ -114,26 +114,29 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
 //                            M = 128 channels, N, K = 64 accumulating)
 //   O = Qp S0 + Aqk Delta    (M = 64 tokens, N, K = 128 + 64, reusing the
 //                            S0 and Delta operand tiles), written out as
-//                            scale * O in BF16 while the next chunk's P runs.
-// w, u and gamma arrive by TMA two chunks ahead (double buffer); Kd^T, Qp
-// and Aqk one chunk ahead (single buffer, refilled once the chunk's last
-// products are done).  Waits are bounded; a timed-out wait ends the walk for
-// the whole CTA and sets the device error word.
+//                            scale * O in BF16 during the next chunk.
+// Only P and the state update are on the chain from one chunk to the next:
+// each is committed on its own, and the two output products queue behind
+// it (Qp S0 behind P, Aqk Delta behind the update) with their own commits.
+// u and gamma arrive by TMA two chunks ahead (double buffer); w and Qp one
+// chunk ahead, refilled once P and Qp S0 are done; Kd^T and Aqk one chunk
+// ahead, refilled once Aqk Delta is done.  Waits are bounded; a timed-out
+// wait ends the walk for the whole CTA and sets the device error word.
 // The "state walk" and "output program" of PR #8638 (opening description)
 // and the walks of PR #7723 (opening description), fused.
 // ---------------------------------------------------------------------------
 template <int N>
 struct WalkTcSmem {
   static constexpr int UB = N < 32 ? 1 : N / 32;  // 32-column TMA boxes of the u slice
-  float W[2][CH * DK];      // A of P: w, rows j, K = c (four 64 x 32 column blocks)
-  float KdT[DK * CH];       // A of the update: Kd^T, rows c, K = j (two 128 x 32 column blocks)
+  float W[CH * DK];         // A of P: w, rows j, K = c (four 64 x 32 column blocks)
   float Qp[CH * DK];        // A of O: Q Gamma, rows i, K = c (four 64 x 32 column blocks)
+  float KdT[DK * CH];       // A of the update: Kd^T, rows c, K = j (two 128 x 32 column blocks)
   float Aqk[CH * CH];       // A of O: Aqk, rows i, K = j (two 64 x 32 column blocks)
   float Sop[N * DK];        // B of P and O: S0, rows v, K = c
   float Dop[N * CH];        // B of the update and O: Delta, rows v, K = j
   float U[2][CH * 32 * UB]; // u slice, rows j, 32-column swizzled blocks
   float gam[2][DK];
-  uint64_t bar_w[2], bar_k, bar_p, bar_u;
+  uint64_t bar_u2[2], bar_wq, bar_k, bar_p, bar_o1, bar_up, bar_o2;
   uint32_t tmem;
 };
 
@@ -144,8 +147,9 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   constexpr int VS = DK / N;  // CTAs per (doc, head)
   constexpr int UB = WalkTcSmem<N>::UB;
   constexpr uint32_t TCOLS = 4 * N < 32 ? 32 : 4 * N;  // S, P, O[2]
-  constexpr uint32_t W_BYTES = (CH * DK + CH * 32 * UB + DK) * 4;
-  constexpr uint32_t K_BYTES = (DK * CH + CH * DK + CH * CH) * 4;
+  constexpr uint32_t U_BYTES = (CH * 32 * UB + DK) * 4;
+  constexpr uint32_t WQ_BYTES = 2 * CH * DK * 4;
+  constexpr uint32_t K_BYTES = (DK * CH + CH * CH) * 4;
   extern __shared__ unsigned char smraw[];
   WalkTcSmem<N>& s = *reinterpret_cast<WalkTcSmem<N>*>(tc::align1024(smraw));
   const int rank = blockIdx.x / (a.HV * VS);  // all heads and slices of the longest document first
@@ -159,11 +163,14 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
 
   if (issuer) {
-    tc::mbar_init(&s.bar_w[0], 1);
-    tc::mbar_init(&s.bar_w[1], 1);
+    tc::mbar_init(&s.bar_u2[0], 1);
+    tc::mbar_init(&s.bar_u2[1], 1);
+    tc::mbar_init(&s.bar_wq, 1);
     tc::mbar_init(&s.bar_k, 1);
     tc::mbar_init(&s.bar_p, 1);
-    tc::mbar_init(&s.bar_u, 1);
+    tc::mbar_init(&s.bar_o1, 1);
+    tc::mbar_init(&s.bar_up, 1);
+    tc::mbar_init(&s.bar_o2, 1);
     tc::mbar_fence_init();
   }
   if (warp == 0) {
@@ -178,22 +185,31 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   const uint32_t tP = tS + N;                                      // P in columns [N, 2N)
   const uint32_t tO = tS + 2 * N;                                  // O[b] in columns [2N + bN, 3N + bN)
 
-  auto issue_w = [&](int m) {  // issuer only: w, u, gamma of chunk m into stage m & 1
+  // Issuer only.  Each stage's copies of chunk m land on its barrier.
+  auto issue_u = [&](int m) {  // u slice and gamma, double-buffered
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     const int item = chunk * a.HV + h;
-    tc::mbar_arrive_expect_tx(&s.bar_w[b], W_BYTES);
-    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(&s.W[b][kb * CH * 32], &a.w_map, kb * 32, item * CH, &s.bar_w[b]);
+    tc::mbar_arrive_expect_tx(&s.bar_u2[b], U_BYTES);
     for (int ub = 0; ub < UB; ++ub)
-      tc::tma_load_2d(&s.U[b][ub * CH * 32], &a.u_map, v0 + 32 * ub, item * CH, &s.bar_w[b]);
-    tc::bulk_load(s.gam[b], &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, &s.bar_w[b]);
+      tc::tma_load_2d(&s.U[b][ub * CH * 32], &a.u_map, v0 + 32 * ub, item * CH, &s.bar_u2[b]);
+    tc::bulk_load(s.gam[b], &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, &s.bar_u2[b]);
   };
-  auto issue_k = [&](int m) {  // issuer only: Kd^T, Qp, Aqk of chunk m
+  auto issue_wq = [&](int m) {  // w and Q Gamma
+    const int item = (dd.chunk0 + m) * a.HV + h;
+    tc::mbar_arrive_expect_tx(&s.bar_wq, WQ_BYTES);
+    for (int kb = 0; kb < 4; ++kb) {
+      tc::tma_load_2d(&s.W[kb * CH * 32], &a.w_map, kb * 32, item * CH, &s.bar_wq);
+      tc::tma_load_2d(&s.Qp[kb * CH * 32], &a.qp_map, kb * 32, item * CH, &s.bar_wq);
+    }
+  };
+  auto issue_k = [&](int m) {  // Kd^T and Aqk
     const int item = (dd.chunk0 + m) * a.HV + h;
     tc::mbar_arrive_expect_tx(&s.bar_k, K_BYTES);
-    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(&s.KdT[kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_k);
-    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(&s.Qp[kb * CH * 32], &a.qp_map, kb * 32, item * CH, &s.bar_k);
-    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(&s.Aqk[kb * CH * 32], &a.aqk_map, kb * 32, item * CH, &s.bar_k);
+    for (int kb = 0; kb < 2; ++kb) {
+      tc::tma_load_2d(&s.KdT[kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_k);
+      tc::tma_load_2d(&s.Aqk[kb * CH * 32], &a.aqk_map, kb * 32, item * CH, &s.bar_k);
+    }
   };
   // scale * O of chunk m (TMEM buffer m & 1) -> out, rows below the chunk's length.
   auto write_out = [&](int m) {  // data warps only
@@ -216,6 +232,9 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
       }
     }
   };
+  auto kstep = [](uint64_t desc, int k, int rows) {  // K = 8 step k of a K-major SW128 operand
+    return desc + (uint64_t)((((k >> 2) * rows * 128) + (k & 3) * 32) >> 4);
+  };
 
   if (tid < DK) {  // S <- h0 (or 0)
 #pragma unroll
@@ -228,10 +247,13 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
     }
     tc::tmem_wait_st();
   }
-  int issued_w = 0, issued_k = 0, waited_k = 0;
-  if (issuer) {
-    if (n > 0) issue_w(0), issue_k(0), ++issued_w, ++issued_k;
-    if (n > 1) issue_w(1), ++issued_w;
+  // Copies and output products issued / waited for (issuer), for the drain after a timeout.
+  int iss_u = 0, iss_wq = 0, iss_k = 0, got_wq = 0, got_k = 0, o1_iss = 0, o1_done = 0, o2_iss = 0, o2_done = 0;
+  if (issuer && n > 0) {
+    issue_u(0), ++iss_u;
+    if (n > 1) issue_u(1), ++iss_u;
+    issue_wq(0), ++iss_wq;
+    issue_k(0), ++iss_k;
   }
   constexpr uint32_t idP = tc::idesc_tf32(CH, N), idU = tc::idesc_tf32(DK, N);
   unsigned char* sop = reinterpret_cast<unsigned char*>(s.Sop);
@@ -242,7 +264,18 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     const size_t toff = tile_off(chunk, h, a.HV);
-    if (tid < DK) ok = tc::mbar_wait(&s.bar_w[b], (m >> 1) & 1) && ok;
+    if (tid < DK) ok = tc::mbar_wait(&s.bar_u2[b], (m >> 1) & 1) && ok;
+    if (issuer) {
+      if (m > 0) {  // Kd^T and Aqk are free once the previous O += Aqk Delta is done
+        const bool r = tc::mbar_wait(&s.bar_o2, (m - 1) & 1);
+        ok = r && ok;
+        o2_done += r;
+        if (r) issue_k(m), ++iss_k;
+      }
+      const bool r = tc::mbar_wait(&s.bar_wq, m & 1);
+      ok = r && ok;
+      got_wq += r;
+    }
     tc::tc_fence_before();
     if (!__syncthreads_and(ok)) break;
     tc::tc_fence_after();
@@ -261,12 +294,16 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
     __syncthreads();
     tc::tc_fence_after();
     if (issuer) {
-      const uint64_t aw = tc::desc_k_sw128(s.W[b]), bs = tc::desc_k_sw128(s.Sop);
+      // P = w S0 (committed alone: the chain waits on it), then O = Qp S0.
+      const uint64_t aw = tc::desc_k_sw128(s.W), aq = tc::desc_k_sw128(s.Qp), bs = tc::desc_k_sw128(s.Sop);
+#pragma unroll
+      for (int k = 0; k < DK / 8; ++k) tc::mma_tf32(tmem + N, kstep(aw, k, CH), kstep(bs, k, N), idP, k > 0);
+      tc::mma_commit(&s.bar_p);
 #pragma unroll
       for (int k = 0; k < DK / 8; ++k)
-        tc::mma_tf32(tmem + N, aw + (uint64_t)((((k >> 2) * CH * 128) + (k & 3) * 32) >> 4),
-                     bs + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idP, k > 0);
-      tc::mma_commit(&s.bar_p);
+        tc::mma_tf32(tmem + 2 * N + b * N, kstep(aq, k, CH), kstep(bs, k, N), idP, k > 0);
+      tc::mma_commit(&s.bar_o1);
+      ++o1_iss;
     }
     if (tid < DK) {
       // While P runs: the tape row, diag(gamma) S0 back into TMEM (columns P
@@ -289,7 +326,11 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
 #pragma unroll
       for (int cb = 0; cb < N; cb += 16) tc::tmem_st16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&sr[cb]));
       tc::tmem_wait_st();
-      if (m > 0) write_out(m - 1);
+      if (m > 0) {
+        ok = tc::mbar_wait(&s.bar_o2, (m - 1) & 1) && ok;  // O of the previous chunk is complete
+        tc::tc_fence_after();
+        write_out(m - 1);
+      }
       ok = tc::mbar_wait(&s.bar_p, m & 1) && ok;
       tc::tc_fence_after();
       // Delta = u - P over the 16-row block of this warp, spread over all 32 lanes:
@@ -316,52 +357,57 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
         }
       }
       tc::fence_proxy_async();
+    } else if (issuer) {
+      // w and Q Gamma are free once P and Qp S0 are done: fetch the next chunk's.
+      const bool r = tc::mbar_wait(&s.bar_o1, m & 1);
+      ok = r && ok;
+      o1_done += r;
+      if (r && m + 1 < n) issue_wq(m + 1), ++iss_wq;
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     if (issuer) {
+      // The state update (committed alone), then O += Aqk Delta.
       const bool kready = tc::mbar_wait(&s.bar_k, m & 1);
       ok = kready && ok;
       if (kready) {
-        ++waited_k;
+        ++got_k;
         const uint64_t ak = tc::desc_k_sw128(s.KdT), bd = tc::desc_k_sw128(s.Dop);
-        const uint64_t aq = tc::desc_k_sw128(s.Qp), bs = tc::desc_k_sw128(s.Sop);
-        const uint64_t aa = tc::desc_k_sw128(s.Aqk);
-        const uint32_t dO = tmem + 2 * N + b * N;
 #pragma unroll
-        for (int k = 0; k < CH / 8; ++k)
-          tc::mma_tf32(tmem, ak + (uint64_t)((((k >> 2) * DK * 128) + (k & 3) * 32) >> 4),
-                       bd + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idU, 1);
-#pragma unroll
-        for (int k = 0; k < DK / 8; ++k)
-          tc::mma_tf32(dO, aq + (uint64_t)((((k >> 2) * CH * 128) + (k & 3) * 32) >> 4),
-                       bs + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idP, k > 0);
-#pragma unroll
-        for (int k = 0; k < CH / 8; ++k)
-          tc::mma_tf32(dO, aa + (uint64_t)((((k >> 2) * CH * 128) + (k & 3) * 32) >> 4),
-                       bd + (uint64_t)((((k >> 2) * N * 128) + (k & 3) * 32) >> 4), idP, 1);
+        for (int k = 0; k < CH / 8; ++k) tc::mma_tf32(tmem, kstep(ak, k, DK), kstep(bd, k, N), idU, 1);
       }
-      tc::mma_commit(&s.bar_u);
+      tc::mma_commit(&s.bar_up);
+      if (kready) {
+        const uint64_t aa = tc::desc_k_sw128(s.Aqk), bd = tc::desc_k_sw128(s.Dop);
+#pragma unroll
+        for (int k = 0; k < CH / 8; ++k) tc::mma_tf32(tmem + 2 * N + b * N, kstep(aa, k, CH), kstep(bd, k, N), idP, 1);
+      }
+      tc::mma_commit(&s.bar_o2);
+      ++o2_iss;
     }
-    // Everyone (the issuer to refill the buffers, the data warps before
-    // reading S) waits for the update and O.
-    if (tid < DK || issuer) ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
+    // The data warps wait for the state update before reading S; the issuer
+    // too, before refilling the u stage.
+    if (tid < DK || issuer) ok = tc::mbar_wait(&s.bar_up, m & 1) && ok;
     tc::tc_fence_after();
-    if (issuer && ok) {
-      if (m + 2 < n) issue_w(m + 2), ++issued_w;
-      if (m + 1 < n) issue_k(m + 1), ++issued_k;
-    }
+    if (issuer && ok && m + 2 < n) issue_u(m + 2), ++iss_u;
   }
   if (m < n) {
-    // A wait ran out: record it and drain the copies still in flight.
+    // A wait ran out: record it and drain the copies and products still in flight.
     if (issuer) {
       atomicExch(a.err, 3);
-      for (int q = m; q < issued_w; ++q) tc::mbar_wait(&s.bar_w[q & 1], (q >> 1) & 1);
-      for (int q = waited_k; q < issued_k; ++q) tc::mbar_wait(&s.bar_k, q & 1);
+      for (int q = m; q < iss_u; ++q) tc::mbar_wait(&s.bar_u2[q & 1], (q >> 1) & 1);
+      for (int q = got_wq; q < iss_wq; ++q) tc::mbar_wait(&s.bar_wq, q & 1);
+      for (int q = got_k; q < iss_k; ++q) tc::mbar_wait(&s.bar_k, q & 1);
+      for (int q = o1_done; q < o1_iss; ++q) tc::mbar_wait(&s.bar_o1, q & 1);
+      for (int q = o2_done; q < o2_iss; ++q) tc::mbar_wait(&s.bar_o2, q & 1);
     }
   } else if (tid < DK) {
-    if (n > 0) write_out(n - 1);
+    if (n > 0) {
+      ok = tc::mbar_wait(&s.bar_o2, (n - 1) & 1) && ok;
+      tc::tc_fence_after();
+      if (ok) write_out(n - 1);
+    }
     if (a.ht) {
 #pragma unroll
       for (int cb = 0; cb < N; cb += 16) {
@@ -372,6 +418,7 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
         for (int q = 0; q < 16; ++q) a.ht[sidx + (size_t)tid * DK + v0 + cb + q] = __uint_as_float(r[q]);
       }
     }
+    if (!ok) atomicExch(a.err, 3);
   }
   tc::tc_fence_before();
   __syncthreads();
