@@ -244,7 +244,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // A row-major FP32 matrix [rows][cols] read in boxes of 32 columns (128 bytes,
 // 128-byte swizzle) x box_rows rows.
-// rows x cols FP32 tensor whose rows are `pitch` elements apart.
+// rows x cols FP32 tensor whose rows are `pitch` elements apart; boxes of 32 x box_rows.
 bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch, uint32_t box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
@@ -253,6 +253,19 @@ bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
   cuuint32_t box[2] = {32, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// rows x cols dense BF16 tensor; boxes of 64 x box_rows.
+bool bf16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -497,6 +510,8 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   gs.dkd = at<float>(scratch, L.dkd);
   gs.dgam = at<float>(scratch, L.dgam);
   gs.daqk = at<float>(scratch, L.daqk);
+  gs.err = wb.err;
+  if (NC > 0 && !bf16_map(&gs.s0_map, gs.tape, (uint64_t)NC * HV * DK, DK, DK)) return GDR_CUDA_ERROR;
   {
     ProfScope ps("grad_state", stream);
     st = cuda_status(launch_grad_state(gs, (int)NC, stream));

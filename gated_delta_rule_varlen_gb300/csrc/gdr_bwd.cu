@@ -212,121 +212,221 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// State-side products (one CTA of 8 warps per (chunk, value head)):
+// State-side products on the tensor cores (one CTA of 8 warps per (chunk,
+// value head)):
 //   dqs = scale dO S0^T,  dw = -dDelta S0^T,  dKd = Delta dS^T,
-//   dgam[c] = sum_v dS[c][v] S0[c][v].
-// Warp w: rows 16 (w % 4), columns 64 (w / 4).  Operands staged in shared
-// memory with cp.async in two groups (S0, dO, dDelta first; dS, Delta second).
+//   dAqk = scale tril(dO Delta^T),  dgam[c] = sum_v dS[c][v] S0[c][v].
+// tcgen05.mma kind::f16 (BF16 operands, FP32 accumulators in TMEM, M = 64
+// tokens).  dO and the two state tapes are BF16 already; Delta and dDelta are
+// FP32 and enter as a BF16 pair hi + lo (hi = bf16(x), lo = bf16(x - hi),
+// about 16 significant bits), so each of their products is two MMAs.  The S0
+// tape arrives by TMA; the dS tape (stored dS^T[v][c]) is transposed into a
+// K-major tile by the warps while the first products run.
 // ---------------------------------------------------------------------------
-constexpr int LDB = DK + 8;  // row stride (elements) of a [128][128] BF16 shared tile
 struct GradStateSmem {
-  uint16_t S0[DK * LDB];
-  uint16_t dS[DK * LDB];
-  uint16_t dO[CH * LDB];
-  float Dl[CH * LDT];
-  float dDl[CH * LDT];
+  uint16_t S0[2 * DK * 64];   // B: S0 [c][v]; two 64-column 128B-swizzled blocks
+  uint16_t dSB[2 * DK * 64];  // B: dS [c][v]
+  uint16_t dO[2 * CH * 64];   // A: dO [i][v]
+  uint16_t Dh[2 * CH * 64];   // Delta hi [i][v] (A of dKd, B of dAqk)
+  uint16_t Dl[2 * CH * 64];   // Delta lo
+  uint16_t Eh[2 * CH * 64];   // dDelta hi [i][v] (A of dw)
+  uint16_t El[2 * CH * 64];   // dDelta lo
+  uint16_t dST[DK * DK];      // the dS tape as stored, dS^T [v][c]
+  uint64_t bar_s0, bar_m1, bar_m2;
+  uint32_t tmem;
 };
 
-__global__ void __launch_bounds__(256) k_grad_state(GradStateArgs a) {
-  extern __shared__ __align__(16) unsigned char smraw[];
-  GradStateSmem& s = *reinterpret_cast<GradStateSmem*>(smraw);
+__global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ GradStateArgs a) {
+  extern __shared__ unsigned char smraw[];
+  GradStateSmem& s = *reinterpret_cast<GradStateSmem*>(tc::align1024(smraw));
   const int chunk = blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
-  const int warp = threadIdx.x >> 5, I = warp & 3, i0 = 16 * I, n0 = (warp >> 2) * 64;
-  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   const size_t toff = tile_off(chunk, h, a.HV);
-  const __nv_bfloat16* S0 = a.tape + state_off(chunk, h, a.HV);
+  constexpr uint32_t TCOLS = 512;  // dq [0,128), dw [128,256), dKd [256,384), dAqk [384,448)
   const __nv_bfloat16* dS = a.dstape + state_off(chunk, h, a.HV);
-  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // S0 rows [c][v]
-    const int c = e >> 4, v8 = (e & 15) * 8;
-    cp_async16(&s.S0[c * LDB + v8], &S0[c * DK + v8]);
+
+  if (tid == 0) {
+    tc::mbar_init(&s.bar_s0, 1);
+    tc::mbar_init(&s.bar_m1, 1);
+    tc::mbar_init(&s.bar_m2, 1);
+    tc::mbar_fence_init();
+    tc::mbar_arrive_expect_tx(&s.bar_s0, DK * DK * 2);
+    const int row = (chunk * a.HV + h) * DK;
+    tc::tma_load_2d(&s.S0[0], &a.s0_map, 0, row, &s.bar_s0);
+    tc::tma_load_2d(&s.S0[DK * 64], &a.s0_map, 64, row, &s.bar_s0);
   }
-  for (int e = threadIdx.x; e < CH * DK / 8; e += 256) {
-    const int i = e >> 4, v8 = (e & 15) * 8;
+  if (warp == 0) {
+    tc::tmem_alloc(&s.tmem, TCOLS);
+    tc::tmem_relinquish();
+  }
+  unsigned char* sdO = reinterpret_cast<unsigned char*>(s.dO);
+  // dO rows (zero beyond the chunk) into the swizzled A tile; the dS tape as stored.
+  for (int e = tid; e < CH * 16; e += 256) {
+    const int i = e >> 4, kc = e & 15;
+    void* dst = sdO + tc::sw128_bf16_piece(i, kc, CH);
     if (i < cd.len)
-      cp_async16(&s.dO[i * LDB + v8], &a.dout[((size_t)(cd.tok0 + i) * a.HV + h) * DK + v8]);
+      cp_async16(dst, &a.dout[((size_t)(cd.tok0 + i) * a.HV + h) * DK + kc * 8]);
     else
-      *reinterpret_cast<uint4*>(&s.dO[i * LDB + v8]) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
   }
-  for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
-    const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&s.dDl[i * LDT + c4], &a.ddelta[toff + i * DK + c4]);
-  }
+  for (int e = tid; e < DK * 16; e += 256) cp_async16(&s.dST[e * 8], &dS[e * 8]);
   cp_async_commit();
-  for (int e = threadIdx.x; e < DK * DK / 8; e += 256) {  // dS^T rows [v][c]
-    const int v = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(&s.dS[v * LDB + c8], &dS[v * DK + c8]);
-  }
-  for (int e = threadIdx.x; e < CH * DK / 4; e += 256) {
-    const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&s.Dl[i * LDT + c4], &a.delta[toff + i * DK + c4]);
-  }
-  cp_async_commit();
-  cp_async_wait<1>();
-  __syncthreads();
+  // Delta and dDelta -> BF16 hi / lo tiles.  Task e: tensor e / 1024, row (e / 16) % 64, piece e % 16.
   {
-    float dq[8][4], dw[8][4];
-    zero_acc(dq);
-    zero_acc(dw);
-    for (int kk = 0; kk < 16; ++kk) {
-      const int va = kk * 8 + t, vb = va + 4;
-      const int r0 = i0 + g, r1 = i0 + g + 8;
-      uint32_t aO[4] = {(uint32_t)s.dO[r0 * LDB + va] << 16, (uint32_t)s.dO[r1 * LDB + va] << 16,
-                        (uint32_t)s.dO[r0 * LDB + vb] << 16, (uint32_t)s.dO[r1 * LDB + vb] << 16};
-      uint32_t aD[4] = {tf32(s.dDl[r0 * LDT + va]), tf32(s.dDl[r1 * LDT + va]), tf32(s.dDl[r0 * LDT + vb]),
-                        tf32(s.dDl[r1 * LDT + vb])};
+    float4 x[8][2];
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int c = n0 + nt * 8 + g;
-        uint32_t b[2] = {(uint32_t)s.S0[c * LDB + va] << 16, (uint32_t)s.S0[c * LDB + vb] << 16};
-        mma8(dq[nt], aO, b);
-        mma8(dw[nt], aD, b);
-      }
+    for (int q = 0; q < 8; ++q) {
+      const int e = tid + 256 * q;
+      const float* src = (e < 1024 ? a.delta : a.ddelta) + toff + (size_t)((e >> 4) & 63) * DK + (e & 15) * 8;
+      x[q][0] = __ldg(reinterpret_cast<const float4*>(src));
+      x[q][1] = __ldg(reinterpret_cast<const float4*>(src) + 1);
     }
-    acc_foreach(dq, [&](int r, int c, float& x) { a.dqs[toff + (i0 + r) * DK + n0 + c] = a.scale * x; });
-    acc_foreach(dw, [&](int r, int c, float& x) { a.dw[toff + (i0 + r) * DK + n0 + c] = -x; });
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = tid + 256 * q;
+      const int i = (e >> 4) & 63, kc = e & 15;
+      const float f[8] = {x[q][0].x, x[q][0].y, x[q][0].z, x[q][0].w, x[q][1].x, x[q][1].y, x[q][1].z, x[q][1].w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * p]), h1 = __float2bfloat16_rn(f[2 * p + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(f[2 * p] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(f[2 * p + 1] - __bfloat162float(h1));
+        hi[p] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lo[p] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      const uint32_t off = tc::sw128_bf16_piece(i, kc, CH);
+      unsigned char* th = reinterpret_cast<unsigned char*>(e < 1024 ? s.Dh : s.Eh);
+      unsigned char* tl = reinterpret_cast<unsigned char*>(e < 1024 ? s.Dl : s.El);
+      *reinterpret_cast<uint4*>(th + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(tl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
   }
   cp_async_wait<0>();
-  __syncthreads();
-  {
-    float acc[8][4];
-    zero_acc(acc);
-    for (int kk = 0; kk < 16; ++kk)
-      mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int v) { return s.Dl[(i0 + i) * LDT + v]; },
-                   [&](int v, int c) { return bfbits2f(s.dS[v * LDB + n0 + c]); });
-    acc_foreach(acc, [&](int r, int c, float& x) { a.dkd[toff + (i0 + r) * DK + n0 + c] = x; });
-  }
-  {  // dAqk = scale tril(dO Delta^T): this warp's rows, columns j in [32 (w / 4), +32)
-    const int jt0 = (warp >> 2) * 4;
-    float acc[4][4];
-    zero_acc(acc);
-    for (int kk = 0; kk < 16; ++kk) {
-      const int va = kk * 8 + t, vb = va + 4;
-      const int r0 = i0 + g, r1 = i0 + g + 8;
-      uint32_t aO[4] = {(uint32_t)s.dO[r0 * LDB + va] << 16, (uint32_t)s.dO[r1 * LDB + va] << 16,
-                        (uint32_t)s.dO[r0 * LDB + vb] << 16, (uint32_t)s.dO[r1 * LDB + vb] << 16};
+  tc::fence_proxy_async();
+  bool ok = tc::mbar_wait(&s.bar_s0, 0);
+  tc::tc_fence_before();
+  ok = __syncthreads_and(ok);
+  tc::tc_fence_after();
+  const uint32_t tmem = s.tmem;
+  constexpr uint32_t id128 = tc::idesc_bf16(CH, DK), id64 = tc::idesc_bf16(CH, CH);
+  if (ok && tid == 0) {
+    const uint64_t aO = tc::desc_k_sw128(s.dO), bS0 = tc::desc_k_sw128(s.S0);
+    const uint64_t aEh = tc::desc_k_sw128(s.Eh), aEl = tc::desc_k_sw128(s.El);
+    const uint64_t bDh = tc::desc_k_sw128(s.Dh), bDl = tc::desc_k_sw128(s.Dl);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        if (jt0 + nt < 2 * I + 2) {
-          const int j = (jt0 + nt) * 8 + g;
-          uint32_t b[2] = {tf32(s.Dl[j * LDT + va]), tf32(s.Dl[j * LDT + vb])};
-          mma8(acc[nt], aO, b);
-        }
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem, tc::kstep32(aO, k, CH), tc::kstep32(bS0, k, DK), id128, k > 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aEh, k, CH), tc::kstep32(bS0, k, DK), id128, k > 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aEl, k, CH), tc::kstep32(bS0, k, DK), id128, 1);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 384, tc::kstep32(aO, k, CH), tc::kstep32(bDh, k, CH), id64, k > 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 384, tc::kstep32(aO, k, CH), tc::kstep32(bDl, k, CH), id64, 1);
+    tc::mma_commit(&s.bar_m1);
+  }
+  // While those run: dS^T [v][c] -> the K-major B tile dS [c][v]; task: channel c, piece kc.
+  {
+    unsigned char* sdS = reinterpret_cast<unsigned char*>(s.dSB);
+#pragma unroll 2
+    for (int q = 0; q < 8; ++q) {
+      const int e = tid + 256 * q;
+      const int c = e & 127, kc = e >> 7;
+      uint32_t w[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        w[p] = (uint32_t)s.dST[(kc * 8 + 2 * p) * DK + c] | ((uint32_t)s.dST[(kc * 8 + 2 * p + 1) * DK + c] << 16);
+      *reinterpret_cast<uint4*>(sdS + tc::sw128_bf16_piece(c, kc, DK)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  tc::fence_proxy_async();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (ok && tid == 0) {
+    const uint64_t aDh = tc::desc_k_sw128(s.Dh), aDl = tc::desc_k_sw128(s.Dl), bdS = tc::desc_k_sw128(s.dSB);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 256, tc::kstep32(aDh, k, CH), tc::kstep32(bdS, k, DK), id128, k > 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 256, tc::kstep32(aDl, k, CH), tc::kstep32(bdS, k, DK), id128, 1);
+    tc::mma_commit(&s.bar_m2);
+  }
+  if (tid < DK) {  // dgam[c] = sum_v S0[c][v] dS[c][v], both tiles [c][v]
+    const int c = tid;
+    const unsigned char* p0 = reinterpret_cast<const unsigned char*>(s.S0);
+    const unsigned char* p1 = reinterpret_cast<const unsigned char*>(s.dSB);
+    float sum = 0.f;
+#pragma unroll 4
+    for (int kc = 0; kc < 16; ++kc) {
+      const uint32_t off = tc::sw128_bf16_piece(c, kc, DK);
+      const uint4 x = *reinterpret_cast<const uint4*>(p0 + off);
+      const uint4 y = *reinterpret_cast<const uint4*>(p1 + off);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        sum += __uint_as_float(xs[p] << 16) * __uint_as_float(ys[p] << 16);
+        sum += __uint_as_float(xs[p] & 0xffff0000u) * __uint_as_float(ys[p] & 0xffff0000u);
       }
     }
-    float* daqk = a.daqk + sq_off(chunk, h, a.HV);
-    acc_foreach(acc, [&](int r, int col, float& x) {
-      const int i = i0 + r, j = jt0 * 8 + col;
-      daqk[i * CH + j] = j <= i ? a.scale * x : 0.f;
-    });
-  }
-  if (threadIdx.x < DK) {  // dgam[c] = sum_v S0[c][v] dS[c][v]  (S0 tile [c][v], dS tile [v][c])
-    const int c = threadIdx.x;
-    float sum = 0.f;
-#pragma unroll 8
-    for (int v = 0; v < DK; ++v) sum += bfbits2f(s.S0[c * LDB + v]) * bfbits2f(s.dS[v * LDB + c]);
     a.dgam[((size_t)chunk * a.HV + h) * DK + c] = sum;
   }
+  // Epilogue: warp w reads the rows of TMEM lane quadrant w % 4 (tokens 16 (w % 4) ..)
+  // and half w / 4 of the columns.
+  const int quad = warp & 3, hf = warp >> 2, g = lane >> 2, u2 = (lane & 3) * 2;
+  const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
+  auto drain = [&](uint32_t col0, int ncols, auto&& store) {  // ncols multiple of 16
+    for (int cb = 0; cb < ncols; cb += 16) {
+      uint32_t r[8];
+      tc::tmem_ld16x256b_x2(tq + col0 + cb, r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+          store(16 * quad + g + 8 * hr, cb + 8 * q + u2, __uint_as_float(r[4 * q + 2 * hr]),
+                __uint_as_float(r[4 * q + 2 * hr + 1]));
+    }
+  };
+  const bool ok1 = __syncthreads_and(ok && tc::mbar_wait(&s.bar_m1, 0));  // uniform: the loads below are warp-wide
+  tc::tc_fence_after();
+  if (ok1) {
+    const int c0 = 64 * hf;
+    drain(c0, 64, [&](int i, int c, float x0, float x1) {
+      *reinterpret_cast<float2*>(&a.dqs[toff + i * DK + c0 + c]) = make_float2(a.scale * x0, a.scale * x1);
+    });
+    drain(128 + c0, 64, [&](int i, int c, float x0, float x1) {
+      *reinterpret_cast<float2*>(&a.dw[toff + i * DK + c0 + c]) = make_float2(-x0, -x1);
+    });
+    float* daqk = a.daqk + sq_off(chunk, h, a.HV);
+    const int j0 = 32 * hf;
+    drain(384 + j0, 32, [&](int i, int c, float x0, float x1) {
+      const int j = j0 + c;
+      *reinterpret_cast<float2*>(&daqk[i * CH + j]) =
+          make_float2(j <= i ? a.scale * x0 : 0.f, j + 1 <= i ? a.scale * x1 : 0.f);
+    });
+  }
+  const bool ok2 = __syncthreads_and(ok && tc::mbar_wait(&s.bar_m2, 0));
+  tc::tc_fence_after();
+  if (ok2) {
+    const int c0 = 64 * hf;
+    drain(256 + c0, 64, [&](int i, int c, float x0, float x1) {
+      *reinterpret_cast<float2*>(&a.dkd[toff + i * DK + c0 + c]) = make_float2(x0, x1);
+    });
+  }
+  if (tid == 0 && !(ok1 && ok2)) {
+    // A wait ran out: record it and let the copies and products in flight finish.
+    atomicExch(a.err, 6);
+    tc::mbar_wait(&s.bar_s0, 0);
+    if (ok) {
+      tc::mbar_wait(&s.bar_m1, 0);
+      tc::mbar_wait(&s.bar_m2, 0);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -712,7 +812,7 @@ cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, 
 
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st) {
   if (nchunks == 0) return cudaSuccess;
-  const size_t sm = sizeof(GradStateSmem);
+  const size_t sm = sizeof(GradStateSmem) + 1024;
   cudaFuncSetAttribute(k_grad_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   k_grad_state<<<dim3(nchunks, a.HV), 256, sm, st>>>(a);
   return cudaGetLastError();

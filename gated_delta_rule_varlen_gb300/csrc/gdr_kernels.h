@@ -60,6 +60,7 @@ struct WalkBwdArgs {
 };
 
 struct GradStateArgs {
+  CUtensorMap s0_map;  // S0 tape as a 2-D BF16 tensor [NC*HV*128][128], 64 x 128 boxes, 128-byte swizzle
   const ChunkDesc* chunks;
   int HV;
   float scale;
@@ -68,6 +69,7 @@ struct GradStateArgs {
   const float *delta, *ddelta;
   float *dqs, *dw, *dkd, *dgam;  // scratch outputs
   float* daqk;                   // scale * tril(dO Delta^T), [NC][HV][64][64]
+  int* err;                      // device error word
 };
 
 struct GradArgs {

@@ -114,12 +114,27 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f16 with BF16 A and B, FP32 accumulator,
+// both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // ---- MMA --------------------------------------------------------------------
 // D[tmem] (+)= A[smem] * B[smem]^T for one K = 8 step (TF32).  Issued by one thread.
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T for one K = 16 step (BF16).  Issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
@@ -160,6 +175,17 @@ __device__ __forceinline__ void tmem_ld16x256b_x2(uint32_t taddr, uint32_t (&r)[
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
+// Byte offset of the 16-byte piece kc (elements 8 kc .. 8 kc + 7) of row r
+// inside a K-major 128B-swizzled BF16 operand of R rows and K = 128 (two
+// column blocks of R x 128 B).
+__host__ __device__ constexpr uint32_t sw128_bf16_piece(int r, int kc, int R) {
+  return (uint32_t)((kc >> 3) * R * 128 + r * 128 + (((kc & 7) ^ (r & 7)) << 4));
+}
+// Advances a K-major SW128 descriptor to K step k (32 bytes of K per step; four
+// steps per 128-byte column block of `rows` rows).
+__host__ __device__ constexpr uint64_t kstep32(uint64_t desc, int k, int rows) {
+  return desc + (uint64_t)((((k >> 2) * rows * 128) + (k & 3) * 32) >> 4);
+}
 // Byte offset of FP32 element (r, k) inside a K-major 128B-swizzled operand
 // of R rows and K = 128 (four column blocks of R x 128 B).
 __host__ __device__ constexpr uint32_t sw128_offset(int r, int k, int R) {
