@@ -334,8 +334,8 @@ def main():
     if not args.no_e2e:
         names_in = ("q", "k", "v", "g", "beta", "dout")
         host_in = {k: x[k].cpu().pin_memory() for k in names_in}
-        dev_in = [{k: torch.empty_like(x[k]) for k in names_in} for _ in range(2)]
-        dev_out = [{"out": torch.empty_like(out), **{k: torch.empty_like(v) for k, v in grads.items()}}, None]
+        dev_in = [{k: x[k] for k in names_in}, {k: torch.empty_like(x[k]) for k in names_in}]
+        dev_out = [{"out": out, **grads}, None]
         dev_out[1] = {k: torch.empty_like(v) for k, v in dev_out[0].items()}
         host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in dev_out[0].items()}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())

@@ -201,13 +201,11 @@ def _bwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, sa
         sb, cb = gdn_workspace_bytes(T, Hqk, HV, arr)
     dev = q.device
     grads = dict(grads or {})
-    grads.setdefault("dq", torch.empty_like(q))
-    grads.setdefault("dk", torch.empty_like(k))
-    grads.setdefault("dv", torch.empty_like(v))
-    grads.setdefault("dg", torch.empty_like(g))
-    grads.setdefault("dbeta", torch.empty_like(beta))
-    if want_dh0:
-        grads.setdefault("dh0", torch.empty((N, HV, D, D), dtype=torch.float32, device=dev))
+    for name, like in (("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta)):
+        if name not in grads:  # allocate only what the caller did not pass
+            grads[name] = torch.empty_like(like)
+    if want_dh0 and "dh0" not in grads:
+        grads["dh0"] = torch.empty((N, HV, D, D), dtype=torch.float32, device=dev)
     if scratch is None:
         scratch = _empty_bytes(cb, dev)
     lib = load()
