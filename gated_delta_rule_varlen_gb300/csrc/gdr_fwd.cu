@@ -116,11 +116,14 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
 //                            S0 and Delta operand tiles), written out as
 //                            scale * O in BF16 during the next chunk.
 // Only P and the state update are on the chain from one chunk to the next:
-// each is committed on its own, and the two output products queue behind
-// it (Qp S0 behind P, Aqk Delta behind the update) with their own commits.
-// u and gamma arrive by TMA two chunks ahead (double buffer); w and Qp one
-// chunk ahead, refilled once P and Qp S0 are done; Kd^T and Aqk one chunk
-// ahead, refilled once Aqk Delta is done.  Waits are bounded; a timed-out
+// each is committed on its own.  Qp S0 queues behind P; Aqk Delta of a chunk
+// is issued at the head of the next chunk's first batch (ahead of P, which
+// is needed later than it is ready), so the state update is the only
+// product between forming Delta and the next chunk.
+// w, Qp, Kd^T and Aqk of the next chunk are fetched by TMA as soon as this
+// chunk's P and Qp S0 are done (w and Qp single-buffered; Kd^T and Aqk into
+// the second of two stages, free because the previous chunk's Aqk Delta was
+// issued before P); u and gamma one chunk ahead, refilled once Delta is formed.  Waits are bounded; a timed-out
 // wait ends the walk for the whole CTA and sets the device error word.
 // The "state walk" and "output program" of PR #8638 (opening description)
 // and the walks of PR #7723 (opening description), fused.
@@ -130,13 +133,13 @@ struct WalkTcSmem {
   static constexpr int UB = N < 32 ? 1 : N / 32;  // 32-column TMA boxes of the u slice
   float W[CH * DK];         // A of P: w, rows j, K = c (four 64 x 32 column blocks)
   float Qp[CH * DK];        // A of O: Q Gamma, rows i, K = c (four 64 x 32 column blocks)
-  float KdT[DK * CH];       // A of the update: Kd^T, rows c, K = j (two 128 x 32 column blocks)
-  float Aqk[CH * CH];       // A of O: Aqk, rows i, K = j (two 64 x 32 column blocks)
+  float KdT[2][DK * CH];    // A of the update: Kd^T, rows c, K = j (two 128 x 32 column blocks)
+  float Aqk[2][CH * CH];    // A of O: Aqk, rows i, K = j (two 64 x 32 column blocks)
   float Sop[N * DK];        // B of P and O: S0, rows v, K = c
   float Dop[N * CH];        // B of the update and O: Delta, rows v, K = j
-  float U[2][CH * 32 * UB]; // u slice, rows j, 32-column swizzled blocks
-  float gam[2][DK];
-  uint64_t bar_u2[2], bar_wq, bar_k, bar_p, bar_o1, bar_up, bar_o2;
+  float U[CH * 32 * UB];    // u slice, rows j, 32-column swizzled blocks
+  float gam[DK];
+  uint64_t bar_u, bar_wq, bar_k[2], bar_p, bar_o1, bar_up, bar_o2;
   uint32_t tmem;
 };
 
@@ -163,10 +166,10 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
 
   if (issuer) {
-    tc::mbar_init(&s.bar_u2[0], 1);
-    tc::mbar_init(&s.bar_u2[1], 1);
+    tc::mbar_init(&s.bar_u, 1);
     tc::mbar_init(&s.bar_wq, 1);
-    tc::mbar_init(&s.bar_k, 1);
+    tc::mbar_init(&s.bar_k[0], 1);
+    tc::mbar_init(&s.bar_k[1], 1);
     tc::mbar_init(&s.bar_p, 1);
     tc::mbar_init(&s.bar_o1, 1);
     tc::mbar_init(&s.bar_up, 1);
@@ -186,14 +189,12 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   const uint32_t tO = tS + 2 * N;                                  // O[b] in columns [2N + bN, 3N + bN)
 
   // Issuer only.  Each stage's copies of chunk m land on its barrier.
-  auto issue_u = [&](int m) {  // u slice and gamma, double-buffered
-    const int b = m & 1;
+  auto issue_u = [&](int m) {  // u slice and gamma
     const int chunk = dd.chunk0 + m;
     const int item = chunk * a.HV + h;
-    tc::mbar_arrive_expect_tx(&s.bar_u2[b], U_BYTES);
-    for (int ub = 0; ub < UB; ++ub)
-      tc::tma_load_2d(&s.U[b][ub * CH * 32], &a.u_map, v0 + 32 * ub, item * CH, &s.bar_u2[b]);
-    tc::bulk_load(s.gam[b], &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, &s.bar_u2[b]);
+    tc::mbar_arrive_expect_tx(&s.bar_u, U_BYTES);
+    for (int ub = 0; ub < UB; ++ub) tc::tma_load_2d(&s.U[ub * CH * 32], &a.u_map, v0 + 32 * ub, item * CH, &s.bar_u);
+    tc::bulk_load(s.gam, &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, &s.bar_u);
   };
   auto issue_wq = [&](int m) {  // w and Q Gamma
     const int item = (dd.chunk0 + m) * a.HV + h;
@@ -203,12 +204,13 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
       tc::tma_load_2d(&s.Qp[kb * CH * 32], &a.qp_map, kb * 32, item * CH, &s.bar_wq);
     }
   };
-  auto issue_k = [&](int m) {  // Kd^T and Aqk
+  auto issue_k = [&](int m) {  // Kd^T and Aqk into stage m & 1
+    const int b = m & 1;
     const int item = (dd.chunk0 + m) * a.HV + h;
-    tc::mbar_arrive_expect_tx(&s.bar_k, K_BYTES);
+    tc::mbar_arrive_expect_tx(&s.bar_k[b], K_BYTES);
     for (int kb = 0; kb < 2; ++kb) {
-      tc::tma_load_2d(&s.KdT[kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_k);
-      tc::tma_load_2d(&s.Aqk[kb * CH * 32], &a.aqk_map, kb * 32, item * CH, &s.bar_k);
+      tc::tma_load_2d(&s.KdT[b][kb * DK * 32], &a.kdt_map, kb * 32, item * DK, &s.bar_k[b]);
+      tc::tma_load_2d(&s.Aqk[b][kb * CH * 32], &a.aqk_map, kb * 32, item * CH, &s.bar_k[b]);
     }
   };
   // scale * O of chunk m (TMEM buffer m & 1) -> out, rows below the chunk's length.
@@ -250,35 +252,33 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   // Copies and output products issued / waited for (issuer), for the drain after a timeout.
   int iss_u = 0, iss_wq = 0, iss_k = 0, got_wq = 0, got_k = 0, o1_iss = 0, o1_done = 0, o2_iss = 0, o2_done = 0;
   if (issuer && n > 0) {
-    issue_u(0), ++iss_u;
-    if (n > 1) issue_u(1), ++iss_u;
     issue_wq(0), ++iss_wq;
     issue_k(0), ++iss_k;
+    issue_u(0), ++iss_u;
   }
   constexpr uint32_t idP = tc::idesc_tf32(CH, N), idU = tc::idesc_tf32(DK, N);
   unsigned char* sop = reinterpret_cast<unsigned char*>(s.Sop);
   unsigned char* dop = reinterpret_cast<unsigned char*>(s.Dop);
-  bool ok = true;
+  bool ok = true, kprev = false;  // kprev: the previous chunk's Kd^T / Aqk stage was ready
+  // O += Aqk Delta of chunk q (issuer; needs Delta of q in the operand tile).
+  auto issue_o2 = [&](int q) {
+    const uint64_t aa = tc::desc_k_sw128(s.Aqk[q & 1]), bd = tc::desc_k_sw128(s.Dop);
+#pragma unroll
+    for (int k = 0; k < CH / 8; ++k)
+      tc::mma_tf32(tmem + 2 * N + (q & 1) * N, kstep(aa, k, CH), kstep(bd, k, N), idP, 1);
+    tc::mma_commit(&s.bar_o2);
+    ++o2_iss;
+  };
   int m = 0;
   for (; m < n; ++m) {
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     const size_t toff = tile_off(chunk, h, a.HV);
-    if (tid < DK) ok = tc::mbar_wait(&s.bar_u2[b], (m >> 1) & 1) && ok;
     if (issuer) {
-      if (m > 0) {  // Kd^T and Aqk are free once the previous O += Aqk Delta is done
-        const bool r = tc::mbar_wait(&s.bar_o2, (m - 1) & 1);
-        ok = r && ok;
-        o2_done += r;
-        if (r) issue_k(m), ++iss_k;
-      }
       const bool r = tc::mbar_wait(&s.bar_wq, m & 1);
       ok = r && ok;
       got_wq += r;
     }
-    tc::tc_fence_before();
-    if (!__syncthreads_and(ok)) break;
-    tc::tc_fence_after();
     uint32_t sr[N];
     if (tid < DK) {
       // S0 row c = tid; S0 as the B operand of P and O (row v, k = c).
@@ -291,10 +291,12 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
       tc::fence_proxy_async();
     }
     tc::tc_fence_before();
-    __syncthreads();
+    if (!__syncthreads_and(ok)) break;
     tc::tc_fence_after();
     if (issuer) {
-      // P = w S0 (committed alone: the chain waits on it), then O = Qp S0.
+      // The previous chunk's O += Aqk Delta, then P = w S0 (committed alone:
+      // the chain waits on it), then O = Qp S0.
+      if (m > 0 && kprev) issue_o2(m - 1);
       const uint64_t aw = tc::desc_k_sw128(s.W), aq = tc::desc_k_sw128(s.Qp), bs = tc::desc_k_sw128(s.Sop);
 #pragma unroll
       for (int k = 0; k < DK / 8; ++k) tc::mma_tf32(tmem + N, kstep(aw, k, CH), kstep(bs, k, N), idP, k > 0);
@@ -320,7 +322,8 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
                                  *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
         }
       }
-      const float gm = s.gam[b][tid];
+      ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;  // u and gamma of this chunk
+      const float gm = s.gam[tid];
 #pragma unroll
       for (int v = 0; v < N; ++v) sr[v] = __float_as_uint(__uint_as_float(sr[v]) * gm);
 #pragma unroll
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
       for (int cb = 0; cb < N; cb += 16) tc::tmem_ld16x256b_x2(tP + cb, *reinterpret_cast<uint32_t(*)[8]>(&pr[cb / 2]));
       tc::tmem_wait_ld();
       const int g = lane >> 2, u2 = (lane & 3) * 2;
-      const unsigned char* ub = reinterpret_cast<const unsigned char*>(s.U[b]);
+      const unsigned char* ub = reinterpret_cast<const unsigned char*>(s.U);
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int j = 16 * warp + g + 8 * hr;
@@ -358,67 +361,73 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
       }
       tc::fence_proxy_async();
     } else if (issuer) {
-      // w and Q Gamma are free once P and Qp S0 are done: fetch the next chunk's.
+      // Once P and Qp S0 are done, w and Q Gamma are free, and so is the Kd^T /
+      // Aqk stage of the previous chunk (its Aqk Delta was issued before P):
+      // fetch the next chunk's w, Q Gamma, Kd^T and Aqk (the latter into the
+      // stage this chunk's update does not read).
       const bool r = tc::mbar_wait(&s.bar_o1, m & 1);
       ok = r && ok;
       o1_done += r;
-      if (r && m + 1 < n) issue_wq(m + 1), ++iss_wq;
+      if (r) {
+        if (m > 0) ++o2_done;  // covered by this commit
+        if (m + 1 < n) {
+          issue_wq(m + 1), ++iss_wq;
+          issue_k(m + 1), ++iss_k;
+        }
+      }
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     if (issuer) {
       // The state update (committed alone), then O += Aqk Delta.
-      const bool kready = tc::mbar_wait(&s.bar_k, m & 1);
+      const bool kready = tc::mbar_wait(&s.bar_k[b], (m >> 1) & 1);
       ok = kready && ok;
       if (kready) {
         ++got_k;
-        const uint64_t ak = tc::desc_k_sw128(s.KdT), bd = tc::desc_k_sw128(s.Dop);
+        const uint64_t ak = tc::desc_k_sw128(s.KdT[b]), bd = tc::desc_k_sw128(s.Dop);
 #pragma unroll
         for (int k = 0; k < CH / 8; ++k) tc::mma_tf32(tmem, kstep(ak, k, DK), kstep(bd, k, N), idU, 1);
       }
       tc::mma_commit(&s.bar_up);
-      if (kready) {
-        const uint64_t aa = tc::desc_k_sw128(s.Aqk), bd = tc::desc_k_sw128(s.Dop);
-#pragma unroll
-        for (int k = 0; k < CH / 8; ++k) tc::mma_tf32(tmem + 2 * N + b * N, kstep(aa, k, CH), kstep(bd, k, N), idP, 1);
-      }
-      tc::mma_commit(&s.bar_o2);
-      ++o2_iss;
+      kprev = kready;
+      if (ok && m + 1 < n) issue_u(m + 1), ++iss_u;  // u and gamma were last read before this barrier
     }
     // The data warps wait for the state update before reading S; the issuer
     // too, before refilling the u stage.
     if (tid < DK || issuer) ok = tc::mbar_wait(&s.bar_up, m & 1) && ok;
     tc::tc_fence_after();
-    if (issuer && ok && m + 2 < n) issue_u(m + 2), ++iss_u;
   }
   if (m < n) {
     // A wait ran out: record it and drain the copies and products still in flight.
     if (issuer) {
       atomicExch(a.err, 3);
-      for (int q = m; q < iss_u; ++q) tc::mbar_wait(&s.bar_u2[q & 1], (q >> 1) & 1);
+      for (int q = m > 0 ? m - 1 : 0; q < iss_u; ++q) tc::mbar_wait(&s.bar_u, q & 1);
       for (int q = got_wq; q < iss_wq; ++q) tc::mbar_wait(&s.bar_wq, q & 1);
-      for (int q = got_k; q < iss_k; ++q) tc::mbar_wait(&s.bar_k, q & 1);
+      for (int q = got_k; q < iss_k; ++q) tc::mbar_wait(&s.bar_k[q & 1], (q >> 1) & 1);
       for (int q = o1_done; q < o1_iss; ++q) tc::mbar_wait(&s.bar_o1, q & 1);
       for (int q = o2_done; q < o2_iss; ++q) tc::mbar_wait(&s.bar_o2, q & 1);
     }
-  } else if (tid < DK) {
-    if (n > 0) {
-      ok = tc::mbar_wait(&s.bar_o2, (n - 1) & 1) && ok;
-      tc::tc_fence_after();
-      if (ok) write_out(n - 1);
-    }
-    if (a.ht) {
-#pragma unroll
-      for (int cb = 0; cb < N; cb += 16) {
-        uint32_t r[16];
-        tc::tmem_ld16(tS + cb, r);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 16; ++q) a.ht[sidx + (size_t)tid * DK + v0 + cb + q] = __uint_as_float(r[q]);
+  } else {
+    if (issuer && n > 0 && kprev) issue_o2(n - 1);  // the last chunk's O += Aqk Delta
+    if (tid < DK) {
+      if (n > 0) {
+        ok = tc::mbar_wait(&s.bar_o2, (n - 1) & 1) && ok;
+        tc::tc_fence_after();
+        if (ok) write_out(n - 1);
       }
+      if (a.ht) {
+#pragma unroll
+        for (int cb = 0; cb < N; cb += 16) {
+          uint32_t r[16];
+          tc::tmem_ld16(tS + cb, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 16; ++q) a.ht[sidx + (size_t)tid * DK + v0 + cb + q] = __uint_as_float(r[q]);
+        }
+      }
+      if (!ok) atomicExch(a.err, 3);
     }
-    if (!ok) atomicExch(a.err, 3);
   }
   tc::tc_fence_before();
   __syncthreads();
