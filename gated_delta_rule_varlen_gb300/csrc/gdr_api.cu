@@ -88,7 +88,6 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
   Layout L;
   L.NC = NC;
   const size_t tile = (size_t)NC * HV * CH * DK * sizeof(float);
-  const size_t sq = (size_t)NC * HV * CH * CH * sizeof(float);
   const size_t vec = (size_t)NC * HV * DK * sizeof(float);
   const size_t st = (size_t)NC * HV * DK * DK * sizeof(uint16_t);  // BF16 state tapes
   size_t o = 0;
@@ -101,24 +100,24 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
   L.chunks = take((size_t)std::max<int64_t>(NC, 1) * sizeof(ChunkDesc));
   L.order = take((size_t)std::max(N, 1) * sizeof(int));
   L.w = take((size_t)NC * HV * CH * LDT * sizeof(float));
-  L.u = take(tile);
+  L.u = take((size_t)NC * HV * CH * LDF * sizeof(float));
   L.qp = take((size_t)NC * HV * CH * LDF * sizeof(float));
   L.kd = take((size_t)NC * HV * DK * LDS * sizeof(float));
   L.delta = take(tile);
   L.aqk = take((size_t)NC * HV * CH * LDS * sizeof(float));
-  L.amat = take(sq);
-  L.tmat = take(sq);
+  L.amat = take((size_t)NC * HV * CH * LDS * sizeof(float));
+  L.tmat = take((size_t)NC * HV * CH * LDS * sizeof(float));
   L.gam = take(vec);
   L.tape = take(st);
   L.saved_total = o;
   o = 0;
   L.dstape = take(st);
-  L.ddelta = take(tile);
+  L.ddelta = take((size_t)NC * HV * CH * LDF * sizeof(float));
   L.dqs = take(tile);
-  L.dw = take(tile);
+  L.dw = take((size_t)NC * HV * CH * LDF * sizeof(float));
   L.dkd = take(tile);
   L.dgam = take(vec);
-  L.daqk = take(sq);
+  L.daqk = take((size_t)NC * HV * CH * LDS * sizeof(float));
   if (grouped) {
     L.dqp = take(tile);
     L.dkp = take(tile);
@@ -426,7 +425,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   if (!wa.err) return GDR_CUDA_ERROR;
   if (NC > 0 && (!fp32_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, LDT, CH) ||
                  !fp32_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, LDS, DK) ||
-                 !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, DK, CH) ||
+                 !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, LDF, CH) ||
                  !fp32_map(&wa.qp_map, pa.qp, (uint64_t)NC * HV * CH, DK, LDF, CH) ||
                  !fp32_map(&wa.aqk_map, pa.aqk, (uint64_t)NC * HV * CH, CH, LDS, CH)))
     return GDR_CUDA_ERROR;
@@ -541,6 +540,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   ga.dkd = gs.dkd;
   ga.dgam = gs.dgam;
   ga.daqk = gs.daqk;
+  ga.err = wb.err;
   ga.amat = at<float>(saved, L.amat);
   ga.tmat = at<float>(saved, L.tmat);
   ga.dq = static_cast<__nv_bfloat16*>(dq);

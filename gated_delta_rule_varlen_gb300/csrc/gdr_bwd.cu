@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
         mma8(E[nt], av, b);
       }
     }
-    acc_foreach(E, [&](int r, int j, float& x) { a.ddelta[toff + (size_t)j * DK + v0 + r] = x; });
+    acc_foreach(E, [&](int r, int j, float& x) { a.ddelta[tf_off(chunk, h, a.HV) + (size_t)j * LDF + v0 + r] = x; });
     ok = tc::mbar_wait(&sb.barB, s & 1) && ok;  // Qp, w of this step
     if (!__syncthreads_and(ok)) break;
     doneB = s + 1;
@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int e = tid + 256 * q;
-      const float* src = (e < 1024 ? a.delta : a.ddelta) + toff + (size_t)((e >> 4) & 63) * DK + (e & 15) * 8;
+      const float* src = e < 1024 ? a.delta + toff + (size_t)((e >> 4) & 63) * DK + (e & 15) * 8
+                                  : a.ddelta + tf_off(chunk, h, a.HV) + (size_t)((e >> 4) & 63) * LDF + (e & 15) * 8;
       x[q][0] = __ldg(reinterpret_cast<const float4*>(src));
       x[q][1] = __ldg(reinterpret_cast<const float4*>(src) + 1);
     }
@@ -397,13 +398,13 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
       *reinterpret_cast<float2*>(&a.dqs[toff + i * DK + c0 + c]) = make_float2(a.scale * x0, a.scale * x1);
     });
     drain(128 + c0, 64, [&](int i, int c, float x0, float x1) {
-      *reinterpret_cast<float2*>(&a.dw[toff + i * DK + c0 + c]) = make_float2(-x0, -x1);
+      *reinterpret_cast<float2*>(&a.dw[tf_off(chunk, h, a.HV) + i * LDF + c0 + c]) = make_float2(-x0, -x1);
     });
-    float* daqk = a.daqk + sq_off(chunk, h, a.HV);
+    float* daqk = a.daqk + ts_off(chunk, h, a.HV);
     const int j0 = 32 * hf;
     drain(384 + j0, 32, [&](int i, int c, float x0, float x1) {
       const int j = j0 + c;
-      *reinterpret_cast<float2*>(&daqk[i * CH + j]) =
+      *reinterpret_cast<float2*>(&daqk[i * LDS + j]) =
           make_float2(j <= i ? a.scale * x0 : 0.f, j + 1 <= i ? a.scale * x1 : 0.f);
     });
   }
@@ -443,6 +444,7 @@ struct GradSmem {
   float dbeta[3][CH];  // per channel half (X.Kp + Y.V), and sum_j dA_ij At_ij
   float col[4 * DK];
   float rowsum[CH];
+  uint64_t bar_ld, bar_u;
 };
 
 // 8 warps: warp w owns rows 16 (w % 4) .. +15 and channels 64 (w / 4) .. +63
@@ -462,27 +464,35 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
   const int I = warp & 3, i0 = 16 * I, hc = warp >> 2, c0 = 64 * hc;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
-  const size_t qoff = sq_off(chunk, h, a.HV);
+  const size_t fo = tf_off(chunk, h, a.HV), so = ts_off(chunk, h, a.HV);
   // gamma * dgamma of channel tid % 128 (per-channel gate), for the dg epilogue.
   const float gdg = VEC ? __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))]) *
                               __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))])
                         : 0.f;
-  // dw and dDelta (the B operands of X and Y) into the staging tiles; dAqk,
-  // and the forward's At and T of this chunk.
-  for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
-    const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&sg.dK[i * LDF + c4], &a.dw[toff + i * DK + c4]);
-    cp_async16(&sg.dG[i * LDF + c4], &a.ddelta[toff + i * DK + c4]);
+  // Whole tiles, stored with these shared pitches, by one bulk copy each: dw
+  // and dDelta (the B operands of X and Y) into the staging tiles, dAqk, and
+  // the forward's At and T of this chunk.
+  if (tid == 0) {
+    tc::mbar_init(&sg.bar_ld, 1);
+    tc::mbar_init(&sg.bar_u, 1);
+    tc::mbar_fence_init();
+    tc::mbar_arrive_expect_tx(&sg.bar_ld, (2 * CH * LDF + 3 * CH * LDS) * 4);
+    tc::bulk_load(sg.dK, &a.dw[fo], CH * LDF * 4, &sg.bar_ld);
+    tc::bulk_load(sg.dG, &a.ddelta[fo], CH * LDF * 4, &sg.bar_ld);
+    tc::bulk_load(sg.dAqk, &a.daqk[so], CH * LDS * 4, &sg.bar_ld);
+    tc::bulk_load(s.At, &a.amat[so], CH * LDS * 4, &sg.bar_ld);
+    tc::bulk_load(s.T, &a.tmat[so], CH * LDS * 4, &sg.bar_ld);
   }
-  for (int e = tid; e < CH * CH / 4; e += blockDim.x) {
-    const int i = e >> 4, c4 = (e & 15) * 4;
-    cp_async16(&sg.dAqk[i * LDS + c4], &a.daqk[qoff + i * CH + c4]);
-    cp_async16(&s.At[i * LDS + c4], &a.amat[qoff + i * CH + c4]);
-    cp_async16(&s.T[i * LDS + c4], &a.tmat[qoff + i * CH + c4]);
-  }
-  cp_async_commit();
   load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
                          a.HV);
+  // (load_chunk's barriers made the barrier set-up visible.)
+  if (!__syncthreads_and(tc::mbar_wait(&sg.bar_ld, 0))) {
+    if (tid == 0) {  // a wait ran out: record it and let the copies finish
+      atomicExch(a.err, 7);
+      tc::mbar_wait(&sg.bar_ld, 0);
+    }
+    return;
+  }
   // Gate of (i, c) and (i, c + 1).
   auto gl2 = [&](int i, int c) -> float2 { return VEC ? s.g2(i, c) : make_float2(s.gs[i], s.gs[i]); };
 
@@ -520,18 +530,28 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
     }
   }
   __syncthreads();
-  // w and u (B operands of dA) into the staging tiles.
+  // w and u (B operands of dA) into the staging tiles: u by one bulk copy, w
+  // (stored with the backward walk's pitch) by cp.async.
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&sg.bar_u, CH * LDF * 4);
+    tc::bulk_load(sg.dG, &a.u[fo], CH * LDF * 4, &sg.bar_u);
+  }
   for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
     const int i = e >> 5, c4 = (e & 31) * 4;
     cp_async16(&sg.dK[i * LDF + c4], &a.w[w_off(chunk, h, a.HV) + i * LDT + c4]);
-    cp_async16(&sg.dG[i * LDF + c4], &a.u[toff + i * DK + c4]);
   }
   cp_async_commit();
   // Partial dA over this warp's channel half: X w^T + Y u^T.
   float dAacc[8][4];
   zero_acc(dAacc);
   cp_async_wait<0>();
-  __syncthreads();
+  if (!__syncthreads_and(tc::mbar_wait(&sg.bar_u, 0))) {
+    if (tid == 0) {
+      atomicExch(a.err, 7);
+      tc::mbar_wait(&sg.bar_u, 0);
+    }
+    return;
+  }
   {
     const float* w = sg.dK;
     const float* u = sg.dG;

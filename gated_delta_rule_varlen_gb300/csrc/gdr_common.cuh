@@ -160,9 +160,6 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return
 __device__ __forceinline__ size_t tile_off(int chunk, int h, int HV) {  // [NC][HV][64][128]
   return ((size_t)chunk * HV + h) * (CH * DK);
 }
-__device__ __forceinline__ size_t sq_off(int chunk, int h, int HV) {    // [NC][HV][64][64]
-  return ((size_t)chunk * HV + h) * (CH * CH);
-}
 __device__ __forceinline__ size_t state_off(int chunk, int h, int HV) { // [NC][HV][128][128]
   return ((size_t)chunk * HV + h) * (DK * DK);
 }
@@ -173,5 +170,9 @@ __device__ __forceinline__ size_t w_off(int chunk, int h, int HV) { return ((siz
 __device__ __forceinline__ size_t qp_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDF); }
 __device__ __forceinline__ size_t kd_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (DK * LDS); }
 __device__ __forceinline__ size_t aqk_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDS); }
+// Tiles the gradient kernel moves whole keep its pitches too: u, dw, dDelta
+// [64][LDF]; At, T, dAqk [64][LDS].
+__device__ __forceinline__ size_t tf_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDF); }
+__device__ __forceinline__ size_t ts_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDS); }
 
 }  // namespace gdr

@@ -28,11 +28,11 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   invert(s);
   // At and T for the backward: the values its gradient kernel needs, bit for bit.
   if (a.amat) {
-    const size_t qo = sq_off(chunk, h, a.HV);
+    const size_t qo = ts_off(chunk, h, a.HV);
     for (int e = tid; e < CH * CH / 4; e += blockDim.x) {
       const int i = e >> 4, j4 = (e & 15) * 4;
-      *reinterpret_cast<float4*>(&a.amat[qo + i * CH + j4]) = *reinterpret_cast<const float4*>(&s.At[i * LDS + j4]);
-      *reinterpret_cast<float4*>(&a.tmat[qo + i * CH + j4]) = *reinterpret_cast<const float4*>(&s.T[i * LDS + j4]);
+      *reinterpret_cast<float4*>(&a.amat[qo + i * LDS + j4]) = *reinterpret_cast<const float4*>(&s.At[i * LDS + j4]);
+      *reinterpret_cast<float4*>(&a.tmat[qo + i * LDS + j4]) = *reinterpret_cast<const float4*>(&s.T[i * LDS + j4]);
     }
   }
   // Qp, Kd, gamma (elementwise; factors exp(gc) and exp(gc_last - gc) are <= 1).
@@ -79,8 +79,8 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   {
     const int prod = warp >> 2, q = warp & 3, c0 = 64 * (q & 1);
     const int Ia = (q >> 1) ? 2 : 3, Ib = 3 - Ia;
-    float* out = prod ? a.u + toff : a.w + w_off(chunk, h, a.HV);
-    const int ldo = prod ? DK : LDT;
+    float* out = prod ? a.u + tf_off(chunk, h, a.HV) : a.w + w_off(chunk, h, a.HV);
+    const int ldo = prod ? LDF : LDT;
     auto bw = [&](int j, int c) { return s.G[j * LDT + c]; };
     auto bu = [&](int j, int c) { return s.beta[j] * s.q(j, c); };
 #pragma unroll

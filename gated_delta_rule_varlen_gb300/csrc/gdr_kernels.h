@@ -88,6 +88,7 @@ struct GradArgs {
   float *dq_part, *dk_part;      // [NC][HV][64][128] per value head when HV > Hqk
   float* dg;
   void* dbeta;
+  int* err;  // device error word
 };
 
 struct GroupReduceArgs {

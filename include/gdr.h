@@ -175,7 +175,7 @@ gdr_status gdr_check_device(void);
  * completes; after limit_ns nanoseconds (1 <= limit_ns <= 1e8, else
  * GDR_INVALID_ARG) it records the timeout in the error word and exits.
  * Device error codes: 3 forward walk, 4 backward walk, 5 this self-test,
- * 6 state-side gradient products. */
+ * 6 state-side gradient products, 7 chunk-local gradients. */
 gdr_status gdr_inject_device_error(int code);
 gdr_status gdr_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
 
