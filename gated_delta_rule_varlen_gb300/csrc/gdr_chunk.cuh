@@ -135,48 +135,29 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const int ra = i0 + g, rb = i0 + g + 8;
   const float* G = s.G;
-  // Off-diagonal n-tiles [0, 2I) (and, with a scalar gate, the diagonal ones)
-  // in accK/accQ; diagonal n-tiles 2I, 2I+1 of a per-channel gate in dK/dQ.
-  float accK[8][4], accQ[8][4], dK[2][4], dQ[2][4];
+  // n-tiles [0, 2I + 2) of row block I (the rest is zero).
+  float accK[8][4], accQ[8][4];
   zero_acc(accK);
   zero_acc(accQ);
-  zero_acc(dK);
-  zero_acc(dQ);
   if (VEC) {
 #pragma unroll 2
     for (int kk = 8 * hk; kk < 8 * hk + 8; ++kk) {
       const int c0 = kk * 8 + t, c1 = c0 + 4;
-      const float ka0 = s.k(ra, c0), kb0 = s.k(rb, c0), ka1 = s.k(ra, c1), kb1 = s.k(rb, c1);
-      const float qa0 = s.q(ra, c0), qb0 = s.q(rb, c0), qa1 = s.q(ra, c1), qb1 = s.q(rb, c1);
-      const float ga0 = G[ra * LG + c0], gb0 = G[rb * LG + c0], ga1 = G[ra * LG + c1], gb1 = G[rb * LG + c1];
-      // Off-diagonal blocks: reference = gc at the end of block I-1.
-      if (I > 0) {
-        const float b0 = G[(i0 - 1) * LG + c0], b1 = G[(i0 - 1) * LG + c1];
-        const float e00 = ex2(ga0 - b0), e10 = ex2(gb0 - b0), e01 = ex2(ga1 - b1), e11 = ex2(gb1 - b1);
-        uint32_t aK[4] = {tf32(ka0 * e00), tf32(kb0 * e10), tf32(ka1 * e01), tf32(kb1 * e11)};
-        uint32_t aQ[4] = {tf32(qa0 * e00), tf32(qb0 * e10), tf32(qa1 * e01), tf32(qb1 * e11)};
+      // Reference: gc at row i0 + 7, for the diagonal and the earlier blocks alike.
+      const float m0 = G[(i0 + 7) * LG + c0], m1 = G[(i0 + 7) * LG + c1];
+      const float e00 = ex2(G[ra * LG + c0] - m0), e10 = ex2(G[rb * LG + c0] - m0);
+      const float e01 = ex2(G[ra * LG + c1] - m1), e11 = ex2(G[rb * LG + c1] - m1);
+      uint32_t aK[4] = {tf32(s.k(ra, c0) * e00), tf32(s.k(rb, c0) * e10), tf32(s.k(ra, c1) * e01),
+                        tf32(s.k(rb, c1) * e11)};
+      uint32_t aQ[4] = {tf32(s.q(ra, c0) * e00), tf32(s.q(rb, c0) * e10), tf32(s.q(ra, c1) * e01),
+                        tf32(s.q(rb, c1) * e11)};
 #pragma unroll
-        for (int nt = 0; nt < 6; ++nt) {
-          if (nt < 2 * I) {
-            const int j = nt * 8 + g;
-            uint32_t b[2] = {tf32(s.k(j, c0) * ex2(b0 - G[j * LG + c0])), tf32(s.k(j, c1) * ex2(b1 - G[j * LG + c1]))};
-            mma8(accK[nt], aK, b);
-            mma8(accQ[nt], aQ, b);
-          }
-        }
-      }
-      // Diagonal block: reference = gc at row i0 + 7.
-      {
-        const float m0 = G[(i0 + 7) * LG + c0], m1 = G[(i0 + 7) * LG + c1];
-        const float e00 = ex2(ga0 - m0), e10 = ex2(gb0 - m0), e01 = ex2(ga1 - m1), e11 = ex2(gb1 - m1);
-        uint32_t aK[4] = {tf32(ka0 * e00), tf32(kb0 * e10), tf32(ka1 * e01), tf32(kb1 * e11)};
-        uint32_t aQ[4] = {tf32(qa0 * e00), tf32(qb0 * e10), tf32(qa1 * e01), tf32(qb1 * e11)};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int j = i0 + nt * 8 + g;
+      for (int nt = 0; nt < 8; ++nt) {
+        if (nt < 2 * I + 2) {
+          const int j = nt * 8 + g;
           uint32_t b[2] = {tf32(s.k(j, c0) * ex2(m0 - G[j * LG + c0])), tf32(s.k(j, c1) * ex2(m1 - G[j * LG + c1]))};
-          mma8(dK[nt], aK, b);
-          mma8(dQ[nt], aQ, b);
+          mma8(accK[nt], aK, b);
+          mma8(accQ[nt], aQ, b);
         }
       }
     }
@@ -197,12 +178,6 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
       }
     }
   }
-  // Raw (unmasked) sum of this warp's channel half at accumulator slot (nt, r).
-  auto raw = [&](const float (&acc)[8][4], const float (&dg)[2][4], int nt, int r) -> float {
-    if (VEC && nt == 2 * I) return dg[0][r];
-    if (VEC && nt == 2 * I + 1) return dg[1][r];
-    return acc[nt][r];
-  };
   float* tq = s.T;  // partial Aqk of the upper channel half
   if (hk == 1) {
 #pragma unroll
@@ -211,8 +186,8 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
       for (int r = 0; r < 4; ++r) {
         const int row = i0 + g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
         if (nt < 2 * I + 2) {
-          s.At[row * LDS + col] = raw(accK, dK, nt, r);
-          tq[row * LDS + col] = raw(accQ, dQ, nt, r);
+          s.At[row * LDS + col] = accK[nt][r];
+          tq[row * LDS + col] = accQ[nt][r];
         }
       }
   }
@@ -225,8 +200,8 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
         const int row = i0 + g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
         float vK = 0.f, vQ = 0.f;
         if (nt < 2 * I + 2 && col <= row) {
-          vK = raw(accK, dK, nt, r) + s.At[row * LDS + col];
-          vQ = raw(accQ, dQ, nt, r) + tq[row * LDS + col];
+          vK = accK[nt][r] + s.At[row * LDS + col];
+          vQ = accQ[nt][r] + tq[row * LDS + col];
           if (!VEC) {
             const float dec = ex2(s.gs[row] - s.gs[col]);
             vK *= dec;
@@ -308,71 +283,10 @@ __device__ void invert(ChunkSmemT<ET, LG>& s) {
   __syncthreads();
 }
 
-// Z_i += sum_{j<=i} M_ij Y_j * exp(gc_i - gc_j) for rows i of block I
-// (16I .. 16I+15) and channels c0 .. c0 + 8 NT - 1.  M is a masked [64][64]
-// shared tile (stride LDS); fy(j, c) returns Y_jc.
-template <bool VEC, int NT, typename ET, int LG, class FY>
-__device__ void left_apply(const ChunkSmemT<ET, LG>& s, const float* __restrict__ M, FY fy, float (&Z)[NT][4], int I,
-                           int c0) {
-  const int i0 = 16 * I;
-  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
-  if (VEC) {
-    float acc[NT][4];
-    zero_acc(acc);
-    if (I > 0) {
-      for (int kk = 0; kk < 2 * I; ++kk) {  // j in [0, 16I)
-        const int j0 = kk * 8 + t, j1 = j0 + 4;
-        uint32_t a[4] = {tf32(M[(i0 + g) * LDS + j0]), tf32(M[(i0 + g + 8) * LDS + j0]),
-                         tf32(M[(i0 + g) * LDS + j1]), tf32(M[(i0 + g + 8) * LDS + j1])};
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int c = c0 + nt * 8 + g;
-          const float bI = s.G[(i0 - 1) * LG + c];
-          uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LG + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LG + c]))};
-          mma8(acc[nt], a, b);
-        }
-      }
-      acc_foreach(acc, [&](int r, int col, float& x) {
-        Z[col >> 3][(r >> 3) * 2 + (col & 1)] +=
-            x * ex2(s.G[(i0 + r) * LG + c0 + col] - s.G[(i0 - 1) * LG + c0 + col]);
-      });
-    }
-    zero_acc(acc);
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {  // j in the diagonal block
-      const int j0 = i0 + kk * 8 + t, j1 = j0 + 4;
-      uint32_t a[4] = {tf32(M[(i0 + g) * LDS + j0]), tf32(M[(i0 + g + 8) * LDS + j0]),
-                       tf32(M[(i0 + g) * LDS + j1]), tf32(M[(i0 + g + 8) * LDS + j1])};
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int c = c0 + nt * 8 + g;
-        const float mI = s.G[(i0 + 7) * LG + c];
-        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LG + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LG + c]))};
-        mma8(acc[nt], a, b);
-      }
-    }
-    acc_foreach(acc, [&](int r, int col, float& x) {
-      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[(i0 + r) * LG + c0 + col] - s.G[(i0 + 7) * LG + c0 + col]);
-    });
-  } else {
-    for (int kk = 0; kk < 2 * I + 2; ++kk) {
-      const int j0 = kk * 8 + t, j1 = j0 + 4;
-      const int ra = i0 + g, rb = i0 + g + 8;
-      auto mv = [&](int i, int j) { return j <= i ? M[i * LDS + j] * ex2(s.gs[i] - s.gs[j]) : 0.f; };
-      uint32_t a[4] = {tf32(mv(ra, j0)), tf32(mv(rb, j0)), tf32(mv(ra, j1)), tf32(mv(rb, j1))};
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int c = c0 + nt * 8 + g;
-        uint32_t b[2] = {tf32(fy(j0, c)), tf32(fy(j1, c))};
-        mma8(Z[nt], a, b);
-      }
-    }
-  }
-}
-
-// Two left applies that share Y: Z0 += [M0 (x) decay] Y, Z1 += [M1 (x) decay] Y
-// over the rows of block I and channels c0 .. c0 + 8 NT - 1 (each gated Y
-// fragment is formed once and feeds both products).
+// Two left applies that share Y: Z0_i += sum_{j<=i} M0_ij Y_j exp(gc_i - gc_j),
+// Z1 likewise with M1, over the rows i of block I (16I .. 16I+15) and channels
+// c0 .. c0 + 8 NT - 1; M0, M1 are masked [64][64] shared tiles, fy(j, c)
+// returns Y_jc.  Each gated Y fragment is formed once and feeds both products.
 template <bool VEC, int NT, typename ET, int LG, class FY>
 __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict__ M0, const float* __restrict__ M1, FY fy,
                             float (&Z0)[NT][4], float (&Z1)[NT][4], int I, int c0) {
@@ -386,38 +300,10 @@ __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict
       a[2] = tf32(M[(i0 + g) * LDS + j1]);
       a[3] = tf32(M[(i0 + g + 8) * LDS + j1]);
     };
-    if (I > 0) {
-      zero_acc(acc0);
-      zero_acc(acc1);
-      for (int kk = 0; kk < 2 * I; ++kk) {  // j in [0, 16I): reference gc at row 16I - 1
-        const int j0 = kk * 8 + t, j1 = j0 + 4;
-        uint32_t a0[4], a1[4];
-        afrag(M0, j0, j1, a0);
-        afrag(M1, j0, j1, a1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int c = c0 + nt * 8 + g;
-          const float bI = s.G[(i0 - 1) * LG + c];
-          uint32_t b[2] = {tf32(fy(j0, c) * ex2(bI - s.G[j0 * LG + c])), tf32(fy(j1, c) * ex2(bI - s.G[j1 * LG + c]))};
-          mma8(acc0[nt], a0, b);
-          mma8(acc1[nt], a1, b);
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int row = g + 8 * (r >> 1), col = nt * 8 + 2 * t + (r & 1);
-          const float e = ex2(s.G[(i0 + row) * LG + c0 + col] - s.G[(i0 - 1) * LG + c0 + col]);
-          Z0[nt][r] += acc0[nt][r] * e;
-          Z1[nt][r] += acc1[nt][r] * e;
-        }
-    }
     zero_acc(acc0);
     zero_acc(acc1);
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {  // j in the diagonal block: reference gc at row 16I + 7
-      const int j0 = i0 + kk * 8 + t, j1 = j0 + 4;
+    for (int kk = 0; kk < 2 * I + 2; ++kk) {  // j in [0, 16I + 16): reference gc at row 16I + 7
+      const int j0 = kk * 8 + t, j1 = j0 + 4;
       uint32_t a0[4], a1[4];
       afrag(M0, j0, j1, a0);
       afrag(M1, j0, j1, a1);
@@ -471,32 +357,9 @@ __device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restric
   if (VEC) {
     float acc[NT][4];
     zero_acc(acc);
-    const int ref = j0b + 15;  // gc at the end of block J
-    for (int kk = 2 * J + 2; kk < 8; ++kk) {  // i in blocks after J
+    const int mref = j0b + 7;  // reference: gc at row 16J + 7, for block J and the later blocks alike
+    for (int kk = 2 * J; kk < 8; ++kk) {  // i in block J and after
       const int ia = kk * 8 + t, ib = ia + 4;
-      uint32_t a0[4] = {tf32(M0[ia * LDS + j0b + g]), tf32(M0[ia * LDS + j0b + g + 8]),
-                        tf32(M0[ib * LDS + j0b + g]), tf32(M0[ib * LDS + j0b + g + 8])};
-      uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + j0b + g]), tf32(s.beta[ia] * M1[ia * LDS + j0b + g + 8]),
-                        tf32(s.beta[ib] * M1[ib * LDS + j0b + g]), tf32(s.beta[ib] * M1[ib * LDS + j0b + g + 8])};
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int c = c0 + nt * 8 + g;
-        const float bJ = s.G[ref * LG + c];
-        const float ea = ex2(s.G[ia * LG + c] - bJ), eb = ex2(s.G[ib * LG + c] - bJ);
-        uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
-        uint32_t b1[2] = {tf32(f1(ia, c) * ea), tf32(f1(ib, c) * eb)};
-        mma8(acc[nt], a0, b0);
-        mma8(acc[nt], a1, b1);
-      }
-    }
-    acc_foreach(acc, [&](int r, int col, float& x) {
-      Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[ref * LG + c0 + col] - s.G[(j0b + r) * LG + c0 + col]);
-    });
-    zero_acc(acc);
-    const int mref = j0b + 7;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const int ia = j0b + kk * 8 + t, ib = ia + 4;
       uint32_t a0[4] = {tf32(M0[ia * LDS + j0b + g]), tf32(M0[ia * LDS + j0b + g + 8]),
                         tf32(M0[ib * LDS + j0b + g]), tf32(M0[ib * LDS + j0b + g + 8])};
       uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + j0b + g]), tf32(s.beta[ia] * M1[ia * LDS + j0b + g + 8]),

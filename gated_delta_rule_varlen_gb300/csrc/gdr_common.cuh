@@ -19,11 +19,13 @@
 //
 // Per-channel decays exp(gc_i - gc_j) are never split as exp(gc_i)*exp(-gc_j)
 // over a whole chunk (exp(-gc) overflows FP32 after ~18 tokens at g = -5).
-// Instead products over channels are factored per 16-row block pair with a
-// reference point between the two rows: for rows i in block I and j in an
-// earlier block, ref = gc at the end of block I-1 makes both factors <= 1;
-// inside a diagonal block, ref = gc at the block's 8th row bounds each factor
-// by exp(8 * max|g|) (< FP32 max for g >= -10).
+// Instead products over channels are factored per 16-row block with the
+// reference point r = gc at the block's 8th row: for rows i of the block and
+// columns j <= i, exp(gc_i - gc_j) = exp(gc_i - r) * exp(r - gc_j), where the
+// row factor lies within exp(+-8 max|g|) (2^+-116 for g >= -10, finite in FP32)
+// and the column factor is <= 1 for every j before the 8th row and within
+// exp(8 max|g|) after it.  A column factor that flushes to zero belongs to a
+// term below 2^-25 of the result.
 //
 // Matrix products use warp-level mma.sync m16n8k8 with TF32 operands
 // (round-to-nearest) and FP32 accumulation.  BF16 operands were measured on
