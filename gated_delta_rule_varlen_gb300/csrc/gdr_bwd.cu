@@ -465,10 +465,9 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
   const size_t fo = tf_off(chunk, h, a.HV), so = ts_off(chunk, h, a.HV);
-  // gamma * dgamma of channel tid % 128 (per-channel gate), for the dg epilogue.
-  const float gdg = VEC ? __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))]) *
-                              __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))])
-                        : 0.f;
+  // gamma * dgamma of channel tid % 128, for the dg epilogue.
+  const float gdg = __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))]) *
+                    __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))]);
   // Whole tiles, stored with these shared pitches, by one bulk copy each: dw
   // and dDelta (the B operands of X and Y) into the staging tiles, dAqk, and
   // the forward's At and T of this chunk.
@@ -765,19 +764,29 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
       if (i < cd.len) a.dg[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c] = acc;
     }
   } else {
-    if (tid < CH) {
+    // Scalar gate: dg_i = sum_{i' >= i} rowsum(dgc)_i' + the chunk-end term
+    // sum_c (gamma dgamma + colsum(Kd dKd)).  Row sums: four threads per row
+    // (channels q4, q4 + 4, ...); the chunk-end term: one channel per thread,
+    // reduced per warp.
+    {
+      const int row = tid >> 2, q4 = tid & 3;
       float acc = 0.f;
-      for (int c = 0; c < DK; ++c) acc += dG[tid * LDF + c];
-      sg.rowsum[tid] = acc;
+#pragma unroll 8
+      for (int k = 0; k < DK / 4; ++k) acc += dG[row * LDF + q4 + 4 * k];
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (q4 == 0) sg.rowsum[row] = acc;
+    }
+    if (tid < DK) {
+      const int c = tid;
+      float e = gdg + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) e += __shfl_xor_sync(0xffffffffu, e, m);
+      if (lane == 0) s.tmp[warp] = e;
     }
     __syncthreads();
     if (tid == 0) {
-      const float* gam = a.gam + ((size_t)chunk * a.HV + h) * DK;
-      const float* dgam = a.dgam + ((size_t)chunk * a.HV + h) * DK;
-      float extra = 0.f;
-      for (int c = 0; c < DK; ++c)
-        extra += gam[c] * dgam[c] + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
-      float acc = extra;
+      float acc = (s.tmp[0] + s.tmp[1]) + (s.tmp[2] + s.tmp[3]);
       for (int i = CH - 1; i >= 0; --i) {
         acc += sg.rowsum[i];
         if (i < cd.len) a.dg[(size_t)(cd.tok0 + i) * a.HV + h] = acc;
