@@ -111,12 +111,19 @@ __device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restric
         s.G[i * LG + tid] = acc;
       }
     }
-  } else if (tid == 0) {
-    float acc = 0.f;
-    for (int i = 0; i < CH; ++i) {
-      acc += s.gs[i];
-      s.gs[i] = acc;
+  } else if (tid < CH) {
+    // Inclusive scan over the 64 rows: per warp by shuffles, then the first
+    // warp's total added to the second warp's rows.
+    float x = s.gs[tid];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, d);
+      if ((tid & 31) >= d) x += y;
     }
+    if (tid == 31) s.tmp[0] = x;
+    named_sync(1, CH);
+    if (tid >= 32) x += s.tmp[0];
+    s.gs[tid] = x;
   }
   __syncthreads();
 }
