@@ -433,27 +433,32 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
 // ---------------------------------------------------------------------------
 // Chunk-local gradients (one CTA per (chunk, value head)).  Warp I owns rows
 // 16I..16I+15 of every per-row result; dk and the gate adjoint accumulate in
-// shared memory, dg is the reverse chunk-local cumsum of dgc.  The
+// registers, dg is the reverse chunk-local cumsum of dgc.  The
 // "fused gradient" / "gate epilogue" stages named on PR #8218.
 // ---------------------------------------------------------------------------
+constexpr int GRAD_WARPS = 16;   // 4 row blocks x 4 channel quarters
+constexpr int GRAD_NT = 4;       // 8-channel n-tiles per warp (32 channels)
+
 struct GradSmem {
   ChunkSmemBB c;
   float dAqk[CH * LDS];
   float dK[CH * LDF];  // staging: dw, then w; finally unused
   float dG[CH * LDF];  // staging: dDelta, then u; finally the gate adjoint dgc
-  float dbeta[3][CH];  // per channel half (X.Kp + Y.V), and sum_j dA_ij At_ij
+  float dbeta[5][CH];  // per channel quarter (X.Kp + Y.V), and sum_j dA_ij At_ij
   float col[4 * DK];
   float rowsum[CH];
   uint64_t bar_ld, bar_u;
 };
 
-// 8 warps: warp w owns rows 16 (w % 4) .. +15 and channels 64 (w / 4) .. +63
+// 16 warps: warp w owns rows 16 (w % 4) .. +15 and channels 32 (w / 4) .. +31
 // of every per-row result, held in registers in the m16n8 accumulator layout
 // (thread: rows i0 + g and i0 + g + 8, channel pairs c0 + 8 nt + 2 t).  The one
-// product that contracts over channels (dA) is summed over the two channel
-// halves in two ordered passes.
+// product that contracts over channels (dA) is summed over the four channel
+// quarters in four ordered passes.
 template <bool VEC, typename BetaT>
-__global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
+__global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
+  constexpr int NT = GRAD_NT;
+  constexpr int NTH = GRAD_WARPS * 32;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   GradSmem& sg = *reinterpret_cast<GradSmem*>(smem_raw);
   ChunkSmemBB& s = sg.c;
@@ -461,13 +466,10 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int I = warp & 3, i0 = 16 * I, hc = warp >> 2, c0 = 64 * hc;
+  const int I = warp & 3, i0 = 16 * I, qc = warp >> 2, c0 = 8 * NT * qc;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
   const size_t fo = tf_off(chunk, h, a.HV), so = ts_off(chunk, h, a.HV);
-  // gamma * dgamma of channel tid % 128, for the dg epilogue.
-  const float gdg = __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))]) *
-                    __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + (tid & (DK - 1))]);
   // Whole tiles, stored with these shared pitches, by one bulk copy each: dw
   // and dDelta (the B operands of X and Y) into the staging tiles, dAqk, and
   // the forward's At and T of this chunk.
@@ -497,9 +499,9 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
 
   // v of this thread's accumulator positions, fetched now so that its latency
   // hides behind X, Y and dA.
-  __nv_bfloat162 vpre[8][2];
+  __nv_bfloat162 vpre[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = i0 + g + 8 * hr;
@@ -507,8 +509,8 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
                                       &a.v[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c0 + nt * 8 + 2 * t])
                                 : __floats2bfloat162_rn(0.f, 0.f);
     }
-  // X = T^T dw, Y = T^T dDelta (rows of block I, this warp's channel half)
-  float X[8][4], Y[8][4];
+  // X = T^T dw, Y = T^T dDelta (rows of block I, this warp's channels)
+  float X[NT][4], Y[NT][4];
   zero_acc(X);
   zero_acc(Y);
   {
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
       uint32_t av[4] = {tf32(s.T[ja * LDS + i0 + g]), tf32(s.T[ja * LDS + i0 + g + 8]),
                         tf32(s.T[jb * LDS + i0 + g]), tf32(s.T[jb * LDS + i0 + g + 8])};
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
         uint32_t bx[2] = {tf32(dw[ja * LDF + c]), tf32(dw[jb * LDF + c])};
         uint32_t by[2] = {tf32(dd[ja * LDF + c]), tf32(dd[jb * LDF + c])};
@@ -535,12 +537,12 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
     tc::mbar_arrive_expect_tx(&sg.bar_u, CH * LDF * 4);
     tc::bulk_load(sg.dG, &a.u[fo], CH * LDF * 4, &sg.bar_u);
   }
-  for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
+  for (int e = tid; e < CH * DK / 4; e += NTH) {
     const int i = e >> 5, c4 = (e & 31) * 4;
     cp_async16(&sg.dK[i * LDF + c4], &a.w[w_off(chunk, h, a.HV) + i * LDT + c4]);
   }
   cp_async_commit();
-  // Partial dA over this warp's channel half: X w^T + Y u^T.
+  // Partial dA over this warp's channels: X w^T + Y u^T.
   float dAacc[8][4];
   zero_acc(dAacc);
   cp_async_wait<0>();
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
     const float* w = sg.dK;
     const float* u = sg.dG;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < NT; ++kk) {
       uint32_t ax[4] = {tf32(X[kk][0]), tf32(X[kk][2]), tf32(X[kk][1]), tf32(X[kk][3])};
       uint32_t ay[4] = {tf32(Y[kk][0]), tf32(Y[kk][2]), tf32(Y[kk][1]), tf32(Y[kk][3])};
       const int cc = c0 + kk * 8 + 2 * t;
@@ -573,13 +575,22 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
       }
     }
   }
-  // dA = -strict_tril(sum of the two halves) into s.T (T is no longer read).
-  // The second pass also forms sum_j dA_ij At_ij of its rows (part of dbeta).
+  // dA = -strict_tril(sum over the four quarters) into s.T (T is no longer
+  // read), in quarter order.  The last pass also forms sum_j dA_ij At_ij of its
+  // rows (part of dbeta).
   float* sDA = s.T;
-  if (hc == 0)
+  if (qc == 0)
     acc_foreach(dAacc, [&](int r, int col, float& x) { sDA[(i0 + r) * LDS + col] = col < i0 + r ? -x : 0.f; });
   __syncthreads();
-  if (hc == 1) {
+#pragma unroll
+  for (int pass = 1; pass < 3; ++pass) {
+    if (qc == pass)
+      acc_foreach(dAacc, [&](int r, int col, float& x) {
+        if (col < i0 + r) sDA[(i0 + r) * LDS + col] -= x;
+      });
+    __syncthreads();
+  }
+  if (qc == 3) {
     float p0 = 0.f, p1 = 0.f;
     acc_foreach(dAacc, [&](int r, int col, float& x) {
       const int i = i0 + r;
@@ -594,17 +605,17 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
     p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
     p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
     if (t == 0) {
-      sg.dbeta[2][i0 + g] = p0;
-      sg.dbeta[2][i0 + g + 8] = p1;
+      sg.dbeta[4][i0 + g] = p0;
+      sg.dbeta[4][i0 + g + 8] = p1;
     }
   }
-  // dK, dG: this warp's rows and channel half, accumulator layout.
-  float dKr[8][4], dGr[8][4];
+  // dK, dG: this warp's rows and channels, accumulator layout.
+  float dKr[NT][4], dGr[NT][4];
   // Row-local: dV, dbeta (X.Kp + Y.V), dKp' = beta X Gamma.
   {
     float db0 = 0.f, db1 = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int i = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
@@ -630,46 +641,43 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
     db1 += __shfl_xor_sync(0xffffffffu, db1, 1);
     db1 += __shfl_xor_sync(0xffffffffu, db1, 2);
     if (t == 0) {
-      sg.dbeta[hc][i0 + g] = db0;
-      sg.dbeta[hc][i0 + g + 8] = db1;
+      sg.dbeta[qc][i0 + g] = db0;
+      sg.dbeta[qc][i0 + g + 8] = db1;
     }
   }
   __syncthreads();  // dA complete
   auto kf = [&](int j, int c) { return s.k(j, c); };
   auto qf = [&](int j, int c) { return s.q(j, c); };
-  // dqs at this thread's accumulator positions, fetched ahead of the applies.
-  float2 dqspre[8][2];
+  // dqs at this thread's accumulator positions, fetched ahead of the apply.
+  float2 dqspre[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr)
       dqspre[nt][hr] = __ldg(reinterpret_cast<const float2*>(&a.dqs[toff + (i0 + g + 8 * hr) * DK + c0 + nt * 8 + 2 * t]));
-  // dKp' += beta [dA (x) decay] K  and  dQ = dqs * Gamma + [dAqk (x) decay] K,
-  // one 32-channel half at a time.
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int cq = c0 + 32 * hh;
-    float Z0[4][4], Z1[4][4];
+  // dKp' += beta [dA (x) decay] K  and  dQ = dqs * Gamma + [dAqk (x) decay] K.
+  {
+    float Z0[NT][4], Z1[NT][4];
     zero_acc(Z0);
     zero_acc(Z1);
-    left_apply2<VEC, 4>(s, sDA, sg.dAqk, kf, Z0, Z1, I, cq);
+    left_apply2<VEC, NT>(s, sDA, sg.dAqk, kf, Z0, Z1, I, c0);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        const int i = i0 + g + 8 * hr, c = cq + nt * 8 + 2 * t, n = 4 * hh + nt;
+        const int i = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
         const float bi = s.beta[i];
         const float2 kv = s.k2(i, c), qv = s.q2(i, c), gv = gl2(i, c);
         const float v0 = bi * Z0[nt][2 * hr], v1 = bi * Z0[nt][2 * hr + 1];
-        dKr[n][2 * hr] += v0;
-        dKr[n][2 * hr + 1] += v1;
-        dGr[n][2 * hr] += kv.x * v0;
-        dGr[n][2 * hr + 1] += kv.y * v1;
-        const float2 dqs = dqspre[n][hr];
+        dKr[nt][2 * hr] += v0;
+        dKr[nt][2 * hr + 1] += v1;
+        dGr[nt][2 * hr] += kv.x * v0;
+        dGr[nt][2 * hr + 1] += kv.y * v1;
+        const float2 dqs = dqspre[nt][hr];
         const float dq0 = dqs.x * ex2(gv.x) + Z1[nt][2 * hr];
         const float dq1 = dqs.y * ex2(gv.y) + Z1[nt][2 * hr + 1];
-        dGr[n][2 * hr] += qv.x * dq0;
-        dGr[n][2 * hr + 1] += qv.y * dq1;
+        dGr[nt][2 * hr] += qv.x * dq0;
+        dGr[nt][2 * hr + 1] += qv.y * dq1;
         if (a.dq_part) {
           *reinterpret_cast<float2*>(&a.dq_part[toff + i * DK + c]) = make_float2(dq0, dq1);
         } else if (i < cd.len) {
@@ -679,35 +687,33 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
       }
   }
   // dKd at this thread's accumulator positions, fetched ahead of the last apply.
-  float2 dkdpre[8][2];
+  float2 dkdpre[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr)
       dkdpre[nt][hr] = __ldg(reinterpret_cast<const float2*>(&a.dkd[toff + (i0 + g + 8 * hr) * DK + c0 + nt * 8 + 2 * t]));
-  // dKn' = [dAqk (x) decay]^T Q + [beta dA (x) decay]^T K, one 32-channel half at a time.
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int cq = c0 + 32 * hh;
-    float Z[4][4];
+  // dKn' = [dAqk (x) decay]^T Q + [beta dA (x) decay]^T K.
+  {
+    float Z[NT][4];
     zero_acc(Z);
-    right_apply2<VEC, 4>(s, sg.dAqk, qf, sDA, kf, Z, I, cq);
+    right_apply2<VEC, NT>(s, sg.dAqk, qf, sDA, kf, Z, I, c0);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        const int i = i0 + g + 8 * hr, c = cq + nt * 8 + 2 * t, n = 4 * hh + nt;
+        const int i = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
         const float2 kv = s.k2(i, c);
-        dKr[n][2 * hr] += Z[nt][2 * hr];
-        dKr[n][2 * hr + 1] += Z[nt][2 * hr + 1];
-        dGr[n][2 * hr] -= kv.x * Z[nt][2 * hr];
-        dGr[n][2 * hr + 1] -= kv.y * Z[nt][2 * hr + 1];
+        dKr[nt][2 * hr] += Z[nt][2 * hr];
+        dKr[nt][2 * hr + 1] += Z[nt][2 * hr + 1];
+        dGr[nt][2 * hr] -= kv.x * Z[nt][2 * hr];
+        dGr[nt][2 * hr + 1] -= kv.y * Z[nt][2 * hr + 1];
       }
   }
   // dKd terms, dk, and the column sums of Kd*dKd over this warp's rows.
   {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
       const int c = c0 + nt * 8 + 2 * t;
       const float2 glast = gl2(CH - 1, c);
       float cs0 = 0.f, cs1 = 0.f;
@@ -740,26 +746,27 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
   // The gate adjoint dgc of this warp's positions into the (free) staging tile.
   float* dG = sg.dG;
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr)
       *reinterpret_cast<float2*>(&dG[(i0 + g + 8 * hr) * LDF + c0 + nt * 8 + 2 * t]) =
           make_float2(dGr[nt][2 * hr], dGr[nt][2 * hr + 1]);
   __syncthreads();
   if (VEC) {
-    // Reverse cumsum over rows: threads 128..255 take rows 63..32, threads
-    // 0..127 rows 31..0 starting from the sum of rows 32..63.
-    const int c = tid & (DK - 1), half = tid >> 7;
-    float acc = gdg + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
-    if (half == 0) {
-      float up[4] = {0.f, 0.f, 0.f, 0.f};
+    // Reverse cumsum over rows: thread group r (128 threads, one channel each)
+    // takes rows 16r .. 16r + 15, starting from the sums of the later groups.
+    const int c = tid & (DK - 1), r = tid >> 7;
+    const float gdg = __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + c]) *
+                      __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + c]);
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = CH / 2; i < CH; ++i) up[i & 3] += dG[i * LDF + c];
-      acc += (up[0] + up[1]) + (up[2] + up[3]);
-    }
-    const int hi = half ? CH - 1 : CH / 2 - 1;
-#pragma unroll 8
-    for (int i = hi; i > hi - CH / 2; --i) {
+    for (int i = 0; i < 16; ++i) part[i & 3] += dG[(16 * r + i) * LDF + c];
+    s.tmp[r * DK + c] = (part[0] + part[1]) + (part[2] + part[3]);
+    __syncthreads();
+    float acc = gdg + ((sg.col[c] + sg.col[DK + c]) + (sg.col[2 * DK + c] + sg.col[3 * DK + c]));
+    for (int r2 = 3; r2 > r; --r2) acc += s.tmp[r2 * DK + c];
+#pragma unroll
+    for (int i = 16 * r + 15; i >= 16 * r; --i) {
       acc += dG[i * LDF + c];
       if (i < cd.len) a.dg[((size_t)(cd.tok0 + i) * a.HV + h) * DK + c] = acc;
     }
@@ -768,7 +775,7 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
     // sum_c (gamma dgamma + colsum(Kd dKd)).  Row sums: four threads per row
     // (channels q4, q4 + 4, ...); the chunk-end term: one channel per thread,
     // reduced per warp.
-    {
+    if (tid < 4 * CH) {
       const int row = tid >> 2, q4 = tid & 3;
       float acc = 0.f;
 #pragma unroll 8
@@ -779,7 +786,8 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
     }
     if (tid < DK) {
       const int c = tid;
-      float e = gdg + sg.col[c] + sg.col[DK + c] + sg.col[2 * DK + c] + sg.col[3 * DK + c];
+      float e = __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + c]) * __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + c]) +
+                ((sg.col[c] + sg.col[DK + c]) + (sg.col[2 * DK + c] + sg.col[3 * DK + c]));
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) e += __shfl_xor_sync(0xffffffffu, e, m);
       if (lane == 0) s.tmp[warp] = e;
@@ -795,7 +803,7 @@ __global__ void __launch_bounds__(256, 1) k_grad(GradArgs a) {
   }
   if (tid < cd.len)
     reinterpret_cast<BetaT*>(a.dbeta)[(size_t)(cd.tok0 + tid) * a.HV + h] =
-        from_f<BetaT>((sg.dbeta[0][tid] + sg.dbeta[2][tid]) + sg.dbeta[1][tid]);
+        from_f<BetaT>(((sg.dbeta[0][tid] + sg.dbeta[1][tid]) + (sg.dbeta[2][tid] + sg.dbeta[3][tid])) + sg.dbeta[4][tid]);
 }
 
 // dq / dk of a Q/K head = FP32 sum over its value heads, rounded once.
@@ -853,16 +861,16 @@ cudaError_t launch_grad(const GradArgs& a, int nchunks, bool vec, bool beta_bf16
   dim3 grid(nchunks, a.HV);
   if (vec && beta_bf16) {
     cudaFuncSetAttribute(k_grad<true, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_grad<true, __nv_bfloat16><<<grid, 256, sm, st>>>(a);
+    k_grad<true, __nv_bfloat16><<<grid, GRAD_WARPS * 32, sm, st>>>(a);
   } else if (vec) {
     cudaFuncSetAttribute(k_grad<true, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_grad<true, float><<<grid, 256, sm, st>>>(a);
+    k_grad<true, float><<<grid, GRAD_WARPS * 32, sm, st>>>(a);
   } else if (beta_bf16) {
     cudaFuncSetAttribute(k_grad<false, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_grad<false, __nv_bfloat16><<<grid, 256, sm, st>>>(a);
+    k_grad<false, __nv_bfloat16><<<grid, GRAD_WARPS * 32, sm, st>>>(a);
   } else {
     cudaFuncSetAttribute(k_grad<false, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_grad<false, float><<<grid, 256, sm, st>>>(a);
+    k_grad<false, float><<<grid, GRAD_WARPS * 32, sm, st>>>(a);
   }
   return cudaGetLastError();
 }
