@@ -153,8 +153,8 @@ def source_hash():
 
 
 def ncu_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
+    """DRAM bytes per (token, value head) of `kernel` from the committed ncu
+    summary, if it was taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -163,7 +163,7 @@ def ncu_traffic(kernel: str):
     rec = data.get(kernel)
     if not rec or rec.get("source_hash") != source_hash():
         return None
-    return rec.get("dram_bytes_per_launch")
+    return rec.get("dram_bytes_per_token_head")
 
 
 def oracle_sample(wl, x_host, max_tokens: int):
@@ -305,7 +305,7 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_step = float(tt.item())
     value = world * T / (ms_step / 1e3)
-    gpu_launches = sum(n for n, _ in kern.values())
+    gpu_launches = sum(v[0] for v in kern.values())
 
     # ---- ckpt: forward (no save), forward (save), backward -----------------
     ckpt_ms = None
@@ -394,12 +394,16 @@ def main():
     top = max(kern.items(), key=lambda kv: kv[1][1])[0] if kern else None
     roofline = None
     kernels = {}
-    for name, (n, ms) in kern.items():
+    # A kernel may run as one launch per document group per call (groups on
+    # streams of their own can overlap): bytes per launch = the model's bytes
+    # per (token, value head) x the token-heads of the launch.
+    for name, (n, ms, units_all) in kern.items():
         avg_ms = ms / n
-        entry = {"launches": n, "total_ms": ms, "avg_ms": avg_ms, "share": ms / max(sum(v[1] for v in kern.values()), 1e-9)}
+        entry = {"launches": n, "total_ms": ms, "avg_ms": avg_ms, "share": ms / max(sum(v[1] for v in kern.values()), 1e-9),
+                 "ms_per_call": ms / args.steps}
         if name in KERNEL_MODEL:
             b_th, f_th = KERNEL_MODEL[name]
-            units = T * HV
+            units = units_all / n
             bytes_ = b_th * units
             flops = f_th * units
             gbs = bytes_ / (avg_ms / 1e3) / 1e9
@@ -419,7 +423,8 @@ def main():
             roofline = {"kernel": top, "bound": "tensor", "achieved": k["tflops"], "peak": tf32_peak,
                         "unit": "TFLOP/s", "frac": k["tensor_frac"],
                         "peak_source": pk["source"] + " bf16 x nominal tf32/bf16 ratio"}
-        roofline["traffic"] = ncu_traffic(top)
+        per_th = ncu_traffic(top)
+        roofline["traffic"] = None if per_th is None else per_th * kern[top][2] / kern[top][0]
         roofline["alg_bytes_per_launch"] = k["alg_bytes"]
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ------

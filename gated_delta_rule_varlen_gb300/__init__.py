@@ -45,6 +45,7 @@ EXPORTED = (
     "gdr_check_device",
     "gdr_inject_device_error",
     "gdr_selftest_wait",
+    "gdr_doc_groups",
 )
 
 _lock = threading.Lock()
@@ -64,6 +65,7 @@ _SIGS = {
     "gdr_check_device": ([], ctypes.c_int),
     "gdr_inject_device_error": ([ctypes.c_int], ctypes.c_int),
     "gdr_selftest_wait": ([ctypes.c_uint64, P], ctypes.c_int),
+    "gdr_doc_groups": ([I32, PI32, PI32, ctypes.POINTER(ctypes.c_int64), PI32], ctypes.c_int),
     "gdr_profile_report": ([ctypes.c_char_p, SZ], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
@@ -255,14 +257,26 @@ def gdr_profile_enable(on: bool = True):
 
 
 def gdr_profile_report():
-    """{kernel name: (launches, total_ms)} of the launches recorded while profiling was on."""
+    """{kernel name: (launches, total_ms, token_heads)} of the launches recorded while
+    profiling was on (sums over the launches)."""
     buf = ctypes.create_string_buffer(1 << 16)
     _check(load().gdr_profile_report(buf, len(buf)), "gdr_profile_report")
     out = {}
     for line in buf.value.decode().splitlines():
-        name, n, ms = line.split()
-        out[name] = (int(n), float(ms))
+        name, n, ms, units = line.split()
+        out[name] = (int(n), float(ms), float(units))
     return out
+
+
+def gdr_doc_groups(cu_seqlens_host):
+    """[(rank_begin, rank_end, chunk_begin, chunk_end)] of the backward's document
+    groups for these cu_seqlens (host-side plan; no device work)."""
+    arr, cup = _cu_host(cu_seqlens_host)
+    ranks = (ctypes.c_int32 * 5)()
+    chunks = (ctypes.c_int64 * 5)()
+    n = ctypes.c_int32(0)
+    _check(load().gdr_doc_groups(arr.shape[0] - 1, cup, ranks, chunks, ctypes.byref(n)), "gdr_doc_groups")
+    return [(ranks[i], ranks[i + 1], chunks[i], chunks[i + 1]) for i in range(n.value)]
 
 
 def kda_fwd_noalloc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, out, ht=None, h0=None, stream=None):

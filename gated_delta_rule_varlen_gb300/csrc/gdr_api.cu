@@ -29,17 +29,42 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Planning kernel: document and chunk tables from the device cu_seqlens, and
 // the longest-first document order for the walks (the LPT rule of PR #7723
 // "perf(cake_gdn): prefetch offset adjoint walk, default LPT segment plan",
-// applied here to whole documents on one GPU).  One block; no host copy.
+// applied here to whole documents on one GPU).  Chunks are numbered in that
+// order (the longest document's chunks first), so that any run of documents
+// in it owns one contiguous range of chunks.  Ties go to the lower document
+// index; above kRankLimit documents the order is the given one.  One block; no
+// host copy.  plan_ranks() on the host reproduces the same order.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N, DocDesc* docs, ChunkDesc* chunks,
                                                int* order) {
   __shared__ int part[1024];
   __shared__ int lens[kRankLimit];
+  __shared__ int ord[kRankLimit];
   const int tid = threadIdx.x, nt = blockDim.x;
+  const bool ranked = N <= kRankLimit;
+  if (ranked) {
+    for (int n = tid; n < N; n += nt) lens[n] = cu[n + 1] - cu[n];
+    __syncthreads();
+    for (int n = tid; n < N; n += nt) {
+      const int ln = lens[n];
+      int rank = 0;
+      for (int m = 0; m < N; ++m) rank += (lens[m] > ln) || (lens[m] == ln && m < n);
+      ord[rank] = n;
+      order[rank] = n;
+    }
+  } else {
+    for (int n = tid; n < N; n += nt) order[n] = n;
+  }
+  __syncthreads();
+  auto doc_at = [&](int r) { return ranked ? ord[r] : r; };
+  // Chunk offsets: a prefix sum of chunk counts over the ranks.
   const int per = (N + nt - 1) / nt;
-  const int n0 = min(N, tid * per), n1 = min(N, n0 + per);
+  const int r0 = min(N, tid * per), r1 = min(N, r0 + per);
   int sum = 0;
-  for (int n = n0; n < n1; ++n) sum += (cu[n + 1] - cu[n] + CH - 1) / CH;
+  for (int r = r0; r < r1; ++r) {
+    const int n = doc_at(r);
+    sum += (cu[n + 1] - cu[n] + CH - 1) / CH;
+  }
   part[tid] = sum;
   __syncthreads();
   if (tid == 0) {
@@ -52,24 +77,62 @@ __global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N
   }
   __syncthreads();
   int c = part[tid];
-  for (int n = n0; n < n1; ++n) {
+  for (int r = r0; r < r1; ++r) {
+    const int n = doc_at(r);
     const int tok0 = cu[n], len = cu[n + 1] - tok0, nch = (len + CH - 1) / CH;
     docs[n] = DocDesc{tok0, len, c, nch};
     for (int j = 0; j < nch; ++j) chunks[c + j] = ChunkDesc{tok0 + CH * j, min(CH, len - CH * j), n, j};
     c += nch;
   }
-  if (N <= kRankLimit) {
-    for (int n = tid; n < N; n += nt) lens[n] = cu[n + 1] - cu[n];
-    __syncthreads();
-    for (int n = tid; n < N; n += nt) {
-      const int ln = lens[n];
-      int rank = 0;
-      for (int m = 0; m < N; ++m) rank += (lens[m] > ln) || (lens[m] == ln && m < n);
-      order[rank] = n;
+}
+
+// Host copy of the plan's document order, and the split of the backward into
+// document groups that run on streams of their own: each of the first
+// kMaxSolo documents (longest first) with at least kSoloChunks chunks is a
+// group, and the remaining documents form one more.  A group's chunks are one
+// contiguous range (k_plan numbers them in this order).
+constexpr int kMaxGroups = 4;
+constexpr int kMaxSolo = kMaxGroups - 1;
+constexpr int kSoloChunks = 64;
+struct DocGroup {
+  int r0, r1;        // ranks [r0, r1) of order[]
+  int64_t c0, c1;    // chunks [c0, c1)
+  int64_t tokens;
+};
+std::vector<DocGroup> plan_groups(int32_t N, const int32_t* cu) {
+  std::vector<int> ord(N);
+  for (int n = 0; n < N; ++n) ord[n] = n;
+  if (N <= kRankLimit)
+    std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) { return cu[x + 1] - cu[x] > cu[y + 1] - cu[y]; });
+  std::vector<DocGroup> gr;
+  int64_t c = 0;
+  int r = 0;
+  while (r < N) {
+    const int n = ord[r];
+    const int64_t nch = (cu[n + 1] - cu[n] + CH - 1) / CH;
+    if ((int)gr.size() < kMaxSolo && nch >= kSoloChunks) {
+      gr.push_back(DocGroup{r, r + 1, c, c + nch, (int64_t)(cu[n + 1] - cu[n])});
+      c += nch;
+      ++r;
+      continue;
     }
-  } else {
-    for (int n = tid; n < N; n += nt) order[n] = n;
+    DocGroup g{r, N, c, c, 0};
+    for (; r < N; ++r) {
+      const int m = ord[r];
+      g.c1 += (cu[m + 1] - cu[m] + CH - 1) / CH;
+      g.tokens += cu[m + 1] - cu[m];
+    }
+    gr.push_back(g);
   }
+  if (gr.size() <= 1) {
+    int64_t nc = 0, tok = 0;
+    for (int n = 0; n < N; ++n) {
+      nc += (cu[n + 1] - cu[n] + CH - 1) / CH;
+      tok += cu[n + 1] - cu[n];
+    }
+    return {DocGroup{0, N, 0, nc, tok}};
+  }
+  return gr;
 }
 
 // ---------------------------------------------------------------------------
@@ -307,6 +370,7 @@ int* device_error_ptr() {
 struct ProfRec {
   const char* name;
   cudaEvent_t a, b;
+  double units;  // token-heads the launch works on
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
@@ -323,10 +387,10 @@ void prof_clear_locked() {
 struct ProfScope {
   cudaStream_t st;
   bool on;
-  ProfScope(const char* name, cudaStream_t s) : st(s), on(false) {
+  ProfScope(const char* name, cudaStream_t s, double units = 0) : st(s), on(false) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (!g_prof_on) return;
-    ProfRec r{name, nullptr, nullptr};
+    ProfRec r{name, nullptr, nullptr, units};
     if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
     cudaEventRecord(r.a, st);
     g_prof.push_back(r);
@@ -337,6 +401,77 @@ struct ProfScope {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     cudaEventRecord(g_prof.back().b, st);
   }
+};
+
+// ---------------------------------------------------------------------------
+// Streams the backward's document groups run on (per device, created once,
+// the first with the highest priority), and the fork from / join back to the
+// caller's stream around them.  A single group runs on the caller's stream.
+// ---------------------------------------------------------------------------
+std::mutex g_lane_mu;
+cudaStream_t g_lanes[64][kMaxGroups] = {};
+
+const cudaStream_t* lanes_for_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_lane_mu);
+  if (!g_lanes[dev][kMaxGroups - 1]) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    for (int i = 0; i < kMaxGroups; ++i) {
+      if (g_lanes[dev][i]) continue;
+      const int prio = std::min(least, greatest + i);  // numerically lower = higher priority
+      if (cudaStreamCreateWithPriority(&g_lanes[dev][i], cudaStreamNonBlocking, prio) != cudaSuccess) {
+        g_lanes[dev][i] = nullptr;
+        return nullptr;
+      }
+    }
+  }
+  return g_lanes[dev];
+}
+
+class Fork {
+ public:
+  Fork(cudaStream_t main, int n) : main_(main), n_(n) {}
+  Fork(const Fork&) = delete;
+  Fork& operator=(const Fork&) = delete;
+  // Makes every lane wait for the work already on the caller's stream.
+  bool begin() {
+    if (n_ <= 1) return true;
+    lanes_ = lanes_for_device();
+    if (!lanes_) return false;
+    cudaEvent_t ev;
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return false;
+    bool ok = cudaEventRecord(ev, main_) == cudaSuccess;
+    for (int i = 0; ok && i < n_; ++i) ok = cudaStreamWaitEvent(lanes_[i], ev, 0) == cudaSuccess;
+    cudaEventDestroy(ev);
+    forked_ = ok;
+    return ok;
+  }
+  cudaStream_t lane(int i) const { return n_ > 1 ? lanes_[i] : main_; }
+  // Makes the caller's stream wait for everything enqueued on the lanes.
+  bool join() {
+    if (!forked_) return true;
+    forked_ = false;
+    bool ok = true;
+    for (int i = 0; i < n_; ++i) {
+      cudaEvent_t ev;
+      if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+        ok = false;
+        continue;
+      }
+      ok = cudaEventRecord(ev, lanes_[i]) == cudaSuccess && cudaStreamWaitEvent(main_, ev, 0) == cudaSuccess && ok;
+      cudaEventDestroy(ev);
+    }
+    return ok;
+  }
+  ~Fork() { join(); }
+
+ private:
+  cudaStream_t main_;
+  int n_;
+  const cudaStream_t* lanes_ = nullptr;
+  bool forked_ = false;
 };
 
 
@@ -410,11 +545,6 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   pa.gam = at<float>(base, L.gam);
   pa.amat = save_for_bwd ? at<float>(base, L.amat) : nullptr;
   pa.tmat = save_for_bwd ? at<float>(base, L.tmat) : nullptr;
-  {
-    ProfScope ps("prep", stream);
-    st = cuda_status(launch_prep(pa, (int)NC, vec, vec, stream));
-  }
-  if (st != GDR_OK) return st;
   WalkArgs wa{};
   wa.docs = docs;
   wa.order = order;
@@ -436,9 +566,30 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   wa.ht = ht;
   wa.out = static_cast<__nv_bfloat16*>(out);
   wa.scale = scale;
+  // Document groups as in the backward: each group's walk needs only its own
+  // prep, so the longest document's walk starts once its chunks are prepared.
   {
-    ProfScope ps("walk_fwd", stream);
-    st = cuda_status(launch_walk_fwd(wa, N, walk_tc_cols((int64_t)N * HV), stream));
+    const std::vector<DocGroup> groups = plan_groups(N, cu_host);
+    Fork fork(stream, (int)groups.size());
+    if (!fork.begin()) return GDR_CUDA_ERROR;
+    const int cols = walk_tc_cols((int64_t)N * HV);
+    for (size_t i = 0; i < groups.size() && st == GDR_OK; ++i) {
+      const DocGroup& G = groups[i];
+      const cudaStream_t ls = fork.lane((int)i);
+      const double units = (double)G.tokens * HV;
+      pa.chunk_base = (int)G.c0;
+      wa.rank_base = G.r0;
+      {
+        ProfScope ps("prep", ls, units);
+        st = cuda_status(launch_prep(pa, (int)(G.c1 - G.c0), vec, vec, ls));
+      }
+      if (st != GDR_OK) break;
+      {
+        ProfScope ps("walk_fwd", ls, units);
+        st = cuda_status(launch_walk_fwd(wa, G.r1 - G.r0, cols, ls));
+      }
+    }
+    if (!fork.join() && st == GDR_OK) st = GDR_CUDA_ERROR;
   }
   if (st != GDR_OK) return st;
   if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, hash_cu(cu_host, N)});
@@ -489,11 +640,6 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   wb.dh0 = dh0;
   wb.err = device_error_ptr();
   if (!wb.err) return GDR_CUDA_ERROR;
-  {
-    ProfScope ps("walk_bwd", stream);
-    st = cuda_status(launch_walk_bwd(wb, N, walk_warps((int64_t)N * HV), stream));
-  }
-  if (st != GDR_OK) return st;
 
   GradStateArgs gs{};
   gs.chunks = chunks;
@@ -511,11 +657,6 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   gs.daqk = at<float>(scratch, L.daqk);
   gs.err = wb.err;
   if (NC > 0 && !bf16_map(&gs.s0_map, gs.tape, (uint64_t)NC * HV * DK, DK, DK)) return GDR_CUDA_ERROR;
-  {
-    ProfScope ps("grad_state", stream);
-    st = cuda_status(launch_grad_state(gs, (int)NC, stream));
-  }
-  if (st != GDR_OK) return st;
 
   GradArgs ga{};
   ga.q = static_cast<const __nv_bfloat16*>(q);
@@ -551,26 +692,51 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   ga.dk_part = grouped ? at<float>(scratch, L.dkp) : nullptr;
   ga.dg = dg;
   ga.dbeta = dbeta;
-  {
-    ProfScope ps("grad", stream);
-    st = cuda_status(launch_grad(ga, (int)NC, vec, vec, stream));
-  }
-  if (st != GDR_OK) return st;
-  if (grouped) {
-    GroupReduceArgs gr{};
-    gr.chunks = chunks;
-    gr.Hqk = Hqk;
-    gr.HV = HV;
-    gr.dq_part = ga.dq_part;
-    gr.dk_part = ga.dk_part;
-    gr.dq = ga.dq;
-    gr.dk = ga.dk;
+  GroupReduceArgs gr{};
+  gr.chunks = chunks;
+  gr.Hqk = Hqk;
+  gr.HV = HV;
+  gr.dq_part = ga.dq_part;
+  gr.dk_part = ga.dk_part;
+  gr.dq = ga.dq;
+  gr.dk = ga.dk;
+
+  // Document groups (longest documents first, each on a stream of its own):
+  // a group's gradient kernels need only its own walk, so the gradients of the
+  // documents whose walks end first run on the SMs the other walks leave idle.
+  const std::vector<DocGroup> groups = plan_groups(N, cu_host);
+  Fork fork(stream, (int)groups.size());
+  if (!fork.begin()) return GDR_CUDA_ERROR;
+  const int nw = walk_warps((int64_t)N * HV);
+  for (size_t i = 0; i < groups.size() && st == GDR_OK; ++i) {
+    const DocGroup& G = groups[i];
+    const cudaStream_t ls = fork.lane((int)i);
+    const double units = (double)G.tokens * HV;
+    const int nc = (int)(G.c1 - G.c0);
+    wb.rank_base = G.r0;
+    gs.chunk_base = ga.chunk_base = gr.chunk_base = (int)G.c0;
     {
-      ProfScope ps("group_reduce", stream);
-      st = cuda_status(launch_group_reduce(gr, (int)NC, stream));
+      ProfScope ps("walk_bwd", ls, units);
+      st = cuda_status(launch_walk_bwd(wb, G.r1 - G.r0, nw, ls));
     }
-    if (st != GDR_OK) return st;
+    if (st != GDR_OK) break;
+    {
+      ProfScope ps("grad_state", ls, units);
+      st = cuda_status(launch_grad_state(gs, nc, ls));
+    }
+    if (st != GDR_OK) break;
+    {
+      ProfScope ps("grad", ls, units);
+      st = cuda_status(launch_grad(ga, nc, vec, vec, ls));
+    }
+    if (st != GDR_OK || !grouped) continue;
+    {
+      ProfScope ps("group_reduce", ls, units);
+      st = cuda_status(launch_group_reduce(gr, nc, ls));
+    }
   }
+  if (!fork.join() && st == GDR_OK) st = GDR_CUDA_ERROR;
+  if (st != GDR_OK) return st;
   return GDR_OK;
 }
 
@@ -690,6 +856,27 @@ gdr_status kda_fwd_noalloc(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16*
                        0, scratch, gdr::kStaticScratchBytes, stream);
 }
 
+gdr_status gdr_doc_groups(int32_t N, const int32_t* cu_seqlens_host, int32_t* rank_bounds, int64_t* chunk_bounds,
+                          int32_t* n_groups) {
+  if (N < 0 || !cu_seqlens_host || !rank_bounds || !chunk_bounds || !n_groups) return GDR_INVALID_ARG;
+  if (cu_seqlens_host[0] != 0) return GDR_BAD_CU_SEQLENS;
+  for (int32_t n = 0; n < N; ++n)
+    if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return GDR_BAD_CU_SEQLENS;
+  if (N == 0) {
+    *n_groups = 0;
+    return GDR_OK;
+  }
+  const std::vector<gdr::DocGroup> g = gdr::plan_groups(N, cu_seqlens_host);
+  *n_groups = (int32_t)g.size();
+  for (size_t i = 0; i < g.size(); ++i) {
+    rank_bounds[i] = g[i].r0;
+    rank_bounds[i + 1] = g[i].r1;
+    chunk_bounds[i] = g[i].c0;
+    chunk_bounds[i + 1] = g[i].c1;
+  }
+  return GDR_OK;
+}
+
 gdr_status gdr_inject_device_error(int code) {
   if (code <= 0) return GDR_INVALID_ARG;
   int* p = gdr::device_error_ptr();
@@ -728,25 +915,26 @@ int gdr_profile_enable(int on) {
 
 gdr_status gdr_profile_report(char* buf, size_t buf_bytes) {
   std::lock_guard<std::mutex> lk(gdr::g_prof_mu);
-  std::map<std::string, std::pair<int, double>> agg;
+  struct Agg {
+    int n = 0;
+    double ms = 0, units = 0;
+  };
+  std::map<std::string, Agg> agg;
   std::vector<std::string> order;
   for (auto& r : gdr::g_prof) {
     if (cudaEventSynchronize(r.b) != cudaSuccess) return GDR_CUDA_ERROR;
     float ms = 0.f;
     if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return GDR_CUDA_ERROR;
-    auto it = agg.find(r.name);
-    if (it == agg.end()) {
-      order.push_back(r.name);
-      agg[r.name] = {1, (double)ms};
-    } else {
-      it->second.first += 1;
-      it->second.second += ms;
-    }
+    if (agg.find(r.name) == agg.end()) order.push_back(r.name);
+    Agg& a = agg[r.name];
+    a.n += 1;
+    a.ms += ms;
+    a.units += r.units;
   }
   std::string out;
   for (auto& n : order) {
-    char line[160];
-    std::snprintf(line, sizeof(line), "%s %d %.6f\n", n.c_str(), agg[n].first, agg[n].second);
+    char line[200];
+    std::snprintf(line, sizeof(line), "%s %d %.6f %.0f\n", n.c_str(), agg[n].n, agg[n].ms, agg[n].units);
     out += line;
   }
   if (!buf || buf_bytes < out.size() + 1) return GDR_INVALID_ARG;

@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
   extern __shared__ __align__(16) unsigned char smraw[];
   SA* sa = reinterpret_cast<SA*>(smraw);
   WalkBwdB& sb = *reinterpret_cast<WalkBwdB*>(smraw + 2 * sizeof(SA));
-  const int rank = blockIdx.x / (a.HV * VS);  // longest document first, all its heads
+  const int rank = a.rank_base + blockIdx.x / (a.HV * VS);  // longest document first, all its heads
   const int h = (blockIdx.x / VS) % a.HV;
   const int doc = a.order[rank];
   const DocDesc dd = a.docs[doc];
@@ -239,7 +239,7 @@ struct GradStateSmem {
 __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ GradStateArgs a) {
   extern __shared__ unsigned char smraw[];
   GradStateSmem& s = *reinterpret_cast<GradStateSmem*>(tc::align1024(smraw));
-  const int chunk = blockIdx.x, h = blockIdx.y;
+  const int chunk = a.chunk_base + blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   const size_t toff = tile_off(chunk, h, a.HV);
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   GradSmem& sg = *reinterpret_cast<GradSmem*>(smem_raw);
   ChunkSmemBB& s = sg.c;
-  const int chunk = blockIdx.x, h = blockIdx.y;
+  const int chunk = a.chunk_base + blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
 
 // dq / dk of a Q/K head = FP32 sum over its value heads, rounded once.
 __global__ void __launch_bounds__(256) k_group_reduce(GroupReduceArgs a) {
-  const int chunk = blockIdx.x, hq = blockIdx.y;
+  const int chunk = a.chunk_base + blockIdx.x, hq = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int G = a.HV / a.Hqk;
   for (int e = threadIdx.x; e < cd.len * DK; e += blockDim.x) {

@@ -18,7 +18,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ChunkSmemB& s = *reinterpret_cast<ChunkSmemB*>(smem_raw);
   constexpr int LDK = ChunkSmemB::LD;
-  const int chunk = blockIdx.x, h = blockIdx.y;
+  const int chunk = a.chunk_base + blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(160) k_walk_fwd(const __grid_constant__ WalkAr
   constexpr uint32_t K_BYTES = (DK * CH + CH * CH) * 4;
   extern __shared__ unsigned char smraw[];
   WalkTcSmem<N>& s = *reinterpret_cast<WalkTcSmem<N>*>(tc::align1024(smraw));
-  const int rank = blockIdx.x / (a.HV * VS);  // all heads and slices of the longest document first
+  const int rank = a.rank_base + blockIdx.x / (a.HV * VS);  // all heads and slices of the longest document first
   const int h = (blockIdx.x / VS) % a.HV;
   const int doc = a.order[rank];
   const DocDesc dd = a.docs[doc];

@@ -21,6 +21,7 @@ struct PrepArgs {
   int Hqk, HV;
   float *w, *u, *qp, *kd, *aqk, *gam;  // w, qp, kd, aqk with the padded pitches of gdr_common.cuh
   float *amat, *tmat;  // At and T per chunk ([64][64] FP32), or null when nothing is saved
+  int chunk_base;      // block x works on chunk chunk_base + x
 };
 
 struct WalkArgs {
@@ -41,6 +42,7 @@ struct WalkArgs {
   __nv_bfloat16* out;  // [T][HV][128]
   float scale;
   int* err;          // device error word
+  int rank_base;     // documents order[rank_base ..] (longest first)
 };
 
 
@@ -57,6 +59,7 @@ struct WalkBwdArgs {
   float* ddelta;              // dDelta per chunk
   float* dh0;                 // or null
   int* err;                   // device error word
+  int rank_base;              // documents order[rank_base ..] (longest first)
 };
 
 struct GradStateArgs {
@@ -70,6 +73,7 @@ struct GradStateArgs {
   float *dqs, *dw, *dkd, *dgam;  // scratch outputs
   float* daqk;                   // scale * tril(dO Delta^T), [NC][HV][64][64]
   int* err;                      // device error word
+  int chunk_base;                // block x works on chunk chunk_base + x
 };
 
 struct GradArgs {
@@ -89,6 +93,7 @@ struct GradArgs {
   float* dg;
   void* dbeta;
   int* err;  // device error word
+  int chunk_base;  // block x works on chunk chunk_base + x
 };
 
 struct GroupReduceArgs {
@@ -96,6 +101,7 @@ struct GroupReduceArgs {
   int Hqk, HV;
   const float *dq_part, *dk_part;
   __nv_bfloat16 *dq, *dk;
+  int chunk_base;  // block x works on chunk chunk_base + x
 };
 
 cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);

@@ -177,6 +177,20 @@ gdr_status gdr_check_device(void);
  * Device error codes: 3 forward walk, 4 backward walk, 5 this self-test,
  * 6 state-side gradient products, 7 chunk-local gradients. */
 gdr_status gdr_inject_device_error(int code);
+
+/* Host-side plan of the backward's document groups (no device work).  The
+ * backward ranks the documents longest first (ties: lower index first; above
+ * 4096 documents the given order), numbers chunks in that order, and runs
+ * each group's walk and gradient kernels on a stream of its own: each of the
+ * first 3 documents with at least 64 chunks is a group, the remaining
+ * documents form one more (a single group when that leaves one).  Writes
+ * *n_groups (at most 4) and the group bounds: group i holds ranks
+ * [rank_bounds[i], rank_bounds[i+1]) and chunks [chunk_bounds[i],
+ * chunk_bounds[i+1]); both arrays need room for 5 entries.  Errors:
+ * GDR_INVALID_ARG for null pointers or N < 0, GDR_BAD_CU_SEQLENS for a
+ * cu_seqlens that does not start at 0 or decreases. */
+gdr_status gdr_doc_groups(int32_t N, const int32_t* cu_seqlens_host, int32_t* rank_bounds, int64_t* chunk_bounds,
+                          int32_t* n_groups);
 gdr_status gdr_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
 
 /* Benchmark support (no counterpart on the pages): opt-in per-kernel timing.
@@ -184,9 +198,11 @@ gdr_status gdr_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
  * kernel launch of this library record a pair of CUDA events on its stream;
  * gdr_profile_enable(0) stops recording and keeps the records for the report.  gdr_profile_report synchronizes the
  * recorded events and writes one line per kernel, "<name> <launches>
- * <total_ms>\n", in first-launch order, NUL-terminated, into buf; it returns
- * GDR_INVALID_ARG if buf_bytes is too small.  Kernel names: plan, prep,
- * walk_fwd, walk_bwd, grad_state, grad, group_reduce. */
+ * <total_ms> <token_heads>\n" (the sum over its launches of their durations
+ * and of the (token, value head) pairs each worked on; launches of different
+ * document groups may overlap in time), in first-launch order, NUL-terminated,
+ * into buf; it returns GDR_INVALID_ARG if buf_bytes is too small.  Kernel
+ * names: plan, prep, walk_fwd, walk_bwd, grad_state, grad, group_reduce. */
 int gdr_profile_enable(int on);
 gdr_status gdr_profile_report(char* buf, size_t buf_bytes);
 
