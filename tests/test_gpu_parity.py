@@ -88,6 +88,36 @@ def test_packed_equals_per_document_bitwise():
         assert torch.equal(whole["dh0"][n], one["dh0"][0])
 
 
+def test_kda_document_groups_on_their_own_streams():
+    # Three documents of at least 64 chunks run as groups of their own, the rest as one more
+    # (four streams in the forward and the backward); every element against the oracle.
+    import gated_delta_rule_varlen_gb300 as gdr
+    lengths = [4200, 130, 4096, 0, 4500, 64]
+    assert len(gdr.gdr_doc_groups(synth.cu_from_lengths(lengths))) == 4
+    _check("kda", lengths, 2, 2, seed=13, h0=True, dht=True)
+
+
+def test_gdn_document_groups_on_their_own_streams():
+    import gated_delta_rule_varlen_gb300 as gdr
+    lengths = [100, 4160, 5000]
+    assert len(gdr.gdr_doc_groups(synth.cu_from_lengths(lengths))) == 3
+    _check("gdn", lengths, 1, 2, seed=14, h0=True, dht=True)
+
+
+def test_grouped_pack_equals_per_document_bitwise():
+    lengths = [4200, 70, 4096, 4500]
+    x, cu, h0, dht = _case("kda", lengths, 2, 2, seed=15, h0=True, dht=True)
+    whole = run_gpu("kda", x, cu, h0=h0, dht=dht, want_dh0=True)
+    for n in range(len(lengths)):
+        s, e = cu[n], cu[n + 1]
+        xs = {k: v[s:e] for k, v in x.items()}
+        one = run_gpu("kda", xs, [0, e - s], h0=h0[n:n + 1], dht=dht[n:n + 1], want_dh0=True)
+        for name in ("out", "dq", "dk", "dv", "dg", "dbeta"):
+            assert torch.equal(whole[name][s:e], one[name]), name
+        assert torch.equal(whole["ht"][n], one["ht"][0])
+        assert torch.equal(whole["dh0"][n], one["dh0"][0])
+
+
 def test_repeat_is_bitwise_deterministic():
     x, cu, h0, dht = _case("gdn", [200, 333], 2, 6, seed=9)
     a = run_gpu("gdn", x, cu)
