@@ -51,7 +51,13 @@
  *   - Errors are returned as gdr_status, never thrown; a call that returns an
  *     error has enqueued nothing (except GDR_CUDA_ERROR from a launch).
  *   - Calls on one stream are ordered; calls that share a workspace must not
- *     overlap on the GPU.
+ *     overlap on the GPU.  Inside a call, packs whose longest documents have
+ *     at least 64 chunks run their document groups (see gdr_doc_groups) on up
+ *     to four internal streams of the current device (created on first use,
+ *     shared by all callers, highest priority first), forked from and joined
+ *     back to the caller's stream with events; the call's work is still
+ *     ordered after the stream's earlier work and before its later work,
+ *     also under stream capture.
  *   - Results are deterministic (no floating-point atomics).
  */
 #ifndef GDR_H_
