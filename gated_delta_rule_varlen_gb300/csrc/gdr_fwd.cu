@@ -38,12 +38,16 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   // Qp, Kd, gamma (elementwise; factors exp(gc) and exp(gc_last - gc) are <= 1).
   // Qp and Kd are only ever MMA operands: stored rounded to TF32.
   const size_t toff = tile_off(chunk, h, a.HV);
-  for (int e = tid; e < CH * DK; e += blockDim.x) {
-    const int i = e >> 7, d = e & 127;
-    const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
-    const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
-    a.qp[qp_off(chunk, h, a.HV) + i * LDF + d] = __uint_as_float(tf32(s.q(i, d) * ex2(gl)));
-    if (i == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d] = ex2(glast);
+  for (int e = tid; e < CH * DK / 4; e += blockDim.x) {  // four channels per thread, one 16-byte store
+    const int i = e >> 5, d = (e & 31) * 4;
+    float r[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float gl = VEC ? s.G[i * LDT + d + q] : s.gs[i];
+      r[q] = __uint_as_float(tf32(s.q(i, d + q) * ex2(gl)));
+      if (i == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d + q] = ex2(VEC ? s.G[(CH - 1) * LDT + d + q] : s.gs[CH - 1]);
+    }
+    *reinterpret_cast<float4*>(&a.qp[qp_off(chunk, h, a.HV) + i * LDF + d]) = make_float4(r[0], r[1], r[2], r[3]);
   }
   // Kd stored transposed, [c][j] (the K-major A operand of the walk's state update).
   // A warp covers rows i = 8k .. 8k+7 of channels d .. d+3 (lane bits 0-2 -> i,
@@ -96,7 +100,15 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
           mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
                        [&](int j, int c) { return bw(j, c0 + c); });
       }
-      acc_foreach(acc, [&](int r, int c, float& x) { out[(i0 + r) * ldo + c0 + c] = __uint_as_float(tf32(x)); });
+      {  // rows i0 + g (+8), channel pairs c0 + 8 nt + 2 t: 8-byte stores
+        const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr)
+            *reinterpret_cast<float2*>(&out[(i0 + g + 8 * hr) * ldo + c0 + nt * 8 + 2 * t]) = make_float2(
+                __uint_as_float(tf32(acc[nt][2 * hr])), __uint_as_float(tf32(acc[nt][2 * hr + 1])));
+      }
     }
   }
 }

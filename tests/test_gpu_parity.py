@@ -232,3 +232,33 @@ def test_fullsize_gdn_sampled_chains(name, samples):
     for k in ("out", "dq", "dk", "dv", "dg", "dbeta"):
         assert torch.isfinite(gpu[k]).all(), k
     _sample_check(wl, x, gpu, samples)
+
+
+def test_graph_capture_of_grouped_fwd_bwd_replays_bitwise():
+    # The document groups fork onto internal streams; a captured fwd + bwd must replay to the
+    # eager results, bit for bit.
+    import gated_delta_rule_varlen_gb300 as gdr
+    lengths = [4200, 130, 4096, 4500]
+    x, cu, _, _ = _case("kda", lengths, 1, 1, seed=16)
+    xd = {k: v.cuda() for k, v in x.items()}
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+
+    def step():
+        out, ht, saved = gdr.kda_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE)
+        grads = gdr.kda_bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE, xd["dout"], saved)
+        return out, ht, grads
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        eager = step()  # also creates the library's internal streams before the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = step()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(cap[0], eager[0]) and torch.equal(cap[1], eager[1])
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(cap[2][name], eager[2][name]), name
