@@ -69,3 +69,13 @@ def test_bad_cu_seqlens():
     with pytest.raises(ValueError):
         gdr.gdr_doc_groups(np.array([0, 5, 3], dtype=np.int32))
     assert gdr.gdr_doc_groups(np.array([0], dtype=np.int32)) == []
+
+
+def test_above_the_ranking_limit_the_given_order_is_kept():
+    # Above 4096 documents the plan keeps the given order (no ranking), on the device and here.
+    lengths = [10] * 4097 + [10000]
+    g = gdr.gdr_doc_groups(_cu(lengths))
+    assert g == [(0, 4098, 0, 4097 + 157)]
+    lengths = [10000] + [10] * 4097
+    g = gdr.gdr_doc_groups(_cu(lengths))
+    assert g == [(0, 1, 0, 157), (1, 4098, 157, 157 + 4097)]
