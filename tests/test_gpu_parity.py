@@ -104,6 +104,15 @@ def test_gdn_document_groups_on_their_own_streams():
     _check("gdn", lengths, 1, 2, seed=14, h0=True, dht=True)
 
 
+def test_more_documents_than_the_ranking_limit():
+    # Above 4096 documents the plan keeps the given order; the long first document is still a
+    # group of its own.
+    import gated_delta_rule_varlen_gb300 as gdr
+    lengths = [10000] + [10] * 4097
+    assert len(gdr.gdr_doc_groups(synth.cu_from_lengths(lengths))) == 2
+    _check("kda", lengths, 1, 1, seed=17)
+
+
 def test_grouped_pack_equals_per_document_bitwise():
     lengths = [4200, 70, 4096, 4500]
     x, cu, h0, dht = _case("kda", lengths, 2, 2, seed=15, h0=True, dht=True)
