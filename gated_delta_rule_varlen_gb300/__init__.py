@@ -159,9 +159,28 @@ def _empty_bytes(n, device):
     return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
 
 
+def _check_shapes(variant, q, k, v, g, beta, dout=None):
+    """Shapes the C ABI assumes (it receives pointers only): q, k [T, Hqk, 128]; v (and dout)
+    [T, HV, 128]; g [T, HV, 128] (KDA) or [T, HV] (GDN); beta [T, HV]; Hqk == HV for KDA."""
+    T, Hqk, D = q.shape
+    HV = v.shape[1]
+    want = {"k": (k, (T, Hqk, D)), "v": (v, (T, HV, D)), "beta": (beta, (T, HV)),
+            "g": (g, (T, HV, D) if variant == "kda" else (T, HV))}
+    if dout is not None:
+        want["dout"] = (dout, (T, HV, D))
+    for name, (t, shape) in want.items():
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{variant}: {name} has shape {tuple(t.shape)}, expected {shape}")
+    if D != 128:
+        raise ValueError(f"{variant}: head dim {D}, only 128 is supported")
+    if variant == "kda" and Hqk != HV:
+        raise ValueError(f"kda: q/k have {Hqk} heads and v has {HV}; KDA needs the same count")
+
+
 def _fwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out, ht, want_ht, saved,
          save_for_bwd, scratch, stream):
     import torch
+    _check_shapes(variant, q, k, v, g, beta)
     T, Hqk, D = q.shape
     HV = v.shape[1]
     arr, cup = _cu_host(cu_seqlens_host)
@@ -193,6 +212,7 @@ def _fwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out,
 def _bwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0, scratch,
          grads, stream):
     import torch
+    _check_shapes(variant, q, k, v, g, beta, dout)
     T, Hqk, D = q.shape
     HV = v.shape[1]
     arr, cup = _cu_host(cu_seqlens_host)
@@ -283,6 +303,7 @@ def kda_fwd_noalloc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, out, h
     """KDA forward whose intermediates live in the library's fixed 64 MiB device
     array (for callers that cannot allocate; see include/gdr.h).  `out` (and
     `ht`, if wanted) must be preallocated: this wrapper allocates nothing."""
+    _check_shapes("kda", q, k, v, g, beta)
     T, H, _ = q.shape
     arr, cup = _cu_host(cu_seqlens_host)
     st = load().kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), cup,

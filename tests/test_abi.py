@@ -163,3 +163,24 @@ def test_diagnostics_validate_arguments_before_any_cuda_call(gdr):
     assert lib.gdr_inject_device_error(-3) == gdr.GDR_INVALID_ARG
     assert lib.gdr_selftest_wait(0, None) == gdr.GDR_INVALID_ARG
     assert lib.gdr_selftest_wait(100000001, None) == gdr.GDR_INVALID_ARG
+
+
+def test_binding_rejects_mismatched_shapes_before_any_device_work(gdr):
+    # The C ABI receives pointers only; the binding checks the shapes it derives sizes from.
+    import torch
+    T = 10
+    q = torch.zeros(T, 2, 128, dtype=torch.bfloat16)
+    v = torch.zeros(T, 2, 128, dtype=torch.bfloat16)
+    g = torch.zeros(T, 2, 128)
+    beta = torch.zeros(T, 2, dtype=torch.bfloat16)
+    cu = [0, T]
+    with pytest.raises(ValueError):  # KDA needs as many q/k heads as v heads
+        gdr.kda_fwd(q[:, :1], q[:, :1], v, g, beta, None, cu, 1.0)
+    with pytest.raises(ValueError):  # KDA gate is per channel
+        gdr.kda_fwd(q, q, v, g[:, :, 0], beta, None, cu, 1.0)
+    with pytest.raises(ValueError):  # GDN gate is per head
+        gdr.gdn_fwd(q, q, v, g, beta.float(), None, cu, 1.0)
+    with pytest.raises(ValueError):  # dout shaped like v
+        gdr.kda_bwd(q, q, v, g, beta, None, cu, 1.0, v[:, :1], None)
+    with pytest.raises(ValueError):  # head dim 128 only
+        gdr.kda_fwd(q[..., :64], q[..., :64], v[..., :64], g[..., :64], beta, None, cu, 1.0)

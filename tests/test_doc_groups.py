@@ -79,3 +79,10 @@ def test_above_the_ranking_limit_the_given_order_is_kept():
     lengths = [10000] + [10] * 4097
     g = gdr.gdr_doc_groups(_cu(lengths))
     assert g == [(0, 1, 0, 157), (1, 4098, 157, 157 + 4097)]
+
+
+def test_last_group_may_hold_only_empty_documents():
+    lengths = [4200, 4096, 0, 4500]
+    g = gdr.gdr_doc_groups(_cu(lengths))
+    assert g == [(0, 1, 0, 71), (1, 2, 71, 137), (2, 3, 137, 201), (3, 4, 201, 201)]
+    _check_cover(g, lengths)

@@ -104,6 +104,19 @@ def test_gdn_document_groups_on_their_own_streams():
     _check("gdn", lengths, 1, 2, seed=14, h0=True, dht=True)
 
 
+def test_document_groups_with_an_empty_last_group():
+    # Three long documents stand alone; the remaining group holds only an empty document, whose
+    # final state is its initial state and whose dh0 is its dht.
+    import gated_delta_rule_varlen_gb300 as gdr
+    lengths = [4200, 4096, 0, 4500]
+    groups = gdr.gdr_doc_groups(synth.cu_from_lengths(lengths))
+    assert len(groups) == 4 and groups[3][2] == groups[3][3]
+    gpu, _ = _check("kda", lengths, 2, 2, seed=18, h0=True, dht=True)
+    x, cu, h0, dht = _case("kda", lengths, 2, 2, seed=18, h0=True, dht=True)
+    assert torch.equal(gpu["ht"][2].cpu(), h0[2])
+    assert torch.equal(gpu["dh0"][2].cpu(), dht[2])
+
+
 def test_more_documents_than_the_ranking_limit():
     # Above 4096 documents the plan keeps the given order; the long first document is still a
     # group of its own.
