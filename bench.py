@@ -31,6 +31,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KDA fwd+bwd tokens/s (T=261392, H=16, D=128, 1 GB300); % of roofline"
+# The five workloads whose fwd, bwd and ckpt are reported in the line's "configs".
+CONFIGS = ("kda_tiny", "kda_pack_h4", "kda_pack_h16", "kda_pack_h64", "gdn_p1", "gdn_1doc")
 UNIT = "tokens/s"
 
 # Algorithmic bytes and FLOPs per (token, value head) of each kernel: every
@@ -65,6 +67,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ckpt", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     return ap.parse_args()
 
 
@@ -220,6 +223,96 @@ def run_reference(args):
     return 0
 
 
+# Minimal I/O of one call (SURVEY §8(d) "algorithmic bytes"): every input read
+# once and every output written once, per token (all heads).
+def io_bytes(variant: str, Hqk: int, HV: int):
+    qk = 2 * Hqk * D * 2
+    vrow = HV * D * 2
+    gate = HV * D * 4 if variant == "kda" else HV * 4
+    beta = HV * 2 if variant == "kda" else HV * 4
+    fwd = qk + vrow + gate + beta + vrow                      # q, k, v, g, beta -> out
+    bwd = (qk + vrow + gate + beta + vrow) + (qk + vrow + gate + beta)  # + dout -> dq, dk, dv, dg, dbeta
+    return fwd, bwd
+
+
+# Chunked-algorithm flops per (token, value head): forward
+# 140.6 kflop, backward 282.6 kflop.  GDN shares its Gram products across the
+# value heads of a Q/K head; the KDA count is used for it too (an upper bound).
+FLOPS_FWD, FLOPS_BWD = 140.6e3, 282.6e3
+
+
+def binding_roofline(variant, T, Hqk, HV, ms, pk, kind="fwd+bwd"):
+    fb, bb = io_bytes(variant, Hqk, HV)
+    per_tok = {"fwd": fb, "bwd": bb, "fwd+bwd": fb + bb, "ckpt": 2 * fb + bb}[kind]
+    per_th_fl = {"fwd": FLOPS_FWD, "bwd": FLOPS_BWD, "fwd+bwd": FLOPS_FWD + FLOPS_BWD,
+                 "ckpt": 2 * FLOPS_FWD + FLOPS_BWD}[kind]
+    nbytes = per_tok * T
+    flops = per_th_fl * T * HV
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops_sustained"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return {"bound": bound, "alg_bytes": nbytes, "alg_flops": flops, "t_hbm_ms": 1e3 * t_hbm, "t_tc_ms": 1e3 * t_tc,
+            "frac": 1e3 * max(t_hbm, t_tc) / ms}
+
+
+class Workload:
+    """Device inputs, outputs and workspaces of one workload, and its calls."""
+
+    def __init__(self, name, dev, seed=0):
+        import torch
+        import gated_delta_rule_varlen_gb300 as gdr
+        import synth
+        self.wl = wl = synth.workload(name)
+        self.T, self.Hqk, self.HV = wl.T, wl.Hqk, wl.HV
+        self.cu_host = wl.cu_seqlens
+        self.x = synth.make_inputs(wl.variant, wl.T, wl.Hqk, wl.HV, D, seed=seed, device=dev)
+        self.cu_d = torch.tensor(self.cu_host, dtype=torch.int32, device=dev)
+        self.scale = D ** -0.5
+        kda = wl.variant == "kda"
+        self.fwd = gdr.kda_fwd if kda else gdr.gdn_fwd
+        self.bwd = gdr.kda_bwd if kda else gdr.gdn_bwd
+        wsb = (gdr.kda_workspace_bytes(wl.T, wl.HV, self.cu_host) if kda
+               else gdr.gdn_workspace_bytes(wl.T, wl.Hqk, wl.HV, self.cu_host))
+        self.saved = torch.empty(wsb[0], dtype=torch.uint8, device=dev)
+        self.scratch = torch.empty(max(wsb), dtype=torch.uint8, device=dev)
+        x = self.x
+        self.out = torch.empty((wl.T, wl.HV, D), dtype=torch.bfloat16, device=dev)
+        self.ht = torch.empty((len(wl.lengths), wl.HV, D, D), dtype=torch.float32, device=dev)
+        self.grads = {"dq": torch.empty_like(x["q"]), "dk": torch.empty_like(x["k"]), "dv": torch.empty_like(x["v"]),
+                      "dg": torch.empty_like(x["g"]), "dbeta": torch.empty_like(x["beta"])}
+
+    def fwd_call(self, save=True, xx=None, out=None):
+        xx = xx or self.x
+        return self.fwd(xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], self.cu_d, self.cu_host, self.scale,
+                        out=self.out if out is None else out, ht=self.ht, saved=self.saved if save else None,
+                        save_for_bwd=save, scratch=None if save else self.scratch)
+
+    def bwd_call(self, xx=None, grads=None):
+        xx = xx or self.x
+        return self.bwd(xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], self.cu_d, self.cu_host, self.scale,
+                        xx["dout"], self.saved, scratch=self.scratch, grads=self.grads if grads is None else grads)
+
+
+def time_steps(w, stream, flush, nsteps, ckpt=False):
+    """Per-step CUDA-event times (ms) of fwd(save) + bwd (fwd and bwd split),
+    or of the ckpt sequence fwd(no save) + fwd(save) + bwd; L2 flushed before
+    each step (outside the events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(nsteps)]
+    for e0, e1, e2 in evs:
+        flush.zero_()
+        e0.record(stream)
+        if ckpt:
+            w.fwd_call(save=False)
+        w.fwd_call()
+        e1.record(stream)
+        w.bwd_call()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b, _ in evs], [b.elapsed_time(c) for _, b, c in evs]
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -229,7 +322,6 @@ def main():
     import torch.distributed as dist
 
     import gated_delta_rule_varlen_gb300 as gdr
-    import synth
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -237,33 +329,12 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     gdr.load()
+    pk = peaks()
 
-    wl = synth.workload(args.workload)
-    T, Hqk, HV = wl.T, wl.Hqk, wl.HV
-    cu_host = wl.cu_seqlens
-    x = synth.make_inputs(wl.variant, T, Hqk, HV, D, seed=0, device=dev)
-    cu_d = torch.tensor(cu_host, dtype=torch.int32, device=dev)
-    scale = D ** -0.5
-    kda = wl.variant == "kda"
-    fwd = gdr.kda_fwd if kda else gdr.gdn_fwd
-    bwd = gdr.kda_bwd if kda else gdr.gdn_bwd
-    wsb = gdr.kda_workspace_bytes(T, HV, cu_host) if kda else gdr.gdn_workspace_bytes(T, Hqk, HV, cu_host)
-    saved = torch.empty(wsb[0], dtype=torch.uint8, device=dev)
-    scratch = torch.empty(max(wsb), dtype=torch.uint8, device=dev)
-    out = torch.empty((T, HV, D), dtype=torch.bfloat16, device=dev)
-    ht = torch.empty((len(wl.lengths), HV, D, D), dtype=torch.float32, device=dev)
-    grads = {"dq": torch.empty_like(x["q"]), "dk": torch.empty_like(x["k"]), "dv": torch.empty_like(x["v"]),
-             "dg": torch.empty_like(x["g"]), "dbeta": torch.empty_like(x["beta"])}
+    w = Workload(args.workload, dev)
+    wl, T, Hqk, HV, x = w.wl, w.T, w.Hqk, w.HV, w.x
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-
-    def fwd_call(xx, save=True):
-        return fwd(xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_d, cu_host, scale, out=out, ht=ht,
-                   saved=saved if save else None, save_for_bwd=save, scratch=None if save else scratch)
-
-    def bwd_call(xx):
-        return bwd(xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu_d, cu_host, scale, xx["dout"], saved,
-                   scratch=scratch, grads=grads)
 
     def barrier():
         torch.cuda.synchronize()
@@ -271,57 +342,105 @@ def main():
             dist.barrier()
 
     for _ in range(max(args.warmup, 1)):
-        fwd_call(x)
-        bwd_call(x)
+        w.fwd_call()
+        w.bwd_call()
     barrier()
 
-    # ---- timed region: K steps of fwd + bwd -------------------------------
+    # ---- timed region: K steps of fwd + bwd, no instrumentation ------------
+    # The K steps are split into up to 5 consecutive groups; the step time is
+    # the median over all K, and the drift is the largest deviation of a
+    # group's median from it.
     sampler = ClockSampler(local)
     sampler.start()
-    gdr.gdr_profile_enable(True)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    launches_before = 0
+    launches0 = gdr.gdr_launch_count()
     barrier()
     wall0 = time.perf_counter()
-    for e0, e1, e2 in evs:
-        flush.zero_()
-        e0.record(stream)
-        fwd_call(x)
-        e1.record(stream)
-        bwd_call(x)
-        e2.record(stream)
+    t_fwd, t_bwd = time_steps(w, stream, flush, args.steps)
     barrier()
     wall = time.perf_counter() - wall0
-    gdr.gdr_profile_enable(False)
+    gpu_launches = gdr.gdr_launch_count() - launches0
     clocks = sampler.stop()
-    kern = gdr.gdr_profile_report()
-    t_fwd = [a.elapsed_time(b) for a, b, _ in evs]
-    t_bwd = [b.elapsed_time(c) for _, b, c in evs]
     t_step = [f + b for f, b in zip(t_fwd, t_bwd)]
-    ms_step = statistics.mean(t_step)
+    ms_step = statistics.median(t_step)
+    ngroups = min(5, len(t_step))
+    per = len(t_step) // ngroups
+    group_medians = [statistics.median(t_step[i * per:(i + 1) * per]) for i in range(ngroups)]
+    drift = max(abs(m - ms_step) for m in group_medians) / ms_step
     if world > 1:
         tt = torch.tensor([ms_step], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_step = float(tt.item())
     value = world * T / (ms_step / 1e3)
-    gpu_launches = sum(v[0] for v in kern.values())
 
     # ---- ckpt: forward (no save), forward (save), backward -----------------
     ckpt_ms = None
     if not args.no_ckpt:
-        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(max(args.steps // 4, 2))]
         barrier()
-        for a, b in cev:
-            flush.zero_()
-            a.record(stream)
-            fwd_call(x, save=False)
-            fwd_call(x, save=True)
-            bwd_call(x)
-            b.record(stream)
-        barrier()
-        ckpt_ms = statistics.median([a.elapsed_time(b) for a, b in cev])
+        cf, cb = time_steps(w, stream, flush, max(args.steps // 4, 3), ckpt=True)
+        ckpt_ms = statistics.median([f + b for f, b in zip(cf, cb)])
+
+    # ---- per-kernel times: a separate pass with every launch on the caller's
+    # stream (no overlap between document groups) and CUDA events around each.
+    barrier()
+    prev_serial = gdr.gdr_set_serial(True)
+    gdr.gdr_profile_enable(True)
+    nprof = 3
+    sf, sb = time_steps(w, stream, flush, nprof)
+    gdr.gdr_profile_enable(False)
+    gdr.gdr_set_serial(prev_serial)
+    kern = gdr.gdr_profile_report()
+    serial_ms = statistics.median([f + b for f, b in zip(sf, sb)])
+    kernels = {}
+    tf32_peak = pk["bf16_tflops"] * (1.1 / 2.25)  # measured BF16 x the nominal TF32/BF16 ratio
+    total_kms = max(sum(v[1] for v in kern.values()), 1e-9)
+    for name, (n, ms, units_all) in kern.items():
+        avg_ms = ms / n
+        entry = {"launches_per_step": n / nprof, "ms_per_step": ms / nprof, "avg_launch_ms": avg_ms,
+                 "share": ms / total_kms}
+        if name in KERNEL_MODEL:
+            b_th, f_th = KERNEL_MODEL[name]
+            units = units_all / n
+            gbs = b_th * units / (avg_ms / 1e3) / 1e9
+            tfs = f_th * units / (avg_ms / 1e3) / 1e12
+            per_th = ncu_traffic(name)
+            entry.update(design_bytes_per_token_head=b_th, gbs=gbs, tflops=tfs, hbm_frac=gbs / pk["hbm_gbs"],
+                         tf32_frac=tfs / tf32_peak,
+                         ncu_bytes_per_token_head=per_th,
+                         traffic_over_design=None if per_th is None else per_th / b_th)
+        kernels[name] = entry
+    # The dominant kernel: the largest share of the serialized kernel time.
+    top = max(kern, key=lambda nm: kern[nm][1]) if kern else None
+    top_roofline = None
+    if top is not None and "gbs" in kernels[top]:
+        k = kernels[top]
+        n, ms, units_all = kern[top]
+        units = units_all / n
+        per_th = k["ncu_bytes_per_token_head"]
+        if k["hbm_frac"] >= k["tf32_frac"]:
+            top_roofline = {"kernel": top, "bound": "hbm", "achieved": k["gbs"], "peak": pk["hbm_gbs"],
+                            "unit": "GB/s", "frac": k["hbm_frac"]}
+        else:
+            top_roofline = {"kernel": top, "bound": "tensor", "achieved": k["tflops"], "peak": tf32_peak,
+                            "unit": "TFLOP/s", "frac": k["tf32_frac"]}
+        top_roofline.update(share=k["share"], alg_bytes_per_launch=KERNEL_MODEL[top][0] * units,
+                            traffic=None if per_th is None else per_th * units,
+                            bytes_model="the kernel's own inputs read once and outputs written once at their "
+                                        "stored precision (bench.KERNEL_MODEL)")
+
+    # ---- the whole step against the binding roofline ---------
+    rf = binding_roofline(wl.variant, T, Hqk, HV, ms_step, pk)
+    traffic = None
+    if all(kernels.get(nm, {}).get("ncu_bytes_per_token_head") is not None for nm in kernels if nm in KERNEL_MODEL):
+        per_th = sum(kernels[nm]["ncu_bytes_per_token_head"] for nm in kernels if nm in KERNEL_MODEL)
+        traffic = per_th * T * HV if per_th else None
+    roofline = {"bound": rf["bound"], "achieved": rf["alg_bytes"] / (ms_step / 1e3) / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": rf["frac"], "traffic": traffic, "alg_bytes_per_step": rf["alg_bytes"],
+                "alg_flops_per_step": rf["alg_flops"], "t_hbm_ms": rf["t_hbm_ms"], "t_tc_ms": rf["t_tc_ms"],
+                "peak_source": pk["source"], "scope": "whole fwd+bwd step: minimal I/O at HBM bandwidth vs "
+                "chunked-algorithm flops at the sustained BF16 peak, over the median step time"}
+    if rf["bound"] == "tensor":
+        roofline.update(achieved=rf["alg_flops"] / (ms_step / 1e3) / 1e12, peak=pk["bf16_tflops_sustained"],
+                        unit="TFLOP/s")
 
     # ---- end to end through the C ABI with host buffers --------------------
     # Every step copies its inputs from pinned host memory and its results
@@ -335,7 +454,7 @@ def main():
         names_in = ("q", "k", "v", "g", "beta", "dout")
         host_in = {k: x[k].cpu().pin_memory() for k in names_in}
         dev_in = [{k: x[k] for k in names_in}, {k: torch.empty_like(x[k]) for k in names_in}]
-        dev_out = [{"out": out, **grads}, None]
+        dev_out = [{"out": w.out, **w.grads}, None]
         dev_out[1] = {k: torch.empty_like(v) for k, v in dev_out[0].items()}
         host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in dev_out[0].items()}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -361,10 +480,8 @@ def main():
                 stream.wait_event(landed[b])
                 stream.wait_event(drained[b])
                 o = dev_out[b]
-                fwd(dev_in[b]["q"], dev_in[b]["k"], dev_in[b]["v"], dev_in[b]["g"], dev_in[b]["beta"], cu_d, cu_host,
-                    scale, out=o["out"], ht=ht, saved=saved, save_for_bwd=True)
-                bwd(dev_in[b]["q"], dev_in[b]["k"], dev_in[b]["v"], dev_in[b]["g"], dev_in[b]["beta"], cu_d, cu_host,
-                    scale, dev_in[b]["dout"], saved, scratch=scratch, grads={k: o[k] for k in grads})
+                w.fwd_call(xx=dev_in[b], out=o["out"])
+                w.bwd_call(xx=dev_in[b], grads={k: o[k] for k in w.grads})
                 done[b].record(stream)
                 s_out.wait_event(done[b])
                 with torch.cuda.stream(s_out):
@@ -389,48 +506,39 @@ def main():
                "pipelined": "inputs of step s+1 copied in and results of step s-1 copied out while step s computes"}
         del host_in, host_out, dev_in, dev_out
 
-    # ---- roofline of the dominant kernel ------------------------------------
-    pk = peaks()
-    # The dominant kernel: the one that moves the most algorithmic bytes per call.
-    # (Launch durations of different document groups overlap one another on
-    # their streams, so the largest summed duration would pick the kernel that
-    # waits longest for SMs, not the one with the most work.)
-    modeled = [name for name in kern if name in KERNEL_MODEL]
-    top = max(modeled, key=lambda nm: KERNEL_MODEL[nm][0] * kern[nm][2]) if modeled else None
-    roofline = None
-    kernels = {}
-    # A kernel may run as one launch per document group per call (groups on
-    # streams of their own can overlap): bytes per launch = the model's bytes
-    # per (token, value head) x the token-heads of the launch.
-    for name, (n, ms, units_all) in kern.items():
-        avg_ms = ms / n
-        entry = {"launches": n, "total_ms": ms, "avg_ms": avg_ms, "share": ms / max(sum(v[1] for v in kern.values()), 1e-9),
-                 "ms_per_call": ms / args.steps}
-        if name in KERNEL_MODEL:
-            b_th, f_th = KERNEL_MODEL[name]
-            units = units_all / n
-            bytes_ = b_th * units
-            flops = f_th * units
-            gbs = bytes_ / (avg_ms / 1e3) / 1e9
-            tfs = flops / (avg_ms / 1e3) / 1e12
-            # TF32 tensor peak = measured BF16 peak x the nominal TF32/BF16 ratio (1.1 / 2.25).
-            tf32_peak = pk["bf16_tflops"] * (1.1 / 2.25)
-            entry.update(alg_bytes=bytes_, alg_flops=flops, gbs=gbs, tflops=tfs,
-                         hbm_frac=gbs / pk["hbm_gbs"], tensor_frac=tfs / tf32_peak)
-        kernels[name] = entry
-    if top is not None and "hbm_frac" in kernels[top]:
-        k = kernels[top]
-        tf32_peak = pk["bf16_tflops"] * (1.1 / 2.25)
-        if k["hbm_frac"] >= k["tensor_frac"]:
-            roofline = {"kernel": top, "bound": "hbm", "achieved": k["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": k["hbm_frac"], "peak_source": pk["source"]}
-        else:
-            roofline = {"kernel": top, "bound": "tensor", "achieved": k["tflops"], "peak": tf32_peak,
-                        "unit": "TFLOP/s", "frac": k["tensor_frac"],
-                        "peak_source": pk["source"] + " bf16 x nominal tf32/bf16 ratio"}
-        per_th = ncu_traffic(top)
-        roofline["traffic"] = None if per_th is None else per_th * kern[top][2] / kern[top][0]
-        roofline["alg_bytes_per_launch"] = k["alg_bytes"]
+    headline = {"fwd_ms": statistics.median(t_fwd), "bwd_ms": statistics.median(t_bwd), "ckpt_ms": ckpt_ms}
+
+    # ---- every configuration: fwd, bwd, ckpt, tokens/s, binding fraction ----
+    configs = None
+    if not args.no_configs:
+        configs = {}
+        for name in CONFIGS:
+            if name == args.workload:
+                c = dict(headline, steps=args.steps)
+                fms, bms, cms = headline["fwd_ms"], headline["bwd_ms"], ckpt_ms
+                cw = w
+            else:
+                cw = Workload(name, dev)
+                for _ in range(2):
+                    cw.fwd_call()
+                    cw.bwd_call()
+                nst = max(3, args.steps // 4)
+                f_, b_ = time_steps(cw, stream, flush, nst)
+                cf, cb = time_steps(cw, stream, flush, max(2, nst // 2), ckpt=True)
+                fms, bms = statistics.median(f_), statistics.median(b_)
+                cms = statistics.median([p + q for p, q in zip(cf, cb)])
+                c = {"fwd_ms": fms, "bwd_ms": bms, "ckpt_ms": cms, "steps": nst}
+            c.update(tokens_per_s=cw.T / ((fms + bms) / 1e3), T=cw.T, Hqk=cw.Hqk, HV=cw.HV,
+                     docs=len(cw.wl.lengths),
+                     frac_fwd_bwd=binding_roofline(cw.wl.variant, cw.T, cw.Hqk, cw.HV, fms + bms, pk)["frac"],
+                     frac_fwd=binding_roofline(cw.wl.variant, cw.T, cw.Hqk, cw.HV, fms, pk, "fwd")["frac"],
+                     frac_bwd=binding_roofline(cw.wl.variant, cw.T, cw.Hqk, cw.HV, bms, pk, "bwd")["frac"],
+                     frac_ckpt=(None if cms is None else
+                                binding_roofline(cw.wl.variant, cw.T, cw.Hqk, cw.HV, cms, pk, "ckpt")["frac"]))
+            configs[name] = c
+            if cw is not w:
+                del cw
+                torch.cuda.empty_cache()
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ------
     cpu = None
@@ -450,11 +558,15 @@ def main():
             "config": {"workload": wl.name, "variant": wl.variant, "T": T, "Hqk": Hqk, "HV": HV, "D": D,
                        "docs": list(wl.lengths), "l2": "inputs larger than L2; 256 MiB flush between steps",
                        "parallelism": f"replicas x{world}"},
-            "fwd_ms": statistics.mean(t_fwd), "bwd_ms": statistics.mean(t_bwd), "ckpt_ms": ckpt_ms,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": gpu_launches, "kernels": kernels, "wall_s_timed": wall,
-            "kernel_timing": "CUDA events around each launch on its own stream, timed region; launches of "
-                             "different document groups run on separate streams and overlap",
+            **headline,
+            "timing": {"statistic": "median of per-step CUDA-event times", "mean_ms": statistics.mean(t_step),
+                       "groups": ngroups, "group_medians_ms": group_medians, "drift": drift},
+            "roofline": roofline, "top_kernel_roofline": top_roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": gpu_launches, "configs": configs, "kernels": kernels,
+            "kernel_timing": f"separate pass of {nprof} steps with every launch on the caller's stream "
+                             f"(document groups serialized; {serial_ms:.2f} ms per step), CUDA events around "
+                             "each launch; shares are of the summed kernel time",
+            "wall_s_timed": wall,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

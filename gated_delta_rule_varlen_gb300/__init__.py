@@ -46,6 +46,8 @@ EXPORTED = (
     "gdr_inject_device_error",
     "gdr_selftest_wait",
     "gdr_doc_groups",
+    "gdr_launch_count",
+    "gdr_set_serial",
 )
 
 _lock = threading.Lock()
@@ -67,6 +69,8 @@ _SIGS = {
     "gdr_selftest_wait": ([ctypes.c_uint64, P], ctypes.c_int),
     "gdr_doc_groups": ([I32, PI32, PI32, ctypes.POINTER(ctypes.c_int64), PI32], ctypes.c_int),
     "gdr_profile_report": ([ctypes.c_char_p, SZ], ctypes.c_int),
+    "gdr_launch_count": ([], ctypes.c_uint64),
+    "gdr_set_serial": ([ctypes.c_int], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P], ctypes.c_int),
@@ -269,6 +273,17 @@ def gdn_bwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h
             scratch=None, grads=None, stream=None):
     return _bwd("gdn", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0,
                 scratch, grads, stream)
+
+
+def gdr_launch_count() -> int:
+    """Kernel launches the library's compute calls have enqueued since it was loaded."""
+    return int(load().gdr_launch_count())
+
+
+def gdr_set_serial(on: bool) -> bool:
+    """Run every call's launches on the caller's stream (document groups in
+    turn) while on; returns the previous setting."""
+    return bool(load().gdr_set_serial(int(bool(on))))
 
 
 def gdr_profile_enable(on: bool = True):

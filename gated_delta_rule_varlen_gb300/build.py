@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libgdr.so")
-SOURCES = ["gdr_fwd.cu", "gdr_bwd.cu", "gdr_api.cu"]
+SOURCES = ["gdr_fwd.cu", "gdr_walk.cu", "gdr_bwd.cu", "gdr_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -1,6 +1,7 @@
 // gdr_api.cu -- the C ABI (include/gdr.h): validation, planning, workspace
 // layout, the saved-buffer stamp, and the launch sequences.
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -384,10 +385,18 @@ void prof_clear_locked() {
   g_prof.clear();
 }
 
+// Kernel launches enqueued by the compute calls since the library was loaded
+// (every launch site opens a ProfScope).
+std::atomic<uint64_t> g_launches{0};
+// While set, every call runs all its launches on the caller's stream (its
+// document groups one after another): per-kernel timing without overlap.
+std::atomic<bool> g_serial{false};
+
 struct ProfScope {
   cudaStream_t st;
   bool on;
   ProfScope(const char* name, cudaStream_t s, double units = 0) : st(s), on(false) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (!g_prof_on) return;
     ProfRec r{name, nullptr, nullptr, units};
@@ -432,7 +441,7 @@ const cudaStream_t* lanes_for_device() {
 
 class Fork {
  public:
-  Fork(cudaStream_t main, int n) : main_(main), n_(n) {}
+  Fork(cudaStream_t main, int n) : main_(main), n_(g_serial.load() ? 1 : n) {}
   Fork(const Fork&) = delete;
   Fork& operator=(const Fork&) = delete;
   // Makes every lane wait for the work already on the caller's stream.
@@ -572,7 +581,6 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
     const std::vector<DocGroup> groups = plan_groups(N, cu_host);
     Fork fork(stream, (int)groups.size());
     if (!fork.begin()) return GDR_CUDA_ERROR;
-    const int cols = walk_tc_cols((int64_t)N * HV);
     for (size_t i = 0; i < groups.size() && st == GDR_OK; ++i) {
       const DocGroup& G = groups[i];
       const cudaStream_t ls = fork.lane((int)i);
@@ -586,7 +594,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
       if (st != GDR_OK) break;
       {
         ProfScope ps("walk_fwd", ls, units);
-        st = cuda_status(launch_walk_fwd(wa, G.r1 - G.r0, cols, ls));
+        st = cuda_status(launch_walk_fwd(wa, G.r1 - G.r0, walk_tc_cols((int64_t)N * HV), ls));
       }
     }
     if (!fork.join() && st == GDR_OK) st = GDR_CUDA_ERROR;
@@ -905,6 +913,10 @@ gdr_status gdr_check_device(void) {
   }
   return GDR_OK;
 }
+
+uint64_t gdr_launch_count(void) { return gdr::g_launches.load(); }
+
+int gdr_set_serial(int on) { return gdr::g_serial.exchange(on != 0) ? 1 : 0; }
 
 int gdr_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(gdr::g_prof_mu);

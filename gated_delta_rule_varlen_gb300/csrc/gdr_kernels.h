@@ -106,6 +106,7 @@ struct GroupReduceArgs {
 
 cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
 cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int cols_per_cta, cudaStream_t st);
+cudaError_t launch_walk_fwd_v(const WalkArgs& a, int ndocs, cudaStream_t st);
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, cudaStream_t st);
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_grad(const GradArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);

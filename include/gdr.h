@@ -212,6 +212,17 @@ gdr_status gdr_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
 int gdr_profile_enable(int on);
 gdr_status gdr_profile_report(char* buf, size_t buf_bytes);
 
+/* gdr_launch_count(): the number of kernel launches the compute calls of this
+ * library have enqueued since it was loaded (all devices, all threads); a
+ * benchmark reads it before and after a timed region.
+ * gdr_set_serial(on): while on != 0, every compute call enqueues all its
+ * launches on the caller's stream, its document groups one after another
+ * (same kernels, same results, no overlap between groups), so that
+ * per-kernel event timing measures each launch alone.  Process-wide; returns
+ * the previous setting.  Default off. */
+uint64_t gdr_launch_count(void);
+int gdr_set_serial(int on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ def gdr():
 def _declared_functions():
     src = open(os.path.join(ROOT, "include", "gdr.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|gdr_status|int)\s+(\w+)\s*\(", src, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|gdr_status|int|uint64_t)\s+(\w+)\s*\(", src, flags=re.M)))
 
 
 def test_exports_every_declared_symbol(gdr):

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import synth
-from gpu_util import SCALE, TOL, assert_within, compare, f64, rel, run_gpu, run_oracle
+from gpu_util import SCALE, TOL, assert_within, compare, err_stats, f64, rel, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -219,7 +219,7 @@ def _sample_check(wl, x, gpu, samples):
             "dk": f64(gpu["dk"][s:e, hq:hq + 1]), "dv": f64(gpu["dv"][s:e, hv]), "dg": f64(gpu["dg"][s:e, hv]),
             "dbeta": f64(gpu["dbeta"][s:e, hv]),
         }
-        return sample, {k: rel(got[k], ref[k]) for k in got}
+        return sample, {k: err_stats(got[k], ref[k]) for k in got}
 
     with ThreadPoolExecutor(max_workers=len(samples)) as ex:
         results = list(ex.map(one, samples))
@@ -227,33 +227,75 @@ def _sample_check(wl, x, gpu, samples):
         print(wl.name, sample, assert_within(errs))
 
 
+def _every_group_samples(wl, heads):
+    """One (document, Q/K head) sample per document group of the pack: the
+    documents in longest-first order take the given heads in turn, so the
+    longest document (the longest chain) is always sampled, and every group
+    (each of the three longest documents with >= 64 chunks is a group of its
+    own; the rest form one more) is covered.  For packs of more documents
+    than heads the shortest document is added as well."""
+    import gated_delta_rule_varlen_gb300 as gdr
+    order = sorted(range(len(wl.lengths)), key=lambda n: (-wl.lengths[n], n))
+    rank_of = {n: r for r, n in enumerate(order)}
+    groups = gdr.gdr_doc_groups(wl.cu_seqlens)
+    picks = []
+    for (r0, r1, _, _) in groups:
+        picks.append(order[r0])  # the group's longest document
+    shortest = order[-1]
+    if shortest not in picks:
+        picks.append(shortest)
+    assert picks[0] == order[0] and all(any(r0 <= rank_of[n] < r1 for n in picks) for r0, r1, _, _ in groups)
+    return [(n, heads[i % len(heads)]) for i, n in enumerate(picks)]
+
+
 @pytest.mark.slow
-@pytest.mark.parametrize("name,samples", [
-    ("kda_pack_h16", [(0, 3), (3, 11)]),
-    ("kda_pack_h4", [(1, 0)]),
-    ("kda_pack_h64", [(2, 63)]),
+@pytest.mark.parametrize("name,heads", [
+    ("kda_pack_h16", [3, 11, 0, 15]),
+    ("kda_pack_h4", [0, 1, 2, 3]),
+    ("kda_pack_h64", [63, 17, 40, 5]),
 ])
-def test_fullsize_kda_sampled_chains(name, samples):
+def test_fullsize_kda_sampled_chains(name, heads):
     wl, x = _full_case(name)
     gpu = run_gpu("kda", x, wl.cu_seqlens)
     for k in ("out", "dq", "dk", "dv", "dg", "dbeta"):
         assert torch.isfinite(gpu[k]).all(), k
+    _sample_check(wl, x, gpu, _every_group_samples(wl, heads))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,heads", [
+    ("gdn_p1", [7, 0, 15, 9]),
+    ("gdn_1doc", [2]),
+])
+def test_fullsize_gdn_sampled_chains(name, heads):
+    wl, x = _full_case(name)
+    gpu = run_gpu("gdn", x, wl.cu_seqlens)
+    for k in ("out", "dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.isfinite(gpu[k]).all(), k
+    samples = _every_group_samples(wl, heads)
+    assert int(np.argmax(wl.lengths)) == samples[0][0] and int(np.argmin(wl.lengths)) in [n for n, _ in samples]
     _sample_check(wl, x, gpu, samples)
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,samples", [
-    ("gdn_p1", [(None, 7)]),
-    ("gdn_1doc", [(0, 2)]),
-])
-def test_fullsize_gdn_sampled_chains(name, samples):
-    wl, x = _full_case(name)
-    if samples[0][0] is None:  # the shortest document of the seeded pack
-        samples = [(int(np.argmin(wl.lengths)), samples[0][1])]
-    gpu = run_gpu("gdn", x, wl.cu_seqlens)
-    for k in ("out", "dq", "dk", "dv", "dg", "dbeta"):
-        assert torch.isfinite(gpu[k]).all(), k
-    _sample_check(wl, x, gpu, samples)
+def test_fullsize_ckpt_sequence_matches_plain_backward():
+    # ckpt at the H = 16 pack: forward (no save), forward (save), backward gives the plain
+    # forward + backward results bit for bit (the plain results are oracle-checked above).
+    import gated_delta_rule_varlen_gb300 as gdr
+    wl, x = _full_case("kda_pack_h16")
+    cu = wl.cu_seqlens
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    o0, h0_, saved = gdr.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_d, cu, SCALE)
+    g0 = gdr.kda_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_d, cu, SCALE, x["dout"], saved)
+    del saved
+    o1, _, _ = gdr.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_d, cu, SCALE, save_for_bwd=False)
+    o2, _, saved = gdr.kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_d, cu, SCALE)
+    g1 = gdr.kda_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_d, cu, SCALE, x["dout"], saved)
+    torch.cuda.synchronize()
+    gdr.gdr_check_device()
+    assert torch.equal(o1, o0) and torch.equal(o2, o0)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(g1[name], g0[name]), name
 
 
 def test_graph_capture_of_grouped_fwd_bwd_replays_bitwise():

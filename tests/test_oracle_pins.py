@@ -82,6 +82,23 @@ def test_fd_gradients_with_empty_document():
     _check_fd(P, scale=1.0)
 
 
+# The reverse pass replays each chain from square-root checkpoints taken every
+# max(ceil(sqrt(L)), 16) tokens.  Documents of 40, 23 and 37 tokens hold three,
+# two and three such segments, so these cases run the segment replay (which
+# checkpoint a segment starts from, where it ends, the adjoint carried across
+# a segment boundary) under the same independent finite-difference check.
+def test_fd_gradients_kda_multi_segment_replay():
+    rng = np.random.default_rng(20)
+    P = _rand_problem(rng, [40, 23], Hqk=2, HV=2, D=4, per_channel=True, glow=-0.3)
+    _check_fd(P, scale=0.6)
+
+
+def test_fd_gradients_gdn_grouped_multi_segment_replay():
+    rng = np.random.default_rng(21)
+    P = _rand_problem(rng, [37], Hqk=1, HV=3, D=4, per_channel=False, glow=-0.3)
+    _check_fd(P, scale=0.8)
+
+
 def test_delta_rule_write_invariant():
     # beta = 1, |k| = 1, q = k  =>  out_t = scale * S_t^T k_t = scale * v_t for every t.
     rng = np.random.default_rng(3)

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import synth
-from gpu_util import SCALE, TOL, rel, f64
+from gpu_util import SCALE, TOL, assert_within, compare, f64, rel, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -64,6 +64,33 @@ def test_noalloc_forward_matches_kda_fwd_twice(lib):
         outs.append((out, ref_out))
     for out, ref in outs:
         assert torch.isfinite(out).all()
+
+
+def test_noalloc_forward_multi_group_matches_oracle(lib):
+    # Three documents of 64 chunks each run as document groups of their own and the short
+    # fourth as one more: four groups forked onto the library's internal streams, with the
+    # intermediates in the fixed array (about 50 MB of it).  Checked against the FP64 oracle,
+    # twice in a row.
+    gdr = lib
+    lengths, H = [4096, 4096, 4096, 100], 1
+    T = sum(lengths)
+    cu = synth.cu_from_lengths(lengths)
+    assert len(gdr.gdr_doc_groups(cu)) == 4
+    saved_bytes, _ = gdr.kda_workspace_bytes(T, H, cu)
+    assert saved_bytes <= 64 << 20
+    xh = synth.make_inputs("kda", T, H, H, 128, seed=21)
+    h0h = synth.make_states(len(lengths), H, 128, seed=22, scale=0.05)
+    x = {k: v.cuda() for k, v in xh.items()}
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    ref = run_oracle(xh, cu, h0=h0h, backward=False)
+    for _ in range(2):
+        out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ht = torch.full((len(lengths), H, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
+        st = _noalloc(gdr, x, cu_d, cu, H, out, ht, h0=h0h.cuda())
+        assert st == gdr.GDR_OK, gdr.status_string(st)
+        torch.cuda.synchronize()
+        gdr.gdr_check_device()
+        print("noalloc multi-group", assert_within(compare({"out": out, "ht": ht}, ref)))
 
 
 def test_noalloc_rejects_problem_beyond_the_fixed_array(lib):
