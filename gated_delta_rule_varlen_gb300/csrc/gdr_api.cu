@@ -594,7 +594,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
       if (st != GDR_OK) break;
       {
         ProfScope ps("walk_fwd", ls, units);
-        st = cuda_status(launch_walk_fwd(wa, G.r1 - G.r0, walk_tc_cols((int64_t)N * HV), ls));
+        st = cuda_status(launch_walk_fwd_v(wa, G.r1 - G.r0, ls));
       }
     }
     if (!fork.join() && st == GDR_OK) st = GDR_CUDA_ERROR;
@@ -648,6 +648,11 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   wb.dh0 = dh0;
   wb.err = device_error_ptr();
   if (!wb.err) return GDR_CUDA_ERROR;
+  if (NC > 0 && (!fp32_map(&wb.w_map, wb.w, (uint64_t)NC * HV * CH, DK, LDT, CH) ||
+                 !fp32_map(&wb.kdt_map, wb.kd, (uint64_t)NC * HV * DK, CH, LDS, DK) ||
+                 !fp32_map(&wb.qp_map, wb.qp, (uint64_t)NC * HV * CH, DK, LDF, CH) ||
+                 !fp32_map(&wb.aqk_map, wb.aqk, (uint64_t)NC * HV * CH, CH, LDS, CH)))
+    return GDR_CUDA_ERROR;
 
   GradStateArgs gs{};
   gs.chunks = chunks;
@@ -664,7 +669,6 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   gs.dgam = at<float>(scratch, L.dgam);
   gs.daqk = at<float>(scratch, L.daqk);
   gs.err = wb.err;
-  if (NC > 0 && !bf16_map(&gs.s0_map, gs.tape, (uint64_t)NC * HV * DK, DK, DK)) return GDR_CUDA_ERROR;
 
   GradArgs ga{};
   ga.q = static_cast<const __nv_bfloat16*>(q);
@@ -715,7 +719,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   const std::vector<DocGroup> groups = plan_groups(N, cu_host);
   Fork fork(stream, (int)groups.size());
   if (!fork.begin()) return GDR_CUDA_ERROR;
-  const int nw = walk_warps((int64_t)N * HV);
+
   for (size_t i = 0; i < groups.size() && st == GDR_OK; ++i) {
     const DocGroup& G = groups[i];
     const cudaStream_t ls = fork.lane((int)i);
@@ -725,7 +729,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
     gs.chunk_base = ga.chunk_base = gr.chunk_base = (int)G.c0;
     {
       ProfScope ps("walk_bwd", ls, units);
-      st = cuda_status(launch_walk_bwd(wb, G.r1 - G.r0, nw, ls));
+      st = cuda_status(launch_walk_bwd_v(wb, G.r1 - G.r0, ls));
     }
     if (st != GDR_OK) break;
     {

@@ -219,19 +219,21 @@ __global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
 // tcgen05.mma kind::f16 (BF16 operands, FP32 accumulators in TMEM, M = 64
 // tokens).  dO and the two state tapes are BF16 already; Delta and dDelta are
 // FP32 and enter as a BF16 pair hi + lo (hi = bf16(x), lo = bf16(x - hi),
-// about 16 significant bits), so each of their products is two MMAs.  The S0
-// tape arrives by TMA; the dS tape (stored dS^T[v][c]) is transposed into a
-// K-major tile by the warps while the first products run.
+// about 16 significant bits), so each of their products is two MMAs.  Both
+// state tapes are stored chunk-major (element (v, c) of a chunk's tile at
+// ((c / 8) * 128 + v) * 8 + c % 8, as the walks write them) and arrive as one
+// bulk copy each; that layout is the canonical no-swizzle MN-major operand
+// layout (8 channels x 8 value columns per 128-byte core matrix), so they are
+// the B operands (N = channel c, K = value column v) as they are.
 // ---------------------------------------------------------------------------
 struct GradStateSmem {
-  uint16_t S0[2 * DK * 64];   // B: S0 [c][v]; two 64-column 128B-swizzled blocks
-  uint16_t dSB[2 * DK * 64];  // B: dS [c][v]
+  uint16_t S0[DK * DK];       // B (MN-major, no swizzle): the S0 tape tile, chunk-major
+  uint16_t dSB[DK * DK];      // B (MN-major, no swizzle): the dS tape tile, chunk-major
   uint16_t dO[2 * CH * 64];   // A: dO [i][v]
   uint16_t Dh[2 * CH * 64];   // Delta hi [i][v] (A of dKd, B of dAqk)
   uint16_t Dl[2 * CH * 64];   // Delta lo
   uint16_t Eh[2 * CH * 64];   // dDelta hi [i][v] (A of dw)
   uint16_t El[2 * CH * 64];   // dDelta lo
-  uint16_t dST[DK * DK];      // the dS tape as stored, dS^T [v][c]
   uint64_t bar_s0, bar_m1, bar_m2;
   uint32_t tmem;
 };
@@ -244,24 +246,22 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   const size_t toff = tile_off(chunk, h, a.HV);
   constexpr uint32_t TCOLS = 512;  // dq [0,128), dw [128,256), dKd [256,384), dAqk [384,448)
-  const __nv_bfloat16* dS = a.dstape + state_off(chunk, h, a.HV);
 
   if (tid == 0) {
     tc::mbar_init(&s.bar_s0, 1);
     tc::mbar_init(&s.bar_m1, 1);
     tc::mbar_init(&s.bar_m2, 1);
     tc::mbar_fence_init();
-    tc::mbar_arrive_expect_tx(&s.bar_s0, DK * DK * 2);
-    const int row = (chunk * a.HV + h) * DK;
-    tc::tma_load_2d(&s.S0[0], &a.s0_map, 0, row, &s.bar_s0);
-    tc::tma_load_2d(&s.S0[DK * 64], &a.s0_map, 64, row, &s.bar_s0);
+    tc::mbar_arrive_expect_tx(&s.bar_s0, 2 * DK * DK * 2);
+    tc::bulk_load(s.S0, a.tape + state_off(chunk, h, a.HV), DK * DK * 2, &s.bar_s0);
+    tc::bulk_load(s.dSB, a.dstape + state_off(chunk, h, a.HV), DK * DK * 2, &s.bar_s0);
   }
   if (warp == 0) {
     tc::tmem_alloc(&s.tmem, TCOLS);
     tc::tmem_relinquish();
   }
   unsigned char* sdO = reinterpret_cast<unsigned char*>(s.dO);
-  // dO rows (zero beyond the chunk) into the swizzled A tile; the dS tape as stored.
+  // dO rows (zero beyond the chunk) into the swizzled A tile.
   for (int e = tid; e < CH * 16; e += 256) {
     const int i = e >> 4, kc = e & 15;
     void* dst = sdO + tc::sw128_bf16_piece(i, kc, CH);
@@ -270,7 +270,6 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
     else
       *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
   }
-  for (int e = tid; e < DK * 16; e += 256) cp_async16(&s.dST[e * 8], &dS[e * 8]);
   cp_async_commit();
   // Delta and dDelta -> BF16 hi / lo tiles.  Task e: tensor e / 1024, row (e / 16) % 64, piece e % 16.
   {
@@ -311,67 +310,60 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
   ok = __syncthreads_and(ok);
   tc::tc_fence_after();
   const uint32_t tmem = s.tmem;
-  constexpr uint32_t id128 = tc::idesc_bf16(CH, DK), id64 = tc::idesc_bf16(CH, CH);
+  constexpr uint32_t id64 = tc::idesc_bf16(CH, CH);
+  constexpr uint32_t id128t = tc::idesc_bf16(CH, DK) | tc::kIdescTransposeB;  // B MN-major
+  // K step k (16 value columns v: two core matrices of 8 v, 128 bytes apart) of
+  // a chunk-major state tile; 8-channel groups are 128 x 16 bytes apart.
+  auto bmn = [](const uint16_t* tile, int k) { return tc::desc_mn_none(tile + k * 16 * 8, 128, DK * 16); };
   if (ok && tid == 0) {
-    const uint64_t aO = tc::desc_k_sw128(s.dO), bS0 = tc::desc_k_sw128(s.S0);
+    const uint64_t aO = tc::desc_k_sw128(s.dO);
     const uint64_t aEh = tc::desc_k_sw128(s.Eh), aEl = tc::desc_k_sw128(s.El);
     const uint64_t bDh = tc::desc_k_sw128(s.Dh), bDl = tc::desc_k_sw128(s.Dl);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem, tc::kstep32(aO, k, CH), tc::kstep32(bS0, k, DK), id128, k > 0);
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem, tc::kstep32(aO, k, CH), bmn(s.S0, k), id128t, k > 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aEh, k, CH), tc::kstep32(bS0, k, DK), id128, k > 0);
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aEh, k, CH), bmn(s.S0, k), id128t, k > 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aEl, k, CH), tc::kstep32(bS0, k, DK), id128, 1);
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aEl, k, CH), bmn(s.S0, k), id128t, 1);
 #pragma unroll
     for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 384, tc::kstep32(aO, k, CH), tc::kstep32(bDh, k, CH), id64, k > 0);
 #pragma unroll
     for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 384, tc::kstep32(aO, k, CH), tc::kstep32(bDl, k, CH), id64, 1);
     tc::mma_commit(&s.bar_m1);
   }
-  // While those run: dS^T [v][c] -> the K-major B tile dS [c][v]; task: channel c, piece kc.
-  {
-    unsigned char* sdS = reinterpret_cast<unsigned char*>(s.dSB);
-#pragma unroll 2
-    for (int q = 0; q < 8; ++q) {
-      const int e = tid + 256 * q;
-      const int c = e & 127, kc = e >> 7;
-      uint32_t w[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p)
-        w[p] = (uint32_t)s.dST[(kc * 8 + 2 * p) * DK + c] | ((uint32_t)s.dST[(kc * 8 + 2 * p + 1) * DK + c] << 16);
-      *reinterpret_cast<uint4*>(sdS + tc::sw128_bf16_piece(c, kc, DK)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-  tc::fence_proxy_async();
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
   if (ok && tid == 0) {
-    const uint64_t aDh = tc::desc_k_sw128(s.Dh), aDl = tc::desc_k_sw128(s.Dl), bdS = tc::desc_k_sw128(s.dSB);
+    const uint64_t aDh = tc::desc_k_sw128(s.Dh), aDl = tc::desc_k_sw128(s.Dl);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 256, tc::kstep32(aDh, k, CH), tc::kstep32(bdS, k, DK), id128, k > 0);
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 256, tc::kstep32(aDh, k, CH), bmn(s.dSB, k), id128t, k > 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 256, tc::kstep32(aDl, k, CH), tc::kstep32(bdS, k, DK), id128, 1);
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 256, tc::kstep32(aDl, k, CH), bmn(s.dSB, k), id128t, 1);
     tc::mma_commit(&s.bar_m2);
   }
-  if (tid < DK) {  // dgam[c] = sum_v S0[c][v] dS[c][v], both tiles [c][v]
-    const int c = tid;
-    const unsigned char* p0 = reinterpret_cast<const unsigned char*>(s.S0);
-    const unsigned char* p1 = reinterpret_cast<const unsigned char*>(s.dSB);
-    float sum = 0.f;
-#pragma unroll 4
-    for (int kc = 0; kc < 16; ++kc) {
-      const uint32_t off = tc::sw128_bf16_piece(c, kc, DK);
-      const uint4 x = *reinterpret_cast<const uint4*>(p0 + off);
-      const uint4 y = *reinterpret_cast<const uint4*>(p1 + off);
+  {  // dgam[c] = sum_v S0[c][v] dS[c][v]: thread (q, vg) sums channels 8 q .. 8 q + 7 over
+     // value columns vg, vg + 16, ..; the 16 partial sums of a channel group are then
+     // added within the half warp in a fixed order.
+    const int q = tid >> 4, vg = tid & 15;
+    const uint4* p0 = reinterpret_cast<const uint4*>(s.S0) + q * DK;
+    const uint4* p1 = reinterpret_cast<const uint4*>(s.dSB) + q * DK;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const uint4 x = p0[vg + 16 * r], y = p1[vg + 16 * r];
       const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
-        sum += __uint_as_float(xs[p] << 16) * __uint_as_float(ys[p] << 16);
-        sum += __uint_as_float(xs[p] & 0xffff0000u) * __uint_as_float(ys[p] & 0xffff0000u);
+        acc[2 * p] += __uint_as_float(xs[p] << 16) * __uint_as_float(ys[p] << 16);
+        acc[2 * p + 1] += __uint_as_float(xs[p] & 0xffff0000u) * __uint_as_float(ys[p] & 0xffff0000u);
       }
     }
-    a.dgam[((size_t)chunk * a.HV + h) * DK + c] = sum;
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    if (vg == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a.dgam[((size_t)chunk * a.HV + h) * DK + 8 * q + e] = acc[e];
+    }
   }
   // Epilogue: warp w reads the rows of TMEM lane quadrant w % 4 (tokens 16 (w % 4) ..)
   // and half w / 4 of the columns.

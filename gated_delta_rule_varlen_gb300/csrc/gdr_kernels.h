@@ -12,7 +12,8 @@ struct DocDesc;
 
 // Chunk-major intermediates: tiles [NC][HV][64][128] FP32, Aqk [NC][HV][64][64],
 // Kd stored transposed per chunk ([NC][HV][128 c][64 j]), gamma [NC][HV][128],
-// BF16 state tapes [NC][HV][128][128]: S0 as S[c][v], dS transposed (dS^T[v][c]).
+// BF16 state tapes [NC][HV][128 x 128], chunk-major: element (v, c) of a tile at
+// ((c / 8) * 128 + v) * 8 + c % 8 (S0 of each chunk; dS, the adjoint of its end state).
 struct PrepArgs {
   const __nv_bfloat16 *q, *k, *v;
   const float* g;
@@ -47,6 +48,8 @@ struct WalkArgs {
 
 
 struct WalkBwdArgs {
+  // The saved tiles as the forward reads them (FP32, 32-column boxes, 128-byte swizzle):
+  CUtensorMap w_map, kdt_map, qp_map, aqk_map;
   const DocDesc* docs;
   const int* order;
   const ChunkDesc* chunks;
@@ -63,7 +66,6 @@ struct WalkBwdArgs {
 };
 
 struct GradStateArgs {
-  CUtensorMap s0_map;  // S0 tape as a 2-D BF16 tensor [NC*HV*128][128], 64 x 128 boxes, 128-byte swizzle
   const ChunkDesc* chunks;
   int HV;
   float scale;
@@ -108,6 +110,7 @@ cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16
 cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int cols_per_cta, cudaStream_t st);
 cudaError_t launch_walk_fwd_v(const WalkArgs& a, int ndocs, cudaStream_t st);
 cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, cudaStream_t st);
+cudaError_t launch_walk_bwd_v(const WalkBwdArgs& a, int ndocs, cudaStream_t st);
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_grad(const GradArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
 cudaError_t launch_group_reduce(const GroupReduceArgs& a, int nchunks, cudaStream_t st);

@@ -111,6 +111,35 @@ __device__ __forceinline__ uint64_t desc_k_sw128(const void* tile) {
   d |= (uint64_t)2 << 61;              // 128-byte swizzle
   return d;
 }
+// Shared-memory matrix descriptor: MN-major, 128-byte swizzle.  The tile is
+// blocks of 128 bytes along MN (64 BF16) by K rows of 128 bytes each, 8-row
+// groups 1024 bytes apart (`sbo`), MN blocks `lbo` bytes apart; `tile` is
+// the first K row of the step.  Used with kind::f16 only (the transpose bit
+// has no effect for kind::tf32 operands: TF32 operands must be K-major).
+__device__ __forceinline__ uint64_t desc_mn_sw128(const void* tile, uint32_t lbo, uint32_t sbo) {
+  const uint32_t a = smem_u32(tile);
+  uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Shared-memory matrix descriptor: MN-major, no swizzle (16-bit types).  The
+// operand is 128-byte core matrices of 8 MN elements x 8 K rows (16 bytes per
+// K row); `lbo` is the byte distance between core matrices along K, `sbo`
+// along MN.
+__device__ __forceinline__ uint64_t desc_mn_none(const void* tile, uint32_t lbo, uint32_t sbo) {
+  const uint32_t a = smem_u32(tile);
+  uint64_t d = (uint64_t)((a >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+// Instruction-descriptor bit selecting an MN-major B operand.
+constexpr uint32_t kIdescTransposeB = 1u << 16;
+
 // Instruction descriptor for kind::tf32: FP32 accumulator, TF32 A and B,
 // both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {

@@ -1,16 +1,17 @@
-// gdr_walk.cu -- inter-chunk state walk with the chunk outputs, the whole
-// 128 x 128 state of one (document, value head) chain in one CTA.
+// gdr_walk.cu -- the inter-chunk state walks (forward with the chunk outputs,
+// and the reverse adjoint walk), the whole 128 x 128 state of one (document,
+// value head) chain in one CTA.
 //
-// The FP32 state is kept TRANSPOSED in tensor memory: TMEM lane v holds row v
-// of S^T (value column v of S), its 128 columns the channels c.  Laid out that
-// way the state is directly the A operand of the products that read it
-// (tcgen05.mma with A in tensor memory), so no copy of the state ever goes
+// Forward.  The FP32 state is kept TRANSPOSED in tensor memory: TMEM lane v
+// holds row v of S^T (value column v of S), its 128 columns the channels c.
+// Laid out that way the state is directly the A operand of the products that
+// read it (tcgen05.mma with A in tensor memory), so no copy of the state goes
 // through shared memory:
 //   [P^T | O^T]  = S0'^T [w ; Qp]^T           (M = 128 value rows, N = 128, K = 128 channels)
 //   [O^T | S^T] += Delta^T [Aqk ; Kd^T]^T     (M = 128, N = 192, K = 64 tokens)
-// with S0' the state rounded to TF32 (a second TMEM copy, the operand), the
-// accumulator P^T pre-loaded with -u^T (so the product leaves u^T - P^T =
-// Delta^T ... negated), O^T pre-zeroed, and S^T scaled by diag(gamma) in TMEM
+// with S0' the state rounded to TF32 (a second TMEM copy, the operand: the
+// tensor cores truncate FP32 A operands read from tensor memory), Delta^T =
+// u^T - P^T formed by the data warps, and S^T scaled by diag(gamma) in place
 // before the second product.  Per chunk (the chunked identities in
 // gdr_common.cuh):
 //   Delta = u - w S0,   O = scale (Qp S0 + Aqk Delta),
@@ -24,14 +25,19 @@
 // Delta in place) and O[m&1]: the first product writes [Pd[0] | O[0]] (even m,
 // B rows [w ; Qp]) or [O[1] | Pd[1]] (odd m, B rows [Qp ; w]); the second
 // accumulates into [O[0] | S] (even, B rows [Aqk ; Kd^T]) or [S | O[1]] (odd,
-// B rows [Kd^T ; Aqk]).  The other parity's buffers are drained and refilled
-// off the chunk-to-chunk chain.
+// B rows [Kd^T ; Aqk]).  O of a chunk is written out while the next chunk's
+// first product runs.
+//
+// The state tape (S0 of every chunk, BF16, for the backward) is stored
+// chunk-major: element (v, c) of a chunk's 128 x 128 tile at
+// ((c / 8) * 128 + v) * 8 + c % 8, so that the 32 lanes of a warp (32
+// consecutive v) store 512 contiguous bytes per 8-channel piece.
 //
 // Threads: 8 data warps (warp w: TMEM lanes 32 (w % 4) .., value rows v; warp
 // halves w / 4 split the columns) and one issuer warp (its lane 0 issues every
-// TMA copy and MMA).  Shared memory holds the B operands only, two stages
-// each: [w ; Qp] (64 KB) and [Kd^T ; Aqk] + gamma (48 KB).  Waits are bounded;
-// a timed-out wait ends the walk for the whole CTA and sets the device error
+// TMA copy and MMA).  Shared memory: [w ; Qp] + gamma in two stages (64 KB
+// each), [Kd^T ; Aqk] (48 KB) and u (32 KB) in one.  Waits are bounded; a
+// timed-out wait ends the walk for the whole CTA and sets the device error
 // word.
 #include "gdr_common.cuh"
 #include "gdr_kernels.h"
@@ -40,20 +46,25 @@
 namespace gdr {
 
 struct WalkVSmem {
-  float B1[2][2 * CH * DK];       // per stage: 4 column blocks of 128 rows x 32 (16 KB each)
-  float B2[2][(DK + CH) * CH];    // per stage: 2 column blocks of 192 rows x 32 (24 KB each)
-  float gam[2][DK];               // gamma, with the B2 stage
-  uint64_t bar_b1[2], bar_b2[2], bar_s1, bar_s2;
+  float B1[2][2 * CH * DK];    // per stage: 4 column blocks of 128 rows x 32 (16 KB each)
+  float B2[(DK + CH) * CH];    // 2 column blocks of 192 rows x 32 (24 KB each)
+  float U[CH * DK];            // u: 4 blocks of 64 rows j x 32 value columns (128-byte swizzle)
+  float gam[2][DK];            // gamma, with the B1 stage
+  uint64_t bar_b1[2], bar_b2, bar_u, bar_s1, bar_s2;
   uint32_t tmem;
 };
 constexpr int WALKV_THREADS = 288;
-constexpr uint32_t WALKV_B1_BYTES = 2 * CH * DK * 4;
-constexpr uint32_t WALKV_B2_BYTES = (DK + CH) * CH * 4 + DK * 4;
+constexpr uint32_t WALKV_B1_BYTES = 2 * CH * DK * 4 + DK * 4;
+constexpr uint32_t WALKV_B2_BYTES = (DK + CH) * CH * 4;
+constexpr uint32_t WALKV_U_BYTES = CH * DK * 4;
 constexpr uint32_t kColS = 128, kColSp = 384;
 __device__ __forceinline__ uint32_t colPd(int b) { return b ? 320u : 0u; }   // P, then Delta, of parity b
 __device__ __forceinline__ uint32_t colO(int b) { return b ? 256u : 64u; }   // O of parity b
 __device__ __forceinline__ uint32_t colD1(int b) { return b ? 256u : 0u; }   // D of [P | O] / [O | P]
 __device__ __forceinline__ uint32_t colD2(int b) { return b ? 128u : 64u; }  // D of [O | S] / [S | O]
+
+// Element offset of (v, c) in a chunk-major BF16 state tile.
+__device__ __forceinline__ size_t tape_off(int v, int c) { return ((size_t)(c >> 3) * DK + v) * 8 + (c & 7); }
 
 __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_constant__ WalkArgs a) {
   extern __shared__ unsigned char smraw[];
@@ -72,8 +83,8 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
   if (issuer) {
     tc::mbar_init(&s.bar_b1[0], 1);
     tc::mbar_init(&s.bar_b1[1], 1);
-    tc::mbar_init(&s.bar_b2[0], 1);
-    tc::mbar_init(&s.bar_b2[1], 1);
+    tc::mbar_init(&s.bar_b2, 1);
+    tc::mbar_init(&s.bar_u, 1);
     tc::mbar_init(&s.bar_s1, 1);
     tc::mbar_init(&s.bar_s2, 1);
     tc::mbar_fence_init();
@@ -88,8 +99,8 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
   const uint32_t tm = s.tmem;
   const uint32_t tl = tm + ((uint32_t)(32 * q4) << 16);  // this warp's lanes
 
-  // Issuer only.  Stage b = m & 1 of each operand.
-  auto issue_b1 = [&](int m) {  // [w ; Qp] (even) or [Qp ; w] (odd)
+  // Issuer only.
+  auto issue_b1 = [&](int m) {  // [w ; Qp] (even m) or [Qp ; w] (odd m), and gamma, into stage m & 1
     const int b = m & 1, item = (dd.chunk0 + m) * a.HV + h;
     unsigned char* base = reinterpret_cast<unsigned char*>(s.B1[b]);
     const int wr = b ? 64 : 0, qr = b ? 0 : 64;
@@ -98,29 +109,24 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       tc::tma_load_2d(base + kb * 16384 + wr * 128, &a.w_map, kb * 32, item * CH, &s.bar_b1[b]);
       tc::tma_load_2d(base + kb * 16384 + qr * 128, &a.qp_map, kb * 32, item * CH, &s.bar_b1[b]);
     }
+    tc::bulk_load(s.gam[b], &a.gam[(size_t)item * DK], DK * 4, &s.bar_b1[b]);
   };
-  auto issue_b2 = [&](int m) {  // [Aqk ; Kd^T] (even) or [Kd^T ; Aqk] (odd), and gamma
-    const int b = m & 1, item = (dd.chunk0 + m) * a.HV + h;
-    unsigned char* base = reinterpret_cast<unsigned char*>(s.B2[b]);
-    const int ar = b ? 128 : 0, kr = b ? 0 : 64;
-    tc::mbar_arrive_expect_tx(&s.bar_b2[b], WALKV_B2_BYTES);
+  auto issue_b2 = [&](int m) {  // [Aqk ; Kd^T] (even m) or [Kd^T ; Aqk] (odd m)
+    const int item = (dd.chunk0 + m) * a.HV + h;
+    unsigned char* base = reinterpret_cast<unsigned char*>(s.B2);
+    const int ar = (m & 1) ? 128 : 0, kr = (m & 1) ? 0 : 64;
+    tc::mbar_arrive_expect_tx(&s.bar_b2, WALKV_B2_BYTES);
     for (int kb = 0; kb < 2; ++kb) {
-      tc::tma_load_2d(base + kb * 24576 + ar * 128, &a.aqk_map, kb * 32, item * CH, &s.bar_b2[b]);
-      tc::tma_load_2d(base + kb * 24576 + kr * 128, &a.kdt_map, kb * 32, item * DK, &s.bar_b2[b]);
+      tc::tma_load_2d(base + kb * 24576 + ar * 128, &a.aqk_map, kb * 32, item * CH, &s.bar_b2);
+      tc::tma_load_2d(base + kb * 24576 + kr * 128, &a.kdt_map, kb * 32, item * DK, &s.bar_b2);
     }
-    tc::bulk_load(s.gam[b], &a.gam[(size_t)item * DK], DK * 4, &s.bar_b2[b]);
   };
-  // u of chunk m, rows j = 32 hf .. 32 hf + 31 at value column v, negated,
-  // into the P accumulator Pd[m & 1] (data threads).
-  auto load_neg_u = [&](int m) {
-    const float* up = a.u + tf_off(dd.chunk0 + m, h, a.HV) + (size_t)(32 * hf) * LDF + v;
-    uint32_t r[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(-__ldg(up + (size_t)j * LDF));
-    tc::tmem_st32(tl + colPd(m & 1) + 32 * hf, r);
+  auto issue_u = [&](int m) {
+    const int item = (dd.chunk0 + m) * a.HV + h;
+    tc::mbar_arrive_expect_tx(&s.bar_u, WALKV_U_BYTES);
+    for (int vb = 0; vb < 4; ++vb) tc::tma_load_2d(s.U + vb * CH * 32, &a.u_map, vb * 32, item * CH, &s.bar_u);
   };
-  // scale * O of chunk m (buffer O[m & 1]) -> out; the buffer is zeroed again
-  // for chunk m + 2 (data threads).
+  // scale * O of chunk m (buffer O[m & 1]) -> out, rows i = 32 hf .. (data threads).
   auto drain_out = [&](int m) {
     const int i0 = 32 * hf, len = min(CH, dd.len - CH * m);
     uint32_t r[32];
@@ -130,9 +136,6 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (i0 + i < len) op[(size_t)i * a.HV * DK] = __float2bfloat16_rn(a.scale * __uint_as_float(r[i]));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = 0u;
-    tc::tmem_st32(tl + colO(m & 1) + i0, r);
   };
 
   if (data) {
@@ -147,20 +150,15 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       }
       tc::tmem_st32(tl + kColS + 64 * hf + cb, r);
     }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = 0u;
-    tc::tmem_st32(tl + colO(0) + 32 * hf, r);
-    tc::tmem_st32(tl + colO(1) + 32 * hf, r);
-    if (n > 0) load_neg_u(0);
     tc::tmem_wait_st();
   }
   // Copies issued and consumed (issuer), for the drain after a timeout.
-  int b1_iss[2] = {0, 0}, b1_got[2] = {0, 0}, b2_iss[2] = {0, 0}, b2_got[2] = {0, 0}, s1_iss = 0, s2_iss = 0;
-  if (issuer) {
-    for (int m = 0; m < 2 && m < n; ++m) {
-      issue_b1(m), ++b1_iss[m];
-      issue_b2(m), ++b2_iss[m];
-    }
+  int b1_iss[2] = {0, 0}, b1_got[2] = {0, 0}, b2_iss = 0, b2_got = 0, u_iss = 0, u_got = 0, s1_iss = 0, s2_iss = 0;
+  if (issuer && n > 0) {
+    issue_b1(0), ++b1_iss[0];
+    if (n > 1) issue_b1(1), ++b1_iss[1];
+    issue_b2(0), ++b2_iss;
+    issue_u(0), ++u_iss;
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -172,99 +170,110 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
   for (; m < n; ++m) {
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
-    uint32_t s0[64];  // S0 row v, columns 64 hf .. 64 hf + 63 (data threads)
     if (data) {
       if (m > 0) {
         ok = tc::mbar_wait(&s.bar_s2, (m - 1) & 1) && ok;  // S0 of this chunk, O of the previous one
         tc::tc_fence_after();
       }
-      tc::tmem_ld32(tl + kColS + 64 * hf, s0);
-      tc::tmem_ld32(tl + kColS + 64 * hf + 32, s0 + 32);
-      tc::tmem_wait_ld();
-      uint32_t r[32];
+      ok = tc::mbar_wait(&s.bar_b1[b], (m >> 1) & 1) && ok;  // gamma of this chunk
+      // Columns 64 hf .. 64 hf + 63 in two halves: the tape tile (chunk-major: 512
+      // contiguous bytes per warp and 8-channel piece), S0' = S0 rounded to TF32
+      // (the A operand), and diag(gamma) S0 into S.
+      const float* gm = s.gam[b] + 64 * hf;
+      __nv_bfloat16* tp = a.tape ? a.tape + state_off(chunk, h, a.HV) : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
+        const int c0 = 64 * hf + 32 * half;
+        uint32_t s0[32], r[32];
+        tc::tmem_ld32(tl + kColS + c0, s0);
+        tc::tmem_wait_ld();
+        if (tp) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = tf32(__uint_as_float(s0[32 * half + j]));
-        tc::tmem_st32(tl + kColSp + 64 * hf + 32 * half, r);
+          for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162 p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              p[e] = __floats2bfloat162_rn(__uint_as_float(s0[8 * q + 2 * e]), __uint_as_float(s0[8 * q + 2 * e + 1]));
+            *reinterpret_cast<uint4*>(tp + tape_off(v, c0 + 8 * q)) = *reinterpret_cast<uint4*>(p);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = tf32(__uint_as_float(s0[j]));
+        tc::tmem_st32(tl + kColSp + c0, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(s0[j]) * gm[32 * half + j]);
+        tc::tmem_st32(tl + kColS + c0, r);
       }
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
-    if (!named_sync_and(1, WALKV_THREADS, ok)) break;  // S0' is in place
+    if (!named_sync_and(1, WALKV_THREADS, ok)) break;  // S0', diag(gamma) S0 in place
     tc::tc_fence_after();
     if (issuer) {
-      const bool r1 = tc::mbar_wait(&s.bar_b1[b], b1_got[b] & 1);
-      ok = r1 && ok;
-      if (r1) {
-        ++b1_got[b];
-        tc::tc_fence_after();
-        const uint64_t bd = tc::desc_k_sw128(s.B1[b]);
-#pragma unroll
-        for (int k = 0; k < DK / 8; ++k) tc::mma_tf32_ta(tm + colD1(b), tm + kColSp + 8 * k, tc::kstep32(bd, k, 128), kId1, 1);
-        tc::mma_commit(&s.bar_s1);
-        ++s1_iss;
-      }
-    }
-    if (data) {
-      // While [P | O] runs: diag(gamma) S0 into S, the tape row, the previous
-      // chunk's output, -u of the next chunk.
-      const bool rg = tc::mbar_wait(&s.bar_b2[b], (m >> 1) & 1);  // gamma of this chunk
-      ok = rg && ok;
-      const float* gm = s.gam[b] + 64 * hf;
-      uint32_t r[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(s0[32 * half + j]) * gm[32 * half + j]);
-        tc::tmem_st32(tl + kColS + 64 * hf + 32 * half, r);
-      }
-      if (a.tape) {  // S0[c][v] as BF16
-        __nv_bfloat16* tp = a.tape + state_off(chunk, h, a.HV) + (size_t)(64 * hf) * DK + v;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) tp[(size_t)j * DK] = __float2bfloat16_rn(__uint_as_float(s0[j]));
-      }
-      if (m > 0) drain_out(m - 1);
-      if (m + 1 < n) load_neg_u(m + 1);
-      tc::tmem_wait_st();
-      // Delta = -(P - u), rounded to TF32 in place (the A operand of the
-      // second product); the FP32 Delta for the backward.
-      ok = tc::mbar_wait(&s.bar_s1, m & 1) && ok;
+      ok = tc::mbar_wait(&s.bar_b1[b], (m >> 1) & 1) && ok;  // complete: the data threads waited for it
+      ++b1_got[b];
       tc::tc_fence_after();
+      const uint64_t bd = tc::desc_k_sw128(s.B1[b]);
+#pragma unroll
+      for (int k = 0; k < DK / 8; ++k)
+        tc::mma_tf32_ta(tm + colD1(b), tm + kColSp + 8 * k, tc::kstep32(bd, k, 128), kId1, k > 0);
+      tc::mma_commit(&s.bar_s1);
+      ++s1_iss;
+    }
+    float dlt[32];  // Delta rows j = 32 hf .., stored to HBM after the second product is issued
+    if (data) {
+      // While [P | O] runs: the previous chunk's output.
+      if (m > 0) drain_out(m - 1);
+      // Delta = u - P (rows j = 32 hf ..), rounded to TF32 in place (the A
+      // operand of the second product); the FP32 Delta for the backward.
+      ok = tc::mbar_wait(&s.bar_s1, m & 1) && ok;
+      ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
+      tc::tc_fence_after();
+      uint32_t r[32];
       tc::tmem_ld32(tl + colPd(b) + 32 * hf, r);
       tc::tmem_wait_ld();
-      float* dp = a.delta ? a.delta + tile_off(chunk, h, a.HV) + (size_t)(32 * hf) * DK + v : nullptr;
+      const unsigned char* ub = reinterpret_cast<const unsigned char*>(s.U) + q4 * (CH * 128) + (lane & 3) * 4;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float d = -__uint_as_float(r[j]);
-        if (dp) dp[(size_t)j * DK] = d;
-        r[j] = tf32(d);
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * hf + jj;
+        dlt[jj] = *reinterpret_cast<const float*>(ub + j * 128 + ((((lane >> 2)) ^ (j & 7)) << 4)) -
+                  __uint_as_float(r[jj]);
+        r[jj] = tf32(dlt[jj]);
       }
       tc::tmem_st32(tl + colPd(b) + 32 * hf, r);
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
-    if (!named_sync_and(2, WALKV_THREADS, ok)) break;  // Delta, gamma S0 in place
+    if (!named_sync_and(2, WALKV_THREADS, ok)) break;  // Delta in place; u read
     tc::tc_fence_after();
+    if (data && a.delta) {  // the FP32 Delta for the backward, while the update runs
+      float* dp = a.delta + tile_off(chunk, h, a.HV) + (size_t)(32 * hf) * DK + v;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) dp[(size_t)jj * DK] = dlt[jj];
+    }
     if (issuer) {
-      const bool r2 = tc::mbar_wait(&s.bar_b2[b], b2_got[b] & 1);
+      const bool r2 = tc::mbar_wait(&s.bar_b2, b2_got & 1);
       ok = r2 && ok;
       if (r2) {
-        ++b2_got[b];
+        ++b2_got;
+        ++u_got;
         tc::tc_fence_after();
-        const uint64_t bd = tc::desc_k_sw128(s.B2[b]);
+        const uint64_t bd = tc::desc_k_sw128(s.B2);
 #pragma unroll
-        for (int k = 0; k < CH / 8; ++k) tc::mma_tf32_ta(tm + colD2(b), tm + colPd(b) + 8 * k, tc::kstep32(bd, k, 192), kId2, 1);
+        for (int k = 0; k < CH / 8; ++k)
+          tc::mma_tf32_ta(tm + colD2(b), tm + colPd(b) + 8 * k, tc::kstep32(bd, k, 192), kId2, 1);
         tc::mma_commit(&s.bar_s2);
         ++s2_iss;
       }
-      // [P | O] of this chunk is done (the data threads waited for it): its
-      // B1 stage takes chunk m + 2.  The B2 stage once the update is done.
+      // Refills: stage b of [w ; Qp] (its product is done) with chunk m + 2,
+      // u (read before the barrier) and, once the update is done, [Kd^T ;
+      // Aqk] with chunk m + 1.
       if (ok && m + 2 < n) issue_b1(m + 2), ++b1_iss[b];
-      if (ok && m + 2 < n) {
+      if (ok && m + 1 < n) {
+        issue_u(m + 1), ++u_iss;
         const bool r3 = tc::mbar_wait(&s.bar_s2, m & 1);
         ok = r3 && ok;
-        if (r3) issue_b2(m + 2), ++b2_iss[b];
+        if (r3) issue_b2(m + 1), ++b2_iss;
       }
     }
   }
@@ -272,10 +281,10 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
     // A wait ran out: record it and drain the copies and products in flight.
     if (issuer) {
       atomicExch(a.err, 3);
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < 2; ++q)
         if (b1_iss[q] > b1_got[q]) tc::mbar_wait(&s.bar_b1[q], (b1_iss[q] - 1) & 1);
-        if (b2_iss[q] > b2_got[q]) tc::mbar_wait(&s.bar_b2[q], (b2_iss[q] - 1) & 1);
-      }
+      if (b2_iss > b2_got) tc::mbar_wait(&s.bar_b2, (b2_iss - 1) & 1);
+      if (u_iss > u_got) tc::mbar_wait(&s.bar_u, (u_iss - 1) & 1);
       if (s1_iss > 0) tc::mbar_wait(&s.bar_s1, (s1_iss - 1) & 1);
       if (s2_iss > 0) tc::mbar_wait(&s.bar_s2, (s2_iss - 1) & 1);
     }
@@ -307,6 +316,346 @@ cudaError_t launch_walk_fwd_v(const WalkArgs& a, int ndocs, cudaStream_t st) {
   const size_t sm = sizeof(WalkVSmem) + 1024;
   cudaFuncSetAttribute(k_walk_fwd_v, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   k_walk_fwd_v<<<ndocs * a.HV, WALKV_THREADS, sm, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Reverse adjoint walk, the whole 128 x 128 adjoint of one (document, value
+// head) chain in one CTA, chunks in reverse.  With dS the adjoint of the
+// chunk's end state (the chunked identities in gdr_bwd.cu's header):
+//   dDelta = scale Aqk^T dO + Kd dS
+//   dS0    = diag(gamma) dS + scale Qp^T dO - w^T dDelta
+// The adjoint is kept transposed in tensor memory (lane v, columns c) and is
+// the A operand (from tensor memory) of the products that read it:
+//   dDelta^T  = dS'^T Kd^T                                (M = 128, N = 64, K = 128 channels)
+//   [dDelta^T | dS^T] += (scale dO)'^T [Aqk^T ; Qp^T]^T  (M = 128, N = 192, K = 64 tokens)
+//   dS^T += (-dDelta')^T (w^T)^T                          (M = 128, N = 128, K = 64 tokens)
+// (primes: TF32-rounded copies in tensor memory; dS^T is scaled by
+// diag(gamma) in place before the second product).  These products contract
+// each saved tile over its other index than the forward's products do, and
+// TF32 operands must be K-major, so the B operands are the forward's tiles
+// transposed: TMA brings each chunk's tiles as stored (w, Q Gamma, Kd^T, Aqk)
+// into a staging area, and the data warps transpose them, 4 x 4 elements per
+// thread, into the 128-byte-swizzled K-major operand stage, each tile just
+// before the product that reads it: Kd with the adjoint's copy, [Aqk^T ;
+// Qp^T] before the second product, w^T while it runs.  A staging group is
+// refilled with the next chunk's tiles as soon as it has been transposed, a
+// whole chunk ahead of its next use.  Each chunk stores the adjoint of its
+// end state as the BF16 dS tape (chunk-major like the state tape) and dDelta
+// (FP32).
+// The "adjoint walk" of PR #7723 "perf(cake_gdn): prefetch offset adjoint
+// walk, default LPT segment plan" (opening description), which also
+// prefetches its operands one step ahead.
+//
+// Tensor-memory columns: dDelta 0..63, dS 64..191, dS' 192..319, (scale dO)'
+// for even and odd steps 320..383 and 384..447.
+// ---------------------------------------------------------------------------
+struct WalkBvSmem {
+  // Operand stage (K-major, 128-byte swizzle):
+  float BA[(CH + DK) * CH];  // [Aqk^T ; Qp^T]: rows j then c, K = i; 2 column blocks of 192 rows
+  float BK[CH * DK];         // Kd [j][c]: rows j, K = c; 4 column blocks of 64 rows
+  float BW[DK * CH];         // w^T [c][j]: rows c, K = j; 2 column blocks of 128 rows
+  // Staging, the saved tiles as the forward reads them (TMA, 128-byte swizzle):
+  float SK[DK * CH];         // Kd^T [c][j]: 2 column blocks of 128 rows
+  float SA[CH * CH];         // Aqk [i][j]: 2 column blocks of 64 rows
+  float SQ[CH * DK];         // Q Gamma [i][c]: 4 column blocks of 64 rows
+  float SW[CH * DK];         // w [j][c]: 4 column blocks of 64 rows
+  float gam[DK];             // gamma, with the Kd^T group
+  uint64_t bar_k, bar_a, bar_w, bar_ab, bar_c;
+  uint32_t tmem;
+};
+constexpr uint32_t kBColD = 0, kBColS = 64, kBColSp = 192;
+__device__ __forceinline__ uint32_t colDO(int b) { return b ? 384u : 320u; }
+constexpr uint32_t WALKB_K_BYTES = DK * CH * 4 + DK * 4, WALKB_A_BYTES = (CH * CH + CH * DK) * 4,
+                   WALKB_W_BYTES = CH * DK * 4;
+
+// Byte offset of FP32 element (row r, k) of a K-major 128B-swizzled operand of
+// R rows (column blocks of 32 k).
+__device__ __forceinline__ uint32_t sw_off(int r, int k, int R) {
+  return (uint32_t)((k >> 5) * R * 128 + r * 128 + ((((k & 31) >> 2) ^ (r & 7)) << 4) + ((k & 3) << 2));
+}
+
+// One group of 32 4 x 4 blocks of a transposed copy between two K-major
+// 128B-swizzled tiles: source rows sr0 .. sr0+15 (of R_s rows), source columns
+// sc0 .. sc0+31 become destination rows roff + sc0 .. (of R_d rows) with the
+// source rows as their K index.  A 16-byte shared access is served a quarter
+// warp at a time, so the eight lanes of each quarter take row quads and column
+// quads such that their reads (row 4 rq + a, column chunk cq) and their writes
+// (row 4 cq + b, K chunk rq) each fall on eight different 16-byte bank groups:
+// lane (quarter qq, index i) takes row quad 2 ((i >> 1) & 1) + (i >> 2) and
+// column quad (i & 1) + 2 (((i >> 1) & 1) ^ (qq & 1)) + 4 (qq >> 1).
+__device__ __forceinline__ void transpose_group(const unsigned char* src, int Rs, int sr0, int sc0, unsigned char* dst,
+                                                int Rd, int roff) {
+  const int l = lane_id(), qq = l >> 3, i = l & 7;
+  const int rq = 2 * ((i >> 1) & 1) + (i >> 2), cq = (i & 1) + 2 * (((i >> 1) & 1) ^ (qq & 1)) + 4 * (qq >> 1);
+  const int r0 = sr0 + 4 * rq, c0 = sc0 + 4 * cq;
+  float4 x[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) x[a] = *reinterpret_cast<const float4*>(src + sw_off(r0 + a, c0, Rs));
+  *reinterpret_cast<float4*>(dst + sw_off(roff + c0 + 0, r0, Rd)) = make_float4(x[0].x, x[1].x, x[2].x, x[3].x);
+  *reinterpret_cast<float4*>(dst + sw_off(roff + c0 + 1, r0, Rd)) = make_float4(x[0].y, x[1].y, x[2].y, x[3].y);
+  *reinterpret_cast<float4*>(dst + sw_off(roff + c0 + 2, r0, Rd)) = make_float4(x[0].z, x[1].z, x[2].z, x[3].z);
+  *reinterpret_cast<float4*>(dst + sw_off(roff + c0 + 3, r0, Rd)) = make_float4(x[0].w, x[1].w, x[2].w, x[3].w);
+}
+
+__global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_constant__ WalkBwdArgs a) {
+  extern __shared__ unsigned char smraw[];
+  WalkBvSmem& s = *reinterpret_cast<WalkBvSmem*>(tc::align1024(smraw));
+  const int rank = a.rank_base + blockIdx.x / a.HV;  // all heads of the longest document first
+  const int h = blockIdx.x % a.HV;
+  const int doc = a.order[rank];
+  const DocDesc dd = a.docs[doc];
+  const int n = dd.nchunks;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
+  const bool data = tid < 256, issuer = tid == 256;
+  const int q4 = warp & 3, hf = (warp >> 2) & 1;
+  const int v = 32 * q4 + lane;
+  const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
+  unsigned char* const BA = reinterpret_cast<unsigned char*>(s.BA);
+  unsigned char* const BK = reinterpret_cast<unsigned char*>(s.BK);
+  unsigned char* const BW = reinterpret_cast<unsigned char*>(s.BW);
+  const unsigned char* const SK = reinterpret_cast<const unsigned char*>(s.SK);
+  const unsigned char* const SA = reinterpret_cast<const unsigned char*>(s.SA);
+  const unsigned char* const SQ = reinterpret_cast<const unsigned char*>(s.SQ);
+  const unsigned char* const SW = reinterpret_cast<const unsigned char*>(s.SW);
+
+  if (issuer) {
+    tc::mbar_init(&s.bar_k, 1);
+    tc::mbar_init(&s.bar_a, 1);
+    tc::mbar_init(&s.bar_w, 1);
+    tc::mbar_init(&s.bar_ab, 1);
+    tc::mbar_init(&s.bar_c, 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&s.tmem, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tm = s.tmem;
+  const uint32_t tl = tm + ((uint32_t)(32 * q4) << 16);
+
+  // Issuer: the staging groups of chunk m.
+  auto issue_k = [&](int m) {
+    const int item = (dd.chunk0 + m) * a.HV + h;
+    tc::mbar_arrive_expect_tx(&s.bar_k, WALKB_K_BYTES);
+    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(s.SK + kb * DK * 32, &a.kdt_map, kb * 32, item * DK, &s.bar_k);
+    tc::bulk_load(s.gam, &a.gam[(size_t)item * DK], DK * 4, &s.bar_k);
+  };
+  auto issue_a = [&](int m) {
+    const int item = (dd.chunk0 + m) * a.HV + h;
+    tc::mbar_arrive_expect_tx(&s.bar_a, WALKB_A_BYTES);
+    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(s.SA + kb * CH * 32, &a.aqk_map, kb * 32, item * CH, &s.bar_a);
+    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(s.SQ + kb * CH * 32, &a.qp_map, kb * 32, item * CH, &s.bar_a);
+  };
+  auto issue_w = [&](int m) {
+    const int item = (dd.chunk0 + m) * a.HV + h;
+    tc::mbar_arrive_expect_tx(&s.bar_w, WALKB_W_BYTES);
+    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(s.SW + kb * CH * 32, &a.w_map, kb * 32, item * CH, &s.bar_w);
+  };
+  // dO of chunk m, rows i = 32 hf .., at value column v, as raw BF16 bits into
+  // registers (loaded a step before use; rows beyond the chunk read its first
+  // row and are zeroed when stored), and (scale dO)' into tensor memory.
+  auto load_do = [&](int m, uint16_t (&d)[32]) {  // raw BF16 bits; not used before the next step
+    const int i0 = 32 * hf, len = min(CH, dd.len - CH * m);
+    const uint16_t* dp = reinterpret_cast<const uint16_t*>(a.dout) + ((size_t)(dd.tok0 + CH * m) * a.HV + h) * DK + v;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) d[i] = __ldg(dp + (size_t)(i0 + i < len ? i0 + i : 0) * a.HV * DK);
+  };
+  auto store_do = [&](int m, int b, const uint16_t (&d)[32]) {
+    const int i0 = 32 * hf, len = min(CH, dd.len - CH * m);
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = i0 + i < len ? tf32(a.scale * bfbits2f(d[i])) : 0u;
+    tc::tmem_st32(tl + colDO(b) + 32 * hf, r);
+  };
+
+  uint16_t don[32];  // dO of the next step's chunk, loaded a step ahead
+  if (data) {
+    // dS <- dht (or 0), transposed: dS^T[v][c] = dht[c][v].
+    uint32_t r[32];
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 32) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int c = 64 * hf + cb + j;
+        r[j] = __float_as_uint(a.dht ? a.dht[sidx + (size_t)c * DK + v] : 0.f);
+      }
+      tc::tmem_st32(tl + kBColS + 64 * hf + cb, r);
+    }
+    if (n > 0) {
+      load_do(n - 1, don);
+      store_do(n - 1, 0, don);
+    }
+    if (n > 1) load_do(n - 2, don);
+    tc::tmem_wait_st();
+  }
+  int k_iss = 0, a_iss = 0, w_iss = 0, k_got = 0, a_got = 0, w_got = 0, ab_iss = 0, c_iss = 0;
+  if (issuer && n > 0) {
+    issue_k(n - 1), ++k_iss;
+    issue_a(n - 1), ++a_iss;
+    issue_w(n - 1), ++w_iss;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+
+  constexpr uint32_t kIdB = tc::idesc_tf32(128, 64), kIdA = tc::idesc_tf32(128, 192), kIdC = tc::idesc_tf32(128, 128);
+  bool ok = true;
+  int st = 0;
+  for (; st < n; ++st) {
+    const int b = st & 1;
+    const int m = n - 1 - st;
+    const int chunk = dd.chunk0 + m;
+    float ddl[32];  // dDelta rows j = 32 hf .., stored to HBM after the last product is issued
+    if (data) {
+      if (st > 0) {
+        ok = tc::mbar_wait(&s.bar_c, (st - 1) & 1) && ok;  // the adjoint of this chunk's end state
+        tc::tc_fence_after();
+      }
+      ok = tc::mbar_wait(&s.bar_k, st & 1) && ok;  // Kd^T and gamma of this chunk
+      // Kd [j][c] from Kd^T [c][j]: 16 groups.
+      for (int g = warp; g < 16; g += 8) transpose_group(SK, DK, 16 * (g >> 1), 32 * (g & 1), BK, CH, 0);
+      // Columns 64 hf .. 64 hf + 63 of the adjoint in two halves: the dS tape
+      // (chunk-major like the state tape), dS' (TF32, the A operand) and
+      // diag(gamma) dS into place.
+      const float* gm = s.gam + 64 * hf;
+      __nv_bfloat16* tp = a.dstape + state_off(chunk, h, a.HV);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int c0 = 64 * hf + 32 * half;
+        uint32_t ds[32], r[32];
+        tc::tmem_ld32(tl + kBColS + c0, ds);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          __nv_bfloat162 p[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            p[e] = __floats2bfloat162_rn(__uint_as_float(ds[8 * q + 2 * e]), __uint_as_float(ds[8 * q + 2 * e + 1]));
+          *reinterpret_cast<uint4*>(tp + tape_off(v, c0 + 8 * q)) = *reinterpret_cast<uint4*>(p);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = tf32(__uint_as_float(ds[j]));
+        tc::tmem_st32(tl + kBColSp + c0, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(ds[j]) * gm[32 * half + j]);
+        tc::tmem_st32(tl + kBColS + c0, r);
+      }
+      tc::fence_proxy_async();
+      tc::tmem_wait_st();
+    }
+    tc::tc_fence_before();
+    if (!named_sync_and(1, WALKV_THREADS, ok)) break;  // Kd in place; dS', diag(gamma) dS in TMEM
+    tc::tc_fence_after();
+    if (issuer) {
+      ++k_got;
+      const uint64_t bk = tc::desc_k_sw128(s.BK);
+#pragma unroll
+      for (int k = 0; k < DK / 8; ++k)
+        tc::mma_tf32_ta(tm + kBColD, tm + kBColSp + 8 * k, tc::kstep32(bk, k, CH), kIdB, k > 0);
+      if (st + 1 < n) issue_k(m - 1), ++k_iss;  // Kd^T and gamma were read before the barrier
+    }
+    if (data) {
+      ok = tc::mbar_wait(&s.bar_a, st & 1) && ok;  // Aqk, Q Gamma of this chunk
+      // Aqk^T [j][i] (8 groups) and Qp^T [c][i] (16 groups) into [Aqk^T ; Qp^T].
+      for (int g = warp; g < 24; g += 8) {
+        if (g < 8) transpose_group(SA, CH, 16 * (g >> 1), 32 * (g & 1), BA, CH + DK, 0);
+        else transpose_group(SQ, CH, 16 * ((g - 8) >> 2), 32 * ((g - 8) & 3), BA, CH + DK, CH);
+      }
+      if (st + 1 < n) store_do(m - 1, b ^ 1, don);
+      if (st + 2 < n) load_do(m - 2, don);
+      tc::fence_proxy_async();
+      tc::tmem_wait_st();
+    }
+    tc::tc_fence_before();
+    if (!named_sync_and(3, WALKV_THREADS, ok)) break;  // [Aqk^T ; Qp^T] in place
+    tc::tc_fence_after();
+    if (issuer) {
+      ++a_got;
+      const uint64_t ba = tc::desc_k_sw128(s.BA);
+#pragma unroll
+      for (int k = 0; k < CH / 8; ++k)
+        tc::mma_tf32_ta(tm + kBColD, tm + colDO(b) + 8 * k, tc::kstep32(ba, k, CH + DK), kIdA, 1);
+      tc::mma_commit(&s.bar_ab);
+      ++ab_iss;
+      if (st + 1 < n) issue_a(m - 1), ++a_iss;
+    }
+    if (data) {
+      ok = tc::mbar_wait(&s.bar_w, st & 1) && ok;  // w of this chunk
+      for (int g = warp; g < 16; g += 8) transpose_group(SW, CH, 16 * (g >> 2), 32 * (g & 3), BW, DK, 0);
+      tc::fence_proxy_async();
+      ok = tc::mbar_wait(&s.bar_ab, st & 1) && ok;
+      tc::tc_fence_after();
+      uint32_t r[32];
+      tc::tmem_ld32(tl + kBColD + 32 * hf, r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        ddl[j] = __uint_as_float(r[j]);
+        r[j] = tf32(-ddl[j]);
+      }
+      tc::tmem_st32(tl + kBColD + 32 * hf, r);
+      tc::tmem_wait_st();
+    }
+    tc::tc_fence_before();
+    if (!named_sync_and(2, WALKV_THREADS, ok)) break;  // -dDelta' in TMEM, w^T in place
+    tc::tc_fence_after();
+    if (data) {  // the FP32 dDelta for the gradient kernels, while the last product runs
+      float* dp = a.ddelta + tf_off(chunk, h, a.HV) + (size_t)(32 * hf) * LDF + v;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) dp[(size_t)j * LDF] = ddl[j];
+    }
+    if (issuer) {
+      ++w_got;
+      const uint64_t bw = tc::desc_k_sw128(s.BW);
+#pragma unroll
+      for (int k = 0; k < CH / 8; ++k)
+        tc::mma_tf32_ta(tm + kBColS, tm + kBColD + 8 * k, tc::kstep32(bw, k, DK), kIdC, 1);
+      tc::mma_commit(&s.bar_c);
+      ++c_iss;
+      if (st + 1 < n) issue_w(m - 1), ++w_iss;
+    }
+  }
+  if (st < n) {
+    // A wait ran out: record it and drain the copies and products in flight.
+    if (issuer) {
+      atomicExch(a.err, 4);
+      if (k_iss > k_got) tc::mbar_wait(&s.bar_k, (k_iss - 1) & 1);
+      if (a_iss > a_got) tc::mbar_wait(&s.bar_a, (a_iss - 1) & 1);
+      if (w_iss > w_got) tc::mbar_wait(&s.bar_w, (w_iss - 1) & 1);
+      if (ab_iss > 0) tc::mbar_wait(&s.bar_ab, (ab_iss - 1) & 1);
+      if (c_iss > 0) tc::mbar_wait(&s.bar_c, (c_iss - 1) & 1);
+    }
+  } else if (data) {
+    if (n > 0) {
+      ok = tc::mbar_wait(&s.bar_c, (n - 1) & 1) && ok;
+      tc::tc_fence_after();
+    }
+    if (a.dh0 && ok) {  // dh0[c][v] = dS^T[v][c]
+      uint32_t r[32];
+#pragma unroll
+      for (int cb = 0; cb < 64; cb += 32) {
+        tc::tmem_ld32(tl + kBColS + 64 * hf + cb, r);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a.dh0[sidx + (size_t)(64 * hf + cb + j) * DK + v] = __uint_as_float(r[j]);
+      }
+    }
+    if (!ok) atomicExch(a.err, 4);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
+
+cudaError_t launch_walk_bwd_v(const WalkBwdArgs& a, int ndocs, cudaStream_t st) {
+  if (ndocs == 0) return cudaSuccess;
+  const size_t sm = sizeof(WalkBvSmem) + 1024;
+  cudaFuncSetAttribute(k_walk_bwd_v, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  k_walk_bwd_v<<<ndocs * a.HV, WALKV_THREADS, sm, st>>>(a);
   return cudaGetLastError();
 }
 
