@@ -48,6 +48,7 @@ EXPORTED = (
     "gdr_doc_groups",
     "gdr_launch_count",
     "gdr_set_serial",
+    "gdr_set_segment_chunks",
 )
 
 _lock = threading.Lock()
@@ -71,6 +72,7 @@ _SIGS = {
     "gdr_profile_report": ([ctypes.c_char_p, SZ], ctypes.c_int),
     "gdr_launch_count": ([], ctypes.c_uint64),
     "gdr_set_serial": ([ctypes.c_int], ctypes.c_int),
+    "gdr_set_segment_chunks": ([ctypes.c_int], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
     "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P], ctypes.c_int),
@@ -284,6 +286,12 @@ def gdr_set_serial(on: bool) -> bool:
     """Run every call's launches on the caller's stream (document groups in
     turn) while on; returns the previous setting."""
     return bool(load().gdr_set_serial(int(bool(on))))
+
+
+def gdr_set_segment_chunks(chunks: int) -> int:
+    """Force walk segments of about `chunks` chunks (0: the library's choice);
+    returns the previous setting."""
+    return int(load().gdr_set_segment_chunks(int(chunks)))
 
 
 def gdr_profile_enable(on: bool = True):

@@ -36,9 +36,9 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // index; above kRankLimit documents the order is the given one.  One block; no
 // host copy.  plan_ranks() on the host reproduces the same order.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N, DocDesc* docs, ChunkDesc* chunks,
-                                               int* order) {
-  __shared__ int part[1024];
+__global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N, int lseg, DocDesc* docs,
+                                               ChunkDesc* chunks, int* order, SegDesc* segs) {
+  __shared__ int part[1024], spart[1024];
   __shared__ int lens[kRankLimit];
   __shared__ int ord[kRankLimit];
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -58,32 +58,45 @@ __global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N
   }
   __syncthreads();
   auto doc_at = [&](int r) { return ranked ? ord[r] : r; };
-  // Chunk offsets: a prefix sum of chunk counts over the ranks.
+  // Chunk and segment offsets: prefix sums of chunk and segment counts over the ranks.
   const int per = (N + nt - 1) / nt;
   const int r0 = min(N, tid * per), r1 = min(N, r0 + per);
-  int sum = 0;
+  int sum = 0, ssum = 0;
   for (int r = r0; r < r1; ++r) {
     const int n = doc_at(r);
-    sum += (cu[n + 1] - cu[n] + CH - 1) / CH;
+    const int nch = (cu[n + 1] - cu[n] + CH - 1) / CH;
+    sum += nch;
+    ssum += nch == 0 ? 1 : (nch + lseg - 1) / lseg;
   }
   part[tid] = sum;
+  spart[tid] = ssum;
   __syncthreads();
   if (tid == 0) {
-    int acc = 0;
+    int acc = 0, sacc = 0;
     for (int i = 0; i < nt; ++i) {
-      const int v = part[i];
+      const int v = part[i], sv = spart[i];
       part[i] = acc;
+      spart[i] = sacc;
       acc += v;
+      sacc += sv;
     }
   }
   __syncthreads();
-  int c = part[tid];
+  int c = part[tid], sg = spart[tid];
   for (int r = r0; r < r1; ++r) {
     const int n = doc_at(r);
     const int tok0 = cu[n], len = cu[n + 1] - tok0, nch = (len + CH - 1) / CH;
     docs[n] = DocDesc{tok0, len, c, nch};
     for (int j = 0; j < nch; ++j) chunks[c + j] = ChunkDesc{tok0 + CH * j, min(CH, len - CH * j), n, j};
+    const int nseg = nch == 0 ? 1 : (nch + lseg - 1) / lseg;
+    const int base = nseg > 0 ? nch / nseg : 0, rem = nseg > 0 ? nch % nseg : 0;
+    for (int i = 0; i < nseg; ++i) {
+      const int off = i * base + min(i, rem), cnt = base + (i < rem ? 1 : 0);
+      const int t0 = tok0 + CH * off;
+      segs[sg + i] = SegDesc{n, t0, min(CH * cnt, len - CH * off), c + off, cnt, i, nseg, sg};
+    }
     c += nch;
+    sg += nseg;
   }
 }
 
@@ -99,6 +112,8 @@ struct DocGroup {
   int r0, r1;        // ranks [r0, r1) of order[]
   int64_t c0, c1;    // chunks [c0, c1)
   int64_t tokens;
+  int64_t s0 = 0, s1 = 0;  // segments [s0, s1) (k_plan numbers them in rank order)
+  bool split = false;       // some document of the group has more than one segment
 };
 std::vector<DocGroup> plan_groups(int32_t N, const int32_t* cu) {
   std::vector<int> ord(N);
@@ -136,21 +151,90 @@ std::vector<DocGroup> plan_groups(int32_t N, const int32_t* cu) {
   return gr;
 }
 
+// Segments of the state walks.  A chain (document, value head) is walked one
+// chunk after another; a long document is split into segments of about
+// `lseg` chunks whose walks run in parallel: summary walks give each
+// segment's affine map of its start state, a merge chains the start states,
+// and the full walks of all segments then run from their start states (the
+// segment plan of PR #7723, "perf(cake_gdn): prefetch offset adjoint walk,
+// default LPT segment plan", on one GPU).  Splitting adds walk work (the
+// summary walks), so it pays only when the longest document's chain, walked
+// whole, outlasts the work of all the other documents spread over the SMs
+// (which the document groups run beside it): per chunk, the forward and
+// backward walk steps take about kWalkStepNs on the chain, and a chunk of one
+// head costs about kChunkHeadNs of SM time over the whole step (prep, walks,
+// gradients), both measured on GB300.  A split pack gets segments of
+// lseg = max(kMinSegChunks, chunks x heads / SMs), which about fill the SMs.
+constexpr int kMinSegChunks = 64;
+constexpr int kNoSplit = 1 << 30;
+constexpr double kWalkStepNs = 8300.0, kChunkHeadNs = 50000.0;
+std::atomic<int> g_seg_chunks{0};  // gdr_set_segment_chunks: 0 = choose
+
+int sm_count();
+
+int segment_chunks(int32_t N, const int32_t* cu, int32_t HV) {
+  const int forced = g_seg_chunks.load();
+  if (forced > 0) return forced;
+  int64_t total = 0, longest = 0;
+  for (int32_t n = 0; n < N; ++n) {
+    const int64_t nch = (cu[n + 1] - cu[n] + CH - 1) / CH;
+    total += nch;
+    longest = std::max(longest, nch);
+  }
+  const int64_t sms = sm_count();
+  const double chain_ns = (double)longest * kWalkStepNs;
+  const double others_ns = (double)(total - longest) * HV * kChunkHeadNs / (double)sms;
+  if (chain_ns <= others_ns) return kNoSplit;
+  const int64_t l = std::max<int64_t>(kMinSegChunks, (total * HV + sms - 1) / sms);
+  return longest <= l ? kNoSplit : (int)l;
+}
+
+int64_t doc_segments(int64_t nch, int lseg) { return nch == 0 ? 1 : (nch + lseg - 1) / lseg; }
+
+// Segment ranges of the groups (the documents' segments in rank order) and
+// the total segment count.
+int64_t assign_segments(std::vector<DocGroup>& groups, int32_t N, const int32_t* cu, int lseg) {
+  std::vector<int> ord(N);
+  for (int n = 0; n < N; ++n) ord[n] = n;
+  if (N <= kRankLimit)
+    std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) { return cu[x + 1] - cu[x] > cu[y + 1] - cu[y]; });
+  std::vector<int64_t> first(N + 1, 0);
+  std::vector<bool> split(N, false);
+  for (int r = 0; r < N; ++r) {
+    const int64_t nch = (cu[ord[r] + 1] - cu[ord[r]] + CH - 1) / CH;
+    const int64_t ns = doc_segments(nch, lseg);
+    first[r + 1] = first[r] + ns;
+    split[r] = ns > 1;
+  }
+  for (DocGroup& g : groups) {
+    g.s0 = first[g.r0];
+    g.s1 = first[g.r1];
+    g.split = false;
+    for (int r = g.r0; r < g.r1; ++r) g.split = g.split || split[r];
+  }
+  return first[N];
+}
+
 // ---------------------------------------------------------------------------
 // Workspace layout.
 // ---------------------------------------------------------------------------
 struct Layout {
-  int64_t NC = 0;
-  size_t docs = 0, chunks = 0, order = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, amat = 0, tmat = 0,
-         gam = 0, tape = 0;
+  int64_t NC = 0, NSEG = 0;
+  size_t docs = 0, chunks = 0, order = 0, segs = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, amat = 0,
+         tmat = 0, gam = 0, tape = 0, smap = 0, sstart = 0, sbias = 0;
   size_t saved_total = 0;
-  size_t dstape = 0, ddelta = 0, dqs = 0, dw = 0, dkd = 0, dgam = 0, daqk = 0, dqp = 0, dkp = 0;
+  size_t dstape = 0, ddelta = 0, dqs = 0, dw = 0, dkd = 0, dgam = 0, daqk = 0, dqp = 0, dkp = 0, dsend = 0, dsbias = 0;
   size_t bwd_total = 0;
 };
 
-Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
+// NSEG: segments of the walks (equal to N when no document is split); the
+// per-segment state buffers are only laid out when some document is.
+Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped, int64_t NSEG) {
   Layout L;
   L.NC = NC;
+  L.NSEG = NSEG;
+  const bool split = NSEG > N;
+  const size_t segstate = split ? (size_t)NSEG * HV * DK * DK * sizeof(float) : 0;
   const size_t tile = (size_t)NC * HV * CH * DK * sizeof(float);
   const size_t vec = (size_t)NC * HV * DK * sizeof(float);
   const size_t st = (size_t)NC * HV * DK * DK * sizeof(uint16_t);  // BF16 state tapes
@@ -163,6 +247,10 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
   L.docs = take((size_t)std::max(N, 1) * sizeof(DocDesc));
   L.chunks = take((size_t)std::max<int64_t>(NC, 1) * sizeof(ChunkDesc));
   L.order = take((size_t)std::max(N, 1) * sizeof(int));
+  L.segs = take((size_t)std::max<int64_t>(NSEG, 1) * sizeof(SegDesc));
+  L.smap = take(segstate);    // each split segment's state map (the backward merge needs it too)
+  L.sstart = take(segstate);  // start state of each segment
+  L.sbias = take(segstate);   // each segment's end state from a zero start
   L.w = take((size_t)NC * HV * CH * LDT * sizeof(float));
   L.u = take((size_t)NC * HV * CH * LDF * sizeof(float));
   L.qp = take((size_t)NC * HV * CH * LDF * sizeof(float));
@@ -182,6 +270,8 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped) {
   L.dkd = take(tile);
   L.dgam = take(vec);
   L.daqk = take((size_t)NC * HV * CH * LDS * sizeof(float));
+  L.dsend = take(segstate);   // adjoint of each segment's end state
+  L.dsbias = take(segstate);  // each segment's start adjoint from a zero end adjoint
   if (grouped) {
     L.dqp = take(tile);
     L.dkp = take(tile);
@@ -218,7 +308,7 @@ uint64_t hash_cu(const int32_t* cu, int32_t N) {
 // by the buffer address (no device read, no host synchronization).
 struct Stamp {
   int64_t T;
-  int32_t N, Hqk, HV, variant;
+  int32_t N, Hqk, HV, variant, lseg;
   uint64_t cu_hash;
 };
 std::mutex g_stamp_mu;
@@ -234,7 +324,7 @@ bool stamp_check(const void* saved, const Stamp& s) {
   if (it == g_stamps.end()) return false;
   const Stamp& r = it->second;
   return r.T == s.T && r.N == s.N && r.Hqk == s.Hqk && r.HV == s.HV && r.variant == s.variant &&
-         r.cu_hash == s.cu_hash;
+         r.lseg == s.lseg && r.cu_hash == s.cu_hash;
 }
 
 gdr_status check_device() {
@@ -499,7 +589,9 @@ gdr_status workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const 
   int64_t NC = 0;
   const gdr_status st = plan_host(T, N, cu, &NC);
   if (st != GDR_OK) return st;
-  const Layout L = make_layout(NC, N, HV, HV != Hqk);
+  std::vector<DocGroup> groups = plan_groups(N, cu);
+  const int64_t NSEG = assign_segments(groups, N, cu, segment_chunks(N, cu, HV));
+  const Layout L = make_layout(NC, N, HV, HV != Hqk, NSEG);
   if (saved_bytes) *saved_bytes = L.saved_total;
   if (scratch_bytes) *scratch_bytes = L.bwd_total;
   return GDR_OK;
@@ -519,7 +611,10 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   if (!aligned_to(q, 16) || !aligned_to(k, 16) || !aligned_to(v, 16) || !aligned_to(g, 16) || !aligned_to(out, 4))
     return GDR_INVALID_ARG;
   if (save_for_bwd && !saved) return GDR_INVALID_ARG;
-  const Layout L = make_layout(NC, N, HV, HV != Hqk);
+  const int lseg = segment_chunks(N, cu_host, HV);
+  std::vector<DocGroup> groups = plan_groups(N, cu_host);
+  const int64_t NSEG = assign_segments(groups, N, cu_host, lseg);
+  const Layout L = make_layout(NC, N, HV, HV != Hqk, NSEG);
   void* base = saved ? saved : scratch;
   const size_t have = saved ? saved_bytes : scratch_bytes;
   if (!base) return GDR_INVALID_ARG;
@@ -531,9 +626,10 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   DocDesc* docs = at<DocDesc>(base, L.docs);
   ChunkDesc* chunks = at<ChunkDesc>(base, L.chunks);
   int* order = at<int>(base, L.order);
+  SegDesc* segs = at<SegDesc>(base, L.segs);
   {
     ProfScope ps("plan", stream);
-    k_plan<<<1, 1024, 0, stream>>>(cu, N, docs, chunks, order);
+    k_plan<<<1, 1024, 0, stream>>>(cu, N, std::min(lseg, kNoSplit), docs, chunks, order, segs);
   }
   if (cudaGetLastError() != cudaSuccess) return GDR_CUDA_ERROR;
   const bool vec = variant == 0;
@@ -555,9 +651,18 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   pa.amat = save_for_bwd ? at<float>(base, L.amat) : nullptr;
   pa.tmat = save_for_bwd ? at<float>(base, L.tmat) : nullptr;
   WalkArgs wa{};
-  wa.docs = docs;
-  wa.order = order;
+  wa.segs = segs;
   wa.HV = HV;
+  const bool split = NSEG > N;
+  wa.smap = split ? at<float>(base, L.smap) : nullptr;
+  wa.sstart = split ? at<float>(base, L.sstart) : nullptr;
+  wa.sbias = split ? at<float>(base, L.sbias) : nullptr;
+  MergeArgs ma{};
+  ma.segs = segs;
+  ma.HV = HV;
+  ma.smap = wa.smap;
+  ma.state = wa.sstart;
+  ma.bias = wa.sbias;
   wa.u = pa.u;
   wa.gam = pa.gam;
   wa.err = device_error_ptr();
@@ -578,29 +683,43 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   // Document groups as in the backward: each group's walk needs only its own
   // prep, so the longest document's walk starts once its chunks are prepared.
   {
-    const std::vector<DocGroup> groups = plan_groups(N, cu_host);
     Fork fork(stream, (int)groups.size());
     if (!fork.begin()) return GDR_CUDA_ERROR;
     for (size_t i = 0; i < groups.size() && st == GDR_OK; ++i) {
       const DocGroup& G = groups[i];
       const cudaStream_t ls = fork.lane((int)i);
       const double units = (double)G.tokens * HV;
+      const int nsg = (int)(G.s1 - G.s0);
       pa.chunk_base = (int)G.c0;
-      wa.rank_base = G.r0;
+      wa.seg_base = ma.seg_base = (int)G.s0;
       {
         ProfScope ps("prep", ls, units);
         st = cuda_status(launch_prep(pa, (int)(G.c1 - G.c0), vec, vec, ls));
       }
       if (st != GDR_OK) break;
+      if (G.split) {
+        wa.mode = 1;
+        {
+          ProfScope ps("walk_fwd_sum", ls, units);
+          st = cuda_status(launch_walk_fwd_v(wa, nsg, ls));
+        }
+        if (st != GDR_OK) break;
+        {
+          ProfScope ps("merge_fwd", ls, units);
+          st = cuda_status(launch_merge(ma, nsg, false, ls));
+        }
+        if (st != GDR_OK) break;
+      }
+      wa.mode = 0;
       {
         ProfScope ps("walk_fwd", ls, units);
-        st = cuda_status(launch_walk_fwd_v(wa, G.r1 - G.r0, ls));
+        st = cuda_status(launch_walk_fwd_v(wa, nsg, ls));
       }
     }
     if (!fork.join() && st == GDR_OK) st = GDR_CUDA_ERROR;
   }
   if (st != GDR_OK) return st;
-  if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, hash_cu(cu_host, N)});
+  if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, lseg, hash_cu(cu_host, N)});
   return GDR_OK;
 }
 
@@ -620,21 +739,30 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
       !aligned_to(dq, 4) || !aligned_to(dk, 4) || !aligned_to(dv, 4))
     return GDR_INVALID_ARG;
   if (!aligned(saved) || !aligned(scratch)) return GDR_INVALID_ARG;
-  const Layout L = make_layout(NC, N, HV, HV != Hqk);
+  const int lseg = segment_chunks(N, cu_host, HV);
+  std::vector<DocGroup> groups = plan_groups(N, cu_host);
+  const int64_t NSEG = assign_segments(groups, N, cu_host, lseg);
+  const Layout L = make_layout(NC, N, HV, HV != Hqk, NSEG);
   if (saved_bytes < L.saved_total || scratch_bytes < L.bwd_total) return GDR_WORKSPACE_TOO_SMALL;
-  if (!stamp_check(saved, Stamp{T, N, Hqk, HV, variant, hash_cu(cu_host, N)})) return GDR_STALE_WORKSPACE;
+  if (!stamp_check(saved, Stamp{T, N, Hqk, HV, variant, lseg, hash_cu(cu_host, N)})) return GDR_STALE_WORKSPACE;
   st = check_device();
   if (st != GDR_OK) return st;
   const bool vec = variant == 0;
-  const DocDesc* docs = at<DocDesc>(saved, L.docs);
   const ChunkDesc* chunks = at<ChunkDesc>(saved, L.chunks);
-  const int* order = at<int>(saved, L.order);
 
+  const SegDesc* segs = at<SegDesc>(saved, L.segs);
+  const bool split = NSEG > N;
   WalkBwdArgs wb{};
-  wb.docs = docs;
-  wb.order = order;
-  wb.chunks = chunks;
+  wb.segs = segs;
   wb.HV = HV;
+  wb.dsend = split ? at<float>(scratch, L.dsend) : nullptr;
+  wb.dsbias = split ? at<float>(scratch, L.dsbias) : nullptr;
+  MergeArgs mb{};
+  mb.segs = segs;
+  mb.HV = HV;
+  mb.smap = split ? at<float>(saved, L.smap) : nullptr;
+  mb.state = wb.dsend;
+  mb.bias = wb.dsbias;
   wb.scale = scale;
   wb.w = at<float>(saved, L.w);
   wb.qp = at<float>(saved, L.qp);
@@ -716,7 +844,6 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   // Document groups (longest documents first, each on a stream of its own):
   // a group's gradient kernels need only its own walk, so the gradients of the
   // documents whose walks end first run on the SMs the other walks leave idle.
-  const std::vector<DocGroup> groups = plan_groups(N, cu_host);
   Fork fork(stream, (int)groups.size());
   if (!fork.begin()) return GDR_CUDA_ERROR;
 
@@ -724,12 +851,26 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
     const DocGroup& G = groups[i];
     const cudaStream_t ls = fork.lane((int)i);
     const double units = (double)G.tokens * HV;
-    const int nc = (int)(G.c1 - G.c0);
-    wb.rank_base = G.r0;
+    const int nc = (int)(G.c1 - G.c0), nsg = (int)(G.s1 - G.s0);
+    wb.seg_base = mb.seg_base = (int)G.s0;
     gs.chunk_base = ga.chunk_base = gr.chunk_base = (int)G.c0;
+    if (G.split) {
+      wb.mode = 1;
+      {
+        ProfScope ps("walk_bwd_sum", ls, units);
+        st = cuda_status(launch_walk_bwd_v(wb, nsg, ls));
+      }
+      if (st != GDR_OK) break;
+      {
+        ProfScope ps("merge_bwd", ls, units);
+        st = cuda_status(launch_merge(mb, nsg, true, ls));
+      }
+      if (st != GDR_OK) break;
+    }
+    wb.mode = 0;
     {
       ProfScope ps("walk_bwd", ls, units);
-      st = cuda_status(launch_walk_bwd_v(wb, G.r1 - G.r0, ls));
+      st = cuda_status(launch_walk_bwd_v(wb, nsg, ls));
     }
     if (st != GDR_OK) break;
     {
@@ -921,6 +1062,8 @@ gdr_status gdr_check_device(void) {
 uint64_t gdr_launch_count(void) { return gdr::g_launches.load(); }
 
 int gdr_set_serial(int on) { return gdr::g_serial.exchange(on != 0) ? 1 : 0; }
+
+int gdr_set_segment_chunks(int chunks) { return gdr::g_seg_chunks.exchange(chunks > 0 ? chunks : 0); }
 
 int gdr_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(gdr::g_prof_mu);

@@ -24,194 +24,6 @@
 namespace gdr {
 
 // ---------------------------------------------------------------------------
-// Reverse adjoint walk (one CTA per (document, value head, value-column
-// slice), chunks in reverse).  Each warp owns 16 value columns of dS^T.
-// Per chunk: phase 1 uses Aqk, Kd, dO (tiles of group A, double-buffered),
-// phase 2 uses Qp, w (group B, single-buffered, copied while phase 1 of the
-// same chunk runs).  The saved tiles are stored with their shared-memory
-// pitch and arrive as one bulk copy each on an mbarrier (waits bounded: a
-// timed-out wait ends the walk and sets the device error word); the dO
-// slice comes by cp.async.  The "adjoint walk" of PR #7723 "perf(cake_gdn):
-// prefetch offset adjoint walk, default LPT segment plan" (opening
-// description), which also loads its operands one step ahead.
-// ---------------------------------------------------------------------------
-template <int NW>
-struct WalkBwdA {
-  float Aqk[CH * LDS];
-  float Kd[DK * LDS];  // Kd^T, [c][j]
-  uint16_t dO[CH * (NW * 16 + 8)];
-  float gam[DK];
-};
-struct WalkBwdB {
-  float Qp[CH * LDF];  // read with the row on the thread-in-group index
-  float W[CH * LDT];   // read on rows 2t, 2t+1
-  uint64_t barA[2], barB;
-};
-
-template <int NW>
-__global__ void __launch_bounds__(NW * 32) k_walk_bwd(WalkBwdArgs a) {
-  constexpr int VS = 8 / NW;
-  constexpr int LDO = NW * 16 + 8;  // row stride (elements) of the BF16 dO slice
-  constexpr int NTH = NW * 32;
-  using SA = WalkBwdA<NW>;
-  extern __shared__ __align__(16) unsigned char smraw[];
-  SA* sa = reinterpret_cast<SA*>(smraw);
-  WalkBwdB& sb = *reinterpret_cast<WalkBwdB*>(smraw + 2 * sizeof(SA));
-  const int rank = a.rank_base + blockIdx.x / (a.HV * VS);  // longest document first, all its heads
-  const int h = (blockIdx.x / VS) % a.HV;
-  const int doc = a.order[rank];
-  const DocDesc dd = a.docs[doc];
-  const int warp = threadIdx.x >> 5;
-  const int lane = lane_id(), g = lane >> 2, t = lane & 3;
-  const int vcta = (blockIdx.x % VS) * NW * 16;
-  const int v0 = vcta + warp * 16, w16 = warp * 16;
-  const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
-  const int n = dd.nchunks;
-
-  if (threadIdx.x == 0) {
-    tc::mbar_init(&sb.barA[0], 1);
-    tc::mbar_init(&sb.barA[1], 1);
-    tc::mbar_init(&sb.barB, 1);
-    tc::mbar_fence_init();
-  }
-  __syncthreads();
-
-  auto issueA = [&](int s, SA& A, uint64_t* bar) {  // step s processes chunk n-1-s
-    const int chunk = dd.chunk0 + n - 1 - s;
-    const ChunkDesc cd = a.chunks[chunk];
-    if (threadIdx.x == 0) {
-      tc::mbar_arrive_expect_tx(bar, (DK * LDS + CH * LDS + DK) * 4);
-      tc::bulk_load(A.Kd, &a.kd[kd_off(chunk, h, a.HV)], DK * LDS * 4, bar);
-      tc::bulk_load(A.Aqk, &a.aqk[aqk_off(chunk, h, a.HV)], CH * LDS * 4, bar);
-      tc::bulk_load(A.gam, &a.gam[((size_t)chunk * a.HV + h) * DK], DK * 4, bar);
-    }
-    for (int e = threadIdx.x; e < CH * NW * 2; e += NTH) {  // 16-byte pieces of 8 BF16
-      const int i = e / (NW * 2), c8 = (e % (NW * 2)) * 8;
-      if (i < cd.len) {
-        cp_async16(&A.dO[i * LDO + c8], &a.dout[((size_t)(cd.tok0 + i) * a.HV + h) * DK + vcta + c8]);
-      } else {
-        *reinterpret_cast<uint4*>(&A.dO[i * LDO + c8]) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-  };
-  auto issueB = [&](int s) {  // thread 0
-    const int chunk = dd.chunk0 + n - 1 - s;
-    tc::mbar_arrive_expect_tx(&sb.barB, (CH * LDF + CH * LDT) * 4);
-    tc::bulk_load(sb.Qp, &a.qp[qp_off(chunk, h, a.HV)], CH * LDF * 4, &sb.barB);
-    tc::bulk_load(sb.W, &a.w[w_off(chunk, h, a.HV)], CH * LDT * 4, &sb.barB);
-  };
-
-  float S[16][4];  // dS^T rows v0+g(+8), cols c
-  acc_foreach(S, [&](int r, int c, float& x) { x = a.dht ? a.dht[sidx + (size_t)c * DK + v0 + r] : 0.f; });
-
-  int issuedA = 0, issuedB = 0, doneA = 0, doneB = 0;
-  if (n > 0) {
-    issueA(0, sa[0], &sb.barA[0]);
-    if (threadIdx.x == 0) issueB(0);
-    issuedA = issuedB = 1;
-  }
-  cp_async_commit();
-  bool ok = true;
-  int s = 0;
-  for (; s < n; ++s) {
-    const int chunk = dd.chunk0 + n - 1 - s;
-    const size_t toff = tile_off(chunk, h, a.HV);
-    if (s + 1 < n) {  // buffer (s+1) & 1 was last read in step s-1
-      issueA(s + 1, sa[(s + 1) & 1], &sb.barA[(s + 1) & 1]);
-      issuedA = s + 2;
-    }
-    cp_async_commit();
-    cp_async_wait<1>();  // dO of this step
-    ok = tc::mbar_wait(&sb.barA[s & 1], (s >> 1) & 1) && ok;  // Kd, Aqk, gamma of this step
-    if (!__syncthreads_and(ok)) break;
-    doneA = s + 1;
-    const SA& A = sa[s & 1];
-    {  // dS^T, [v][c], as BF16 pairs
-      __nv_bfloat16* tp = a.dstape + state_off(chunk, h, a.HV);
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int c = nt * 8 + 2 * t;
-        *reinterpret_cast<__nv_bfloat162*>(&tp[(size_t)(v0 + g) * DK + c]) = __floats2bfloat162_rn(S[nt][0], S[nt][1]);
-        *reinterpret_cast<__nv_bfloat162*>(&tp[(size_t)(v0 + g + 8) * DK + c]) =
-            __floats2bfloat162_rn(S[nt][2], S[nt][3]);
-      }
-    }
-    // E = dDelta^T (16 x 64) = scale dO^T Aqk + dS^T Kd^T
-    float E[8][4];
-    zero_acc(E);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int ia = kk * 8 + t, ib = ia + 4;
-      uint32_t av[4] = {(uint32_t)A.dO[ia * LDO + w16 + g] << 16, (uint32_t)A.dO[ia * LDO + w16 + g + 8] << 16,
-                        (uint32_t)A.dO[ib * LDO + w16 + g] << 16, (uint32_t)A.dO[ib * LDO + w16 + g + 8] << 16};
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        if (nt <= kk) {
-          uint32_t b[2] = {__float_as_uint(A.Aqk[ia * LDS + nt * 8 + g]), __float_as_uint(A.Aqk[ib * LDS + nt * 8 + g])};
-          mma8(E[nt], av, b);
-        }
-      }
-    }
-    acc_foreach(E, [&](int r, int j, float& x) { x *= a.scale; });
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      uint32_t av[4] = {tf32(S[kk][0]), tf32(S[kk][2]), tf32(S[kk][1]), tf32(S[kk][3])};
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        uint32_t b[2] = {__float_as_uint(A.Kd[(kk * 8 + 2 * t) * LDS + nt * 8 + g]),
-                         __float_as_uint(A.Kd[(kk * 8 + 2 * t + 1) * LDS + nt * 8 + g])};
-        mma8(E[nt], av, b);
-      }
-    }
-    acc_foreach(E, [&](int r, int j, float& x) { a.ddelta[tf_off(chunk, h, a.HV) + (size_t)j * LDF + v0 + r] = x; });
-    ok = tc::mbar_wait(&sb.barB, s & 1) && ok;  // Qp, w of this step
-    if (!__syncthreads_and(ok)) break;
-    doneB = s + 1;
-    // dS^T <- dS^T diag(gamma) + scale dO^T Qp - dDelta^T w
-    acc_foreach(S, [&](int r, int c, float& x) { x *= A.gam[c]; });
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int ia = kk * 8 + t, ib = ia + 4;
-      uint32_t av[4] = {tf32(a.scale * bfbits2f(A.dO[ia * LDO + w16 + g])),
-                        tf32(a.scale * bfbits2f(A.dO[ia * LDO + w16 + g + 8])),
-                        tf32(a.scale * bfbits2f(A.dO[ib * LDO + w16 + g])),
-                        tf32(a.scale * bfbits2f(A.dO[ib * LDO + w16 + g + 8]))};
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {__float_as_uint(sb.Qp[ia * LDF + nt * 8 + g]), __float_as_uint(sb.Qp[ib * LDF + nt * 8 + g])};
-        mma8(S[nt], av, b);
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t av[4] = {tf32(-E[kk][0]), tf32(-E[kk][2]), tf32(-E[kk][1]), tf32(-E[kk][3])};
-      const int j0 = kk * 8 + 2 * t;
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        uint32_t b[2] = {__float_as_uint(sb.W[j0 * LDT + nt * 8 + g]), __float_as_uint(sb.W[(j0 + 1) * LDT + nt * 8 + g])};
-        mma8(S[nt], av, b);
-      }
-    }
-    __syncthreads();
-    if (s + 1 < n) {
-      if (threadIdx.x == 0) issueB(s + 1);
-      issuedB = s + 2;
-    }
-  }
-  cp_async_wait<0>();
-  if (s < n) {
-    // A wait ran out: record it and drain the copies still in flight.
-    if (threadIdx.x == 0) {
-      atomicExch(a.err, 4);
-      for (int q = doneA; q < issuedA; ++q) tc::mbar_wait(&sb.barA[q & 1], (q >> 1) & 1);
-      for (int q = doneB; q < issuedB; ++q) tc::mbar_wait(&sb.barB, q & 1);
-    }
-    return;
-  }
-  if (a.dh0) acc_foreach(S, [&](int r, int c, float& x) { a.dh0[sidx + (size_t)c * DK + v0 + r] = x; });
-}
-
-// ---------------------------------------------------------------------------
 // State-side products on the tensor cores (one CTA of 8 warps per (chunk,
 // value head)):
 //   dqs = scale dO S0^T,  dw = -dDelta S0^T,  dKd = Delta dS^T,
@@ -820,25 +632,6 @@ __global__ void __launch_bounds__(256) k_group_reduce(GroupReduceArgs a) {
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
-template <int NW>
-static cudaError_t launch_walk_bwd_nw(const WalkBwdArgs& a, int ndocs, cudaStream_t st) {
-  const size_t sm = 2 * sizeof(WalkBwdA<NW>) + sizeof(WalkBwdB);
-  cudaFuncSetAttribute(k_walk_bwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  dim3 grid(ndocs * a.HV * (8 / NW));
-  k_walk_bwd<NW><<<grid, NW * 32, sm, st>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, cudaStream_t st) {
-  if (ndocs == 0) return cudaSuccess;
-  switch (warps_per_cta) {
-    case 1: return launch_walk_bwd_nw<1>(a, ndocs, st);
-    case 2: return launch_walk_bwd_nw<2>(a, ndocs, st);
-    case 4: return launch_walk_bwd_nw<4>(a, ndocs, st);
-    default: return launch_walk_bwd_nw<8>(a, ndocs, st);
-  }
-}
-
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st) {
   if (nchunks == 0) return cudaSuccess;
   const size_t sm = sizeof(GradStateSmem) + 1024;

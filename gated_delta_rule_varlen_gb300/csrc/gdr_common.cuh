@@ -57,6 +57,22 @@ struct DocDesc {
   int tok0, len, chunk0, nchunks;
 };
 
+// One segment of a document's chunks, the unit of work of a state-walk CTA.
+// A document of n chunks is split into nseg >= 1 segments of balanced length
+// (the first n % nseg get one chunk more); an empty document is one empty
+// segment.  Segments are numbered in the walks' document order, so that the
+// segments of a run of documents form one contiguous range.
+struct SegDesc {
+  int doc;      // document index
+  int tok0;     // first token
+  int len;      // tokens
+  int chunk0;   // first chunk (global chunk index)
+  int nchunks;  // chunks
+  int idx;      // index within the document
+  int nseg;     // segments of the document
+  int first;    // global index of the document's first segment
+};
+
 __device__ __forceinline__ uint32_t tf32(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));

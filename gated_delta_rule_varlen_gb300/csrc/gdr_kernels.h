@@ -9,6 +9,7 @@ namespace gdr {
 
 struct ChunkDesc;
 struct DocDesc;
+struct SegDesc;
 
 // Chunk-major intermediates: tiles [NC][HV][64][128] FP32, Aqk [NC][HV][64][64],
 // Kd stored transposed per chunk ([NC][HV][128 c][64 j]), gamma [NC][HV][128],
@@ -32,27 +33,29 @@ struct WalkArgs {
   CUtensorMap u_map;    // u        [NC*HV*64][128], pitch 128, 32 x 64 boxes
   CUtensorMap qp_map;   // Q Gamma  [NC*HV*64][128], pitch LDF, 32 x 64 boxes
   CUtensorMap aqk_map;  // Aqk      [NC*HV*64][64],  pitch LDS, 32 x 64 boxes
-  const DocDesc* docs;
-  const int* order;  // documents, longest first
+  const SegDesc* segs;  // walk segments, the longest document's first
   int HV;
   const float *u, *gam;
   const float* h0;   // [N][HV][128][128] or null
-  __nv_bfloat16* tape;  // S0 per chunk (BF16, S[c][v]), or null
+  __nv_bfloat16* tape;  // S0 per chunk (BF16, chunk-major), or null
   float* delta;      // Delta per chunk, or null
   float* ht;         // [N][HV][128][128] or null
   __nv_bfloat16* out;  // [T][HV][128]
+  // Per-segment states [NSEG][HV][128][128] (S[c][v]) of split documents:
+  float* smap;       // the segment's state map M (end state = M start + bias)
+  float* sstart;     // the segment's start state
+  float* sbias;      // the segment's end state from a zero start
   float scale;
   int* err;          // device error word
-  int rank_base;     // documents order[rank_base ..] (longest first)
+  int seg_base;      // segments seg_base + blockIdx.x / HV
+  int mode;          // 0 the full walks, 1 the summary walks (blockIdx.y: role)
 };
 
 
 struct WalkBwdArgs {
   // The saved tiles as the forward reads them (FP32, 32-column boxes, 128-byte swizzle):
   CUtensorMap w_map, kdt_map, qp_map, aqk_map;
-  const DocDesc* docs;
-  const int* order;
-  const ChunkDesc* chunks;
+  const SegDesc* segs;
   int HV;
   float scale;
   const float *w, *qp, *kd, *aqk, *gam;
@@ -61,8 +64,21 @@ struct WalkBwdArgs {
   __nv_bfloat16* dstape;      // dS (adjoint of each chunk's end state), BF16
   float* ddelta;              // dDelta per chunk
   float* dh0;                 // or null
+  float* dsend;               // per segment: the adjoint of its end state
+  float* dsbias;              // per segment: its start adjoint from a zero end adjoint
   int* err;                   // device error word
-  int rank_base;              // documents order[rank_base ..] (longest first)
+  int seg_base;
+  int mode;                   // 0 the full walks, 1 the summary walks (blockIdx.y: role)
+};
+
+// Merges of the segment states of split documents (one CTA per (segment,
+// head, 16-column slice); only a document's first segment works).
+struct MergeArgs {
+  const SegDesc* segs;
+  int HV, seg_base;
+  const float* smap;
+  float* state;       // forward: start states; backward: end adjoints
+  const float* bias;  // forward: end states from zero; backward: start adjoints from zero
 };
 
 struct GradStateArgs {
@@ -107,10 +123,9 @@ struct GroupReduceArgs {
 };
 
 cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
-cudaError_t launch_walk_fwd(const WalkArgs& a, int ndocs, int cols_per_cta, cudaStream_t st);
-cudaError_t launch_walk_fwd_v(const WalkArgs& a, int ndocs, cudaStream_t st);
-cudaError_t launch_walk_bwd(const WalkBwdArgs& a, int ndocs, int warps_per_cta, cudaStream_t st);
-cudaError_t launch_walk_bwd_v(const WalkBwdArgs& a, int ndocs, cudaStream_t st);
+cudaError_t launch_walk_fwd_v(const WalkArgs& a, int nsegs, cudaStream_t st);
+cudaError_t launch_merge(const MergeArgs& a, int nsegs, bool backward, cudaStream_t st);
+cudaError_t launch_walk_bwd_v(const WalkBwdArgs& a, int nsegs, cudaStream_t st);
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_grad(const GradArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
 cudaError_t launch_group_reduce(const GroupReduceArgs& a, int nchunks, cudaStream_t st);

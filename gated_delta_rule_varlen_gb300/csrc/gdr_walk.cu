@@ -22,7 +22,9 @@
 //
 // Tensor-memory columns (512): Pd[0] 0..63, O[0] 64..127, S 128..255,
 // O[1] 256..319, Pd[1] 320..383, S' 384..511.  Chunk m uses Pd[m&1] (P, then
-// Delta in place) and O[m&1]: the first product writes [Pd[0] | O[0]] (even m,
+// the FP32 Delta in place; its TF32 copy, the A operand of the update, goes
+// to the first 64 columns of S', which the first product no longer reads)
+// and O[m&1]: the first product writes [Pd[0] | O[0]] (even m,
 // B rows [w ; Qp]) or [O[1] | Pd[1]] (odd m, B rows [Qp ; w]); the second
 // accumulates into [O[0] | S] (even, B rows [Aqk ; Kd^T]) or [S | O[1]] (odd,
 // B rows [Kd^T ; Aqk]).  O of a chunk is written out while the next chunk's
@@ -58,6 +60,7 @@ constexpr uint32_t WALKV_B1_BYTES = 2 * CH * DK * 4 + DK * 4;
 constexpr uint32_t WALKV_B2_BYTES = (DK + CH) * CH * 4;
 constexpr uint32_t WALKV_U_BYTES = CH * DK * 4;
 constexpr uint32_t kColS = 128, kColSp = 384;
+constexpr uint32_t kColDl = 384;  // TF32 Delta: the first 64 columns of S', free once [P | O] is done
 __device__ __forceinline__ uint32_t colPd(int b) { return b ? 320u : 0u; }   // P, then Delta, of parity b
 __device__ __forceinline__ uint32_t colO(int b) { return b ? 256u : 64u; }   // O of parity b
 __device__ __forceinline__ uint32_t colD1(int b) { return b ? 256u : 0u; }   // D of [P | O] / [O | P]
@@ -69,16 +72,39 @@ __device__ __forceinline__ size_t tape_off(int v, int c) { return ((size_t)(c >>
 __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_constant__ WalkArgs a) {
   extern __shared__ unsigned char smraw[];
   WalkVSmem& s = *reinterpret_cast<WalkVSmem*>(tc::align1024(smraw));
-  const int rank = a.rank_base + blockIdx.x / a.HV;  // all heads of the longest document first
+  const int seg = a.seg_base + blockIdx.x / a.HV;  // all heads of the longest document's segments first
   const int h = blockIdx.x % a.HV;
-  const int doc = a.order[rank];
-  const DocDesc dd = a.docs[doc];
+  const SegDesc dd = a.segs[seg];
   const int n = dd.nchunks;
+  // What this CTA walks: its segment's full walk with the outputs (mode 0);
+  // in the summary launch (mode 1), by blockIdx.y: 0 the first segment of a
+  // split document from h0, giving the start state of the second; 1 a middle
+  // segment from a zero state (its bias); 2 a middle segment from the
+  // identity without u (its state map M).
+  int kind = 0;
+  if (a.mode == 1) {
+    kind = 1 + (int)blockIdx.y;
+    const bool on = blockIdx.y == 0 ? (dd.idx == 0 && dd.nseg > 1) : (dd.idx >= 1 && dd.idx <= dd.nseg - 2);
+    if (!on) return;
+  }
+  const bool outputs = kind == 0, use_u = kind != 3;
+  // Start and end states (S[c][v]): h0 / ht of the document, or per-segment
+  // buffers [NSEG][HV][128][128].
+  auto start_state = [&]() -> const float* {
+    const size_t sidx = ((size_t)dd.doc * a.HV + h) * DK * DK, gidx = ((size_t)seg * a.HV + h) * DK * DK;
+    return (kind == 0 && dd.idx > 0) ? a.sstart + gidx : (kind <= 1 && a.h0 ? a.h0 + sidx : nullptr);
+  };
+  auto end_state = [&]() -> float* {
+    const size_t sidx = ((size_t)dd.doc * a.HV + h) * DK * DK, gidx = ((size_t)seg * a.HV + h) * DK * DK;
+    return kind == 0   ? (dd.idx == dd.nseg - 1 && a.ht ? a.ht + sidx : nullptr)
+           : kind == 1 ? a.sstart + gidx + (size_t)a.HV * DK * DK
+           : kind == 2 ? a.sbias + gidx
+                       : a.smap + gidx;
+  };
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   const bool data = tid < 256, issuer = tid == 256;
   const int q4 = warp & 3, hf = (warp >> 2) & 1;
   const int v = 32 * q4 + lane;  // value row of a data thread
-  const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
 
   if (issuer) {
     tc::mbar_init(&s.bar_b1[0], 1);
@@ -139,14 +165,16 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
   };
 
   if (data) {
-    // S <- h0 (or 0), transposed: S^T[v][c] = h0[c][v].
+    // S <- the start state (h0, a merged segment start, the identity or 0),
+    // transposed: S^T[v][c] = start[c][v].
     uint32_t r[32];
+    const float* start = start_state();
 #pragma unroll
     for (int cb = 0; cb < 64; cb += 32) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int c = 64 * hf + cb + j;
-        r[j] = __float_as_uint(a.h0 ? a.h0[sidx + (size_t)c * DK + v] : 0.f);
+        r[j] = __float_as_uint(start ? start[(size_t)c * DK + v] : (kind == 3 && c == v ? 1.f : 0.f));
       }
       tc::tmem_st32(tl + kColS + 64 * hf + cb, r);
     }
@@ -158,7 +186,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
     issue_b1(0), ++b1_iss[0];
     if (n > 1) issue_b1(1), ++b1_iss[1];
     issue_b2(0), ++b2_iss;
-    issue_u(0), ++u_iss;
+    if (use_u) issue_u(0), ++u_iss;
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -178,9 +206,11 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       ok = tc::mbar_wait(&s.bar_b1[b], (m >> 1) & 1) && ok;  // gamma of this chunk
       // Columns 64 hf .. 64 hf + 63 in two halves: the tape tile (chunk-major: 512
       // contiguous bytes per warp and 8-channel piece), S0' = S0 rounded to TF32
-      // (the A operand), and diag(gamma) S0 into S.
+      // (the A operand), and diag(gamma) S0 into S.  (Scaling S while [P | O]
+      // runs instead measured slower: the products read their A operand from
+      // tensor memory, and the warps' tensor-memory traffic slows them.)
       const float* gm = s.gam[b] + 64 * hf;
-      __nv_bfloat16* tp = a.tape ? a.tape + state_off(chunk, h, a.HV) : nullptr;
+      __nv_bfloat16* tp = a.tape && outputs ? a.tape + state_off(chunk, h, a.HV) : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int c0 = 64 * hf + 32 * half;
@@ -220,48 +250,53 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       tc::mma_commit(&s.bar_s1);
       ++s1_iss;
     }
-    float dlt[32];  // Delta rows j = 32 hf .., stored to HBM after the second product is issued
     if (data) {
       // While [P | O] runs: the previous chunk's output.
-      if (m > 0) drain_out(m - 1);
+      if (outputs && m > 0) drain_out(m - 1);
       // Delta = u - P (rows j = 32 hf ..), rounded to TF32 in place (the A
       // operand of the second product); the FP32 Delta for the backward.
       ok = tc::mbar_wait(&s.bar_s1, m & 1) && ok;
-      ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
+      if (use_u) ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
       tc::tc_fence_after();
       uint32_t r[32];
       tc::tmem_ld32(tl + colPd(b) + 32 * hf, r);
       tc::tmem_wait_ld();
       const unsigned char* ub = reinterpret_cast<const unsigned char*>(s.U) + q4 * (CH * 128) + (lane & 3) * 4;
+      uint32_t rr[32];
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * hf + jj;
-        dlt[jj] = *reinterpret_cast<const float*>(ub + j * 128 + ((((lane >> 2)) ^ (j & 7)) << 4)) -
-                  __uint_as_float(r[jj]);
-        r[jj] = tf32(dlt[jj]);
+        const float uu = use_u ? *reinterpret_cast<const float*>(ub + j * 128 + ((((lane >> 2)) ^ (j & 7)) << 4)) : 0.f;
+        const float d = uu - __uint_as_float(r[jj]);
+        r[jj] = __float_as_uint(d);
+        rr[jj] = tf32(d);
       }
-      tc::tmem_st32(tl + colPd(b) + 32 * hf, r);
+      tc::tmem_st32(tl + colPd(b) + 32 * hf, r);      // FP32 Delta, written out below
+      tc::tmem_st32(tl + kColDl + 32 * hf, rr);       // TF32 Delta, the A operand of the update
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
     if (!named_sync_and(2, WALKV_THREADS, ok)) break;  // Delta in place; u read
     tc::tc_fence_after();
-    if (data && a.delta) {  // the FP32 Delta for the backward, while the update runs
+    if (data && a.delta && outputs) {  // the FP32 Delta for the backward, while the update runs
+      uint32_t r[32];
+      tc::tmem_ld32(tl + colPd(b) + 32 * hf, r);
+      tc::tmem_wait_ld();
       float* dp = a.delta + tile_off(chunk, h, a.HV) + (size_t)(32 * hf) * DK + v;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) dp[(size_t)jj * DK] = dlt[jj];
+      for (int jj = 0; jj < 32; ++jj) dp[(size_t)jj * DK] = __uint_as_float(r[jj]);
     }
     if (issuer) {
       const bool r2 = tc::mbar_wait(&s.bar_b2, b2_got & 1);
       ok = r2 && ok;
       if (r2) {
         ++b2_got;
-        ++u_got;
+        u_got += use_u;
         tc::tc_fence_after();
         const uint64_t bd = tc::desc_k_sw128(s.B2);
 #pragma unroll
         for (int k = 0; k < CH / 8; ++k)
-          tc::mma_tf32_ta(tm + colD2(b), tm + colPd(b) + 8 * k, tc::kstep32(bd, k, 192), kId2, 1);
+          tc::mma_tf32_ta(tm + colD2(b), tm + kColDl + 8 * k, tc::kstep32(bd, k, 192), kId2, 1);
         tc::mma_commit(&s.bar_s2);
         ++s2_iss;
       }
@@ -270,7 +305,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       // Aqk] with chunk m + 1.
       if (ok && m + 2 < n) issue_b1(m + 2), ++b1_iss[b];
       if (ok && m + 1 < n) {
-        issue_u(m + 1), ++u_iss;
+        if (use_u) issue_u(m + 1), ++u_iss;
         const bool r3 = tc::mbar_wait(&s.bar_s2, m & 1);
         ok = r3 && ok;
         if (r3) issue_b2(m + 1), ++b2_iss;
@@ -292,16 +327,17 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
     if (n > 0) {
       ok = tc::mbar_wait(&s.bar_s2, (n - 1) & 1) && ok;
       tc::tc_fence_after();
-      if (ok) drain_out(n - 1);
+      if (ok && outputs) drain_out(n - 1);
     }
-    if (a.ht && ok) {  // ht[c][v] = S^T[v][c]
+    float* end = end_state();
+    if (end && ok) {  // end[c][v] = S^T[v][c]
       uint32_t r[32];
 #pragma unroll
       for (int cb = 0; cb < 64; cb += 32) {
         tc::tmem_ld32(tl + kColS + 64 * hf + cb, r);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) a.ht[sidx + (size_t)(64 * hf + cb + j) * DK + v] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) end[(size_t)(64 * hf + cb + j) * DK + v] = __uint_as_float(r[j]);
       }
     }
     if (!ok) atomicExch(a.err, 3);
@@ -311,11 +347,11 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
   if (warp == 0) tc::tmem_dealloc(tm, 512);
 }
 
-cudaError_t launch_walk_fwd_v(const WalkArgs& a, int ndocs, cudaStream_t st) {
-  if (ndocs == 0) return cudaSuccess;
+cudaError_t launch_walk_fwd_v(const WalkArgs& a, int nsegs, cudaStream_t st) {
+  if (nsegs == 0) return cudaSuccess;
   const size_t sm = sizeof(WalkVSmem) + 1024;
   cudaFuncSetAttribute(k_walk_fwd_v, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  k_walk_fwd_v<<<ndocs * a.HV, WALKV_THREADS, sm, st>>>(a);
+  k_walk_fwd_v<<<dim3(nsegs * a.HV, a.mode == 1 ? 3 : 1), WALKV_THREADS, sm, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -348,7 +384,7 @@ cudaError_t launch_walk_fwd_v(const WalkArgs& a, int ndocs, cudaStream_t st) {
 // prefetches its operands one step ahead.
 //
 // Tensor-memory columns: dDelta 0..63, dS 64..191, dS' 192..319, (scale dO)'
-// for even and odd steps 320..383 and 384..447.
+// for even and odd steps 320..383 and 384..447, -dDelta' (TF32) 448..511.
 // ---------------------------------------------------------------------------
 struct WalkBvSmem {
   // Operand stage (K-major, 128-byte swizzle):
@@ -361,10 +397,11 @@ struct WalkBvSmem {
   float SQ[CH * DK];         // Q Gamma [i][c]: 4 column blocks of 64 rows
   float SW[CH * DK];         // w [j][c]: 4 column blocks of 64 rows
   float gam[DK];             // gamma, with the Kd^T group
+  float gamc[DK];            // this chunk's gamma, copied before the Kd^T group is refilled
   uint64_t bar_k, bar_a, bar_w, bar_ab, bar_c;
   uint32_t tmem;
 };
-constexpr uint32_t kBColD = 0, kBColS = 64, kBColSp = 192;
+constexpr uint32_t kBColD = 0, kBColS = 64, kBColSp = 192, kBColDn = 448;
 __device__ __forceinline__ uint32_t colDO(int b) { return b ? 384u : 320u; }
 constexpr uint32_t WALKB_K_BYTES = DK * CH * 4 + DK * 4, WALKB_A_BYTES = (CH * CH + CH * DK) * 4,
                    WALKB_W_BYTES = CH * DK * 4;
@@ -401,16 +438,37 @@ __device__ __forceinline__ void transpose_group(const unsigned char* src, int Rs
 __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_constant__ WalkBwdArgs a) {
   extern __shared__ unsigned char smraw[];
   WalkBvSmem& s = *reinterpret_cast<WalkBvSmem*>(tc::align1024(smraw));
-  const int rank = a.rank_base + blockIdx.x / a.HV;  // all heads of the longest document first
+  const int seg = a.seg_base + blockIdx.x / a.HV;  // all heads of the longest document's segments first
   const int h = blockIdx.x % a.HV;
-  const int doc = a.order[rank];
-  const DocDesc dd = a.docs[doc];
+  const SegDesc dd = a.segs[seg];
   const int n = dd.nchunks;
+  // What this CTA walks: its segment's full adjoint walk with the outputs
+  // (mode 0); in the summary launch (mode 1), by blockIdx.y: 0 the last
+  // segment of a split document from dht, giving the end adjoint of the one
+  // before; 1 a middle segment from a zero end adjoint (its start adjoint).
+  int kind = 0;
+  if (a.mode == 1) {
+    kind = 1 + (int)blockIdx.y;
+    const bool on = blockIdx.y == 0 ? (dd.idx == dd.nseg - 1 && dd.nseg > 1) : (dd.idx >= 1 && dd.idx <= dd.nseg - 2);
+    if (!on) return;
+  }
+  const bool outputs = kind == 0;
+  // Start (end-of-segment) and end (start-of-segment) adjoints: dht / dh0 of the
+  // document, or per-segment buffers [NSEG][HV][128][128].
+  auto start_adj = [&]() -> const float* {
+    const size_t sidx = ((size_t)dd.doc * a.HV + h) * DK * DK, gidx = ((size_t)seg * a.HV + h) * DK * DK;
+    return (kind == 0 && dd.idx < dd.nseg - 1) ? a.dsend + gidx : (kind <= 1 && a.dht ? a.dht + sidx : nullptr);
+  };
+  auto end_adj = [&]() -> float* {
+    const size_t sidx = ((size_t)dd.doc * a.HV + h) * DK * DK, gidx = ((size_t)seg * a.HV + h) * DK * DK;
+    return kind == 0   ? (dd.idx == 0 && a.dh0 ? a.dh0 + sidx : nullptr)
+           : kind == 1 ? a.dsend + gidx - (size_t)a.HV * DK * DK
+                       : a.dsbias + gidx;
+  };
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   const bool data = tid < 256, issuer = tid == 256;
   const int q4 = warp & 3, hf = (warp >> 2) & 1;
   const int v = 32 * q4 + lane;
-  const size_t sidx = ((size_t)doc * a.HV + h) * DK * DK;
   unsigned char* const BA = reinterpret_cast<unsigned char*>(s.BA);
   unsigned char* const BK = reinterpret_cast<unsigned char*>(s.BK);
   unsigned char* const BW = reinterpret_cast<unsigned char*>(s.BW);
@@ -474,14 +532,16 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
 
   uint16_t don[32];  // dO of the next step's chunk, loaded a step ahead
   if (data) {
-    // dS <- dht (or 0), transposed: dS^T[v][c] = dht[c][v].
+    // dS <- the end adjoint (dht, a merged segment end adjoint or 0),
+    // transposed: dS^T[v][c] = start[c][v].
     uint32_t r[32];
+    const float* start = start_adj();
 #pragma unroll
     for (int cb = 0; cb < 64; cb += 32) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int c = 64 * hf + cb + j;
-        r[j] = __float_as_uint(a.dht ? a.dht[sidx + (size_t)c * DK + v] : 0.f);
+        r[j] = __float_as_uint(start ? start[(size_t)c * DK + v] : 0.f);
       }
       tc::tmem_st32(tl + kBColS + 64 * hf + cb, r);
     }
@@ -509,7 +569,6 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
     const int b = st & 1;
     const int m = n - 1 - st;
     const int chunk = dd.chunk0 + m;
-    float ddl[32];  // dDelta rows j = 32 hf .., stored to HBM after the last product is issued
     if (data) {
       if (st > 0) {
         ok = tc::mbar_wait(&s.bar_c, (st - 1) & 1) && ok;  // the adjoint of this chunk's end state
@@ -518,11 +577,10 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       ok = tc::mbar_wait(&s.bar_k, st & 1) && ok;  // Kd^T and gamma of this chunk
       // Kd [j][c] from Kd^T [c][j]: 16 groups.
       for (int g = warp; g < 16; g += 8) transpose_group(SK, DK, 16 * (g >> 1), 32 * (g & 1), BK, CH, 0);
+      if (tid < DK) s.gamc[tid] = s.gam[tid];
       // Columns 64 hf .. 64 hf + 63 of the adjoint in two halves: the dS tape
-      // (chunk-major like the state tape), dS' (TF32, the A operand) and
-      // diag(gamma) dS into place.
-      const float* gm = s.gam + 64 * hf;
-      __nv_bfloat16* tp = a.dstape + state_off(chunk, h, a.HV);
+      // (chunk-major like the state tape) and dS' (TF32, the A operand).
+      __nv_bfloat16* tp = outputs ? a.dstape + state_off(chunk, h, a.HV) : nullptr;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int c0 = 64 * hf + 32 * half;
@@ -530,7 +588,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
         tc::tmem_ld32(tl + kBColS + c0, ds);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 4 && tp; ++q) {
           __nv_bfloat162 p[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
@@ -540,15 +598,12 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = tf32(__uint_as_float(ds[j]));
         tc::tmem_st32(tl + kBColSp + c0, r);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(ds[j]) * gm[32 * half + j]);
-        tc::tmem_st32(tl + kBColS + c0, r);
       }
       tc::fence_proxy_async();
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
-    if (!named_sync_and(1, WALKV_THREADS, ok)) break;  // Kd in place; dS', diag(gamma) dS in TMEM
+    if (!named_sync_and(1, WALKV_THREADS, ok)) break;  // Kd in place; dS' in TMEM
     tc::tc_fence_after();
     if (issuer) {
       ++k_got;
@@ -559,6 +614,18 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       if (st + 1 < n) issue_k(m - 1), ++k_iss;  // Kd^T and gamma were read before the barrier
     }
     if (data) {
+      {  // diag(gamma) dS into place (only the second product accumulates into dS)
+        const float* gm = s.gamc + 64 * hf;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tc::tmem_ld32(tl + kBColS + 64 * hf + 32 * half, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gm[32 * half + j]);
+          tc::tmem_st32(tl + kBColS + 64 * hf + 32 * half, r);
+        }
+      }
       ok = tc::mbar_wait(&s.bar_a, st & 1) && ok;  // Aqk, Q Gamma of this chunk
       // Aqk^T [j][i] (8 groups) and Qp^T [c][i] (16 groups) into [Aqk^T ; Qp^T].
       for (int g = warp; g < 24; g += 8) {
@@ -571,7 +638,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
-    if (!named_sync_and(3, WALKV_THREADS, ok)) break;  // [Aqk^T ; Qp^T] in place
+    if (!named_sync_and(3, WALKV_THREADS, ok)) break;  // [Aqk^T ; Qp^T] in place, diag(gamma) dS in TMEM
     tc::tc_fence_after();
     if (issuer) {
       ++a_got;
@@ -593,27 +660,27 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       tc::tmem_ld32(tl + kBColD + 32 * hf, r);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        ddl[j] = __uint_as_float(r[j]);
-        r[j] = tf32(-ddl[j]);
-      }
-      tc::tmem_st32(tl + kBColD + 32 * hf, r);
+      for (int j = 0; j < 32; ++j) r[j] = tf32(-__uint_as_float(r[j]));
+      tc::tmem_st32(tl + kBColDn + 32 * hf, r);  // -dDelta' (the FP32 dDelta stays for the store below)
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
     if (!named_sync_and(2, WALKV_THREADS, ok)) break;  // -dDelta' in TMEM, w^T in place
     tc::tc_fence_after();
-    if (data) {  // the FP32 dDelta for the gradient kernels, while the last product runs
+    if (data && outputs) {  // the FP32 dDelta for the gradient kernels, while the last product runs
+      uint32_t r[32];
+      tc::tmem_ld32(tl + kBColD + 32 * hf, r);
+      tc::tmem_wait_ld();
       float* dp = a.ddelta + tf_off(chunk, h, a.HV) + (size_t)(32 * hf) * LDF + v;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) dp[(size_t)j * LDF] = ddl[j];
+      for (int j = 0; j < 32; ++j) dp[(size_t)j * LDF] = __uint_as_float(r[j]);
     }
     if (issuer) {
       ++w_got;
       const uint64_t bw = tc::desc_k_sw128(s.BW);
 #pragma unroll
       for (int k = 0; k < CH / 8; ++k)
-        tc::mma_tf32_ta(tm + kBColS, tm + kBColD + 8 * k, tc::kstep32(bw, k, DK), kIdC, 1);
+        tc::mma_tf32_ta(tm + kBColS, tm + kBColDn + 8 * k, tc::kstep32(bw, k, DK), kIdC, 1);
       tc::mma_commit(&s.bar_c);
       ++c_iss;
       if (st + 1 < n) issue_w(m - 1), ++w_iss;
@@ -634,14 +701,15 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       ok = tc::mbar_wait(&s.bar_c, (n - 1) & 1) && ok;
       tc::tc_fence_after();
     }
-    if (a.dh0 && ok) {  // dh0[c][v] = dS^T[v][c]
+    float* end = end_adj();
+    if (end && ok) {  // end[c][v] = dS^T[v][c]
       uint32_t r[32];
 #pragma unroll
       for (int cb = 0; cb < 64; cb += 32) {
         tc::tmem_ld32(tl + kBColS + 64 * hf + cb, r);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) a.dh0[sidx + (size_t)(64 * hf + cb + j) * DK + v] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) end[(size_t)(64 * hf + cb + j) * DK + v] = __uint_as_float(r[j]);
       }
     }
     if (!ok) atomicExch(a.err, 4);
@@ -651,11 +719,89 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
   if (warp == 0) tc::tmem_dealloc(tm, 512);
 }
 
-cudaError_t launch_walk_bwd_v(const WalkBwdArgs& a, int ndocs, cudaStream_t st) {
-  if (ndocs == 0) return cudaSuccess;
+cudaError_t launch_walk_bwd_v(const WalkBwdArgs& a, int nsegs, cudaStream_t st) {
+  if (nsegs == 0) return cudaSuccess;
   const size_t sm = sizeof(WalkBvSmem) + 1024;
   cudaFuncSetAttribute(k_walk_bwd_v, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  k_walk_bwd_v<<<ndocs * a.HV, WALKV_THREADS, sm, st>>>(a);
+  k_walk_bwd_v<<<dim3(nsegs * a.HV, a.mode == 1 ? 2 : 1), WALKV_THREADS, sm, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Merges of the segment states of a split document (one CTA per (segment,
+// head, 16-column slice of the state); only a document's first segment with
+// at least three segments works; 256 threads, thread (c, half) computes
+// channel c of 8 columns).  Segment s's walk maps its start state to
+//   S_end = M_s S_start + B_s       (M_s: the end state from the identity
+//                                    without u; B_s: from a zero state),
+// so the adjoints map back as  dS_start = M_s^T dS_end + dB_s.  FP32 on the
+// CUDA cores, each sum in a fixed order.
+//   forward:  S_start[s+1] = M_s S_start[s] + B_s,   s = 1 .. nseg-2
+//             (S_start[1] from the first segment's summary walk)
+//   backward: dS_end[s-1] = M_s^T dS_end[s] + dB_s,  s = nseg-2 .. 1
+//             (dS_end[nseg-2] from the last segment's summary walk)
+// ---------------------------------------------------------------------------
+constexpr int MERGE_LDM = DK + 1;
+template <bool BWD>
+__global__ void __launch_bounds__(256) k_merge(const MergeArgs a) {
+  extern __shared__ float msm[];
+  float* Ms = msm;                   // M_s [c][c'], padded rows
+  float* Ss = msm + DK * MERGE_LDM;  // the state slice [c][16]
+  const int seg = a.seg_base + blockIdx.x / (a.HV * 8);
+  const int h = (blockIdx.x / 8) % a.HV, vs = (blockIdx.x % 8) * 16;
+  const SegDesc sd = a.segs[seg];
+  if (sd.idx != 0 || sd.nseg < 3) return;
+  const int tid = threadIdx.x, c = tid >> 1, v0 = 8 * (tid & 1);
+  auto at = [&](int g) { return ((size_t)g * a.HV + h) * DK * DK; };
+  const int s_first = BWD ? sd.nseg - 2 : 1, s_last = BWD ? 1 : sd.nseg - 2;
+  const int step = BWD ? -1 : 1;
+  // The first input state slice.
+  {
+    const float* src = a.state + at(sd.first + s_first);
+    for (int e = tid; e < DK * 16; e += 256) Ss[e] = src[(size_t)(e >> 4) * DK + vs + (e & 15)];
+  }
+  for (int s = s_first;; s += step) {
+    const float* M = a.smap + at(sd.first + s);
+    for (int e = tid; e < DK * DK / 4; e += 256) {
+      const float4 x = reinterpret_cast<const float4*>(M)[e];
+      const int r = e >> 5, k = (e & 31) * 4;
+      Ms[r * MERGE_LDM + k] = x.x;
+      Ms[r * MERGE_LDM + k + 1] = x.y;
+      Ms[r * MERGE_LDM + k + 2] = x.z;
+      Ms[r * MERGE_LDM + k + 3] = x.w;
+    }
+    __syncthreads();
+    const float* bias = a.bias + at(sd.first + s);
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = bias[(size_t)c * DK + vs + v0 + j];
+    for (int k = 0; k < DK; ++k) {
+      const float m = BWD ? Ms[k * MERGE_LDM + c] : Ms[c * MERGE_LDM + k];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(m, Ss[k * 16 + v0 + j], acc[j]);
+    }
+    __syncthreads();
+    float* dst = a.state + at(sd.first + s + step);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      dst[(size_t)c * DK + vs + v0 + j] = acc[j];
+      Ss[c * 16 + v0 + j] = acc[j];
+    }
+    if (s == s_last) break;
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_merge(const MergeArgs& a, int nsegs, bool backward, cudaStream_t st) {
+  if (nsegs == 0) return cudaSuccess;
+  const size_t sm = (DK * MERGE_LDM + DK * 16) * sizeof(float);
+  if (backward) {
+    cudaFuncSetAttribute(k_merge<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    k_merge<true><<<nsegs * a.HV * 8, 256, sm, st>>>(a);
+  } else {
+    cudaFuncSetAttribute(k_merge<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    k_merge<false><<<nsegs * a.HV * 8, 256, sm, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

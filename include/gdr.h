@@ -223,6 +223,20 @@ gdr_status gdr_profile_report(char* buf, size_t buf_bytes);
 uint64_t gdr_launch_count(void);
 int gdr_set_serial(int on);
 
+/* gdr_set_segment_chunks(chunks): the state walks split a long document into
+ * segments walked in parallel (summary walks give each segment's affine map
+ * of its start state, a merge chains the segments' start states, then every
+ * segment's walk runs from its own start state; flashinfer PR #7723,
+ * "perf(cake_gdn): prefetch offset adjoint walk, default LPT segment plan",
+ * segment plan).  By default (chunks = 0) a segment has about
+ * max(64, total chunks x heads / SM count) chunks, and a pack whose longest
+ * document has at most twice that is not split.  chunks > 0 forces segments
+ * of about that many chunks (tests and tuning).  Process-wide, read by every
+ * *_workspace_bytes, forward and backward call; the saved-buffer stamp
+ * records it, so a backward planned with another setting than its forward
+ * returns GDR_STALE_WORKSPACE.  Returns the previous setting. */
+int gdr_set_segment_chunks(int chunks);
+
 #ifdef __cplusplus
 }
 #endif

@@ -326,3 +326,74 @@ def test_graph_capture_of_grouped_fwd_bwd_replays_bitwise():
     assert torch.equal(cap[0], eager[0]) and torch.equal(cap[1], eager[1])
     for name in ("dq", "dk", "dv", "dg", "dbeta"):
         assert torch.equal(cap[2][name], eager[2][name]), name
+
+
+# ---------------------------------------------------------------------------
+# Segment-parallel walks: documents split into segments walked in parallel
+# (summary walks, a merge of the segment start states, then every segment's
+# walk).  Forced to short segments so that small cases cover one, two (no
+# merge) and many segments per document.
+# ---------------------------------------------------------------------------
+@pytest.fixture
+def segments():
+    import gated_delta_rule_varlen_gb300 as gdr
+
+    def force(chunks):
+        gdr.gdr_set_segment_chunks(chunks)
+
+    yield force
+    gdr.gdr_set_segment_chunks(0)
+
+
+def test_kda_segments_mild_gates_long_document(segments):
+    # 64 chunks in segments of 8: 8 segments, 6 merged; mild gates keep the state alive across
+    # all of them, so a wrong segment map or start state shows in out, ht and every gradient.
+    segments(8)
+    _check("kda", [4096], 1, 1, seed=4, glow=-0.05, h0=True, dht=True)
+
+
+def test_kda_segments_zero_gate(segments):
+    segments(3)
+    _check("kda", [1000], 1, 1, seed=6, glow=0.0, ghigh=0.0, h0=True, dht=True)
+
+
+def test_gdn_segments_grouped_mild_gates(segments):
+    segments(5)
+    _check("gdn", [4096, 700], 1, 3, seed=5, glow=-0.05, h0=True, dht=True)
+
+
+def test_kda_segments_ragged_pack(segments):
+    # Segments of 5 chunks: documents of 1 (16 chunks: 4 segments), 2 (10 chunks, no merge),
+    # 1 segment (5 chunks and 1 token), an empty document, and a long one (13 segments).
+    segments(5)
+    _check("kda", [1000, 640, 300, 1, 0, 4096], 2, 2, seed=19, glow=-0.2, h0=True, dht=True)
+
+
+def test_segments_packed_equals_per_document_bitwise(segments):
+    segments(4)
+    lengths = [1500, 64, 700]
+    x, cu, h0, dht = _case("kda", lengths, 2, 2, seed=20, h0=True, dht=True, glow=-0.3)
+    whole = run_gpu("kda", x, cu, h0=h0, dht=dht, want_dh0=True)
+    for n in range(len(lengths)):
+        s, e = cu[n], cu[n + 1]
+        xs = {k: v[s:e] for k, v in x.items()}
+        one = run_gpu("kda", xs, [0, e - s], h0=h0[n:n + 1], dht=dht[n:n + 1], want_dh0=True)
+        for name in ("out", "dq", "dk", "dv", "dg", "dbeta"):
+            assert torch.equal(whole[name][s:e], one[name]), name
+        assert torch.equal(whole["ht"][n], one["ht"][0])
+        assert torch.equal(whole["dh0"][n], one["dh0"][0])
+
+
+def test_segments_ckpt_matches_plain(segments):
+    import gated_delta_rule_varlen_gb300 as gdr
+    segments(6)
+    x, cu, _, _ = _case("kda", [3000, 500], 2, 2, seed=12)
+    xd = {k: v.cuda() for k, v in x.items()}
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    a = run_gpu("kda", x, cu)
+    o1, _, _ = gdr.kda_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE, save_for_bwd=False)
+    o2, _, saved = gdr.kda_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE)
+    gr = gdr.kda_bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE, xd["dout"], saved)
+    assert torch.equal(o1, a["out"]) and torch.equal(o2, a["out"])
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(gr[name], a[name]), name
