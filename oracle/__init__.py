@@ -110,17 +110,52 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def run(q, k, v, g, beta, cu_seqlens, scale, h0=None, dout=None, dht=None, threads=0):
+# In-kernel q/k L2 normalization (the pages' ``use_qk_l2norm_in_kernel``,
+# flashinfer PR #8638 "perf(cake_gdn_kcp): ... graph-replay checkpoint
+# recompute hands its tapes to the backward", workload description): each
+# (token, Q/K head) vector x of q and of k enters the recurrence as
+#     n = x * r,   r = (sum_c x_c^2 + L2NORM_EPS)^(-1/2).
+# The pages give the flag but not the formula; this reading (a reciprocal
+# square root with a small additive epsilon, so that a zero vector stays
+# zero) is recorded with the others.  Its adjoint: with dn the gradient of
+# the normalized vector,
+#     dx = r * (dn - n * (n . dn)).
+L2NORM_EPS = 1e-6
+
+
+def l2norm(x):
+    """(n, r) for x [T, H, D]: the normalized vectors and their scales r [T, H]."""
+    x = np.asarray(x, dtype=np.float64)
+    r = 1.0 / np.sqrt((x * x).sum(-1) + L2NORM_EPS)
+    return x * r[..., None], r
+
+
+def l2norm_backward(n, r, dn):
+    """dx from the normalized vectors n, their scales r and the gradient dn."""
+    return r[..., None] * (dn - n * (n * dn).sum(-1, keepdims=True))
+
+
+def run(q, k, v, g, beta, cu_seqlens, scale, h0=None, dout=None, dht=None, threads=0, qk_l2norm=False):
     """Run the oracle.
 
     Shapes: q, k [T, Hqk, D]; v [T, HV, D]; g [T, HV, D] (KDA, per-channel gate)
     or [T, HV] (GDN, scalar gate); beta [T, HV]; cu_seqlens [N+1] int;
     h0 / dht [N, HV, D, D] or None; dout [T, HV, D] or None (forward only).
+    qk_l2norm: normalize q and k first (``l2norm``); dq, dk are then the
+    gradients with respect to the raw q, k.
 
     Returns a dict with ``out`` and ``ht`` and, when ``dout`` is given,
     ``dq dk dv dg dbeta`` and ``dh0`` (the latter only when ``h0`` is given).
     All arrays float64.
     """
+    if qk_l2norm:
+        qn, rq = l2norm(q)
+        kn, rk = l2norm(k)
+        res = run(qn, kn, v, g, beta, cu_seqlens, scale, h0=h0, dout=dout, dht=dht, threads=threads)
+        if dout is not None:
+            res["dq"] = l2norm_backward(qn, rq, res["dq"])
+            res["dk"] = l2norm_backward(kn, rk, res["dk"])
+        return res
     lib = _load()
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
     h0, dout, dht = _f64(h0), _f64(dout), _f64(dht)

@@ -39,16 +39,16 @@ def _rand_problem(rng, lengths, Hqk, HV, D, per_channel, glow=-1.0, with_h0=True
     return dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, dout=dout, dht=dht, cu=cu)
 
 
-def _loss(P, scale, **over):
+def _loss(P, scale, l2=False, **over):
     x = dict(P)
     x.update(over)
-    r = oracle.run(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], scale, h0=x["h0"])
+    r = oracle.run(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu"], scale, h0=x["h0"], qk_l2norm=l2)
     return float((r["out"] * x["dout"]).sum() + (r["ht"] * x["dht"]).sum())
 
 
-def _check_fd(P, scale, eps=1e-6, tol=1e-6):
+def _check_fd(P, scale, eps=1e-6, tol=1e-6, l2=False):
     r = oracle.run(P["q"], P["k"], P["v"], P["g"], P["beta"], P["cu"], scale,
-                   h0=P["h0"], dout=P["dout"], dht=P["dht"])
+                   h0=P["h0"], dout=P["dout"], dht=P["dht"], qk_l2norm=l2)
     names = [("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"), ("h0", "dh0")]
     for name, gname in names:
         x = P[name]
@@ -58,7 +58,7 @@ def _check_fd(P, scale, eps=1e-6, tol=1e-6):
             idx = it.multi_index
             xp = x.copy(); xp[idx] += eps
             xm = x.copy(); xm[idx] -= eps
-            fd[idx] = (_loss(P, scale, **{name: xp}) - _loss(P, scale, **{name: xm})) / (2 * eps)
+            fd[idx] = (_loss(P, scale, l2, **{name: xp}) - _loss(P, scale, l2, **{name: xm})) / (2 * eps)
         an = r[gname]
         err = np.abs(an - fd).max() / max(np.abs(fd).max(), 1e-12)
         assert err < tol, f"{gname}: finite-difference mismatch {err:.3e}"
@@ -276,3 +276,57 @@ def test_oracle_regression_fixture():
                        h0=x["h0"], dout=x["dout"])
         for k, v in case["outputs"].items():
             np.testing.assert_allclose(r[k], np.array(v), rtol=1e-12, atol=1e-14, err_msg=f"{name}:{k}")
+
+
+# In-kernel q/k L2 normalization (qk_l2norm): the recurrence runs on
+# n = x (sum x^2 + eps)^(-1/2) for each (token, Q/K head) vector of q and k.
+def _raw_problem(rng, lengths, Hqk, HV, D, per_channel, glow=-1.0):
+    P = _rand_problem(rng, lengths, Hqk, HV, D, per_channel, glow=glow)
+    # Raw, unnormalized q and k with norms far from 1.
+    P["q"] = rng.standard_normal(P["q"].shape) * rng.uniform(0.2, 3.0, P["q"].shape[:2] + (1,))
+    P["k"] = rng.standard_normal(P["k"].shape) * rng.uniform(0.2, 3.0, P["k"].shape[:2] + (1,))
+    return P
+
+
+def test_fd_gradients_with_qk_l2norm_kda():
+    rng = np.random.default_rng(30)
+    _check_fd(_raw_problem(rng, [5, 3], Hqk=2, HV=2, D=4, per_channel=True), scale=0.7, l2=True)
+
+
+def test_fd_gradients_with_qk_l2norm_gdn_grouped():
+    rng = np.random.default_rng(31)
+    _check_fd(_raw_problem(rng, [4, 3], Hqk=1, HV=3, D=4, per_channel=False), scale=0.6, l2=True)
+
+
+def test_qk_l2norm_is_scale_invariant_and_its_gradients_are_orthogonal():
+    # Scaling a q or k vector by any positive factor leaves every output unchanged (up to
+    # the epsilon), so dq . q = 0 and dk . k = 0 for every (token, head).
+    rng = np.random.default_rng(32)
+    P = _raw_problem(rng, [9, 6], Hqk=2, HV=4, D=8, per_channel=False)
+    args = (P["v"], P["g"], P["beta"], P["cu"], 0.5)
+    r = oracle.run(P["q"], P["k"], *args, h0=P["h0"], dout=P["dout"], dht=P["dht"], qk_l2norm=True)
+    lam = rng.uniform(0.1, 10.0, P["q"].shape[:2] + (1,))
+    mu = rng.uniform(0.1, 10.0, P["k"].shape[:2] + (1,))
+    r2 = oracle.run(P["q"] * lam, P["k"] * mu, *args, h0=P["h0"], qk_l2norm=True)
+    np.testing.assert_allclose(r2["out"], r["out"], rtol=1e-4, atol=1e-6)
+    # (exactly zero without the epsilon; with it x . dx = r (x . dn) eps / (|x|^2 + eps))
+    np.testing.assert_allclose((r["dq"] * P["q"]).sum(-1), 0.0, atol=1e-5)
+    np.testing.assert_allclose((r["dk"] * P["k"]).sum(-1), 0.0, atol=1e-5)
+
+
+def test_qk_l2norm_on_unit_vectors():
+    # With unit q and k (and the epsilon's effect below 1e-6), the flag changes nothing in
+    # the forward, and dq, dk become the flag-off gradients with their components along q,
+    # k removed (the normalization's Jacobian at a unit vector is I - x x^T).
+    rng = np.random.default_rng(33)
+    P = _rand_problem(rng, [7, 5], Hqk=2, HV=2, D=8, per_channel=True)
+    P["q"] /= np.linalg.norm(P["q"], axis=-1, keepdims=True)
+    args = (P["q"], P["k"], P["v"], P["g"], P["beta"], P["cu"], 0.8)
+    off = oracle.run(*args, h0=P["h0"], dout=P["dout"], dht=P["dht"])
+    on = oracle.run(*args, h0=P["h0"], dout=P["dout"], dht=P["dht"], qk_l2norm=True)
+    for name in ("out", "ht", "dv", "dg", "dbeta", "dh0"):
+        np.testing.assert_allclose(on[name], off[name], rtol=2e-6, atol=2e-6)
+    for x, gname in (("q", "dq"), ("k", "dk")):
+        u = P[x]
+        proj = off[gname] - u * (u * off[gname]).sum(-1, keepdims=True)
+        np.testing.assert_allclose(on[gname], proj, rtol=2e-6, atol=2e-6)
