@@ -73,16 +73,17 @@ _SIGS = {
     "gdr_launch_count": ([], ctypes.c_uint64),
     "gdr_set_serial": ([ctypes.c_int], ctypes.c_int),
     "gdr_set_segment_chunks": ([ctypes.c_int], ctypes.c_int),
-    "kda_workspace_bytes": ([I64, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
-    "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, PSZ, PSZ], ctypes.c_int),
-    "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P], ctypes.c_int),
-    "kda_bwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P, SZ, P, P, P, P, P, P, P, SZ, P],
+    "kda_workspace_bytes": ([I64, I32, I32, PI32, ctypes.c_int, PSZ, PSZ], ctypes.c_int),
+    "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, ctypes.c_int, PSZ, PSZ], ctypes.c_int),
+    "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, ctypes.c_int, P, P, P, P, SZ, ctypes.c_int, P, SZ, P],
                 ctypes.c_int),
+    "kda_bwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, ctypes.c_int, P, P, P, P, SZ, P, P, P, P, P, P, P, SZ,
+                 P], ctypes.c_int),
     "kda_fwd_noalloc": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, P, P, P, P], ctypes.c_int),
-    "gdn_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, I32, F32, P, P, P, P, SZ, ctypes.c_int, P, SZ, P],
-                ctypes.c_int),
-    "gdn_bwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, I32, F32, P, P, P, P, SZ, P, P, P, P, P, P, P, SZ, P],
-                ctypes.c_int),
+    "gdn_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, I32, F32, ctypes.c_int, P, P, P, P, SZ, ctypes.c_int, P,
+                 SZ, P], ctypes.c_int),
+    "gdn_bwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, I32, F32, ctypes.c_int, P, P, P, P, SZ, P, P, P, P, P, P,
+                 P, SZ, P], ctypes.c_int),
 }
 
 
@@ -143,20 +144,20 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def kda_workspace_bytes(T: int, H: int, cu_seqlens_host):
+def kda_workspace_bytes(T: int, H: int, cu_seqlens_host, qk_l2norm: bool = False):
     """(saved_bytes, scratch_bytes) for a KDA problem; host only."""
     arr, p = _cu_host(cu_seqlens_host)
     sb, cb = SZ(0), SZ(0)
-    _check(load().kda_workspace_bytes(T, H, arr.shape[0] - 1, p, ctypes.byref(sb), ctypes.byref(cb)),
-           "kda_workspace_bytes")
+    _check(load().kda_workspace_bytes(T, H, arr.shape[0] - 1, p, int(bool(qk_l2norm)), ctypes.byref(sb),
+                                      ctypes.byref(cb)), "kda_workspace_bytes")
     return sb.value, cb.value
 
 
-def gdn_workspace_bytes(T: int, Hqk: int, HV: int, cu_seqlens_host):
+def gdn_workspace_bytes(T: int, Hqk: int, HV: int, cu_seqlens_host, qk_l2norm: bool = False):
     arr, p = _cu_host(cu_seqlens_host)
     sb, cb = SZ(0), SZ(0)
-    _check(load().gdn_workspace_bytes(T, Hqk, HV, arr.shape[0] - 1, p, ctypes.byref(sb), ctypes.byref(cb)),
-           "gdn_workspace_bytes")
+    _check(load().gdn_workspace_bytes(T, Hqk, HV, arr.shape[0] - 1, p, int(bool(qk_l2norm)), ctypes.byref(sb),
+                                      ctypes.byref(cb)), "gdn_workspace_bytes")
     return sb.value, cb.value
 
 
@@ -184,7 +185,7 @@ def _check_shapes(variant, q, k, v, g, beta, dout=None):
 
 
 def _fwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out, ht, want_ht, saved,
-         save_for_bwd, scratch, stream):
+         save_for_bwd, scratch, stream, qk_l2norm=False):
     import torch
     _check_shapes(variant, q, k, v, g, beta)
     T, Hqk, D = q.shape
@@ -192,9 +193,9 @@ def _fwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out,
     arr, cup = _cu_host(cu_seqlens_host)
     N = arr.shape[0] - 1
     if variant == "kda":
-        sb, cb = kda_workspace_bytes(T, HV, arr)
+        sb, cb = kda_workspace_bytes(T, HV, arr, qk_l2norm)
     else:
-        sb, cb = gdn_workspace_bytes(T, Hqk, HV, arr)
+        sb, cb = gdn_workspace_bytes(T, Hqk, HV, arr, qk_l2norm)
     dev = q.device
     if out is None:
         out = torch.empty((T, HV, D), dtype=torch.bfloat16, device=dev)
@@ -207,7 +208,7 @@ def _fwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out,
     lib = load()
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), cup, N, T]
     args += [HV] if variant == "kda" else [Hqk, HV]
-    args += [float(scale), _ptr(h0), _ptr(out), _ptr(ht), _ptr(saved),
+    args += [float(scale), int(bool(qk_l2norm)), _ptr(h0), _ptr(out), _ptr(ht), _ptr(saved),
              0 if saved is None else saved.numel(), int(bool(save_for_bwd)), _ptr(scratch),
              0 if scratch is None else scratch.numel(), _stream(stream)]
     fn = lib.kda_fwd if variant == "kda" else lib.gdn_fwd
@@ -216,7 +217,7 @@ def _fwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out,
 
 
 def _bwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0, scratch,
-         grads, stream):
+         grads, stream, qk_l2norm=False):
     import torch
     _check_shapes(variant, q, k, v, g, beta, dout)
     T, Hqk, D = q.shape
@@ -224,9 +225,9 @@ def _bwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, sa
     arr, cup = _cu_host(cu_seqlens_host)
     N = arr.shape[0] - 1
     if variant == "kda":
-        sb, cb = kda_workspace_bytes(T, HV, arr)
+        sb, cb = kda_workspace_bytes(T, HV, arr, qk_l2norm)
     else:
-        sb, cb = gdn_workspace_bytes(T, Hqk, HV, arr)
+        sb, cb = gdn_workspace_bytes(T, Hqk, HV, arr, qk_l2norm)
     dev = q.device
     grads = dict(grads or {})
     for name, like in (("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta)):
@@ -239,7 +240,7 @@ def _bwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, sa
     lib = load()
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), cup, N, T]
     args += [HV] if variant == "kda" else [Hqk, HV]
-    args += [float(scale), _ptr(h0), _ptr(dout), _ptr(dht), _ptr(saved), saved.numel(),
+    args += [float(scale), int(bool(qk_l2norm)), _ptr(h0), _ptr(dout), _ptr(dht), _ptr(saved), saved.numel(),
              _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dg"]), _ptr(grads["dbeta"]),
              _ptr(grads.get("dh0")), _ptr(scratch), scratch.numel(), _stream(stream)]
     fn = lib.kda_bwd if variant == "kda" else lib.gdn_bwd
@@ -248,33 +249,35 @@ def _bwd(variant, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, sa
 
 
 def kda_fwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0=None, out=None, ht=None, want_ht=True,
-            saved=None, save_for_bwd=True, scratch=None, stream=None):
+            saved=None, save_for_bwd=True, scratch=None, stream=None, qk_l2norm=False):
     """KDA forward.  q, k, v bf16 [T,H,128]; g fp32 [T,H,128]; beta bf16 [T,H];
-    cu_seqlens int32 device [N+1] and its host copy.  Returns (out, ht, saved)."""
+    cu_seqlens int32 device [N+1] and its host copy.  qk_l2norm: normalize q, k
+    per (token, head) vector in the kernels (the backward must be called with
+    the same flag).  Returns (out, ht, saved)."""
     return _fwd("kda", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out, ht, want_ht, saved,
-                save_for_bwd, scratch, stream)
+                save_for_bwd, scratch, stream, qk_l2norm)
 
 
 def kda_bwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0=None, dht=None, want_dh0=False,
-            scratch=None, grads=None, stream=None):
+            scratch=None, grads=None, stream=None, qk_l2norm=False):
     """KDA backward from `saved` (filled by kda_fwd(save_for_bwd=True)).
     Returns a dict with dq, dk, dv, dg, dbeta (and dh0 when want_dh0)."""
     return _bwd("kda", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0,
-                scratch, grads, stream)
+                scratch, grads, stream, qk_l2norm)
 
 
 def gdn_fwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0=None, out=None, ht=None, want_ht=True,
-            saved=None, save_for_bwd=True, scratch=None, stream=None):
+            saved=None, save_for_bwd=True, scratch=None, stream=None, qk_l2norm=False):
     """GDN forward.  q, k bf16 [T,Hqk,128]; v bf16 [T,HV,128]; g, beta fp32
     [T,HV].  Returns (out, ht, saved)."""
     return _fwd("gdn", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, h0, out, ht, want_ht, saved,
-                save_for_bwd, scratch, stream)
+                save_for_bwd, scratch, stream, qk_l2norm)
 
 
 def gdn_bwd(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0=None, dht=None, want_dh0=False,
-            scratch=None, grads=None, stream=None):
+            scratch=None, grads=None, stream=None, qk_l2norm=False):
     return _bwd("gdn", q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, dout, saved, h0, dht, want_dh0,
-                scratch, grads, stream)
+                scratch, grads, stream, qk_l2norm)
 
 
 def gdr_launch_count() -> int:

@@ -223,13 +223,15 @@ struct Layout {
   size_t docs = 0, chunks = 0, order = 0, segs = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, amat = 0,
          tmat = 0, gam = 0, tape = 0, smap = 0, sstart = 0, sbias = 0;
   size_t saved_total = 0;
+  size_t qn = 0, kn = 0, rq = 0, rk = 0;  // in-kernel q/k L2 normalization
   size_t dstape = 0, ddelta = 0, dqs = 0, dw = 0, dkd = 0, dgam = 0, daqk = 0, dqp = 0, dkp = 0, dsend = 0, dsbias = 0;
   size_t bwd_total = 0;
 };
 
 // NSEG: segments of the walks (equal to N when no document is split); the
 // per-segment state buffers are only laid out when some document is.
-Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped, int64_t NSEG) {
+Layout make_layout(int64_t T, int64_t NC, int32_t N, int32_t Hqk, int32_t HV, bool l2, int64_t NSEG) {
+  const bool grouped = HV != Hqk || l2;  // FP32 dq / dk partials reduced (and normalized back) per Q/K head
   Layout L;
   L.NC = NC;
   L.NSEG = NSEG;
@@ -261,6 +263,12 @@ Layout make_layout(int64_t NC, int32_t N, int32_t HV, bool grouped, int64_t NSEG
   L.tmat = take((size_t)NC * HV * CH * LDS * sizeof(float));
   L.gam = take(vec);
   L.tape = take(st);
+  if (l2) {
+    L.qn = take((size_t)T * Hqk * DK * 2);
+    L.kn = take((size_t)T * Hqk * DK * 2);
+    L.rq = take((size_t)T * Hqk * 4);
+    L.rk = take((size_t)T * Hqk * 4);
+  }
   L.saved_total = o;
   o = 0;
   L.dstape = take(st);
@@ -309,6 +317,7 @@ uint64_t hash_cu(const int32_t* cu, int32_t N) {
 struct Stamp {
   int64_t T;
   int32_t N, Hqk, HV, variant, lseg;
+  bool l2;
   uint64_t cu_hash;
 };
 std::mutex g_stamp_mu;
@@ -324,7 +333,7 @@ bool stamp_check(const void* saved, const Stamp& s) {
   if (it == g_stamps.end()) return false;
   const Stamp& r = it->second;
   return r.T == s.T && r.N == s.N && r.Hqk == s.Hqk && r.HV == s.HV && r.variant == s.variant &&
-         r.lseg == s.lseg && r.cu_hash == s.cu_hash;
+         r.lseg == s.lseg && r.l2 == s.l2 && r.cu_hash == s.cu_hash;
 }
 
 gdr_status check_device() {
@@ -583,15 +592,15 @@ const T* at(const void* base, size_t off) {
   return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
 }
 
-gdr_status workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const int32_t* cu, size_t* saved_bytes,
-                           size_t* scratch_bytes) {
+gdr_status workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const int32_t* cu, int l2,
+                           size_t* saved_bytes, size_t* scratch_bytes) {
   if (Hqk <= 0 || HV <= 0 || HV % Hqk != 0) return GDR_INVALID_ARG;
   int64_t NC = 0;
   const gdr_status st = plan_host(T, N, cu, &NC);
   if (st != GDR_OK) return st;
   std::vector<DocGroup> groups = plan_groups(N, cu);
   const int64_t NSEG = assign_segments(groups, N, cu, segment_chunks(N, cu, HV));
-  const Layout L = make_layout(NC, N, HV, HV != Hqk, NSEG);
+  const Layout L = make_layout(T, NC, N, Hqk, HV, l2 != 0, NSEG);
   if (saved_bytes) *saved_bytes = L.saved_total;
   if (scratch_bytes) *scratch_bytes = L.bwd_total;
   return GDR_OK;
@@ -599,7 +608,7 @@ gdr_status workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const 
 
 gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, const float* g, const void* beta,
                     const int32_t* cu, const int32_t* cu_host, int32_t N, int64_t T, int32_t Hqk, int32_t HV,
-                    float scale, const float* h0, void* out, float* ht, void* saved, size_t saved_bytes,
+                    float scale, int l2, const float* h0, void* out, float* ht, void* saved, size_t saved_bytes,
                     int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   if (Hqk <= 0 || HV <= 0 || HV % Hqk != 0) return GDR_INVALID_ARG;
   int64_t NC = 0;
@@ -614,7 +623,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   const int lseg = segment_chunks(N, cu_host, HV);
   std::vector<DocGroup> groups = plan_groups(N, cu_host);
   const int64_t NSEG = assign_segments(groups, N, cu_host, lseg);
-  const Layout L = make_layout(NC, N, HV, HV != Hqk, NSEG);
+  const Layout L = make_layout(T, NC, N, Hqk, HV, l2 != 0, NSEG);
   void* base = saved ? saved : scratch;
   const size_t have = saved ? saved_bytes : scratch_bytes;
   if (!base) return GDR_INVALID_ARG;
@@ -636,6 +645,24 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   PrepArgs pa{};
   pa.q = static_cast<const __nv_bfloat16*>(q);
   pa.k = static_cast<const __nv_bfloat16*>(k);
+  if (l2) {  // the rows' L2 scales (and normalized BF16 copies of q, k, for the backward)
+    L2NormArgs la{};
+    la.q = pa.q;
+    la.k = pa.k;
+    la.qn = at<__nv_bfloat16>(base, L.qn);
+    la.kn = at<__nv_bfloat16>(base, L.kn);
+    la.rq = at<float>(base, L.rq);
+    la.rk = at<float>(base, L.rk);
+    la.rows = T * Hqk;
+    {
+      ProfScope ps("l2norm", stream);
+      if (launch_l2norm(la, stream) != cudaSuccess) return GDR_CUDA_ERROR;
+    }
+    // The prep reads the raw q, k and applies the scales in FP32 (the normalized
+    // BF16 copies are for the backward's gradient kernel).
+    pa.rq = la.rq;
+    pa.rk = la.rk;
+  }
   pa.v = static_cast<const __nv_bfloat16*>(v);
   pa.g = g;
   pa.beta = beta;
@@ -719,13 +746,13 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
     if (!fork.join() && st == GDR_OK) st = GDR_CUDA_ERROR;
   }
   if (st != GDR_OK) return st;
-  if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, lseg, hash_cu(cu_host, N)});
+  if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, lseg, l2 != 0, hash_cu(cu_host, N)});
   return GDR_OK;
 }
 
 gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, const float* g, const void* beta,
                     const int32_t* cu, const int32_t* cu_host, int32_t N, int64_t T, int32_t Hqk, int32_t HV,
-                    float scale, const void* dout, const float* dht, const void* saved, size_t saved_bytes,
+                    float scale, int l2, const void* dout, const float* dht, const void* saved, size_t saved_bytes,
                     void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* scratch,
                     size_t scratch_bytes, cudaStream_t stream) {
   if (Hqk <= 0 || HV <= 0 || HV % Hqk != 0) return GDR_INVALID_ARG;
@@ -742,9 +769,10 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   const int lseg = segment_chunks(N, cu_host, HV);
   std::vector<DocGroup> groups = plan_groups(N, cu_host);
   const int64_t NSEG = assign_segments(groups, N, cu_host, lseg);
-  const Layout L = make_layout(NC, N, HV, HV != Hqk, NSEG);
+  const Layout L = make_layout(T, NC, N, Hqk, HV, l2 != 0, NSEG);
   if (saved_bytes < L.saved_total || scratch_bytes < L.bwd_total) return GDR_WORKSPACE_TOO_SMALL;
-  if (!stamp_check(saved, Stamp{T, N, Hqk, HV, variant, lseg, hash_cu(cu_host, N)})) return GDR_STALE_WORKSPACE;
+  if (!stamp_check(saved, Stamp{T, N, Hqk, HV, variant, lseg, l2 != 0, hash_cu(cu_host, N)}))
+    return GDR_STALE_WORKSPACE;
   st = check_device();
   if (st != GDR_OK) return st;
   const bool vec = variant == 0;
@@ -799,8 +827,11 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   gs.err = wb.err;
 
   GradArgs ga{};
-  ga.q = static_cast<const __nv_bfloat16*>(q);
-  ga.k = static_cast<const __nv_bfloat16*>(k);
+  // With the in-kernel L2 normalization the gradient kernels read the forward's
+  // normalized q, k and produce the gradients of those (dn), which the group
+  // reduction maps back to the raw inputs.
+  ga.q = l2 ? at<__nv_bfloat16>(saved, L.qn) : static_cast<const __nv_bfloat16*>(q);
+  ga.k = l2 ? at<__nv_bfloat16>(saved, L.kn) : static_cast<const __nv_bfloat16*>(k);
   ga.v = static_cast<const __nv_bfloat16*>(v);
   ga.g = g;
   ga.beta = beta;
@@ -827,7 +858,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   ga.dq = static_cast<__nv_bfloat16*>(dq);
   ga.dk = static_cast<__nv_bfloat16*>(dk);
   ga.dv = static_cast<__nv_bfloat16*>(dv);
-  const bool grouped = HV != Hqk;
+  const bool grouped = HV != Hqk || l2;
   ga.dq_part = grouped ? at<float>(scratch, L.dqp) : nullptr;
   ga.dk_part = grouped ? at<float>(scratch, L.dkp) : nullptr;
   ga.dg = dg;
@@ -840,6 +871,10 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   gr.dk_part = ga.dk_part;
   gr.dq = ga.dq;
   gr.dk = ga.dk;
+  gr.q = l2 ? static_cast<const __nv_bfloat16*>(q) : nullptr;
+  gr.k = l2 ? static_cast<const __nv_bfloat16*>(k) : nullptr;
+  gr.rq = l2 ? at<float>(saved, L.rq) : nullptr;
+  gr.rk = l2 ? at<float>(saved, L.rk) : nullptr;
 
   // Document groups (longest documents first, each on a stream of its own):
   // a group's gradient kernels need only its own walk, so the gradients of the
@@ -947,50 +982,50 @@ const char* gdr_status_string(gdr_status s) {
   }
 }
 
-gdr_status kda_workspace_bytes(int64_t T, int32_t H, int32_t N, const int32_t* cu_seqlens_host, size_t* saved_bytes,
-                               size_t* scratch_bytes) {
-  return gdr::workspace_bytes(T, H, H, N, cu_seqlens_host, saved_bytes, scratch_bytes);
+gdr_status kda_workspace_bytes(int64_t T, int32_t H, int32_t N, const int32_t* cu_seqlens_host, int qk_l2norm,
+                               size_t* saved_bytes, size_t* scratch_bytes) {
+  return gdr::workspace_bytes(T, H, H, N, cu_seqlens_host, qk_l2norm, saved_bytes, scratch_bytes);
 }
 
 gdr_status gdn_workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const int32_t* cu_seqlens_host,
-                               size_t* saved_bytes, size_t* scratch_bytes) {
-  return gdr::workspace_bytes(T, Hqk, HV, N, cu_seqlens_host, saved_bytes, scratch_bytes);
+                               int qk_l2norm, size_t* saved_bytes, size_t* scratch_bytes) {
+  return gdr::workspace_bytes(T, Hqk, HV, N, cu_seqlens_host, qk_l2norm, saved_bytes, scratch_bytes);
 }
 
 gdr_status kda_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
-                   float scale, const float* h0, gdr_bf16* out, float* ht, void* saved, size_t saved_bytes,
-                   int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
-  return gdr::fwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, h0, out, ht, saved,
-                       saved_bytes, save_for_bwd, scratch, scratch_bytes, stream);
+                   float scale, int qk_l2norm, const float* h0, gdr_bf16* out, float* ht, void* saved,
+                   size_t saved_bytes, int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  return gdr::fwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, qk_l2norm, h0, out, ht,
+                       saved, saved_bytes, save_for_bwd, scratch, scratch_bytes, stream);
 }
 
 gdr_status kda_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
-                   float scale, const float* h0, const gdr_bf16* dout, const float* dht, const void* saved,
-                   size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg, gdr_bf16* dbeta,
-                   float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+                   float scale, int qk_l2norm, const float* h0, const gdr_bf16* dout, const float* dht,
+                   const void* saved, size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg,
+                   gdr_bf16* dbeta, float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   (void)h0;
-  return gdr::bwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, dout, dht, saved,
-                       saved_bytes, dq, dk, dv, dg, dbeta, dh0, scratch, scratch_bytes, stream);
+  return gdr::bwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, qk_l2norm, dout, dht,
+                       saved, saved_bytes, dq, dk, dv, dg, dbeta, dh0, scratch, scratch_bytes, stream);
 }
 
 gdr_status gdn_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const float* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t Hqk,
-                   int32_t HV, float scale, const float* h0, gdr_bf16* out, float* ht, void* saved,
+                   int32_t HV, float scale, int qk_l2norm, const float* h0, gdr_bf16* out, float* ht, void* saved,
                    size_t saved_bytes, int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
-  return gdr::fwd_impl(1, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, Hqk, HV, scale, h0, out, ht, saved,
-                       saved_bytes, save_for_bwd, scratch, scratch_bytes, stream);
+  return gdr::fwd_impl(1, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, Hqk, HV, scale, qk_l2norm, h0, out, ht,
+                       saved, saved_bytes, save_for_bwd, scratch, scratch_bytes, stream);
 }
 
 gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const float* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t Hqk,
-                   int32_t HV, float scale, const float* h0, const gdr_bf16* dout, const float* dht,
+                   int32_t HV, float scale, int qk_l2norm, const float* h0, const gdr_bf16* dout, const float* dht,
                    const void* saved, size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg,
                    float* dbeta, float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   (void)h0;
-  return gdr::bwd_impl(1, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, Hqk, HV, scale, dout, dht, saved,
-                       saved_bytes, dq, dk, dv, dg, dbeta, dh0, scratch, scratch_bytes, stream);
+  return gdr::bwd_impl(1, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, Hqk, HV, scale, qk_l2norm, dout, dht,
+                       saved, saved_bytes, dq, dk, dv, dg, dbeta, dh0, scratch, scratch_bytes, stream);
 }
 
 gdr_status kda_fwd_noalloc(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g,
@@ -998,15 +1033,15 @@ gdr_status kda_fwd_noalloc(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16*
                            int32_t N, int64_t T, int32_t H, float scale, const float* h0, gdr_bf16* out, float* ht,
                            cudaStream_t stream) {
   size_t need = 0;
-  const gdr_status qs = gdr::workspace_bytes(T, H, H, N, cu_seqlens_host, &need, nullptr);
+  const gdr_status qs = gdr::workspace_bytes(T, H, H, N, cu_seqlens_host, 0, &need, nullptr);
   if (qs != GDR_OK) return qs;
   if (need > gdr::kStaticScratchBytes) return GDR_WORKSPACE_TOO_SMALL;
   if (N == 0) return GDR_OK;
   gdr_status st = GDR_OK;
   void* scratch = gdr::static_scratch_ptr(&st);
   if (!scratch) return st;
-  return gdr::fwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, h0, out, ht, nullptr, 0,
-                       0, scratch, gdr::kStaticScratchBytes, stream);
+  return gdr::fwd_impl(0, q, k, v, g, beta, cu_seqlens, cu_seqlens_host, N, T, H, H, scale, 0, h0, out, ht, nullptr,
+                       0, 0, scratch, gdr::kStaticScratchBytes, stream);
 }
 
 gdr_status gdr_doc_groups(int32_t N, const int32_t* cu_seqlens_host, int32_t* rank_bounds, int64_t* chunk_bounds,

@@ -610,22 +610,44 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
         from_f<BetaT>(((sg.dbeta[0][tid] + sg.dbeta[1][tid]) + (sg.dbeta[2][tid] + sg.dbeta[3][tid])) + sg.dbeta[4][tid]);
 }
 
-// dq / dk of a Q/K head = FP32 sum over its value heads, rounded once.
+// dq / dk of a Q/K head = FP32 sum over its value heads, rounded once.  With
+// the in-kernel q/k L2 normalization the sums are the gradients dn of the
+// normalized vectors n = x r (r = (sum x^2 + eps)^(-1/2), saved by the
+// forward's pre-pass), and the raw gradient is dx = r (dn - n (n . dn)).
+// One warp per token row (lane: channels 4 lane .. 4 lane + 3; the dot
+// products summed by shuffles in a fixed order).
 __global__ void __launch_bounds__(256) k_group_reduce(GroupReduceArgs a) {
   const int chunk = a.chunk_base + blockIdx.x, hq = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int G = a.HV / a.Hqk;
-  for (int e = threadIdx.x; e < cd.len * DK; e += blockDim.x) {
-    const int i = e >> 7, c = e & 127;
-    float sq = 0.f, sk = 0.f;
+  const int warp = threadIdx.x >> 5, lane = lane_id(), c = 4 * lane;
+  for (int i = warp; i < cd.len; i += 8) {
+    float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
     for (int gi = 0; gi < G; ++gi) {
       const size_t off = tile_off(chunk, hq * G + gi, a.HV) + (size_t)i * DK + c;
-      sq += a.dq_part[off];
-      sk += a.dk_part[off];
+      const float4 x = *reinterpret_cast<const float4*>(a.dq_part + off);
+      const float4 y = *reinterpret_cast<const float4*>(a.dk_part + off);
+      sq.x += x.x, sq.y += x.y, sq.z += x.z, sq.w += x.w;
+      sk.x += y.x, sk.y += y.y, sk.z += y.z, sk.w += y.w;
     }
-    const size_t o = ((size_t)(cd.tok0 + i) * a.Hqk + hq) * DK + c;
-    a.dq[o] = __float2bfloat16_rn(sq);
-    a.dk[o] = __float2bfloat16_rn(sk);
+    const size_t row = (size_t)(cd.tok0 + i) * a.Hqk + hq, o = row * DK + c;
+    if (a.rq) {  // through the normalization's Jacobian
+      auto jac = [&](float4& d, const __nv_bfloat16* x, float r) {
+        const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + o));
+        const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + o + 2));
+        const float n0 = x01.x * r, n1 = x01.y * r, n2 = x23.x * r, n3 = x23.y * r;
+        float dot = (n0 * d.x + n1 * d.y) + (n2 * d.z + n3 * d.w);
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
+        d = make_float4(r * (d.x - n0 * dot), r * (d.y - n1 * dot), r * (d.z - n2 * dot), r * (d.w - n3 * dot));
+      };
+      jac(sq, a.q, a.rq[row]);
+      jac(sk, a.k, a.rk[row]);
+    }
+    *reinterpret_cast<__nv_bfloat162*>(a.dq + o) = __floats2bfloat162_rn(sq.x, sq.y);
+    *reinterpret_cast<__nv_bfloat162*>(a.dq + o + 2) = __floats2bfloat162_rn(sq.z, sq.w);
+    *reinterpret_cast<__nv_bfloat162*>(a.dk + o) = __floats2bfloat162_rn(sk.x, sk.y);
+    *reinterpret_cast<__nv_bfloat162*>(a.dk + o + 2) = __floats2bfloat162_rn(sk.z, sk.w);
   }
 }
 

@@ -26,6 +26,7 @@ struct ChunkSmemT {
   float At[CH * LDS];  // strict_tril of the gated Gram K K^T (without beta)
   float T[CH * LDS];   // (I + diag(beta) At)^-1
   float tmp[3 * 256];
+  float rq[CH], rk[CH];  // in-kernel L2 normalization: row scales of q and k (when used)
   __device__ __forceinline__ float k(int i, int c) const { return elem(K[i * LD + c]); }
   __device__ __forceinline__ float q(int i, int c) const { return elem(Q[i * LD + c]); }
   // Elements (i, c) and (i, c + 1), c even.
@@ -136,8 +137,11 @@ __device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restric
 // The upper channel half leaves its partial sums in s.At and s.T (free until
 // the inverse); the lower half adds them in, masks, and writes the results.
 // Aqk is stored rounded to TF32 (it is only ever an MMA operand), rows LDS apart.
+// With `scaled` (in-kernel L2 normalization: the tiles hold the raw q, k and
+// s.rq, s.rk their rows' scales) the results are those of the normalized
+// rows: At[i][j] rk_i rk_j and Aqk[i][j] rq_i rk_j, in FP32.
 template <bool VEC, typename ET, int LG>
-__device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
+__device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk, bool scaled = false) {
   const int warp = threadIdx.x >> 5, I = warp & 3, hk = warp >> 2, i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const int ra = i0 + g, rb = i0 + g + 8;
@@ -215,6 +219,10 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk) {
             vQ *= dec;
           }
           if (col == row) vK = 0.f;
+          if (scaled) {
+            vK *= s.rk[row] * s.rk[col];
+            vQ *= s.rq[row] * s.rk[col];
+          }
         }
         s.At[row * LDS + col] = vK;
         aqk[row * LDS + col] = __uint_as_float(tf32(vQ));

@@ -22,9 +22,15 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
   const int tid = threadIdx.x, warp = tid >> 5;
+  const bool scaled = a.rq != nullptr;  // in-kernel L2 normalization
+  if (scaled && tid < CH) {
+    const size_t row = (size_t)(cd.tok0 + min(tid, max(cd.len - 1, 0))) * a.Hqk + hq;
+    s.rq[tid] = a.rq[row];
+    s.rk[tid] = a.rk[row];
+  }
   load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
                          a.HV);
-  gram<VEC>(s, a.aqk + aqk_off(chunk, h, a.HV));
+  gram<VEC>(s, a.aqk + aqk_off(chunk, h, a.HV), scaled);
   invert(s);
   // At and T for the backward: the values its gradient kernel needs, bit for bit.
   if (a.amat) {
@@ -44,7 +50,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float gl = VEC ? s.G[i * LDT + d + q] : s.gs[i];
-      r[q] = __uint_as_float(tf32(s.q(i, d + q) * ex2(gl)));
+      r[q] = __uint_as_float(tf32(s.q(i, d + q) * (scaled ? s.rq[i] : 1.f) * ex2(gl)));
       if (i == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d + q] = ex2(VEC ? s.G[(CH - 1) * LDT + d + q] : s.gs[CH - 1]);
     }
     *reinterpret_cast<float4*>(&a.qp[qp_off(chunk, h, a.HV) + i * LDF + d]) = make_float4(r[0], r[1], r[2], r[3]);
@@ -57,7 +63,8 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
     const int i = (l & 7) + 8 * (w & 7), d = 4 * (w >> 3) + (l >> 3);
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
     const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
-    a.kd[kd_off(chunk, h, a.HV) + d * LDS + i] = __uint_as_float(tf32(s.k(i, d) * ex2(glast - gl)));
+    a.kd[kd_off(chunk, h, a.HV) + d * LDS + i] =
+        __uint_as_float(tf32(s.k(i, d) * (scaled ? s.rk[i] : 1.f) * ex2(glast - gl)));
   }
   __syncthreads();
   // Q tile <- v rows (async), G tile <- beta * K * Gamma (B of w).
@@ -72,7 +79,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   for (int e = tid; e < CH * DK; e += blockDim.x) {
     const int i = e >> 7, d = e & 127;
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
-    s.G[i * LDT + d] = s.beta[i] * s.k(i, d) * ex2(gl);
+    s.G[i * LDT + d] = s.beta[i] * (scaled ? s.rk[i] : 1.f) * s.k(i, d) * ex2(gl);
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -111,6 +118,40 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
       }
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// In-kernel q/k L2 normalization, before the prep: one warp per (token, Q/K
+// head) row of q or of k (lane: elements 4 lane .. 4 lane + 3); the sum of
+// squares by shuffles in a fixed order; the normalized row in BF16 (the
+// inputs the rest of the path reads) and its scale r in FP32 (the backward's
+// Jacobian).  The "use_qk_l2norm_in_kernel" option of PR #8638
+// "perf(cake_gdn_kcp): ... graph-replay checkpoint recompute hands its tapes
+// to the backward" (workload description).
+// ---------------------------------------------------------------------------
+constexpr float kL2NormEps = 1e-6f;
+__global__ void __launch_bounds__(256) k_l2norm(L2NormArgs a) {
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= 2 * a.rows) return;
+  const bool isk = row >= a.rows;
+  const int64_t r0 = isk ? row - a.rows : row;
+  const __nv_bfloat16* x = (isk ? a.k : a.q) + r0 * DK + 4 * lane_id();
+  const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x));
+  const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + 2));
+  float ss = (x01.x * x01.x + x01.y * x01.y) + (x23.x * x23.x + x23.y * x23.y);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+  const float r = rsqrtf(ss + kL2NormEps);
+  __nv_bfloat16* n = (isk ? a.kn : a.qn) + r0 * DK + 4 * lane_id();
+  *reinterpret_cast<__nv_bfloat162*>(n) = __floats2bfloat162_rn(x01.x * r, x01.y * r);
+  *reinterpret_cast<__nv_bfloat162*>(n + 2) = __floats2bfloat162_rn(x23.x * r, x23.y * r);
+  if (lane_id() == 0) (isk ? a.rk : a.rq)[r0] = r;
+}
+
+cudaError_t launch_l2norm(const L2NormArgs& a, cudaStream_t st) {
+  if (a.rows == 0) return cudaSuccess;
+  k_l2norm<<<(unsigned)((2 * a.rows + 7) / 8), 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

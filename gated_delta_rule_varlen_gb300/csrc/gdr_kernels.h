@@ -23,6 +23,10 @@ struct PrepArgs {
   int Hqk, HV;
   float *w, *u, *qp, *kd, *aqk, *gam;  // w, qp, kd, aqk with the padded pitches of gdr_common.cuh
   float *amat, *tmat;  // At and T per chunk ([64][64] FP32), or null when nothing is saved
+  // In-kernel q/k L2 normalization (else null): the scales r [T][Hqk] of q and
+  // k's rows; q and k are then the raw inputs and every product takes the
+  // normalized rows (the scales applied in FP32).
+  const float *rq, *rk;
   int chunk_base;      // block x works on chunk chunk_base + x
 };
 
@@ -119,7 +123,20 @@ struct GroupReduceArgs {
   int Hqk, HV;
   const float *dq_part, *dk_part;
   __nv_bfloat16 *dq, *dk;
+  // In-kernel q/k L2 normalization (else null): the raw q, k and the scales r
+  // [T][Hqk] of their normalized copies.
+  const __nv_bfloat16 *q, *k;
+  const float *rq, *rk;
   int chunk_base;  // block x works on chunk chunk_base + x
+};
+
+// In-kernel q/k L2 normalization (forward pre-pass): each (token, Q/K head)
+// vector x of q and k -> n = x r (BF16), r = (sum x^2 + eps)^(-1/2) (FP32).
+struct L2NormArgs {
+  const __nv_bfloat16 *q, *k;
+  __nv_bfloat16 *qn, *kn;
+  float *rq, *rk;
+  int64_t rows;  // T * Hqk
 };
 
 cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
@@ -129,5 +146,6 @@ cudaError_t launch_walk_bwd_v(const WalkBwdArgs& a, int nsegs, cudaStream_t st);
 cudaError_t launch_grad_state(const GradStateArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_grad(const GradArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
 cudaError_t launch_group_reduce(const GroupReduceArgs& a, int nchunks, cudaStream_t st);
+cudaError_t launch_l2norm(const L2NormArgs& a, cudaStream_t st);
 
 }  // namespace gdr

@@ -86,14 +86,26 @@ typedef int gdr_status;
 /* Human-readable name of a status code (static string). */
 const char* gdr_status_string(gdr_status status);
 
+/* In-kernel q/k L2 normalization (argument qk_l2norm of the calls below; the
+ * pages' "use_qk_l2norm_in_kernel", flashinfer PR #8638 "perf(cake_gdn_kcp):
+ * ... graph-replay checkpoint recompute hands its tapes to the backward",
+ * workload description).  When non-zero, every (token, Q/K head) vector x of
+ * q and of k enters the recurrence as n = x * (sum_c x_c^2 + 1e-6)^(-1/2)
+ * (FP32, rounded to BF16 once), and dq, dk are the gradients with respect to
+ * the raw q, k (dx = r (dn - n (n . dn)), applied in FP32 before the single
+ * rounding).  The forward keeps the normalized q, k and their scales in
+ * `saved`; the flag must be the same for the workspace query, the forward and
+ * the backward (a mismatch with the forward returns GDR_STALE_WORKSPACE). */
+
 /* Workspace sizes for a KDA problem (host-only; no CUDA calls).
- * saved_bytes: the forward's intermediates kept for the backward (chunk
- * tables, w, u, Q*Gamma, Kd, Delta, Aqk, At, T, gamma, and the per-chunk state
- * tape).
+ * saved_bytes: the forward's intermediates kept for the backward (chunk and
+ * segment tables, w, u, Q*Gamma, Kd, Delta, Aqk, At, T, gamma, the per-chunk
+ * state tape, per-segment state maps of split documents, and with qk_l2norm
+ * the normalized q, k).
  * scratch_bytes: temporaries of the backward.  A forward called without a
  * `saved` buffer keeps its intermediates in `scratch`, which must then hold
  * saved_bytes.  Returns GDR_BAD_CU_SEQLENS or GDR_INVALID_ARG on bad input. */
-gdr_status kda_workspace_bytes(int64_t T, int32_t H, int32_t N, const int32_t* cu_seqlens_host,
+gdr_status kda_workspace_bytes(int64_t T, int32_t H, int32_t N, const int32_t* cu_seqlens_host, int qk_l2norm,
                                size_t* saved_bytes, size_t* scratch_bytes);
 
 /* KDA forward.  Writes out [T][H][128] and, when non-null, ht [N][H][128][128].
@@ -103,8 +115,8 @@ gdr_status kda_workspace_bytes(int64_t T, int32_t H, int32_t N, const int32_t* c
  * intermediates go to `scratch`. */
 gdr_status kda_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
-                   float scale, const float* h0, gdr_bf16* out, float* ht, void* saved, size_t saved_bytes,
-                   int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+                   float scale, int qk_l2norm, const float* h0, gdr_bf16* out, float* ht, void* saved,
+                   size_t saved_bytes, int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 
 /* KDA backward from a forward with save_for_bwd = 1 on the same inputs.
  * dout [T][H][128]; dht may be null (zero).  Writes dq, dk, dv [T][H][128]
@@ -113,9 +125,9 @@ gdr_status kda_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
  * the same T, H, N and cu_seqlens in this process. */
 gdr_status kda_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
-                   float scale, const float* h0, const gdr_bf16* dout, const float* dht, const void* saved,
-                   size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg, gdr_bf16* dbeta,
-                   float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+                   float scale, int qk_l2norm, const float* h0, const gdr_bf16* dout, const float* dht,
+                   const void* saved, size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg,
+                   gdr_bf16* dbeta, float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 
 /* No-allocation KDA forward.  The paper has no counterpart; this entry point
  * exists for callers that cannot allocate device memory at call time: code
@@ -124,7 +136,8 @@ gdr_status kda_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
  * and forbids side allocations, and real-time paths that must not take the
  * allocator's locks or risk an out-of-memory failure mid-step.
  *
- * Same arguments and results as kda_fwd with save_for_bwd = 0, but the
+ * Same arguments and results as kda_fwd with save_for_bwd = 0 and
+ * qk_l2norm = 0, but the
  * forward's intermediates live in one fixed 64 MiB device array inside the
  * library (held by every GPU that loads the library until the process exits)
  * instead of caller-provided workspaces, and nothing is saved for a backward.
@@ -149,16 +162,16 @@ gdr_status kda_fwd_noalloc(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16*
  * FP32 gate g [T][HV] and FP32 beta [T][HV]; dq/dk are [T][Hqk][128], summed
  * in FP32 over the value heads of each Q/K head. */
 gdr_status gdn_workspace_bytes(int64_t T, int32_t Hqk, int32_t HV, int32_t N, const int32_t* cu_seqlens_host,
-                               size_t* saved_bytes, size_t* scratch_bytes);
+                               int qk_l2norm, size_t* saved_bytes, size_t* scratch_bytes);
 
 gdr_status gdn_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const float* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t Hqk,
-                   int32_t HV, float scale, const float* h0, gdr_bf16* out, float* ht, void* saved,
+                   int32_t HV, float scale, int qk_l2norm, const float* h0, gdr_bf16* out, float* ht, void* saved,
                    size_t saved_bytes, int save_for_bwd, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 
 gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const float* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t Hqk,
-                   int32_t HV, float scale, const float* h0, const gdr_bf16* dout, const float* dht,
+                   int32_t HV, float scale, int qk_l2norm, const float* h0, const gdr_bf16* dout, const float* dht,
                    const void* saved, size_t saved_bytes, gdr_bf16* dq, gdr_bf16* dk, gdr_bf16* dv, float* dg,
                    float* dbeta, float* dh0, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 

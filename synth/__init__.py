@@ -102,18 +102,25 @@ def _l2norm_bf16(x: torch.Tensor) -> torch.Tensor:
 
 def make_inputs(variant: str, T: int, Hqk: int, HV: int, D: int = 128, seed: int = 0,
                 device="cpu", gate_low: float = -5.0, gate_high: float = 0.0,
-                with_dout: bool = True):
+                with_dout: bool = True, normalize_qk: bool = True):
     """Draw one problem's inputs.  Returns a dict of tensors on `device`:
     q, k [T,Hqk,D] bf16; v [T,HV,D] bf16; g [T,HV,D] (kda) or [T,HV] (gdn) fp32;
-    beta [T,HV] (bf16 kda, fp32 gdn); dout [T,HV,D] bf16 (when with_dout)."""
+    beta [T,HV] (bf16 kda, fp32 gdn); dout [T,HV,D] bf16 (when with_dout).
+    normalize_qk=False leaves q and k as drawn, N(0,1) rows times a per-row
+    factor U(0.25, 4) (raw inputs for the in-kernel L2 normalization)."""
     if variant not in ("kda", "gdn"):
         raise ValueError(variant)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     f32 = dict(dtype=torch.float32, device=device, generator=gen)
     out = {}
-    out["q"] = _l2norm_bf16(torch.randn((T, Hqk, D), **f32))
-    out["k"] = _l2norm_bf16(torch.randn((T, Hqk, D), **f32))
+    if normalize_qk:
+        out["q"] = _l2norm_bf16(torch.randn((T, Hqk, D), **f32))
+        out["k"] = _l2norm_bf16(torch.randn((T, Hqk, D), **f32))
+    else:
+        for name in ("q", "k"):
+            x = torch.randn((T, Hqk, D), **f32)
+            out[name] = (x * (torch.rand((T, Hqk, 1), **f32) * 3.75 + 0.25)).to(torch.bfloat16)
     out["v"] = torch.randn((T, HV, D), **f32).to(torch.bfloat16)
     gshape = (T, HV, D) if variant == "kda" else (T, HV)
     out["g"] = torch.rand(gshape, **f32) * (gate_high - gate_low) + gate_low

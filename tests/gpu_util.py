@@ -30,7 +30,7 @@ def f64(t):
     return None if t is None else t.detach().double().cpu().numpy()
 
 
-def run_gpu(variant, x, cu, scale=SCALE, h0=None, dht=None, backward=True, want_dh0=False, dev="cuda"):
+def run_gpu(variant, x, cu, scale=SCALE, h0=None, dht=None, backward=True, want_dh0=False, dev="cuda", l2=False):
     import gated_delta_rule_varlen_gb300 as gdr
 
     xd = {k: v.to(dev) for k, v in x.items()}
@@ -44,16 +44,16 @@ def run_gpu(variant, x, cu, scale=SCALE, h0=None, dht=None, backward=True, want_
     T, Hqk, D = xd["q"].shape
     HV, N = xd["v"].shape[1], len(cu) - 1
     if variant == "kda":
-        sb, cb = gdr.kda_workspace_bytes(T, HV, cu)
+        sb, cb = gdr.kda_workspace_bytes(T, HV, cu, l2)
     else:
-        sb, cb = gdr.gdn_workspace_bytes(T, Hqk, HV, cu)
+        sb, cb = gdr.gdn_workspace_bytes(T, Hqk, HV, cu, l2)
     poison = lambda n: torch.full((max(int(n), 256),), 0xFF, dtype=torch.uint8, device=dev)
     nan = float("nan")
     out = torch.full((T, HV, D), nan, dtype=torch.bfloat16, device=dev)
     ht = torch.full((N, HV, D, D), nan, dtype=torch.float32, device=dev)
     out, ht, saved = fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, scale, h0=h0d, out=out, ht=ht,
                          saved=poison(sb) if backward else None, scratch=None if backward else poison(sb),
-                         save_for_bwd=backward)
+                         save_for_bwd=backward, qk_l2norm=l2)
     res = {"out": out, "ht": ht}
     if backward:
         grads = {n: torch.full_like(xd[src], nan) for n, src in
@@ -61,16 +61,16 @@ def run_gpu(variant, x, cu, scale=SCALE, h0=None, dht=None, backward=True, want_
         if want_dh0:
             grads["dh0"] = torch.full((N, HV, D, D), nan, dtype=torch.float32, device=dev)
         res.update(bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, scale, xd["dout"], saved, h0=h0d,
-                       dht=dhtd, want_dh0=want_dh0, scratch=poison(cb), grads=grads))
+                       dht=dhtd, want_dh0=want_dh0, scratch=poison(cb), grads=grads, qk_l2norm=l2))
     torch.cuda.synchronize()
     gdr.gdr_check_device()  # no kernel gave up a bounded wait
     return res
 
 
-def run_oracle(x, cu, scale=SCALE, h0=None, dht=None, backward=True):
+def run_oracle(x, cu, scale=SCALE, h0=None, dht=None, backward=True, l2=False):
     f = {k: f64(v) for k, v in x.items()}
     return oracle.run(f["q"], f["k"], f["v"], f["g"], f["beta"], cu, scale, h0=f64(h0),
-                      dout=f["dout"] if backward else None, dht=f64(dht))
+                      dout=f["dout"] if backward else None, dht=f64(dht), qk_l2norm=l2)
 
 
 class Err(float):

@@ -91,35 +91,35 @@ def test_forward_host_validation_before_any_cuda_call(gdr):
     cup = cu.ctypes.data_as(gdr.PI32)
     p = _fake()
     # cu[N] != T
-    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 10, 1, 1.0, None, p, None, p, 1 << 40, 1, None, 0, None)
+    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 10, 1, 1.0, 0, None, p, None, p, 1 << 40, 1, None, 0, None)
     assert st == gdr.GDR_BAD_CU_SEQLENS
     # workspace too small
-    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, _fake(256), 1024, 1, None, 0, None)
+    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, _fake(256), 1024, 1, None, 0, None)
     assert st == gdr.GDR_WORKSPACE_TOO_SMALL
     # misaligned workspace
-    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, ctypes.c_void_p(0x10010), 1 << 40, 1,
+    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, ctypes.c_void_p(0x10010), 1 << 40, 1,
                      None, 0, None)
     assert st == gdr.GDR_INVALID_ARG
     # null input
-    st = lib.kda_fwd(None, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, p, 1 << 40, 1, None, 0, None)
+    st = lib.kda_fwd(None, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, p, 1 << 40, 1, None, 0, None)
     assert st == gdr.GDR_INVALID_ARG
     # save_for_bwd without a saved buffer
-    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, None, 0, 1, p, 1 << 40, None)
+    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, None, 0, 1, p, 1 << 40, None)
     assert st == gdr.GDR_INVALID_ARG
     # q not on a 16-byte boundary (its rows are copied in 16-byte pieces)
-    st = lib.kda_fwd(ctypes.c_void_p(0x10008), p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, p, 1 << 40, 1,
+    st = lib.kda_fwd(ctypes.c_void_p(0x10008), p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, p, 1 << 40, 1,
                      None, 0, None)
     assert st == gdr.GDR_INVALID_ARG
     # out not on a 4-byte boundary
-    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, ctypes.c_void_p(0x10002), None, p, 1 << 40, 1,
+    st = lib.kda_fwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, ctypes.c_void_p(0x10002), None, p, 1 << 40, 1,
                      None, 0, None)
     assert st == gdr.GDR_INVALID_ARG
     # GDN: HV not a multiple of Hqk
-    st = lib.gdn_fwd(p, p, p, p, p, p, cup, 2, 11, 4, 6, 1.0, None, p, None, p, 1 << 40, 1, None, 0, None)
+    st = lib.gdn_fwd(p, p, p, p, p, p, cup, 2, 11, 4, 6, 1.0, 0, None, p, None, p, 1 << 40, 1, None, 0, None)
     assert st == gdr.GDR_INVALID_ARG
     # No documents: nothing to do.
     z = np.array([0], dtype=np.int32)
-    st = lib.kda_fwd(None, None, None, None, None, None, z.ctypes.data_as(gdr.PI32), 0, 0, 1, 1.0, None, None, None,
+    st = lib.kda_fwd(None, None, None, None, None, None, z.ctypes.data_as(gdr.PI32), 0, 0, 1, 1.0, 0, None, None, None,
                      None, 0, 0, None, 0, None)
     assert st == gdr.GDR_OK
 
@@ -130,18 +130,18 @@ def test_backward_rejects_unstamped_workspace(gdr):
     cup = cu.ctypes.data_as(gdr.PI32)
     p = _fake()
     big = 1 << 40
-    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, _fake(512), big, p, p, p, p, p, None,
+    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
                      _fake(1024), big, None)
     assert st == gdr.GDR_STALE_WORKSPACE
-    st = lib.gdn_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 3, 1.0, None, p, None, _fake(512), big, p, p, p, p, p, None,
+    st = lib.gdn_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 3, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
                      _fake(1024), big, None)
     assert st == gdr.GDR_STALE_WORKSPACE
     # dout not on a 16-byte boundary
-    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, ctypes.c_void_p(0x10004), None, _fake(512), big, p,
+    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, ctypes.c_void_p(0x10004), None, _fake(512), big, p,
                      p, p, p, p, None, _fake(1024), big, None)
     assert st == gdr.GDR_INVALID_ARG
     # Too-small scratch is reported before the stamp.
-    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, None, p, None, _fake(512), big, p, p, p, p, p, None,
+    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
                      _fake(1024), 256, None)
     assert st == gdr.GDR_WORKSPACE_TOO_SMALL
 

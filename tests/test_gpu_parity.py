@@ -397,3 +397,34 @@ def test_segments_ckpt_matches_plain(segments):
     assert torch.equal(o1, a["out"]) and torch.equal(o2, a["out"])
     for name in ("dq", "dk", "dv", "dg", "dbeta"):
         assert torch.equal(gr[name], a[name]), name
+
+
+# ---------------------------------------------------------------------------
+# In-kernel q/k L2 normalization (qk_l2norm): raw q, k with row norms from
+# about 0.25 to 4 x sqrt(128); the oracle normalizes in FP64.
+# ---------------------------------------------------------------------------
+def _check_l2(variant, lengths, Hqk, HV, seed, glow=-5.0, states=True):
+    T = sum(lengths)
+    cu = synth.cu_from_lengths(lengths)
+    x = synth.make_inputs(variant, T, Hqk, HV, 128, seed=seed, gate_low=glow, normalize_qk=False)
+    h0 = synth.make_states(len(lengths), HV, 128, seed=seed + 11, scale=0.05) if states else None
+    dht = synth.make_states(len(lengths), HV, 128, seed=seed + 12, scale=0.05) if states else None
+    gpu = run_gpu(variant, x, cu, h0=h0, dht=dht, want_dh0=states, l2=True)
+    ref = run_oracle(x, cu, h0=h0, dht=dht, l2=True)
+    print(variant, "l2", lengths, assert_within(compare(gpu, ref)))
+    return gpu, x
+
+
+def test_kda_qk_l2norm():
+    gpu, x = _check_l2("kda", [300, 77, 0, 129], 2, 2, seed=40)
+    # The gradient with respect to a vector that is normalized has no component along it.
+    dot = (gpu["dq"].double() * x["q"].cuda().double()).sum(-1).abs().max().item()
+    assert dot < 2e-2 * gpu["dq"].double().norm(dim=-1).max().item()
+
+
+def test_gdn_qk_l2norm_grouped():
+    _check_l2("gdn", [5, 64, 130, 71], 2, 6, seed=41)
+
+
+def test_kda_qk_l2norm_mild_gates_long_document():
+    _check_l2("kda", [4096], 1, 1, seed=42, glow=-0.05)
