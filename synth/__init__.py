@@ -79,12 +79,15 @@ class Workload:
 
 def workload(name: str) -> Workload:
     """The named workloads: kda_tiny, kda_pack_h4, kda_pack_h16, kda_pack_h64,
-    gdn_p1 (241817 tokens / 6 docs), gdn_1doc (32768 tokens / 1 doc), and
-    kda_prof (4 x 16384 tokens, H = 4: a profiling-size case)."""
+    gdn_p1 (241817 tokens / 6 docs), gdn_1doc (32768 tokens / 1 doc), and the
+    profiling-size cases kda_prof (4 x 16384 tokens, H = 4) and kda_prof16
+    (4 x 4096 tokens, H = 16)."""
     if name == "kda_tiny":
         return Workload(name, "kda", (512,), 1, 1)
     if name == "kda_prof":  # profiling-size pack: 4 x 16384 tokens, H = 4 (inputs > L2, a few GB in all)
         return Workload(name, "kda", (16384,) * 4, 4, 4)
+    if name == "kda_prof16":  # profiling-size pack with H = 16 chains per document: 4 x 4096 tokens, H = 16
+        return Workload(name, "kda", (4096,) * 4, 16, 16)
     if name.startswith("kda_pack_h"):
         h = int(name[len("kda_pack_h"):])
         return Workload(name, "kda", KDA_PACK_DOCS, h, h)
