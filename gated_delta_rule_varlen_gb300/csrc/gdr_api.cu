@@ -353,34 +353,6 @@ int sm_count() {
   return n > 0 ? n : 152;
 }
 
-// Warps per walk CTA (each warp carries 16 value columns, a chain's 128
-// columns are split over 8 / warps CTAs).  A walk CTA fills most of an SM's
-// shared memory, so one runs per SM: take the fewest warps per CTA (the most
-// SMs per chain) that still fit every CTA in one wave.
-int walk_warps(int64_t chains) {
-  if (const char* e = std::getenv("GDR_WALK_WARPS")) {
-    const int v = std::atoi(e);
-    if (v == 1 || v == 2 || v == 4 || v == 8) return v;
-  }
-  const int64_t sms = sm_count();
-  for (int nw = 1; nw < 8; nw *= 2)
-    if (chains * (8 / nw) <= sms) return nw;
-  return 8;
-}
-
-// Value columns per tensor-core walk CTA (16, 32 or 64; one CTA per SM):
-// the narrowest slice that still fits every CTA in one wave, else 64.
-int walk_tc_cols(int64_t chains) {
-  if (const char* e = std::getenv("GDR_WALK_COLS")) {
-    const int v = std::atoi(e);
-    if (v == 16 || v == 32 || v == 64) return v;
-  }
-  const int64_t sms = sm_count();
-  for (int cols = 16; cols < 64; cols *= 2)
-    if (chains * (DK / cols) <= sms) return cols;
-  return 64;
-}
-
 bool aligned(const void* p) { return ((uintptr_t)p % kAlign) == 0; }
 // Tensors the kernels copy in 16-byte pieces (q, k, v, g, dout) or store in
 // pairs must start on these boundaries.
@@ -404,9 +376,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A row-major FP32 matrix [rows][cols] read in boxes of 32 columns (128 bytes,
-// 128-byte swizzle) x box_rows rows.
-// rows x cols FP32 tensor whose rows are `pitch` elements apart; boxes of 32 x box_rows.
+// A row-major FP32 matrix [rows][cols] whose rows are `pitch` elements apart,
+// read in boxes of 32 columns (128 bytes, 128-byte swizzle) x box_rows rows.
 bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch, uint32_t box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
@@ -415,19 +386,6 @@ bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
   cuuint32_t box[2] = {32, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// rows x cols dense BF16 tensor; boxes of 64 x box_rows.
-bool bf16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

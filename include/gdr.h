@@ -59,6 +59,11 @@
  *     ordered after the stream's earlier work and before its later work,
  *     also under stream capture.
  *   - Results are deterministic (no floating-point atomics).
+ *   - Per-device state.  The library keeps, per device, its internal streams
+ *     and events, an error word and (for kda_fwd_noalloc) the address of its
+ *     device array, all created on first use.  cudaDeviceReset destroys them
+ *     behind the library's back: do not call into the library on a device
+ *     after a cudaDeviceReset of that device in the same process.
  */
 #ifndef GDR_H_
 #define GDR_H_
@@ -221,7 +226,9 @@ gdr_status gdr_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
  * and of the (token, value head) pairs each worked on; launches of different
  * document groups may overlap in time), in first-launch order, NUL-terminated,
  * into buf; it returns GDR_INVALID_ARG if buf_bytes is too small.  Kernel
- * names: plan, prep, walk_fwd, walk_bwd, grad_state, grad, group_reduce. */
+ * names: plan, l2norm, prep, walk_fwd_sum, merge_fwd, walk_fwd, walk_bwd_sum,
+ * merge_bwd, walk_bwd, grad_state, grad, group_reduce (the _sum and merge
+ * launches run only for split packs, l2norm only with qk_l2norm). */
 int gdr_profile_enable(int on);
 gdr_status gdr_profile_report(char* buf, size_t buf_bytes);
 
@@ -241,9 +248,12 @@ int gdr_set_serial(int on);
  * of its start state, a merge chains the segments' start states, then every
  * segment's walk runs from its own start state; flashinfer PR #7723,
  * "perf(cake_gdn): prefetch offset adjoint walk, default LPT segment plan",
- * segment plan).  By default (chunks = 0) a segment has about
- * max(64, total chunks x heads / SM count) chunks, and a pack whose longest
- * document has at most twice that is not split.  chunks > 0 forces segments
+ * segment plan).  By default (chunks = 0) a pack is split only when the
+ * longest document's walk chain (about 8.3 us per chunk, forward and backward
+ * together) outlasts the rest of the pack's work spread over the SMs (about
+ * 50 us of SM time per chunk and head); its segments then have about
+ * max(64, total chunks x heads / SM count) chunks, and documents no longer
+ * than one segment stay whole.  chunks > 0 forces segments
  * of about that many chunks (tests and tuning).  Process-wide, read by every
  * *_workspace_bytes, forward and backward call; the saved-buffer stamp
  * records it, so a backward planned with another setting than its forward
