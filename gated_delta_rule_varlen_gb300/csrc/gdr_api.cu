@@ -27,6 +27,21 @@ constexpr int kRankLimit = 4096;  // documents ranked longest-first on the devic
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // ---------------------------------------------------------------------------
+// Header at the start of a saved buffer: which saving forward filled it.  The
+// saving forward's planning kernel writes it; the backward compares it on the
+// device with what its own arguments imply (kStaleCode in the device error
+// word on a mismatch).  The buffer's contents are position-independent, so a
+// saved buffer copied to another address stays valid.
+struct SavedHeader {
+  uint64_t magic;
+  int64_t T;
+  int32_t N, Hqk, HV, variant, lseg, l2;
+  uint64_t cu_hash;
+  uint64_t counter;  // which saving forward of this process wrote it (1, 2, ...)
+};
+constexpr uint64_t kSavedMagic = 0x3145564153524447ull;
+constexpr int kStaleCode = 8;
+
 // Planning kernel: document and chunk tables from the device cu_seqlens, and
 // the longest-first document order for the walks (the LPT rule of PR #7723
 // "perf(cake_gdn): prefetch offset adjoint walk, default LPT segment plan",
@@ -34,11 +49,14 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // order (the longest document's chunks first), so that any run of documents
 // in it owns one contiguous range of chunks.  Ties go to the lower document
 // index; above kRankLimit documents the order is the given one.  One block; no
-// host copy.  plan_ranks() on the host reproduces the same order.
+// host copy.  plan_ranks() on the host reproduces the same order.  A saving
+// forward also writes the saved buffer's header (hdr_out).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N, int lseg, DocDesc* docs,
-                                               ChunkDesc* chunks, int* order, SegDesc* segs) {
+                                               ChunkDesc* chunks, int* order, SegDesc* segs, SavedHeader hdr,
+                                               SavedHeader* hdr_out) {
   __shared__ int part[1024], spart[1024];
+  if (hdr_out && threadIdx.x == 0) *hdr_out = hdr;
   __shared__ int lens[kRankLimit];
   __shared__ int ord[kRankLimit];
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -98,6 +116,18 @@ __global__ void __launch_bounds__(1024) k_plan(const int* __restrict__ cu, int N
     c += nch;
     sg += nseg;
   }
+}
+
+// The backward's check of a saved buffer's header (one thread): a mismatch
+// with the expected header (the counter only when `with_counter`) sets
+// kStaleCode in the device error word.
+__global__ void k_check_header(SavedHeader want, const SavedHeader* __restrict__ have, int with_counter, int* err) {
+  if (threadIdx.x != 0) return;
+  const SavedHeader h = *have;
+  const bool ok = h.magic == want.magic && h.T == want.T && h.N == want.N && h.Hqk == want.Hqk && h.HV == want.HV &&
+                  h.variant == want.variant && h.lseg == want.lseg && h.l2 == want.l2 && h.cu_hash == want.cu_hash &&
+                  (!with_counter || h.counter == want.counter);
+  if (!ok) atomicExch(err, kStaleCode);
 }
 
 // Host copy of the plan's document order, and the split of the backward into
@@ -220,6 +250,8 @@ int64_t assign_segments(std::vector<DocGroup>& groups, int32_t N, const int32_t*
 // ---------------------------------------------------------------------------
 struct Layout {
   int64_t NC = 0, NSEG = 0;
+  size_t header = 0;                             // SavedHeader (saved buffers)
+  size_t bdocs = 0, bchunks = 0, border = 0, bsegs = 0;  // the backward's own plan (scratch)
   size_t docs = 0, chunks = 0, order = 0, segs = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, amat = 0,
          tmat = 0, gam = 0, tape = 0, smap = 0, sstart = 0, sbias = 0;
   size_t saved_total = 0;
@@ -246,6 +278,7 @@ Layout make_layout(int64_t T, int64_t NC, int32_t N, int32_t Hqk, int32_t HV, bo
     o = align_up(o + bytes);
     return at;
   };
+  L.header = take(sizeof(SavedHeader));
   L.docs = take((size_t)std::max(N, 1) * sizeof(DocDesc));
   L.chunks = take((size_t)std::max<int64_t>(NC, 1) * sizeof(ChunkDesc));
   L.order = take((size_t)std::max(N, 1) * sizeof(int));
@@ -271,6 +304,12 @@ Layout make_layout(int64_t T, int64_t NC, int32_t N, int32_t Hqk, int32_t HV, bo
   }
   L.saved_total = o;
   o = 0;
+  // The backward plans again into its scratch, so that no index it follows
+  // comes from the saved buffer.
+  L.bdocs = take((size_t)std::max(N, 1) * sizeof(DocDesc));
+  L.bchunks = take((size_t)std::max<int64_t>(NC, 1) * sizeof(ChunkDesc));
+  L.border = take((size_t)std::max(N, 1) * sizeof(int));
+  L.bsegs = take((size_t)std::max<int64_t>(NSEG, 1) * sizeof(SegDesc));
   L.dstape = take(st);
   L.ddelta = take((size_t)NC * HV * CH * LDF * sizeof(float));
   L.dqs = take(tile);
@@ -312,28 +351,54 @@ uint64_t hash_cu(const int32_t* cu, int32_t N) {
   return h;
 }
 
-// Stamp of a saved buffer: which forward filled it.  Host-side registry keyed
-// by the buffer address (no device read, no host synchronization).
+// Host registry of the saved buffers this process filled, keyed by address:
+// the stamp of the last saving forward into each.  The backward rejects,
+// before enqueueing anything, a registered buffer whose stamp does not match
+// its arguments; an unregistered one (copied to another address, or filled
+// by another process) is left to the device-side header check alone.
 struct Stamp {
   int64_t T;
   int32_t N, Hqk, HV, variant, lseg;
   bool l2;
   uint64_t cu_hash;
+  uint64_t counter;
 };
 std::mutex g_stamp_mu;
 std::unordered_map<const void*, Stamp> g_stamps;
+std::atomic<uint64_t> g_save_counter{0};
+
+enum class StampState { kUnknown, kMatch, kMismatch };
 
 void stamp_set(const void* saved, const Stamp& s) {
   std::lock_guard<std::mutex> lk(g_stamp_mu);
   g_stamps[saved] = s;
 }
-bool stamp_check(const void* saved, const Stamp& s) {
+// On kMatch, *counter is the registered forward's counter.
+StampState stamp_check(const void* saved, const Stamp& s, uint64_t* counter) {
   std::lock_guard<std::mutex> lk(g_stamp_mu);
   auto it = g_stamps.find(saved);
-  if (it == g_stamps.end()) return false;
+  if (it == g_stamps.end()) return StampState::kUnknown;
   const Stamp& r = it->second;
-  return r.T == s.T && r.N == s.N && r.Hqk == s.Hqk && r.HV == s.HV && r.variant == s.variant &&
-         r.lseg == s.lseg && r.l2 == s.l2 && r.cu_hash == s.cu_hash;
+  const bool same = r.T == s.T && r.N == s.N && r.Hqk == s.Hqk && r.HV == s.HV && r.variant == s.variant &&
+                    r.lseg == s.lseg && r.l2 == s.l2 && r.cu_hash == s.cu_hash;
+  if (!same) return StampState::kMismatch;
+  *counter = r.counter;
+  return StampState::kMatch;
+}
+
+SavedHeader header_of(const Stamp& s) {
+  SavedHeader h{};
+  h.magic = kSavedMagic;
+  h.T = s.T;
+  h.N = s.N;
+  h.Hqk = s.Hqk;
+  h.HV = s.HV;
+  h.variant = s.variant;
+  h.lseg = s.lseg;
+  h.l2 = s.l2 ? 1 : 0;
+  h.cu_hash = s.cu_hash;
+  h.counter = s.counter;
+  return h;
 }
 
 gdr_status check_device() {
@@ -594,9 +659,12 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   ChunkDesc* chunks = at<ChunkDesc>(base, L.chunks);
   int* order = at<int>(base, L.order);
   SegDesc* segs = at<SegDesc>(base, L.segs);
+  Stamp stamp{T, N, Hqk, HV, variant, lseg, l2 != 0, hash_cu(cu_host, N), 0};
+  if (save_for_bwd) stamp.counter = g_save_counter.fetch_add(1) + 1;
   {
     ProfScope ps("plan", stream);
-    k_plan<<<1, 1024, 0, stream>>>(cu, N, std::min(lseg, kNoSplit), docs, chunks, order, segs);
+    k_plan<<<1, 1024, 0, stream>>>(cu, N, std::min(lseg, kNoSplit), docs, chunks, order, segs, header_of(stamp),
+                                   save_for_bwd ? at<SavedHeader>(base, L.header) : nullptr);
   }
   if (cudaGetLastError() != cudaSuccess) return GDR_CUDA_ERROR;
   const bool vec = variant == 0;
@@ -704,7 +772,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
     if (!fork.join() && st == GDR_OK) st = GDR_CUDA_ERROR;
   }
   if (st != GDR_OK) return st;
-  if (save_for_bwd) stamp_set(saved, Stamp{T, N, Hqk, HV, variant, lseg, l2 != 0, hash_cu(cu_host, N)});
+  if (save_for_bwd) stamp_set(saved, stamp);
   return GDR_OK;
 }
 
@@ -729,14 +797,29 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   const int64_t NSEG = assign_segments(groups, N, cu_host, lseg);
   const Layout L = make_layout(T, NC, N, Hqk, HV, l2 != 0, NSEG);
   if (saved_bytes < L.saved_total || scratch_bytes < L.bwd_total) return GDR_WORKSPACE_TOO_SMALL;
-  if (!stamp_check(saved, Stamp{T, N, Hqk, HV, variant, lseg, l2 != 0, hash_cu(cu_host, N)}))
-    return GDR_STALE_WORKSPACE;
+  Stamp want{T, N, Hqk, HV, variant, lseg, l2 != 0, hash_cu(cu_host, N), 0};
+  const StampState known = stamp_check(saved, want, &want.counter);
+  if (known == StampState::kMismatch) return GDR_STALE_WORKSPACE;
   st = check_device();
   if (st != GDR_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return GDR_CUDA_ERROR;
   const bool vec = variant == 0;
-  const ChunkDesc* chunks = at<ChunkDesc>(saved, L.chunks);
-
-  const SegDesc* segs = at<SegDesc>(saved, L.segs);
+  // The backward's own plan (the same tables the forward made), and the
+  // device-side check of the saved buffer's header.
+  ChunkDesc* chunks = at<ChunkDesc>(scratch, L.bchunks);
+  SegDesc* segs = at<SegDesc>(scratch, L.bsegs);
+  {
+    ProfScope ps("plan", stream);
+    k_plan<<<1, 1024, 0, stream>>>(cu, N, std::min(lseg, kNoSplit), at<DocDesc>(scratch, L.bdocs), chunks,
+                                   at<int>(scratch, L.border), segs, SavedHeader{}, nullptr);
+  }
+  {
+    ProfScope ps("check", stream);
+    k_check_header<<<1, 32, 0, stream>>>(header_of(want), at<SavedHeader>(saved, L.header),
+                                         known == StampState::kMatch ? 1 : 0, err);
+  }
+  if (cudaGetLastError() != cudaSuccess) return GDR_CUDA_ERROR;
   const bool split = NSEG > N;
   WalkBwdArgs wb{};
   wb.segs = segs;
@@ -1047,7 +1130,7 @@ gdr_status gdr_check_device(void) {
   if (code != 0) {
     const int zero = 0;
     cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
-    return GDR_DEVICE_TIMEOUT;
+    return code == gdr::kStaleCode ? GDR_STALE_WORKSPACE : GDR_DEVICE_TIMEOUT;
   }
   return GDR_OK;
 }

@@ -84,7 +84,9 @@ typedef int gdr_status;
 #define GDR_BAD_CU_SEQLENS 2       /* cu[0] != 0, decreasing, or cu[N] != T */
 #define GDR_WORKSPACE_TOO_SMALL 3  /* saved_bytes / scratch_bytes below *_workspace_bytes */
 #define GDR_UNSUPPORTED 4          /* device is not sm_103 (GB300 / B300) */
-#define GDR_STALE_WORKSPACE 5      /* `saved` not filled by a matching forward with save_for_bwd = 1 */
+#define GDR_STALE_WORKSPACE 5      /* `saved` not filled by a matching forward with save_for_bwd = 1
+                                    * (returned by the backward, or by gdr_check_device for the
+                                    * device-side header check) */
 #define GDR_CUDA_ERROR 6           /* a CUDA launch or runtime call failed */
 #define GDR_DEVICE_TIMEOUT 7       /* a kernel's bounded wait ran out (reported by gdr_check_device) */
 
@@ -126,8 +128,23 @@ gdr_status kda_fwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
 /* KDA backward from a forward with save_for_bwd = 1 on the same inputs.
  * dout [T][H][128]; dht may be null (zero).  Writes dq, dk, dv [T][H][128]
  * BF16, dg [T][H][128] FP32, dbeta [T][H] BF16 and, when non-null, dh0.
- * Returns GDR_STALE_WORKSPACE when `saved` was not stamped by a forward with
- * the same T, H, N and cu_seqlens in this process. */
+ *
+ * Saved-buffer stamp.  A saving forward writes a header at the start of
+ * `saved`: a magic word, T, N, the head counts, the variant, the segment
+ * length, the qk_l2norm flag, a hash of cu_seqlens_host and the number of
+ * the saving forward in this process (1, 2, ...); it also records the header
+ * in a host registry keyed by the buffer's address.  The backward checks it
+ * twice.  On the host, before enqueueing anything: a buffer this process last
+ * filled with other arguments returns GDR_STALE_WORKSPACE.  On the device
+ * (asynchronously, no host synchronization): the header must match the
+ * backward's arguments, and for a registered address also the forward's
+ * number, so that a buffer overwritten in place by another saved buffer is
+ * caught; a mismatch makes the next gdr_check_device return
+ * GDR_STALE_WORKSPACE, and the backward's outputs are then unspecified (its
+ * kernels follow only tables it plans itself, so a bad buffer yields wrong
+ * numbers, never an out-of-bounds access).  The contents are
+ * position-independent: a saved buffer copied to another address (not
+ * registered) is accepted by its header alone. */
 gdr_status kda_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, const float* g, const gdr_bf16* beta,
                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int32_t N, int64_t T, int32_t H,
                    float scale, int qk_l2norm, const float* h0, const gdr_bf16* dout, const float* dht,
@@ -183,9 +200,11 @@ gdr_status gdn_bwd(const gdr_bf16* q, const gdr_bf16* k, const gdr_bf16* v, cons
 /* Diagnostic (no counterpart on the pages): synchronizes the current device
  * and reports whether any kernel of this library gave up a bounded wait on
  * its own asynchronous copies or tensor-core operations since the last check
- * (GDR_DEVICE_TIMEOUT; the word is then cleared), or a CUDA error occurred
- * (GDR_CUDA_ERROR).  Kernels never spin without a time limit; a kernel that
- * times out skips the dependent work, so its outputs are then incomplete. */
+ * (GDR_DEVICE_TIMEOUT; the word is then cleared), whether a backward found a
+ * saved-buffer header that does not match it (GDR_STALE_WORKSPACE, also
+ * cleared), or a CUDA error occurred (GDR_CUDA_ERROR).  Kernels never spin
+ * without a time limit; a kernel that times out skips the dependent work, so
+ * its outputs are then incomplete. */
 gdr_status gdr_check_device(void);
 
 /* Failure-detection diagnostics (no counterpart on the pages; they exist so
@@ -199,7 +218,9 @@ gdr_status gdr_check_device(void);
  * completes; after limit_ns nanoseconds (1 <= limit_ns <= 1e8, else
  * GDR_INVALID_ARG) it records the timeout in the error word and exits.
  * Device error codes: 3 forward walk, 4 backward walk, 5 this self-test,
- * 6 state-side gradient products, 7 chunk-local gradients. */
+ * 6 state-side gradient products, 7 chunk-local gradients (all reported as
+ * GDR_DEVICE_TIMEOUT); 8 a saved-buffer header that does not match the
+ * backward (reported as GDR_STALE_WORKSPACE). */
 gdr_status gdr_inject_device_error(int code);
 
 /* Host-side plan of the backward's document groups (no device work).  The
@@ -226,7 +247,7 @@ gdr_status gdr_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
  * and of the (token, value head) pairs each worked on; launches of different
  * document groups may overlap in time), in first-launch order, NUL-terminated,
  * into buf; it returns GDR_INVALID_ARG if buf_bytes is too small.  Kernel
- * names: plan, l2norm, prep, walk_fwd_sum, merge_fwd, walk_fwd, walk_bwd_sum,
+ * names: plan, check, l2norm, prep, walk_fwd_sum, merge_fwd, walk_fwd, walk_bwd_sum,
  * merge_bwd, walk_bwd, grad_state, grad, group_reduce (the _sum and merge
  * launches run only for split packs, l2norm only with qk_l2norm). */
 int gdr_profile_enable(int on);

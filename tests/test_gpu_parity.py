@@ -173,6 +173,58 @@ def test_workspace_errors_on_gpu():
                     scratch=torch.empty(1024, dtype=torch.uint8, device="cuda"))
 
 
+def _kda_small(lengths, seed):
+    x, cu, _, _ = _case("kda", lengths, 2, 2, seed=seed)
+    xd = {k: v.cuda() for k, v in x.items()}
+    return xd, torch.tensor(cu, dtype=torch.int32, device="cuda"), cu
+
+
+def test_saved_buffer_copied_to_another_address_is_accepted():
+    # The saved buffer's header travels with it: a copy at another address,
+    # unknown to the host registry, gives the same gradients.
+    import gated_delta_rule_varlen_gb300 as gdr
+    gdr.gdr_check_device()
+    xd, cu_d, cu = _kda_small([300, 77], 13)
+    args = (xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE)
+    _, _, saved = gdr.kda_fwd(*args)
+    a = gdr.kda_bwd(*args, xd["dout"], saved)
+    b = gdr.kda_bwd(*args, xd["dout"], saved.clone())
+    gdr.gdr_check_device()
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(a[name], b[name]), name
+
+
+def test_saved_buffer_overwritten_or_clobbered_is_reported():
+    import gated_delta_rule_varlen_gb300 as gdr
+    gdr.gdr_check_device()
+    xd, cu_d, cu = _kda_small([300, 77], 14)
+    args = (xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE)
+    _, _, s1 = gdr.kda_fwd(*args)
+    _, _, s2 = gdr.kda_fwd(*args)
+    # Another forward's saved buffer copied over a registered one: same
+    # problem, but the header names another forward than the one the host
+    # registry recorded for this address.
+    s1.copy_(s2)
+    gdr.kda_bwd(*args, xd["dout"], s1)
+    with pytest.raises(gdr.GdrError) as ei:
+        gdr.gdr_check_device()
+    assert ei.value.status == gdr.GDR_STALE_WORKSPACE
+    gdr.gdr_check_device()  # the report cleared the word
+    # A copy (unregistered) whose magic word was overwritten.
+    c = s2.clone()
+    c[:8] = 0
+    gdr.kda_bwd(*args, xd["dout"], c)
+    with pytest.raises(gdr.GdrError) as ei:
+        gdr.gdr_check_device()
+    assert ei.value.status == gdr.GDR_STALE_WORKSPACE
+    # The registered, untouched buffer still works, and the context is usable.
+    ref = run_gpu("kda", {k: v.cpu() for k, v in xd.items()}, cu)
+    good = gdr.kda_bwd(*args, xd["dout"], s2)
+    gdr.gdr_check_device()
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(good[name], ref[name]), name
+
+
 def test_ckpt_sequence_matches_plain_backward():
     # ckpt = forward (no save), forward (save), backward: same results as forward + backward.
     import gated_delta_rule_varlen_gb300 as gdr
