@@ -455,6 +455,20 @@ bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [T][H][128] BF16 tensor (q, k or v) read one head at a time: boxes of 64
+// channels x 1 head x 64 tokens, 128-byte swizzle (zero fill past T).
+bool bf16_head_map(CUtensorMap* map, const void* base, uint64_t T, uint64_t H) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {DK, H, T};
+  cuuint64_t strides[2] = {DK * 2, H * DK * 2};
+  cuuint32_t box[3] = {64, 1, CH};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Device error word: a kernel whose bounded wait runs out writes a non-zero
 // code here (and skips the work that depended on the wait).
 // One warp waits on a barrier that nothing completes, with the walks' bounded
@@ -703,6 +717,15 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   pa.gam = at<float>(base, L.gam);
   pa.amat = save_for_bwd ? at<float>(base, L.amat) : nullptr;
   pa.tmat = save_for_bwd ? at<float>(base, L.tmat) : nullptr;
+  // Grouped GDN: the tensor-core prep (one CTA per chunk and Q/K head) reads
+  // q, k, v through tensor maps.
+  PrepTcArgs pt{};
+  if (!vec && T > 0) {
+    pt.err = device_error_ptr();
+    if (!pt.err || !bf16_head_map(&pt.q_map, pa.q, T, Hqk) || !bf16_head_map(&pt.k_map, pa.k, T, Hqk) ||
+        !bf16_head_map(&pt.v_map, pa.v, T, HV))
+      return GDR_CUDA_ERROR;
+  }
   WalkArgs wa{};
   wa.segs = segs;
   wa.HV = HV;
@@ -747,7 +770,12 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
       wa.seg_base = ma.seg_base = (int)G.s0;
       {
         ProfScope ps("prep", ls, units);
-        st = cuda_status(launch_prep(pa, (int)(G.c1 - G.c0), vec, vec, ls));
+        if (vec) {
+          st = cuda_status(launch_prep(pa, (int)(G.c1 - G.c0), true, true, ls));
+        } else {
+          pt.p = pa;
+          st = cuda_status(launch_prep_gdn(pt, (int)(G.c1 - G.c0), ls));
+        }
       }
       if (st != GDR_OK) break;
       if (G.split) {

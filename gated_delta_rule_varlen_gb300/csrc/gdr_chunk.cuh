@@ -239,8 +239,9 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk, bool scaled
 //   T_IJ = -T_II * diag(beta_I) * sum_{K=J}^{I-1} At_IK T_KJ,
 // which needs only blocks of those columns that the same warp made before,
 // so the off-diagonal part synchronizes within the warp only.
-template <typename ET, int LG>
-__device__ void invert(ChunkSmemT<ET, LG>& s) {
+// At, T: [64][LDS] shared tiles; beta: [64]; tmp: 6 x 128 floats of scratch.
+__device__ __forceinline__ void invert_tiles(const float* __restrict__ At, float* __restrict__ T,
+                                             const float* __restrict__ beta, float* __restrict__ tmp_all) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   if (warp < 4 && lane < 16) {
     const int i0 = warp * 16, j = lane;
@@ -248,54 +249,59 @@ __device__ void invert(ChunkSmemT<ET, LG>& s) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       float acc = (i == j) ? 1.f : 0.f;
-      const float bi = s.beta[i0 + i];
+      const float bi = beta[i0 + i];
 #pragma unroll
-      for (int m = 0; m < i; ++m) acc -= bi * s.At[(i0 + i) * LDS + i0 + m] * x[m];
+      for (int m = 0; m < i; ++m) acc -= bi * At[(i0 + i) * LDS + i0 + m] * x[m];
       x[i] = acc;
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) s.T[(i0 + i) * LDS + i0 + j] = x[i];
+    for (int i = 0; i < 16; ++i) T[(i0 + i) * LDS + i0 + j] = x[i];
   }
   // Zero the strictly upper blocks.
   for (int e = tid; e < CH * CH; e += blockDim.x) {
     const int i = e >> 6, j = e & 63;
-    if ((j >> 4) > (i >> 4)) s.T[i * LDS + j] = 0.f;
+    if ((j >> 4) > (i >> 4)) T[i * LDS + j] = 0.f;
   }
   __syncthreads();
   if ((warp & 3) < 3) {
     const int J = warp & 3, r = lane >> 1, q4 = (lane & 1) * 4;
     const int cw = 8 * (warp >> 2);          // column offset of this warp inside block J
     const int cb = 16 * J + cw + q4;         // this lane's first column
-    float* tmp = s.tmp + ((warp >> 2) * 3 + J) * 128;  // [16][8]: diag(beta_I) sum_K At_IK T_KJ
+    float* tmp = tmp_all + ((warp >> 2) * 3 + J) * 128;  // [16][8]: diag(beta_I) sum_K At_IK T_KJ
     for (int I = J + 1; I < 4; ++I) {
       const int row = 16 * I + r;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
       for (int k = 16 * J; k < 16 * I; ++k) {
-        const float av = s.At[row * LDS + k];
-        const float4 tv = *reinterpret_cast<const float4*>(&s.T[k * LDS + cb]);
+        const float av = At[row * LDS + k];
+        const float4 tv = *reinterpret_cast<const float4*>(&T[k * LDS + cb]);
         acc[0] += av * tv.x;
         acc[1] += av * tv.y;
         acc[2] += av * tv.z;
         acc[3] += av * tv.w;
       }
-      const float bi = s.beta[row];
+      const float bi = beta[row];
       *reinterpret_cast<float4*>(&tmp[r * 8 + q4]) = make_float4(bi * acc[0], bi * acc[1], bi * acc[2], bi * acc[3]);
       __syncwarp();
       float out[4] = {0.f, 0.f, 0.f, 0.f};
       for (int m = 0; m <= r; ++m) {
-        const float tv = s.T[row * LDS + 16 * I + m];
+        const float tv = T[row * LDS + 16 * I + m];
         const float4 x = *reinterpret_cast<const float4*>(&tmp[m * 8 + q4]);
         out[0] += tv * x.x;
         out[1] += tv * x.y;
         out[2] += tv * x.z;
         out[3] += tv * x.w;
       }
-      *reinterpret_cast<float4*>(&s.T[row * LDS + cb]) = make_float4(-out[0], -out[1], -out[2], -out[3]);
+      *reinterpret_cast<float4*>(&T[row * LDS + cb]) = make_float4(-out[0], -out[1], -out[2], -out[3]);
       __syncwarp();
     }
   }
   __syncthreads();
+}
+
+template <typename ET, int LG>
+__device__ void invert(ChunkSmemT<ET, LG>& s) {
+  invert_tiles(s.At, s.T, s.beta, s.tmp);
 }
 
 // Two left applies that share Y: Z0_i += sum_{j<=i} M0_ij Y_j exp(gc_i - gc_j),

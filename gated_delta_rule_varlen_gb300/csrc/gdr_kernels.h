@@ -30,6 +30,16 @@ struct PrepArgs {
   int chunk_base;      // block x works on chunk chunk_base + x
 };
 
+// The tensor-core prep of grouped GDN (one CTA per (chunk, Q/K head), all
+// value heads of the group): the prep's arguments plus 3-D BF16 tensor maps
+// of q, k ([T][Hqk][128]) and v ([T][HV][128]), boxes of 64 channels x 1 head
+// x 64 tokens, 128-byte swizzle.
+struct PrepTcArgs {
+  PrepArgs p;
+  CUtensorMap q_map, k_map, v_map;
+  int* err;  // device error word (bounded waits)
+};
+
 struct WalkArgs {
   // 2-D FP32 tensor maps (rows x columns, row pitch), 32-column boxes, 128-byte swizzle:
   CUtensorMap w_map;    // w        [NC*HV*64][128], pitch LDT, 32 x 64 boxes
@@ -140,6 +150,7 @@ struct L2NormArgs {
 };
 
 cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
+cudaError_t launch_prep_gdn(const PrepTcArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_walk_fwd_v(const WalkArgs& a, int nsegs, cudaStream_t st);
 cudaError_t launch_merge(const MergeArgs& a, int nsegs, bool backward, cudaStream_t st);
 cudaError_t launch_walk_bwd_v(const WalkBwdArgs& a, int nsegs, cudaStream_t st);

@@ -218,9 +218,9 @@ gdr_status gdr_check_device(void);
  * completes; after limit_ns nanoseconds (1 <= limit_ns <= 1e8, else
  * GDR_INVALID_ARG) it records the timeout in the error word and exits.
  * Device error codes: 3 forward walk, 4 backward walk, 5 this self-test,
- * 6 state-side gradient products, 7 chunk-local gradients (all reported as
- * GDR_DEVICE_TIMEOUT); 8 a saved-buffer header that does not match the
- * backward (reported as GDR_STALE_WORKSPACE). */
+ * 6 state-side gradient products, 7 chunk-local gradients, 9 the grouped-GDN
+ * prep (all reported as GDR_DEVICE_TIMEOUT); 8 a saved-buffer header that
+ * does not match the backward (reported as GDR_STALE_WORKSPACE). */
 gdr_status gdr_inject_device_error(int code);
 
 /* Host-side plan of the backward's document groups (no device work).  The
