@@ -80,8 +80,8 @@ class Workload:
 def workload(name: str) -> Workload:
     """The named workloads: kda_tiny, kda_pack_h4, kda_pack_h16, kda_pack_h64,
     gdn_p1 (241817 tokens / 6 docs), gdn_1doc (32768 tokens / 1 doc), and the
-    profiling-size cases kda_prof (4 x 16384 tokens, H = 4) and kda_prof16
-    (4 x 4096 tokens, H = 16)."""
+    profiling-size cases kda_prof (4 x 16384 tokens, H = 4), kda_prof16
+    (4 x 4096 tokens, H = 16) and gdn_prof (2 x 4096 tokens, (16, 48))."""
     if name == "kda_tiny":
         return Workload(name, "kda", (512,), 1, 1)
     if name == "kda_prof":  # profiling-size pack: 4 x 16384 tokens, H = 4 (inputs > L2, a few GB in all)
@@ -95,6 +95,8 @@ def workload(name: str) -> Workload:
         return Workload(name, "gdn", tuple(random_pack_lengths(GDN_P1_TOKENS, GDN_P1_DOCS, 0)), 16, 48)
     if name == "gdn_1doc":
         return Workload(name, "gdn", (GDN_1DOC_TOKENS,), 16, 48)
+    if name == "gdn_prof":  # profiling-size grouped pack: 2 x 4096 tokens, (Hqk, HV) = (16, 48)
+        return Workload(name, "gdn", (4096,) * 2, 16, 48)
     raise KeyError(name)
 
 
