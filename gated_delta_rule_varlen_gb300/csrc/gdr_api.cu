@@ -286,12 +286,12 @@ Layout make_layout(int64_t T, int64_t NC, int32_t N, int32_t Hqk, int32_t HV, bo
   L.smap = take(segstate);    // each split segment's state map (the backward merge needs it too)
   L.sstart = take(segstate);  // start state of each segment
   L.sbias = take(segstate);   // each segment's end state from a zero start
-  L.w = take((size_t)NC * HV * CH * LDT * sizeof(float));
+  L.w = take((size_t)NC * HV * CH * DK * sizeof(__half));
   L.u = take((size_t)NC * HV * CH * LDF * sizeof(float));
-  L.qp = take((size_t)NC * HV * CH * LDF * sizeof(float));
-  L.kd = take((size_t)NC * HV * DK * LDS * sizeof(float));
+  L.qp = take((size_t)NC * HV * CH * DK * sizeof(__half));
+  L.kd = take((size_t)NC * HV * DK * CH * sizeof(__half));
   L.delta = take(tile);
-  L.aqk = take((size_t)NC * HV * CH * LDS * sizeof(float));
+  L.aqk = take((size_t)NC * HV * CH * CH * sizeof(__half));
   L.amat = take((size_t)NC * HV * CH * LDS * sizeof(float));
   L.tmat = take((size_t)NC * HV * CH * LDS * sizeof(float));
   L.gam = take(vec);
@@ -451,6 +451,19 @@ bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
   cuuint32_t box[2] = {32, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// rows x cols dense FP16 tensor; boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool fp16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -709,11 +722,11 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   pa.chunks = chunks;
   pa.Hqk = Hqk;
   pa.HV = HV;
-  pa.w = at<float>(base, L.w);
+  pa.w = at<__half>(base, L.w);
   pa.u = at<float>(base, L.u);
-  pa.qp = at<float>(base, L.qp);
-  pa.kd = at<float>(base, L.kd);
-  pa.aqk = at<float>(base, L.aqk);
+  pa.qp = at<__half>(base, L.qp);
+  pa.kd = at<__half>(base, L.kd);
+  pa.aqk = at<__half>(base, L.aqk);
   pa.gam = at<float>(base, L.gam);
   pa.amat = save_for_bwd ? at<float>(base, L.amat) : nullptr;
   pa.tmat = save_for_bwd ? at<float>(base, L.tmat) : nullptr;
@@ -743,11 +756,11 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   wa.gam = pa.gam;
   wa.err = device_error_ptr();
   if (!wa.err) return GDR_CUDA_ERROR;
-  if (NC > 0 && (!fp32_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, LDT, CH) ||
-                 !fp32_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, LDS, DK) ||
+  if (NC > 0 && (!fp16_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, CH) ||
+                 !fp16_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, DK) ||
                  !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, LDF, CH) ||
-                 !fp32_map(&wa.qp_map, pa.qp, (uint64_t)NC * HV * CH, DK, LDF, CH) ||
-                 !fp32_map(&wa.aqk_map, pa.aqk, (uint64_t)NC * HV * CH, CH, LDS, CH)))
+                 !fp16_map(&wa.qp_map, pa.qp, (uint64_t)NC * HV * CH, DK, CH) ||
+                 !fp16_map(&wa.aqk_map, pa.aqk, (uint64_t)NC * HV * CH, CH, CH)))
     return GDR_CUDA_ERROR;
   wa.h0 = h0;
   // The state tape and Delta are only kept for a backward.
@@ -861,10 +874,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   mb.state = wb.dsend;
   mb.bias = wb.dsbias;
   wb.scale = scale;
-  wb.w = at<float>(saved, L.w);
-  wb.qp = at<float>(saved, L.qp);
-  wb.kd = at<float>(saved, L.kd);
-  wb.aqk = at<float>(saved, L.aqk);
+  const __half* sw = at<__half>(saved, L.w);
   wb.gam = at<float>(saved, L.gam);
   wb.dout = static_cast<const __nv_bfloat16*>(dout);
   wb.dht = dht;
@@ -873,10 +883,10 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   wb.dh0 = dh0;
   wb.err = device_error_ptr();
   if (!wb.err) return GDR_CUDA_ERROR;
-  if (NC > 0 && (!fp32_map(&wb.w_map, wb.w, (uint64_t)NC * HV * CH, DK, LDT, CH) ||
-                 !fp32_map(&wb.kdt_map, wb.kd, (uint64_t)NC * HV * DK, CH, LDS, DK) ||
-                 !fp32_map(&wb.qp_map, wb.qp, (uint64_t)NC * HV * CH, DK, LDF, CH) ||
-                 !fp32_map(&wb.aqk_map, wb.aqk, (uint64_t)NC * HV * CH, CH, LDS, CH)))
+  if (NC > 0 && (!fp16_map(&wb.w_map, sw, (uint64_t)NC * HV * CH, DK, CH) ||
+                 !fp16_map(&wb.kdt_map, at<__half>(saved, L.kd), (uint64_t)NC * HV * DK, CH, DK) ||
+                 !fp16_map(&wb.qp_map, at<__half>(saved, L.qp), (uint64_t)NC * HV * CH, DK, CH) ||
+                 !fp16_map(&wb.aqk_map, at<__half>(saved, L.aqk), (uint64_t)NC * HV * CH, CH, CH)))
     return GDR_CUDA_ERROR;
 
   GradStateArgs gs{};
@@ -909,11 +919,9 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   ga.Hqk = Hqk;
   ga.HV = HV;
   ga.scale = scale;
-  ga.w = wb.w;
+  ga.w = sw;
   ga.u = at<float>(saved, L.u);
-  ga.kd = wb.kd;
   ga.gam = wb.gam;
-  ga.aqk = wb.aqk;
   ga.delta = gs.delta;
   ga.ddelta = wb.ddelta;
   ga.dqs = gs.dqs;

@@ -336,14 +336,16 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   }
   __syncthreads();
   // w and u (B operands of dA) into the staging tiles: u by one bulk copy, w
-  // (stored with the backward walk's pitch) by cp.async.
+  // (FP16, dense rows) by cp.async into the dw staging tile, which X no longer
+  // reads, as FP16 rows 136 elements apart.
   if (tid == 0) {
     tc::mbar_arrive_expect_tx(&sg.bar_u, CH * LDF * 4);
     tc::bulk_load(sg.dG, &a.u[fo], CH * LDF * 4, &sg.bar_u);
   }
-  for (int e = tid; e < CH * DK / 4; e += NTH) {
-    const int i = e >> 5, c4 = (e & 31) * 4;
-    cp_async16(&sg.dK[i * LDF + c4], &a.w[w_off(chunk, h, a.HV) + i * LDT + c4]);
+  __half* const wsh = reinterpret_cast<__half*>(sg.dK);
+  for (int e = tid; e < CH * DK / 8; e += NTH) {
+    const int i = e >> 4, c8 = (e & 15) * 8;
+    cp_async16(&wsh[i * LDF + c8], &a.w[w_off(chunk, h, a.HV) + i * DK + c8]);
   }
   cp_async_commit();
   // Partial dA over this warp's channels: X w^T + Y u^T.
@@ -358,7 +360,6 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     return;
   }
   {
-    const float* w = sg.dK;
     const float* u = sg.dG;
 #pragma unroll
     for (int kk = 0; kk < NT; ++kk) {
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
       for (int nt = 0; nt < 8; ++nt) {
         if (nt < 2 * I + 2) {
           const int j = nt * 8 + g;
-          const float2 wv = *reinterpret_cast<const float2*>(&w[j * LDF + cc]);
+          const float2 wv = __half22float2(*reinterpret_cast<const __half2*>(&wsh[j * LDF + cc]));
           const float2 uv = *reinterpret_cast<const float2*>(&u[j * LDF + cc]);
           uint32_t bw[2] = {__float_as_uint(wv.x), __float_as_uint(wv.y)};
           uint32_t bu[2] = {__float_as_uint(uv.x), __float_as_uint(uv.y)};

@@ -136,12 +136,12 @@ __device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restric
 // Per-channel gates use the block factorization described in gdr_common.cuh.
 // The upper channel half leaves its partial sums in s.At and s.T (free until
 // the inverse); the lower half adds them in, masks, and writes the results.
-// Aqk is stored rounded to TF32 (it is only ever an MMA operand), rows LDS apart.
+// Aqk is stored in FP16 (it is only ever an MMA operand), dense rows of 64.
 // With `scaled` (in-kernel L2 normalization: the tiles hold the raw q, k and
 // s.rq, s.rk their rows' scales) the results are those of the normalized
 // rows: At[i][j] rk_i rk_j and Aqk[i][j] rq_i rk_j, in FP32.
 template <bool VEC, typename ET, int LG>
-__device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk, bool scaled = false) {
+__device__ void gram(ChunkSmemT<ET, LG>& s, __half* __restrict__ aqk, bool scaled = false) {
   const int warp = threadIdx.x >> 5, I = warp & 3, hk = warp >> 2, i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const int ra = i0 + g, rb = i0 + g + 8;
@@ -225,7 +225,7 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, float* __restrict__ aqk, bool scaled
           }
         }
         s.At[row * LDS + col] = vK;
-        aqk[row * LDS + col] = __uint_as_float(tf32(vQ));
+        aqk[row * CH + col] = __float2half_rn(vQ);
       }
   }
   __syncthreads();

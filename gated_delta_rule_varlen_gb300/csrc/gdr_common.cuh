@@ -33,6 +33,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace gdr {
@@ -193,13 +194,14 @@ __device__ __forceinline__ size_t tile_off(int chunk, int h, int HV) {  // [NC][
 __device__ __forceinline__ size_t state_off(int chunk, int h, int HV) { // [NC][HV][128][128]
   return ((size_t)chunk * HV + h) * (DK * DK);
 }
-// Saved tiles that the walks copy whole are kept in HBM with the padded row
-// pitch of their shared-memory copies, so that one bulk copy moves a tile:
-//   w [64][LDT],  Q Gamma [64][LDF],  Kd^T [128][LDS],  Aqk [64][LDS].
-__device__ __forceinline__ size_t w_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDT); }
-__device__ __forceinline__ size_t qp_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDF); }
-__device__ __forceinline__ size_t kd_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (DK * LDS); }
-__device__ __forceinline__ size_t aqk_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDS); }
+// The walks' operand tiles, FP16 with dense rows (element offsets): w [64][128],
+// Q Gamma [64][128], Kd^T [128][64], Aqk [64][64].  They depend on q, k, g
+// and beta only, so their entries are of order one; FP16 keeps the 11-bit
+// significand the TF32 products use.
+__device__ __forceinline__ size_t w_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * DK); }
+__device__ __forceinline__ size_t qp_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * DK); }
+__device__ __forceinline__ size_t kd_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (DK * CH); }
+__device__ __forceinline__ size_t aqk_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * CH); }
 // Tiles the gradient kernel moves whole keep its pitches too: u, dw, dDelta
 // [64][LDF]; At, T, dAqk [64][LDS].
 __device__ __forceinline__ size_t tf_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDF); }

@@ -42,29 +42,30 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
     }
   }
   // Qp, Kd, gamma (elementwise; factors exp(gc) and exp(gc_last - gc) are <= 1).
-  // Qp and Kd are only ever MMA operands: stored rounded to TF32.
+  // Qp and Kd are only ever MMA operands: stored in FP16.
   const size_t toff = tile_off(chunk, h, a.HV);
-  for (int e = tid; e < CH * DK / 4; e += blockDim.x) {  // four channels per thread, one 16-byte store
+  for (int e = tid; e < CH * DK / 4; e += blockDim.x) {  // four channels per thread, one 8-byte store
     const int i = e >> 5, d = (e & 31) * 4;
     float r[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float gl = VEC ? s.G[i * LDT + d + q] : s.gs[i];
-      r[q] = __uint_as_float(tf32(s.q(i, d + q) * (scaled ? s.rq[i] : 1.f) * ex2(gl)));
+      r[q] = s.q(i, d + q) * (scaled ? s.rq[i] : 1.f) * ex2(gl);
       if (i == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d + q] = ex2(VEC ? s.G[(CH - 1) * LDT + d + q] : s.gs[CH - 1]);
     }
-    *reinterpret_cast<float4*>(&a.qp[qp_off(chunk, h, a.HV) + i * LDF + d]) = make_float4(r[0], r[1], r[2], r[3]);
+    const __half2 p0 = __floats2half2_rn(r[0], r[1]), p1 = __floats2half2_rn(r[2], r[3]);
+    *reinterpret_cast<uint2*>(&a.qp[qp_off(chunk, h, a.HV) + i * DK + d]) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1));
   }
   // Kd stored transposed, [c][j] (the K-major A operand of the walk's state update).
   // A warp covers rows i = 8k .. 8k+7 of channels d .. d+3 (lane bits 0-2 -> i,
-  // 3-4 -> d): shared reads are conflict-free, each 8-lane group writes 32 bytes.
+  // 3-4 -> d): shared reads are conflict-free, each 8-lane group writes 16 bytes.
   for (int e = tid; e < CH * DK; e += blockDim.x) {
     const int l = e & 31, w = e >> 5;
     const int i = (l & 7) + 8 * (w & 7), d = 4 * (w >> 3) + (l >> 3);
     const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
     const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
-    a.kd[kd_off(chunk, h, a.HV) + d * LDS + i] =
-        __uint_as_float(tf32(s.k(i, d) * (scaled ? s.rk[i] : 1.f) * ex2(glast - gl)));
+    a.kd[kd_off(chunk, h, a.HV) + d * CH + i] = __float2half_rn(s.k(i, d) * (scaled ? s.rk[i] : 1.f) * ex2(glast - gl));
   }
   __syncthreads();
   // Q tile <- v rows (async), G tile <- beta * K * Gamma (B of w).
@@ -90,8 +91,8 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   {
     const int prod = warp >> 2, q = warp & 3, c0 = 64 * (q & 1);
     const int Ia = (q >> 1) ? 2 : 3, Ib = 3 - Ia;
-    float* out = prod ? a.u + tf_off(chunk, h, a.HV) : a.w + w_off(chunk, h, a.HV);
-    const int ldo = prod ? LDF : LDT;
+    float* uo = a.u + tf_off(chunk, h, a.HV);
+    __half* wo = a.w + w_off(chunk, h, a.HV);
     auto bw = [&](int j, int c) { return s.G[j * LDT + c]; };
     auto bu = [&](int j, int c) { return s.beta[j] * s.q(j, c); };
 #pragma unroll
@@ -107,14 +108,19 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
           mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
                        [&](int j, int c) { return bw(j, c0 + c); });
       }
-      {  // rows i0 + g (+8), channel pairs c0 + 8 nt + 2 t: 8-byte stores
+      {  // rows i0 + g (+8), channel pairs c0 + 8 nt + 2 t: u as TF32-rounded FP32 pairs, w as FP16 pairs
         const int lane = lane_id(), g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-          for (int hr = 0; hr < 2; ++hr)
-            *reinterpret_cast<float2*>(&out[(i0 + g + 8 * hr) * ldo + c0 + nt * 8 + 2 * t]) = make_float2(
-                __uint_as_float(tf32(acc[nt][2 * hr])), __uint_as_float(tf32(acc[nt][2 * hr + 1])));
+          for (int hr = 0; hr < 2; ++hr) {
+            const int row = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
+            if (prod)
+              *reinterpret_cast<float2*>(&uo[row * LDF + c]) =
+                  make_float2(__uint_as_float(tf32(acc[nt][2 * hr])), __uint_as_float(tf32(acc[nt][2 * hr + 1])));
+            else
+              *reinterpret_cast<__half2*>(&wo[row * DK + c]) = __floats2half2_rn(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+          }
       }
     }
   }
@@ -198,9 +204,11 @@ __device__ __forceinline__ void build_a(PrepGdnSmem& s, const float* __restrict_
   }
 }
 
-// The M = 64 accumulator at TMEM column 128 (w or u) -> rows of `out` (pitch
-// ld), rounded to TF32.  Warp (quadrant, half): rows 16 quad .., channels 64 half ..
-__device__ __forceinline__ void drain_wu(uint32_t tmem, float* __restrict__ out, int ld) {
+// The M = 64 accumulator at TMEM column 128 (w or u) -> rows of `out`: u
+// rounded to TF32 (pitch LDF), w in FP16 (dense rows).  Warp (quadrant,
+// half): rows 16 quad .., channels 64 half ..
+template <typename OT>
+__device__ __forceinline__ void drain_wu(uint32_t tmem, OT* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const int quad = warp & 3, hf = warp >> 2, g = lane >> 2, u2 = (lane & 3) * 2;
   const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + 128 + 64 * hf;
@@ -214,9 +222,12 @@ __device__ __forceinline__ void drain_wu(uint32_t tmem, float* __restrict__ out,
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int row = 16 * quad + g + 8 * hr, c = 64 * hf + cb + 8 * q + u2;
-        *reinterpret_cast<float2*>(&out[row * ld + c]) =
-            make_float2(__uint_as_float(tf32(__uint_as_float(rr[4 * q + 2 * hr]))),
-                        __uint_as_float(tf32(__uint_as_float(rr[4 * q + 2 * hr + 1]))));
+        const float x0 = __uint_as_float(rr[4 * q + 2 * hr]), x1 = __uint_as_float(rr[4 * q + 2 * hr + 1]);
+        if constexpr (sizeof(OT) == 4)
+          *reinterpret_cast<float2*>(&out[row * LDF + c]) =
+              make_float2(__uint_as_float(tf32(x0)), __uint_as_float(tf32(x1)));
+        else
+          *reinterpret_cast<__half2*>(&out[row * DK + c]) = __floats2half2_rn(x0, x1);
       }
   }
 }
@@ -333,7 +344,8 @@ __global__ void __launch_bounds__(256, 2) k_prep_gdn(const __grid_constant__ Pre
       const int qd = warp & 3, hf = warp >> 2, i = 32 * (qd & 1) + lane;
       const bool isq = qd >= 2;
       const float gi = s.gs[i], ri = isq ? s.rq[i] : s.rk[i];
-      float* dst = isq ? a.aqk + aqk_off(chunk, h, a.HV) + i * LDS : s.At + i * LDS;
+      __half* aq_row = a.aqk + aqk_off(chunk, h, a.HV) + i * CH;
+      float* at_row = s.At + i * LDS;
 #pragma unroll 1
       for (int j0 = 32 * hf; j0 < 32 * hf + 32; j0 += 16) {
         uint32_t v[16];
@@ -347,9 +359,15 @@ __global__ void __launch_bounds__(256, 2) k_prep_gdn(const __grid_constant__ Pre
             const int j = j0 + j4 + q;
             const bool keep = isq ? j <= i : j < i;
             const float x = ((__uint_as_float(v[j4 + q]) * ex2(gi - s.gs[j])) * ri) * s.rk[j];
-            o[q] = keep ? (isq ? __uint_as_float(tf32(x)) : x) : 0.f;
+            o[q] = keep ? x : 0.f;
           }
-          *reinterpret_cast<float4*>(dst + j0 + j4) = make_float4(o[0], o[1], o[2], o[3]);
+          if (isq) {
+            const __half2 p0 = __floats2half2_rn(o[0], o[1]), p1 = __floats2half2_rn(o[2], o[3]);
+            *reinterpret_cast<uint2*>(aq_row + j0 + j4) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1));
+          } else {
+            *reinterpret_cast<float4*>(at_row + j0 + j4) = make_float4(o[0], o[1], o[2], o[3]);
+          }
         }
       }
     }
@@ -374,27 +392,27 @@ __global__ void __launch_bounds__(256, 2) k_prep_gdn(const __grid_constant__ Pre
     }
     ++m_issued;
     // While it runs: Q Gamma and Kd^T.
-    for (int e = tid; e < CH * DK / 4; e += 256) {  // four channels per thread, one 16-byte store
+    for (int e = tid; e < CH * DK / 4; e += 256) {  // four channels per thread, one 8-byte store
       const int i = e >> 5, d = (e & 31) * 4;
       const uint2 raw = *reinterpret_cast<const uint2*>(kq + sw_elem(CH + i, d, KQ_BLOCK));
       const float f = s.rq[i] * s.gm[i];
       const float x0 = __uint_as_float(raw.x << 16), x1 = __uint_as_float(raw.x & 0xffff0000u);
       const float x2 = __uint_as_float(raw.y << 16), x3 = __uint_as_float(raw.y & 0xffff0000u);
-      *reinterpret_cast<float4*>(&a.qp[qp_off(chunk, h, a.HV) + i * LDF + d]) =
-          make_float4(__uint_as_float(tf32(x0 * f)), __uint_as_float(tf32(x1 * f)), __uint_as_float(tf32(x2 * f)),
-                      __uint_as_float(tf32(x3 * f)));
+      const __half2 p0 = __floats2half2_rn(x0 * f, x1 * f), p1 = __floats2half2_rn(x2 * f, x3 * f);
+      *reinterpret_cast<uint2*>(&a.qp[qp_off(chunk, h, a.HV) + i * DK + d]) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1));
     }
     for (int e = tid; e < CH * DK; e += 256) {  // Kd^T [c][j]: lanes 0-7 rows, 8-lane groups channels
       const int l = e & 31, wq = e >> 5;
       const int i = (l & 7) + 8 * (wq & 7), d = 4 * (wq >> 3) + (l >> 3);
       const uint16_t raw = *reinterpret_cast<const uint16_t*>(kq + sw_elem(i, d, KQ_BLOCK));
-      a.kd[kd_off(chunk, h, a.HV) + d * LDS + i] = __uint_as_float(tf32(bfbits2f(raw) * s.rk[i] * s.ed[i]));
+      a.kd[kd_off(chunk, h, a.HV) + d * CH + i] = __float2half_rn(bfbits2f(raw) * s.rk[i] * s.ed[i]);
     }
     ok = __syncthreads_and(tc::mbar_wait(&s.bar_m, 0));
     ++m_waited;
     tc::tc_fence_after();
     if (!ok) break;
-    drain_wu(tmem, a.w + w_off(chunk, h, a.HV), LDT);
+    drain_wu(tmem, a.w + w_off(chunk, h, a.HV));
     tc::tc_fence_before();
     __syncthreads();
     // u = (T diag(beta)) V.
@@ -443,7 +461,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_gdn(const __grid_constant__ Pre
       }
       ++v_issued;
     }
-    drain_wu(tmem, a.u + tf_off(chunk, h, a.HV), LDF);
+    drain_wu(tmem, a.u + tf_off(chunk, h, a.HV));
     tc::tc_fence_before();
     __syncthreads();
   }

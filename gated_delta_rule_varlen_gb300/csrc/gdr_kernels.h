@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace gdr {
@@ -21,7 +22,8 @@ struct PrepArgs {
   const void* beta;  // bf16 (KDA) or fp32 (GDN)
   const ChunkDesc* chunks;
   int Hqk, HV;
-  float *w, *u, *qp, *kd, *aqk, *gam;  // w, qp, kd, aqk with the padded pitches of gdr_common.cuh
+  __half *w, *qp, *kd, *aqk;  // FP16, dense rows (gdr_common.cuh)
+  float *u, *gam;             // u with the padded pitch LDF
   float *amat, *tmat;  // At and T per chunk ([64][64] FP32), or null when nothing is saved
   // In-kernel q/k L2 normalization (else null): the scales r [T][Hqk] of q and
   // k's rows; q and k are then the raw inputs and every product takes the
@@ -41,12 +43,13 @@ struct PrepTcArgs {
 };
 
 struct WalkArgs {
-  // 2-D FP32 tensor maps (rows x columns, row pitch), 32-column boxes, 128-byte swizzle:
-  CUtensorMap w_map;    // w        [NC*HV*64][128], pitch LDT, 32 x 64 boxes
-  CUtensorMap kdt_map;  // Kd^T     [NC*HV*128][64], pitch LDS, 32 x 128 boxes
-  CUtensorMap u_map;    // u        [NC*HV*64][128], pitch 128, 32 x 64 boxes
-  CUtensorMap qp_map;   // Q Gamma  [NC*HV*64][128], pitch LDF, 32 x 64 boxes
-  CUtensorMap aqk_map;  // Aqk      [NC*HV*64][64],  pitch LDS, 32 x 64 boxes
+  // 2-D tensor maps (rows x columns), 128-byte swizzle: the FP16 operand
+  // tiles in boxes of 64 columns, u (FP32) in boxes of 32 columns.
+  CUtensorMap w_map;    // w        [NC*HV*64][128] FP16, 64 x 64 boxes
+  CUtensorMap kdt_map;  // Kd^T     [NC*HV*128][64] FP16, 64 x 128 boxes
+  CUtensorMap u_map;    // u        [NC*HV*64][128] FP32, pitch LDF, 32 x 64 boxes
+  CUtensorMap qp_map;   // Q Gamma  [NC*HV*64][128] FP16, 64 x 64 boxes
+  CUtensorMap aqk_map;  // Aqk      [NC*HV*64][64]  FP16, 64 x 64 boxes
   const SegDesc* segs;  // walk segments, the longest document's first
   int HV;
   const float *u, *gam;
@@ -67,12 +70,12 @@ struct WalkArgs {
 
 
 struct WalkBwdArgs {
-  // The saved tiles as the forward reads them (FP32, 32-column boxes, 128-byte swizzle):
+  // The saved FP16 tiles as the forward walk reads them (64-column boxes, 128-byte swizzle):
   CUtensorMap w_map, kdt_map, qp_map, aqk_map;
   const SegDesc* segs;
   int HV;
   float scale;
-  const float *w, *qp, *kd, *aqk, *gam;
+  const float* gam;
   const __nv_bfloat16* dout;  // [T][HV][128]
   const float* dht;           // [N][HV][128][128] or null
   __nv_bfloat16* dstape;      // dS (adjoint of each chunk's end state), BF16
@@ -116,7 +119,8 @@ struct GradArgs {
   const ChunkDesc* chunks;
   int Hqk, HV;
   float scale;
-  const float *w, *u, *kd, *gam, *aqk, *delta, *ddelta;
+  const __half* w;  // FP16 [64][128] per chunk
+  const float *u, *gam, *delta, *ddelta;
   const float *dqs, *dw, *dkd, *dgam, *daqk;
   const float *amat, *tmat;  // At and T of each chunk, saved by the forward
   // outputs

@@ -9,10 +9,13 @@
 // through shared memory:
 //   [P^T | O^T]  = S0'^T [w ; Qp]^T           (M = 128 value rows, N = 128, K = 128 channels)
 //   [O^T | S^T] += Delta^T [Aqk ; Kd^T]^T     (M = 128, N = 192, K = 64 tokens)
-// with S0' the state rounded to TF32 (a second TMEM copy, the operand: the
-// tensor cores truncate FP32 A operands read from tensor memory), Delta^T =
-// u^T - P^T formed by the data warps, and S^T scaled by diag(gamma) in place
-// before the second product.  Per chunk (the chunked identities in
+// as tcgen05.mma kind::f16 series: S0' is the state rounded to FP16 (a second
+// TMEM copy, two elements per 32-bit column; the FP32 state stays the
+// accumulator), the B tiles [w ; Qp] and [Aqk ; Kd^T] are the FP16 tiles the
+// prep stored, Delta^T = u^T - P^T is formed in FP32 by the data warps and
+// enters the second product as its FP16 copy Delta'^T, and S^T is scaled by
+// diag(gamma) in place before it.  FP16 keeps the 11-bit significand of TF32
+// (the operands depend on q, k, g, beta or are of the size of the values v).  Per chunk (the chunked identities in
 // gdr_common.cuh):
 //   Delta = u - w S0,   O = scale (Qp S0 + Aqk Delta),
 //   S_end = diag(gamma) S0 + Kd^T Delta.
@@ -21,10 +24,9 @@
 // description), fused, with the whole value width of a chain on one SM.
 //
 // Tensor-memory columns (512): Pd[0] 0..63, O[0] 64..127, S 128..255,
-// O[1] 256..319, Pd[1] 320..383, S' 384..511.  Chunk m uses Pd[m&1] (P, then
-// the FP32 Delta in place; its TF32 copy, the A operand of the update, goes
-// to the first 64 columns of S', which the first product no longer reads)
-// and O[m&1]: the first product writes [Pd[0] | O[0]] (even m,
+// O[1] 256..319, Pd[1] 320..383, S' 384..447 (FP16 pairs), Delta' 448..479
+// (FP16 pairs).  Chunk m uses Pd[m&1] (P, then the FP32 Delta in place) and
+// O[m&1]: the first product writes [Pd[0] | O[0]] (even m,
 // B rows [w ; Qp]) or [O[1] | Pd[1]] (odd m, B rows [Qp ; w]); the second
 // accumulates into [O[0] | S] (even, B rows [Aqk ; Kd^T]) or [S | O[1]] (odd,
 // B rows [Kd^T ; Aqk]).  O of a chunk is written out while the next chunk's
@@ -37,8 +39,8 @@
 //
 // Threads: 8 data warps (warp w: TMEM lanes 32 (w % 4) .., value rows v; warp
 // halves w / 4 split the columns) and one issuer warp (its lane 0 issues every
-// TMA copy and MMA).  Shared memory: [w ; Qp] + gamma in two stages (64 KB
-// each), [Kd^T ; Aqk] (48 KB) and u (32 KB) in one.  Waits are bounded; a
+// TMA copy and MMA).  Shared memory: [w ; Qp] + gamma in two stages (32 KB
+// each), [Kd^T ; Aqk] (24 KB) and u (32 KB) in one.  Waits are bounded; a
 // timed-out wait ends the walk for the whole CTA and sets the device error
 // word.
 #include "gdr_common.cuh"
@@ -48,19 +50,19 @@
 namespace gdr {
 
 struct WalkVSmem {
-  float B1[2][2 * CH * DK];    // per stage: 4 column blocks of 128 rows x 32 (16 KB each)
-  float B2[(DK + CH) * CH];    // 2 column blocks of 192 rows x 32 (24 KB each)
+  uint16_t B1[2][2 * CH * DK];  // per stage, FP16: 2 column blocks of 128 rows x 64 channels (16 KB each)
+  uint16_t B2[(DK + CH) * CH];  // FP16: 1 column block of 192 rows x 64 tokens
   float U[CH * DK];            // u: 4 blocks of 64 rows j x 32 value columns (128-byte swizzle)
   float gam[2][DK];            // gamma, with the B1 stage
   uint64_t bar_b1[2], bar_b2, bar_u, bar_s1, bar_s2;
   uint32_t tmem;
 };
 constexpr int WALKV_THREADS = 288;
-constexpr uint32_t WALKV_B1_BYTES = 2 * CH * DK * 4 + DK * 4;
-constexpr uint32_t WALKV_B2_BYTES = (DK + CH) * CH * 4;
+constexpr uint32_t WALKV_B1_BYTES = 2 * CH * DK * 2 + DK * 4;
+constexpr uint32_t WALKV_B2_BYTES = (DK + CH) * CH * 2;
 constexpr uint32_t WALKV_U_BYTES = CH * DK * 4;
-constexpr uint32_t kColS = 128, kColSp = 384;
-constexpr uint32_t kColDl = 384;  // TF32 Delta: the first 64 columns of S', free once [P | O] is done
+constexpr uint32_t kColS = 128, kColSp = 384;  // S (FP32), S' (FP16 pairs)
+constexpr uint32_t kColDl = 448;                // Delta' (FP16 pairs)
 __device__ __forceinline__ uint32_t colPd(int b) { return b ? 320u : 0u; }   // P, then Delta, of parity b
 __device__ __forceinline__ uint32_t colO(int b) { return b ? 256u : 64u; }   // O of parity b
 __device__ __forceinline__ uint32_t colD1(int b) { return b ? 256u : 0u; }   // D of [P | O] / [O | P]
@@ -131,9 +133,9 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
     unsigned char* base = reinterpret_cast<unsigned char*>(s.B1[b]);
     const int wr = b ? 64 : 0, qr = b ? 0 : 64;
     tc::mbar_arrive_expect_tx(&s.bar_b1[b], WALKV_B1_BYTES);
-    for (int kb = 0; kb < 4; ++kb) {
-      tc::tma_load_2d(base + kb * 16384 + wr * 128, &a.w_map, kb * 32, item * CH, &s.bar_b1[b]);
-      tc::tma_load_2d(base + kb * 16384 + qr * 128, &a.qp_map, kb * 32, item * CH, &s.bar_b1[b]);
+    for (int kb = 0; kb < 2; ++kb) {
+      tc::tma_load_2d(base + kb * 16384 + wr * 128, &a.w_map, kb * 64, item * CH, &s.bar_b1[b]);
+      tc::tma_load_2d(base + kb * 16384 + qr * 128, &a.qp_map, kb * 64, item * CH, &s.bar_b1[b]);
     }
     tc::bulk_load(s.gam[b], &a.gam[(size_t)item * DK], DK * 4, &s.bar_b1[b]);
   };
@@ -142,10 +144,8 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
     unsigned char* base = reinterpret_cast<unsigned char*>(s.B2);
     const int ar = (m & 1) ? 128 : 0, kr = (m & 1) ? 0 : 64;
     tc::mbar_arrive_expect_tx(&s.bar_b2, WALKV_B2_BYTES);
-    for (int kb = 0; kb < 2; ++kb) {
-      tc::tma_load_2d(base + kb * 24576 + ar * 128, &a.aqk_map, kb * 32, item * CH, &s.bar_b2);
-      tc::tma_load_2d(base + kb * 24576 + kr * 128, &a.kdt_map, kb * 32, item * DK, &s.bar_b2);
-    }
+    tc::tma_load_2d(base + ar * 128, &a.aqk_map, 0, item * CH, &s.bar_b2);
+    tc::tma_load_2d(base + kr * 128, &a.kdt_map, 0, item * DK, &s.bar_b2);
   };
   auto issue_u = [&](int m) {
     const int item = (dd.chunk0 + m) * a.HV + h;
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
   __syncthreads();
   tc::tc_fence_after();
 
-  constexpr uint32_t kId1 = tc::idesc_tf32(128, 128), kId2 = tc::idesc_tf32(128, 192);
+  constexpr uint32_t kId1 = tc::idesc_f16(128, 128), kId2 = tc::idesc_f16(128, 192);
   bool ok = true;
   int m = 0;
   for (; m < n; ++m) {
@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       }
       ok = tc::mbar_wait(&s.bar_b1[b], (m >> 1) & 1) && ok;  // gamma of this chunk
       // Columns 64 hf .. 64 hf + 63 in two halves: the tape tile (chunk-major: 512
-      // contiguous bytes per warp and 8-channel piece), S0' = S0 rounded to TF32
-      // (the A operand), and diag(gamma) S0 into S.  (Scaling S while [P | O]
+      // contiguous bytes per warp and 8-channel piece), S0' = S0 rounded to FP16
+      // (the A operand, two channels per column), and diag(gamma) S0 into S.  (Scaling S while [P | O]
       // runs instead measured slower: the products read their A operand from
       // tensor memory, and the warps' tensor-memory traffic slows them.)
       const float* gm = s.gam[b] + 64 * hf;
@@ -228,8 +228,11 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
           }
         }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = tf32(__uint_as_float(s0[j]));
-        tc::tmem_st32(tl + kColSp + c0, r);
+        for (int j = 0; j < 16; ++j) {
+          const __half2 p = __floats2half2_rn(__uint_as_float(s0[2 * j]), __uint_as_float(s0[2 * j + 1]));
+          r[j] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+        tc::tmem_st16(tl + kColSp + c0 / 2, *reinterpret_cast<const uint32_t(*)[16]>(r));
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(s0[j]) * gm[32 * half + j]);
         tc::tmem_st32(tl + kColS + c0, r);
@@ -245,16 +248,16 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       tc::tc_fence_after();
       const uint64_t bd = tc::desc_k_sw128(s.B1[b]);
 #pragma unroll
-      for (int k = 0; k < DK / 8; ++k)
-        tc::mma_tf32_ta(tm + colD1(b), tm + kColSp + 8 * k, tc::kstep32(bd, k, 128), kId1, k > 0);
+      for (int k = 0; k < DK / 16; ++k)
+        tc::mma_f16_ta(tm + colD1(b), tm + kColSp + 8 * k, tc::kstep32(bd, k, 128), kId1, k > 0);
       tc::mma_commit(&s.bar_s1);
       ++s1_iss;
     }
     if (data) {
       // While [P | O] runs: the previous chunk's output.
       if (outputs && m > 0) drain_out(m - 1);
-      // Delta = u - P (rows j = 32 hf ..), rounded to TF32 in place (the A
-      // operand of the second product); the FP32 Delta for the backward.
+      // Delta = u - P (rows j = 32 hf ..) in FP32 in place (for the backward),
+      // and its FP16 copy (the A operand of the second product).
       ok = tc::mbar_wait(&s.bar_s1, m & 1) && ok;
       if (use_u) ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
       tc::tc_fence_after();
@@ -262,17 +265,20 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       tc::tmem_ld32(tl + colPd(b) + 32 * hf, r);
       tc::tmem_wait_ld();
       const unsigned char* ub = reinterpret_cast<const unsigned char*>(s.U) + q4 * (CH * 128) + (lane & 3) * 4;
-      uint32_t rr[32];
+      uint32_t rr[16];
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * hf + jj;
         const float uu = use_u ? *reinterpret_cast<const float*>(ub + j * 128 + ((((lane >> 2)) ^ (j & 7)) << 4)) : 0.f;
-        const float d = uu - __uint_as_float(r[jj]);
-        r[jj] = __float_as_uint(d);
-        rr[jj] = tf32(d);
+        r[jj] = __float_as_uint(uu - __uint_as_float(r[jj]));
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const __half2 p = __floats2half2_rn(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
+        rr[q] = *reinterpret_cast<const uint32_t*>(&p);
       }
       tc::tmem_st32(tl + colPd(b) + 32 * hf, r);      // FP32 Delta, written out below
-      tc::tmem_st32(tl + kColDl + 32 * hf, rr);       // TF32 Delta, the A operand of the update
+      tc::tmem_st16(tl + kColDl + 16 * hf, rr);       // FP16 Delta, the A operand of the update
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
@@ -295,8 +301,8 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
         tc::tc_fence_after();
         const uint64_t bd = tc::desc_k_sw128(s.B2);
 #pragma unroll
-        for (int k = 0; k < CH / 8; ++k)
-          tc::mma_tf32_ta(tm + colD2(b), tm + kColDl + 8 * k, tc::kstep32(bd, k, 192), kId2, 1);
+        for (int k = 0; k < CH / 16; ++k)
+          tc::mma_f16_ta(tm + colD2(b), tm + kColDl + 8 * k, tc::kstep32(bd, k, 192), kId2, 1);
         tc::mma_commit(&s.bar_s2);
         ++s2_iss;
       }
@@ -367,13 +373,15 @@ cudaError_t launch_walk_fwd_v(const WalkArgs& a, int nsegs, cudaStream_t st) {
 //   [dDelta^T | dS^T] += (scale dO)'^T [Aqk^T ; Qp^T]^T  (M = 128, N = 192, K = 64 tokens)
 //   dS^T += (-dDelta')^T (w^T)^T                          (M = 128, N = 128, K = 64 tokens)
 // (primes: TF32-rounded copies in tensor memory; dS^T is scaled by
-// diag(gamma) in place before the second product).  These products contract
-// each saved tile over its other index than the forward's products do, and
-// TF32 operands must be K-major, so the B operands are the forward's tiles
-// transposed: TMA brings each chunk's tiles as stored (w, Q Gamma, Kd^T, Aqk)
-// into a staging area, and the data warps transpose them, 4 x 4 elements per
-// thread, into the 128-byte-swizzled K-major operand stage, each tile just
-// before the product that reads it: Kd with the adjoint's copy, [Aqk^T ;
+// diag(gamma) in place before the second product).  The adjoints are
+// gradients, whose scale the caller's loss sets, so these products keep
+// TF32 operands (FP32 range).  They contract each saved tile over its other
+// index than the forward's products do, and TF32 operands must be K-major,
+// so the B operands are the forward's tiles transposed: TMA brings each
+// chunk's FP16 tiles as stored (w, Q Gamma, Kd^T, Aqk) into a staging area,
+// and the data warps transpose them, 4 x 4 elements per thread, into the
+// 128-byte-swizzled K-major FP32 operand stage (FP16 values are exact in
+// TF32), each tile just before the product that reads it: Kd with the adjoint's copy, [Aqk^T ;
 // Qp^T] before the second product, w^T while it runs.  A staging group is
 // refilled with the next chunk's tiles as soon as it has been transposed, a
 // whole chunk ahead of its next use.  Each chunk stores the adjoint of its
@@ -391,11 +399,11 @@ struct WalkBvSmem {
   float BA[(CH + DK) * CH];  // [Aqk^T ; Qp^T]: rows j then c, K = i; 2 column blocks of 192 rows
   float BK[CH * DK];         // Kd [j][c]: rows j, K = c; 4 column blocks of 64 rows
   float BW[DK * CH];         // w^T [c][j]: rows c, K = j; 2 column blocks of 128 rows
-  // Staging, the saved tiles as the forward reads them (TMA, 128-byte swizzle):
-  float SK[DK * CH];         // Kd^T [c][j]: 2 column blocks of 128 rows
-  float SA[CH * CH];         // Aqk [i][j]: 2 column blocks of 64 rows
-  float SQ[CH * DK];         // Q Gamma [i][c]: 4 column blocks of 64 rows
-  float SW[CH * DK];         // w [j][c]: 4 column blocks of 64 rows
+  // Staging, the saved FP16 tiles as the forward reads them (TMA, 128-byte swizzle):
+  uint16_t SK[DK * CH];      // Kd^T [c][j]: 1 column block of 128 rows
+  uint16_t SA[CH * CH];      // Aqk [i][j]: 1 column block of 64 rows
+  uint16_t SQ[CH * DK];      // Q Gamma [i][c]: 2 column blocks of 64 rows
+  uint16_t SW[CH * DK];      // w [j][c]: 2 column blocks of 64 rows
   float gam[DK];             // gamma, with the Kd^T group
   float gamc[DK];            // this chunk's gamma, copied before the Kd^T group is refilled
   uint64_t bar_k, bar_a, bar_w, bar_ab, bar_c;
@@ -403,8 +411,8 @@ struct WalkBvSmem {
 };
 constexpr uint32_t kBColD = 0, kBColS = 64, kBColSp = 192, kBColDn = 448;
 __device__ __forceinline__ uint32_t colDO(int b) { return b ? 384u : 320u; }
-constexpr uint32_t WALKB_K_BYTES = DK * CH * 4 + DK * 4, WALKB_A_BYTES = (CH * CH + CH * DK) * 4,
-                   WALKB_W_BYTES = CH * DK * 4;
+constexpr uint32_t WALKB_K_BYTES = DK * CH * 2 + DK * 4, WALKB_A_BYTES = (CH * CH + CH * DK) * 2,
+                   WALKB_W_BYTES = CH * DK * 2;
 
 // Byte offset of FP32 element (row r, k) of a K-major 128B-swizzled operand of
 // R rows (column blocks of 32 k).
@@ -412,10 +420,16 @@ __device__ __forceinline__ uint32_t sw_off(int r, int k, int R) {
   return (uint32_t)((k >> 5) * R * 128 + r * 128 + ((((k & 31) >> 2) ^ (r & 7)) << 4) + ((k & 3) << 2));
 }
 
-// One group of 32 4 x 4 blocks of a transposed copy between two K-major
-// 128B-swizzled tiles: source rows sr0 .. sr0+15 (of R_s rows), source columns
-// sc0 .. sc0+31 become destination rows roff + sc0 .. (of R_d rows) with the
-// source rows as their K index.  A 16-byte shared access is served a quarter
+// Byte offset of FP16 element (row r, k) of a 128B-swizzled tile of R rows
+// (column blocks of 64 k).
+__device__ __forceinline__ uint32_t sw_off_h(int r, int k, int R) {
+  return (uint32_t)((k >> 6) * R * 128 + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4) + ((k & 7) << 1));
+}
+
+// One group of 32 4 x 4 blocks of a transposed copy from a 128B-swizzled FP16
+// tile to a K-major 128B-swizzled FP32 tile: source rows sr0 .. sr0+15 (of
+// R_s rows), source columns sc0 .. sc0+31 become destination rows roff + sc0
+// .. (of R_d rows) with the source rows as their K index.  A 16-byte shared access is served a quarter
 // warp at a time, so the eight lanes of each quarter take row quads and column
 // quads such that their reads (row 4 rq + a, column chunk cq) and their writes
 // (row 4 cq + b, K chunk rq) each fall on eight different 16-byte bank groups:
@@ -428,7 +442,12 @@ __device__ __forceinline__ void transpose_group(const unsigned char* src, int Rs
   const int r0 = sr0 + 4 * rq, c0 = sc0 + 4 * cq;
   float4 x[4];
 #pragma unroll
-  for (int a = 0; a < 4; ++a) x[a] = *reinterpret_cast<const float4*>(src + sw_off(r0 + a, c0, Rs));
+  for (int a = 0; a < 4; ++a) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(src + sw_off_h(r0 + a, c0, Rs));
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    x[a] = make_float4(lo.x, lo.y, hi.x, hi.y);
+  }
   *reinterpret_cast<float4*>(dst + sw_off(roff + c0 + 0, r0, Rd)) = make_float4(x[0].x, x[1].x, x[2].x, x[3].x);
   *reinterpret_cast<float4*>(dst + sw_off(roff + c0 + 1, r0, Rd)) = make_float4(x[0].y, x[1].y, x[2].y, x[3].y);
   *reinterpret_cast<float4*>(dst + sw_off(roff + c0 + 2, r0, Rd)) = make_float4(x[0].z, x[1].z, x[2].z, x[3].z);
@@ -499,19 +518,19 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
   auto issue_k = [&](int m) {
     const int item = (dd.chunk0 + m) * a.HV + h;
     tc::mbar_arrive_expect_tx(&s.bar_k, WALKB_K_BYTES);
-    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(s.SK + kb * DK * 32, &a.kdt_map, kb * 32, item * DK, &s.bar_k);
+    tc::tma_load_2d(s.SK, &a.kdt_map, 0, item * DK, &s.bar_k);
     tc::bulk_load(s.gam, &a.gam[(size_t)item * DK], DK * 4, &s.bar_k);
   };
   auto issue_a = [&](int m) {
     const int item = (dd.chunk0 + m) * a.HV + h;
     tc::mbar_arrive_expect_tx(&s.bar_a, WALKB_A_BYTES);
-    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(s.SA + kb * CH * 32, &a.aqk_map, kb * 32, item * CH, &s.bar_a);
-    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(s.SQ + kb * CH * 32, &a.qp_map, kb * 32, item * CH, &s.bar_a);
+    tc::tma_load_2d(s.SA, &a.aqk_map, 0, item * CH, &s.bar_a);
+    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(s.SQ + kb * CH * 64, &a.qp_map, kb * 64, item * CH, &s.bar_a);
   };
   auto issue_w = [&](int m) {
     const int item = (dd.chunk0 + m) * a.HV + h;
     tc::mbar_arrive_expect_tx(&s.bar_w, WALKB_W_BYTES);
-    for (int kb = 0; kb < 4; ++kb) tc::tma_load_2d(s.SW + kb * CH * 32, &a.w_map, kb * 32, item * CH, &s.bar_w);
+    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(s.SW + kb * CH * 64, &a.w_map, kb * 64, item * CH, &s.bar_w);
   };
   // dO of chunk m, rows i = 32 hf .., at value column v, as raw BF16 bits into
   // registers (loaded a step before use; rows beyond the chunk read its first

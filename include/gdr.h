@@ -41,6 +41,15 @@
  *   - Gate precondition: g finite and >= -10 (the per-block gate
  *     factorization keeps every exponent below FP32 overflow for 8 tokens x
  *     10 = 80 < 88.7).  Outside that range results are unspecified.
+ *   - Range precondition of the forward's FP16 operands.  The intermediates
+ *     w, Q Gamma, Kd^T and Aqk (functions of q, k, g, beta: of order |q| |k|)
+ *     are stored, and the forward walk's copies of the state and of Delta
+ *     (of the order of the values v) are multiplied, in FP16, which has the
+ *     11-bit significand of the TF32 products but a largest finite value of
+ *     65504: q, k rows of norm up to about 100 and state entries below that
+ *     bound are required (unit-norm q, k and values v of moderate size, as in
+ *     training, satisfy it by orders of magnitude).  The backward's adjoints
+ *     are gradients and stay in FP32 / TF32.
  *   - Workspaces.  `saved` carries the forward's intermediates to the
  *     backward; `scratch` holds temporaries.  Sizes come from
  *     *_workspace_bytes.  Both must be 256-byte aligned.

@@ -56,6 +56,16 @@ def test_gdn_production_heads_small_pack():
     _check("gdn", [300, 211], 16, 48, seed=3)
 
 
+def test_gdn_ungrouped_heads_ragged():
+    # One value head per Q/K head (no grouping): the prep's per-group loop runs once.
+    _check("gdn", [1, 63, 64, 65, 0, 129], 2, 2, seed=23, h0=True, dht=True)
+
+
+def test_gdn_eight_value_heads_per_qk_head():
+    # Eight value heads share each Q/K head's Gram; gate and v tiles rotate through the buffers.
+    _check("gdn", [100, 64, 77], 1, 8, seed=24, h0=True, dht=True)
+
+
 def test_kda_mild_gates_long_document():
     # Gates near zero keep the state alive across all 64 chunks.
     _check("kda", [4096], 1, 1, seed=4, glow=-0.05, h0=True, dht=True)
