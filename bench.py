@@ -43,17 +43,17 @@ C, D = 64, 128
 _TILE = D * 4           # one FP32 row of a [64][128] intermediate
 _STATE = D * D * 4 / C  # one FP32 128x128 state per chunk, per token
 KERNEL_MODEL = {
-    # name: (bytes per token-head, flops per token-head).  w, Q Gamma, Kd^T and
-    # Aqk are stored in FP16 (2 bytes), the other intermediates in FP32.
-    "prep": (3 * 2 * D + 4 * D + 2 + _TILE + 3 * 2 * D + C * 2 + 2 * C * 4 + 4 * D / C,
+    # name: (bytes per token-head, flops per token-head).  w, u, Q Gamma, Kd^T
+    # and Aqk are stored in FP16 (2 bytes), the other intermediates in FP32.
+    "prep": (3 * 2 * D + 4 * D + 2 + 4 * 2 * D + C * 2 + 2 * C * 4 + 4 * D / C,
              2 * (2 * 0.5 * C * D) + 2 * (2 * 0.5 * C * D) + C * C / 3),
     # state walk with the outputs: reads w, u, Kd^T, Q Gamma, Aqk, gamma; writes
     # Delta, the BF16 state tape and the BF16 output.
-    "walk_fwd": (_TILE + 3 * 2 * D + C * 2 + 4 * D / C + _TILE + _STATE / 2 + 2 * D,
+    "walk_fwd": (4 * 2 * D + C * 2 + 4 * D / C + _TILE + _STATE / 2 + 2 * D,
                  3 * (2 * D * D) + 2 * 0.5 * C * D),
     "walk_bwd": (C * 2 + 3 * 2 * D + 2 * D + _STATE / 2 + _TILE, 2 * (2 * D * D) + 2 * D * D + 2 * 0.5 * C * D),
     "grad_state": (2 * D + _STATE + 2 * _TILE + 3 * _TILE + 4 * D / C + C * 4, 3 * (2 * D * D)),
-    "grad": (3 * 2 * D + 4 * D + 2 + 2 * D + 2 * D + 2 * _TILE + 3 * C * 4 + 2 * _TILE + 3 * _TILE + 3 * 2 * D + 4 * D + 2,
+    "grad": (3 * 2 * D + 4 * D + 2 + 2 * D + 2 * D + 2 * D + _TILE + 3 * C * 4 + 2 * _TILE + 3 * _TILE + 3 * 2 * D + 4 * D + 2,
              11 * (2 * 0.5 * C * D) + 2 * (2 * C * D)),
 }
 

@@ -287,7 +287,7 @@ Layout make_layout(int64_t T, int64_t NC, int32_t N, int32_t Hqk, int32_t HV, bo
   L.sstart = take(segstate);  // start state of each segment
   L.sbias = take(segstate);   // each segment's end state from a zero start
   L.w = take((size_t)NC * HV * CH * DK * sizeof(__half));
-  L.u = take((size_t)NC * HV * CH * LDF * sizeof(float));
+  L.u = take((size_t)NC * HV * CH * LDF * sizeof(__half));
   L.qp = take((size_t)NC * HV * CH * DK * sizeof(__half));
   L.kd = take((size_t)NC * HV * DK * CH * sizeof(__half));
   L.delta = take(tile);
@@ -441,26 +441,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A row-major FP32 matrix [rows][cols] whose rows are `pitch` elements apart,
-// read in boxes of 32 columns (128 bytes, 128-byte swizzle) x box_rows rows.
-bool fp32_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch, uint32_t box_rows) {
+// rows x cols FP16 tensor whose rows are `pitch` elements apart (default:
+// dense); boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool fp16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              uint64_t pitch = 0) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {pitch * sizeof(float)};
-  cuuint32_t box[2] = {32, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// rows x cols dense FP16 tensor; boxes of 64 columns x box_rows rows, 128-byte swizzle.
-bool fp16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {(pitch ? pitch : cols) * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
@@ -723,7 +711,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   pa.Hqk = Hqk;
   pa.HV = HV;
   pa.w = at<__half>(base, L.w);
-  pa.u = at<float>(base, L.u);
+  pa.u = at<__half>(base, L.u);
   pa.qp = at<__half>(base, L.qp);
   pa.kd = at<__half>(base, L.kd);
   pa.aqk = at<__half>(base, L.aqk);
@@ -752,13 +740,12 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   ma.smap = wa.smap;
   ma.state = wa.sstart;
   ma.bias = wa.sbias;
-  wa.u = pa.u;
   wa.gam = pa.gam;
   wa.err = device_error_ptr();
   if (!wa.err) return GDR_CUDA_ERROR;
   if (NC > 0 && (!fp16_map(&wa.w_map, pa.w, (uint64_t)NC * HV * CH, DK, CH) ||
                  !fp16_map(&wa.kdt_map, pa.kd, (uint64_t)NC * HV * DK, CH, DK) ||
-                 !fp32_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, LDF, CH) ||
+                 !fp16_map(&wa.u_map, pa.u, (uint64_t)NC * HV * CH, DK, CH, LDF) ||
                  !fp16_map(&wa.qp_map, pa.qp, (uint64_t)NC * HV * CH, DK, CH) ||
                  !fp16_map(&wa.aqk_map, pa.aqk, (uint64_t)NC * HV * CH, CH, CH)))
     return GDR_CUDA_ERROR;
@@ -920,7 +907,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   ga.HV = HV;
   ga.scale = scale;
   ga.w = sw;
-  ga.u = at<float>(saved, L.u);
+  ga.u = at<__half>(saved, L.u);
   ga.gam = wb.gam;
   ga.delta = gs.delta;
   ga.ddelta = wb.ddelta;

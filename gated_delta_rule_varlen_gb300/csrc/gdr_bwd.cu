@@ -335,12 +335,13 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     }
   }
   __syncthreads();
-  // w and u (B operands of dA) into the staging tiles: u by one bulk copy, w
-  // (FP16, dense rows) by cp.async into the dw staging tile, which X no longer
-  // reads, as FP16 rows 136 elements apart.
+  // w and u (FP16, B operands of dA) into the staging tiles as rows 136
+  // elements apart: u (stored with that pitch) by one bulk copy into the
+  // dDelta staging tile, w (dense rows) by cp.async into the dw staging tile
+  // (X and Y no longer read them).
   if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&sg.bar_u, CH * LDF * 4);
-    tc::bulk_load(sg.dG, &a.u[fo], CH * LDF * 4, &sg.bar_u);
+    tc::mbar_arrive_expect_tx(&sg.bar_u, CH * LDF * 2);
+    tc::bulk_load(sg.dG, &a.u[fo], CH * LDF * 2, &sg.bar_u);
   }
   __half* const wsh = reinterpret_cast<__half*>(sg.dK);
   for (int e = tid; e < CH * DK / 8; e += NTH) {
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     return;
   }
   {
-    const float* u = sg.dG;
+    const __half* u = reinterpret_cast<const __half*>(sg.dG);
 #pragma unroll
     for (int kk = 0; kk < NT; ++kk) {
       uint32_t ax[4] = {tf32(X[kk][0]), tf32(X[kk][2]), tf32(X[kk][1]), tf32(X[kk][3])};
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
         if (nt < 2 * I + 2) {
           const int j = nt * 8 + g;
           const float2 wv = __half22float2(*reinterpret_cast<const __half2*>(&wsh[j * LDF + cc]));
-          const float2 uv = *reinterpret_cast<const float2*>(&u[j * LDF + cc]);
+          const float2 uv = __half22float2(*reinterpret_cast<const __half2*>(&u[j * LDF + cc]));
           uint32_t bw[2] = {__float_as_uint(wv.x), __float_as_uint(wv.y)};
           uint32_t bu[2] = {__float_as_uint(uv.x), __float_as_uint(uv.y)};
           mma8(dAacc[nt], ax, bw);

@@ -202,8 +202,8 @@ __device__ __forceinline__ size_t w_off(int chunk, int h, int HV) { return ((siz
 __device__ __forceinline__ size_t qp_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * DK); }
 __device__ __forceinline__ size_t kd_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (DK * CH); }
 __device__ __forceinline__ size_t aqk_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * CH); }
-// Tiles the gradient kernel moves whole keep its pitches too: u, dw, dDelta
-// [64][LDF]; At, T, dAqk [64][LDS].
+// Tiles the gradient kernel moves whole keep its pitches too: dw, dDelta
+// [64][LDF] and u (FP16) [64][LDF]; At, T, dAqk [64][LDS].
 __device__ __forceinline__ size_t tf_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDF); }
 __device__ __forceinline__ size_t ts_off(int chunk, int h, int HV) { return ((size_t)chunk * HV + h) * (CH * LDS); }
 

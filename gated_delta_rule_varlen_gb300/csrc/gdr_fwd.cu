@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   {
     const int prod = warp >> 2, q = warp & 3, c0 = 64 * (q & 1);
     const int Ia = (q >> 1) ? 2 : 3, Ib = 3 - Ia;
-    float* uo = a.u + tf_off(chunk, h, a.HV);
+    __half* uo = a.u + tf_off(chunk, h, a.HV);
     __half* wo = a.w + w_off(chunk, h, a.HV);
     auto bw = [&](int j, int c) { return s.G[j * LDT + c]; };
     auto bu = [&](int j, int c) { return s.beta[j] * s.q(j, c); };
@@ -108,18 +108,18 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
           mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
                        [&](int j, int c) { return bw(j, c0 + c); });
       }
-      {  // rows i0 + g (+8), channel pairs c0 + 8 nt + 2 t: u as TF32-rounded FP32 pairs, w as FP16 pairs
+      {  // rows i0 + g (+8), channel pairs c0 + 8 nt + 2 t: FP16 pairs
         const int lane = lane_id(), g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             const int row = i0 + g + 8 * hr, c = c0 + nt * 8 + 2 * t;
+            const __half2 p = __floats2half2_rn(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
             if (prod)
-              *reinterpret_cast<float2*>(&uo[row * LDF + c]) =
-                  make_float2(__uint_as_float(tf32(acc[nt][2 * hr])), __uint_as_float(tf32(acc[nt][2 * hr + 1])));
+              *reinterpret_cast<__half2*>(&uo[row * LDF + c]) = p;
             else
-              *reinterpret_cast<__half2*>(&wo[row * DK + c]) = __floats2half2_rn(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+              *reinterpret_cast<__half2*>(&wo[row * DK + c]) = p;
           }
       }
     }
@@ -204,11 +204,9 @@ __device__ __forceinline__ void build_a(PrepGdnSmem& s, const float* __restrict_
   }
 }
 
-// The M = 64 accumulator at TMEM column 128 (w or u) -> rows of `out`: u
-// rounded to TF32 (pitch LDF), w in FP16 (dense rows).  Warp (quadrant,
-// half): rows 16 quad .., channels 64 half ..
-template <typename OT>
-__device__ __forceinline__ void drain_wu(uint32_t tmem, OT* __restrict__ out) {
+// The M = 64 accumulator at TMEM column 128 (w or u) -> FP16 rows of `out`,
+// `ld` elements apart.  Warp (quadrant, half): rows 16 quad .., channels 64 half ..
+__device__ __forceinline__ void drain_wu(uint32_t tmem, __half* __restrict__ out, int ld) {
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const int quad = warp & 3, hf = warp >> 2, g = lane >> 2, u2 = (lane & 3) * 2;
   const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + 128 + 64 * hf;
@@ -223,11 +221,7 @@ __device__ __forceinline__ void drain_wu(uint32_t tmem, OT* __restrict__ out) {
       for (int hr = 0; hr < 2; ++hr) {
         const int row = 16 * quad + g + 8 * hr, c = 64 * hf + cb + 8 * q + u2;
         const float x0 = __uint_as_float(rr[4 * q + 2 * hr]), x1 = __uint_as_float(rr[4 * q + 2 * hr + 1]);
-        if constexpr (sizeof(OT) == 4)
-          *reinterpret_cast<float2*>(&out[row * LDF + c]) =
-              make_float2(__uint_as_float(tf32(x0)), __uint_as_float(tf32(x1)));
-        else
-          *reinterpret_cast<__half2*>(&out[row * DK + c]) = __floats2half2_rn(x0, x1);
+        *reinterpret_cast<__half2*>(&out[row * ld + c]) = __floats2half2_rn(x0, x1);
       }
   }
 }
@@ -412,7 +406,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_gdn(const __grid_constant__ Pre
     ++m_waited;
     tc::tc_fence_after();
     if (!ok) break;
-    drain_wu(tmem, a.w + w_off(chunk, h, a.HV));
+    drain_wu(tmem, a.w + w_off(chunk, h, a.HV), DK);
     tc::tc_fence_before();
     __syncthreads();
     // u = (T diag(beta)) V.
@@ -461,7 +455,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_gdn(const __grid_constant__ Pre
       }
       ++v_issued;
     }
-    drain_wu(tmem, a.u + tf_off(chunk, h, a.HV));
+    drain_wu(tmem, a.u + tf_off(chunk, h, a.HV), LDF);
     tc::tc_fence_before();
     __syncthreads();
   }

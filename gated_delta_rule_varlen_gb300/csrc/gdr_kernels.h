@@ -23,7 +23,8 @@ struct PrepArgs {
   const ChunkDesc* chunks;
   int Hqk, HV;
   __half *w, *qp, *kd, *aqk;  // FP16, dense rows (gdr_common.cuh)
-  float *u, *gam;             // u with the padded pitch LDF
+  __half* u;                  // FP16, rows LDF apart
+  float* gam;
   float *amat, *tmat;  // At and T per chunk ([64][64] FP32), or null when nothing is saved
   // In-kernel q/k L2 normalization (else null): the scales r [T][Hqk] of q and
   // k's rows; q and k are then the raw inputs and every product takes the
@@ -43,16 +44,15 @@ struct PrepTcArgs {
 };
 
 struct WalkArgs {
-  // 2-D tensor maps (rows x columns), 128-byte swizzle: the FP16 operand
-  // tiles in boxes of 64 columns, u (FP32) in boxes of 32 columns.
+  // 2-D FP16 tensor maps (rows x columns), 128-byte swizzle, boxes of 64 columns:
   CUtensorMap w_map;    // w        [NC*HV*64][128] FP16, 64 x 64 boxes
   CUtensorMap kdt_map;  // Kd^T     [NC*HV*128][64] FP16, 64 x 128 boxes
-  CUtensorMap u_map;    // u        [NC*HV*64][128] FP32, pitch LDF, 32 x 64 boxes
+  CUtensorMap u_map;    // u        [NC*HV*64][128] FP16, pitch LDF, 64 x 64 boxes
   CUtensorMap qp_map;   // Q Gamma  [NC*HV*64][128] FP16, 64 x 64 boxes
   CUtensorMap aqk_map;  // Aqk      [NC*HV*64][64]  FP16, 64 x 64 boxes
   const SegDesc* segs;  // walk segments, the longest document's first
   int HV;
-  const float *u, *gam;
+  const float* gam;
   const float* h0;   // [N][HV][128][128] or null
   __nv_bfloat16* tape;  // S0 per chunk (BF16, chunk-major), or null
   float* delta;      // Delta per chunk, or null
@@ -120,7 +120,8 @@ struct GradArgs {
   int Hqk, HV;
   float scale;
   const __half* w;  // FP16 [64][128] per chunk
-  const float *u, *gam, *delta, *ddelta;
+  const __half* u;  // FP16 [64][LDF] per chunk
+  const float *gam, *delta, *ddelta;
   const float *dqs, *dw, *dkd, *dgam, *daqk;
   const float *amat, *tmat;  // At and T of each chunk, saved by the forward
   // outputs

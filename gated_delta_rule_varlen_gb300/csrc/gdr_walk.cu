@@ -40,7 +40,7 @@
 // Threads: 8 data warps (warp w: TMEM lanes 32 (w % 4) .., value rows v; warp
 // halves w / 4 split the columns) and one issuer warp (its lane 0 issues every
 // TMA copy and MMA).  Shared memory: [w ; Qp] + gamma in two stages (32 KB
-// each), [Kd^T ; Aqk] (24 KB) and u (32 KB) in one.  Waits are bounded; a
+// each), [Kd^T ; Aqk] (24 KB) and u (16 KB) in one.  Waits are bounded; a
 // timed-out wait ends the walk for the whole CTA and sets the device error
 // word.
 #include "gdr_common.cuh"
@@ -52,7 +52,7 @@ namespace gdr {
 struct WalkVSmem {
   uint16_t B1[2][2 * CH * DK];  // per stage, FP16: 2 column blocks of 128 rows x 64 channels (16 KB each)
   uint16_t B2[(DK + CH) * CH];  // FP16: 1 column block of 192 rows x 64 tokens
-  float U[CH * DK];            // u: 4 blocks of 64 rows j x 32 value columns (128-byte swizzle)
+  uint16_t U[CH * DK];         // u (FP16): 2 blocks of 64 rows j x 64 value columns (128-byte swizzle)
   float gam[2][DK];            // gamma, with the B1 stage
   uint64_t bar_b1[2], bar_b2, bar_u, bar_s1, bar_s2;
   uint32_t tmem;
@@ -60,7 +60,7 @@ struct WalkVSmem {
 constexpr int WALKV_THREADS = 288;
 constexpr uint32_t WALKV_B1_BYTES = 2 * CH * DK * 2 + DK * 4;
 constexpr uint32_t WALKV_B2_BYTES = (DK + CH) * CH * 2;
-constexpr uint32_t WALKV_U_BYTES = CH * DK * 4;
+constexpr uint32_t WALKV_U_BYTES = CH * DK * 2;
 constexpr uint32_t kColS = 128, kColSp = 384;  // S (FP32), S' (FP16 pairs)
 constexpr uint32_t kColDl = 448;                // Delta' (FP16 pairs)
 __device__ __forceinline__ uint32_t colPd(int b) { return b ? 320u : 0u; }   // P, then Delta, of parity b
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
   auto issue_u = [&](int m) {
     const int item = (dd.chunk0 + m) * a.HV + h;
     tc::mbar_arrive_expect_tx(&s.bar_u, WALKV_U_BYTES);
-    for (int vb = 0; vb < 4; ++vb) tc::tma_load_2d(s.U + vb * CH * 32, &a.u_map, vb * 32, item * CH, &s.bar_u);
+    for (int vb = 0; vb < 2; ++vb) tc::tma_load_2d(s.U + vb * CH * 64, &a.u_map, vb * 64, item * CH, &s.bar_u);
   };
   // scale * O of chunk m (buffer O[m & 1]) -> out, rows i = 32 hf .. (data threads).
   auto drain_out = [&](int m) {
@@ -264,12 +264,14 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       uint32_t r[32];
       tc::tmem_ld32(tl + colPd(b) + 32 * hf, r);
       tc::tmem_wait_ld();
-      const unsigned char* ub = reinterpret_cast<const unsigned char*>(s.U) + q4 * (CH * 128) + (lane & 3) * 4;
+      const int vv = v & 63;  // u[j][v]: block v / 64, 16-byte piece vv / 8 (swizzled by j), element vv % 8
+      const unsigned char* ub = reinterpret_cast<const unsigned char*>(s.U) + (v >> 6) * (CH * 128) + (vv & 7) * 2;
       uint32_t rr[16];
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * hf + jj;
-        const float uu = use_u ? *reinterpret_cast<const float*>(ub + j * 128 + ((((lane >> 2)) ^ (j & 7)) << 4)) : 0.f;
+        const float uu = use_u ? __half2float(*reinterpret_cast<const __half*>(ub + j * 128 + (((vv >> 3) ^ (j & 7)) << 4)))
+                               : 0.f;
         r[jj] = __float_as_uint(uu - __uint_as_float(r[jj]));
       }
 #pragma unroll
