@@ -545,8 +545,13 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xh = {k: v.cpu() for k, v in x.items()}
+        # A bounded sample of about 10-30 s of CPU work: a 4096-token probe,
+        # then, if it ran short, a longer prefix of every document sized to ~12 s.
         toks = 4096
         n, dt, threads = oracle_sample(wl, xh, toks)
+        if dt < 8.0 and toks < max(wl.lengths):
+            toks = min(max(wl.lengths), int(toks * 12.0 / max(dt, 1e-3)))
+            n, dt, threads = oracle_sample(wl, xh, toks)
         cpu = {"value": n / dt / HV, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"first {toks} tokens of each of the {len(wl.lengths)} documents, all {HV} heads, "
                          f"fwd+bwd ({n} token-heads, {dt:.1f} s)"}

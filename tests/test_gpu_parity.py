@@ -66,6 +66,18 @@ def test_gdn_eight_value_heads_per_qk_head():
     _check("gdn", [100, 64, 77], 1, 8, seed=24, h0=True, dht=True)
 
 
+def test_kda_large_values_within_the_fp16_operand_range():
+    # The forward walk multiplies FP16 copies of the state and of Delta, which
+    # scale with the values v: v 300 times larger than the workloads' (entries
+    # up to ~1e3, state entries in the thousands) stays well inside FP16's range.
+    x, cu, h0, dht = _case("kda", [700, 129], 2, 2, seed=25, glow=-0.05, h0=True, dht=True)
+    x["v"] = (x["v"].float() * 300.0).to(torch.bfloat16)
+    h0 = h0 * 300.0
+    gpu = run_gpu("kda", x, cu, h0=h0, dht=dht, want_dh0=True)
+    ref = run_oracle(x, cu, h0=h0, dht=dht)
+    print("large v", assert_within(compare(gpu, ref)))
+
+
 def test_kda_mild_gates_long_document():
     # Gates near zero keep the state alive across all 64 chunks.
     _check("kda", [4096], 1, 1, seed=4, glow=-0.05, h0=True, dht=True)
