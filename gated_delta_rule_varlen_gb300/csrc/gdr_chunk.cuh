@@ -264,35 +264,38 @@ __device__ __forceinline__ void invert_tiles(const float* __restrict__ At, float
   }
   __syncthreads();
   if ((warp & 3) < 3) {
-    const int J = warp & 3, r = lane >> 1, q4 = (lane & 1) * 4;
-    const int cw = 8 * (warp >> 2);          // column offset of this warp inside block J
-    const int cb = 16 * J + cw + q4;         // this lane's first column
-    float* tmp = tmp_all + ((warp >> 2) * 3 + J) * 128;  // [16][8]: diag(beta_I) sum_K At_IK T_KJ
+    // Warp (J, half): the 16 x 8 tile of columns n0 .. n0 + 7 of T_IJ, one
+    // m16n8k8 accumulator, as split-TF32 tensor-core products (hi*hi + hi*lo
+    // + lo*hi, about FP32 accuracy): C = At_I,[16J, 16I) T_[16J, 16I),J, then
+    // X = diag(beta_I) C through shared memory into the B layout, then
+    // T_IJ = -T_II X.
+    const int J = warp & 3, n0 = 16 * J + 8 * (warp >> 2);
+    const int g = lane >> 2, t = lane & 3;
+    float* xs = tmp_all + ((warp >> 2) * 3 + J) * 128;  // X [16][8]
     for (int I = J + 1; I < 4; ++I) {
-      const int row = 16 * I + r;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int k = 16 * J; k < 16 * I; ++k) {
-        const float av = At[row * LDS + k];
-        const float4 tv = *reinterpret_cast<const float4*>(&T[k * LDS + cb]);
-        acc[0] += av * tv.x;
-        acc[1] += av * tv.y;
-        acc[2] += av * tv.z;
-        acc[3] += av * tv.w;
+      const int r0 = 16 * I;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k0 = 16 * J; k0 < r0; k0 += 8) {
+        const float a[4] = {At[(r0 + g) * LDS + k0 + t], At[(r0 + g + 8) * LDS + k0 + t],
+                            At[(r0 + g) * LDS + k0 + t + 4], At[(r0 + g + 8) * LDS + k0 + t + 4]};
+        const float b[2] = {T[(k0 + t) * LDS + n0 + g], T[(k0 + t + 4) * LDS + n0 + g]};
+        mma8_split(c, a, b);
       }
-      const float bi = beta[row];
-      *reinterpret_cast<float4*>(&tmp[r * 8 + q4]) = make_float4(bi * acc[0], bi * acc[1], bi * acc[2], bi * acc[3]);
+      xs[g * 8 + 2 * t] = beta[r0 + g] * c[0];
+      xs[g * 8 + 2 * t + 1] = beta[r0 + g] * c[1];
+      xs[(g + 8) * 8 + 2 * t] = beta[r0 + g + 8] * c[2];
+      xs[(g + 8) * 8 + 2 * t + 1] = beta[r0 + g + 8] * c[3];
       __syncwarp();
-      float out[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int m = 0; m <= r; ++m) {
-        const float tv = T[row * LDS + 16 * I + m];
-        const float4 x = *reinterpret_cast<const float4*>(&tmp[m * 8 + q4]);
-        out[0] += tv * x.x;
-        out[1] += tv * x.y;
-        out[2] += tv * x.z;
-        out[3] += tv * x.w;
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k0 = 0; k0 < 16; k0 += 8) {
+        const float a[4] = {T[(r0 + g) * LDS + r0 + k0 + t], T[(r0 + g + 8) * LDS + r0 + k0 + t],
+                            T[(r0 + g) * LDS + r0 + k0 + t + 4], T[(r0 + g + 8) * LDS + r0 + k0 + t + 4]};
+        const float b[2] = {xs[(k0 + t) * 8 + g], xs[(k0 + t + 4) * 8 + g]};
+        mma8_split(o, a, b);
       }
-      *reinterpret_cast<float4*>(&T[row * LDS + cb]) = make_float4(-out[0], -out[1], -out[2], -out[3]);
+      *reinterpret_cast<float2*>(&T[(r0 + g) * LDS + n0 + 2 * t]) = make_float2(-o[0], -o[1]);
+      *reinterpret_cast<float2*>(&T[(r0 + g + 8) * LDS + n0 + 2 * t]) = make_float2(-o[2], -o[3]);
       __syncwarp();
     }
   }

@@ -95,6 +95,25 @@ __device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], cons
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
+// d += a b with FP32 operands split as x = hi + lo (hi = x rounded to TF32,
+// lo = the remainder rounded to TF32): lo*hi + hi*lo + hi*hi, the small
+// terms first; about FP32 accuracy from three TF32 products.
+__device__ __forceinline__ void mma8_split(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ah[i] = tf32(a[i]);
+    al[i] = tf32(a[i] - __uint_as_float(ah[i]));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    bh[i] = tf32(b[i]);
+    bl[i] = tf32(b[i] - __uint_as_float(bh[i]));
+  }
+  mma8(d, al, bh);
+  mma8(d, ah, bl);
+  mma8(d, ah, bh);
+}
 
 
 // 16-byte asynchronous global -> shared copy (L2 only) and its group fences.
