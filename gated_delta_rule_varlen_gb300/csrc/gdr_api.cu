@@ -771,7 +771,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
       {
         ProfScope ps("prep", ls, units);
         if (vec) {
-          st = cuda_status(launch_prep(pa, (int)(G.c1 - G.c0), true, true, ls));
+          st = cuda_status(launch_prep(pa, (int)(G.c1 - G.c0), ls));
         } else {
           pt.p = pa;
           st = cuda_status(launch_prep_gdn(pt, (int)(G.c1 - G.c0), ls));

@@ -6,7 +6,8 @@
 namespace gdr {
 
 // ---------------------------------------------------------------------------
-// Prep (one CTA of 8 warps per (chunk, value head)): gate cumsum, gated Gram
+// KDA prep (one CTA of 8 warps per (chunk, head); grouped GDN's scalar gate
+// has the tensor-core prep k_prep_gdn below): gate cumsum, gated Gram
 // matrices, T = (I + diag(beta) At)^-1, and the chunk tiles the walk and the
 // backward need:  w = T beta (K*Gamma),  u = T beta V,  Qp = Q*Gamma,
 // Kd = K*exp(gc_last - gc),  gamma = exp(gc_last),  Aqk, At, T.
@@ -41,31 +42,39 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
       *reinterpret_cast<float4*>(&a.tmat[qo + i * LDS + j4]) = *reinterpret_cast<const float4*>(&s.T[i * LDS + j4]);
     }
   }
-  // Qp, Kd, gamma (elementwise; factors exp(gc) and exp(gc_last - gc) are <= 1).
-  // Qp and Kd are only ever MMA operands: stored in FP16.
-  const size_t toff = tile_off(chunk, h, a.HV);
+  // Kd, gamma, Qp (elementwise; factors exp(gc) and exp(gc_last - gc) are <= 1),
+  // only ever MMA operands: stored in FP16.  Kd transposed, [c][j] (the
+  // operand layout of the walk's state update): thread (channel d = e % 128,
+  // rows i0 .. i0 + 7) writes one 16-byte piece; gamma with each channel's first.
+  for (int e = tid; e < DK * CH / 8; e += blockDim.x) {
+    const int d = e & (DK - 1), i0 = 8 * (e >> 7);
+    const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
+    if (i0 == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d] = ex2(glast);
+    uint32_t p[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + 2 * q;
+      const float g0 = VEC ? s.G[i * LDT + d] : s.gs[i], g1 = VEC ? s.G[(i + 1) * LDT + d] : s.gs[i + 1];
+      const __half2 hv = __floats2half2_rn(s.k(i, d) * (scaled ? s.rk[i] : 1.f) * ex2(glast - g0),
+                                           s.k(i + 1, d) * (scaled ? s.rk[i + 1] : 1.f) * ex2(glast - g1));
+      p[q] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(&a.kd[kd_off(chunk, h, a.HV) + d * CH + i0]) = make_uint4(p[0], p[1], p[2], p[3]);
+  }
+  __syncthreads();  // the reads of gc above are done: the pass below turns it into Gamma in place
+  // Qp = Q * Gamma; Gamma = exp(gc) kept in the G tile for the B operand of w.
   for (int e = tid; e < CH * DK / 4; e += blockDim.x) {  // four channels per thread, one 8-byte store
     const int i = e >> 5, d = (e & 31) * 4;
     float r[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float gl = VEC ? s.G[i * LDT + d + q] : s.gs[i];
-      r[q] = s.q(i, d + q) * (scaled ? s.rq[i] : 1.f) * ex2(gl);
-      if (i == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d + q] = ex2(VEC ? s.G[(CH - 1) * LDT + d + q] : s.gs[CH - 1]);
+      const float gm = ex2(VEC ? s.G[i * LDT + d + q] : s.gs[i]);
+      if (VEC) s.G[i * LDT + d + q] = gm;
+      r[q] = s.q(i, d + q) * (scaled ? s.rq[i] : 1.f) * gm;
     }
     const __half2 p0 = __floats2half2_rn(r[0], r[1]), p1 = __floats2half2_rn(r[2], r[3]);
     *reinterpret_cast<uint2*>(&a.qp[qp_off(chunk, h, a.HV) + i * DK + d]) =
         make_uint2(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1));
-  }
-  // Kd stored transposed, [c][j] (the K-major A operand of the walk's state update).
-  // A warp covers rows i = 8k .. 8k+7 of channels d .. d+3 (lane bits 0-2 -> i,
-  // 3-4 -> d): shared reads are conflict-free, each 8-lane group writes 16 bytes.
-  for (int e = tid; e < CH * DK; e += blockDim.x) {
-    const int l = e & 31, w = e >> 5;
-    const int i = (l & 7) + 8 * (w & 7), d = 4 * (w >> 3) + (l >> 3);
-    const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
-    const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
-    a.kd[kd_off(chunk, h, a.HV) + d * CH + i] = __float2half_rn(s.k(i, d) * (scaled ? s.rk[i] : 1.f) * ex2(glast - gl));
   }
   __syncthreads();
   // Q tile <- v rows (async), G tile <- beta * K * Gamma (B of w).
@@ -79,8 +88,8 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   cp_async_commit();
   for (int e = tid; e < CH * DK; e += blockDim.x) {
     const int i = e >> 7, d = e & 127;
-    const float gl = VEC ? s.G[i * LDT + d] : s.gs[i];
-    s.G[i * LDT + d] = s.beta[i] * (scaled ? s.rk[i] : 1.f) * s.k(i, d) * ex2(gl);
+    const float gm = VEC ? s.G[i * LDT + d] : ex2(s.gs[i]);  // Gamma
+    s.G[i * LDT + d] = s.beta[i] * (scaled ? s.rk[i] : 1.f) * s.k(i, d) * gm;
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -396,11 +405,18 @@ __global__ void __launch_bounds__(256, 2) k_prep_gdn(const __grid_constant__ Pre
       *reinterpret_cast<uint2*>(&a.qp[qp_off(chunk, h, a.HV) + i * DK + d]) =
           make_uint2(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1));
     }
-    for (int e = tid; e < CH * DK; e += 256) {  // Kd^T [c][j]: lanes 0-7 rows, 8-lane groups channels
-      const int l = e & 31, wq = e >> 5;
-      const int i = (l & 7) + 8 * (wq & 7), d = 4 * (wq >> 3) + (l >> 3);
-      const uint16_t raw = *reinterpret_cast<const uint16_t*>(kq + sw_elem(i, d, KQ_BLOCK));
-      a.kd[kd_off(chunk, h, a.HV) + d * CH + i] = __float2half_rn(bfbits2f(raw) * s.rk[i] * s.ed[i]);
+    for (int e = tid; e < DK * CH / 8; e += 256) {  // Kd^T [c][j]: thread (channel d, rows i0 .. i0 + 7), 16 bytes
+      const int d = e & (DK - 1), i0 = 8 * (e >> 7);
+      uint32_t p[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + 2 * q;
+        const uint16_t r0 = *reinterpret_cast<const uint16_t*>(kq + sw_elem(i, d, KQ_BLOCK));
+        const uint16_t r1 = *reinterpret_cast<const uint16_t*>(kq + sw_elem(i + 1, d, KQ_BLOCK));
+        const __half2 hv = __floats2half2_rn(bfbits2f(r0) * s.rk[i] * s.ed[i], bfbits2f(r1) * s.rk[i + 1] * s.ed[i + 1]);
+        p[q] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      *reinterpret_cast<uint4*>(&a.kd[kd_off(chunk, h, a.HV) + d * CH + i0]) = make_uint4(p[0], p[1], p[2], p[3]);
     }
     ok = __syncthreads_and(tc::mbar_wait(&s.bar_m, 0));
     ++m_waited;
@@ -510,23 +526,11 @@ cudaError_t launch_l2norm(const L2NormArgs& a, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
-cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st) {
+cudaError_t launch_prep(const PrepArgs& a, int nchunks, cudaStream_t st) {
   if (nchunks == 0) return cudaSuccess;
   const size_t sm = sizeof(ChunkSmemB);
-  dim3 grid(nchunks, a.HV);
-  if (vec && beta_bf16) {
-    cudaFuncSetAttribute(k_prep<true, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_prep<true, __nv_bfloat16><<<grid, 256, sm, st>>>(a);
-  } else if (vec) {
-    cudaFuncSetAttribute(k_prep<true, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_prep<true, float><<<grid, 256, sm, st>>>(a);
-  } else if (beta_bf16) {
-    cudaFuncSetAttribute(k_prep<false, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_prep<false, __nv_bfloat16><<<grid, 256, sm, st>>>(a);
-  } else {
-    cudaFuncSetAttribute(k_prep<false, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    k_prep<false, float><<<grid, 256, sm, st>>>(a);
-  }
+  cudaFuncSetAttribute(k_prep<true, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  k_prep<true, __nv_bfloat16><<<dim3(nchunks, a.HV), 256, sm, st>>>(a);
   return cudaGetLastError();
 }
 

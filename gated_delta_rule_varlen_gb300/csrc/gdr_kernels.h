@@ -154,7 +154,7 @@ struct L2NormArgs {
   int64_t rows;  // T * Hqk
 };
 
-cudaError_t launch_prep(const PrepArgs& a, int nchunks, bool vec, bool beta_bf16, cudaStream_t st);
+cudaError_t launch_prep(const PrepArgs& a, int nchunks, cudaStream_t st);  // KDA (per-channel gate)
 cudaError_t launch_prep_gdn(const PrepTcArgs& a, int nchunks, cudaStream_t st);
 cudaError_t launch_walk_fwd_v(const WalkArgs& a, int nsegs, cudaStream_t st);
 cudaError_t launch_merge(const MergeArgs& a, int nsegs, bool backward, cudaStream_t st);
