@@ -39,34 +39,68 @@ namespace gdr {
 // the B operands (N = channel c, K = value column v) as they are.
 // ---------------------------------------------------------------------------
 struct GradStateSmem {
-  uint16_t S0[DK * DK];       // B (MN-major, no swizzle): the S0 tape tile, chunk-major
-  uint16_t dSB[DK * DK];      // B (MN-major, no swizzle): the dS tape tile, chunk-major
-  uint16_t dO[2 * CH * 64];   // A: dO [i][v]
-  uint16_t Dh[2 * CH * 64];   // Delta hi [i][v] (A of dKd, B of dAqk)
-  uint16_t Dl[2 * CH * 64];   // Delta lo
-  uint16_t Eh[2 * CH * 64];   // dDelta hi [i][v] (A of dw)
-  uint16_t El[2 * CH * 64];   // dDelta lo
-  uint64_t bar_s0, bar_m1, bar_m2;
+  uint16_t Tp[DK * DK];      // B (MN-major, no swizzle): the S0 tape tile, then the dS tape tile
+  uint16_t dO[2 * CH * 64];  // A: dO [i][v]
+  uint16_t Hi[2 * CH * 64];  // dDelta hi [i][v] (A of dw), then Delta hi (A of dKd, B of dAqk)
+  uint16_t Lo[2 * CH * 64];  // the lo parts
+  uint64_t bar_t1, bar_t2, bar_m1, bar_m2;
   uint32_t tmem;
 };
 
-__global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ GradStateArgs a) {
+// FP32 rows of a [64][128] tile (pitch ld) -> BF16 hi / lo pairs in the
+// swizzled K-major A layout: task e = row (e / 16), 16-byte piece e % 16;
+// x holds the 8 values of each of the thread's 4 tasks.
+__device__ __forceinline__ void load_hilo_rows(const float* __restrict__ src, int ld, float4 (&x)[4][2]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    const float* p = src + (size_t)(e >> 4) * ld + (e & 15) * 8;
+    x[q][0] = __ldg(reinterpret_cast<const float4*>(p));
+    x[q][1] = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+}
+__device__ __forceinline__ void store_hilo_rows(const float4 (&x)[4][2], uint16_t* hi_t, uint16_t* lo_t) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    const float f[8] = {x[q][0].x, x[q][0].y, x[q][0].z, x[q][0].w, x[q][1].x, x[q][1].y, x[q][1].z, x[q][1].w};
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * p]), h1 = __float2bfloat16_rn(f[2 * p + 1]);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(f[2 * p] - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(f[2 * p + 1] - __bfloat162float(h1));
+      hi[p] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      lo[p] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    const uint32_t off = tc::sw128_bf16_piece(e >> 4, e & 15, CH);
+    *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(hi_t) + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(lo_t) + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// Two phases in one CTA, so that two CTAs fit on an SM (256 TMEM columns,
+// ~80 KB of shared memory) and one CTA's copies overlap the other's products:
+//   1. dqs = scale dO S0^T (TMEM 0..127), dw = -dDelta S0^T (128..255);
+//   2. (the dS tape into the S0 tape's place, Delta's pairs into dDelta's)
+//      dKd = Delta dS^T (0..127), dAqk = scale tril(dO Delta^T) (128..191);
+// and dgam from the dS tile and the S0 tape read again (from L2).
+__global__ void __launch_bounds__(256, 2) k_grad_state(const __grid_constant__ GradStateArgs a) {
   extern __shared__ unsigned char smraw[];
   GradStateSmem& s = *reinterpret_cast<GradStateSmem*>(tc::align1024(smraw));
   const int chunk = a.chunk_base + blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int tid = threadIdx.x, warp = tid >> 5, lane = lane_id();
   const size_t toff = tile_off(chunk, h, a.HV);
-  constexpr uint32_t TCOLS = 512;  // dq [0,128), dw [128,256), dKd [256,384), dAqk [384,448)
-
+  constexpr uint32_t TCOLS = 256;
   if (tid == 0) {
-    tc::mbar_init(&s.bar_s0, 1);
+    tc::mbar_init(&s.bar_t1, 1);
+    tc::mbar_init(&s.bar_t2, 1);
     tc::mbar_init(&s.bar_m1, 1);
     tc::mbar_init(&s.bar_m2, 1);
     tc::mbar_fence_init();
-    tc::mbar_arrive_expect_tx(&s.bar_s0, 2 * DK * DK * 2);
-    tc::bulk_load(s.S0, a.tape + state_off(chunk, h, a.HV), DK * DK * 2, &s.bar_s0);
-    tc::bulk_load(s.dSB, a.dstape + state_off(chunk, h, a.HV), DK * DK * 2, &s.bar_s0);
+    tc::mbar_arrive_expect_tx(&s.bar_t1, DK * DK * 2);
+    tc::bulk_load(s.Tp, a.tape + state_off(chunk, h, a.HV), DK * DK * 2, &s.bar_t1);
   }
   if (warp == 0) {
     tc::tmem_alloc(&s.tmem, TCOLS);
@@ -83,41 +117,13 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
       *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
   }
   cp_async_commit();
-  // Delta and dDelta -> BF16 hi / lo tiles.  Task e: tensor e / 1024, row (e / 16) % 64, piece e % 16.
-  {
-    float4 x[8][2];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = tid + 256 * q;
-      const float* src = e < 1024 ? a.delta + toff + (size_t)((e >> 4) & 63) * DK + (e & 15) * 8
-                                  : a.ddelta + tf_off(chunk, h, a.HV) + (size_t)((e >> 4) & 63) * LDF + (e & 15) * 8;
-      x[q][0] = __ldg(reinterpret_cast<const float4*>(src));
-      x[q][1] = __ldg(reinterpret_cast<const float4*>(src) + 1);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = tid + 256 * q;
-      const int i = (e >> 4) & 63, kc = e & 15;
-      const float f[8] = {x[q][0].x, x[q][0].y, x[q][0].z, x[q][0].w, x[q][1].x, x[q][1].y, x[q][1].z, x[q][1].w};
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * p]), h1 = __float2bfloat16_rn(f[2 * p + 1]);
-        const __nv_bfloat16 l0 = __float2bfloat16_rn(f[2 * p] - __bfloat162float(h0));
-        const __nv_bfloat16 l1 = __float2bfloat16_rn(f[2 * p + 1] - __bfloat162float(h1));
-        hi[p] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lo[p] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-      }
-      const uint32_t off = tc::sw128_bf16_piece(i, kc, CH);
-      unsigned char* th = reinterpret_cast<unsigned char*>(e < 1024 ? s.Dh : s.Eh);
-      unsigned char* tl = reinterpret_cast<unsigned char*>(e < 1024 ? s.Dl : s.El);
-      *reinterpret_cast<uint4*>(th + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(tl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-  }
+  float4 x[4][2];
+  load_hilo_rows(a.ddelta + tf_off(chunk, h, a.HV), LDF, x);
+  store_hilo_rows(x, s.Hi, s.Lo);
+  load_hilo_rows(a.delta + toff, DK, x);  // Delta, for the second phase: its latency hides behind the first
   cp_async_wait<0>();
   tc::fence_proxy_async();
-  bool ok = tc::mbar_wait(&s.bar_s0, 0);
+  bool ok = tc::mbar_wait(&s.bar_t1, 0);
   tc::tc_fence_before();
   ok = __syncthreads_and(ok);
   tc::tc_fence_after();
@@ -129,56 +135,17 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
   auto bmn = [](const uint16_t* tile, int k) { return tc::desc_mn_none(tile + k * 16 * 8, 128, DK * 16); };
   if (ok && tid == 0) {
     const uint64_t aO = tc::desc_k_sw128(s.dO);
-    const uint64_t aEh = tc::desc_k_sw128(s.Eh), aEl = tc::desc_k_sw128(s.El);
-    const uint64_t bDh = tc::desc_k_sw128(s.Dh), bDl = tc::desc_k_sw128(s.Dl);
+    const uint64_t aH = tc::desc_k_sw128(s.Hi), aL = tc::desc_k_sw128(s.Lo);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem, tc::kstep32(aO, k, CH), bmn(s.S0, k), id128t, k > 0);
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem, tc::kstep32(aO, k, CH), bmn(s.Tp, k), id128t, k > 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aEh, k, CH), bmn(s.S0, k), id128t, k > 0);
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aH, k, CH), bmn(s.Tp, k), id128t, k > 0);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aEl, k, CH), bmn(s.S0, k), id128t, 1);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 384, tc::kstep32(aO, k, CH), tc::kstep32(bDh, k, CH), id64, k > 0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 384, tc::kstep32(aO, k, CH), tc::kstep32(bDl, k, CH), id64, 1);
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aL, k, CH), bmn(s.Tp, k), id128t, 1);
     tc::mma_commit(&s.bar_m1);
   }
-  if (ok && tid == 0) {
-    const uint64_t aDh = tc::desc_k_sw128(s.Dh), aDl = tc::desc_k_sw128(s.Dl);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 256, tc::kstep32(aDh, k, CH), bmn(s.dSB, k), id128t, k > 0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 256, tc::kstep32(aDl, k, CH), bmn(s.dSB, k), id128t, 1);
-    tc::mma_commit(&s.bar_m2);
-  }
-  {  // dgam[c] = sum_v S0[c][v] dS[c][v]: thread (q, vg) sums channels 8 q .. 8 q + 7 over
-     // value columns vg, vg + 16, ..; the 16 partial sums of a channel group are then
-     // added within the half warp in a fixed order.
-    const int q = tid >> 4, vg = tid & 15;
-    const uint4* p0 = reinterpret_cast<const uint4*>(s.S0) + q * DK;
-    const uint4* p1 = reinterpret_cast<const uint4*>(s.dSB) + q * DK;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const uint4 x = p0[vg + 16 * r], y = p1[vg + 16 * r];
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        acc[2 * p] += __uint_as_float(xs[p] << 16) * __uint_as_float(ys[p] << 16);
-        acc[2 * p + 1] += __uint_as_float(xs[p] & 0xffff0000u) * __uint_as_float(ys[p] & 0xffff0000u);
-      }
-    }
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-    if (vg == 0) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) a.dgam[((size_t)chunk * a.HV + h) * DK + 8 * q + e] = acc[e];
-    }
-  }
-  // Epilogue: warp w reads the rows of TMEM lane quadrant w % 4 (tokens 16 (w % 4) ..)
-  // and half w / 4 of the columns.
+  // Epilogue helpers: warp w reads the rows of TMEM lane quadrant w % 4 (tokens
+  // 16 (w % 4) ..) and half w / 4 of the columns.
   const int quad = warp & 3, hf = warp >> 2, g = lane >> 2, u2 = (lane & 3) * 2;
   const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
   auto drain = [&](uint32_t col0, int ncols, auto&& store) {  // ncols multiple of 16
@@ -196,7 +163,12 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
   };
   const bool ok1 = __syncthreads_and(ok && tc::mbar_wait(&s.bar_m1, 0));  // uniform: the loads below are warp-wide
   tc::tc_fence_after();
+  if (ok1 && tid == 0) {  // the S0 tape's products are done: the dS tape into its place
+    tc::mbar_arrive_expect_tx(&s.bar_t2, DK * DK * 2);
+    tc::bulk_load(s.Tp, a.dstape + state_off(chunk, h, a.HV), DK * DK * 2, &s.bar_t2);
+  }
   if (ok1) {
+    store_hilo_rows(x, s.Hi, s.Lo);  // Delta hi / lo in dDelta's place
     const int c0 = 64 * hf;
     drain(c0, 64, [&](int i, int c, float x0, float x1) {
       *reinterpret_cast<float2*>(&a.dqs[toff + i * DK + c0 + c]) = make_float2(a.scale * x0, a.scale * x1);
@@ -204,30 +176,72 @@ __global__ void __launch_bounds__(256, 1) k_grad_state(const __grid_constant__ G
     drain(128 + c0, 64, [&](int i, int c, float x0, float x1) {
       *reinterpret_cast<float2*>(&a.dw[tf_off(chunk, h, a.HV) + i * LDF + c0 + c]) = make_float2(-x0, -x1);
     });
+  }
+  tc::fence_proxy_async();
+  tc::tc_fence_before();
+  const bool ok2 = __syncthreads_and(ok1 && tc::mbar_wait(&s.bar_t2, 0));
+  tc::tc_fence_after();
+  if (ok2 && tid == 0) {
+    const uint64_t aO = tc::desc_k_sw128(s.dO);
+    const uint64_t aH = tc::desc_k_sw128(s.Hi), aL = tc::desc_k_sw128(s.Lo);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem, tc::kstep32(aH, k, CH), bmn(s.Tp, k), id128t, k > 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem, tc::kstep32(aL, k, CH), bmn(s.Tp, k), id128t, 1);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aO, k, CH), tc::kstep32(aH, k, CH), id64, k > 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tc::mma_bf16(tmem + 128, tc::kstep32(aO, k, CH), tc::kstep32(aL, k, CH), id64, 1);
+    tc::mma_commit(&s.bar_m2);
+  }
+  if (ok2) {  // dgam[c] = sum_v S0[c][v] dS[c][v]: thread (q, vg) sums channels 8 q .. 8 q + 7 over
+              // value columns vg, vg + 16, ..; the 16 partial sums of a channel group are then
+              // added within the half warp in a fixed order.  S0 from the tape in memory.
+    const int q = tid >> 4, vg = tid & 15;
+    const uint4* p0 = reinterpret_cast<const uint4*>(a.tape + state_off(chunk, h, a.HV)) + q * DK;
+    const uint4* p1 = reinterpret_cast<const uint4*>(s.Tp) + q * DK;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const uint4 xs4 = __ldg(p0 + vg + 16 * r), y = p1[vg + 16 * r];
+      const uint32_t xs[4] = {xs4.x, xs4.y, xs4.z, xs4.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        acc[2 * p] += __uint_as_float(xs[p] << 16) * __uint_as_float(ys[p] << 16);
+        acc[2 * p + 1] += __uint_as_float(xs[p] & 0xffff0000u) * __uint_as_float(ys[p] & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    if (vg == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a.dgam[((size_t)chunk * a.HV + h) * DK + 8 * q + e] = acc[e];
+    }
+  }
+  const bool ok3 = __syncthreads_and(ok2 && tc::mbar_wait(&s.bar_m2, 0));
+  tc::tc_fence_after();
+  if (ok3) {
+    const int c0 = 64 * hf;
+    drain(c0, 64, [&](int i, int c, float x0, float x1) {
+      *reinterpret_cast<float2*>(&a.dkd[toff + i * DK + c0 + c]) = make_float2(x0, x1);
+    });
     float* daqk = a.daqk + ts_off(chunk, h, a.HV);
     const int j0 = 32 * hf;
-    drain(384 + j0, 32, [&](int i, int c, float x0, float x1) {
+    drain(128 + j0, 32, [&](int i, int c, float x0, float x1) {
       const int j = j0 + c;
       *reinterpret_cast<float2*>(&daqk[i * LDS + j]) =
           make_float2(j <= i ? a.scale * x0 : 0.f, j + 1 <= i ? a.scale * x1 : 0.f);
     });
   }
-  const bool ok2 = __syncthreads_and(ok && tc::mbar_wait(&s.bar_m2, 0));
-  tc::tc_fence_after();
-  if (ok2) {
-    const int c0 = 64 * hf;
-    drain(256 + c0, 64, [&](int i, int c, float x0, float x1) {
-      *reinterpret_cast<float2*>(&a.dkd[toff + i * DK + c0 + c]) = make_float2(x0, x1);
-    });
-  }
-  if (tid == 0 && !(ok1 && ok2)) {
+  if (tid == 0 && !ok3) {
     // A wait ran out: record it and let the copies and products in flight finish.
     atomicExch(a.err, 6);
-    tc::mbar_wait(&s.bar_s0, 0);
-    if (ok) {
-      tc::mbar_wait(&s.bar_m1, 0);
-      tc::mbar_wait(&s.bar_m2, 0);
-    }
+    tc::mbar_wait(&s.bar_t1, 0);
+    if (ok) tc::mbar_wait(&s.bar_m1, 0);
+    if (ok1) tc::mbar_wait(&s.bar_t2, 0);
+    if (ok2) tc::mbar_wait(&s.bar_m2, 0);
   }
   tc::tc_fence_before();
   __syncthreads();
