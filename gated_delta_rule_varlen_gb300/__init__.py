@@ -49,6 +49,7 @@ EXPORTED = (
     "gdr_launch_count",
     "gdr_set_serial",
     "gdr_set_segment_chunks",
+    "gdr_set_slice_chunks",
 )
 
 _lock = threading.Lock()
@@ -73,6 +74,7 @@ _SIGS = {
     "gdr_launch_count": ([], ctypes.c_uint64),
     "gdr_set_serial": ([ctypes.c_int], ctypes.c_int),
     "gdr_set_segment_chunks": ([ctypes.c_int], ctypes.c_int),
+    "gdr_set_slice_chunks": ([ctypes.c_int], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, ctypes.c_int, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, ctypes.c_int, PSZ, PSZ], ctypes.c_int),
     "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, ctypes.c_int, P, P, P, P, SZ, ctypes.c_int, P, SZ, P],
@@ -295,6 +297,11 @@ def gdr_set_segment_chunks(chunks: int) -> int:
     """Force walk segments of about `chunks` chunks (0: the library's choice);
     returns the previous setting."""
     return int(load().gdr_set_segment_chunks(int(chunks)))
+
+
+def gdr_set_slice_chunks(chunks: int) -> int:
+    """Slice length (chunks) of pipelined walks, 0 for the default; returns the previous setting."""
+    return int(load().gdr_set_slice_chunks(int(chunks)))
 
 
 def gdr_profile_enable(on: bool = True):

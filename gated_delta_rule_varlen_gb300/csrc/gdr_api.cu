@@ -1,6 +1,7 @@
 // gdr_api.cu -- the C ABI (include/gdr.h): validation, planning, workspace
 // layout, the saved-buffer stamp, and the launch sequences.
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -253,7 +254,7 @@ struct Layout {
   size_t header = 0;                             // SavedHeader (saved buffers)
   size_t bdocs = 0, bchunks = 0, border = 0, bsegs = 0;  // the backward's own plan (scratch)
   size_t docs = 0, chunks = 0, order = 0, segs = 0, w = 0, u = 0, qp = 0, kd = 0, delta = 0, aqk = 0, amat = 0,
-         tmat = 0, gam = 0, tape = 0, smap = 0, sstart = 0, sbias = 0;
+         tmat = 0, gam = 0, tape = 0, smap = 0, sstart = 0, sbias = 0, fcarry = 0, bcarry = 0;
   size_t saved_total = 0;
   size_t qn = 0, kn = 0, rq = 0, rk = 0;  // in-kernel q/k L2 normalization
   size_t dstape = 0, ddelta = 0, dqs = 0, dw = 0, dkd = 0, dgam = 0, daqk = 0, dqp = 0, dkp = 0, dsend = 0, dsbias = 0;
@@ -286,6 +287,7 @@ Layout make_layout(int64_t T, int64_t NC, int32_t N, int32_t Hqk, int32_t HV, bo
   L.smap = take(segstate);    // each split segment's state map (the backward merge needs it too)
   L.sstart = take(segstate);  // start state of each segment
   L.sbias = take(segstate);   // each segment's end state from a zero start
+  L.fcarry = take((size_t)std::max<int64_t>(NSEG, 1) * HV * DK * DK * sizeof(float));  // pipelined walks
   L.w = take((size_t)NC * HV * CH * DK * sizeof(__half));
   L.u = take((size_t)NC * HV * CH * LDF * sizeof(__half));
   L.qp = take((size_t)NC * HV * CH * DK * sizeof(__half));
@@ -319,6 +321,7 @@ Layout make_layout(int64_t T, int64_t NC, int32_t N, int32_t Hqk, int32_t HV, bo
   L.daqk = take((size_t)NC * HV * CH * LDS * sizeof(float));
   L.dsend = take(segstate);   // adjoint of each segment's end state
   L.dsbias = take(segstate);  // each segment's start adjoint from a zero end adjoint
+  L.bcarry = take((size_t)std::max<int64_t>(NSEG, 1) * HV * DK * DK * sizeof(float));  // pipelined walks
   if (grouped) {
     L.dqp = take(tile);
     L.dkp = take(tile);
@@ -555,16 +558,20 @@ struct ProfScope {
 // caller's stream around them.  A single group runs on the caller's stream.
 // ---------------------------------------------------------------------------
 std::mutex g_lane_mu;
-cudaStream_t g_lanes[64][kMaxGroups] = {};
+// Lane i is group i's first lane (its walks), lane kMaxGroups + i its second
+// (the prep or the gradient kernels of a pipelined walk), at a lower priority
+// so that the walk slices win the SMs that free up.
+constexpr int kLanes = 2 * kMaxGroups;
+cudaStream_t g_lanes[64][kLanes] = {};
 
 const cudaStream_t* lanes_for_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lk(g_lane_mu);
-  if (!g_lanes[dev][kMaxGroups - 1]) {
+  if (!g_lanes[dev][kLanes - 1]) {
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
-    for (int i = 0; i < kMaxGroups; ++i) {
+    for (int i = 0; i < kLanes; ++i) {
       if (g_lanes[dev][i]) continue;
       const int prio = std::min(least, greatest + i);  // numerically lower = higher priority
       if (cudaStreamCreateWithPriority(&g_lanes[dev][i], cudaStreamNonBlocking, prio) != cudaSuccess) {
@@ -578,37 +585,43 @@ const cudaStream_t* lanes_for_device() {
 
 class Fork {
  public:
-  Fork(cudaStream_t main, int n) : main_(main), n_(g_serial.load() ? 1 : n) {}
+  // n groups; `second`: some group also uses its second lane.
+  Fork(cudaStream_t main, int n, bool second = false)
+      : main_(main), n_(g_serial.load() ? 1 : n), on_(!g_serial.load() && (n > 1 || second)) {}
   Fork(const Fork&) = delete;
   Fork& operator=(const Fork&) = delete;
   // Makes every lane wait for the work already on the caller's stream.
   bool begin() {
-    if (n_ <= 1) return true;
+    if (!on_) return true;
     lanes_ = lanes_for_device();
     if (!lanes_) return false;
     cudaEvent_t ev;
     if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return false;
     bool ok = cudaEventRecord(ev, main_) == cudaSuccess;
-    for (int i = 0; ok && i < n_; ++i) ok = cudaStreamWaitEvent(lanes_[i], ev, 0) == cudaSuccess;
+    for (int i = 0; ok && i < n_; ++i)
+      ok = cudaStreamWaitEvent(lanes_[i], ev, 0) == cudaSuccess &&
+           cudaStreamWaitEvent(lanes_[kMaxGroups + i], ev, 0) == cudaSuccess;
     cudaEventDestroy(ev);
     forked_ = ok;
     return ok;
   }
-  cudaStream_t lane(int i) const { return n_ > 1 ? lanes_[i] : main_; }
+  cudaStream_t lane(int i) const { return on_ ? lanes_[i] : main_; }
+  cudaStream_t lane2(int i) const { return on_ ? lanes_[kMaxGroups + i] : main_; }
+  // Makes `to` wait for the work enqueued so far on `from`.
+  static bool link(cudaStream_t from, cudaStream_t to) {
+    if (from == to) return true;
+    cudaEvent_t ev;
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return false;
+    const bool ok = cudaEventRecord(ev, from) == cudaSuccess && cudaStreamWaitEvent(to, ev, 0) == cudaSuccess;
+    cudaEventDestroy(ev);
+    return ok;
+  }
   // Makes the caller's stream wait for everything enqueued on the lanes.
   bool join() {
     if (!forked_) return true;
     forked_ = false;
     bool ok = true;
-    for (int i = 0; i < n_; ++i) {
-      cudaEvent_t ev;
-      if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
-        ok = false;
-        continue;
-      }
-      ok = cudaEventRecord(ev, lanes_[i]) == cudaSuccess && cudaStreamWaitEvent(main_, ev, 0) == cudaSuccess && ok;
-      cudaEventDestroy(ev);
-    }
+    for (int i = 0; i < n_; ++i) ok = link(lanes_[i], main_) && link(lanes_[kMaxGroups + i], main_) && ok;
     return ok;
   }
   ~Fork() { join(); }
@@ -616,10 +629,23 @@ class Fork {
  private:
   cudaStream_t main_;
   int n_;
+  bool on_;
   const cudaStream_t* lanes_ = nullptr;
   bool forked_ = false;
 };
 
+// Slices of a pipelined walk (chunks, even): the walk of a group that holds
+// one unsplit document longer than a slice runs slice by slice (the state, or
+// the adjoint, passed on exactly in FP32 through a carry buffer), so that the
+// forward walk starts once the first slice is prepared, and the backward's
+// gradient kernels of a slice run while the walk goes on with the next one.
+constexpr int kSliceChunks = 128;
+std::atomic<int> g_slice_chunks{0};  // gdr_set_slice_chunks: 0 = kSliceChunks
+int slice_chunks() {
+  const int v = g_slice_chunks.load();
+  return v > 0 ? v : kSliceChunks;
+}
+bool pipelined(const DocGroup& G, int S) { return !G.split && G.r1 - G.r0 == 1 && G.c1 - G.c0 > S; }
 
 template <typename T>
 T* at(void* base, size_t off) {
@@ -757,26 +783,51 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
   wa.out = static_cast<__nv_bfloat16*>(out);
   wa.scale = scale;
   // Document groups as in the backward: each group's walk needs only its own
-  // prep, so the longest document's walk starts once its chunks are prepared.
+  // prep, so the longest document's walk starts once its chunks are prepared;
+  // a pipelined group's walk starts once its first slice is (prep slices on
+  // the group's second lane, walk slices on its first).
+  wa.carry = at<float>(base, L.fcarry);
+  wa.m0 = 0;
+  wa.m1 = INT_MAX;
   {
-    Fork fork(stream, (int)groups.size());
+    const int S = slice_chunks();
+    bool any_pipe = false;
+    for (const DocGroup& G : groups) any_pipe = any_pipe || pipelined(G, S);
+    Fork fork(stream, (int)groups.size(), any_pipe);
     if (!fork.begin()) return GDR_CUDA_ERROR;
+    auto prep = [&](int64_t c0, int nc, double units, cudaStream_t ls) {
+      ProfScope ps("prep", ls, units);
+      pa.chunk_base = (int)c0;
+      if (vec) return cuda_status(launch_prep(pa, nc, ls));
+      pt.p = pa;
+      return cuda_status(launch_prep_gdn(pt, nc, ls));
+    };
     for (size_t i = 0; i < groups.size() && st == GDR_OK; ++i) {
       const DocGroup& G = groups[i];
       const cudaStream_t ls = fork.lane((int)i);
       const double units = (double)G.tokens * HV;
       const int nsg = (int)(G.s1 - G.s0);
-      pa.chunk_base = (int)G.c0;
       wa.seg_base = ma.seg_base = (int)G.s0;
-      {
-        ProfScope ps("prep", ls, units);
-        if (vec) {
-          st = cuda_status(launch_prep(pa, (int)(G.c1 - G.c0), ls));
-        } else {
-          pt.p = pa;
-          st = cuda_status(launch_prep_gdn(pt, (int)(G.c1 - G.c0), ls));
+      if (pipelined(G, S)) {
+        const cudaStream_t lp = fork.lane2((int)i);
+        const int nch = (int)(G.c1 - G.c0);
+        wa.mode = 0;
+        for (int m0 = 0; m0 < nch && st == GDR_OK; m0 += S) {
+          const int nc = std::min(S, nch - m0);
+          const double su = (double)std::min<int64_t>((int64_t)nc * CH, G.tokens - (int64_t)m0 * CH) * HV;
+          st = prep(G.c0 + m0, nc, su, lp);
+          if (st == GDR_OK && !Fork::link(lp, ls)) st = GDR_CUDA_ERROR;
+          if (st != GDR_OK) break;
+          wa.m0 = m0;
+          wa.m1 = m0 + nc;
+          ProfScope ps("walk_fwd", ls, su);
+          st = cuda_status(launch_walk_fwd_v(wa, nsg, ls));
         }
+        wa.m0 = 0;
+        wa.m1 = INT_MAX;
+        continue;
       }
+      st = prep(G.c0, (int)(G.c1 - G.c0), units, ls);
       if (st != GDR_OK) break;
       if (G.split) {
         wa.mode = 1;
@@ -824,10 +875,11 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   std::vector<DocGroup> groups = plan_groups(N, cu_host);
   const int64_t NSEG = assign_segments(groups, N, cu_host, lseg);
   const Layout L = make_layout(T, NC, N, Hqk, HV, l2 != 0, NSEG);
-  if (saved_bytes < L.saved_total || scratch_bytes < L.bwd_total) return GDR_WORKSPACE_TOO_SMALL;
+  // A buffer this process filled for other arguments is stale whatever its size.
   Stamp want{T, N, Hqk, HV, variant, lseg, l2 != 0, hash_cu(cu_host, N), 0};
   const StampState known = stamp_check(saved, want, &want.counter);
   if (known == StampState::kMismatch) return GDR_STALE_WORKSPACE;
+  if (saved_bytes < L.saved_total || scratch_bytes < L.bwd_total) return GDR_WORKSPACE_TOO_SMALL;
   st = check_device();
   if (st != GDR_OK) return st;
   int* err = device_error_ptr();
@@ -943,8 +995,33 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
   // Document groups (longest documents first, each on a stream of its own):
   // a group's gradient kernels need only its own walk, so the gradients of the
   // documents whose walks end first run on the SMs the other walks leave idle.
-  Fork fork(stream, (int)groups.size());
+  // Per group: its adjoint walk, then the gradient kernels of its chunks; a
+  // pipelined group's walk runs slice by slice (last slice first) on its first
+  // lane and each slice's gradient kernels on its second, while the walk goes on.
+  wb.carry = at<float>(scratch, L.bcarry);
+  wb.m0 = 0;
+  wb.m1 = INT_MAX;
+  const int S = slice_chunks();
+  bool any_pipe = false;
+  for (const DocGroup& G : groups) any_pipe = any_pipe || pipelined(G, S);
+  Fork fork(stream, (int)groups.size(), any_pipe);
   if (!fork.begin()) return GDR_CUDA_ERROR;
+  auto grads = [&](int64_t c0, int nc, double units, cudaStream_t ls) {
+    gs.chunk_base = ga.chunk_base = gr.chunk_base = (int)c0;
+    gdr_status r;
+    {
+      ProfScope ps("grad_state", ls, units);
+      r = cuda_status(launch_grad_state(gs, nc, ls));
+    }
+    if (r != GDR_OK) return r;
+    {
+      ProfScope ps("grad", ls, units);
+      r = cuda_status(launch_grad(ga, nc, vec, vec, ls));
+    }
+    if (r != GDR_OK || !grouped) return r;
+    ProfScope ps("group_reduce", ls, units);
+    return cuda_status(launch_group_reduce(gr, nc, ls));
+  };
 
   for (size_t i = 0; i < groups.size() && st == GDR_OK; ++i) {
     const DocGroup& G = groups[i];
@@ -952,7 +1029,25 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
     const double units = (double)G.tokens * HV;
     const int nc = (int)(G.c1 - G.c0), nsg = (int)(G.s1 - G.s0);
     wb.seg_base = mb.seg_base = (int)G.s0;
-    gs.chunk_base = ga.chunk_base = gr.chunk_base = (int)G.c0;
+    if (pipelined(G, S)) {
+      const cudaStream_t lg = fork.lane2((int)i);
+      wb.mode = 0;
+      for (int m0 = ((nc - 1) / S) * S; m0 >= 0 && st == GDR_OK; m0 -= S) {
+        const int sn = std::min(S, nc - m0);
+        const double su = (double)std::min<int64_t>((int64_t)sn * CH, G.tokens - (int64_t)m0 * CH) * HV;
+        wb.m0 = m0;
+        wb.m1 = m0 + sn;
+        {
+          ProfScope ps("walk_bwd", ls, su);
+          st = cuda_status(launch_walk_bwd_v(wb, nsg, ls));
+        }
+        if (st == GDR_OK && !Fork::link(ls, lg)) st = GDR_CUDA_ERROR;
+        if (st == GDR_OK) st = grads(G.c0 + m0, sn, su, lg);
+      }
+      wb.m0 = 0;
+      wb.m1 = INT_MAX;
+      continue;
+    }
     if (G.split) {
       wb.mode = 1;
       {
@@ -972,20 +1067,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
       st = cuda_status(launch_walk_bwd_v(wb, nsg, ls));
     }
     if (st != GDR_OK) break;
-    {
-      ProfScope ps("grad_state", ls, units);
-      st = cuda_status(launch_grad_state(gs, nc, ls));
-    }
-    if (st != GDR_OK) break;
-    {
-      ProfScope ps("grad", ls, units);
-      st = cuda_status(launch_grad(ga, nc, vec, vec, ls));
-    }
-    if (st != GDR_OK || !grouped) continue;
-    {
-      ProfScope ps("group_reduce", ls, units);
-      st = cuda_status(launch_group_reduce(gr, nc, ls));
-    }
+    st = grads(G.c0, nc, units, ls);
   }
   if (!fork.join() && st == GDR_OK) st = GDR_CUDA_ERROR;
   if (st != GDR_OK) return st;
@@ -1163,6 +1245,10 @@ uint64_t gdr_launch_count(void) { return gdr::g_launches.load(); }
 int gdr_set_serial(int on) { return gdr::g_serial.exchange(on != 0) ? 1 : 0; }
 
 int gdr_set_segment_chunks(int chunks) { return gdr::g_seg_chunks.exchange(chunks > 0 ? chunks : 0); }
+
+int gdr_set_slice_chunks(int chunks) {
+  return gdr::g_slice_chunks.exchange(chunks > 0 ? std::max(2, chunks & ~1) : 0);
+}
 
 int gdr_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(gdr::g_prof_mu);

@@ -66,6 +66,11 @@ struct WalkArgs {
   int* err;          // device error word
   int seg_base;      // segments seg_base + blockIdx.x / HV
   int mode;          // 0 the full walks, 1 the summary walks (blockIdx.y: role)
+  // Full walks: the chunk range [m0, m1) of every segment (m0 even; m1 past
+  // the end for all of it), and per (segment, head) the carry state
+  // [NSEG][HV][128][128] that passes between the slices of a pipelined walk.
+  int m0, m1;
+  float* carry;
 };
 
 
@@ -86,6 +91,8 @@ struct WalkBwdArgs {
   int* err;                   // device error word
   int seg_base;
   int mode;                   // 0 the full walks, 1 the summary walks (blockIdx.y: role)
+  int m0, m1;                 // full walks: the chunk range, as for the forward walk
+  float* carry;               // the carry adjoint between slices [NSEG][HV][128][128]
 };
 
 // Merges of the segment states of split documents (one CTA per (segment,

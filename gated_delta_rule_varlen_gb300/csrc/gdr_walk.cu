@@ -90,14 +90,21 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
     if (!on) return;
   }
   const bool outputs = kind == 0, use_u = kind != 3;
+  // The chunks of this launch, [mb, me) of the segment: all of them, or one
+  // slice of a pipelined walk (mb even), which starts from the previous
+  // slice's end state and leaves its own in the carry buffer.
+  if (kind == 0 && a.m0 > 0 && a.m0 >= n) return;
+  const int mb = kind == 0 ? min(a.m0, n) : 0, me = kind == 0 ? min(a.m1, n) : n;
   // Start and end states (S[c][v]): h0 / ht of the document, or per-segment
   // buffers [NSEG][HV][128][128].
   auto start_state = [&]() -> const float* {
     const size_t sidx = ((size_t)dd.doc * a.HV + h) * DK * DK, gidx = ((size_t)seg * a.HV + h) * DK * DK;
+    if (kind == 0 && mb > 0) return a.carry + gidx;
     return (kind == 0 && dd.idx > 0) ? a.sstart + gidx : (kind <= 1 && a.h0 ? a.h0 + sidx : nullptr);
   };
   auto end_state = [&]() -> float* {
     const size_t sidx = ((size_t)dd.doc * a.HV + h) * DK * DK, gidx = ((size_t)seg * a.HV + h) * DK * DK;
+    if (kind == 0 && me < n) return a.carry + gidx;
     return kind == 0   ? (dd.idx == dd.nseg - 1 && a.ht ? a.ht + sidx : nullptr)
            : kind == 1 ? a.sstart + gidx + (size_t)a.HV * DK * DK
            : kind == 2 ? a.sbias + gidx
@@ -182,11 +189,11 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
   }
   // Copies issued and consumed (issuer), for the drain after a timeout.
   int b1_iss[2] = {0, 0}, b1_got[2] = {0, 0}, b2_iss = 0, b2_got = 0, u_iss = 0, u_got = 0, s1_iss = 0, s2_iss = 0;
-  if (issuer && n > 0) {
-    issue_b1(0), ++b1_iss[0];
-    if (n > 1) issue_b1(1), ++b1_iss[1];
-    issue_b2(0), ++b2_iss;
-    if (use_u) issue_u(0), ++u_iss;
+  if (issuer && me > mb) {
+    issue_b1(mb), ++b1_iss[0];
+    if (me - mb > 1) issue_b1(mb + 1), ++b1_iss[1];
+    issue_b2(mb), ++b2_iss;
+    if (use_u) issue_u(mb), ++u_iss;
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -194,16 +201,17 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
 
   constexpr uint32_t kId1 = tc::idesc_f16(128, 128), kId2 = tc::idesc_f16(128, 192);
   bool ok = true;
-  int m = 0;
-  for (; m < n; ++m) {
+  int m = mb;
+  for (; m < me; ++m) {
+    const int mm = m - mb;  // barrier phases count from the launch's first chunk
     const int b = m & 1;
     const int chunk = dd.chunk0 + m;
     if (data) {
-      if (m > 0) {
-        ok = tc::mbar_wait(&s.bar_s2, (m - 1) & 1) && ok;  // S0 of this chunk, O of the previous one
+      if (mm > 0) {
+        ok = tc::mbar_wait(&s.bar_s2, (mm - 1) & 1) && ok;  // S0 of this chunk, O of the previous one
         tc::tc_fence_after();
       }
-      ok = tc::mbar_wait(&s.bar_b1[b], (m >> 1) & 1) && ok;  // gamma of this chunk
+      ok = tc::mbar_wait(&s.bar_b1[b], (mm >> 1) & 1) && ok;  // gamma of this chunk
       // Columns 64 hf .. 64 hf + 63 in two halves: the tape tile (chunk-major: 512
       // contiguous bytes per warp and 8-channel piece), S0' = S0 rounded to FP16
       // (the A operand, two channels per column), and diag(gamma) S0 into S.  (Scaling S while [P | O]
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
     if (!named_sync_and(1, WALKV_THREADS, ok)) break;  // S0', diag(gamma) S0 in place
     tc::tc_fence_after();
     if (issuer) {
-      ok = tc::mbar_wait(&s.bar_b1[b], (m >> 1) & 1) && ok;  // complete: the data threads waited for it
+      ok = tc::mbar_wait(&s.bar_b1[b], (mm >> 1) & 1) && ok;  // complete: the data threads waited for it
       ++b1_got[b];
       tc::tc_fence_after();
       const uint64_t bd = tc::desc_k_sw128(s.B1[b]);
@@ -255,11 +263,11 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
     }
     if (data) {
       // While [P | O] runs: the previous chunk's output.
-      if (outputs && m > 0) drain_out(m - 1);
+      if (outputs && mm > 0) drain_out(m - 1);
       // Delta = u - P (rows j = 32 hf ..) in FP32 in place (for the backward),
       // and its FP16 copy (the A operand of the second product).
-      ok = tc::mbar_wait(&s.bar_s1, m & 1) && ok;
-      if (use_u) ok = tc::mbar_wait(&s.bar_u, m & 1) && ok;
+      ok = tc::mbar_wait(&s.bar_s1, mm & 1) && ok;
+      if (use_u) ok = tc::mbar_wait(&s.bar_u, mm & 1) && ok;
       tc::tc_fence_after();
       uint32_t r[32];
       tc::tmem_ld32(tl + colPd(b) + 32 * hf, r);
@@ -311,16 +319,16 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       // Refills: stage b of [w ; Qp] (its product is done) with chunk m + 2,
       // u (read before the barrier) and, once the update is done, [Kd^T ;
       // Aqk] with chunk m + 1.
-      if (ok && m + 2 < n) issue_b1(m + 2), ++b1_iss[b];
-      if (ok && m + 1 < n) {
+      if (ok && m + 2 < me) issue_b1(m + 2), ++b1_iss[b];
+      if (ok && m + 1 < me) {
         if (use_u) issue_u(m + 1), ++u_iss;
-        const bool r3 = tc::mbar_wait(&s.bar_s2, m & 1);
+        const bool r3 = tc::mbar_wait(&s.bar_s2, mm & 1);
         ok = r3 && ok;
         if (r3) issue_b2(m + 1), ++b2_iss;
       }
     }
   }
-  if (m < n) {
+  if (m < me) {
     // A wait ran out: record it and drain the copies and products in flight.
     if (issuer) {
       atomicExch(a.err, 3);
@@ -332,10 +340,10 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_fwd_v(const __grid_co
       if (s2_iss > 0) tc::mbar_wait(&s.bar_s2, (s2_iss - 1) & 1);
     }
   } else if (data) {
-    if (n > 0) {
-      ok = tc::mbar_wait(&s.bar_s2, (n - 1) & 1) && ok;
+    if (me > mb) {
+      ok = tc::mbar_wait(&s.bar_s2, (me - 1 - mb) & 1) && ok;
       tc::tc_fence_after();
-      if (ok && outputs) drain_out(n - 1);
+      if (ok && outputs) drain_out(me - 1);
     }
     float* end = end_state();
     if (end && ok) {  // end[c][v] = S^T[v][c]
@@ -474,14 +482,22 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
     if (!on) return;
   }
   const bool outputs = kind == 0;
+  // The chunks of this launch, [mb, me) of the segment walked from me - 1
+  // down: all of them, or one slice of a pipelined walk (mb even), which
+  // starts from the adjoint the later slice left in the carry buffer and
+  // leaves its own there.
+  if (kind == 0 && a.m0 > 0 && a.m0 >= n) return;
+  const int mb = kind == 0 ? min(a.m0, n) : 0, me = kind == 0 ? min(a.m1, n) : n, cnt = me - mb;
   // Start (end-of-segment) and end (start-of-segment) adjoints: dht / dh0 of the
   // document, or per-segment buffers [NSEG][HV][128][128].
   auto start_adj = [&]() -> const float* {
     const size_t sidx = ((size_t)dd.doc * a.HV + h) * DK * DK, gidx = ((size_t)seg * a.HV + h) * DK * DK;
+    if (kind == 0 && me < n) return a.carry + gidx;
     return (kind == 0 && dd.idx < dd.nseg - 1) ? a.dsend + gidx : (kind <= 1 && a.dht ? a.dht + sidx : nullptr);
   };
   auto end_adj = [&]() -> float* {
     const size_t sidx = ((size_t)dd.doc * a.HV + h) * DK * DK, gidx = ((size_t)seg * a.HV + h) * DK * DK;
+    if (kind == 0 && mb > 0) return a.carry + gidx;
     return kind == 0   ? (dd.idx == 0 && a.dh0 ? a.dh0 + sidx : nullptr)
            : kind == 1 ? a.dsend + gidx - (size_t)a.HV * DK * DK
                        : a.dsbias + gidx;
@@ -566,18 +582,18 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       }
       tc::tmem_st32(tl + kBColS + 64 * hf + cb, r);
     }
-    if (n > 0) {
-      load_do(n - 1, don);
-      store_do(n - 1, 0, don);
+    if (cnt > 0) {
+      load_do(me - 1, don);
+      store_do(me - 1, 0, don);
     }
-    if (n > 1) load_do(n - 2, don);
+    if (cnt > 1) load_do(me - 2, don);
     tc::tmem_wait_st();
   }
   int k_iss = 0, a_iss = 0, w_iss = 0, k_got = 0, a_got = 0, w_got = 0, ab_iss = 0, c_iss = 0;
-  if (issuer && n > 0) {
-    issue_k(n - 1), ++k_iss;
-    issue_a(n - 1), ++a_iss;
-    issue_w(n - 1), ++w_iss;
+  if (issuer && cnt > 0) {
+    issue_k(me - 1), ++k_iss;
+    issue_a(me - 1), ++a_iss;
+    issue_w(me - 1), ++w_iss;
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -586,9 +602,9 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
   constexpr uint32_t kIdB = tc::idesc_tf32(128, 64), kIdA = tc::idesc_tf32(128, 192), kIdC = tc::idesc_tf32(128, 128);
   bool ok = true;
   int st = 0;
-  for (; st < n; ++st) {
+  for (; st < cnt; ++st) {
     const int b = st & 1;
-    const int m = n - 1 - st;
+    const int m = me - 1 - st;
     const int chunk = dd.chunk0 + m;
     if (data) {
       if (st > 0) {
@@ -632,7 +648,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
 #pragma unroll
       for (int k = 0; k < DK / 8; ++k)
         tc::mma_tf32_ta(tm + kBColD, tm + kBColSp + 8 * k, tc::kstep32(bk, k, CH), kIdB, k > 0);
-      if (st + 1 < n) issue_k(m - 1), ++k_iss;  // Kd^T and gamma were read before the barrier
+      if (st + 1 < cnt) issue_k(m - 1), ++k_iss;  // Kd^T and gamma were read before the barrier
     }
     if (data) {
       {  // diag(gamma) dS into place (only the second product accumulates into dS)
@@ -653,8 +669,8 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
         if (g < 8) transpose_group(SA, CH, 16 * (g >> 1), 32 * (g & 1), BA, CH + DK, 0);
         else transpose_group(SQ, CH, 16 * ((g - 8) >> 2), 32 * ((g - 8) & 3), BA, CH + DK, CH);
       }
-      if (st + 1 < n) store_do(m - 1, b ^ 1, don);
-      if (st + 2 < n) load_do(m - 2, don);
+      if (st + 1 < cnt) store_do(m - 1, b ^ 1, don);
+      if (st + 2 < cnt) load_do(m - 2, don);
       tc::fence_proxy_async();
       tc::tmem_wait_st();
     }
@@ -669,7 +685,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
         tc::mma_tf32_ta(tm + kBColD, tm + colDO(b) + 8 * k, tc::kstep32(ba, k, CH + DK), kIdA, 1);
       tc::mma_commit(&s.bar_ab);
       ++ab_iss;
-      if (st + 1 < n) issue_a(m - 1), ++a_iss;
+      if (st + 1 < cnt) issue_a(m - 1), ++a_iss;
     }
     if (data) {
       ok = tc::mbar_wait(&s.bar_w, st & 1) && ok;  // w of this chunk
@@ -704,10 +720,10 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
         tc::mma_tf32_ta(tm + kBColS, tm + kBColDn + 8 * k, tc::kstep32(bw, k, DK), kIdC, 1);
       tc::mma_commit(&s.bar_c);
       ++c_iss;
-      if (st + 1 < n) issue_w(m - 1), ++w_iss;
+      if (st + 1 < cnt) issue_w(m - 1), ++w_iss;
     }
   }
-  if (st < n) {
+  if (st < cnt) {
     // A wait ran out: record it and drain the copies and products in flight.
     if (issuer) {
       atomicExch(a.err, 4);
@@ -718,8 +734,8 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       if (c_iss > 0) tc::mbar_wait(&s.bar_c, (c_iss - 1) & 1);
     }
   } else if (data) {
-    if (n > 0) {
-      ok = tc::mbar_wait(&s.bar_c, (n - 1) & 1) && ok;
+    if (cnt > 0) {
+      ok = tc::mbar_wait(&s.bar_c, (cnt - 1) & 1) && ok;
       tc::tc_fence_after();
     }
     float* end = end_adj();

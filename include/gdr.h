@@ -290,6 +290,16 @@ int gdr_set_serial(int on);
  * returns GDR_STALE_WORKSPACE.  Returns the previous setting. */
 int gdr_set_segment_chunks(int chunks);
 
+/* gdr_set_slice_chunks(chunks): a document group that holds one unsplit
+ * document longer than a slice walks it slice by slice (the state, or the
+ * adjoint, passed on exactly in FP32 between the slices' launches), so that
+ * the forward walk starts once the first slice is prepared and the
+ * backward's gradient kernels of a slice run while the walk goes on with the
+ * next; the results are bit for bit those of the whole walk.  chunks > 0 sets
+ * the slice length (rounded down to an even number, at least 2); 0 restores
+ * the default of 128 chunks.  Process-wide; returns the previous setting. */
+int gdr_set_slice_chunks(int chunks);
+
 #ifdef __cplusplus
 }
 #endif

@@ -502,3 +502,63 @@ def test_gdn_qk_l2norm_grouped():
 
 def test_kda_qk_l2norm_mild_gates_long_document():
     _check_l2("kda", [4096], 1, 1, seed=42, glow=-0.05)
+
+
+# ---------------------------------------------------------------------------
+# Pipelined walks: a group's one long document walked slice by slice (forced
+# short slices here), the prep (forward) or the gradient kernels (backward)
+# of each slice running beside the next slice's walk.
+# ---------------------------------------------------------------------------
+@pytest.fixture
+def slices():
+    import gated_delta_rule_varlen_gb300 as gdr
+
+    def force(chunks):
+        gdr.gdr_set_slice_chunks(chunks)
+
+    yield force
+    gdr.gdr_set_slice_chunks(0)
+
+
+def test_kda_pipelined_walks_mild_gates_long_document(slices):
+    # 64 chunks in slices of 16 (also one of 10, which rounds to an even 10): the state and
+    # the adjoint cross every slice boundary through the carry buffers.
+    for sl in (16, 10):
+        slices(sl)
+        _check("kda", [4096], 2, 2, seed=31, glow=-0.05, h0=True, dht=True)
+
+
+def test_gdn_pipelined_walks_grouped_with_a_rest_group(slices):
+    # A pipelined 64-chunk document beside a group of short ones (walked whole).
+    slices(12)
+    _check("gdn", [4096, 700, 65], 1, 3, seed=32, glow=-0.05, h0=True, dht=True)
+
+
+def test_pipelined_walks_equal_whole_walks_bitwise(slices):
+    # Slicing only reorders launches: every output is bit for bit the whole walk's.
+    for variant, hqk, hv in (("kda", 2, 2), ("gdn", 1, 3)):
+        x, cu, h0, dht = _case(variant, [4096, 300], hqk, hv, seed=33, h0=True, dht=True)
+        slices(0)
+        a = run_gpu(variant, x, cu, h0=h0, dht=dht, want_dh0=True)
+        slices(8)
+        b = run_gpu(variant, x, cu, h0=h0, dht=dht, want_dh0=True)
+        for name in a:
+            if a[name] is not None:
+                assert torch.equal(a[name], b[name]), (variant, name)
+
+
+def test_pipelined_walks_ckpt_and_l2(slices):
+    # The checkpoint sequence and the in-kernel L2 norm with pipelined walks.
+    import gated_delta_rule_varlen_gb300 as gdr
+    slices(16)
+    x, cu, _, _ = _case("kda", [4096, 77], 2, 2, seed=34, glow=-0.05)
+    xd = {k: v.cuda() for k, v in x.items()}
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    a = run_gpu("kda", x, cu)
+    o1, _, _ = gdr.kda_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE, save_for_bwd=False)
+    o2, _, saved = gdr.kda_fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE)
+    gr = gdr.kda_bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["beta"], cu_d, cu, SCALE, xd["dout"], saved)
+    assert torch.equal(o1, a["out"]) and torch.equal(o2, a["out"])
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert torch.equal(gr[name], a[name]), name
+    _check_l2("kda", [4096, 77], 2, 2, seed=35)
