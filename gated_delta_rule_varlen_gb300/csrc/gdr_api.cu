@@ -194,14 +194,18 @@ std::vector<DocGroup> plan_groups(int32_t N, const int32_t* cu) {
 // (which the document groups run beside it): per chunk, the forward and
 // backward walk steps take about kWalkStepNs on the chain, and a chunk of one
 // head costs about kChunkHeadNs of SM time over the whole step (prep, walks,
-// gradients), both measured on GB300.  A split pack gets segments of
-// lseg = max(kMinSegChunks, chunks x heads / SMs), which about fill the SMs.
+// gradients), both measured on GB300.  A longest document that would walk
+// pipelined (a group of its own, longer than a slice) overlaps its walk with
+// its own prep and gradient work too, so that work counts on the other side.
+// A split pack gets segments of lseg = max(kMinSegChunks, chunks x heads /
+// SMs), which about fill the SMs.
 constexpr int kMinSegChunks = 64;
 constexpr int kNoSplit = 1 << 30;
-constexpr double kWalkStepNs = 8300.0, kChunkHeadNs = 50000.0;
+constexpr double kWalkStepNs = 7700.0, kChunkHeadNs = 50000.0;
 std::atomic<int> g_seg_chunks{0};  // gdr_set_segment_chunks: 0 = choose
 
 int sm_count();
+int slice_chunks();
 
 int segment_chunks(int32_t N, const int32_t* cu, int32_t HV) {
   const int forced = g_seg_chunks.load();
@@ -214,7 +218,8 @@ int segment_chunks(int32_t N, const int32_t* cu, int32_t HV) {
   }
   const int64_t sms = sm_count();
   const double chain_ns = (double)longest * kWalkStepNs;
-  const double others_ns = (double)(total - longest) * HV * kChunkHeadNs / (double)sms;
+  const bool own = longest >= kSoloChunks && longest > slice_chunks();
+  const double others_ns = (double)(own ? total : total - longest) * HV * kChunkHeadNs / (double)sms;
   if (chain_ns <= others_ns) return kNoSplit;
   const int64_t l = std::max<int64_t>(kMinSegChunks, (total * HV + sms - 1) / sms);
   return longest <= l ? kNoSplit : (int)l;
