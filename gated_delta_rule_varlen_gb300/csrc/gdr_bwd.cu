@@ -268,9 +268,12 @@ struct GradSmem {
   uint64_t bar_ld, bar_u;
 };
 
-// 16 warps: warp w owns rows 16 (w % 4) .. +15 and channels 32 (w / 4) .. +31
-// of every per-row result, held in registers in the m16n8 accumulator layout
-// (thread: rows i0 + g and i0 + g + 8, channel pairs c0 + 8 nt + 2 t).  The one
+// 16 warps: warp w owns channels 32 qc .. +31 (qc = w / 4) and rows 16 I ..
+// +15 (I = (w + qc) % 4) of every per-row result, held in registers in the
+// m16n8 accumulator layout (thread: rows i0 + g and i0 + g + 8, channel pairs
+// c0 + 8 nt + 2 t).  Warp w issues from the SM sub-partition w % 4, so each
+// sub-partition holds one warp of every row block and the triangular products
+// (whose work grows or shrinks with I) split evenly over the four.  The one
 // product that contracts over channels (dA) is summed over the four channel
 // quarters in four ordered passes.
 template <bool VEC, typename BetaT>
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int I = warp & 3, i0 = 16 * I, qc = warp >> 2, c0 = 8 * NT * qc;
+  const int qc = warp >> 2, I = (warp + qc) & 3, i0 = 16 * I, c0 = 8 * NT * qc;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
   const size_t fo = tf_off(chunk, h, a.HV), so = ts_off(chunk, h, a.HV);

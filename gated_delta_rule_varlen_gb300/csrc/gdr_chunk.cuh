@@ -132,7 +132,10 @@ __device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restric
 // Gated Gram matrices of one chunk,
 //   At[i][j]  = sum_c K_ic K_jc exp(gc_ic - gc_jc)   for j <  i (else 0)  -> s.At
 //   Aqk[i][j] = sum_c Q_ic K_jc exp(gc_ic - gc_jc)   for j <= i (else 0)  -> aqk (global, [64][64])
-// on 8 warps: warp w takes row block I = w % 4 and channels [64 (w / 4), +64).
+// on 8 warps: warp w takes channels [64 hk, +64) (hk = w / 4) and row block
+// I = w % 4 (hk = 0) or 3 - w % 4 (hk = 1).  Row block I has 2I + 2 n-tiles and
+// warp w issues from the SM sub-partition w % 4, so each sub-partition gets
+// 10 n-tiles.
 // Per-channel gates use the block factorization described in gdr_common.cuh.
 // The upper channel half leaves its partial sums in s.At and s.T (free until
 // the inverse); the lower half adds them in, masks, and writes the results.
@@ -142,7 +145,7 @@ __device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restric
 // rows: At[i][j] rk_i rk_j and Aqk[i][j] rq_i rk_j, in FP32.
 template <bool VEC, typename ET, int LG>
 __device__ void gram(ChunkSmemT<ET, LG>& s, __half* __restrict__ aqk, bool scaled = false) {
-  const int warp = threadIdx.x >> 5, I = warp & 3, hk = warp >> 2, i0 = 16 * I;
+  const int warp = threadIdx.x >> 5, hk = warp >> 2, I = hk ? 3 - (warp & 3) : (warp & 3), i0 = 16 * I;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const int ra = i0 + g, rb = i0 + g + 8;
   const float* G = s.G;
@@ -234,11 +237,14 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, __half* __restrict__ aqk, bool scale
 // s.T = (I + diag(beta) At)^-1, unit lower triangular, in FP32 on CUDA cores,
 // on 8 warps.  Diagonal 16x16 blocks by forward substitution (warp I < 4,
 // one column per lane of its first 16), then the blocks below them column
-// block by column block: warps J and J + 4 (J < 3) take columns
-// [16 J + 8 (w / 4), +8) of column block J and compute, for I = J+1 .. 3 in order,
+// block by column block: six warps (J, half), J < 3, take columns
+// [16 J + 8 half, +8) of column block J and compute, for I = J+1 .. 3 in order,
 //   T_IJ = -T_II * diag(beta_I) * sum_{K=J}^{I-1} At_IK T_KJ,
 // which needs only blocks of those columns that the same warp made before,
-// so the off-diagonal part synchronizes within the warp only.
+// so the off-diagonal part synchronizes within the warp only.  Column block J
+// makes 3 - J blocks, so the two J = 0 warps go to different SM
+// sub-partitions (warp w issues from w % 4): warps 0 and 3 take J = 0, warps 1
+// and 6 J = 1, warps 2 and 5 J = 2 (halves in that order); 4 and 7 wait.
 // At, T: [64][LDS] shared tiles; beta: [64]; tmp: 6 x 128 floats of scratch.
 __device__ __forceinline__ void invert_tiles(const float* __restrict__ At, float* __restrict__ T,
                                              const float* __restrict__ beta, float* __restrict__ tmp_all) {
@@ -263,15 +269,18 @@ __device__ __forceinline__ void invert_tiles(const float* __restrict__ At, float
     if ((j >> 4) > (i >> 4)) T[i * LDS + j] = 0.f;
   }
   __syncthreads();
-  if ((warp & 3) < 3) {
+  // (J, half) of warps 0..7 as J * 2 + half, -1 for the idle ones.
+  constexpr unsigned kJH = 0u | (2u << 4) | (4u << 8) | (1u << 12) | (15u << 16) | (5u << 20) | (3u << 24) | (15u << 28);
+  const int jh = (int)((kJH >> (4 * warp)) & 15u);
+  if (jh != 15) {
     // Warp (J, half): the 16 x 8 tile of columns n0 .. n0 + 7 of T_IJ, one
     // m16n8k8 accumulator, as split-TF32 tensor-core products (hi*hi + hi*lo
     // + lo*hi, about FP32 accuracy): C = At_I,[16J, 16I) T_[16J, 16I),J, then
     // X = diag(beta_I) C through shared memory into the B layout, then
     // T_IJ = -T_II X.
-    const int J = warp & 3, n0 = 16 * J + 8 * (warp >> 2);
+    const int J = jh >> 1, half = jh & 1, n0 = 16 * J + 8 * half;
     const int g = lane >> 2, t = lane & 3;
-    float* xs = tmp_all + ((warp >> 2) * 3 + J) * 128;  // X [16][8]
+    float* xs = tmp_all + (half * 3 + J) * 128;  // X [16][8]
     for (int I = J + 1; I < 4; ++I) {
       const int r0 = 16 * I;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
