@@ -335,6 +335,7 @@ __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict
     };
     zero_acc(acc0);
     zero_acc(acc1);
+#pragma unroll 2
     for (int kk = 0; kk < 2 * I + 2; ++kk) {  // j in [0, 16I + 16): reference gc at row 16I + 7
       const int j0 = kk * 8 + t, j1 = j0 + 4;
       uint32_t a0[4], a1[4];
@@ -360,6 +361,7 @@ __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict
       }
   } else {
     const int ra = i0 + g, rb = i0 + g + 8;
+#pragma unroll 2
     for (int kk = 0; kk < 2 * I + 2; ++kk) {
       const int j0 = kk * 8 + t, j1 = j0 + 4;
       auto dec = [&](int i, int j) { return j <= i ? ex2(s.gs[i] - s.gs[j]) : 0.f; };
@@ -391,6 +393,7 @@ __device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restric
     float acc[NT][4];
     zero_acc(acc);
     const int mref = j0b + 7;  // reference: gc at row 16J + 7, for block J and the later blocks alike
+#pragma unroll 2
     for (int kk = 2 * J; kk < 8; ++kk) {  // i in block J and after
       const int ia = kk * 8 + t, ib = ia + 4;
       uint32_t a0[4] = {tf32(M0[ia * LDS + j0b + g]), tf32(M0[ia * LDS + j0b + g + 8]),
@@ -412,6 +415,7 @@ __device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restric
       Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[mref * LG + c0 + col] - s.G[(j0b + r) * LG + c0 + col]);
     });
   } else {
+#pragma unroll 2
     for (int kk = 2 * J; kk < 8; ++kk) {
       const int ia = kk * 8 + t, ib = ia + 4;
       const int ja = j0b + g, jb = j0b + g + 8;
