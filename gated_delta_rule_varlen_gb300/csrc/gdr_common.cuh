@@ -74,11 +74,14 @@ struct SegDesc {
   int first;    // global index of the document's first segment
 };
 
-__device__ __forceinline__ uint32_t tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
+// An MMA operand at TF32 precision, rounded to nearest with ties away from
+// zero: half a unit in the last TF32 place is added to the magnitude bits (a
+// carry into the exponent is the correct rounding up).  The tensor cores read
+// a TF32 operand's 19 high bits (sign, exponent, 10 mantissa bits) and ignore
+// the 13 low bits left behind; tf32_value clears them, for code that uses the
+// rounded number itself.  One integer add per element.
+__device__ __forceinline__ uint32_t tf32(float x) { return __float_as_uint(x) + 0x1000u; }
+__device__ __forceinline__ uint32_t tf32_value(float x) { return (__float_as_uint(x) + 0x1000u) & 0xffffe000u; }
 
 // 2^x (the PTX approximate base-2 exponential).
 __device__ __forceinline__ float ex2(float x) {
@@ -102,12 +105,12 @@ __device__ __forceinline__ void mma8_split(float (&d)[4], const float (&a)[4], c
   uint32_t ah[4], al[4], bh[2], bl[2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    ah[i] = tf32(a[i]);
+    ah[i] = tf32_value(a[i]);
     al[i] = tf32(a[i] - __uint_as_float(ah[i]));
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    bh[i] = tf32(b[i]);
+    bh[i] = tf32_value(b[i]);
     bl[i] = tf32(b[i] - __uint_as_float(bh[i]));
   }
   mma8(d, al, bh);
