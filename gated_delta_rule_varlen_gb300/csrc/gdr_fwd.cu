@@ -42,73 +42,72 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
       *reinterpret_cast<float4*>(&a.tmat[qo + i * LDS + j4]) = *reinterpret_cast<const float4*>(&s.T[i * LDS + j4]);
     }
   }
-  // Kd, gamma, Qp (elementwise; factors exp(gc) and exp(gc_last - gc) are <= 1),
-  // only ever MMA operands: stored in FP16.  Kd transposed, [c][j] (the
-  // operand layout of the walk's state update): thread (channel d = e % 128,
-  // rows i0 .. i0 + 7) writes one 16-byte piece; gamma with each channel's first.
-  for (int e = tid; e < DK * CH / 8; e += blockDim.x) {
-    const int d = e & (DK - 1), i0 = 8 * (e >> 7);
-    const float glast = VEC ? s.G[(CH - 1) * LDT + d] : s.gs[CH - 1];
-    if (i0 == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d] = ex2(glast);
-    uint32_t p[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int i = i0 + 2 * q;
-      const float g0 = VEC ? s.G[i * LDT + d] : s.gs[i], g1 = VEC ? s.G[(i + 1) * LDT + d] : s.gs[i + 1];
-      const __half2 hv = __floats2half2_rn(s.k(i, d) * (scaled ? s.rk[i] : 1.f) * ex2(glast - g0),
-                                           s.k(i + 1, d) * (scaled ? s.rk[i + 1] : 1.f) * ex2(glast - g1));
-      p[q] = *reinterpret_cast<const uint32_t*>(&hv);
-    }
-    *reinterpret_cast<uint4*>(&a.kd[kd_off(chunk, h, a.HV) + d * CH + i0]) = make_uint4(p[0], p[1], p[2], p[3]);
-  }
-  __syncthreads();  // the reads of gc above are done: the pass below turns it into Gamma in place
-  // Qp = Q * Gamma; Gamma = exp(gc) kept in the G tile for the B operand of w.
-  for (int e = tid; e < CH * DK / 4; e += blockDim.x) {  // four channels per thread, one 8-byte store
-    const int i = e >> 5, d = (e & 31) * 4;
-    float r[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float gm = ex2(VEC ? s.G[i * LDT + d + q] : s.gs[i]);
-      if (VEC) s.G[i * LDT + d + q] = gm;
-      r[q] = s.q(i, d + q) * (scaled ? s.rq[i] : 1.f) * gm;
-    }
-    const __half2 p0 = __floats2half2_rn(r[0], r[1]), p1 = __floats2half2_rn(r[2], r[3]);
-    *reinterpret_cast<uint2*>(&a.qp[qp_off(chunk, h, a.HV) + i * DK + d]) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1));
-  }
-  __syncthreads();
-  // Q tile <- v rows (async), G tile <- beta * K * Gamma (B of w).
+  // Each thread keeps one channel, d = tid % 128, in the pass below; its
+  // gc_last is read before the pass overwrites the gate tile.
+  const int dch = tid & (DK - 1);
+  const float glast = VEC ? s.G[(CH - 1) * LDT + dch] : s.gs[CH - 1];
+  __syncthreads();  // At is stored (or unused) and every gc_last is read
+  // v rows (async) into the At tile, free from here on (BF16 rows at the q/k
+  // pitch take exactly its size).
+  uint16_t* const Vt = reinterpret_cast<uint16_t*>(s.At);
+  static_assert(sizeof(s.At) == CH * LDK * sizeof(uint16_t), "the v tile takes the At tile's place");
   for (int e = tid; e < CH * DK / 8; e += blockDim.x) {
     const int i = e >> 4, d8 = (e & 15) * 8;
     if (i < cd.len)
-      cp_async16(&s.Q[i * LDK + d8], a.v + ((size_t)(cd.tok0 + i) * a.HV + h) * DK + d8);
+      cp_async16(&Vt[i * LDK + d8], a.v + ((size_t)(cd.tok0 + i) * a.HV + h) * DK + d8);
     else
-      *reinterpret_cast<uint4*>(&s.Q[i * LDK + d8]) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(&Vt[i * LDK + d8]) = make_uint4(0u, 0u, 0u, 0u);
   }
   cp_async_commit();
-  for (int e = tid; e < CH * DK; e += blockDim.x) {
-    const int i = e >> 7, d = e & 127;
-    const float gm = VEC ? s.G[i * LDT + d] : ex2(s.gs[i]);  // Gamma
-    s.G[i * LDT + d] = s.beta[i] * (scaled ? s.rk[i] : 1.f) * s.k(i, d) * gm;
+  // One elementwise pass: thread (channel d, rows i0 .. i0 + 7) forms
+  //   Kd = K exp(gc_last - gc)  one 16-byte piece of Kd^T ([c][j], the operand
+  //                             layout of the walk's state update),
+  //   Qp = Q exp(gc)            one FP16 element per row,
+  //   beta K exp(gc)            the B operand of w, FP32, in place of gc,
+  // and gamma = exp(gc_last) with the channel's first piece.  Kd and Qp are
+  // only ever MMA operands and their factors are <= 1: stored in FP16.
+  for (int e = tid; e < DK * CH / 8; e += blockDim.x) {
+    const int d = e & (DK - 1), i0 = 8 * (e >> 7);
+    if (i0 == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d] = ex2(glast);
+    __half* const qo = a.qp + qp_off(chunk, h, a.HV) + d;
+    uint32_t p[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float kd[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = i0 + 2 * q + u;
+        const float gc = VEC ? s.G[i * LDT + d] : s.gs[i];
+        const float ki = s.k(i, d);
+        kd[u] = ki * (scaled ? s.rk[i] : 1.f) * ex2(glast - gc);
+        const float gm = ex2(gc);
+        qo[i * DK] = __float2half_rn(s.q(i, d) * (scaled ? s.rq[i] : 1.f) * gm);
+        s.G[i * LDT + d] = s.beta[i] * (scaled ? s.rk[i] : 1.f) * ki * gm;
+      }
+      const __half2 hv = __floats2half2_rn(kd[0], kd[1]);
+      p[q] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(&a.kd[kd_off(chunk, h, a.HV) + d * CH + i0]) = make_uint4(p[0], p[1], p[2], p[3]);
   }
   cp_async_wait<0>();
   __syncthreads();
   // w (warps 0-3) and u (warps 4-7) = T B over rows j <= i.  Warp q of a
   // product takes channel half q % 2 of row blocks {3, 0} (q < 2) or {2, 1},
   // so that the four warps do equal work.  B of u, beta_j V_jc, is formed from
-  // the BF16 v tile as it is read.
+  // the BF16 v tile (in the At tile) as it is read.
   {
     const int prod = warp >> 2, q = warp & 3, c0 = 64 * (q & 1);
     const int Ia = (q >> 1) ? 2 : 3, Ib = 3 - Ia;
     __half* uo = a.u + tf_off(chunk, h, a.HV);
     __half* wo = a.w + w_off(chunk, h, a.HV);
     auto bw = [&](int j, int c) { return s.G[j * LDT + c]; };
-    auto bu = [&](int j, int c) { return s.beta[j] * s.q(j, c); };
+    auto bu = [&](int j, int c) { return s.beta[j] * bfbits2f(Vt[j * LDK + c]); };
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
       const int I = pass ? Ib : Ia, i0 = 16 * I;
       float acc[8][4];
       zero_acc(acc);
+#pragma unroll 2
       for (int kk = 0; kk < 2 * I + 2; ++kk) {
         if (prod)
           mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
