@@ -335,8 +335,11 @@ __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict
     };
     zero_acc(acc0);
     zero_acc(acc1);
+    float mI[NT];  // reference gc at row 16I + 7 of this thread's B columns
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mI[nt] = s.G[(i0 + 7) * LG + c0 + nt * 8 + g];
 #pragma unroll 2
-    for (int kk = 0; kk < 2 * I + 2; ++kk) {  // j in [0, 16I + 16): reference gc at row 16I + 7
+    for (int kk = 0; kk < 2 * I + 2; ++kk) {  // j in [0, 16I + 16)
       const int j0 = kk * 8 + t, j1 = j0 + 4;
       uint32_t a0[4], a1[4];
       afrag(M0, j0, j1, a0);
@@ -344,8 +347,8 @@ __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
-        const float mI = s.G[(i0 + 7) * LG + c];
-        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI - s.G[j0 * LG + c])), tf32(fy(j1, c) * ex2(mI - s.G[j1 * LG + c]))};
+        uint32_t b[2] = {tf32(fy(j0, c) * ex2(mI[nt] - s.G[j0 * LG + c])),
+                         tf32(fy(j1, c) * ex2(mI[nt] - s.G[j1 * LG + c]))};
         mma8(acc0[nt], a0, b);
         mma8(acc1[nt], a1, b);
       }
@@ -393,6 +396,9 @@ __device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restric
     float acc[NT][4];
     zero_acc(acc);
     const int mref = j0b + 7;  // reference: gc at row 16J + 7, for block J and the later blocks alike
+    float mJ[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mJ[nt] = s.G[mref * LG + c0 + nt * 8 + g];
 #pragma unroll 2
     for (int kk = 2 * J; kk < 8; ++kk) {  // i in block J and after
       const int ia = kk * 8 + t, ib = ia + 4;
@@ -403,8 +409,7 @@ __device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restric
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
-        const float mJ = s.G[mref * LG + c];
-        const float ea = ex2(s.G[ia * LG + c] - mJ), eb = ex2(s.G[ib * LG + c] - mJ);
+        const float ea = ex2(s.G[ia * LG + c] - mJ[nt]), eb = ex2(s.G[ib * LG + c] - mJ[nt]);
         uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
         uint32_t b1[2] = {tf32(f1(ia, c) * ea), tf32(f1(ib, c) * eb)};
         mma8(acc[nt], a0, b0);
