@@ -415,7 +415,6 @@ struct WalkBvSmem {
   uint16_t SQ[CH * DK];      // Q Gamma [i][c]: 2 column blocks of 64 rows
   uint16_t SW[CH * DK];      // w [j][c]: 2 column blocks of 64 rows
   float gam[DK];             // gamma, with the Kd^T group
-  float gamc[DK];            // this chunk's gamma, copied before the Kd^T group is refilled
   uint64_t bar_k, bar_a, bar_w, bar_ab, bar_c;
   uint32_t tmem;
 };
@@ -614,10 +613,12 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       ok = tc::mbar_wait(&s.bar_k, st & 1) && ok;  // Kd^T and gamma of this chunk
       // Kd [j][c] from Kd^T [c][j]: 16 groups.
       for (int g = warp; g < 16; g += 8) transpose_group(SK, DK, 16 * (g >> 1), 32 * (g & 1), BK, CH, 0);
-      if (tid < DK) s.gamc[tid] = s.gam[tid];
       // Columns 64 hf .. 64 hf + 63 of the adjoint in two halves: the dS tape
-      // (chunk-major like the state tape) and dS' (TF32, the A operand).
+      // (chunk-major like the state tape), dS' (TF32, the A operand) and
+      // diag(gamma) dS in place (only the later products accumulate into dS;
+      // gamma is read from its landing buffer, refilled after the barrier).
       __nv_bfloat16* tp = outputs ? a.dstape + state_off(chunk, h, a.HV) : nullptr;
+      const float* gm = s.gam + 64 * hf;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int c0 = 64 * hf + 32 * half;
@@ -635,12 +636,15 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = tf32(__uint_as_float(ds[j]));
         tc::tmem_st32(tl + kBColSp + c0, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(ds[j]) * gm[32 * half + j]);
+        tc::tmem_st32(tl + kBColS + c0, r);
       }
       tc::fence_proxy_async();
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
-    if (!named_sync_and(1, WALKV_THREADS, ok)) break;  // Kd in place; dS' in TMEM
+    if (!named_sync_and(1, WALKV_THREADS, ok)) break;  // Kd in place; dS', diag(gamma) dS in TMEM
     tc::tc_fence_after();
     if (issuer) {
       ++k_got;
@@ -651,18 +655,6 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       if (st + 1 < cnt) issue_k(m - 1), ++k_iss;  // Kd^T and gamma were read before the barrier
     }
     if (data) {
-      {  // diag(gamma) dS into place (only the second product accumulates into dS)
-        const float* gm = s.gamc + 64 * hf;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tc::tmem_ld32(tl + kBColS + 64 * hf + 32 * half, r);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gm[32 * half + j]);
-          tc::tmem_st32(tl + kBColS + 64 * hf + 32 * half, r);
-        }
-      }
       ok = tc::mbar_wait(&s.bar_a, st & 1) && ok;  // Aqk, Q Gamma of this chunk
       // Aqk^T [j][i] (8 groups) and Qp^T [c][i] (16 groups) into [Aqk^T ; Qp^T].
       for (int g = warp; g < 24; g += 8) {
@@ -675,7 +667,7 @@ __global__ void __launch_bounds__(WALKV_THREADS, 1) k_walk_bwd_v(const __grid_co
       tc::tmem_wait_st();
     }
     tc::tc_fence_before();
-    if (!named_sync_and(3, WALKV_THREADS, ok)) break;  // [Aqk^T ; Qp^T] in place, diag(gamma) dS in TMEM
+    if (!named_sync_and(3, WALKV_THREADS, ok)) break;  // [Aqk^T ; Qp^T] in place
     tc::tc_fence_after();
     if (issuer) {
       ++a_got;
