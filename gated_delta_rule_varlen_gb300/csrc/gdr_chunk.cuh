@@ -243,8 +243,9 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, __half* __restrict__ aqk, bool scale
 // which needs only blocks of those columns that the same warp made before,
 // so the off-diagonal part synchronizes within the warp only.  Column block J
 // makes 3 - J blocks, so the two J = 0 warps go to different SM
-// sub-partitions (warp w issues from w % 4): warps 0 and 3 take J = 0, warps 1
-// and 6 J = 1, warps 2 and 5 J = 2 (halves in that order); 4 and 7 wait.
+// sub-partitions (warp w issues from w % 4): warp w of half w / 4 takes
+// J = w (first half) or J = 7 - w (second half) when that is below 3, so
+// warps 0 and 7 take J = 0, 1 and 6 J = 1, 2 and 5 J = 2; 3 and 4 wait.
 // At, T: [64][LDS] shared tiles; beta: [64]; tmp: 6 x 128 floats of scratch.
 __device__ __forceinline__ void invert_tiles(const float* __restrict__ At, float* __restrict__ T,
                                              const float* __restrict__ beta, float* __restrict__ tmp_all) {
@@ -269,16 +270,14 @@ __device__ __forceinline__ void invert_tiles(const float* __restrict__ At, float
     if ((j >> 4) > (i >> 4)) T[i * LDS + j] = 0.f;
   }
   __syncthreads();
-  // (J, half) of warps 0..7 as J * 2 + half, -1 for the idle ones.
-  constexpr unsigned kJH = 0u | (2u << 4) | (4u << 8) | (1u << 12) | (15u << 16) | (5u << 20) | (3u << 24) | (15u << 28);
-  const int jh = (int)((kJH >> (4 * warp)) & 15u);
-  if (jh != 15) {
+  const int half = warp >> 2, J = half ? 7 - warp : warp;
+  if (J < 3) {
     // Warp (J, half): the 16 x 8 tile of columns n0 .. n0 + 7 of T_IJ, one
     // m16n8k8 accumulator, as split-TF32 tensor-core products (hi*hi + hi*lo
     // + lo*hi, about FP32 accuracy): C = At_I,[16J, 16I) T_[16J, 16I),J, then
     // X = diag(beta_I) C through shared memory into the B layout, then
     // T_IJ = -T_II X.
-    const int J = jh >> 1, half = jh & 1, n0 = 16 * J + 8 * half;
+    const int n0 = 16 * J + 8 * half;
     const int g = lane >> 2, t = lane & 3;
     float* xs = tmp_all + (half * 3 + J) * 128;  // X [16][8]
     for (int I = J + 1; I < 4; ++I) {
