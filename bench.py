@@ -224,8 +224,8 @@ def run_reference(args):
     return 0
 
 
-# Minimal I/O of one call (SURVEY §8(d) "algorithmic bytes"): every input read
-# once and every output written once, per token (all heads).
+# Minimal I/O of one call (the algorithmic bytes of the binding roofline):
+# every input read once and every output written once, per token (all heads).
 def io_bytes(variant: str, Hqk: int, HV: int):
     qk = 2 * Hqk * D * 2
     vrow = HV * D * 2
@@ -236,8 +236,9 @@ def io_bytes(variant: str, Hqk: int, HV: int):
     return fwd, bwd
 
 
-# Chunked-algorithm flops per (token, value head): forward
-# 140.6 kflop, backward 282.6 kflop.  GDN shares its Gram products across the
+# Chunked-algorithm flops per (token, value head) (the chunk-64 products of
+# the forward and backward as counted in the design notes): forward 140.6
+# kflop, backward 282.6 kflop.  GDN shares its Gram products across the
 # value heads of a Q/K head; the KDA count is used for it too (an upper bound).
 FLOPS_FWD, FLOPS_BWD = 140.6e3, 282.6e3
 
@@ -428,7 +429,7 @@ def main():
                             bytes_model="the kernel's own inputs read once and outputs written once at their "
                                         "stored precision (bench.KERNEL_MODEL)")
 
-    # ---- the whole step against the binding roofline ---------
+    # ---- the whole step against the binding roofline: max(bytes / HBM, flops / BF16) ----
     rf = binding_roofline(wl.variant, T, Hqk, HV, ms_step, pk)
     traffic = None
     if all(kernels.get(nm, {}).get("ncu_bytes_per_token_head") is not None for nm in kernels if nm in KERNEL_MODEL):
