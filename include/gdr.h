@@ -61,12 +61,13 @@
  *     error has enqueued nothing (except GDR_CUDA_ERROR from a launch).
  *   - Calls on one stream are ordered; calls that share a workspace must not
  *     overlap on the GPU.  Inside a call, packs whose longest documents have
- *     at least 64 chunks run their document groups (see gdr_doc_groups) on up
- *     to four internal streams of the current device (created on first use,
- *     shared by all callers, highest priority first), forked from and joined
- *     back to the caller's stream with events; the call's work is still
- *     ordered after the stream's earlier work and before its later work,
- *     also under stream capture.
+ *     at least 64 chunks run their document groups (see gdr_doc_groups) on
+ *     internal streams of the current device: two per group (its walks; its
+ *     prep or gradient slices), at most eight, created on first use and
+ *     shared by all callers, the walks at the highest priorities.  They are
+ *     forked from and joined back to the caller's stream with events; the
+ *     call's work is still ordered after the stream's earlier work and before
+ *     its later work, also under stream capture.
  *   - Results are deterministic (no floating-point atomics).
  *   - Per-device state.  The library keeps, per device, its internal streams
  *     and events, an error word and (for kda_fwd_noalloc) the address of its
