@@ -652,6 +652,29 @@ int slice_chunks() {
 }
 bool pipelined(const DocGroup& G, int S) { return !G.split && G.r1 - G.r0 == 1 && G.c1 - G.c0 > S; }
 
+// Slice boundaries of a pipelined walk over nch > S chunks: a first and a last
+// slice of about a quarter of S (the forward walk starts after less prep, the
+// backward's gradient kernels after less walk, and the slice that runs alone
+// at the end of the forward is short), the chunks between them in equal
+// slices of about S; every slice starts at an even chunk.  A walk too short
+// for that is cut into slices of S.
+std::vector<int> slice_bounds(int nch, int S) {
+  const int e = std::max(2, (S / 4) & ~1);
+  std::vector<int> b{0};
+  if (nch < 2 * e + 2) {
+    for (int m = S; m < nch; m += S) b.push_back(m);
+    b.push_back(nch);
+    return b;
+  }
+  const int last = (nch - e) & ~1;
+  b.push_back(e);
+  const int L = last - e, k = (L + S - 1) / S;
+  for (int j = 1; j < k; ++j) b.push_back((e + (int)((int64_t)L * j / k)) & ~1);
+  if (last > b.back()) b.push_back(last);
+  b.push_back(nch);
+  return b;
+}
+
 template <typename T>
 T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
@@ -815,10 +838,10 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
       wa.seg_base = ma.seg_base = (int)G.s0;
       if (pipelined(G, S)) {
         const cudaStream_t lp = fork.lane2((int)i);
-        const int nch = (int)(G.c1 - G.c0);
+        const std::vector<int> sb = slice_bounds((int)(G.c1 - G.c0), S);
         wa.mode = 0;
-        for (int m0 = 0; m0 < nch && st == GDR_OK; m0 += S) {
-          const int nc = std::min(S, nch - m0);
+        for (size_t j = 0; j + 1 < sb.size() && st == GDR_OK; ++j) {
+          const int m0 = sb[j], nc = sb[j + 1] - sb[j];
           const double su = (double)std::min<int64_t>((int64_t)nc * CH, G.tokens - (int64_t)m0 * CH) * HV;
           st = prep(G.c0 + m0, nc, su, lp);
           if (st == GDR_OK && !Fork::link(lp, ls)) st = GDR_CUDA_ERROR;
@@ -1037,8 +1060,9 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
     if (pipelined(G, S)) {
       const cudaStream_t lg = fork.lane2((int)i);
       wb.mode = 0;
-      for (int m0 = ((nc - 1) / S) * S; m0 >= 0 && st == GDR_OK; m0 -= S) {
-        const int sn = std::min(S, nc - m0);
+      const std::vector<int> sb = slice_bounds(nc, S);
+      for (size_t j = sb.size() - 1; j > 0 && st == GDR_OK; --j) {
+        const int m0 = sb[j - 1], sn = sb[j] - sb[j - 1];
         const double su = (double)std::min<int64_t>((int64_t)sn * CH, G.tokens - (int64_t)m0 * CH) * HV;
         wb.m0 = m0;
         wb.m1 = m0 + sn;
