@@ -653,13 +653,14 @@ int slice_chunks() {
 bool pipelined(const DocGroup& G, int S) { return !G.split && G.r1 - G.r0 == 1 && G.c1 - G.c0 > S; }
 
 // Slice boundaries of a pipelined walk over nch > S chunks: a first and a last
-// slice of about a quarter of S (the forward walk starts after less prep, the
+// slice of S / div chunks (the forward walk starts after less prep, the
 // backward's gradient kernels after less walk, and the slice that runs alone
-// at the end of the forward is short), the chunks between them in equal
-// slices of about S; every slice starts at an even chunk.  A walk too short
-// for that is cut into slices of S.
-std::vector<int> slice_bounds(int nch, int S) {
-  const int e = std::max(2, (S / 4) & ~1);
+// at the end is short), the chunks between them in equal slices of about S;
+// every slice starts at an even chunk.  A walk too short for that is cut into
+// slices of S.  Measured on GB300: div = 2 for the forward, 4 for the
+// backward (div = 8 slower for both).
+std::vector<int> slice_bounds(int nch, int S, int div) {
+  const int e = std::max(2, (S / div) & ~1);
   std::vector<int> b{0};
   if (nch < 2 * e + 2) {
     for (int m = S; m < nch; m += S) b.push_back(m);
@@ -838,7 +839,7 @@ gdr_status fwd_impl(int variant, const void* q, const void* k, const void* v, co
       wa.seg_base = ma.seg_base = (int)G.s0;
       if (pipelined(G, S)) {
         const cudaStream_t lp = fork.lane2((int)i);
-        const std::vector<int> sb = slice_bounds((int)(G.c1 - G.c0), S);
+        const std::vector<int> sb = slice_bounds((int)(G.c1 - G.c0), S, 2);
         wa.mode = 0;
         for (size_t j = 0; j + 1 < sb.size() && st == GDR_OK; ++j) {
           const int m0 = sb[j], nc = sb[j + 1] - sb[j];
@@ -1060,7 +1061,7 @@ gdr_status bwd_impl(int variant, const void* q, const void* k, const void* v, co
     if (pipelined(G, S)) {
       const cudaStream_t lg = fork.lane2((int)i);
       wb.mode = 0;
-      const std::vector<int> sb = slice_bounds(nc, S);
+      const std::vector<int> sb = slice_bounds(nc, S, 4);
       for (size_t j = sb.size() - 1; j > 0 && st == GDR_OK; --j) {
         const int m0 = sb[j - 1], sn = sb[j] - sb[j - 1];
         const double su = (double)std::min<int64_t>((int64_t)sn * CH, G.tokens - (int64_t)m0 * CH) * HV;
