@@ -547,6 +547,22 @@ def test_pipelined_walks_equal_whole_walks_bitwise(slices):
                 assert torch.equal(a[name], b[name]), (variant, name)
 
 
+def test_pipelined_walks_uneven_slices_equal_whole_walks_bitwise(slices):
+    # Documents of 67 chunks (odd: the last slice takes the extra chunk) and 65 chunks (with
+    # slices of 64 the forward's end slices of 32 do not fit, and it is cut into slices of 64
+    # and 1), both ragged in their last chunk, against their whole walks.
+    for variant, hqk, hv in (("kda", 2, 2), ("gdn", 1, 3)):
+        x, cu, h0, dht = _case(variant, [4250, 4100], hqk, hv, seed=36, h0=True, dht=True)
+        slices(0)
+        a = run_gpu(variant, x, cu, h0=h0, dht=dht, want_dh0=True)
+        for sl in (8, 64):
+            slices(sl)
+            b = run_gpu(variant, x, cu, h0=h0, dht=dht, want_dh0=True)
+            for name in a:
+                if a[name] is not None:
+                    assert torch.equal(a[name], b[name]), (variant, sl, name)
+
+
 def test_pipelined_walks_ckpt_and_l2(slices):
     # The checkpoint sequence and the in-kernel L2 norm with pipelined walks.
     import gated_delta_rule_varlen_gb300 as gdr
