@@ -337,8 +337,9 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   {
     const float* dw = sg.dK;
     const float* dd = sg.dG;
-#pragma unroll 2
-    for (int kk = 2 * I; kk < 8; ++kk) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      if (kk < 2 * I) continue;
       const int ja = kk * 8 + t, jb = ja + 4;
       uint32_t av[4] = {tf32(s.T[ja * LDS + i0 + g]), tf32(s.T[ja * LDS + i0 + g + 8]),
                         tf32(s.T[jb * LDS + i0 + g]), tf32(s.T[jb * LDS + i0 + g + 8])};
