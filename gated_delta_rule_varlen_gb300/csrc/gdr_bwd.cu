@@ -535,6 +535,13 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
         dGr[nt][2 * hr + 1] -= kv.y * Z[nt][2 * hr + 1];
       }
   }
+  // gamma * dgamma of this thread's channel (the chunk-end term of dg), fetched
+  // here so that its latency hides behind the dKd terms.
+  float gdg = 0.f;
+  if (VEC || tid < DK) {
+    const int c = tid & (DK - 1);
+    gdg = __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + c]) * __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + c]);
+  }
   // dKd terms, dk, and the column sums of Kd*dKd over this warp's rows.
   {
 #pragma unroll
@@ -581,8 +588,6 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     // Reverse cumsum over rows: thread group r (128 threads, one channel each)
     // takes rows 16r .. 16r + 15, starting from the sums of the later groups.
     const int c = tid & (DK - 1), r = tid >> 7;
-    const float gdg = __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + c]) *
-                      __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + c]);
     float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 16; ++i) part[i & 3] += dG[(16 * r + i) * LDF + c];
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     }
     if (tid < DK) {
       const int c = tid;
-      float e = __ldg(&a.gam[((size_t)chunk * a.HV + h) * DK + c]) * __ldg(&a.dgam[((size_t)chunk * a.HV + h) * DK + c]) +
+      float e = gdg +
                 ((sg.col[c] + sg.col[DK + c]) + (sg.col[2 * DK + c] + sg.col[3 * DK + c]));
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) e += __shfl_xor_sync(0xffffffffu, e, m);
