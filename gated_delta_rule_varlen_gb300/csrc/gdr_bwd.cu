@@ -623,12 +623,22 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
       if (lane == 0) s.tmp[warp] = e;
     }
     __syncthreads();
-    if (tid == 0) {
-      float acc = (s.tmp[0] + s.tmp[1]) + (s.tmp[2] + s.tmp[3]);
-      for (int i = CH - 1; i >= 0; --i) {
-        acc += sg.rowsum[i];
-        if (i < cd.len) a.dg[(size_t)(cd.tok0 + i) * a.HV + h] = acc;
+    if (tid < 32) {
+      // dg_i = e + sum_{i' >= i} rowsum_i': lane l holds rows 2l and 2l + 1,
+      // the sums of the later lanes by a reverse shuffle scan (fixed order).
+      const float e = (s.tmp[0] + s.tmp[1]) + (s.tmp[2] + s.tmp[3]);
+      const float t1 = sg.rowsum[2 * tid + 1], t0 = sg.rowsum[2 * tid] + t1;
+      float x = t0;  // becomes the sum of lanes tid .. 31
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, x, d);
+        if (tid + d < 32) x += y;
       }
+      float later = __shfl_down_sync(0xffffffffu, x, 1);  // lanes tid + 1 .. 31
+      if (tid == 31) later = 0.f;
+      const float base = e + later;
+      if (2 * tid < cd.len) a.dg[(size_t)(cd.tok0 + 2 * tid) * a.HV + h] = base + t0;
+      if (2 * tid + 1 < cd.len) a.dg[(size_t)(cd.tok0 + 2 * tid + 1) * a.HV + h] = base + t1;
     }
   }
   if (tid < cd.len)
