@@ -471,6 +471,19 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     }
   }
   __syncthreads();  // dA complete
+  if (!VEC) {
+    // Scalar gate: both masked matrices are only read with the decay
+    // exp(gc_i - gc_j) from here on, so it is applied once, in place.
+    for (int e = tid; e < CH * CH; e += NTH) {
+      const int i = e >> 6, j = e & (CH - 1);
+      if (j <= i) {
+        const float d = ex2(s.gs[i] - s.gs[j]);
+        sDA[i * LDS + j] *= d;
+        sg.dAqk[i * LDS + j] *= d;
+      }
+    }
+    __syncthreads();
+  }
   auto kf = [&](int j, int c) { return s.k(j, c); };
   auto qf = [&](int j, int c) { return s.q(j, c); };
   // dqs at this thread's accumulator positions, fetched ahead of the apply.

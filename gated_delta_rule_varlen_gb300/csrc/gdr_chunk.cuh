@@ -319,6 +319,7 @@ __device__ void invert(ChunkSmemT<ET, LG>& s) {
 // Z1 likewise with M1, over the rows i of block I (16I .. 16I+15) and channels
 // c0 .. c0 + 8 NT - 1; M0, M1 are masked [64][64] shared tiles, fy(j, c)
 // returns Y_jc.  Each gated Y fragment is formed once and feeds both products.
+// With a scalar gate (VEC false) M0 and M1 already carry exp(gc_i - gc_j).
 template <bool VEC, int NT, typename ET, int LG, class FY>
 __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict__ M0, const float* __restrict__ M1, FY fy,
                             float (&Z0)[NT][4], float (&Z1)[NT][4], int I, int c0) {
@@ -362,16 +363,15 @@ __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict
         Z1[nt][r] += acc1[nt][r] * e;
       }
   } else {
+    // Scalar gate: M0 and M1 arrive with the decay exp(gc_i - gc_j) applied.
     const int ra = i0 + g, rb = i0 + g + 8;
 #pragma unroll 2
     for (int kk = 0; kk < 2 * I + 2; ++kk) {
       const int j0 = kk * 8 + t, j1 = j0 + 4;
-      auto dec = [&](int i, int j) { return j <= i ? ex2(s.gs[i] - s.gs[j]) : 0.f; };
-      const float d00 = dec(ra, j0), d10 = dec(rb, j0), d01 = dec(ra, j1), d11 = dec(rb, j1);
-      uint32_t a0[4] = {tf32(M0[ra * LDS + j0] * d00), tf32(M0[rb * LDS + j0] * d10), tf32(M0[ra * LDS + j1] * d01),
-                        tf32(M0[rb * LDS + j1] * d11)};
-      uint32_t a1[4] = {tf32(M1[ra * LDS + j0] * d00), tf32(M1[rb * LDS + j0] * d10), tf32(M1[ra * LDS + j1] * d01),
-                        tf32(M1[rb * LDS + j1] * d11)};
+      uint32_t a0[4] = {tf32(M0[ra * LDS + j0]), tf32(M0[rb * LDS + j0]), tf32(M0[ra * LDS + j1]),
+                        tf32(M0[rb * LDS + j1])};
+      uint32_t a1[4] = {tf32(M1[ra * LDS + j0]), tf32(M1[rb * LDS + j0]), tf32(M1[ra * LDS + j1]),
+                        tf32(M1[rb * LDS + j1])};
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
@@ -385,7 +385,8 @@ __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict
 
 // Z_j += sum_{i>=j} (M0_ij Y0_i + beta_i M1_ij Y1_i) * exp(gc_i - gc_j) for rows
 // j of block J and channels c0 .. c0 + 8 NT - 1.  M0, M1 masked [64][64]
-// shared tiles; f0(i, c), f1(i, c) return Y0_ic, Y1_ic.
+// shared tiles; f0(i, c), f1(i, c) return Y0_ic, Y1_ic.  With a scalar gate
+// (VEC false) M0 and M1 already carry exp(gc_i - gc_j).
 template <bool VEC, int NT, typename ET, int LG, class F0, class F1>
 __device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict__ M0, F0 f0, const float* __restrict__ M1,
                              F1 f1, float (&Z)[NT][4], int J, int c0) {
@@ -419,16 +420,15 @@ __device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restric
       Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[mref * LG + c0 + col] - s.G[(j0b + r) * LG + c0 + col]);
     });
   } else {
+    // Scalar gate: M0 and M1 arrive with the decay exp(gc_i - gc_j) applied.
 #pragma unroll 2
     for (int kk = 2 * J; kk < 8; ++kk) {
       const int ia = kk * 8 + t, ib = ia + 4;
       const int ja = j0b + g, jb = j0b + g + 8;
-      auto dec = [&](int i, int j) { return i >= j ? ex2(s.gs[i] - s.gs[j]) : 0.f; };
-      const float da0 = dec(ia, ja), da1 = dec(ia, jb), db0 = dec(ib, ja), db1 = dec(ib, jb);
-      uint32_t a0[4] = {tf32(M0[ia * LDS + ja] * da0), tf32(M0[ia * LDS + jb] * da1), tf32(M0[ib * LDS + ja] * db0),
-                        tf32(M0[ib * LDS + jb] * db1)};
-      uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + ja] * da0), tf32(s.beta[ia] * M1[ia * LDS + jb] * da1),
-                        tf32(s.beta[ib] * M1[ib * LDS + ja] * db0), tf32(s.beta[ib] * M1[ib * LDS + jb] * db1)};
+      uint32_t a0[4] = {tf32(M0[ia * LDS + ja]), tf32(M0[ia * LDS + jb]), tf32(M0[ib * LDS + ja]),
+                        tf32(M0[ib * LDS + jb])};
+      uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + ja]), tf32(s.beta[ia] * M1[ia * LDS + jb]),
+                        tf32(s.beta[ib] * M1[ib * LDS + ja]), tf32(s.beta[ib] * M1[ib * LDS + jb])};
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = c0 + nt * 8 + g;
