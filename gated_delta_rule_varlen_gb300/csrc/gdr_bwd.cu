@@ -258,10 +258,10 @@ constexpr int GRAD_WARPS = 16;   // 4 row blocks x 4 channel quarters
 constexpr int GRAD_NT = 4;       // 8-channel n-tiles per warp (32 channels)
 
 struct GradSmem {
-  ChunkSmemBB c;
-  float dAqk[CH * LDS];
-  float dK[CH * LDF];  // staging: dw, then w; finally unused
-  float dG[CH * LDF];  // staging: dDelta, then u; finally the gate adjoint dgc
+  ChunkSmemBB c;       // its At tile holds w (FP16 rows LDF elements apart) instead
+  float uh[CH * LDS];  // u: FP16 rows LDF elements apart (the same bytes)
+  float dK[CH * LDF];  // staging: dw, then the forward's At and dAqk
+  float dG[CH * LDF];  // staging: dDelta, then the gate adjoint dgc
   float dbeta[5][CH];  // per channel quarter (X.Kp + Y.V), and sum_j dA_ij At_ij
   float col[4 * DK];
   float rowsum[CH];
@@ -291,24 +291,35 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
   const size_t toff = tile_off(chunk, h, a.HV);
   const size_t fo = tf_off(chunk, h, a.HV), so = ts_off(chunk, h, a.HV);
-  // Whole tiles, stored with these shared pitches, by one bulk copy each: dw
-  // and dDelta (the B operands of X and Y) into the staging tiles, dAqk, and
-  // the forward's At and T of this chunk.
+  // Everything the first products read, issued at once.  Whole tiles, stored
+  // with these shared pitches, by one bulk copy each: dw and dDelta (the B
+  // operands of X and Y) into the staging tiles, the forward's T, and u (FP16,
+  // a B operand of dA).  w (dense FP16 rows) by cp.async into the At tile with
+  // u's pitch; the forward's At and dAqk follow once X and Y have freed the dw
+  // staging tile.
   if (tid == 0) {
     tc::mbar_init(&sg.bar_ld, 1);
     tc::mbar_init(&sg.bar_u, 1);
     tc::mbar_fence_init();
-    tc::mbar_arrive_expect_tx(&sg.bar_ld, (2 * CH * LDF + 3 * CH * LDS) * 4);
+    tc::mbar_arrive_expect_tx(&sg.bar_ld, (2 * CH * LDF + CH * LDS) * 4 + CH * LDF * 2);
     tc::bulk_load(sg.dK, &a.dw[fo], CH * LDF * 4, &sg.bar_ld);
     tc::bulk_load(sg.dG, &a.ddelta[fo], CH * LDF * 4, &sg.bar_ld);
-    tc::bulk_load(sg.dAqk, &a.daqk[so], CH * LDS * 4, &sg.bar_ld);
-    tc::bulk_load(s.At, &a.amat[so], CH * LDS * 4, &sg.bar_ld);
     tc::bulk_load(s.T, &a.tmat[so], CH * LDS * 4, &sg.bar_ld);
+    tc::bulk_load(sg.uh, &a.u[fo], CH * LDF * 2, &sg.bar_ld);
   }
-  load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
-                         a.HV);
-  // (load_chunk's barriers made the barrier set-up visible.)
+  __half* const wsh = reinterpret_cast<__half*>(s.At);
+  static_assert(sizeof(s.At) == CH * LDF * sizeof(__half), "w takes the At tile's place");
+  for (int e = tid; e < CH * DK / 8; e += NTH) {
+    const int i = e >> 4, c8 = (e & 15) * 8;
+    cp_async16(&wsh[i * LDF + c8], &a.w[w_off(chunk, h, a.HV) + i * DK + c8]);
+  }
+  // k, q, the gate and beta (one commit group with w), waited for after X and
+  // Y, which do not read them.
+  const RowScalars rows = load_chunk_issue<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta),
+                                                       cd.tok0, cd.len, hq, h, a.Hqk, a.HV);
+  __syncthreads();  // the barrier set-up is visible
   if (!__syncthreads_and(tc::mbar_wait(&sg.bar_ld, 0))) {
+    cp_async_wait<0>();
     if (tid == 0) {  // a wait ran out: record it and let the copies finish
       atomicExch(a.err, 7);
       tc::mbar_wait(&sg.bar_ld, 0);
@@ -354,33 +365,21 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     }
   }
   __syncthreads();
-  // w and u (FP16, B operands of dA) into the staging tiles as rows 136
-  // elements apart: u (stored with that pitch) by one bulk copy into the
-  // dDelta staging tile, w (dense rows) by cp.async into the dw staging tile
-  // (X and Y no longer read them).
+  // The forward's At and dAqk (masked [64][64] FP32 tiles) into the dw staging
+  // tile, which X and Y no longer read; they land during dA.
+  float* const At = sg.dK;
+  float* const dAqk = sg.dK + CH * LDS;
   if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&sg.bar_u, CH * LDF * 2);
-    tc::bulk_load(sg.dG, &a.u[fo], CH * LDF * 2, &sg.bar_u);
+    tc::mbar_arrive_expect_tx(&sg.bar_u, 2 * CH * LDS * 4);
+    tc::bulk_load(At, &a.amat[so], CH * LDS * 4, &sg.bar_u);
+    tc::bulk_load(dAqk, &a.daqk[so], CH * LDS * 4, &sg.bar_u);
   }
-  __half* const wsh = reinterpret_cast<__half*>(sg.dK);
-  for (int e = tid; e < CH * DK / 8; e += NTH) {
-    const int i = e >> 4, c8 = (e & 15) * 8;
-    cp_async16(&wsh[i * LDF + c8], &a.w[w_off(chunk, h, a.HV) + i * DK + c8]);
-  }
-  cp_async_commit();
+  load_chunk_finish<VEC, NTH>(s, rows);  // (also makes w visible)
   // Partial dA over this warp's channels: X w^T + Y u^T.
   float dAacc[8][4];
   zero_acc(dAacc);
-  cp_async_wait<0>();
-  if (!__syncthreads_and(tc::mbar_wait(&sg.bar_u, 0))) {
-    if (tid == 0) {
-      atomicExch(a.err, 7);
-      tc::mbar_wait(&sg.bar_u, 0);
-    }
-    return;
-  }
   {
-    const __half* u = reinterpret_cast<const __half*>(sg.dG);
+    const __half* u = reinterpret_cast<const __half*>(sg.uh);
 #pragma unroll
     for (int kk = 0; kk < NT; ++kk) {
       uint32_t ax[4] = {tf32(X[kk][0]), tf32(X[kk][2]), tf32(X[kk][1]), tf32(X[kk][3])};
@@ -406,7 +405,13 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   float* sDA = s.T;
   if (qc == 0)
     acc_foreach(dAacc, [&](int r, int col, float& x) { sDA[(i0 + r) * LDS + col] = col < i0 + r ? -x : 0.f; });
-  __syncthreads();
+  if (!__syncthreads_and(tc::mbar_wait(&sg.bar_u, 0))) {  // (At and dAqk have landed)
+    if (tid == 0) {
+      atomicExch(a.err, 7);
+      tc::mbar_wait(&sg.bar_u, 0);
+    }
+    return;
+  }
 #pragma unroll
   for (int pass = 1; pass < 3; ++pass) {
     if (qc == pass)
@@ -422,7 +427,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
       if (col < i) {
         const float d = sDA[i * LDS + col] - x;
         sDA[i * LDS + col] = d;
-        if (r < 8) p0 += d * s.At[i * LDS + col]; else p1 += d * s.At[i * LDS + col];
+        if (r < 8) p0 += d * At[i * LDS + col]; else p1 += d * At[i * LDS + col];
       }
     });
     p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
@@ -479,7 +484,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
       if (j <= i) {
         const float d = ex2(s.gs[i] - s.gs[j]);
         sDA[i * LDS + j] *= d;
-        sg.dAqk[i * LDS + j] *= d;
+        dAqk[i * LDS + j] *= d;
       }
     }
     __syncthreads();
@@ -498,7 +503,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     float Z0[NT][4], Z1[NT][4];
     zero_acc(Z0);
     zero_acc(Z1);
-    left_apply2<VEC, NT>(s, sDA, sg.dAqk, kf, Z0, Z1, I, c0);
+    left_apply2<VEC, NT>(s, sDA, dAqk, kf, Z0, Z1, I, c0);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -535,7 +540,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   {
     float Z[NT][4];
     zero_acc(Z);
-    right_apply2<VEC, NT>(s, sg.dAqk, qf, sDA, kf, Z, I, c0);
+    right_apply2<VEC, NT>(s, dAqk, qf, sDA, kf, Z, I, c0);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

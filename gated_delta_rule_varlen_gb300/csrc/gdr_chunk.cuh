@@ -9,7 +9,8 @@
 namespace gdr {
 
 // Shared-memory tiles of one chunk.  K and Q are kept either as FP32 (ET =
-// float) or as their exact BF16 input bits (ET = uint16_t, half the space).
+// float) or as their exact BF16 input bits (ET = uint16_t, half the space; the
+// chunk loads below fill this form).
 // LG_ is the row stride of the gate tile: 132 (= 4 mod 32) suits fragment
 // reads with the row on the group index (A operands of K K^T), 136 (= 8 mod 32)
 // fragment reads with the row on the thread-in-group index (B operands of the
@@ -45,76 +46,88 @@ using ChunkSmem = ChunkSmemT<float>;
 using ChunkSmemB = ChunkSmemT<uint16_t>;
 using ChunkSmemBB = ChunkSmemT<uint16_t, LDF>;
 
-// Loads k, q (of Q/K head hq), the gate (cumsum, base-2 scaled) and beta of
-// value head h for the chunk rows [tok0, tok0+len).  Rows >= len are zero
-// (zero gate rows keep the cumsum flat, so gc at row 63 equals gc at the
-// chunk's last token).
-template <bool VEC, typename BetaT, typename ET, int LG>
-__device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                           const float* __restrict__ g, const BetaT* __restrict__ beta, int tok0, int len, int hq,
-                           int h, int Hqk, int HV) {
-  constexpr int LD = ChunkSmemT<ET>::LD;
+// Row scalars of one chunk, read into registers by the first half of a chunk
+// load (threads tid < CH, row tid) and stored by the second.
+struct RowScalars {
+  float beta, g;
+};
+
+// First half of a chunk load of k, q (of Q/K head hq), the gate and beta of
+// value head h for the chunk rows [tok0, tok0+len): the raw BF16 k and q rows
+// (and the per-channel gate rows) by 16-byte async copies as one commit group
+// (rows >= len are zero-filled), and this thread's row of beta and of the
+// scalar gate into registers.  Nothing is waited for, so the caller may work
+// on other tiles while the copies land.
+template <bool VEC, typename BetaT, int LG>
+__device__ RowScalars load_chunk_issue(ChunkSmemT<uint16_t, LG>& s, const __nv_bfloat16* __restrict__ q,
+                                       const __nv_bfloat16* __restrict__ k, const float* __restrict__ g,
+                                       const BetaT* __restrict__ beta, int tok0, int len, int hq, int h, int Hqk,
+                                       int HV) {
+  constexpr int LD = ChunkSmemT<uint16_t, LG>::LD;
   const int tid = threadIdx.x;
-  if (sizeof(ET) == 2) {
-    // Raw BF16 rows straight into shared memory (16-byte async copies).
-    for (int e = tid; e < CH * DK / 8; e += blockDim.x) {
-      const int i = e >> 4, d8 = (e & 15) * 8;
-      if (i < len) {
-        const size_t off = ((size_t)(tok0 + i) * Hqk + hq) * DK + d8;
-        cp_async16(&s.K[i * LD + d8], k + off);
-        cp_async16(&s.Q[i * LD + d8], q + off);
-      } else {
-        *reinterpret_cast<uint4*>(&s.K[i * LD + d8]) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(&s.Q[i * LD + d8]) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    if (VEC) {
-      for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
-        const int i = e >> 5, d4 = (e & 31) * 4;
-        if (i < len)
-          cp_async16(&s.G[i * LG + d4], g + ((size_t)(tok0 + i) * HV + h) * DK + d4);
-        else
-          *reinterpret_cast<float4*>(&s.G[i * LG + d4]) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    cp_async_commit();
-  } else {
-    for (int e = tid; e < CH * DK / 2; e += blockDim.x) {
-      const int i = e / (DK / 2), d = (e % (DK / 2)) * 2;
-      float2 kv = make_float2(0.f, 0.f), qv = make_float2(0.f, 0.f);
-      if (i < len) {
-        const size_t off = ((size_t)(tok0 + i) * Hqk + hq) * DK + d;
-        kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(k + off));
-        qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q + off));
-      }
-      *reinterpret_cast<float2*>(reinterpret_cast<float*>(&s.K[0]) + i * LD + d) = kv;
-      *reinterpret_cast<float2*>(reinterpret_cast<float*>(&s.Q[0]) + i * LD + d) = qv;
-      if (VEC) {
-        float2 gv = make_float2(0.f, 0.f);
-        if (i < len) gv = *reinterpret_cast<const float2*>(g + ((size_t)(tok0 + i) * HV + h) * DK + d);
-        *reinterpret_cast<float2*>(&s.G[i * LG + d]) = gv;
-      }
+  for (int e = tid; e < CH * DK / 8; e += blockDim.x) {
+    const int i = e >> 4, d8 = (e & 15) * 8;
+    if (i < len) {
+      const size_t off = ((size_t)(tok0 + i) * Hqk + hq) * DK + d8;
+      cp_async16(&s.K[i * LD + d8], k + off);
+      cp_async16(&s.Q[i * LD + d8], q + off);
+    } else {
+      *reinterpret_cast<uint4*>(&s.K[i * LD + d8]) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(&s.Q[i * LD + d8]) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  if (VEC) {
+    for (int e = tid; e < CH * DK / 4; e += blockDim.x) {
+      const int i = e >> 5, d4 = (e & 31) * 4;
+      if (i < len)
+        cp_async16(&s.G[i * LG + d4], g + ((size_t)(tok0 + i) * HV + h) * DK + d4);
+      else
+        *reinterpret_cast<float4*>(&s.G[i * LG + d4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  cp_async_commit();
+  RowScalars r{0.f, 0.f};
+  if (tid < len && tid < CH) {
+    r.beta = to_f<BetaT>(beta[(size_t)(tok0 + tid) * HV + h]);
+    if (!VEC) r.g = g[(size_t)(tok0 + tid) * HV + h];
+  }
+  return r;
+}
+
+// Second half: waits for every async copy of this thread, stores the row
+// scalars, and forms the chunk-local gate cumsum (base-2 scaled).  Zero gate
+// rows past len keep the cumsum flat, so gc at row 63 equals gc at the chunk's
+// last token.  NTH = blockDim.x (256 or 512).  Per-channel gate: thread (c, r)
+// of the NTH / 128 row groups scans its CH * 128 / NTH rows of channel c in
+// registers, then adds the totals of the earlier groups in order.  Scalar
+// gate: one shuffle scan per warp over the 64 rows, then the first warp's
+// total added to the second warp's rows (the same order as the tensor-core
+// prep of the scalar gate).  Ends with a block barrier.
+template <bool VEC, int NTH, int LG>
+__device__ void load_chunk_finish(ChunkSmemT<uint16_t, LG>& s, RowScalars r) {
+  static_assert(NTH == 256 || NTH == 512, "row groups of the per-channel cumsum");
+  const int tid = threadIdx.x;
+  cp_async_wait<0>();
   if (tid < CH) {
-    const bool ok = tid < len;
-    s.beta[tid] = ok ? to_f<BetaT>(beta[(size_t)(tok0 + tid) * HV + h]) : 0.f;
-    if (!VEC) s.gs[tid] = ok ? g[(size_t)(tok0 + tid) * HV + h] * LOG2E : 0.f;
+    s.beta[tid] = r.beta;
+    if (!VEC) s.gs[tid] = r.g * LOG2E;
   }
-  if (sizeof(ET) == 2) cp_async_wait<0>();
   __syncthreads();
   if (VEC) {
-    if (tid < DK) {
-      float acc = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < CH; ++i) {
-        acc += s.G[i * LG + tid] * LOG2E;
-        s.G[i * LG + tid] = acc;
-      }
-    }
+    constexpr int RG = CH * DK / NTH;  // rows per group
+    const int c = tid & (DK - 1), grp = tid / DK;
+    float x[RG];
+#pragma unroll
+    for (int i = 0; i < RG; ++i) x[i] = s.G[(grp * RG + i) * LG + c] * LOG2E;
+#pragma unroll
+    for (int i = 1; i < RG; ++i) x[i] += x[i - 1];
+    s.tmp[grp * DK + c] = x[RG - 1];
+    __syncthreads();
+    float off = 0.f;
+    for (int r2 = 0; r2 < grp; ++r2) off += s.tmp[r2 * DK + c];
+#pragma unroll
+    for (int i = 0; i < RG; ++i) s.G[(grp * RG + i) * LG + c] = x[i] + off;
   } else if (tid < CH) {
-    // Inclusive scan over the 64 rows: per warp by shuffles, then the first
-    // warp's total added to the second warp's rows.
     float x = s.gs[tid];
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -127,6 +140,14 @@ __device__ void load_chunk(ChunkSmemT<ET, LG>& s, const __nv_bfloat16* __restric
     s.gs[tid] = x;
   }
   __syncthreads();
+}
+
+// Both halves of a chunk load back to back.
+template <bool VEC, typename BetaT, int NTH, int LG>
+__device__ void load_chunk(ChunkSmemT<uint16_t, LG>& s, const __nv_bfloat16* __restrict__ q,
+                           const __nv_bfloat16* __restrict__ k, const float* __restrict__ g,
+                           const BetaT* __restrict__ beta, int tok0, int len, int hq, int h, int Hqk, int HV) {
+  load_chunk_finish<VEC, NTH>(s, load_chunk_issue<VEC, BetaT>(s, q, k, g, beta, tok0, len, hq, h, Hqk, HV));
 }
 
 // Gated Gram matrices of one chunk,
