@@ -265,7 +265,7 @@ struct GradSmem {
   float dbeta[5][CH];  // per channel quarter (X.Kp + Y.V), and sum_j dA_ij At_ij
   float col[4 * DK];
   float rowsum[CH];
-  uint64_t bar_ld, bar_u;
+  uint64_t bar_ld, bar_w, bar_u;
 };
 
 // 16 warps: warp w owns channels 32 qc .. +31 (qc = w / 4) and rows 16 I ..
@@ -292,20 +292,22 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   const size_t toff = tile_off(chunk, h, a.HV);
   const size_t fo = tf_off(chunk, h, a.HV), so = ts_off(chunk, h, a.HV);
   // Everything the first products read, issued at once.  Whole tiles, stored
-  // with these shared pitches, by one bulk copy each: dw and dDelta (the B
-  // operands of X and Y) into the staging tiles, the forward's T, and u (FP16,
-  // a B operand of dA).  w (dense FP16 rows) by cp.async into the At tile with
-  // u's pitch; the forward's At and dAqk follow once X and Y have freed the dw
-  // staging tile.
+  // with these shared pitches, by one bulk copy each: the forward's T, dw and
+  // dDelta (the operands of X and Y, waited for first), then u (FP16, a B
+  // operand of dA, on a barrier of its own).  w (dense FP16 rows) by cp.async
+  // into the At tile with u's pitch; the forward's At and dAqk follow once X
+  // and Y have freed the dw staging tile.
   if (tid == 0) {
     tc::mbar_init(&sg.bar_ld, 1);
+    tc::mbar_init(&sg.bar_w, 1);
     tc::mbar_init(&sg.bar_u, 1);
     tc::mbar_fence_init();
-    tc::mbar_arrive_expect_tx(&sg.bar_ld, (2 * CH * LDF + CH * LDS) * 4 + CH * LDF * 2);
+    tc::mbar_arrive_expect_tx(&sg.bar_ld, (2 * CH * LDF + CH * LDS) * 4);
+    tc::bulk_load(s.T, &a.tmat[so], CH * LDS * 4, &sg.bar_ld);
     tc::bulk_load(sg.dK, &a.dw[fo], CH * LDF * 4, &sg.bar_ld);
     tc::bulk_load(sg.dG, &a.ddelta[fo], CH * LDF * 4, &sg.bar_ld);
-    tc::bulk_load(s.T, &a.tmat[so], CH * LDS * 4, &sg.bar_ld);
-    tc::bulk_load(sg.uh, &a.u[fo], CH * LDF * 2, &sg.bar_ld);
+    tc::mbar_arrive_expect_tx(&sg.bar_w, CH * LDF * 2);
+    tc::bulk_load(sg.uh, &a.u[fo], CH * LDF * 2, &sg.bar_w);
   }
   __half* const wsh = reinterpret_cast<__half*>(s.At);
   static_assert(sizeof(s.At) == CH * LDF * sizeof(__half), "w takes the At tile's place");
@@ -323,6 +325,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     if (tid == 0) {  // a wait ran out: record it and let the copies finish
       atomicExch(a.err, 7);
       tc::mbar_wait(&sg.bar_ld, 0);
+      tc::mbar_wait(&sg.bar_w, 0);
     }
     return;
   }
@@ -375,7 +378,10 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     tc::bulk_load(dAqk, &a.daqk[so], CH * LDS * 4, &sg.bar_u);
   }
   load_chunk_finish<VEC, NTH>(s, rows);  // (also makes w visible)
-  // Partial dA over this warp's channels: X w^T + Y u^T.
+  // Partial dA over this warp's channels: X w^T + Y u^T.  (A thread whose
+  // wait for u runs out computes on whatever the tile holds; the barrier
+  // after dA turns that into an error return.)
+  const bool u_ok = tc::mbar_wait(&sg.bar_w, 0);
   float dAacc[8][4];
   zero_acc(dAacc);
   {
@@ -405,9 +411,10 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   float* sDA = s.T;
   if (qc == 0)
     acc_foreach(dAacc, [&](int r, int col, float& x) { sDA[(i0 + r) * LDS + col] = col < i0 + r ? -x : 0.f; });
-  if (!__syncthreads_and(tc::mbar_wait(&sg.bar_u, 0))) {  // (At and dAqk have landed)
+  if (!__syncthreads_and(tc::mbar_wait(&sg.bar_u, 0) && u_ok)) {  // (At and dAqk have landed)
     if (tid == 0) {
       atomicExch(a.err, 7);
+      tc::mbar_wait(&sg.bar_w, 0);
       tc::mbar_wait(&sg.bar_u, 0);
     }
     return;
@@ -490,7 +497,6 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     __syncthreads();
   }
   auto kf = [&](int j, int c) { return s.k(j, c); };
-  auto qf = [&](int j, int c) { return s.q(j, c); };
   // dqs at this thread's accumulator positions, fetched ahead of the apply.
   float2 dqspre[NT][2];
 #pragma unroll
@@ -540,7 +546,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   {
     float Z[NT][4];
     zero_acc(Z);
-    right_apply2<VEC, NT>(s, dAqk, qf, sDA, kf, Z, I, c0);
+    right_apply2<VEC, NT>(s, dAqk, sDA, Z, I, c0);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

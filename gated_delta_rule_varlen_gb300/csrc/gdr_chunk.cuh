@@ -404,62 +404,69 @@ __device__ void left_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict
   }
 }
 
-// Z_j += sum_{i>=j} (M0_ij Y0_i + beta_i M1_ij Y1_i) * exp(gc_i - gc_j) for rows
-// j of block J and channels c0 .. c0 + 8 NT - 1.  M0, M1 masked [64][64]
-// shared tiles; f0(i, c), f1(i, c) return Y0_ic, Y1_ic.  With a scalar gate
-// (VEC false) M0 and M1 already carry exp(gc_i - gc_j).
-template <bool VEC, int NT, typename ET, int LG, class F0, class F1>
-__device__ void right_apply2(const ChunkSmemT<ET, LG>& s, const float* __restrict__ M0, F0 f0, const float* __restrict__ M1,
-                             F1 f1, float (&Z)[NT][4], int J, int c0) {
+// Z_j += sum_{i>=j} (M0_ij Q_i + beta_i M1_ij K_i) * exp(gc_i - gc_j) for rows
+// j of block J and channels c0 .. c0 + 31 (four n-tiles).  M0, M1 masked
+// [64][64] shared tiles; Q, K the chunk's BF16 tiles.  With a scalar gate (VEC
+// false) M0 and M1 already carry exp(gc_i - gc_j).
+// Each k-step (rows i = 8 kk .. 8 kk + 7) takes the B fragments of all four
+// n-tiles of Q, and of K, from one transposing matrix load each, which hands
+// thread (g, t) rows 8 kk + 2t and 8 kk + 2t + 1 of channel c0 + 8 nt + g.  So
+// the step's k slots t and t + 4 stand for those two rows (the order of the
+// terms within a step is free), and the A fragments (M0, M1 read down a column)
+// follow the same assignment; with the [64][68] tiles those reads are free of
+// bank conflicts.
+template <bool VEC, int NT, int LG>
+__device__ void right_apply2(const ChunkSmemT<uint16_t, LG>& s, const float* __restrict__ M0,
+                             const float* __restrict__ M1, float (&Z)[NT][4], int J, int c0) {
+  static_assert(NT == 4, "one x4 matrix load covers four n-tiles");
+  constexpr int LD = ChunkSmemT<uint16_t, LG>::LD;
   const int j0b = 16 * J;
   const int lane = lane_id(), g = lane >> 2, t = lane & 3;
+  const int ja = j0b + g, jb = ja + 8;
+  // This lane's row of the four 8 x 8 matrices (n-tile lane / 8, row lane % 8).
+  const uint16_t* const qrow = s.Q + (lane & 7) * LD + c0 + 8 * (lane >> 3);
+  const uint16_t* const krow = s.K + (lane & 7) * LD + c0 + 8 * (lane >> 3);
+  float acc[NT][4];  // VEC only: the sums before the row factors
+  if (VEC) zero_acc(acc);
+  auto& dst = VEC ? acc : Z;
+  float mJ[NT];  // VEC: reference gc at row 16J + 7, for block J and the later blocks alike
+  const int mref = j0b + 7;
   if (VEC) {
-    float acc[NT][4];
-    zero_acc(acc);
-    const int mref = j0b + 7;  // reference: gc at row 16J + 7, for block J and the later blocks alike
-    float mJ[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) mJ[nt] = s.G[mref * LG + c0 + nt * 8 + g];
+  }
 #pragma unroll 2
-    for (int kk = 2 * J; kk < 8; ++kk) {  // i in block J and after
-      const int ia = kk * 8 + t, ib = ia + 4;
-      uint32_t a0[4] = {tf32(M0[ia * LDS + j0b + g]), tf32(M0[ia * LDS + j0b + g + 8]),
-                        tf32(M0[ib * LDS + j0b + g]), tf32(M0[ib * LDS + j0b + g + 8])};
-      uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + j0b + g]), tf32(s.beta[ia] * M1[ia * LDS + j0b + g + 8]),
-                        tf32(s.beta[ib] * M1[ib * LDS + j0b + g]), tf32(s.beta[ib] * M1[ib * LDS + j0b + g + 8])};
+  for (int kk = 2 * J; kk < 8; ++kk) {  // i in block J and after
+    const int ia = kk * 8 + 2 * t, ib = ia + 1;
+    uint32_t yq[4], yk[4];
+    ldsm_x4_trans(yq, qrow + kk * 8 * LD);
+    ldsm_x4_trans(yk, krow + kk * 8 * LD);
+    const float2 bb = *reinterpret_cast<const float2*>(&s.beta[ia]);
+    uint32_t a0[4] = {tf32(M0[ia * LDS + ja]), tf32(M0[ia * LDS + jb]), tf32(M0[ib * LDS + ja]),
+                      tf32(M0[ib * LDS + jb])};
+    uint32_t a1[4] = {tf32(bb.x * M1[ia * LDS + ja]), tf32(bb.x * M1[ia * LDS + jb]), tf32(bb.y * M1[ib * LDS + ja]),
+                      tf32(bb.y * M1[ib * LDS + jb])};
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
+      float qa = bf_lo(yq[nt]), qb = bf_hi(yq[nt]), ka = bf_lo(yk[nt]), kb = bf_hi(yk[nt]);
+      if (VEC) {
         const int c = c0 + nt * 8 + g;
         const float ea = ex2(s.G[ia * LG + c] - mJ[nt]), eb = ex2(s.G[ib * LG + c] - mJ[nt]);
-        uint32_t b0[2] = {tf32(f0(ia, c) * ea), tf32(f0(ib, c) * eb)};
-        uint32_t b1[2] = {tf32(f1(ia, c) * ea), tf32(f1(ib, c) * eb)};
-        mma8(acc[nt], a0, b0);
-        mma8(acc[nt], a1, b1);
+        qa *= ea;
+        ka *= ea;
+        qb *= eb;
+        kb *= eb;
       }
+      uint32_t b0[2] = {tf32(qa), tf32(qb)};
+      uint32_t b1[2] = {tf32(ka), tf32(kb)};
+      mma8(dst[nt], a0, b0);
+      mma8(dst[nt], a1, b1);
     }
+  }
+  if (VEC)
     acc_foreach(acc, [&](int r, int col, float& x) {
       Z[col >> 3][(r >> 3) * 2 + (col & 1)] += x * ex2(s.G[mref * LG + c0 + col] - s.G[(j0b + r) * LG + c0 + col]);
     });
-  } else {
-    // Scalar gate: M0 and M1 arrive with the decay exp(gc_i - gc_j) applied.
-#pragma unroll 2
-    for (int kk = 2 * J; kk < 8; ++kk) {
-      const int ia = kk * 8 + t, ib = ia + 4;
-      const int ja = j0b + g, jb = j0b + g + 8;
-      uint32_t a0[4] = {tf32(M0[ia * LDS + ja]), tf32(M0[ia * LDS + jb]), tf32(M0[ib * LDS + ja]),
-                        tf32(M0[ib * LDS + jb])};
-      uint32_t a1[4] = {tf32(s.beta[ia] * M1[ia * LDS + ja]), tf32(s.beta[ia] * M1[ia * LDS + jb]),
-                        tf32(s.beta[ib] * M1[ib * LDS + ja]), tf32(s.beta[ib] * M1[ib * LDS + jb])};
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int c = c0 + nt * 8 + g;
-        uint32_t b0[2] = {tf32(f0(ia, c)), tf32(f0(ib, c))};
-        uint32_t b1[2] = {tf32(f1(ia, c)), tf32(f1(ib, c))};
-        mma8(Z[nt], a0, b0);
-        mma8(Z[nt], a1, b1);
-      }
-    }
-  }
 }
 
 }  // namespace gdr
