@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
     tc::bulk_load(At, &a.amat[so], CH * LDS * 4, &sg.bar_u);
     tc::bulk_load(dAqk, &a.daqk[so], CH * LDS * 4, &sg.bar_u);
   }
-  load_chunk_finish<VEC, NTH>(s, rows);  // (also makes w visible)
+  load_chunk_finish<VEC>(s, rows);  // (also makes w visible)
   // Partial dA over this warp's channels: X w^T + Y u^T.  (A thread whose
   // wait for u runs out computes on whatever the tile holds; the barrier
   // after dA turns that into an error return.)

@@ -97,15 +97,14 @@ __device__ RowScalars load_chunk_issue(ChunkSmemT<uint16_t, LG>& s, const __nv_b
 // Second half: waits for every async copy of this thread, stores the row
 // scalars, and forms the chunk-local gate cumsum (base-2 scaled).  Zero gate
 // rows past len keep the cumsum flat, so gc at row 63 equals gc at the chunk's
-// last token.  NTH = blockDim.x (256 or 512).  Per-channel gate: thread (c, r)
-// of the NTH / 128 row groups scans its CH * 128 / NTH rows of channel c in
-// registers, then adds the totals of the earlier groups in order.  Scalar
+// last token.  Per-channel gate: one thread per channel walks the 64 rows in
+// order (measured faster than splitting the rows over more threads, whose
+// extra barrier and pass cost more than the shorter chain saves).  Scalar
 // gate: one shuffle scan per warp over the 64 rows, then the first warp's
 // total added to the second warp's rows (the same order as the tensor-core
 // prep of the scalar gate).  Ends with a block barrier.
-template <bool VEC, int NTH, int LG>
+template <bool VEC, int LG>
 __device__ void load_chunk_finish(ChunkSmemT<uint16_t, LG>& s, RowScalars r) {
-  static_assert(NTH == 256 || NTH == 512, "row groups of the per-channel cumsum");
   const int tid = threadIdx.x;
   cp_async_wait<0>();
   if (tid < CH) {
@@ -114,19 +113,14 @@ __device__ void load_chunk_finish(ChunkSmemT<uint16_t, LG>& s, RowScalars r) {
   }
   __syncthreads();
   if (VEC) {
-    constexpr int RG = CH * DK / NTH;  // rows per group
-    const int c = tid & (DK - 1), grp = tid / DK;
-    float x[RG];
-#pragma unroll
-    for (int i = 0; i < RG; ++i) x[i] = s.G[(grp * RG + i) * LG + c] * LOG2E;
-#pragma unroll
-    for (int i = 1; i < RG; ++i) x[i] += x[i - 1];
-    s.tmp[grp * DK + c] = x[RG - 1];
-    __syncthreads();
-    float off = 0.f;
-    for (int r2 = 0; r2 < grp; ++r2) off += s.tmp[r2 * DK + c];
-#pragma unroll
-    for (int i = 0; i < RG; ++i) s.G[(grp * RG + i) * LG + c] = x[i] + off;
+    if (tid < DK) {
+      float acc = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < CH; ++i) {
+        acc += s.G[i * LG + tid] * LOG2E;
+        s.G[i * LG + tid] = acc;
+      }
+    }
   } else if (tid < CH) {
     float x = s.gs[tid];
 #pragma unroll
@@ -143,11 +137,11 @@ __device__ void load_chunk_finish(ChunkSmemT<uint16_t, LG>& s, RowScalars r) {
 }
 
 // Both halves of a chunk load back to back.
-template <bool VEC, typename BetaT, int NTH, int LG>
+template <bool VEC, typename BetaT, int LG>
 __device__ void load_chunk(ChunkSmemT<uint16_t, LG>& s, const __nv_bfloat16* __restrict__ q,
                            const __nv_bfloat16* __restrict__ k, const float* __restrict__ g,
                            const BetaT* __restrict__ beta, int tok0, int len, int hq, int h, int Hqk, int HV) {
-  load_chunk_finish<VEC, NTH>(s, load_chunk_issue<VEC, BetaT>(s, q, k, g, beta, tok0, len, hq, h, Hqk, HV));
+  load_chunk_finish<VEC>(s, load_chunk_issue<VEC, BetaT>(s, q, k, g, beta, tok0, len, hq, h, Hqk, HV));
 }
 
 // Gated Gram matrices of one chunk,

@@ -29,8 +29,8 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
     s.rq[tid] = a.rq[row];
     s.rk[tid] = a.rk[row];
   }
-  load_chunk<VEC, BetaT, 256>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h,
-                              a.Hqk, a.HV);
+  load_chunk<VEC, BetaT>(s, a.q, a.k, a.g, reinterpret_cast<const BetaT*>(a.beta), cd.tok0, cd.len, hq, h, a.Hqk,
+                         a.HV);
   gram<VEC>(s, a.aqk + aqk_off(chunk, h, a.HV), scaled);
   invert(s);
   // At and T for the backward: the values its gradient kernel needs, bit for bit.
