@@ -94,14 +94,20 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   // w (warps 0-3) and u (warps 4-7) = T B over rows j <= i.  Warp q of a
   // product takes channel half q % 2 of row blocks {3, 0} (q < 2) or {2, 1},
   // so that the four warps do equal work.  B of u, beta_j V_jc, is formed from
-  // the BF16 v tile (in the At tile) as it is read.
+  // the BF16 v tile (in the At tile) as it is read.  Each k-step (rows j = 8 kk
+  // .. 8 kk + 7) puts rows 8 kk + 2t and 8 kk + 2t + 1 in the k slots t and
+  // t + 4 (the order within a step is free): the B reads of w's FP32 tile
+  // (row pitch 132) are then free of bank conflicts, u's B fragments of four
+  // n-tiles come from one transposing 8 x 8 matrix load of v, and each A
+  // fragment row of T is one float2.
   {
     const int prod = warp >> 2, q = warp & 3, c0 = 64 * (q & 1);
     const int Ia = (q >> 1) ? 2 : 3, Ib = 3 - Ia;
+    const int lane = lane_id(), g = lane >> 2, t = lane & 3;
     __half* uo = a.u + tf_off(chunk, h, a.HV);
     __half* wo = a.w + w_off(chunk, h, a.HV);
-    auto bw = [&](int j, int c) { return s.G[j * LDT + c]; };
-    auto bu = [&](int j, int c) { return s.beta[j] * bfbits2f(Vt[j * LDK + c]); };
+    // This lane's row of the 8 x 8 matrices of v (n-tile lane / 8 of each group of four, row lane % 8).
+    const uint16_t* const vrow = Vt + (lane & 7) * LDK + c0 + 8 * (lane >> 3);
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
       const int I = pass ? Ib : Ia, i0 = 16 * I;
@@ -109,15 +115,31 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
       zero_acc(acc);
 #pragma unroll 2
       for (int kk = 0; kk < 2 * I + 2; ++kk) {
-        if (prod)
-          mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
-                       [&](int j, int c) { return bu(j, c0 + c); });
-        else
-          mma_kstep<8>(acc, kk * 8, 0, 8, [&](int i, int j) { return s.T[(i0 + i) * LDS + j]; },
-                       [&](int j, int c) { return bw(j, c0 + c); });
+        const int j0 = kk * 8 + 2 * t;
+        const float2 ta = *reinterpret_cast<const float2*>(&s.T[(i0 + g) * LDS + j0]);
+        const float2 tb = *reinterpret_cast<const float2*>(&s.T[(i0 + g + 8) * LDS + j0]);
+        const uint32_t af[4] = {tf32(ta.x), tf32(tb.x), tf32(ta.y), tf32(tb.y)};
+        if (prod) {
+          uint32_t y[2][4];
+          ldsm_x4_trans(y[0], vrow + kk * 8 * LDK);
+          ldsm_x4_trans(y[1], vrow + kk * 8 * LDK + 32);
+          const float2 bb = *reinterpret_cast<const float2*>(&s.beta[j0]);
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt) {
+            const uint32_t yv = y[nt >> 2][nt & 3];
+            uint32_t b[2] = {tf32(bb.x * bf_lo(yv)), tf32(bb.y * bf_hi(yv))};
+            mma8(acc[nt], af, b);
+          }
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt) {
+            const int c = c0 + nt * 8 + g;
+            uint32_t b[2] = {tf32(s.G[j0 * LDT + c]), tf32(s.G[(j0 + 1) * LDT + c])};
+            mma8(acc[nt], af, b);
+          }
+        }
       }
       {  // rows i0 + g (+8), channel pairs c0 + 8 nt + 2 t: FP16 pairs
-        const int lane = lane_id(), g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
