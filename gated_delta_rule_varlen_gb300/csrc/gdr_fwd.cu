@@ -42,10 +42,11 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
       *reinterpret_cast<float4*>(&a.tmat[qo + i * LDS + j4]) = *reinterpret_cast<const float4*>(&s.T[i * LDS + j4]);
     }
   }
-  // Each thread keeps one channel, d = tid % 128, in the pass below; its
-  // gc_last is read before the pass overwrites the gate tile.
-  const int dch = tid & (DK - 1);
-  const float glast = VEC ? s.G[(CH - 1) * LDT + dch] : s.gs[CH - 1];
+  // Each thread keeps two channels, d = 2 (tid % 64) and d + 1, in the pass
+  // below; their gc_last is read before the pass overwrites the gate tile.
+  const int dch = 2 * (tid & (DK / 2 - 1));
+  const float2 glast = VEC ? *reinterpret_cast<const float2*>(&s.G[(CH - 1) * LDT + dch])
+                           : make_float2(s.gs[CH - 1], s.gs[CH - 1]);
   __syncthreads();  // At is stored (or unused) and every gc_last is read
   // v rows (async) into the At tile, free from here on (BF16 rows at the q/k
   // pitch take exactly its size).
@@ -59,35 +60,42 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
       *reinterpret_cast<uint4*>(&Vt[i * LDK + d8]) = make_uint4(0u, 0u, 0u, 0u);
   }
   cp_async_commit();
-  // One elementwise pass: thread (channel d, rows i0 .. i0 + 7) forms
-  //   Kd = K exp(gc_last - gc)  one 16-byte piece of Kd^T ([c][j], the operand
-  //                             layout of the walk's state update),
-  //   Qp = Q exp(gc)            one FP16 element per row,
+  // One elementwise pass: thread (channels d, d + 1, rows i0 .. i0 + 7) forms
+  //   Kd = K exp(gc_last - gc)  one 16-byte piece of Kd^T per channel ([c][j],
+  //                             the operand layout of the walk's state update),
+  //   Qp = Q exp(gc)            one FP16 pair per row,
   //   beta K exp(gc)            the B operand of w, FP32, in place of gc,
-  // and gamma = exp(gc_last) with the channel's first piece.  Kd and Qp are
+  // and gamma = exp(gc_last) with the channels' first pieces.  Kd and Qp are
   // only ever MMA operands and their factors are <= 1: stored in FP16.
-  for (int e = tid; e < DK * CH / 8; e += blockDim.x) {
-    const int d = e & (DK - 1), i0 = 8 * (e >> 7);
-    if (i0 == 0) a.gam[((size_t)chunk * a.HV + h) * DK + d] = ex2(glast);
+  for (int e = tid; e < DK * CH / 16; e += blockDim.x) {
+    const int d = 2 * (e & (DK / 2 - 1)), i0 = 8 * (e >> 6);
+    if (i0 == 0)
+      *reinterpret_cast<float2*>(&a.gam[((size_t)chunk * a.HV + h) * DK + d]) = make_float2(ex2(glast.x), ex2(glast.y));
     __half* const qo = a.qp + qp_off(chunk, h, a.HV) + d;
-    uint32_t p[4];
+    uint32_t p0[4], p1[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      float kd[2];
+      float kd0[2], kd1[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int i = i0 + 2 * q + u;
-        const float gc = VEC ? s.G[i * LDT + d] : s.gs[i];
-        const float ki = s.k(i, d);
-        kd[u] = ki * (scaled ? s.rk[i] : 1.f) * ex2(glast - gc);
-        const float gm = ex2(gc);
-        qo[i * DK] = __float2half_rn(s.q(i, d) * (scaled ? s.rq[i] : 1.f) * gm);
-        s.G[i * LDT + d] = s.beta[i] * (scaled ? s.rk[i] : 1.f) * ki * gm;
+        const float2 gc = VEC ? *reinterpret_cast<const float2*>(&s.G[i * LDT + d]) : make_float2(s.gs[i], s.gs[i]);
+        const float2 kv = s.k2(i, d), qv = s.q2(i, d);
+        const float rk = scaled ? s.rk[i] : 1.f, rq = scaled ? s.rq[i] : 1.f;
+        kd0[u] = kv.x * rk * ex2(glast.x - gc.x);
+        kd1[u] = kv.y * rk * ex2(glast.y - gc.y);
+        const float gm0 = ex2(gc.x), gm1 = ex2(gc.y);
+        *reinterpret_cast<__half2*>(&qo[i * DK]) = __floats2half2_rn(qv.x * rq * gm0, qv.y * rq * gm1);
+        const float bk = s.beta[i] * rk;
+        *reinterpret_cast<float2*>(&s.G[i * LDT + d]) = make_float2(bk * kv.x * gm0, bk * kv.y * gm1);
       }
-      const __half2 hv = __floats2half2_rn(kd[0], kd[1]);
-      p[q] = *reinterpret_cast<const uint32_t*>(&hv);
+      const __half2 h0 = __floats2half2_rn(kd0[0], kd0[1]), h1 = __floats2half2_rn(kd1[0], kd1[1]);
+      p0[q] = *reinterpret_cast<const uint32_t*>(&h0);
+      p1[q] = *reinterpret_cast<const uint32_t*>(&h1);
     }
-    *reinterpret_cast<uint4*>(&a.kd[kd_off(chunk, h, a.HV) + d * CH + i0]) = make_uint4(p[0], p[1], p[2], p[3]);
+    __half* const ko = a.kd + kd_off(chunk, h, a.HV) + d * CH + i0;
+    *reinterpret_cast<uint4*>(ko) = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+    *reinterpret_cast<uint4*>(ko + CH) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
   }
   cp_async_wait<0>();
   __syncthreads();
