@@ -258,7 +258,7 @@ constexpr int GRAD_WARPS = 16;   // 4 row blocks x 4 channel quarters
 constexpr int GRAD_NT = 4;       // 8-channel n-tiles per warp (32 channels)
 
 struct GradSmem {
-  ChunkSmemBB c;       // its At tile holds w (FP16 rows LDF elements apart) instead
+  ChunkSmemB c;       // its At tile holds w (FP16 rows LDF elements apart) instead
   float uh[CH * LDS];  // u: FP16 rows LDF elements apart (the same bytes)
   float dK[CH * LDF];  // staging: dw, then the forward's At and dAqk
   float dG[CH * LDF];  // staging: dDelta, then the gate adjoint dgc
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(GRAD_WARPS * 32, 1) k_grad(GradArgs a) {
   constexpr int NTH = GRAD_WARPS * 32;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   GradSmem& sg = *reinterpret_cast<GradSmem*>(smem_raw);
-  ChunkSmemBB& s = sg.c;
+  ChunkSmemB& s = sg.c;
   const int chunk = a.chunk_base + blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);

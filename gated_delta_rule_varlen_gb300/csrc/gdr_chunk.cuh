@@ -11,10 +11,11 @@ namespace gdr {
 // Shared-memory tiles of one chunk.  K and Q are kept either as FP32 (ET =
 // float) or as their exact BF16 input bits (ET = uint16_t, half the space; the
 // chunk loads below fill this form).
-// LG_ is the row stride of the gate tile: 132 (= 4 mod 32) suits fragment
-// reads with the row on the group index (A operands of K K^T), 136 (= 8 mod 32)
-// fragment reads with the row on the thread-in-group index (B operands of the
-// applies) and float2 reads of accumulator positions.
+// LG_ is the row stride of the gate tile; the prep and the gradient kernels
+// use 136 (= 8 mod 32), which serves without bank conflicts float2 reads of
+// adjacent channels with the row on the group index (the Gram's fragments,
+// accumulator positions) and scalar reads with the row on the
+// thread-in-group index (B operands of the applies and of w).
 template <typename ET, int LG_ = LDT>
 struct ChunkSmemT {
   static constexpr int LD = sizeof(ET) == 4 ? LDT : DK + 8;  // row stride (elements) of K and Q
@@ -43,8 +44,7 @@ struct ChunkSmemT {
   static __device__ __forceinline__ float elem(uint16_t x) { return bfbits2f(x); }
 };
 using ChunkSmem = ChunkSmemT<float>;
-using ChunkSmemB = ChunkSmemT<uint16_t>;
-using ChunkSmemBB = ChunkSmemT<uint16_t, LDF>;
+using ChunkSmemB = ChunkSmemT<uint16_t, LDF>;
 
 // Row scalars of one chunk, read into registers by the first half of a chunk
 // load (threads tid < CH, row tid) and stored by the second.
@@ -152,6 +152,10 @@ __device__ void load_chunk(ChunkSmemT<uint16_t, LG>& s, const __nv_bfloat16* __r
 // warp w issues from the SM sub-partition w % 4, so each sub-partition gets
 // 10 n-tiles.
 // Per-channel gates use the block factorization described in gdr_common.cuh.
+// Each k-step (channels 8 kk .. 8 kk + 7) puts channels 8 kk + 2t and
+// 8 kk + 2t + 1 in the k slots t and t + 4 (the order of the terms within a
+// step is free), so each fragment pair is one float2 of gates and one BF16
+// pair of k or q.
 // The upper channel half leaves its partial sums in s.At and s.T (free until
 // the inverse); the lower half adds them in, masks, and writes the results.
 // Aqk is stored in FP16 (it is only ever an MMA operand), dense rows of 64.
@@ -169,22 +173,22 @@ __device__ void gram(ChunkSmemT<ET, LG>& s, __half* __restrict__ aqk, bool scale
   zero_acc(accK);
   zero_acc(accQ);
   if (VEC) {
+    auto g2 = [&](int i, int c) { return *reinterpret_cast<const float2*>(&G[i * LG + c]); };
 #pragma unroll 2
     for (int kk = 8 * hk; kk < 8 * hk + 8; ++kk) {
-      const int c0 = kk * 8 + t, c1 = c0 + 4;
+      const int c = kk * 8 + 2 * t;
       // Reference: gc at row i0 + 7, for the diagonal and the earlier blocks alike.
-      const float m0 = G[(i0 + 7) * LG + c0], m1 = G[(i0 + 7) * LG + c1];
-      const float e00 = ex2(G[ra * LG + c0] - m0), e10 = ex2(G[rb * LG + c0] - m0);
-      const float e01 = ex2(G[ra * LG + c1] - m1), e11 = ex2(G[rb * LG + c1] - m1);
-      uint32_t aK[4] = {tf32(s.k(ra, c0) * e00), tf32(s.k(rb, c0) * e10), tf32(s.k(ra, c1) * e01),
-                        tf32(s.k(rb, c1) * e11)};
-      uint32_t aQ[4] = {tf32(s.q(ra, c0) * e00), tf32(s.q(rb, c0) * e10), tf32(s.q(ra, c1) * e01),
-                        tf32(s.q(rb, c1) * e11)};
+      const float2 m = g2(i0 + 7, c), ga = g2(ra, c), gb = g2(rb, c);
+      const float e00 = ex2(ga.x - m.x), e10 = ex2(gb.x - m.x), e01 = ex2(ga.y - m.y), e11 = ex2(gb.y - m.y);
+      const float2 ka = s.k2(ra, c), kb = s.k2(rb, c), qa = s.q2(ra, c), qb = s.q2(rb, c);
+      uint32_t aK[4] = {tf32(ka.x * e00), tf32(kb.x * e10), tf32(ka.y * e01), tf32(kb.y * e11)};
+      uint32_t aQ[4] = {tf32(qa.x * e00), tf32(qb.x * e10), tf32(qa.y * e01), tf32(qb.y * e11)};
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         if (nt < 2 * I + 2) {
           const int j = nt * 8 + g;
-          uint32_t b[2] = {tf32(s.k(j, c0) * ex2(m0 - G[j * LG + c0])), tf32(s.k(j, c1) * ex2(m1 - G[j * LG + c1]))};
+          const float2 gj = g2(j, c), kj = s.k2(j, c);
+          uint32_t b[2] = {tf32(kj.x * ex2(m.x - gj.x)), tf32(kj.y * ex2(m.y - gj.y))};
           mma8(accK[nt], aK, b);
           mma8(accQ[nt], aQ, b);
         }

@@ -18,7 +18,7 @@ template <bool VEC, typename BetaT>
 __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ChunkSmemB& s = *reinterpret_cast<ChunkSmemB*>(smem_raw);
-  constexpr int LDK = ChunkSmemB::LD;
+  constexpr int LDK = ChunkSmemB::LD, LG = ChunkSmemB::LG;
   const int chunk = a.chunk_base + blockIdx.x, h = blockIdx.y;
   const ChunkDesc cd = a.chunks[chunk];
   const int hq = h / (a.HV / a.Hqk);
@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   // Each thread keeps two channels, d = 2 (tid % 64) and d + 1, in the pass
   // below; their gc_last is read before the pass overwrites the gate tile.
   const int dch = 2 * (tid & (DK / 2 - 1));
-  const float2 glast = VEC ? *reinterpret_cast<const float2*>(&s.G[(CH - 1) * LDT + dch])
+  const float2 glast = VEC ? *reinterpret_cast<const float2*>(&s.G[(CH - 1) * LG + dch])
                            : make_float2(s.gs[CH - 1], s.gs[CH - 1]);
   __syncthreads();  // At is stored (or unused) and every gc_last is read
   // v rows (async) into the At tile, free from here on (BF16 rows at the q/k
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int i = i0 + 2 * q + u;
-        const float2 gc = VEC ? *reinterpret_cast<const float2*>(&s.G[i * LDT + d]) : make_float2(s.gs[i], s.gs[i]);
+        const float2 gc = VEC ? *reinterpret_cast<const float2*>(&s.G[i * LG + d]) : make_float2(s.gs[i], s.gs[i]);
         const float2 kv = s.k2(i, d), qv = s.q2(i, d);
         const float rk = scaled ? s.rk[i] : 1.f, rq = scaled ? s.rq[i] : 1.f;
         kd0[u] = kv.x * rk * ex2(glast.x - gc.x);
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
         const float gm0 = ex2(gc.x), gm1 = ex2(gc.y);
         *reinterpret_cast<__half2*>(&qo[i * DK]) = __floats2half2_rn(qv.x * rq * gm0, qv.y * rq * gm1);
         const float bk = s.beta[i] * rk;
-        *reinterpret_cast<float2*>(&s.G[i * LDT + d]) = make_float2(bk * kv.x * gm0, bk * kv.y * gm1);
+        *reinterpret_cast<float2*>(&s.G[i * LG + d]) = make_float2(bk * kv.x * gm0, bk * kv.y * gm1);
       }
       const __half2 h0 = __floats2half2_rn(kd0[0], kd0[1]), h1 = __floats2half2_rn(kd1[0], kd1[1]);
       p0[q] = *reinterpret_cast<const uint32_t*>(&h0);
@@ -102,12 +102,12 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
   // w (warps 0-3) and u (warps 4-7) = T B over rows j <= i.  Warp q of a
   // product takes channel half q % 2 of row blocks {3, 0} (q < 2) or {2, 1},
   // so that the four warps do equal work.  B of u, beta_j V_jc, is formed from
-  // the BF16 v tile (in the At tile) as it is read.  Each k-step (rows j = 8 kk
+  // the BF16 v tile (in the At tile) as it is read: each k-step (rows j = 8 kk
   // .. 8 kk + 7) puts rows 8 kk + 2t and 8 kk + 2t + 1 in the k slots t and
-  // t + 4 (the order within a step is free): the B reads of w's FP32 tile
-  // (row pitch 132) are then free of bank conflicts, u's B fragments of four
+  // t + 4 (the order within a step is free), so that the B fragments of four
   // n-tiles come from one transposing 8 x 8 matrix load of v, and each A
-  // fragment row of T is one float2.
+  // fragment row of T is one float2.  w reads its FP32 B tile (row pitch 136)
+  // with the rows in the slots as they come.
   {
     const int prod = warp >> 2, q = warp & 3, c0 = 64 * (q & 1);
     const int Ia = (q >> 1) ? 2 : 3, Ib = 3 - Ia;
@@ -123,11 +123,11 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
       zero_acc(acc);
 #pragma unroll 2
       for (int kk = 0; kk < 2 * I + 2; ++kk) {
-        const int j0 = kk * 8 + 2 * t;
-        const float2 ta = *reinterpret_cast<const float2*>(&s.T[(i0 + g) * LDS + j0]);
-        const float2 tb = *reinterpret_cast<const float2*>(&s.T[(i0 + g + 8) * LDS + j0]);
-        const uint32_t af[4] = {tf32(ta.x), tf32(tb.x), tf32(ta.y), tf32(tb.y)};
         if (prod) {
+          const int j0 = kk * 8 + 2 * t;
+          const float2 ta = *reinterpret_cast<const float2*>(&s.T[(i0 + g) * LDS + j0]);
+          const float2 tb = *reinterpret_cast<const float2*>(&s.T[(i0 + g + 8) * LDS + j0]);
+          const uint32_t af[4] = {tf32(ta.x), tf32(tb.x), tf32(ta.y), tf32(tb.y)};
           uint32_t y[2][4];
           ldsm_x4_trans(y[0], vrow + kk * 8 * LDK);
           ldsm_x4_trans(y[1], vrow + kk * 8 * LDK + 32);
@@ -139,10 +139,13 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
             mma8(acc[nt], af, b);
           }
         } else {
+          const int ja = kk * 8 + t, jb = ja + 4;
+          const uint32_t af[4] = {tf32(s.T[(i0 + g) * LDS + ja]), tf32(s.T[(i0 + g + 8) * LDS + ja]),
+                                  tf32(s.T[(i0 + g) * LDS + jb]), tf32(s.T[(i0 + g + 8) * LDS + jb])};
 #pragma unroll
           for (int nt = 0; nt < 8; ++nt) {
             const int c = c0 + nt * 8 + g;
-            uint32_t b[2] = {tf32(s.G[j0 * LDT + c]), tf32(s.G[(j0 + 1) * LDT + c])};
+            uint32_t b[2] = {tf32(s.G[ja * LG + c]), tf32(s.G[jb * LG + c])};
             mma8(acc[nt], af, b);
           }
         }
