@@ -291,36 +291,42 @@ __device__ __forceinline__ void invert_tiles(const float* __restrict__ At, float
   __syncthreads();
   const int half = warp >> 2, J = half ? 7 - warp : warp;
   if (J < 3) {
-    // Warp (J, half): the 16 x 8 tile of columns n0 .. n0 + 7 of T_IJ, one
-    // m16n8k8 accumulator, as split-TF32 tensor-core products (hi*hi + hi*lo
-    // + lo*hi, about FP32 accuracy): C = At_I,[16J, 16I) T_[16J, 16I),J, then
-    // X = diag(beta_I) C through shared memory into the B layout, then
-    // T_IJ = -T_II X.
+    // Warp (J, half): the 16 x 8 tile of columns n0 .. n0 + 7 of T_IJ as
+    // split-TF32 tensor-core products (hi*hi + hi*lo + lo*hi, about FP32
+    // accuracy, in three m16n8k8 accumulators): C = At_I,[16J, 16I)
+    // T_[16J, 16I),J, then X = diag(beta_I) C through shared memory into the B
+    // layout, then T_IJ = -T_II X.
     const int n0 = 16 * J + 8 * half;
     const int g = lane >> 2, t = lane & 3;
     float* xs = tmp_all + (half * 3 + J) * 128;  // X [16][8]
     for (int I = J + 1; I < 4; ++I) {
       const int r0 = 16 * I;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      float c3[3][4] = {};
       for (int k0 = 16 * J; k0 < r0; k0 += 8) {
         const float a[4] = {At[(r0 + g) * LDS + k0 + t], At[(r0 + g + 8) * LDS + k0 + t],
                             At[(r0 + g) * LDS + k0 + t + 4], At[(r0 + g + 8) * LDS + k0 + t + 4]};
         const float b[2] = {T[(k0 + t) * LDS + n0 + g], T[(k0 + t + 4) * LDS + n0 + g]};
-        mma8_split(c, a, b);
+        mma8_split3(c3, a, b);
       }
+      float c[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[e] = (c3[0][e] + c3[1][e]) + c3[2][e];
       xs[g * 8 + 2 * t] = beta[r0 + g] * c[0];
       xs[g * 8 + 2 * t + 1] = beta[r0 + g] * c[1];
       xs[(g + 8) * 8 + 2 * t] = beta[r0 + g + 8] * c[2];
       xs[(g + 8) * 8 + 2 * t + 1] = beta[r0 + g + 8] * c[3];
       __syncwarp();
-      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      float o3[3][4] = {};
 #pragma unroll
       for (int k0 = 0; k0 < 16; k0 += 8) {
         const float a[4] = {T[(r0 + g) * LDS + r0 + k0 + t], T[(r0 + g + 8) * LDS + r0 + k0 + t],
                             T[(r0 + g) * LDS + r0 + k0 + t + 4], T[(r0 + g + 8) * LDS + r0 + k0 + t + 4]};
         const float b[2] = {xs[(k0 + t) * 8 + g], xs[(k0 + t + 4) * 8 + g]};
-        mma8_split(o, a, b);
+        mma8_split3(o3, a, b);
       }
+      float o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = (o3[0][e] + o3[1][e]) + o3[2][e];
       *reinterpret_cast<float2*>(&T[(r0 + g) * LDS + n0 + 2 * t]) = make_float2(-o[0], -o[1]);
       *reinterpret_cast<float2*>(&T[(r0 + g + 8) * LDS + n0 + 2 * t]) = make_float2(-o[2], -o[3]);
       __syncwarp();

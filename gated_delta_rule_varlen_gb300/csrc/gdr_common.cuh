@@ -99,9 +99,11 @@ __device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], cons
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 // d += a b with FP32 operands split as x = hi + lo (hi = x rounded to TF32,
-// lo = the remainder rounded to TF32): lo*hi + hi*lo + hi*hi, the small
-// terms first; about FP32 accuracy from three TF32 products.
-__device__ __forceinline__ void mma8_split(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+// lo = the remainder rounded to TF32): about FP32 accuracy from three TF32
+// products, lo*hi, hi*lo and hi*hi, each into an accumulator of its own
+// (d[0], d[1], d[2]: three independent chains instead of one three times as
+// long); the caller adds them, small terms first, as (d[0] + d[1]) + d[2].
+__device__ __forceinline__ void mma8_split3(float (&d)[3][4], const float (&a)[4], const float (&b)[2]) {
   uint32_t ah[4], al[4], bh[2], bl[2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -113,9 +115,9 @@ __device__ __forceinline__ void mma8_split(float (&d)[4], const float (&a)[4], c
     bh[i] = tf32_value(b[i]);
     bl[i] = tf32(b[i] - __uint_as_float(bh[i]));
   }
-  mma8(d, al, bh);
-  mma8(d, ah, bl);
-  mma8(d, ah, bh);
+  mma8(d[0], al, bh);
+  mma8(d[1], ah, bl);
+  mma8(d[2], ah, bh);
 }
 
 
