@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(256, 2) k_prep(PrepArgs a) {
 // of value heads by Q/K head of PR #7723 "perf(cake_gdn): prefetch offset
 // adjoint walk, default LPT segment plan" (opening description).
 // ---------------------------------------------------------------------------
-struct PrepGdnSmem {
+struct __align__(16) PrepGdnSmem {
   uint16_t KQ[2 * 2 * CH * 64];  // 2 channel blocks x [k rows 0..63 ; q rows 64..127] x 64 channels (SW128)
   uint16_t V[2 * CH * 64];       // v of one value head: 2 channel blocks x 64 rows (SW128)
   uint16_t A[2][CH * 64];        // A of w, then of u: BF16 hi, lo (K-major SW128, 64 rows x 64 tokens)
@@ -224,15 +224,24 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
 }
 
 // A operand T diag(f) (rows i, tokens j; T lower triangular) as BF16 hi + lo
-// in the K-major 128-byte-swizzled layout.
+// in the K-major 128-byte-swizzled layout.  Item (row i, 8-token piece kc),
+// the row fastest: a warp's lanes take 32 consecutive rows of one piece, so
+// the two float4 reads of T per item fall on distinct banks, the eight
+// factors f are one broadcast, and the swizzled 16-byte stores are
+// conflict-free.
 __device__ __forceinline__ void build_a(PrepGdnSmem& s, const float* __restrict__ f) {
-  for (int e = threadIdx.x; e < CH * 8; e += blockDim.x) {  // row i, 8-token piece kc
-    const int i = e >> 3, kc = e & 7;
+  for (int e = threadIdx.x; e < CH * 8; e += blockDim.x) {
+    const int i = e & (CH - 1), kc = e >> 6;
+    const float4 t0 = *reinterpret_cast<const float4*>(&s.T[i * LDS + 8 * kc]);
+    const float4 t1 = *reinterpret_cast<const float4*>(&s.T[i * LDS + 8 * kc + 4]);
+    const float4 f0 = *reinterpret_cast<const float4*>(&f[8 * kc]);
+    const float4 f1 = *reinterpret_cast<const float4*>(&f[8 * kc + 4]);
+    const float x[8] = {t0.x * f0.x, t0.y * f0.y, t0.z * f0.z, t0.w * f0.w,
+                        t1.x * f1.x, t1.y * f1.y, t1.z * f1.z, t1.w * f1.w};
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-      const int j = 8 * kc + 2 * p;
-      const float x0 = s.T[i * LDS + j] * f[j], x1 = s.T[i * LDS + j + 1] * f[j + 1];
+      const float x0 = x[2 * p], x1 = x[2 * p + 1];
       const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
       const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
       const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
