@@ -1,8 +1,8 @@
 // gdr_chunk.cuh -- chunk-local building blocks shared by the prep and the
 // gradient kernels: tile loads with the gate cumsum, the gated Gram matrices,
 // the unit-lower-triangular inverse and the gated "apply" products of the
-// backward.  One CTA of 4 warps works on one (chunk, value head); warp I owns
-// rows 16I .. 16I+15 of every 64-row result.
+// backward.  One CTA works on one (chunk, value head); its warps own 16-row
+// blocks of every 64-row result (each kernel maps its warps onto the blocks).
 #pragma once
 #include "gdr_common.cuh"
 
@@ -43,7 +43,6 @@ struct ChunkSmemT {
   static __device__ __forceinline__ float elem(float x) { return x; }
   static __device__ __forceinline__ float elem(uint16_t x) { return bfbits2f(x); }
 };
-using ChunkSmem = ChunkSmemT<float>;
 using ChunkSmemB = ChunkSmemT<uint16_t, LDF>;
 
 // Row scalars of one chunk, read into registers by the first half of a chunk

@@ -169,7 +169,12 @@ __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 //   A: a0 (g, t) a1 (g+8, t) a2 (g, t+4) a3 (g+8, t+4)      [row, k]
 //   B: b0 (t, g) b1 (t+4, g)                                [k, col]
 //   C: c0 (g, 2t) c1 (g, 2t+1) c2 (g+8, 2t) c3 (g+8, 2t+1)  [row, col]
-// with g = lane / 4, t = lane % 4.
+// with g = lane / 4, t = lane % 4.  Which k index fills which of a step's
+// eight k slots is free as long as A and B agree, so kernels put adjacent
+// elements in slots t and t + 4 where that makes the operand reads pairs or
+// conflict-free; with the assignments used here the outputs came out bit for
+// bit those of the plain order (compared on whole forward and backward
+// passes).
 
 // One k-step of 8 (k0 .. k0+7) of a warp product C[16 x 8*NT] += A * B over
 // n-tiles [nt0, nt1).  fa(i, k) and fb(k, n) return FP32 values.
