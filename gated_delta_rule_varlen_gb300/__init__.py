@@ -50,6 +50,7 @@ EXPORTED = (
     "gdr_set_serial",
     "gdr_set_segment_chunks",
     "gdr_set_slice_chunks",
+    "gdr_walk_slices",
 )
 
 _lock = threading.Lock()
@@ -75,6 +76,7 @@ _SIGS = {
     "gdr_set_serial": ([ctypes.c_int], ctypes.c_int),
     "gdr_set_segment_chunks": ([ctypes.c_int], ctypes.c_int),
     "gdr_set_slice_chunks": ([ctypes.c_int], ctypes.c_int),
+    "gdr_walk_slices": ([I32, I32, PI32, I32, PI32], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, ctypes.c_int, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, ctypes.c_int, PSZ, PSZ], ctypes.c_int),
     "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, ctypes.c_int, P, P, P, P, SZ, ctypes.c_int, P, SZ, P],
@@ -330,6 +332,17 @@ def gdr_doc_groups(cu_seqlens_host):
     n = ctypes.c_int32(0)
     _check(load().gdr_doc_groups(arr.shape[0] - 1, cup, ranks, chunks, ctypes.byref(n)), "gdr_doc_groups")
     return [(ranks[i], ranks[i + 1], chunks[i], chunks[i + 1]) for i in range(n.value)]
+
+
+def gdr_walk_slices(nchunks, direction):
+    """Slice bounds [0, .., nchunks] of a pipelined walk over nchunks chunks:
+    direction 0 the forward walk, 1 the backward (host-side plan; no device
+    work)."""
+    cap = nchunks + 2
+    bounds = (ctypes.c_int32 * cap)()
+    n = ctypes.c_int32(0)
+    _check(load().gdr_walk_slices(int(nchunks), int(direction), bounds, cap, ctypes.byref(n)), "gdr_walk_slices")
+    return [bounds[i] for i in range(n.value + 1)]
 
 
 def kda_fwd_noalloc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, scale, out, ht=None, h0=None, stream=None):

@@ -1241,6 +1241,20 @@ gdr_status gdr_doc_groups(int32_t N, const int32_t* cu_seqlens_host, int32_t* ra
   return GDR_OK;
 }
 
+gdr_status gdr_walk_slices(int32_t nchunks, int32_t direction, int32_t* bounds, int32_t cap, int32_t* n_slices) {
+  if (!bounds || !n_slices || nchunks < 0 || (direction != 0 && direction != 1) || cap < 1) return GDR_INVALID_ARG;
+  if (nchunks == 0) {
+    bounds[0] = 0;
+    *n_slices = 0;
+    return GDR_OK;
+  }
+  const std::vector<int> b = gdr::slice_bounds(nchunks, gdr::slice_chunks(), direction ? 4 : 2);
+  if ((int64_t)b.size() > cap) return GDR_INVALID_ARG;
+  for (size_t i = 0; i < b.size(); ++i) bounds[i] = b[i];
+  *n_slices = (int32_t)b.size() - 1;
+  return GDR_OK;
+}
+
 gdr_status gdr_inject_device_error(int code) {
   if (code <= 0) return GDR_INVALID_ARG;
   int* p = gdr::device_error_ptr();

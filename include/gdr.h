@@ -296,10 +296,26 @@ int gdr_set_segment_chunks(int chunks);
  * adjoint, passed on exactly in FP32 between the slices' launches), so that
  * the forward walk starts once the first slice is prepared and the
  * backward's gradient kernels of a slice run while the walk goes on with the
- * next; the results are bit for bit those of the whole walk.  chunks > 0 sets
+ * next; the results are bit for bit those of the whole walk.  The first and
+ * the last slice are shorter (half a slice in the forward walk, a quarter in
+ * the backward walk, at least 2 chunks; the last one may take one chunk
+ * more), the chunks between them go in equal slices of about the slice
+ * length, and every slice starts at an even chunk; a document shorter than
+ * two end slices and two chunks is cut into whole slices.  chunks > 0 sets
  * the slice length (rounded down to an even number, at least 2); 0 restores
  * the default of 128 chunks.  Process-wide; returns the previous setting. */
 int gdr_set_slice_chunks(int chunks);
+
+/* Host-side slice plan of a pipelined walk (no device work), as the forward
+ * (direction 0) or the backward (direction 1) walk cuts a document of
+ * nchunks chunks at the current slice length: writes *n_slices and the slice
+ * bounds 0 = bounds[0] < bounds[1] < ... < bounds[*n_slices] = nchunks
+ * (slice i holds chunks [bounds[i], bounds[i+1]); the backward walks them
+ * last slice first).  nchunks = 0 gives no slice (bounds[0] = 0).  bounds
+ * needs room for *n_slices + 1 entries; cap is its length.  Errors:
+ * GDR_INVALID_ARG for null pointers, nchunks < 0, a direction other than 0
+ * or 1, or a cap too small for the plan. */
+gdr_status gdr_walk_slices(int32_t nchunks, int32_t direction, int32_t* bounds, int32_t cap, int32_t* n_slices);
 
 #ifdef __cplusplus
 }
