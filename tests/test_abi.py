@@ -82,7 +82,7 @@ def test_workspace_validation(gdr):
 
 
 def _fake(n=1):
-    return ctypes.c_void_p(0x10000 * n)  # never dereferenced: validation fails first
+    return ctypes.c_void_p(0x10000 * n)  # never dereferenced: every call below fails host validation
 
 
 def test_forward_host_validation_before_any_cuda_call(gdr):
@@ -124,27 +124,41 @@ def test_forward_host_validation_before_any_cuda_call(gdr):
     assert st == gdr.GDR_OK
 
 
-def test_backward_leaves_unregistered_workspaces_to_the_device_header_check(gdr):
-    # A saved buffer this process never filled (a copy at another address, or
-    # one filled elsewhere) is not rejected by the host registry: the backward
-    # goes on to the device (its header is checked there), which here, with
-    # no GPU, fails the device check instead.
+def test_backward_host_validation_before_any_cuda_call(gdr):
+    # Every call here is rejected on the host before any work reaches the
+    # device (no copy, no launch), so the fake pointers are never handed to a
+    # GPU on any machine.  (A saved buffer that passes these checks goes on to
+    # the device-side header check, which the GPU tests cover with real
+    # buffers.)
     lib = gdr.load()
     cu = np.array([0, 5, 11], dtype=np.int32)
     cup = cu.ctypes.data_as(gdr.PI32)
     p = _fake()
     big = 1 << 40
-    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
+    # cu[N] != T
+    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 10, 1, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
                      _fake(1024), big, None)
-    assert st == gdr.GDR_CUDA_ERROR
-    st = lib.gdn_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 3, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
-                     _fake(1024), big, None)
-    assert st == gdr.GDR_CUDA_ERROR
+    assert st == gdr.GDR_BAD_CU_SEQLENS
     # dout not on a 16-byte boundary
     st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, ctypes.c_void_p(0x10004), None, _fake(512), big, p,
                      p, p, p, p, None, _fake(1024), big, None)
     assert st == gdr.GDR_INVALID_ARG
-    # Too-small scratch is reported before the stamp.
+    # misaligned scratch
+    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
+                     ctypes.c_void_p(0x10010), big, None)
+    assert st == gdr.GDR_INVALID_ARG
+    # null saved buffer
+    st = lib.gdn_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 3, 1.0, 0, None, p, None, None, big, p, p, p, p, p, None,
+                     _fake(1024), big, None)
+    assert st == gdr.GDR_INVALID_ARG
+    # GDN: HV not a multiple of Hqk
+    st = lib.gdn_bwd(p, p, p, p, p, p, cup, 2, 11, 4, 6, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
+                     _fake(1024), big, None)
+    assert st == gdr.GDR_INVALID_ARG
+    # Too-small saved buffer or scratch (reported before the stamp and the device).
+    st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, _fake(512), 256, p, p, p, p, p, None,
+                     _fake(1024), big, None)
+    assert st == gdr.GDR_WORKSPACE_TOO_SMALL
     st = lib.kda_bwd(p, p, p, p, p, p, cup, 2, 11, 1, 1.0, 0, None, p, None, _fake(512), big, p, p, p, p, p, None,
                      _fake(1024), 256, None)
     assert st == gdr.GDR_WORKSPACE_TOO_SMALL
