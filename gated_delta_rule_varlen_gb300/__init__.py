@@ -51,6 +51,7 @@ EXPORTED = (
     "gdr_set_segment_chunks",
     "gdr_set_slice_chunks",
     "gdr_walk_slices",
+    "gdr_segment_plan",
 )
 
 _lock = threading.Lock()
@@ -77,6 +78,7 @@ _SIGS = {
     "gdr_set_segment_chunks": ([ctypes.c_int], ctypes.c_int),
     "gdr_set_slice_chunks": ([ctypes.c_int], ctypes.c_int),
     "gdr_walk_slices": ([I32, I32, PI32, I32, PI32], ctypes.c_int),
+    "gdr_segment_plan": ([I32, PI32, I32, PI32, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
     "kda_workspace_bytes": ([I64, I32, I32, PI32, ctypes.c_int, PSZ, PSZ], ctypes.c_int),
     "gdn_workspace_bytes": ([I64, I32, I32, I32, PI32, ctypes.c_int, PSZ, PSZ], ctypes.c_int),
     "kda_fwd": ([P, P, P, P, P, P, PI32, I32, I64, I32, F32, ctypes.c_int, P, P, P, P, SZ, ctypes.c_int, P, SZ, P],
@@ -332,6 +334,18 @@ def gdr_doc_groups(cu_seqlens_host):
     n = ctypes.c_int32(0)
     _check(load().gdr_doc_groups(arr.shape[0] - 1, cup, ranks, chunks, ctypes.byref(n)), "gdr_doc_groups")
     return [(ranks[i], ranks[i + 1], chunks[i], chunks[i + 1]) for i in range(n.value)]
+
+
+def gdr_segment_plan(cu_seqlens_host, HV):
+    """(segment length in chunks, 0 when nothing is split; number of walk
+    segments) that the compute calls would use for this pack and value-head
+    count (host-side plan; no device work)."""
+    arr, cup = _cu_host(cu_seqlens_host)
+    lseg = ctypes.c_int32(0)
+    nseg = ctypes.c_int64(0)
+    _check(load().gdr_segment_plan(arr.shape[0] - 1, cup, int(HV), ctypes.byref(lseg), ctypes.byref(nseg)),
+           "gdr_segment_plan")
+    return lseg.value, nseg.value
 
 
 def gdr_walk_slices(nchunks, direction):

@@ -1241,6 +1241,24 @@ gdr_status gdr_doc_groups(int32_t N, const int32_t* cu_seqlens_host, int32_t* ra
   return GDR_OK;
 }
 
+gdr_status gdr_segment_plan(int32_t N, const int32_t* cu_seqlens_host, int32_t HV, int32_t* seg_chunks,
+                            int64_t* n_segments) {
+  if (N < 0 || !cu_seqlens_host || HV <= 0 || !seg_chunks || !n_segments) return GDR_INVALID_ARG;
+  if (cu_seqlens_host[0] != 0) return GDR_BAD_CU_SEQLENS;
+  for (int32_t n = 0; n < N; ++n)
+    if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return GDR_BAD_CU_SEQLENS;
+  if (N == 0) {
+    *seg_chunks = 0;
+    *n_segments = 0;
+    return GDR_OK;
+  }
+  const int lseg = gdr::segment_chunks(N, cu_seqlens_host, HV);
+  std::vector<gdr::DocGroup> groups = gdr::plan_groups(N, cu_seqlens_host);
+  *n_segments = gdr::assign_segments(groups, N, cu_seqlens_host, lseg);
+  *seg_chunks = lseg >= gdr::kNoSplit ? 0 : lseg;
+  return GDR_OK;
+}
+
 gdr_status gdr_walk_slices(int32_t nchunks, int32_t direction, int32_t* bounds, int32_t cap, int32_t* n_slices) {
   if (!bounds || !n_slices || nchunks < 0 || (direction != 0 && direction != 1) || cap < 1) return GDR_INVALID_ARG;
   if (nchunks == 0) {

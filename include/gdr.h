@@ -291,6 +291,18 @@ int gdr_set_serial(int on);
  * returns GDR_STALE_WORKSPACE.  Returns the previous setting. */
 int gdr_set_segment_chunks(int chunks);
 
+/* Host-side segment plan of the state walks (no device work): writes the
+ * segment length in chunks that the compute calls would use for this pack
+ * and value-head count (*seg_chunks = 0 when no document is split) and the
+ * number of walk segments (*n_segments: one per document no longer than a
+ * segment, ceil(chunks / segment length) for a longer one).  Reads the
+ * gdr_set_segment_chunks setting and the device's SM count (152 when no
+ * device answers).  Errors: GDR_INVALID_ARG for null pointers, N < 0 or
+ * HV <= 0; GDR_BAD_CU_SEQLENS for a cu_seqlens that does not start at 0 or
+ * decreases. */
+gdr_status gdr_segment_plan(int32_t N, const int32_t* cu_seqlens_host, int32_t HV, int32_t* seg_chunks,
+                            int64_t* n_segments);
+
 /* gdr_set_slice_chunks(chunks): a document group that holds one unsplit
  * document longer than a slice walks it slice by slice (the state, or the
  * adjoint, passed on exactly in FP32 between the slices' launches), so that
