@@ -152,3 +152,45 @@ def test_chunked_identities_match_the_recurrence(C, Hqk, HV, per_channel, glow):
         a, b = got[name], ref[name]
         err = np.abs(a - b).max() / max(np.abs(b).max(), 1e-30)
         assert err < 1e-10, f"{name}: chunked identities differ from the recurrence by {err:.2e}"
+
+
+def _walk(q, k, v, g, beta, S, scale, C):
+    """One (document, head) chain of chunks from S: (end state, per-chunk saved values)."""
+    tape = []
+    for c0 in range(0, q.shape[0], C):
+        c1 = min(c0 + C, q.shape[0])
+        _, S, sv = _chunk_fwd(q[c0:c1], k[c0:c1], v[c0:c1], g[c0:c1], beta[c0:c1], S, scale)
+        tape.append((c0, c1, sv))
+    return S, tape
+
+
+def _walk_back(tape, dout, dS, scale):
+    for c0, c1, sv in reversed(tape):
+        dS = _chunk_bwd(sv, dout[c0:c1], dS, scale)[5]
+    return dS
+
+
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_segment_maps_are_affine(per_channel):
+    # A run of chunks maps its start state affinely, S_end = M S_start + B, with
+    # M the end state walked from the identity with v = 0 (so u = 0) and B the
+    # end state walked from zero; its adjoint maps back as
+    # dS_start = M^T dS_end + dB, with dB walked back from a zero end adjoint.
+    # The segment-parallel walks (summary walks, then a merge) rest on these.
+    rng = np.random.default_rng(11)
+    L, D, scale = 200, 8, 0.4
+    q = rng.standard_normal((L, D))
+    k = rng.standard_normal((L, D))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((L, D))
+    g = rng.uniform(-0.2, 0.0, (L, D)) if per_channel else np.repeat(rng.uniform(-0.2, 0.0, (L, 1)), D, 1)
+    beta = rng.uniform(0.0, 1.0, L)
+    dout = rng.standard_normal((L, D))
+    S_start, dS_end = rng.standard_normal((D, D)), rng.standard_normal((D, D))
+    M, _ = _walk(q, k, np.zeros_like(v), g, beta, np.eye(D), scale, 64)
+    B, tape0 = _walk(q, k, v, g, beta, np.zeros((D, D)), scale, 64)
+    S_end, tape = _walk(q, k, v, g, beta, S_start, scale, 64)
+    assert np.abs(S_end - (M @ S_start + B)).max() < 1e-12 * max(1.0, np.abs(S_end).max())
+    dB = _walk_back(tape0, dout, np.zeros((D, D)), scale)
+    dS_start = _walk_back(tape, dout, dS_end, scale)
+    assert np.abs(dS_start - (M.T @ dS_end + dB)).max() < 1e-12 * max(1.0, np.abs(dS_start).max())
